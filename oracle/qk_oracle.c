@@ -1,0 +1,298 @@
+/*
+ * qk_oracle.c -- the CPU oracle for the quantized Q4_K / Q6_K matmul path.
+ *
+ * TEST INFRASTRUCTURE, NOT PRODUCT CODE.  Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg load this file's library.  The
+ * CUDA library never links, includes or calls it, and it shares no header,
+ * table or helper with the CUDA sources.
+ *
+ * What it computes (sources):
+ *  - DAMASCUS project overview, "[01] the thesis" and "[04] one decode step":
+ *    every linear of a Llama-3.2-3B decoder layer (QKV, O, SwiGLU gate/up,
+ *    down, tied LM head) is a matrix product of the quantized weights with the
+ *    activations; decode is the M = 1 case (a GEMV), prefill the M > 1 case.
+ *  - "Building DAMASCUS", "Read the model, then reproduce its operations":
+ *    the weights are Q4_K and Q6_K blocks that are dequantized before use.
+ *  - "Building DAMASCUS", "A same-weights oracle makes the comparison useful":
+ *    the reference dequantizes the very same quantized blocks.
+ *  The pages do not print the block layouts.  The layouts below are the public
+ *  GGUF Q4_K / Q6_K super-block definitions (256 weights per block; 144 bytes
+ *  and 210 bytes), which is the reading this project takes.
+ *
+ * Precision rules (the reading taken where the pages are silent):
+ *  - fp16 scale fields are widened to fp32 exactly (IEEE binary16 -> binary32).
+ *  - Q4_K weight:  w = fp32(fp32(d) * sc) * q  -  fp32(fp32(dmin) * m),
+ *    Q6_K weight:  w = fp32(fp32(d) * sc) * q,
+ *    each operation a separate fp32 round-to-nearest step (built with
+ *    -ffp-contract=off so no multiply-add is fused).
+ *  - matmul: y[m][n] = sum_k x[m][k] * w[n][k], summed in fp64 in k order;
+ *    x is fp16 widened exactly, w is the fp32 dequantized weight.
+ *  - SwiGLU: out = g / (1 + exp(-g)) * u with g, u the fp64 sums above.
+ *
+ * Parity pins live in the test suite (hand-built blocks with closed forms,
+ * bit-placement tables, an independent bit-level decoder, one-hot and all-ones
+ * activations, a float64 library matmul, linearity and permutation).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_Q4K_BYTES 144
+#define ORACLE_Q6K_BYTES 210
+#define ORACLE_QK 256
+
+/* ------------------------------------------------------------------------ */
+/* IEEE 754 binary16 -> binary32, exact (binary32 holds every binary16).     */
+/* ------------------------------------------------------------------------ */
+float oracle_half_to_float(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 10) & 0x1F;
+    const int frac = h & 0x3FF;
+    float v;
+    if (expo == 31 && frac) {
+        /* NaN: keep its sign and payload (the payload moves up 13 bits) */
+        uint32_t bits = ((uint32_t)sign << 31) | 0x7F800000u | ((uint32_t)frac << 13);
+        memcpy(&v, &bits, 4);
+        return v;
+    }
+    if (expo == 31)
+        v = INFINITY;
+    else if (expo == 0)
+        v = ldexpf((float)frac, -24); /* zero or subnormal: frac * 2^-24 */
+    else
+        v = ldexpf((float)(1024 + frac), expo - 25); /* normal: 1.frac * 2^(expo-15) */
+    return sign ? -v : v;
+}
+
+static uint16_t rd16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* ------------------------------------------------------------------------ */
+/* Q4_K: bytes 0-1 d (fp16), 2-3 dmin (fp16), 4-15 packed 6-bit scales and    */
+/* mins of the 8 sub-blocks of 32 weights, 16-143 the 256 4-bit quants.       */
+/* ------------------------------------------------------------------------ */
+
+/* Scale and min of sub-block j (0..7) from the 12 packed bytes s[0..11]:
+ *  j < 4 : the low 6 bits of s[j] (scale) and of s[j+4] (min);
+ *  j >= 4: low 4 bits from the low / high nibble of s[j+4], the top 2 bits
+ *          from bits 6-7 of s[j-4] (scale) and of s[j] (min). */
+static void q4k_scale_min(const uint8_t *s, int j, int *sc, int *mn)
+{
+    if (j < 4) {
+        *sc = s[j] & 63;
+        *mn = s[j + 4] & 63;
+    } else {
+        *sc = (s[j + 4] & 0x0F) | ((s[j - 4] >> 6) << 4);
+        *mn = (s[j + 4] >> 4) | ((s[j] >> 6) << 4);
+    }
+}
+
+/* 4-bit quant of weight i (0..255): 64-weight group g = i/64 uses bytes
+ * qs[32g .. 32g+31]; its first 32 weights are the low nibbles, the next 32
+ * the high nibbles. */
+static int q4k_quant(const uint8_t *qs, int i)
+{
+    const uint8_t byte = qs[32 * (i / 64) + (i % 32)];
+    return (i % 64) < 32 ? (byte & 0x0F) : (byte >> 4);
+}
+
+static void dequant_q4k_block(const uint8_t *blk, float *out)
+{
+    const float d = oracle_half_to_float(rd16(blk));
+    const float dmin = oracle_half_to_float(rd16(blk + 2));
+    const uint8_t *s = blk + 4;
+    const uint8_t *qs = blk + 16;
+    for (int i = 0; i < ORACLE_QK; ++i) {
+        int sc, mn;
+        q4k_scale_min(s, i / 32, &sc, &mn);
+        const float dsc = d * (float)sc;
+        const float dmn = dmin * (float)mn;
+        const float t = dsc * (float)q4k_quant(qs, i);
+        out[i] = t - dmn;
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q6_K: bytes 0-127 ql (low 4 bits), 128-191 qh (high 2 bits), 192-207 the  */
+/* 16 int8 scales (one per 16 weights), 208-209 d (fp16).                     */
+/* ------------------------------------------------------------------------ */
+
+/* 6-bit quant of weight i, minus 32.  i = 128h + 32g + l (h 0..1, g 0..3,
+ * l 0..31): low 4 bits are the low nibble (g < 2) or high nibble (g >= 2) of
+ * ql[64h + 32(g & 1) + l]; the high 2 bits are bits 2g..2g+1 of qh[32h + l]. */
+static int q6k_quant(const uint8_t *ql, const uint8_t *qh, int i)
+{
+    const int h = i / 128, g = (i % 128) / 32, l = i % 32;
+    const uint8_t lb = ql[64 * h + 32 * (g & 1) + l];
+    const int lo = g < 2 ? (lb & 0x0F) : (lb >> 4);
+    const int hi = (qh[32 * h + l] >> (2 * g)) & 3;
+    return (lo | (hi << 4)) - 32;
+}
+
+static void dequant_q6k_block(const uint8_t *blk, float *out)
+{
+    const uint8_t *ql = blk;
+    const uint8_t *qh = blk + 128;
+    const int8_t *sc = (const int8_t *)(blk + 192);
+    const float d = oracle_half_to_float(rd16(blk + 208));
+    for (int i = 0; i < ORACLE_QK; ++i) {
+        const float dsc = d * (float)sc[i / 16];
+        out[i] = dsc * (float)q6k_quant(ql, qh, i);
+    }
+}
+
+/* qtype: 0 = Q4_K, 1 = Q6_K.  Returns bytes per block, or 0 if unknown. */
+static int64_t block_bytes(int qtype)
+{
+    return qtype == 0 ? ORACLE_Q4K_BYTES : qtype == 1 ? ORACLE_Q6K_BYTES : 0;
+}
+
+static void dequant_block(int qtype, const uint8_t *blk, float *out)
+{
+    if (qtype == 0)
+        dequant_q4k_block(blk, out);
+    else
+        dequant_q6k_block(blk, out);
+}
+
+/* Dequantize n_blocks consecutive blocks into n_blocks*256 fp32 values. */
+int oracle_dequant(int qtype, const uint8_t *blocks, int64_t n_blocks, float *out)
+{
+    const int64_t bb = block_bytes(qtype);
+    if (!bb || n_blocks < 0)
+        return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t b = 0; b < n_blocks; ++b)
+        dequant_block(qtype, blocks + b * bb, out + b * ORACLE_QK);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Matmul: W holds N rows of K/256 blocks (row n = output feature n), x is    */
+/* [M][K] fp16 row-major.  The oracle evaluates only the requested rows:      */
+/* y[m][r] = sum_k x[m][k] * w[rows[r]][k] in fp64, y being [M][n_rows].      */
+/* ------------------------------------------------------------------------ */
+static double *widen_x(const uint16_t *x, int64_t M, int64_t K)
+{
+    double *xd = (double *)malloc((size_t)(M * K) * sizeof(double));
+    if (!xd)
+        return NULL;
+    for (int64_t i = 0; i < M * K; ++i)
+        xd[i] = (double)oracle_half_to_float(x[i]);
+    return xd;
+}
+
+static void dequant_row(int qtype, const uint8_t *W, int64_t n, int64_t K, float *w)
+{
+    const int64_t bb = block_bytes(qtype);
+    const int64_t nb = K / ORACLE_QK;
+    for (int64_t b = 0; b < nb; ++b)
+        dequant_block(qtype, W + (n * nb + b) * bb, w + b * ORACLE_QK);
+}
+
+int oracle_matmul_rows(int qtype, const uint8_t *W, const uint16_t *x, int64_t M, int64_t K,
+                       const int64_t *rows, int64_t n_rows, double *y)
+{
+    if (!block_bytes(qtype) || M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
+        return -1;
+    double *xd = widen_x(x, M, K);
+    if (!xd)
+        return -2;
+    int failed = 0;
+#pragma omp parallel
+    {
+        float *w = (float *)malloc((size_t)K * sizeof(float));
+        if (!w) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            if (!w)
+                continue;
+            dequant_row(qtype, W, rows[r], K, w);
+            for (int64_t m = 0; m < M; ++m) {
+                const double *xm = xd + m * K;
+                double acc = 0.0;
+                for (int64_t k = 0; k < K; ++k)
+                    acc += xm[k] * (double)w[k];
+                y[m * n_rows + r] = acc;
+            }
+        }
+        free(w);
+    }
+    free(xd);
+    return failed ? -2 : 0;
+}
+
+/* SwiGLU over two Q4_K weight sets with the same x:
+ * out[m][r] = silu(g) * u, g = x[m] . wg[rows[r]], u = x[m] . wu[rows[r]],
+ * silu(g) = g / (1 + exp(-g)), all in fp64.  Optionally also returns g and u. */
+int oracle_gateup_swiglu_rows(const uint8_t *Wg, const uint8_t *Wu, const uint16_t *x, int64_t M,
+                              int64_t K, const int64_t *rows, int64_t n_rows, double *out,
+                              double *g_out, double *u_out)
+{
+    if (M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
+        return -1;
+    double *xd = widen_x(x, M, K);
+    if (!xd)
+        return -2;
+    int failed = 0;
+#pragma omp parallel
+    {
+        float *wg = (float *)malloc((size_t)K * sizeof(float));
+        float *wu = (float *)malloc((size_t)K * sizeof(float));
+        if (!wg || !wu) {
+#pragma omp atomic write
+            failed = 1;
+        }
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < n_rows; ++r) {
+            if (!wg || !wu)
+                continue;
+            dequant_row(0, Wg, rows[r], K, wg);
+            dequant_row(0, Wu, rows[r], K, wu);
+            for (int64_t m = 0; m < M; ++m) {
+                const double *xm = xd + m * K;
+                double g = 0.0, u = 0.0;
+                for (int64_t k = 0; k < K; ++k) {
+                    g += xm[k] * (double)wg[k];
+                    u += xm[k] * (double)wu[k];
+                }
+                const double silu = g / (1.0 + exp(-g));
+                out[m * n_rows + r] = silu * u;
+                if (g_out)
+                    g_out[m * n_rows + r] = g;
+                if (u_out)
+                    u_out[m * n_rows + r] = u;
+            }
+        }
+        free(wg);
+        free(wu);
+    }
+    free(xd);
+    return failed ? -2 : 0;
+}
+
+int oracle_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n > 0)
+        omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

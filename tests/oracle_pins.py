@@ -1,0 +1,433 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each ``pin_*`` function takes an ``oracle.Oracle`` and raises AssertionError on
+a mismatch.  ``test_oracle_pins.py`` runs them on the oracle; the mutant test
+runs them on deliberately broken copies of the oracle to show that each
+plausible mistake is caught by at least one pin.
+
+What the pins rest on:
+* IEEE binary16 widening: numpy's float16 -> float32 conversion (a library
+  routine) for all 65536 bit patterns.
+* Block layouts: the hand-written tables in ``tests/golden`` (public GGUF Q4_K /
+  Q6_K definitions; the DAMASCUS pages name the formats in "Building DAMASCUS",
+  "Read the model, then reproduce its operations", but print no layout) drive
+  an independent table-lookup decoder and one-hot bit-placement checks.
+* Worked blocks with hand-derived scales, closed forms (all-zero / all-max
+  quants), one-hot and all-ones activations, a float64 library matmul,
+  linearity, row permutation and the SwiGLU closed form via scipy's expit.
+"""
+from __future__ import annotations
+
+import os
+import re
+
+import numpy as np
+
+from tests import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+Q4K, Q6K = 0, 1
+
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return [ln.strip() for ln in f if ln.strip() and not ln.lstrip().startswith("#")]
+
+
+def _rng(a):
+    lo, hi = (int(v) for v in a.split("-")) if "-" in a else (int(a), int(a))
+    return list(range(lo, hi + 1))
+
+
+# ---------------------------------------------------------------------------
+# Golden tables
+# ---------------------------------------------------------------------------
+def q4k_scale_bit_table():
+    """{(byte, bit): (field, subblock, field_bit)} from q4k_scale_bits.txt."""
+    table = {}
+    for ln in _lines("q4k_scale_bits.txt"):
+        byte, rest = ln.split(":")
+        for bit, dest in enumerate(rest.split()):
+            m = re.fullmatch(r"(sc|m)(\d)\.(\d)", dest)
+            table[(int(byte), bit)] = (m.group(1), int(m.group(2)), int(m.group(3)))
+    assert len(table) == 96
+    return table
+
+
+def q4k_quant_table():
+    """[(qs_byte, nibble_shift, weight)] from q4k_quant_map.txt (256 entries)."""
+    out = []
+    for ln in _lines("q4k_quant_map.txt"):
+        b, lo, hi = ln.split()
+        for byte, wl, wh in zip(_rng(b), _rng(lo), _rng(hi)):
+            out += [(byte, 0, wl), (byte, 4, wh)]
+    assert sorted(w for _, _, w in out) == list(range(256))
+    return out
+
+
+def q6k_quant_table():
+    """(ql entries [(byte, shift, weight)], qh entries [(byte, shift, weight)])."""
+    ql, qh = [], []
+    for ln in _lines("q6k_quant_map.txt"):
+        parts = ln.split()
+        if parts[0] == "ql":
+            for byte, wl, wh in zip(_rng(parts[1]), _rng(parts[2]), _rng(parts[3])):
+                ql += [(byte, 0, wl), (byte, 4, wh)]
+        else:
+            cols = [_rng(p) for p in parts[2:6]]
+            for idx, byte in enumerate(_rng(parts[1])):
+                for pair in range(4):
+                    qh.append((byte, 2 * pair, cols[pair][idx]))
+    assert sorted(w for _, _, w in ql) == list(range(256))
+    assert sorted(w for _, _, w in qh) == list(range(256))
+    return ql, qh
+
+
+# ---------------------------------------------------------------------------
+# An independent, table-driven decoder (numpy, fp32 steps one at a time)
+# ---------------------------------------------------------------------------
+def _f16(b2):
+    return np.ascontiguousarray(b2).view(np.float16).astype(np.float32).reshape(-1)
+
+
+@np.errstate(invalid="ignore", over="ignore")
+def table_decode_q4k(blocks):
+    blocks = np.asarray(blocks, dtype=np.uint8).reshape(-1, 144)
+    nb = blocks.shape[0]
+    d = _f16(blocks[:, 0:2])
+    dmin = _f16(blocks[:, 2:4])
+    sm = blocks[:, 4:16].astype(np.int64)
+    sc = np.zeros((nb, 8), np.int64)
+    mn = np.zeros((nb, 8), np.int64)
+    for (byte, bit), (field, j, fbit) in q4k_scale_bit_table().items():
+        v = ((sm[:, byte] >> bit) & 1) << fbit
+        if field == "sc":
+            sc[:, j] |= v
+        else:
+            mn[:, j] |= v
+    q = np.zeros((nb, 256), np.int16)
+    qs = blocks[:, 16:144].astype(np.int16)
+    for byte, shift, w in q4k_quant_table():
+        q[:, w] = (qs[:, byte] >> shift) & 0xF
+    j = np.arange(256) // 32
+    dsc = (d[:, None] * sc[:, j].astype(np.float32)).astype(np.float32)
+    dmn = (dmin[:, None] * mn[:, j].astype(np.float32)).astype(np.float32)
+    t = (dsc * q.astype(np.float32)).astype(np.float32)
+    return (t - dmn).astype(np.float32).reshape(-1)
+
+
+@np.errstate(invalid="ignore", over="ignore")
+def table_decode_q6k(blocks):
+    blocks = np.asarray(blocks, dtype=np.uint8).reshape(-1, 210)
+    nb = blocks.shape[0]
+    ql_b = blocks[:, 0:128].astype(np.int16)
+    qh_b = blocks[:, 128:192].astype(np.int16)
+    sc = blocks[:, 192:208].view(np.int8).astype(np.float32)
+    d = _f16(blocks[:, 208:210])
+    lo = np.zeros((nb, 256), np.int16)
+    hi = np.zeros((nb, 256), np.int16)
+    ql_t, qh_t = q6k_quant_table()
+    for byte, shift, w in ql_t:
+        lo[:, w] = (ql_b[:, byte] >> shift) & 0xF
+    for byte, shift, w in qh_t:
+        hi[:, w] = (qh_b[:, byte] >> shift) & 0x3
+    q = (lo | (hi << 4)) - 32
+    t = np.arange(256) // 16
+    dsc = (d[:, None] * sc[:, t]).astype(np.float32)
+    return (dsc * q.astype(np.float32)).astype(np.float32).reshape(-1)
+
+
+def same_bits(a, b):
+    """fp32 equality bit for bit, NaN == NaN of any payload."""
+    a = np.asarray(a, np.float32)
+    b = np.asarray(b, np.float32)
+    both_nan = np.isnan(a) & np.isnan(b)
+    eq = (a.view(np.uint32) == b.view(np.uint32)) | both_nan
+    return bool(eq.all())
+
+
+# ---------------------------------------------------------------------------
+# Block builders for hand-made cases
+# ---------------------------------------------------------------------------
+def _half_bytes(v):
+    return np.array([v], dtype=np.float16).view(np.uint8)
+
+
+def q4k_block(d=1.0, dmin=1.0, scales=None, qs=None):
+    blk = np.zeros(144, np.uint8)
+    blk[0:2] = _half_bytes(d)
+    blk[2:4] = _half_bytes(dmin)
+    if scales is not None:
+        blk[4:16] = scales
+    if qs is not None:
+        blk[16:144] = qs
+    return blk
+
+
+def q6k_block(d=1.0, scales=None, ql=None, qh=None):
+    blk = np.zeros(210, np.uint8)
+    if ql is not None:
+        blk[0:128] = ql
+    if qh is not None:
+        blk[128:192] = qh
+    if scales is not None:
+        blk[192:208] = np.asarray(scales, np.int8).view(np.uint8)
+    blk[208:210] = _half_bytes(d)
+    return blk
+
+
+# ---------------------------------------------------------------------------
+# Pins
+# ---------------------------------------------------------------------------
+def pin_half_to_float(O):
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([O.half_to_float(int(b)) for b in bits], dtype=np.float32)
+    assert same_bits(got, ref)
+    nan = np.isnan(ref)
+    # NaN keeps its sign bit
+    assert ((got.view(np.uint32)[nan] >> 31) == (bits[nan] >> 15)).all()
+
+
+def pin_q4k_scale_bits(O):
+    """Each of the 96 scale/min bits lands on the sub-block and field of the table."""
+    for (byte, bit), (field, j, fbit) in q4k_scale_bit_table().items():
+        s = np.zeros(12, np.uint8)
+        s[byte] = 1 << bit
+        if field == "sc":
+            w = O.dequant(Q4K, q4k_block(d=1.0, dmin=0.0, scales=s, qs=np.full(128, 0x11, np.uint8)))
+            expect = np.zeros(256, np.float32)
+            expect[32 * j:32 * j + 32] = float(1 << fbit)
+        else:
+            w = O.dequant(Q4K, q4k_block(d=0.0, dmin=1.0, scales=s, qs=np.zeros(128, np.uint8)))
+            expect = np.zeros(256, np.float32)
+            expect[32 * j:32 * j + 32] = -float(1 << fbit)
+        assert np.array_equal(w + 0.0, expect), (byte, bit)
+
+
+def pin_q4k_quant_map(O):
+    """A single non-zero nibble shows up at exactly the weight the table names."""
+    ones = np.array([1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1], np.uint8)  # all scales 1, all mins 0
+    for byte, shift, wi in q4k_quant_table():
+        qs = np.zeros(128, np.uint8)
+        qs[byte] = 0xF << shift
+        w = O.dequant(Q4K, q4k_block(d=1.0, dmin=1.0, scales=ones, qs=qs))
+        expect = np.zeros(256, np.float32)
+        expect[wi] = 15.0
+        assert np.array_equal(w, expect), (byte, shift, wi)
+
+
+def pin_q4k_worked_block(O):
+    lines = _lines("q4k_worked_block.txt")
+    scales = np.array([int(h, 16) for h in lines[0].split(":")[1].split()], np.uint8)
+    scm = [tuple(int(v) for v in ln.split(":")[1].split()) for ln in lines[1:9]]
+    qs = np.array([(b % 16) | ((15 - b % 16) << 4) for b in range(128)], np.uint8)
+    w = O.dequant(Q4K, q4k_block(d=1.0, dmin=0.5, scales=scales, qs=qs))
+    q = np.zeros(256, np.int64)
+    for byte, shift, wi in q4k_quant_table():
+        q[wi] = (int(qs[byte]) >> shift) & 0xF
+    expect = np.array([scm[i // 32][0] * q[i] - 0.5 * scm[i // 32][1] for i in range(256)], np.float32)
+    assert np.array_equal(w, expect)
+
+
+def pin_q4k_closed_forms(O):
+    """All-zero quants give -dmin*m_j; all-15 quants give 15*d*sc_j - dmin*m_j."""
+    lines = _lines("q4k_worked_block.txt")
+    scales = np.array([int(h, 16) for h in lines[0].split(":")[1].split()], np.uint8)
+    scm = [tuple(int(v) for v in ln.split(":")[1].split()) for ln in lines[1:9]]
+    for d, dmin in [(0.000123, 0.0000456), (3.5, -1.25), (6.0e-8, 65504.0)]:
+        dh = np.float32(np.float16(d))
+        mh = np.float32(np.float16(dmin))
+        w0 = O.dequant(Q4K, q4k_block(d=d, dmin=dmin, scales=scales, qs=np.zeros(128, np.uint8)))
+        w15 = O.dequant(Q4K, q4k_block(d=d, dmin=dmin, scales=scales, qs=np.full(128, 0xFF, np.uint8)))
+        for i in range(256):
+            sc, m = scm[i // 32]
+            dmn = np.float32(mh * np.float32(m))
+            assert w0[i] == np.float32(np.float32(dh * np.float32(sc)) * np.float32(0)) - dmn
+            assert w15[i] == np.float32(np.float32(dh * np.float32(sc)) * np.float32(15)) - dmn
+
+
+def pin_q6k_quant_map(O):
+    ones = np.ones(16, np.int8)
+    ql_t, qh_t = q6k_quant_table()
+    for byte, shift, wi in ql_t:
+        ql = np.zeros(128, np.uint8)
+        ql[byte] = 0xF << shift
+        w = O.dequant(Q6K, q6k_block(d=1.0, scales=ones, ql=ql))
+        expect = np.full(256, -32.0, np.float32)
+        expect[wi] = -17.0
+        assert np.array_equal(w, expect), ("ql", byte, shift)
+    for byte, shift, wi in qh_t:
+        for val in (1, 2, 3):
+            qh = np.zeros(64, np.uint8)
+            qh[byte] = val << shift
+            w = O.dequant(Q6K, q6k_block(d=1.0, scales=ones, qh=qh))
+            expect = np.full(256, -32.0, np.float32)
+            expect[wi] = -32.0 + 16 * val
+            assert np.array_equal(w, expect), ("qh", byte, shift, val)
+
+
+def pin_q6k_scale_map(O):
+    for t in range(16):
+        sc = np.zeros(16, np.int8)
+        sc[t] = -3
+        w = O.dequant(Q6K, q6k_block(d=1.0, scales=sc))
+        expect = np.zeros(256, np.float32)
+        expect[16 * t:16 * t + 16] = 96.0  # (-3) * (0 - 32)
+        assert np.array_equal(w + 0.0, expect), t
+
+
+def pin_q6k_worked_block(O):
+    lines = _lines("q6k_worked_block.txt")
+    sc = [int(v) for v in lines[0].split(":")[1].split()]
+    qg = [int(v) for v in lines[1].split(":")[1].split()]
+    w = O.dequant(Q6K, q6k_block(d=1.0, scales=sc, ql=np.full(128, 0x0F, np.uint8),
+                                  qh=np.full(64, 0x1B, np.uint8)))
+    expect = np.array([sc[i // 16] * qg[i // 32] for i in range(256)], np.float32)
+    assert np.array_equal(w, expect)
+
+
+def pin_q6k_closed_forms(O):
+    sc = np.array([5, -7, 63, -32, 1, 0, 17, -1, 9, 33, -20, 2, 44, -9, 3, 12], np.int8)
+    for d in (0.000123, -2.5, 6.0e-8):
+        dh = np.float32(np.float16(d))
+        lo = O.dequant(Q6K, q6k_block(d=d, scales=sc))
+        hi = O.dequant(Q6K, q6k_block(d=d, scales=sc, ql=np.full(128, 0xFF, np.uint8),
+                                       qh=np.full(64, 0xFF, np.uint8)))
+        for i in range(256):
+            dsc = np.float32(dh * np.float32(sc[i // 16]))
+            assert lo[i] == np.float32(dsc * np.float32(-32))
+            assert hi[i] == np.float32(dsc * np.float32(31))
+
+
+def random_blocks(qtype, n, seed):
+    """Synthetic blocks plus raw random bytes (any fp16 scale, incl. inf / NaN / subnormal)."""
+    rng = synth.rng_for(seed, 991)
+    bb = 144 if qtype == Q4K else 210
+    gen = synth.q4k_weights if qtype == Q4K else synth.q6k_weights
+    a = gen(rng, n // 2, 256).reshape(-1, bb)
+    b = rng.integers(0, 256, size=(n - n // 2, bb), dtype=np.uint8)
+    return np.concatenate([a, b])
+
+
+def pin_bruteforce_vs_table_decoder(O, n=100_000, seed=7):
+    for qtype, dec in ((Q4K, table_decode_q4k), (Q6K, table_decode_q6k)):
+        blocks = random_blocks(qtype, n, seed + qtype)
+        assert same_bits(O.dequant(qtype, blocks), dec(blocks)), qtype
+
+
+def _mat(qtype, N, K, seed):
+    rng = synth.rng_for(seed, 5)
+    W = synth.q4k_weights(rng, N, K) if qtype == Q4K else synth.q6k_weights(rng, N, K)
+    dec = table_decode_q4k if qtype == Q4K else table_decode_q6k
+    return W, dec(W).reshape(N, K)
+
+
+def pin_matmul_onehot(O):
+    """x = e_k picks column k of the dequantized weights, exactly."""
+    for qtype in (Q4K, Q6K):
+        N, K = 37, 512
+        W, Wf = _mat(qtype, N, K, 11)
+        ks = np.array([0, 1, 31, 32, 63, 64, 255, 256, 300, 511])
+        x = np.zeros((ks.size, K), np.float16)
+        x[np.arange(ks.size), ks] = 1.0
+        y = O.matmul(qtype, W, x, N, K)
+        assert np.array_equal(y, Wf[:, ks].T.astype(np.float64))
+        # a scaled one-hot: x = 2^-3 e_k scales exactly
+        y2 = O.matmul(qtype, W, (x * np.float16(0.125)).astype(np.float16), N, K)
+        assert np.array_equal(y2, Wf[:, ks].T.astype(np.float64) * 0.125)
+
+
+def pin_matmul_ones_rowsum(O):
+    """x = ones gives the exact row sums of the dequantized weights (math.fsum)."""
+    import math
+    for qtype in (Q4K, Q6K):
+        N, K = 19, 768
+        W, Wf = _mat(qtype, N, K, 12)
+        y = O.matmul(qtype, W, np.ones((1, K), np.float16), N, K)[0]
+        exact = np.array([math.fsum(Wf[n].astype(np.float64)) for n in range(N)])
+        mag = np.abs(Wf.astype(np.float64)).sum(axis=1)
+        assert (np.abs(y - exact) <= 1e-13 * mag).all()
+
+
+def pin_matmul_vs_numpy_f64(O):
+    for qtype in (Q4K, Q6K):
+        N, K, M = 64, 1024, 5
+        W, Wf = _mat(qtype, N, K, 13)
+        x = synth.activations(synth.rng_for(13, 6), M, K)
+        y = O.matmul(qtype, W, x, N, K)
+        ref = x.astype(np.float64) @ Wf.astype(np.float64).T
+        scale = np.abs(x.astype(np.float64)) @ np.abs(Wf.astype(np.float64)).T
+        assert (np.abs(y - ref) <= 1e-13 * scale + 1e-300).all()
+
+
+def pin_matmul_rows_and_permutation(O):
+    """Row subsets and row permutations of W permute the outputs exactly."""
+    for qtype in (Q4K, Q6K):
+        N, K, M = 40, 512, 3
+        W, _ = _mat(qtype, N, K, 14)
+        x = synth.activations(synth.rng_for(14, 6), M, K)
+        y = O.matmul(qtype, W, x, N, K)
+        perm = synth.rng_for(14, 7).permutation(N)
+        yp = O.matmul(qtype, W.reshape(N, -1)[perm], x, N, K)
+        assert np.array_equal(yp, y[:, perm])
+        sub = np.array([39, 0, 17, 17, 5])
+        assert np.array_equal(O.matmul(qtype, W, x, N, K, rows=sub), y[:, sub])
+
+
+def pin_matmul_linearity(O):
+    """y(x1 + x2) = y(x1) + y(x2) for fp16 inputs whose sum is exact in fp16."""
+    for qtype in (Q4K, Q6K):
+        N, K = 16, 512
+        W, _ = _mat(qtype, N, K, 15)
+        rng = synth.rng_for(15, 8)
+        x1 = rng.integers(-64, 64, size=(2, K)).astype(np.float16)
+        x2 = rng.integers(-64, 64, size=(2, K)).astype(np.float16)
+        y1 = O.matmul(qtype, W, x1, N, K)
+        y2 = O.matmul(qtype, W, x2, N, K)
+        y12 = O.matmul(qtype, W, (x1 + x2).astype(np.float16), N, K)
+        assert np.allclose(y12, y1 + y2, rtol=1e-12, atol=1e-12)
+        # K-ordering: reversing the K blocks of W and of x together leaves y unchanged
+        nb = K // 256
+        Wr = W.reshape(N, nb, -1)[:, ::-1].reshape(N, -1)
+        xr = x1.reshape(2, nb, 256)[:, ::-1].reshape(2, K)
+        assert np.allclose(O.matmul(qtype, Wr, xr, N, K), y1, rtol=1e-12, atol=1e-12)
+
+
+def pin_gateup_swiglu(O):
+    from scipy.special import expit
+    N, K, M = 24, 768, 4
+    rng = synth.rng_for(16, 9)
+    Wg = synth.q4k_weights(rng, N, K)
+    Wu = synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, M, K)
+    out, g, u = O.gateup_swiglu(Wg, Wu, x, N, K, return_gu=True)
+    assert np.array_equal(g, O.matmul(Q4K, Wg, x, N, K))
+    assert np.array_equal(u, O.matmul(Q4K, Wu, x, N, K))
+    assert np.allclose(out, g * expit(g) * u, rtol=1e-14, atol=1e-300)
+    # silu(0) = 0: an all-zero activation row gives exactly zero
+    z = O.gateup_swiglu(Wg, Wu, np.zeros((1, K), np.float16), N, K)
+    assert np.array_equal(z, np.zeros_like(z))
+    # gate and up swapped is not the same function (guards a swapped operand)
+    sw = O.gateup_swiglu(Wu, Wg, x, N, K)
+    assert not np.allclose(sw, out)
+
+
+ALL_PINS = [
+    pin_half_to_float,
+    pin_q4k_scale_bits,
+    pin_q4k_quant_map,
+    pin_q4k_worked_block,
+    pin_q4k_closed_forms,
+    pin_q6k_quant_map,
+    pin_q6k_scale_map,
+    pin_q6k_worked_block,
+    pin_q6k_closed_forms,
+    pin_bruteforce_vs_table_decoder,
+    pin_matmul_onehot,
+    pin_matmul_ones_rowsum,
+    pin_matmul_vs_numpy_f64,
+    pin_matmul_rows_and_permutation,
+    pin_matmul_linearity,
+    pin_gateup_swiglu,
+]
