@@ -1,0 +1,419 @@
+"""Benchmark: Llama-3.2-3B quantized linears on one GB300 (or N replicas).
+
+One step = one pass of the hot path over one batch of seeded synthetic inputs:
+  * prefill at M = 1024 tokens: fused gate/up + SwiGLU (Q4_K, K 3072, N_ff 8192),
+    the Q6_K down projection (K 8192 -> 3072) and the Q6_K attn_v (3072 -> 1024);
+  * decode at M = 1: the seven linears of one layer (q, k, o, gate, up in Q4_K;
+    v, down in Q6_K).
+Reported metric (``value``): prefill GEMM TFLOP/s at M = 1024 (2*M*N*K per
+linear, dequant arithmetic not counted), with the decode GEMV HBM GB/s (packed
+weight + activation + output bytes) alongside.  Inputs rotate over enough
+copies that every step reads more than the 129 MB L2 from HBM.
+
+--impl reference times the CPU oracle (the only reference implementation:
+the pages publish no code) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tests import synth  # noqa: E402
+
+METRIC = "prefill GEMM TFLOP/s (% FP16 tensor peak) at M=1024; decode GEMV HBM GB/s"
+PREFILL_M = 1024
+N_COPIES = 3  # rotating input copies: ~3 x 230 MB per cycle, well above L2
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def prefill_linears():
+    gate = synth.Linear("ffn_gate", synth.Q4K, synth.FFN, synth.HIDDEN)
+    up = synth.Linear("ffn_up", synth.Q4K, synth.FFN, synth.HIDDEN)
+    down = synth.Linear("ffn_down", synth.Q6K, synth.HIDDEN, synth.FFN)
+    v = synth.Linear("attn_v", synth.Q6K, synth.KV_DIM, synth.HIDDEN)
+    return gate, up, down, v
+
+
+def prefill_flops():
+    gate, up, down, v = prefill_linears()
+    return 2.0 * PREFILL_M * (gate.N * gate.K + up.N * up.K + down.N * down.K + v.N * v.K)
+
+
+def decode_linears():
+    return synth.layer_linears(0)  # layer 0: down is Q6_K
+
+
+def decode_bytes():
+    tot = 0
+    for lin in decode_linears():
+        tot += synth.weight_bytes(lin.qtype, lin.N, lin.K) + 2 * lin.K + 4 * lin.N
+    return tot
+
+
+# ----------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ----------------------------------------------------------------------------
+class Clocks:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the oracle on a bounded sample
+# ----------------------------------------------------------------------------
+def cpu_baseline(target_s: float = 12.0):
+    import oracle
+    gate, up, down, v = prefill_linears()
+    rng = synth.rng_for(7, 1)
+    K = synth.HIDDEN
+    Wg = synth.q4k_weights(rng, 64, K)
+    Wu = synth.q4k_weights(rng, 64, K)
+    x = synth.activations(rng, PREFILL_M, K)
+    t0 = time.perf_counter()
+    oracle.gateup_swiglu(Wg, Wu, x, 64, K, rows=np.arange(4))
+    dt = max(time.perf_counter() - t0, 1e-3)
+    rows = int(min(64, max(4, 4 * target_s / dt)))
+    t0 = time.perf_counter()
+    oracle.gateup_swiglu(Wg, Wu, x, 64, K, rows=np.arange(rows))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * 2 * PREFILL_M * K * rows
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "gate/up + SwiGLU of %d of 8192 output features at M=1024, K=3072 (fp64 oracle), %.1f s"
+                      % (rows, dt)}
+
+
+# ----------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------
+class Workload:
+    """Device-resident inputs (N_COPIES rotating copies) and outputs of one step."""
+
+    def __init__(self, torch, dev, seed=0):
+        self.torch = torch
+        self.dev = dev
+        gate, up, down, v = prefill_linears()
+        self.copies = []
+        for c in range(N_COPIES):
+            rng = synth.rng_for(seed, 100 + c)
+            d = {}
+            d["gate"] = torch.from_numpy(synth.q4k_weights(rng, gate.N, gate.K)).to(dev)
+            d["up"] = torch.from_numpy(synth.q4k_weights(rng, up.N, up.K)).to(dev)
+            d["down"] = torch.from_numpy(synth.q6k_weights(rng, down.N, down.K)).to(dev)
+            d["v"] = torch.from_numpy(synth.q6k_weights(rng, v.N, v.K)).to(dev)
+            d["x_gu"] = torch.from_numpy(synth.activations(rng, PREFILL_M, gate.K).view(np.uint16)).to(dev)
+            d["x_down"] = torch.from_numpy(synth.swiglu_activations(rng, PREFILL_M, down.K).view(np.uint16)).to(dev)
+            d["x_v"] = torch.from_numpy(synth.activations(rng, PREFILL_M, v.K).view(np.uint16)).to(dev)
+            dec = []
+            for lin in decode_linears():
+                Wd = torch.from_numpy(synth.weights(rng, lin.qtype, lin.N, lin.K)).to(dev)
+                xd = torch.from_numpy(synth.activations(rng, 1, lin.K).view(np.uint16)).to(dev)
+                dec.append((lin, Wd, xd))
+            d["decode"] = dec
+            self.copies.append(d)
+        self.y_gu = torch.empty(PREFILL_M, gate.N, dtype=torch.float16, device=dev)
+        self.y_down = torch.empty(PREFILL_M, down.N, dtype=torch.float32, device=dev)
+        self.y_v = torch.empty(PREFILL_M, v.N, dtype=torch.float32, device=dev)
+        self.y_dec = [torch.empty(1, lin.N, dtype=torch.float32, device=dev) for lin in decode_linears()]
+
+    def prefill(self, qk, c, stream):
+        d = self.copies[c]
+        gate, up, down, v = prefill_linears()
+        qk.qk_gateup_swiglu_q4k(d["gate"], d["up"], d["x_gu"], self.y_gu, PREFILL_M, gate.N, gate.K, stream)
+        qk.qk_matmul_q6k(d["down"], d["x_down"], self.y_down, PREFILL_M, down.N, down.K, stream)
+        qk.qk_matmul_q6k(d["v"], d["x_v"], self.y_v, PREFILL_M, v.N, v.K, stream)
+        return 3
+
+    def decode(self, qk, c, stream):
+        d = self.copies[c]
+        for (lin, Wd, xd), y in zip(d["decode"], self.y_dec):
+            fn = qk.qk_matmul_q4k if lin.qtype == synth.Q4K else qk.qk_matmul_q6k
+            fn(Wd, xd, y, 1, lin.N, lin.K, stream)
+        return len(d["decode"])
+
+
+def run_gpu(args, rank, world, dist):
+    import torch
+    import quantized_q4_matmul_gb300 as qk
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    qk.lib()
+    wl = Workload(torch, dev, seed=rank)
+    stream = torch.cuda.Stream(device=dev)
+    s = stream.cuda_stream
+    pk = peaks()
+
+    # Per-part timing: events on the launching stream around each part.
+    def step(i, ev=None):
+        c = i % N_COPIES
+        n = 0
+        if ev is not None:
+            ev[0].record(stream)
+        n += wl.prefill(qk, c, s)
+        if ev is not None:
+            ev[1].record(stream)
+        n += wl.decode(qk, c, s)
+        if ev is not None:
+            ev[2].record(stream)
+        return n
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step(i)
+    qk.qk_get_device_status(s)
+    torch.cuda.synchronize()
+
+    # Dominant kernel alone (fused gate/up + SwiGLU), events around each launch.
+    gu_ms = []
+    for i in range(max(3, args.steps)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        d = wl.copies[i % N_COPIES]
+        gate = prefill_linears()[0]
+        e0.record(stream)
+        qk.qk_gateup_swiglu_q4k(d["gate"], d["up"], d["x_gu"], wl.y_gu, PREFILL_M, gate.N, gate.K, s)
+        e1.record(stream)
+        e1.synchronize()
+        gu_ms.append(e0.elapsed_time(e1))
+
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches = 0
+    with Clocks(local) as clk:
+        t_start.record(stream)
+        for i in range(args.steps):
+            launches += step(i, evs[i])
+        t_end.record(stream)
+        t_end.synchronize()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    qk.qk_get_device_status(s)
+    total_ms = t_start.elapsed_time(t_end)
+    pre_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+
+    # End to end through the public API with host buffers: pinned host inputs
+    # copied in and outputs copied out inside the timed region.
+    gate, up, down, v = prefill_linears()
+    c0 = wl.copies[0]
+    h_x = [t.cpu().pin_memory() for t in (c0["x_gu"], c0["x_down"], c0["x_v"])]
+    h_xd = [xd.cpu().pin_memory() for (_, _, xd) in c0["decode"]]
+    h_y = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (wl.y_gu, wl.y_down, wl.y_v)]
+    h_yd = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in wl.y_dec]
+    h2d = sum(t.numel() * t.element_size() for t in h_x + h_xd)
+    d2h = sum(t.numel() * t.element_size() for t in h_y + h_yd)
+    e2e_pre = []
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        with torch.cuda.stream(stream):
+            e[0].record(stream)
+            for hx, dx in zip(h_x, (c0["x_gu"], c0["x_down"], c0["x_v"])):
+                dx.copy_(hx, non_blocking=True)
+            wl.prefill(qk, 0, s)
+            for hy, dy in zip(h_y, (wl.y_gu, wl.y_down, wl.y_v)):
+                hy.copy_(dy, non_blocking=True)
+            e[1].record(stream)
+            for hx, (_, _, dx) in zip(h_xd, c0["decode"]):
+                dx.copy_(hx, non_blocking=True)
+            wl.decode(qk, 0, s)
+            for hy, dy in zip(h_yd, wl.y_dec):
+                hy.copy_(dy, non_blocking=True)
+            e[2].record(stream)
+        e[2].synchronize()
+        e2e_pre.append(e[0].elapsed_time(e[1]))
+    torch.cuda.synchronize()
+
+    flops = prefill_flops()
+    dbytes = decode_bytes()
+    pre_med = statistics.median(pre_ms)
+    dec_med = statistics.median(dec_ms)
+    local_res = {
+        "total_ms": total_ms, "pre_ms": pre_med, "dec_ms": dec_med, "gu_ms": statistics.median(gu_ms),
+        "e2e_pre_ms": statistics.median(e2e_pre), "launches": launches, "clocks": clk.summary(),
+    }
+    if dist is not None:
+        allr = [None] * world
+        dist.all_gather_object(allr, local_res)
+    else:
+        allr = [local_res]
+    if rank != 0:
+        return None
+    max_total = max(r["total_ms"] for r in allr)
+    max_pre = max(r["pre_ms"] for r in allr)
+    max_dec = max(r["dec_ms"] for r in allr)
+    tflops = world * flops / (max_pre * 1e-3) / 1e12
+    dec_gbs = world * dbytes / (max_dec * 1e-3) / 1e9
+    gu_flops = 2.0 * 2 * PREFILL_M * gate.N * gate.K
+    gu_ms_med = local_res["gu_ms"]
+    gu_ach = gu_flops / (gu_ms_med * 1e-3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            traffic = json.load(f).get("gateup_swiglu_m1024")
+    return {
+        "metric": METRIC,
+        "value": tflops,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": max_total / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 (q4_k/q6_k weights, fp32 accumulate)",
+        "data": "synthetic (seeded Llama-3.2-3B-shaped Q4_K/Q6_K weights, fp16 N(0,1) activations)",
+        "config": {"workload": "llama-3.2-3b linears: prefill M=1024 (gate/up+SwiGLU Q4_K, down Q6_K, attn_v Q6_K)"
+                               " + decode M=1 (one layer's 7 linears)",
+                   "prefill_tokens": PREFILL_M, "decode_tokens": 1, "replicas": world,
+                   "l2": "%d rotating input copies, %.0f MB read per step (> 129 MB L2)"
+                         % (N_COPIES, (decode_bytes() + 51.5e6 + 28e6) / 1e6)},
+        "frac_of_fp16_peak": tflops / world / pk["bf16_tflops"],
+        "decode": {"metric": "decode GEMV HBM GB/s", "value": dec_gbs, "unit": "GB/s",
+                   "frac_of_hbm": dec_gbs / world / pk["hbm_gbs"], "ms_per_layer": max_dec,
+                   "bytes_per_layer": dbytes},
+        "roofline": {"bound": "tensor", "kernel": "gemm_tc_kernel<Q4_K, gate/up+SwiGLU> M=1024 N=2x8192 K=3072",
+                     "achieved": gu_ach, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": gu_ach / pk["bf16_tflops"], "traffic": traffic,
+                     "peak_source": pk["source"] + " (cuBLAS bf16 burst; fp16 dense rate equals bf16)"},
+        "e2e": {"value": flops / (statistics.median([r["e2e_pre_ms"] for r in allr]) * 1e-3) / 1e12,
+                "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": sum(r["launches"] for r in allr),
+        "clocks": local_res["clocks"],
+    }
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        cpu_baseline(target_s=1.0)
+    vals, ts = [], []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        r = cpu_baseline(target_s=float(os.environ.get("QK_REF_STEP_S", "10")))
+        ts.append(time.perf_counter() - t0)
+        vals.append(r["value"])
+    v = statistics.median(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(ts), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
+        "config": {"workload": "llama-3.2-3b gate/up+SwiGLU prefill M=1024 (sampled output features)"},
+        "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
+                         "sample": r["sample"]},
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist_mod.init_process_group(backend=backend)
+        dist = dist_mod
+
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+    else:
+        res = run_gpu(args, rank, world, dist)
+        if res is not None and not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_baseline()
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,122 @@
+/*
+ * qk.h -- C ABI of libqk: fused dequantize-and-multiply of GGUF Q4_K / Q6_K
+ * weights with fp16 activations on NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (DAMASCUS project overview, "[01] the thesis",
+ * "[04] one decode step"; "Building DAMASCUS", "Read the model, then
+ * reproduce its operations" and "Prefill and decode need different
+ * performance questions"):
+ *   every linear layer of a Llama-3.2-3B decoder (QKV, O, SwiGLU gate/up,
+ *   down, tied LM head) as y = x . W^T with W stored as quantized Q4_K / Q6_K
+ *   super-blocks and dequantized on the fly; decode is the M = 1 case (a
+ *   bandwidth-bound GEMV), prefill the M > 1 case (a compute-bound GEMM).
+ *
+ * Block formats (public GGUF definitions; the pages name them but do not print
+ * their layout):
+ *   Q4_K, 144 bytes per 256 weights: fp16 d, fp16 dmin, 12 bytes of packed
+ *     6-bit scales/mins for 8 sub-blocks of 32, 128 bytes of 4-bit quants;
+ *     w = (d * sc) * q - (dmin * m).
+ *   Q6_K, 210 bytes per 256 weights: 128 bytes low 4 bits, 64 bytes high 2
+ *     bits, 16 int8 scales (one per 16 weights), fp16 d;
+ *     w = (d * sc) * (q - 32).
+ *
+ * Conventions for every entry point:
+ *   - Weights W: N rows of K/256 consecutive blocks (row n = output feature n),
+ *     rows packed back to back (row stride = K/256 * block bytes).
+ *   - x: [M][K] fp16 (IEEE binary16 bit patterns), row-major, dense.
+ *   - y: [M][N] row-major, dense (fp32, or fp16 for the SwiGLU entry point).
+ *   - All pointers are DEVICE pointers of the current CUDA device (or mapped
+ *     host memory the device can read), 16-byte aligned.  The caller owns every
+ *     buffer; the library allocates no device memory on any call.
+ *   - K must be a positive multiple of 256.  M = 0 or N = 0 is a no-op.
+ *   - y must not overlap x or the weights.
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream).  The return value reports argument and launch errors only; a
+ *     kernel that gives up on a bounded wait sets a device flag that
+ *     qk_get_device_status() reports.
+ *   - No entry point aborts, exits or traps.
+ *   - Results are deterministic: the same inputs give bit-identical outputs.
+ */
+#ifndef QK_H
+#define QK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int qk_status;
+
+#define QK_OK 0
+#define QK_ERR_NULL (-1)               /* a required pointer is NULL */
+#define QK_ERR_ALIGN (-2)              /* a pointer is not 16-byte aligned */
+#define QK_ERR_SHAPE (-3)              /* K % 256 != 0, a negative size, or sizes that overflow */
+#define QK_ERR_CUDA (-4)               /* a CUDA runtime call or kernel launch failed */
+#define QK_ERR_TIMEOUT (-5)            /* a kernel gave up on a bounded wait (see qk_get_device_status) */
+#define QK_ERR_UNSUPPORTED_DEVICE (-6) /* the current device is not an sm_103 GPU */
+#define QK_ERR_ALIAS (-7)              /* the output overlaps an input */
+#define QK_ERR_POINTER (-8)            /* a pointer is not accessible from the current device */
+
+/* A cudaStream_t, spelled without CUDA headers. */
+typedef struct CUstream_st *qk_stream_t;
+
+/*
+ * Dequantize n_blocks consecutive Q4_K blocks (144 B each) into n_blocks*256
+ * fp32 weights, out[256*b + i] = weight i of block b.  Bit-exact with the
+ * fp32 expression fp32(fp32(d)*sc)*q - fp32(fp32(dmin)*m) evaluated left to
+ * right with round-to-nearest and no fused multiply-add ("Building DAMASCUS",
+ * "Read the model, then reproduce its operations": the dequantizers are the
+ * first correctness boundary).  n_blocks = 0 is a no-op.
+ */
+qk_status qk_dequant_q4k(const void *blocks, int64_t n_blocks, float *out, qk_stream_t stream);
+
+/* As qk_dequant_q4k for Q6_K blocks (210 B each): w = fp32(fp32(d)*sc)*(q-32). */
+qk_status qk_dequant_q6k(const void *blocks, int64_t n_blocks, float *out, qk_stream_t stream);
+
+/*
+ * y[m][n] = sum_k x[m][k] * w[n][k] for Q4_K weights W (N x K), fp16 x, fp32 y
+ * (DAMASCUS project overview, "[01] the thesis" / "[04] one decode step";
+ * "Building DAMASCUS", "Prefill and decode need different performance
+ * questions").  M = 1 runs the decode GEMV (fp32 weights, fp32 accumulation);
+ * larger M runs the tensor-core GEMM (weights dequantized to fp16 in shared
+ * memory, never written to device memory; fp32 accumulation in tensor memory),
+ * as the overview's "fused dequant -> matrix unit never materializes FP16
+ * weights" describes.  The two paths agree within rounding; results are not
+ * bit-identical across M.
+ */
+qk_status qk_matmul_q4k(const void *blocks, const uint16_t *x_f16, float *y, int64_t M, int64_t N, int64_t K,
+                        qk_stream_t stream);
+
+/* As qk_matmul_q4k for Q6_K weights. */
+qk_status qk_matmul_q6k(const void *blocks, const uint16_t *x_f16, float *y, int64_t M, int64_t N, int64_t K,
+                        qk_stream_t stream);
+
+/*
+ * Fused SwiGLU feed-forward input projection (DAMASCUS project overview,
+ * "[04] one decode step" and "[06] the target": FFN = SwiGLU):
+ *   g = x . Wg^T, u = x . Wu^T (both N_ff x K, Q4_K), fp32 accumulation,
+ *   y[m][n] = fp16( g / (1 + exp(-g)) * u ), y is [M][N_ff] fp16.
+ * Gate and up weights are two separate Q4_K tensors of the same shape.
+ */
+qk_status qk_gateup_swiglu_q4k(const void *gate_blocks, const void *up_blocks, const uint16_t *x_f16,
+                               uint16_t *y_f16, int64_t M, int64_t N_ff, int64_t K, qk_stream_t stream);
+
+/*
+ * Synchronise `stream`, then report and clear the device-side status flags
+ * that the library's kernels set when a bounded wait expires.  Returns QK_OK,
+ * QK_ERR_TIMEOUT, or QK_ERR_CUDA if the synchronisation itself failed.
+ */
+qk_status qk_get_device_status(qk_stream_t stream);
+
+/* A static, human-readable name for a status code. */
+const char *qk_status_string(qk_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int qk_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QK_H */

@@ -1,0 +1,163 @@
+// qk_api.cu -- the C ABI of libqk: argument validation and kernel selection.
+//
+// Every entry point checks its arguments on the host before anything is
+// enqueued, so a bad call returns an error code instead of faulting the GPU:
+// NULL / misaligned / non-device pointers, shapes (K % 256, negative sizes,
+// overflow), output aliasing an input, and the device architecture.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstdlib>
+
+#include "../../include/qk.h"
+#include "qk_internal.h"
+
+namespace {
+
+using qk::QType;
+
+constexpr int64_t kMaxDim = (int64_t)1 << 31;  // M, N, K each below 2^31
+
+// sm_103 check, cached per device.
+qk_status check_device() {
+  static int checked[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return QK_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return QK_ERR_UNSUPPORTED_DEVICE;
+  if (!checked[dev]) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return QK_ERR_CUDA;
+    checked[dev] = (major == 10 && minor == 3) ? 1 : 2;
+  }
+  return checked[dev] == 1 ? QK_OK : QK_ERR_UNSUPPORTED_DEVICE;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The pointer must be readable by the current device: device or managed
+// memory of this device, or host memory registered with / allocated by CUDA.
+qk_status check_pointer(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return QK_ERR_POINTER;
+  }
+  if (a.type == cudaMemoryTypeUnregistered) return QK_ERR_POINTER;
+  if (a.type == cudaMemoryTypeDevice) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (a.device != dev) return QK_ERR_POINTER;
+  }
+  if (a.type == cudaMemoryTypeHost && a.devicePointer == nullptr) return QK_ERR_POINTER;
+  return QK_OK;
+}
+
+bool overlaps(const void* a, int64_t an, const void* b, int64_t bn) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + (uintptr_t)bn && b0 < a0 + (uintptr_t)an;
+}
+
+// a * b without overflow, both non-negative; false on overflow past 2^62.
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a != 0 && b > ((int64_t)1 << 62) / a) return false;
+  *out = a * b;
+  return true;
+}
+
+qk_status map_cuda(cudaError_t e) { return e == cudaSuccess ? QK_OK : QK_ERR_CUDA; }
+
+qk_status dequant(QType t, const void* blocks, int64_t n_blocks, float* out, cudaStream_t s) {
+  if (n_blocks < 0) return QK_ERR_SHAPE;
+  if (n_blocks == 0) return QK_OK;
+  if (!blocks || !out) return QK_ERR_NULL;
+  if (!aligned16(blocks) || !aligned16(out)) return QK_ERR_ALIGN;
+  int64_t in_bytes, out_elems, out_bytes;
+  if (!mul_ok(n_blocks, qk::block_bytes(t), &in_bytes) || !mul_ok(n_blocks, qk::kQK, &out_elems) ||
+      !mul_ok(out_elems, 4, &out_bytes))
+    return QK_ERR_SHAPE;
+  qk_status st = check_device();
+  if (st != QK_OK) return st;
+  if ((st = check_pointer(blocks)) != QK_OK || (st = check_pointer(out)) != QK_OK) return st;
+  if (overlaps(blocks, in_bytes, out, out_bytes)) return QK_ERR_ALIAS;
+  return map_cuda(qk::launch_dequant(t, blocks, n_blocks, out, s));
+}
+
+qk_status matmul(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N,
+                 int64_t K, bool gateup, cudaStream_t s) {
+  if (M < 0 || N < 0 || K < 0) return QK_ERR_SHAPE;
+  if (K == 0 || K % qk::kQK != 0) return QK_ERR_SHAPE;
+  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return QK_ERR_SHAPE;
+  if (M == 0 || N == 0) return QK_OK;
+  if (!W || !x || !y || (gateup && !W_up)) return QK_ERR_NULL;
+  if (!aligned16(W) || !aligned16(x) || !aligned16(y) || (gateup && !aligned16(W_up))) return QK_ERR_ALIGN;
+  int64_t w_bytes, x_elems, x_bytes, y_elems, y_bytes;
+  if (!mul_ok(N, (K / qk::kQK) * qk::block_bytes(t), &w_bytes) || !mul_ok(M, K, &x_elems) ||
+      !mul_ok(x_elems, 2, &x_bytes) || !mul_ok(M, N, &y_elems) || !mul_ok(y_elems, gateup ? 2 : 4, &y_bytes))
+    return QK_ERR_SHAPE;
+  qk_status st = check_device();
+  if (st != QK_OK) return st;
+  if ((st = check_pointer(W)) != QK_OK || (st = check_pointer(x)) != QK_OK || (st = check_pointer(y)) != QK_OK)
+    return st;
+  if (gateup && (st = check_pointer(W_up)) != QK_OK) return st;
+  if (overlaps(y, y_bytes, x, x_bytes) || overlaps(y, y_bytes, W, w_bytes) ||
+      (gateup && overlaps(y, y_bytes, W_up, w_bytes)))
+    return QK_ERR_ALIAS;
+  if (!gateup && M <= qk::gemv_max_m())
+    return map_cuda(qk::launch_gemv(t, W, x, static_cast<float*>(y), N, K, s));
+  return map_cuda(qk::launch_gemm(t, W, W_up, x, y, M, N, K, gateup, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+qk_status qk_dequant_q4k(const void* blocks, int64_t n_blocks, float* out, qk_stream_t stream) {
+  return dequant(qk::kQ4K, blocks, n_blocks, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qk_status qk_dequant_q6k(const void* blocks, int64_t n_blocks, float* out, qk_stream_t stream) {
+  return dequant(qk::kQ6K, blocks, n_blocks, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qk_status qk_matmul_q4k(const void* blocks, const uint16_t* x_f16, float* y, int64_t M, int64_t N, int64_t K,
+                        qk_stream_t stream) {
+  return matmul(qk::kQ4K, blocks, nullptr, x_f16, y, M, N, K, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qk_status qk_matmul_q6k(const void* blocks, const uint16_t* x_f16, float* y, int64_t M, int64_t N, int64_t K,
+                        qk_stream_t stream) {
+  return matmul(qk::kQ6K, blocks, nullptr, x_f16, y, M, N, K, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qk_status qk_gateup_swiglu_q4k(const void* gate_blocks, const void* up_blocks, const uint16_t* x_f16,
+                               uint16_t* y_f16, int64_t M, int64_t N_ff, int64_t K, qk_stream_t stream) {
+  return matmul(qk::kQ4K, gate_blocks, up_blocks, x_f16, y_f16, M, N_ff, K, true,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+qk_status qk_get_device_status(qk_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QK_ERR_CUDA;
+  const uint32_t v = qk::dequant_take_status() | qk::gemv_take_status() | qk::gemm_take_status();
+  return v ? QK_ERR_TIMEOUT : QK_OK;
+}
+
+const char* qk_status_string(qk_status status) {
+  switch (status) {
+    case QK_OK: return "QK_OK";
+    case QK_ERR_NULL: return "QK_ERR_NULL: a required pointer is NULL";
+    case QK_ERR_ALIGN: return "QK_ERR_ALIGN: a pointer is not 16-byte aligned";
+    case QK_ERR_SHAPE: return "QK_ERR_SHAPE: K must be a positive multiple of 256 and sizes non-negative";
+    case QK_ERR_CUDA: return "QK_ERR_CUDA: a CUDA call or kernel launch failed";
+    case QK_ERR_TIMEOUT: return "QK_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+    case QK_ERR_UNSUPPORTED_DEVICE: return "QK_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
+    case QK_ERR_ALIAS: return "QK_ERR_ALIAS: the output overlaps an input";
+    case QK_ERR_POINTER: return "QK_ERR_POINTER: a pointer is not accessible from the current device";
+    default: return "unknown qk_status";
+  }
+}
+
+int qk_version(void) { return 100; }
+
+}  // extern "C"

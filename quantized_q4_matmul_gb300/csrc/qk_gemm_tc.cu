@@ -1,0 +1,652 @@
+// qk_gemm_tc.cu -- prefill GEMM on the 5th-generation tensor cores (tcgen05):
+// y[m][n] = sum_k x[m][k] * w[n][k] with Q4_K / Q6_K weights dequantized on
+// the fly, plus the fused gate/up + SwiGLU variant.
+//
+// Source: DAMASCUS project overview, "[01] the thesis" (prefill is the whole
+// prompt at once, GEMM-heavy and compute-bound; fused dequant feeding the
+// matrix unit never materializes fp16 weights) and "[04] one decode step"
+// (QKV, SwiGLU FFN, LM head over every prompt position); "Building DAMASCUS",
+// "Prefill and decode need different performance questions".
+//
+// Design (one CTA per 128-weight-row x BN-token output tile, swap-AB so the
+// weights are the UMMA A operand with M = 128 and the tokens are N = BN):
+//   warp 0      producer: TMA loads of the x tile (BN x 64 fp16, 128-byte
+//               swizzle) per 64-wide K step, and of the packed blocks of the
+//               128 weight rows per 256-wide super-block.
+//   warp 1      allocates tensor memory; one thread issues tcgen05.mma
+//               (kind::f16, fp32 accumulate in TMEM) and tcgen05.commit.
+//   warps 2..   dequantize the packed blocks into fp16 A tiles written straight
+//               into shared memory in the UMMA 128-byte-swizzle K-major layout
+//               (the fp16 weights never touch device memory), then run the
+//               epilogue: tcgen05.ld of the accumulator, fp32 y stores or
+//               silu(g) * u -> fp16.
+// Pipelines: packed blocks (PS stages, one super-block each), and K steps
+// (S stages, each an x tile + an A tile).  All waits are bounded mbarrier
+// waits; a timeout raises a device status flag and the CTA drains and exits.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+
+#include "qk_device.cuh"
+#include "qk_internal.h"
+
+namespace qk {
+
+__device__ uint32_t g_gemm_status = 0;
+
+namespace {
+
+constexpr int kBM = 128;               // weight rows per tile (UMMA M)
+constexpr int kBK = 64;                // K per step: one 128-byte swizzle row of fp16
+constexpr int kMaxBN = 256;            // tokens per tile (UMMA N), multiple of 16
+constexpr int kXStageBytes = kMaxBN * kBK * 2;  // 32 KB
+constexpr int kAStageBytes = kBM * kBK * 2;     // 16 KB
+constexpr int kQ6Pitch = 240;          // smem bytes per Q6_K row slot (224 used)
+constexpr uint32_t kH2Magic = 0x64646464u;
+
+template <int QT, bool GATEUP>
+struct Cfg {
+  static constexpr int kDqWarps = GATEUP ? 8 : 4;
+  static constexpr int kThreads = 64 + 32 * kDqWarps;
+  static constexpr int kNumB = GATEUP ? 2 : 1;  // weight tensors per tile
+  static constexpr int kStages = GATEUP ? 2 : 3;
+  static constexpr int kPStages = 2;
+  static constexpr int kPStageBytes =
+      QT == kQ4K ? kBM * kQ4KBytes : (kBM * kQ6Pitch + 16 + 1023) / 1024 * 1024;
+  static constexpr int kXOff = 0;
+  static constexpr int kAOff = kXOff + kStages * kXStageBytes;
+  static constexpr int kPOff = kAOff + kStages * kNumB * kAStageBytes;
+  static constexpr int kBarOff = kPOff + kPStages * kNumB * ((kPStageBytes + 1023) / 1024 * 1024);
+  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
+};
+
+struct Bars {
+  uint64_t x_full[4];
+  uint64_t a_full[4];
+  uint64_t s_empty[4];
+  uint64_t p_full[4];
+  uint64_t p_empty[4];
+  uint64_t acc_full;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+struct Params {
+  const uint8_t* w[2];  // packed weights (gate, up) -- Q6_K path reads through plain bulk copies
+  int64_t w_bytes;      // bytes of each weight tensor
+  void* y;
+  int M, N, K, BN;
+};
+
+__device__ __forceinline__ float h2f(uint32_t bits) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(bits & 0xFFFFu)));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+__device__ __forceinline__ __half2 bits_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
+
+// Offset of 16-byte chunk j (k = 8j .. 8j+7) of row r in a 128 x 64 fp16 tile
+// stored in the UMMA 128-byte-swizzle K-major layout.
+__device__ __forceinline__ uint32_t sw128_off(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
+
+// Four weights from four quant bytes (each < 16) of `b4`: the byte goes into
+// the mantissa of 1024.0 (exact fp16 1024 + q), 1024 is subtracted exactly,
+// then w = fp16(q * dsc - dmn); the two results hold k, k+1 and k+2, k+3.
+__device__ __forceinline__ void q4_emit4(uint32_t b4, __half2 dsc2, __half2 ndmn2, uint4& out0) {
+  // b4 holds four quant values (one per byte) for k, k+1, k+2, k+3.
+  const __half2 k1024 = __float2half2_rn(1024.0f);
+  const __half2 p0 = __hsub2(bits_h2(prmt(b4, kH2Magic, 0x4140u)), k1024);
+  const __half2 p1 = __hsub2(bits_h2(prmt(b4, kH2Magic, 0x4342u)), k1024);
+  out0.x = h2_bits(__hfma2(p0, dsc2, ndmn2));
+  out0.y = h2_bits(__hfma2(p1, dsc2, ndmn2));
+}
+
+// Scale and min of sub-block j (0..7) from the 12 packed bytes held in three
+// little-endian words s03, s47, s811.
+__device__ __forceinline__ void q4_scale_min(uint32_t s03, uint32_t s47, uint32_t s811, int j, float& sc,
+                                             float& mn) {
+  uint32_t a, b;
+  if (j < 4) {
+    a = (s03 >> (8 * j)) & 63u;
+    b = (s47 >> (8 * j)) & 63u;
+  } else {
+    const int jj = j - 4;
+    const uint32_t lo = (s811 >> (8 * jj)) & 0xFFu;
+    a = (lo & 0xFu) | (((s03 >> (8 * jj + 6)) & 3u) << 4);
+    b = (lo >> 4) | (((s47 >> (8 * jj + 6)) & 3u) << 4);
+  }
+  sc = (float)a;
+  mn = (float)b;
+}
+
+// Dequantize K step c (0..3) of a Q4_K super-block row held at `rowp` in
+// shared memory into 64 fp16 weights of row r of the swizzled A tile.
+__device__ __forceinline__ void q4_kstep(const uint8_t* rowp, int c, uint8_t* a_tile, int r) {
+  const uint4 hdr = *reinterpret_cast<const uint4*>(rowp);
+  const float d = h2f(hdr.x), dmin = h2f(hdr.x >> 16);
+  float sc0, mn0, sc1, mn1;
+  q4_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, mn0);
+  q4_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, mn1);
+  const __half2 dsc_lo = __float2half2_rn(d * sc0), ndmn_lo = __float2half2_rn(-(dmin * mn0));
+  const __half2 dsc_hi = __float2half2_rn(d * sc1), ndmn_hi = __float2half2_rn(-(dmin * mn1));
+  const uint4 qa = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * c);
+  const uint4 qb = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * c + 16);
+  const uint32_t wv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // chunk j: k = 8j..8j+7 (low nibbles of words 2j, 2j+1)
+    uint4 o;
+    uint4 t;
+    q4_emit4(wv[2 * j] & 0x0F0F0F0Fu, dsc_lo, ndmn_lo, t);
+    o.x = t.x;
+    o.y = t.y;
+    q4_emit4(wv[2 * j + 1] & 0x0F0F0F0Fu, dsc_lo, ndmn_lo, t);
+    o.z = t.x;
+    o.w = t.y;
+    *reinterpret_cast<uint4*>(a_tile + sw128_off(r, j)) = o;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {  // chunk 4+j: k = 32 + 8j .. (high nibbles)
+    uint4 o;
+    uint4 t;
+    q4_emit4((wv[2 * j] >> 4) & 0x0F0F0F0Fu, dsc_hi, ndmn_hi, t);
+    o.x = t.x;
+    o.y = t.y;
+    q4_emit4((wv[2 * j + 1] >> 4) & 0x0F0F0F0Fu, dsc_hi, ndmn_hi, t);
+    o.z = t.x;
+    o.w = t.y;
+    *reinterpret_cast<uint4*>(a_tile + sw128_off(r, 4 + j)) = o;
+  }
+}
+
+// Q6_K.  The block of a row sits in its smem slot at byte offset MIS (even,
+// 0..14: the misalignment of its global address).  The thread reads aligned
+// 16-byte vectors and extracts block word j (bytes MIS+4j .. MIS+4j+3 of the
+// slot) with compile-time indices and, for MIS % 4 == 2, a funnel shift.
+template <int MIS, int N>
+__device__ __forceinline__ uint32_t q6_pick(const uint32_t (&v)[N], int byte_in_v) {
+  // byte_in_v = MIS + offset relative to the first loaded vector (compile-time)
+  const int w = byte_in_v >> 2;
+  if ((byte_in_v & 3) == 0) return v[w];
+  return __funnelshift_r(v[w], v[w + 1], 16);
+}
+
+template <int NV>
+__device__ __forceinline__ void lds_vecs(const uint8_t* p, uint32_t (&v)[4 * NV]) {
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const uint4 t = reinterpret_cast<const uint4*>(p)[i];
+    v[4 * i] = t.x;
+    v[4 * i + 1] = t.y;
+    v[4 * i + 2] = t.z;
+    v[4 * i + 3] = t.w;
+  }
+}
+
+// Dequantize K steps 2h and 2h+1 of a Q6_K block (both use the same ql / qh
+// bytes 64h..64h+63 / 128+32h..+31) into two A tiles.
+template <int MIS>
+__device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* a_tile0, uint8_t* a_tile1, int r) {
+  uint32_t vl[20], vh[12], vs[8];
+  lds_vecs<5>(slot + 64 * h, vl);         // bytes 64h .. 64h+79
+  lds_vecs<3>(slot + 128 + 32 * h, vh);   // bytes 128+32h .. +47
+  lds_vecs<2>(slot + 192, vs);            // bytes 192 .. 223
+  uint32_t ql[16], qh[8];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ql[i] = q6_pick<MIS>(vl, MIS + 4 * i);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) qh[i] = q6_pick<MIS>(vh, MIS + 4 * i);
+  const uint32_t scw0 = h ? q6_pick<MIS>(vs, MIS + 8) : q6_pick<MIS>(vs, MIS);       // scales 8h .. 8h+3
+  const uint32_t scw1 = h ? q6_pick<MIS>(vs, MIS + 12) : q6_pick<MIS>(vs, MIS + 4);  // scales 8h+4 .. 8h+7
+  const uint32_t dw = vs[(16 + MIS) >> 2];
+  const float d = h2f(((16 + MIS) & 3) ? (dw >> 16) : dw);
+  const __half2 k1056 = __float2half2_rn(1056.0f);  // 1024 + 32
+#pragma unroll
+  for (int side = 0; side < 2; ++side) {  // K step 2h + side
+    uint8_t* a_tile = side ? a_tile1 : a_tile0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {  // chunk j: step-local k = 8j .. 8j+7
+      const int g = 2 * side + (j >> 2);     // 32-weight group within the half
+      const int sidx = 4 * side + (j >> 1);  // 16-weight scale group within the half
+      const uint32_t scw = sidx < 4 ? scw0 : scw1;
+      const float sc = (float)(int8_t)((scw >> (8 * (sidx & 3))) & 0xFFu);
+      const __half2 dsc2 = __float2half2_rn(d * sc);
+      uint32_t o[4];
+#pragma unroll
+      for (int ww = 0; ww < 2; ++ww) {
+        const int i = 2 * j + ww;  // ql word: bytes 64h + 4i, step-local k = 4i .. 4i+3
+        const uint32_t lo4 = (side ? (ql[i] >> 4) : ql[i]) & 0x0F0F0F0Fu;
+        const uint32_t qhw = qh[i & 7];
+        const int sh = 4 - 2 * g;  // bits 2g..2g+1 of every byte -> bits 4..5
+        const uint32_t hs = sh >= 0 ? (qhw << sh) : (qhw >> (-sh));
+        const uint32_t q6 = lo4 | (hs & 0x30303030u);
+        const __half2 p0 = __hsub2(bits_h2(prmt(q6, kH2Magic, 0x4140u)), k1056);
+        const __half2 p1 = __hsub2(bits_h2(prmt(q6, kH2Magic, 0x4342u)), k1056);
+        o[2 * ww] = h2_bits(__hmul2(p0, dsc2));
+        o[2 * ww + 1] = h2_bits(__hmul2(p1, dsc2));
+      }
+      *reinterpret_cast<uint4*>(a_tile + sw128_off(r, j)) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+  }
+}
+
+__device__ __forceinline__ void q6_half_dispatch(int mis, const uint8_t* slot, int h, uint8_t* t0, uint8_t* t1,
+                                                 int r) {
+  switch (mis) {
+    case 0: q6_half<0>(slot, h, t0, t1, r); break;
+    case 2: q6_half<2>(slot, h, t0, t1, r); break;
+    case 4: q6_half<4>(slot, h, t0, t1, r); break;
+    case 6: q6_half<6>(slot, h, t0, t1, r); break;
+    case 8: q6_half<8>(slot, h, t0, t1, r); break;
+    case 10: q6_half<10>(slot, h, t0, t1, r); break;
+    case 12: q6_half<12>(slot, h, t0, t1, r); break;
+    default: q6_half<14>(slot, h, t0, t1, r); break;
+  }
+}
+
+// Slot of tile row rho in a Q6_K packed stage: pitch 240 bytes plus a 16-byte
+// skew on every second group of 8 rows, so the 16-byte reads of 8 consecutive
+// threads (rows rho = 2i + p, see dq_row) hit 8 different bank groups:
+// (15*rho + skew) mod 8 = (6i + 7p + skew) mod 8 is distinct for i = 0..7.
+__device__ __forceinline__ uint32_t q6_slot(int rho) { return (uint32_t)(rho * kQ6Pitch + 16 * ((rho >> 3) & 1)); }
+
+// Row handled by dequant thread t (0..127) of one weight tensor.  Q6_K groups
+// rows of equal parity in a warp so that, for the common K, the misalignment
+// of their blocks is warp-uniform.
+template <int QT>
+__device__ __forceinline__ int dq_row(int t) {
+  if constexpr (QT == kQ4K) {
+    return t;
+  } else {
+    const int w = t >> 5, i = t & 31;
+    return 2 * i + (w & 1) + 64 * (w >> 1);
+  }
+}
+
+template <int QT, bool GATEUP>
+__global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
+                   const __grid_constant__ CUtensorMap tm_w1, const Params p) {
+  using C = Cfg<QT, GATEUP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
+  volatile uint32_t* abort_flag = &bars->abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n0 = blockIdx.x * kBM;
+  const int m0 = blockIdx.y * p.BN;
+  const int nb = p.K / kQK;
+  const int nsteps = nb * 4;
+  const int BN = p.BN;
+  const uint32_t x_bytes = (uint32_t)BN * kBK * 2;
+  constexpr int kPSlotBytes = (C::kPStageBytes + 1023) / 1024 * 1024;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(&bars->x_full[s], 1);
+      mbar_init(&bars->a_full[s], 32 * C::kDqWarps);
+      mbar_init(&bars->s_empty[s], 1);
+    }
+    for (int s = 0; s < C::kPStages; ++s) {
+      mbar_init(&bars->p_full[s], QT == kQ4K ? 1 : 32);
+      mbar_init(&bars->p_empty[s], 32 * C::kDqWarps);
+    }
+    mbar_init(&bars->acc_full, 1);
+    bars->abort_flag = 0;
+    fence_mbar_init();
+  }
+  const uint32_t tmem_cols = GATEUP ? (BN <= 64 ? 128 : BN <= 128 ? 256 : 512)
+                                    : (BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256);
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_x);
+      if (QT == kQ4K) {
+        prefetch_tmap(&tm_w0);
+        if (GATEUP) prefetch_tmap(&tm_w1);
+      }
+    }
+    int step = 0;
+    bool ok = true;
+    for (int kb = 0; kb < nb && ok; ++kb) {
+      const int ps = kb % C::kPStages;
+      const uint32_t pph = (uint32_t)(kb / C::kPStages) & 1u;
+      ok = mbar_wait(&bars->p_empty[ps], pph ^ 1u, abort_flag, &g_gemm_status);
+      if (!ok) break;
+      uint8_t* pst = smem + C::kPOff + ps * C::kNumB * kPSlotBytes;
+      if constexpr (QT == kQ4K) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(C::kNumB * kBM * kQ4KBytes));
+          tma_load_2d(pst, &tm_w0, kb * kQ4KBytes, n0, &bars->p_full[ps]);
+          if (GATEUP) tma_load_2d(pst + kPSlotBytes, &tm_w1, kb * kQ4KBytes, n0, &bars->p_full[ps]);
+        }
+      } else {
+        // One bulk copy per row of the 16-byte-aligned 224-byte window around
+        // its 210-byte block.  Rows past N are skipped; a window that would run
+        // past the end of the tensor is shortened and its last bytes copied by
+        // plain loads.  Each lane announces its bytes before issuing its copies
+        // and arrives after its plain stores.
+        const int64_t RB = (int64_t)nb * kQ6KBytes;
+        uint32_t bytes = 0;
+        for (int i = lane; i < kBM; i += 32) {
+          const int n = n0 + i;
+          if (n >= p.N) continue;
+          const int64_t g = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
+          const int64_t lo = g & ~int64_t(15);
+          bytes += (uint32_t)(lo + 224 <= p.w_bytes ? 224 : ((p.w_bytes - lo) & ~int64_t(15)));
+        }
+        mbar_expect_tx(&bars->p_full[ps], bytes);
+        for (int i = lane; i < kBM; i += 32) {
+          const int n = n0 + i;
+          if (n >= p.N) continue;
+          const int64_t g = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
+          const int64_t lo = g & ~int64_t(15);
+          const int64_t len = lo + 224 <= p.w_bytes ? 224 : ((p.w_bytes - lo) & ~int64_t(15));
+          uint8_t* dst = pst + q6_slot(i);
+          bulk_copy_g2s(dst, p.w[0] + lo, (uint32_t)len, &bars->p_full[ps]);
+          for (int64_t b = lo + len; b < g + kQ6KBytes; b += 2)  // tail bytes (only at the tensor's end)
+            *reinterpret_cast<uint16_t*>(dst + (b - lo)) = *reinterpret_cast<const uint16_t*>(p.w[0] + b);
+        }
+        mbar_arrive(&bars->p_full[ps]);
+      }
+      for (int c = 0; c < 4 && ok; ++c, ++step) {
+        const int s = step % C::kStages;
+        const uint32_t ph = (uint32_t)(step / C::kStages) & 1u;
+        ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
+        if (!ok) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bars->x_full[s], x_bytes);
+          tma_load_2d(smem + C::kXOff + s * kXStageBytes, &tm_x, kb * kQK + c * kBK, m0, &bars->x_full[s]);
+        }
+        __syncwarp();
+      }
+    }
+    // Drain: every x copy this warp issued has completed before the CTA exits
+    // (the packed-block copies are drained by the dequant warps' waits).
+    for (int i = 0; i < C::kStages && i < step; ++i) {
+      const int st = step - 1 - i;
+      mbar_wait(&bars->x_full[st % C::kStages], (uint32_t)(st / C::kStages) & 1u, abort_flag, &g_gemm_status,
+                true);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = umma_idesc_f16(kBM, (uint32_t)BN);
+    bool ok = true;
+    int step = 0;
+    for (; step < nsteps && ok; ++step) {
+      const int s = step % C::kStages;
+      const uint32_t ph = (uint32_t)(step / C::kStages) & 1u;
+      ok = mbar_wait(&bars->x_full[s], ph, abort_flag, &g_gemm_status) &&
+           mbar_wait(&bars->a_full[s], ph, abort_flag, &g_gemm_status);
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t xa = smem_u32(smem + C::kXOff + s * kXStageBytes);
+        const uint64_t bdesc = umma_desc_sw128(xa);
+#pragma unroll
+        for (int t = 0; t < C::kNumB; ++t) {
+          const uint32_t aa = smem_u32(smem + C::kAOff + (s * C::kNumB + t) * kAStageBytes);
+          const uint64_t adesc = umma_desc_sw128(aa);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            // +32 bytes per 16-wide K slice inside the swizzle atom (start address in 16 B units)
+            umma_f16_ss(tmem + (uint32_t)(t * BN), adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                        (step > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        umma_commit(&bars->s_empty[s]);
+        if (step == nsteps - 1) umma_commit(&bars->acc_full);
+      }
+      __syncwarp();
+    }
+    // Drain: the UMMAs issued last have finished reading shared memory and
+    // writing tensor memory before tensor memory is freed.
+    if (step > 0) {
+      const int st = step - 1;
+      mbar_wait(&bars->s_empty[st % C::kStages], (uint32_t)(st / C::kStages) & 1u, abort_flag, &g_gemm_status,
+                true);
+    }
+  } else {
+    // ------------------------------------------------------------------ dequant + epilogue
+    const int t = threadIdx.x - 64;          // 0 .. 32*kDqWarps-1
+    const int which = t >> 7;                // weight tensor (0 = gate/only, 1 = up)
+    const int rho = dq_row<QT>(t & 127);     // tile row this thread dequantizes
+    const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
+    int step = 0;
+    bool ok = true;
+    for (int kb = 0; kb < nb && ok; ++kb) {
+      const int ps = kb % C::kPStages;
+      const uint32_t pph = (uint32_t)(kb / C::kPStages) & 1u;
+      ok = mbar_wait(&bars->p_full[ps], pph, abort_flag, &g_gemm_status);
+      if (!ok) break;
+      const uint8_t* pst = smem + C::kPOff + (ps * C::kNumB + which) * kPSlotBytes;
+      if constexpr (QT == kQ4K) {
+        const uint8_t* rowp = pst + rho * kQ4KBytes;
+        for (int c = 0; c < 4; ++c, ++step) {
+          const int s = step % C::kStages;
+          const uint32_t ph = (uint32_t)(step / C::kStages) & 1u;
+          ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
+          if (!ok) break;
+          uint8_t* a_tile = smem + C::kAOff + (s * C::kNumB + which) * kAStageBytes;
+          q4_kstep(rowp, c, a_tile, rho);
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->a_full[s]);
+        }
+      } else {
+        const int n = min(n0 + rho, p.N - 1);
+        const int mis = (int)(((int64_t)n * RB + (int64_t)kb * kQ6KBytes) & 15);
+        const uint8_t* slot = pst + q6_slot(rho);
+        for (int h = 0; h < 2 && ok; ++h, step += 2) {
+          const int s0 = step % C::kStages, s1 = (step + 1) % C::kStages;
+          const uint32_t ph0 = (uint32_t)(step / C::kStages) & 1u, ph1 = (uint32_t)((step + 1) / C::kStages) & 1u;
+          ok = mbar_wait(&bars->s_empty[s0], ph0 ^ 1u, abort_flag, &g_gemm_status) &&
+               mbar_wait(&bars->s_empty[s1], ph1 ^ 1u, abort_flag, &g_gemm_status);
+          if (!ok) break;
+          uint8_t* t0 = smem + C::kAOff + (s0 * C::kNumB + which) * kAStageBytes;
+          uint8_t* t1 = smem + C::kAOff + (s1 * C::kNumB + which) * kAStageBytes;
+          q6_half_dispatch(mis, slot, h, t0, t1, rho);
+          fence_proxy_async_smem();
+          mbar_arrive(&bars->a_full[s0]);
+          mbar_arrive(&bars->a_full[s1]);
+        }
+      }
+      if (ok) mbar_arrive(&bars->p_empty[ps]);
+    }
+
+    // -------------------------------------------------------------- epilogue
+    if (ok) ok = mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status);
+    if (ok) {
+      tc_fence_after();
+      const int q = warp & 3;                 // TMEM lane quarter this warp may access
+      const int row = q * 32 + lane;
+      const int n = n0 + row;
+      const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+      const int nchunks = BN / 16;
+      if constexpr (!GATEUP) {
+        float* y = static_cast<float*>(p.y);
+        for (int cc = 0; cc < nchunks; ++cc) {
+          uint32_t r[16];
+          tmem_ld16(lane_addr + (uint32_t)(16 * cc), r);
+          tmem_wait_ld();
+          if (n < p.N) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int m = m0 + 16 * cc + i;
+              if (m < p.M) y[(int64_t)m * p.N + n] = __uint_as_float(r[i]);
+            }
+          }
+        }
+      } else {
+        __half* y = static_cast<__half*>(p.y);
+        const int half_chunks = (nchunks + 1) / 2;
+        const int c_begin = which ? half_chunks : 0;
+        const int c_end = which ? nchunks : half_chunks;
+        for (int cc = c_begin; cc < c_end; ++cc) {
+          uint32_t rg[16], ru[16];
+          tmem_ld16(lane_addr + (uint32_t)(16 * cc), rg);
+          tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), ru);
+          tmem_wait_ld();
+          if (n < p.N) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int m = m0 + 16 * cc + i;
+              const float g = __uint_as_float(rg[i]);
+              const float u = __uint_as_float(ru[i]);
+              const float o = g / (1.0f + __expf(-g)) * u;
+              if (m < p.M) y[(int64_t)m * p.N + n] = __float2half_rn(o);
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+bool make_tmap_x(CUtensorMap* tm, const void* x, int64_t M, int64_t K, int BN) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)BN};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Q4_K weights as a byte matrix [N][row_bytes]; one box = one super-block
+// (144 bytes) of 128 rows.
+bool make_tmap_q4k(CUtensorMap* tm, const void* w, int64_t N, int64_t K) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int64_t rb = (K / kQK) * kQ4KBytes;
+  const cuuint64_t dims[2] = {(cuuint64_t)rb, (cuuint64_t)N};
+  const cuuint64_t strides[1] = {(cuuint64_t)rb};
+  const cuuint32_t box[2] = {(cuuint32_t)kQ4KBytes, (cuuint32_t)kBM};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(w), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int g_sms_tc = 0;
+
+int num_sms() {
+  if (!g_sms_tc) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_sms_tc, cudaDevAttrMultiProcessorCount, dev);
+    if (g_sms_tc <= 0) g_sms_tc = 148;
+  }
+  return g_sms_tc;
+}
+
+// Token tile: the multiple of 16 (<= 256) that minimises waves x tile cost.
+int choose_bn(int64_t M, int64_t N) {
+  const int64_t ntn = (N + kBM - 1) / kBM;
+  if (M <= kMaxBN) return (int)((M + 15) / 16 * 16);
+  int best = kMaxBN;
+  double best_cost = 1e30;
+  for (int bn = 128; bn <= kMaxBN; bn += 16) {
+    const int64_t tiles = ntn * ((M + bn - 1) / bn);
+    const int64_t waves = (tiles + num_sms() - 1) / num_sms();
+    const double cost = (double)waves * (bn + 32);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = bn;
+    }
+  }
+  return best;
+}
+
+template <int QT, bool GATEUP>
+cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
+                      cudaStream_t stream) {
+  using C = Cfg<QT, GATEUP>;
+  const int BN = choose_bn(M, N);
+  CUtensorMap tx, tw0, tw1;
+  memset(&tw0, 0, sizeof(tw0));
+  memset(&tw1, 0, sizeof(tw1));
+  if (!make_tmap_x(&tx, x, M, K, BN)) return cudaErrorInvalidValue;
+  if (QT == kQ4K) {
+    if (!make_tmap_q4k(&tw0, W0, N, K)) return cudaErrorInvalidValue;
+    if (GATEUP && !make_tmap_q4k(&tw1, W1, N, K)) return cudaErrorInvalidValue;
+  }
+  Params p;
+  p.w[0] = static_cast<const uint8_t*>(W0);
+  p.w[1] = static_cast<const uint8_t*>(W1);
+  p.w_bytes = N * (K / kQK) * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
+  p.y = y;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.BN = BN;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  dim3 grid((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + BN - 1) / BN));
+  if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
+  gemm_tc_kernel<QT, GATEUP><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tx, tw0, tw1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+uint32_t gemm_take_status() {
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(zero));
+  return v;
+}
+
+cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N,
+                        int64_t K, bool gateup, cudaStream_t s) {
+  if (gateup) return launch_tc<kQ4K, true>(W, W_up, x, y, M, N, K, s);
+  if (t == kQ4K) return launch_tc<kQ4K, false>(W, nullptr, x, y, M, N, K, s);
+  return launch_tc<kQ6K, false>(W, nullptr, x, y, M, N, K, s);
+}
+
+}  // namespace qk

@@ -1,0 +1,36 @@
+// qk_internal.h -- host-side declarations shared by the library's translation
+// units (launchers, status words).  Not part of the public C ABI.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/qk.h"
+
+namespace qk {
+
+enum QType : int { kQ4K = 0, kQ6K = 1 };
+
+constexpr int kQK = 256;
+constexpr int kQ4KBytes = 144;
+constexpr int kQ6KBytes = 210;
+
+inline int64_t block_bytes(QType t) { return t == kQ4K ? kQ4KBytes : kQ6KBytes; }
+
+// Each translation unit with kernels that can time out owns one device status
+// word; these read it (after the stream has been synchronised) and clear it.
+uint32_t dequant_take_status();
+uint32_t gemv_take_status();
+uint32_t gemm_take_status();
+
+// Launchers.  Arguments are already validated; they return cudaGetLastError().
+cudaError_t launch_dequant(QType t, const void* blocks, int64_t n_blocks, float* out, cudaStream_t s);
+cudaError_t launch_gemv(QType t, const void* W, const uint16_t* x, float* y, int64_t N, int64_t K,
+                        cudaStream_t s);
+cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M,
+                        int64_t N, int64_t K, bool gateup, cudaStream_t s);
+
+// Largest M the decode GEMV handles; larger M goes to the tensor-core GEMM.
+int gemv_max_m();
+
+}  // namespace qk

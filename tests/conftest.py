@@ -1,6 +1,8 @@
 import os
 import sys
 
+import pytest
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -8,3 +10,21 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built CUDA library")
+
+
+@pytest.fixture(scope="session")
+def qk_lib():
+    """The CUDA library, built in-tree if needed (nvcc cross-compiles without a GPU)."""
+    from quantized_q4_matmul_gb300 import build as qk_build
+    qk_build.build()
+    import quantized_q4_matmul_gb300 as qk
+    return qk
+
+
+@pytest.fixture(scope="session")
+def cuda(qk_lib):
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")

@@ -1,0 +1,252 @@
+"""GPU path against the oracle, through the C ABI.
+
+Bars (stated by the workload definition):
+* dequant: bit-exact fp32 (NaN matches NaN);
+* matmul: max |y - y_oracle| <= 1e-2 * rms(y_oracle) per call;
+* gate/up + SwiGLU, whose output format is fp16: the same bar on top of the
+  output's own rounding, i.e. |y - y_oracle| - ulp16(y)/2 <= 1e-2 * rms(y_oracle)
+  (the SwiGLU output is heavy-tailed, max ~ 25 x rms, so fp16 rounding of the
+  largest outputs alone reaches ~0.7% of rms).
+Inputs are the seeded synthetic weights / activations of ``tests/synth.py``.
+Full-size workloads are checked on seeded samples of output rows (all tokens),
+which the oracle computes one row at a time.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tests import synth
+from tests.oracle_pins import random_blocks, same_bits
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-2
+QT = {"q4k": oracle.Q4K, "q6k": oracle.Q6K}
+
+
+def _dev(a, cuda):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a)).to(cuda)
+
+
+def _x_dev(x, cuda):
+    return _dev(x.view(np.uint16), cuda)
+
+
+def gpu_matmul(qk, qtype, W, x, N, K, cuda, rows=None):
+    import torch
+    M = x.shape[0]
+    y = torch.empty(M, N, dtype=torch.float32, device=cuda)
+    fn = qk.qk_matmul_q4k if qtype == "q4k" else qk.qk_matmul_q6k
+    fn(_dev(W, cuda), _x_dev(x, cuda), y, M, N, K)
+    qk.qk_get_device_status()
+    y = y.cpu().numpy().astype(np.float64)
+    return y if rows is None else y[:, rows]
+
+
+def check_close(got, ref, what):
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    assert np.isfinite(got).all(), what
+    assert err <= TOL * rms, "%s: max|err| %.3e > %.0e * rms %.3e" % (what, err, TOL, rms)
+    return err / rms if rms else 0.0
+
+
+def check_close_f16out(got, ref, what):
+    """As check_close for an fp16 output: the output format's own rounding (half an
+    fp16 ulp of the value) is allowed on top of the 1e-2 * rms bar."""
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    mag = np.maximum(np.abs(ref), np.abs(got))
+    half_ulp = np.ldexp(0.5, np.floor(np.log2(np.maximum(mag, 2.0 ** -14))).astype(np.int64) - 10)
+    err = np.abs(got - ref)
+    assert np.isfinite(got).all(), what
+    worst = float(np.max(err - half_ulp)) if ref.size else 0.0
+    assert worst <= TOL * rms, "%s: max(|err| - half_ulp) %.3e > %.0e * rms %.3e" % (what, worst, TOL, rms)
+
+
+def sample_rows(N, n, seed):
+    rng = synth.rng_for(seed, 777)
+    k = min(N, n)
+    rows = rng.choice(N, size=k, replace=False)
+    rows[0], rows[-1] = 0, N - 1
+    return np.unique(rows)
+
+
+# ---------------------------------------------------------------------------
+# Dequant
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("qtype", ["q4k", "q6k"])
+@pytest.mark.parametrize("nb", [1, 7, 33, 4099, 250_000])
+def test_dequant_bit_exact(qk_lib, cuda, qtype, nb):
+    import torch
+    blocks = random_blocks(QT[qtype], nb, seed=nb)
+    out = torch.empty(nb * 256, dtype=torch.float32, device=cuda)
+    fn = qk_lib.qk_dequant_q4k if qtype == "q4k" else qk_lib.qk_dequant_q6k
+    fn(_dev(blocks, cuda), nb, out)
+    qk_lib.qk_get_device_status()
+    assert same_bits(out.cpu().numpy(), oracle.dequant(QT[qtype], blocks))
+
+
+def test_dequant_into_unaligned_tail_region(qk_lib, cuda):
+    # Q6_K blocks are 210 bytes: an odd block count leaves the tensor end 2 mod 16.
+    import torch
+    blocks = random_blocks(oracle.Q6K, 3, seed=5)
+    out = torch.empty(3 * 256, dtype=torch.float32, device=cuda)
+    qk_lib.qk_dequant_q6k(_dev(blocks, cuda), 3, out)
+    assert same_bits(out.cpu().numpy(), oracle.dequant(oracle.Q6K, blocks))
+
+
+# ---------------------------------------------------------------------------
+# Matmul: small shapes spanning several tiles with ragged tails
+# ---------------------------------------------------------------------------
+SHAPES = [
+    (1, 128, 256), (1, 200, 768), (1, 1024, 3072), (1, 40, 8192),
+    (2, 128, 256), (5, 300, 512), (16, 256, 768), (17, 130, 1024),
+    (64, 384, 512), (100, 200, 1280), (256, 128, 2048), (300, 260, 512), (513, 128, 256),
+]
+
+
+@pytest.mark.parametrize("qtype", ["q4k", "q6k"])
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_matmul_small(qk_lib, cuda, qtype, M, N, K):
+    rng = synth.rng_for(M * 7 + N, K)
+    W = synth.weights(rng, qtype, N, K)
+    x = synth.activations(rng, M, K)
+    ref = oracle.matmul(QT[qtype], W, x, N, K)
+    check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "%s M%d N%d K%d" % (qtype, M, N, K))
+
+
+@pytest.mark.parametrize("qtype", ["q4k", "q6k"])
+def test_matmul_deterministic(qk_lib, cuda, qtype):
+    rng = synth.rng_for(3, 3)
+    W = synth.weights(rng, qtype, 256, 1024)
+    for M in (1, 200):
+        x = synth.activations(rng, M, 1024)
+        a = gpu_matmul(qk_lib, qtype, W, x, 256, 1024, cuda)
+        b = gpu_matmul(qk_lib, qtype, W, x, 256, 1024, cuda)
+        assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("qtype", ["q4k", "q6k"])
+def test_matmul_special_scales(qk_lib, cuda, qtype):
+    """Zero, subnormal and large fp16 scale fields (finite)."""
+    rng = synth.rng_for(9, 9)
+    N, K = 128, 512
+    W = synth.weights(rng, qtype, N, K).reshape(-1, 144 if qtype == "q4k" else 210).copy()
+    vals = np.array([0.0, 6e-8, 3e-5, 1e-3, 0.25], np.float16).view(np.uint8).reshape(-1, 2)
+    pick = rng.integers(0, len(vals), size=len(W))
+    if qtype == "q4k":
+        W[:, 0:2] = vals[pick]
+        W[:, 2:4] = vals[rng.integers(0, len(vals), size=len(W))]
+    else:
+        W[:, 208:210] = vals[pick]
+    for M in (1, 48):
+        x = synth.activations(rng, M, K)
+        ref = oracle.matmul(QT[qtype], W, x, N, K)
+        check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "special scales M%d" % M)
+
+
+# ---------------------------------------------------------------------------
+# The workloads at full size
+# ---------------------------------------------------------------------------
+def test_workload_attn_q_m16(qk_lib, cuda):
+    """Single Q4_K matmul, M=16, K=3072, N=3072, seed 0 (checked in full)."""
+    rng = synth.rng_for(0, 0)
+    W = synth.q4k_weights(rng, 3072, 3072)
+    x = synth.activations(rng, 16, 3072)
+    ref = oracle.matmul(oracle.Q4K, W, x, 3072, 3072)
+    check_close(gpu_matmul(qk_lib, "q4k", W, x, 3072, 3072, cuda), ref, "attn_q M16")
+
+
+def test_workload_decode_layer_m1(qk_lib, cuda):
+    """Decode GEMV, M=1, over the seven linears of one layer (checked in full)."""
+    for tag, lin, M in synth.workloads()["decode_layer_m1"].linears:
+        rng = synth.rng_for(1, tag)
+        W = synth.weights(rng, lin.qtype, lin.N, lin.K)
+        x = synth.activations(rng, M, lin.K)
+        ref = oracle.matmul(QT[lin.qtype], W, x, lin.N, lin.K)
+        check_close(gpu_matmul(qk_lib, lin.qtype, W, x, lin.N, lin.K, cuda), ref, lin.name)
+
+
+def test_workload_prefill_gateup_swiglu_m1024(qk_lib, cuda):
+    """Fused gate/up + SwiGLU, M=1024, K=3072, N_ff=8192 (sampled output features)."""
+    import torch
+    rng = synth.rng_for(2, 0)
+    M, N, K = 1024, 8192, 3072
+    Wg = synth.q4k_weights(rng, N, K)
+    Wu = synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, M, K)
+    y = torch.empty(M, N, dtype=torch.float16, device=cuda)
+    qk_lib.qk_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), y, M, N, K)
+    qk_lib.qk_get_device_status()
+    rows = sample_rows(N, 96, 2)
+    ref = oracle.gateup_swiglu(Wg, Wu, x, N, K, rows=rows)
+    check_close_f16out(y.float().cpu().numpy().astype(np.float64)[:, rows], ref, "gate/up swiglu")
+
+
+def test_workload_prefill_down_v_m1024(qk_lib, cuda):
+    """Q6_K down 8192->3072 and attn_v 3072->1024 at M=1024 (sampled output features)."""
+    for tag, lin, M in synth.workloads()["prefill_down_v_m1024"].linears:
+        rng = synth.rng_for(3, tag)
+        W = synth.weights(rng, lin.qtype, lin.N, lin.K)
+        x = synth.swiglu_activations(rng, M, lin.K)
+        rows = sample_rows(lin.N, 64, 3 + tag)
+        ref = oracle.matmul(QT[lin.qtype], W, x, lin.N, lin.K, rows=rows)
+        check_close(gpu_matmul(qk_lib, lin.qtype, W, x, lin.N, lin.K, cuda, rows=rows), ref, lin.name)
+
+
+SWEEP_SHAPES = sorted({(lin.qtype, lin.N, lin.K) for _, lin in synth.model_linears()})
+
+
+@pytest.mark.parametrize("qtype,N,K", SWEEP_SHAPES)
+def test_workload_model_sweep(qk_lib, cuda, qtype, N, K):
+    """Every distinct linear of the 3B model (incl. the tied LM head) at M in 1..2048, sampled rows."""
+    rng = synth.rng_for(4, N + K + (qtype == "q6k"))
+    W = synth.weights(rng, qtype, N, K)
+    Wd = _dev(W, cuda)
+    import torch
+    for M in synth.SWEEP_M:
+        x = synth.activations(rng, M, K)
+        y = torch.empty(M, N, dtype=torch.float32, device=cuda)
+        fn = qk_lib.qk_matmul_q4k if qtype == "q4k" else qk_lib.qk_matmul_q6k
+        fn(Wd, _x_dev(x, cuda), y, M, N, K)
+        qk_lib.qk_get_device_status()
+        rows = sample_rows(N, 24 if M >= 512 else 64, M)
+        ref = oracle.matmul(QT[qtype], W, x, N, K, rows=rows)
+        check_close(y.cpu().numpy().astype(np.float64)[:, rows], ref, "%s N%d K%d M%d" % (qtype, N, K, M))
+        del y
+
+
+# ---------------------------------------------------------------------------
+# Gate/up + SwiGLU small shapes
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("M,N,K", [(1, 128, 256), (16, 256, 512), (37, 200, 768), (300, 384, 1024)])
+def test_gateup_small(qk_lib, cuda, M, N, K):
+    import torch
+    rng = synth.rng_for(M, N + K)
+    Wg = synth.q4k_weights(rng, N, K)
+    Wu = synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, M, K)
+    y = torch.empty(M, N, dtype=torch.float16, device=cuda)
+    qk_lib.qk_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), y, M, N, K)
+    qk_lib.qk_get_device_status()
+    ref = oracle.gateup_swiglu(Wg, Wu, x, N, K)
+    check_close_f16out(y.float().cpu().numpy().astype(np.float64), ref, "gateup M%d N%d K%d" % (M, N, K))
+
+
+# ---------------------------------------------------------------------------
+# Boundary checks that need a device
+# ---------------------------------------------------------------------------
+def test_alias_and_host_pointer_rejected(qk_lib, cuda):
+    import torch
+    L = qk_lib.lib()
+    W = torch.zeros(128 * 144, dtype=torch.uint8, device=cuda)
+    x = torch.zeros(4 * 256, dtype=torch.float16, device=cuda)
+    y = torch.zeros(4 * 128, dtype=torch.float32, device=cuda)
+    s = torch.cuda.current_stream().cuda_stream
+    assert L.qk_matmul_q4k(W.data_ptr(), x.data_ptr(), W.data_ptr(), 4, 128, 256, s) == -7  # y aliases W
+    host = np.zeros(1 << 16, np.uint8)
+    hp = (host.ctypes.data + 15) & ~15
+    assert L.qk_matmul_q4k(hp, x.data_ptr(), y.data_ptr(), 4, 128, 256, s) == -8  # pageable host memory
+    assert L.qk_matmul_q4k(W.data_ptr(), x.data_ptr(), y.data_ptr(), 4, 128, 256, s) == 0
+    assert L.qk_get_device_status(s) == 0
