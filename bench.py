@@ -131,24 +131,26 @@ class Clocks:
 # CPU baseline: the oracle on a bounded sample
 # ----------------------------------------------------------------------------
 def cpu_baseline(target_s: float = 12.0):
+    """The oracle on host cores: gate/up + SwiGLU at M=1024 for as many output
+    features as take about `target_s` seconds (calibrated on a short run)."""
     import oracle
-    gate, up, down, v = prefill_linears()
     rng = synth.rng_for(7, 1)
-    K = synth.HIDDEN
-    Wg = synth.q4k_weights(rng, 64, K)
-    Wu = synth.q4k_weights(rng, 64, K)
+    K, N = synth.HIDDEN, synth.FFN
+    Wg = synth.q4k_weights(rng, N, K)
+    Wu = synth.q4k_weights(rng, N, K)
     x = synth.activations(rng, PREFILL_M, K)
+    probe = 4 * oracle.num_threads()
     t0 = time.perf_counter()
-    oracle.gateup_swiglu(Wg, Wu, x, 64, K, rows=np.arange(4))
+    oracle.gateup_swiglu(Wg, Wu, x, N, K, rows=np.arange(probe))
     dt = max(time.perf_counter() - t0, 1e-3)
-    rows = int(min(64, max(4, 4 * target_s / dt)))
+    rows = int(min(N, max(probe, probe * target_s / dt)))
     t0 = time.perf_counter()
-    oracle.gateup_swiglu(Wg, Wu, x, 64, K, rows=np.arange(rows))
+    oracle.gateup_swiglu(Wg, Wu, x, N, K, rows=np.arange(rows))
     dt = time.perf_counter() - t0
     flops = 2.0 * 2 * PREFILL_M * K * rows
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "gate/up + SwiGLU of %d of 8192 output features at M=1024, K=3072 (fp64 oracle), %.1f s"
-                      % (rows, dt)}
+            "sample": "gate/up + SwiGLU of %d of 8192 output features at M=1024, K=3072 (fp64 oracle, %d "
+                      "threads), %.1f s" % (rows, oracle.num_threads(), dt)}
 
 
 # ----------------------------------------------------------------------------
@@ -192,12 +194,31 @@ class Workload:
         qk.qk_matmul_q6k(d["v"], d["x_v"], self.y_v, PREFILL_M, v.N, v.K, stream)
         return 3
 
-    def decode(self, qk, c, stream):
+    def decode(self, qk, c, stream, side=None):
+        """The seven GEMVs with a decoder layer's dependencies: {q, k, v} share x
+        and may run together, then o, then {gate, up}, then down.  With `side`
+        streams (during graph capture) the independent ones are forked."""
+        torch = self.torch
         d = self.copies[c]
-        for (lin, Wd, xd), y in zip(d["decode"], self.y_dec):
-            fn = qk.qk_matmul_q4k if lin.qtype == synth.Q4K else qk.qk_matmul_q6k
-            fn(Wd, xd, y, 1, lin.N, lin.K, stream)
+        groups = [[0, 1, 2], [3], [4, 5], [6]]
+        main = torch.cuda.current_stream()
+        for grp in groups:
+            if side is None or len(grp) == 1:
+                for i in grp:
+                    self._gemv(qk, d, i, stream)
+                continue
+            for j, i in enumerate(grp):
+                side[j].wait_stream(main)
+                with torch.cuda.stream(side[j]):
+                    self._gemv(qk, d, i, side[j].cuda_stream)
+            for j in range(len(grp)):
+                main.wait_stream(side[j])
         return len(d["decode"])
+
+    def _gemv(self, qk, d, i, stream):
+        lin, Wd, xd = d["decode"][i]
+        fn = qk.qk_matmul_q4k if lin.qtype == synth.Q4K else qk.qk_matmul_q6k
+        fn(Wd, xd, self.y_dec[i], 1, lin.N, lin.K, stream)
 
 
 def run_gpu(args, rank, world, dist):
@@ -213,32 +234,35 @@ def run_gpu(args, rank, world, dist):
     s = stream.cuda_stream
     pk = peaks()
 
-    # Per-part timing: events on the launching stream around each part.
-    def step(i, ev=None):
-        c = i % N_COPIES
-        n = 0
-        if ev is not None:
-            ev[0].record(stream)
-        n += wl.prefill(qk, c, s)
-        if ev is not None:
-            ev[1].record(stream)
-        n += wl.decode(qk, c, s)
-        if ev is not None:
-            ev[2].record(stream)
-        return n
-
+    # Warm-up, then capture each part of each rotating copy as a CUDA graph so
+    # the timed region measures the kernels, not host launch overhead.
     with torch.cuda.stream(stream):
         for i in range(args.warmup):
-            step(i)
+            wl.prefill(qk, i % N_COPIES, s)
+            wl.decode(qk, i % N_COPIES, s)
     qk.qk_get_device_status(s)
+    torch.cuda.synchronize()
+    side = [torch.cuda.Stream(device=dev) for _ in range(3)]
+    g_pre, g_dec = [], []
+    for c in range(N_COPIES):
+        for graphs, fn in ((g_pre, lambda: wl.prefill(qk, c, s)), (g_dec, lambda: wl.decode(qk, c, s, side))):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                fn()
+            graphs.append(g)
+    n_pre, n_dec = 3, len(decode_linears())
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            g_pre[i % N_COPIES].replay()
+            g_dec[i % N_COPIES].replay()
     torch.cuda.synchronize()
 
     # Dominant kernel alone (fused gate/up + SwiGLU), events around each launch.
     gu_ms = []
-    for i in range(max(3, args.steps)):
+    gate = prefill_linears()[0]
+    for i in range(max(5, args.steps)):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         d = wl.copies[i % N_COPIES]
-        gate = prefill_linears()[0]
         e0.record(stream)
         qk.qk_gateup_swiglu_q4k(d["gate"], d["up"], d["x_gu"], wl.y_gu, PREFILL_M, gate.N, gate.K, s)
         e1.record(stream)
@@ -252,10 +276,16 @@ def run_gpu(args, rank, world, dist):
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches = 0
     with Clocks(local) as clk:
-        t_start.record(stream)
-        for i in range(args.steps):
-            launches += step(i, evs[i])
-        t_end.record(stream)
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for i in range(args.steps):
+                evs[i][0].record(stream)
+                g_pre[i % N_COPIES].replay()
+                evs[i][1].record(stream)
+                g_dec[i % N_COPIES].replay()
+                evs[i][2].record(stream)
+                launches += n_pre + n_dec
+            t_end.record(stream)
         t_end.synchronize()
     torch.cuda.synchronize()
     if dist is not None:
@@ -289,7 +319,7 @@ def run_gpu(args, rank, world, dist):
             e[1].record(stream)
             for hx, (_, _, dx) in zip(h_xd, c0["decode"]):
                 dx.copy_(hx, non_blocking=True)
-            wl.decode(qk, 0, s)
+            wl.decode(qk, 0, s, side)
             for hy, dy in zip(h_yd, wl.y_dec):
                 hy.copy_(dy, non_blocking=True)
             e[2].record(stream)

@@ -49,7 +49,12 @@ constexpr uint32_t kH2Magic = 0x64646464u;
 
 template <int QT, bool GATEUP>
 struct Cfg {
-  static constexpr int kDqWarps = GATEUP ? 8 : 4;
+  // Dequant warps: two threads per weight row and tensor (each dequantizes
+  // half of every K step), i.e. two warps per SM sub-partition per tensor.
+  static constexpr int kDqWarps = GATEUP ? 16 : 8;
+  // Arrivals that complete an A stage: Q4_K threads each write half of every
+  // step; Q6_K threads write every other step in full.
+  static constexpr int kAArrivals = QT == kQ4K ? 32 * kDqWarps : 32 * kDqWarps / 2;
   static constexpr int kThreads = 64 + 32 * kDqWarps;
   static constexpr int kNumB = GATEUP ? 2 : 1;  // weight tensors per tile
   static constexpr int kStages = GATEUP ? 2 : 3;
@@ -123,42 +128,30 @@ __device__ __forceinline__ void q4_scale_min(uint32_t s03, uint32_t s47, uint32_
   mn = (float)b;
 }
 
-// Dequantize K step c (0..3) of a Q4_K super-block row held at `rowp` in
-// shared memory into 64 fp16 weights of row r of the swizzled A tile.
-__device__ __forceinline__ void q4_kstep(const uint8_t* rowp, int c, uint8_t* a_tile, int r) {
+// Dequantize half `part` of K step c (0..3) of a Q4_K super-block row held at
+// `rowp` in shared memory: part 0 = the low nibbles (sub-block 2c, step-local
+// k 0..31), part 1 = the high nibbles (sub-block 2c+1, k 32..63).  Writes 32
+// fp16 weights into row r of the swizzled A tile.
+__device__ __forceinline__ void q4_kstep(const uint8_t* rowp, int c, int part, uint8_t* a_tile, int r) {
   const uint4 hdr = *reinterpret_cast<const uint4*>(rowp);
   const float d = h2f(hdr.x), dmin = h2f(hdr.x >> 16);
-  float sc0, mn0, sc1, mn1;
-  q4_scale_min(hdr.y, hdr.z, hdr.w, 2 * c, sc0, mn0);
-  q4_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + 1, sc1, mn1);
-  const __half2 dsc_lo = __float2half2_rn(d * sc0), ndmn_lo = __float2half2_rn(-(dmin * mn0));
-  const __half2 dsc_hi = __float2half2_rn(d * sc1), ndmn_hi = __float2half2_rn(-(dmin * mn1));
+  float sc, mn;
+  q4_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + part, sc, mn);
+  const __half2 dsc = __float2half2_rn(d * sc), ndmn = __float2half2_rn(-(dmin * mn));
   const uint4 qa = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * c);
   const uint4 qb = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * c + 16);
   const uint32_t wv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+  const int shift = 4 * part;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {  // chunk j: k = 8j..8j+7 (low nibbles of words 2j, 2j+1)
-    uint4 o;
-    uint4 t;
-    q4_emit4(wv[2 * j] & 0x0F0F0F0Fu, dsc_lo, ndmn_lo, t);
+  for (int j = 0; j < 4; ++j) {  // chunk 4*part + j: k = 32*part + 8j .. +7 (words 2j, 2j+1)
+    uint4 o, t;
+    q4_emit4((wv[2 * j] >> shift) & 0x0F0F0F0Fu, dsc, ndmn, t);
     o.x = t.x;
     o.y = t.y;
-    q4_emit4(wv[2 * j + 1] & 0x0F0F0F0Fu, dsc_lo, ndmn_lo, t);
+    q4_emit4((wv[2 * j + 1] >> shift) & 0x0F0F0F0Fu, dsc, ndmn, t);
     o.z = t.x;
     o.w = t.y;
-    *reinterpret_cast<uint4*>(a_tile + sw128_off(r, j)) = o;
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {  // chunk 4+j: k = 32 + 8j .. (high nibbles)
-    uint4 o;
-    uint4 t;
-    q4_emit4((wv[2 * j] >> 4) & 0x0F0F0F0Fu, dsc_hi, ndmn_hi, t);
-    o.x = t.x;
-    o.y = t.y;
-    q4_emit4((wv[2 * j + 1] >> 4) & 0x0F0F0F0Fu, dsc_hi, ndmn_hi, t);
-    o.z = t.x;
-    o.w = t.y;
-    *reinterpret_cast<uint4*>(a_tile + sw128_off(r, 4 + j)) = o;
+    *reinterpret_cast<uint4*>(a_tile + sw128_off(r, 4 * part + j)) = o;
   }
 }
 
@@ -186,10 +179,11 @@ __device__ __forceinline__ void lds_vecs(const uint8_t* p, uint32_t (&v)[4 * NV]
   }
 }
 
-// Dequantize K steps 2h and 2h+1 of a Q6_K block (both use the same ql / qh
-// bytes 64h..64h+63 / 128+32h..+31) into two A tiles.
+// Dequantize K step 2h + side of a Q6_K block (ql bytes 64h..64h+63, qh bytes
+// 128+32h..+31: low nibbles for side 0, high nibbles for side 1) into row r
+// of an A tile.
 template <int MIS>
-__device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* a_tile0, uint8_t* a_tile1, int r) {
+__device__ __forceinline__ void q6_half(const uint8_t* slot, int h, int side, uint8_t* a_tile, int r) {
   uint32_t vl[20], vh[12], vs[8];
   lds_vecs<5>(slot + 64 * h, vl);         // bytes 64h .. 64h+79
   lds_vecs<3>(slot + 128 + 32 * h, vh);   // bytes 128+32h .. +47
@@ -204,9 +198,7 @@ __device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* a_t
   const uint32_t dw = vs[(16 + MIS) >> 2];
   const float d = h2f(((16 + MIS) & 3) ? (dw >> 16) : dw);
   const __half2 k1056 = __float2half2_rn(1056.0f);  // 1024 + 32
-#pragma unroll
-  for (int side = 0; side < 2; ++side) {  // K step 2h + side
-    uint8_t* a_tile = side ? a_tile1 : a_tile0;
+  {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // chunk j: step-local k = 8j .. 8j+7
       const int g = 2 * side + (j >> 2);     // 32-weight group within the half
@@ -233,17 +225,17 @@ __device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* a_t
   }
 }
 
-__device__ __forceinline__ void q6_half_dispatch(int mis, const uint8_t* slot, int h, uint8_t* t0, uint8_t* t1,
+__device__ __forceinline__ void q6_half_dispatch(int mis, const uint8_t* slot, int h, int side, uint8_t* t,
                                                  int r) {
   switch (mis) {
-    case 0: q6_half<0>(slot, h, t0, t1, r); break;
-    case 2: q6_half<2>(slot, h, t0, t1, r); break;
-    case 4: q6_half<4>(slot, h, t0, t1, r); break;
-    case 6: q6_half<6>(slot, h, t0, t1, r); break;
-    case 8: q6_half<8>(slot, h, t0, t1, r); break;
-    case 10: q6_half<10>(slot, h, t0, t1, r); break;
-    case 12: q6_half<12>(slot, h, t0, t1, r); break;
-    default: q6_half<14>(slot, h, t0, t1, r); break;
+    case 0: q6_half<0>(slot, h, side, t, r); break;
+    case 2: q6_half<2>(slot, h, side, t, r); break;
+    case 4: q6_half<4>(slot, h, side, t, r); break;
+    case 6: q6_half<6>(slot, h, side, t, r); break;
+    case 8: q6_half<8>(slot, h, side, t, r); break;
+    case 10: q6_half<10>(slot, h, side, t, r); break;
+    case 12: q6_half<12>(slot, h, side, t, r); break;
+    default: q6_half<14>(slot, h, side, t, r); break;
   }
 }
 
@@ -288,7 +280,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(&bars->x_full[s], 1);
-      mbar_init(&bars->a_full[s], 32 * C::kDqWarps);
+      mbar_init(&bars->a_full[s], C::kAArrivals);
       mbar_init(&bars->s_empty[s], 1);
     }
     for (int s = 0; s < C::kPStages; ++s) {
@@ -421,9 +413,11 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ dequant + epilogue
-    const int t = threadIdx.x - 64;          // 0 .. 32*kDqWarps-1
-    const int which = t >> 7;                // weight tensor (0 = gate/only, 1 = up)
-    const int rho = dq_row<QT>(t & 127);     // tile row this thread dequantizes
+    const int t = threadIdx.x - 64;               // 0 .. 32*kDqWarps-1
+    const int tpt = 32 * C::kDqWarps / C::kNumB;  // threads per weight tensor (256)
+    const int which = t / tpt;                    // weight tensor (0 = gate/only, 1 = up)
+    const int part = (t % tpt) >> 7;              // which half of the work on this row
+    const int rho = dq_row<QT>(t & 127);          // tile row this thread dequantizes
     const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
     int step = 0;
     bool ok = true;
@@ -441,27 +435,27 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
           if (!ok) break;
           uint8_t* a_tile = smem + C::kAOff + (s * C::kNumB + which) * kAStageBytes;
-          q4_kstep(rowp, c, a_tile, rho);
+          q4_kstep(rowp, c, part, a_tile, rho);
           fence_proxy_async_smem();
           mbar_arrive(&bars->a_full[s]);
         }
       } else {
+        // part p writes K steps 4kb + 2h + p (h = 0, 1).
         const int n = min(n0 + rho, p.N - 1);
         const int mis = (int)(((int64_t)n * RB + (int64_t)kb * kQ6KBytes) & 15);
         const uint8_t* slot = pst + q6_slot(rho);
-        for (int h = 0; h < 2 && ok; ++h, step += 2) {
-          const int s0 = step % C::kStages, s1 = (step + 1) % C::kStages;
-          const uint32_t ph0 = (uint32_t)(step / C::kStages) & 1u, ph1 = (uint32_t)((step + 1) / C::kStages) & 1u;
-          ok = mbar_wait(&bars->s_empty[s0], ph0 ^ 1u, abort_flag, &g_gemm_status) &&
-               mbar_wait(&bars->s_empty[s1], ph1 ^ 1u, abort_flag, &g_gemm_status);
+        for (int h = 0; h < 2 && ok; ++h) {
+          const int st = step + 2 * h + part;
+          const int s = st % C::kStages;
+          const uint32_t ph = (uint32_t)(st / C::kStages) & 1u;
+          ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
           if (!ok) break;
-          uint8_t* t0 = smem + C::kAOff + (s0 * C::kNumB + which) * kAStageBytes;
-          uint8_t* t1 = smem + C::kAOff + (s1 * C::kNumB + which) * kAStageBytes;
-          q6_half_dispatch(mis, slot, h, t0, t1, rho);
+          uint8_t* a_tile = smem + C::kAOff + (s * C::kNumB + which) * kAStageBytes;
+          q6_half_dispatch(mis, slot, h, part, a_tile, rho);
           fence_proxy_async_smem();
-          mbar_arrive(&bars->a_full[s0]);
-          mbar_arrive(&bars->a_full[s1]);
+          mbar_arrive(&bars->a_full[s]);
         }
+        step += 4;
       }
       if (ok) mbar_arrive(&bars->p_empty[ps]);
     }
@@ -475,9 +469,13 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       const int n = n0 + row;
       const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
       const int nchunks = BN / 16;
+      // Warps with the same lane quarter split the columns.
+      const int ngroups = C::kDqWarps / 4, grp = (warp - 2) >> 2;
+      const int per = (nchunks + ngroups - 1) / ngroups;
+      const int c_begin = min(nchunks, grp * per), c_end = min(nchunks, c_begin + per);
       if constexpr (!GATEUP) {
         float* y = static_cast<float*>(p.y);
-        for (int cc = 0; cc < nchunks; ++cc) {
+        for (int cc = c_begin; cc < c_end; ++cc) {
           uint32_t r[16];
           tmem_ld16(lane_addr + (uint32_t)(16 * cc), r);
           tmem_wait_ld();
@@ -491,9 +489,6 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
         }
       } else {
         __half* y = static_cast<__half*>(p.y);
-        const int half_chunks = (nchunks + 1) / 2;
-        const int c_begin = which ? half_chunks : 0;
-        const int c_end = which ? nchunks : half_chunks;
         for (int cc = c_begin; cc < c_end; ++cc) {
           uint32_t rg[16], ru[16];
           tmem_ld16(lane_addr + (uint32_t)(16 * cc), rg);

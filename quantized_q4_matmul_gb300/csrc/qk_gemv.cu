@@ -140,16 +140,28 @@ __device__ __forceinline__ Q4Scales q4k_lane_scales(uint4 hdr, int tig) {
   return r;
 }
 
-__device__ __forceinline__ void q4k_block(const uint8_t* blk0, const uint8_t* blk1, const uint2* xpb,
-                                          const float* sxb, int tig, float& y0, float& y1) {
-  const uint4 h0 = __ldg(reinterpret_cast<const uint4*>(blk0));
-  const uint4 h1 = __ldg(reinterpret_cast<const uint4*>(blk1));
-  uint2 q0[4], q1[4];
+// Registers holding one block of each of the lane's two rows.
+template <int QT>
+struct BlockRegs;
+
+template <>
+struct BlockRegs<kQ4K> {
+  uint4 h0, h1;      // d, dmin, packed scales of rows g, g+8
+  uint2 q0[4], q1[4];  // quant bytes 32G + 8tig .. +7, G = 0..3
+};
+
+__device__ __forceinline__ void load_block(BlockRegs<kQ4K>& r, const uint8_t* blk0, const uint8_t* blk1, int tig) {
+  r.h0 = __ldg(reinterpret_cast<const uint4*>(blk0));
+  r.h1 = __ldg(reinterpret_cast<const uint4*>(blk1));
 #pragma unroll
   for (int G = 0; G < 4; ++G) {
-    q0[G] = ldg_stream8(blk0 + 16 + 32 * G + 8 * tig);
-    q1[G] = ldg_stream8(blk1 + 16 + 32 * G + 8 * tig);
+    r.q0[G] = ldg_stream8(blk0 + 16 + 32 * G + 8 * tig);
+    r.q1[G] = ldg_stream8(blk1 + 16 + 32 * G + 8 * tig);
   }
+}
+
+__device__ __forceinline__ void compute_block(const BlockRegs<kQ4K>& r, const uint2* xpb, const float* sxb, int tig,
+                                              float& y0, float& y1) {
   float dlo0[4], dlo1[4], dhi0[4], dhi1[4];
 #pragma unroll
   for (int G = 0; G < 4; ++G) {
@@ -158,8 +170,8 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk0, const uint8_t* bl
     const uint4 xhi = *reinterpret_cast<const uint4*>(xpb + 16 * G + 8 + 2 * tig);  // k + 32
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const uint32_t w0 = hh ? q0[G].y : q0[G].x;
-      const uint32_t w1 = hh ? q1[G].y : q1[G].x;
+      const uint32_t w0 = hh ? r.q0[G].y : r.q0[G].x;
+      const uint32_t w1 = hh ? r.q1[G].y : r.q1[G].x;
       const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
       const uint32_t bl0 = hh ? xlo.z : xlo.x, bl1 = hh ? xlo.w : xlo.y;
       const uint32_t bh0 = hh ? xhi.z : xhi.x, bh1 = hh ? xhi.w : xhi.y;
@@ -174,8 +186,8 @@ __device__ __forceinline__ void q4k_block(const uint8_t* blk0, const uint8_t* bl
     dhi1[G] = e[2];
   }
   // This lane applies the scales of group G = tig (sub-blocks 2tig, 2tig+1).
-  const Q4Scales r0 = q4k_lane_scales(h0, tig);
-  const Q4Scales r1 = q4k_lane_scales(h1, tig);
+  const Q4Scales r0 = q4k_lane_scales(r.h0, tig);
+  const Q4Scales r1 = q4k_lane_scales(r.h1, tig);
   const float2 sx = make_float2(sxb[4 * tig] + sxb[4 * tig + 1], sxb[4 * tig + 2] + sxb[4 * tig + 3]);
   y0 = fmaf(r0.a_lo, pick4(dlo0, tig), y0);
   y0 = fmaf(-r0.c_lo, sx.x, y0);
@@ -208,29 +220,48 @@ __device__ __forceinline__ void q6k_operands(uint32_t wl, uint32_t wh, int g6, u
   }
 }
 
-__device__ __forceinline__ void q6k_block(const uint8_t* blk0, const uint8_t* blk1, const uint2* xpb,
-                                          const float* sxb, int tig, float& y0, float& y1) {
-  uint32_t ql0[8], ql1[8], qh0[4], qh1[4];
+template <>
+struct BlockRegs<kQ6K> {
+  uint32_t ql0[8], ql1[8], qh0[4], qh1[4];  // the lane's quant words of rows g, g+8
+  uint32_t sc0, sc1;                        // int8 scales t = 4u + tig, u = 0..3 (byte u)
+  uint32_t d;                               // fp16 d of row g (low half) and row g+8 (high half)
+};
+
+__device__ __forceinline__ void load_block(BlockRegs<kQ6K>& r, const uint8_t* blk0, const uint8_t* blk1, int tig) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {  // i = 4h + 2p + s: byte 64h + 32p + 16s + 4tig
     const int off = 64 * (i >> 2) + 32 * ((i >> 1) & 1) + 16 * (i & 1) + 4 * tig;
-    ql0[i] = ld_u32_a2(blk0 + off);
-    ql1[i] = ld_u32_a2(blk1 + off);
+    r.ql0[i] = ld_u32_a2(blk0 + off);
+    r.ql1[i] = ld_u32_a2(blk1 + off);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {  // i = 2h + s: byte 128 + 32h + 16s + 4tig
     const int off = 128 + 32 * (i >> 1) + 16 * (i & 1) + 4 * tig;
-    qh0[i] = ld_u32_a2(blk0 + off);
-    qh1[i] = ld_u32_a2(blk1 + off);
+    r.qh0[i] = ld_u32_a2(blk0 + off);
+    r.qh1[i] = ld_u32_a2(blk1 + off);
   }
+  uint32_t s0 = 0, s1 = 0;
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    s0 |= (uint32_t)__ldg(blk0 + 192 + 4 * u + tig) << (8 * u);
+    s1 |= (uint32_t)__ldg(blk1 + 192 + 4 * u + tig) << (8 * u);
+  }
+  r.sc0 = s0;
+  r.sc1 = s1;
+  r.d = (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(blk0 + 208)) |
+        ((uint32_t)__ldg(reinterpret_cast<const uint16_t*>(blk1 + 208)) << 16);
+}
+
+__device__ __forceinline__ void compute_block(const BlockRegs<kQ6K>& r, const uint2* xpb, const float* sxb, int tig,
+                                              float& y0, float& y1) {
   float d0[16], d1[16];
 #pragma unroll
   for (int t = 0; t < 16; ++t) {
     const int h = t >> 3, g6 = (t >> 1) & 3, s = t & 1;
     const int li = 4 * h + 2 * (g6 & 1) + s, hi = 2 * h + s;
     uint32_t a0, a2, a1, a3;
-    q6k_operands(ql0[li], qh0[hi], g6, a0, a2);
-    q6k_operands(ql1[li], qh1[hi], g6, a1, a3);
+    q6k_operands(r.ql0[li], r.qh0[hi], g6, a0, a2);
+    q6k_operands(r.ql1[li], r.qh1[hi], g6, a1, a3);
     const uint2 b = xpb[4 * t + tig];
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     mma16816(c, a0, a1, a2, a3, b.x, b.y);
@@ -238,19 +269,18 @@ __device__ __forceinline__ void q6k_block(const uint8_t* blk0, const uint8_t* bl
     d1[t] = c[2];
   }
   // Scales: lane tig applies scale groups t = 4u + tig.
-  const float dA = half_lo(*reinterpret_cast<const uint16_t*>(blk0 + 208));
-  const float dB = half_lo(*reinterpret_cast<const uint16_t*>(blk1 + 208));
+  const float dA = half_lo(r.d), dB = half_lo(r.d >> 16);
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
     const int t = 4 * u + tig;
-    const float F = (((t >> 1) & 3) >= 2) ? 0.0625f : 1.0f;  // 1/F
-    const int8_t sc0 = (int8_t)(blk0[192 + t]);
-    const int8_t sc1 = (int8_t)(blk1[192 + t]);
-    const float dsc0 = dA * (float)sc0, dsc1 = dB * (float)sc1;
+    // 1/F: scale group t = 4u + tig has g6 = (2u + tig/2) & 3, which is >= 2 exactly for odd u.
+    const float inv_f = (u & 1) ? 0.0625f : 1.0f;
+    const float dsc0 = dA * (float)(int8_t)((r.sc0 >> (8 * u)) & 0xFFu);
+    const float dsc1 = dB * (float)(int8_t)((r.sc1 >> (8 * u)) & 0xFFu);
     float v0[4] = {d0[4 * u], d0[4 * u + 1], d0[4 * u + 2], d0[4 * u + 3]};
     float v1[4] = {d1[4 * u], d1[4 * u + 1], d1[4 * u + 2], d1[4 * u + 3]};
     const float sxt = sxb[t];
-    const float a0 = dsc0 * F, a1 = dsc1 * F;
+    const float a0 = dsc0 * inv_f, a1 = dsc1 * inv_f;
     y0 = fmaf(a0, pick4(v0, tig), y0);
     y0 = fmaf(-fmaf(1024.0f, a0, 32.0f * dsc0), sxt, y0);
     y1 = fmaf(a1, pick4(v1, tig), y1);
@@ -263,8 +293,10 @@ __device__ __forceinline__ void q6k_block(const uint8_t* blk0, const uint8_t* bl
 // Shared memory: xp (2K bytes), sx16 (K/4 bytes), partial sums (ks*16 floats).
 // ---------------------------------------------------------------------------
 // The kernel: each CTA iteration covers `tpc` 16-row tiles; the `ks` warps of
-// a tile split its K/256 blocks.  Shared memory: xp (2K bytes), sx16 (K/4
-// bytes), partial sums (tpc*ks*16 floats).
+// a tile split its K/256 blocks.  Each warp issues the loads of its first
+// block before the CTA stages x, and loads the next block (or the next tile's
+// first block) while it computes the current one.  Shared memory: xp (2K
+// bytes), sx16 (K/4 bytes), partial sums (tpc*ks*16 floats).
 template <int QT>
 __global__ void __launch_bounds__(512) gemv_m1_kernel(const uint8_t* __restrict__ W,
                                                       const uint16_t* __restrict__ x, float* __restrict__ y, int N,
@@ -273,8 +305,6 @@ __global__ void __launch_bounds__(512) gemv_m1_kernel(const uint8_t* __restrict_
   uint2* xp = reinterpret_cast<uint2*>(smem);
   float* sx16 = reinterpret_cast<float*>(smem + 2 * K);
   float* red = sx16 + K / 16;
-  stage_x(x, K, xp, sx16);
-  __syncthreads();
 
   const int nb = K / kQK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -282,21 +312,38 @@ __global__ void __launch_bounds__(512) gemv_m1_kernel(const uint8_t* __restrict_
   const int sub = warp / ks, kslice = warp % ks;
   const int bpw = nb / ks;
   const int b_begin = kslice * bpw;
-  const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
+  constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
+  const int64_t RB = (int64_t)nb * kBB;
   const int ntiles = (N + 15) / 16;
-  for (int tile0 = blockIdx.x * tpc; tile0 < ntiles; tile0 += gridDim.x * tpc) {
-    const int tile = tile0 + sub;
+  const int stride = gridDim.x * tpc;
+
+  auto row_ptr = [&](int tile, int which) {
+    const int r = min(tile * 16 + g + 8 * which, N - 1);
+    return W + r * RB;
+  };
+
+  BlockRegs<QT> cur;
+  int tile = blockIdx.x * tpc + sub;
+  if (tile < ntiles) load_block(cur, row_ptr(tile, 0) + b_begin * kBB, row_ptr(tile, 1) + b_begin * kBB, tig);
+  stage_x(x, K, xp, sx16);
+  __syncthreads();
+
+  for (int tile0 = blockIdx.x * tpc; tile0 < ntiles; tile0 += stride) {
+    tile = tile0 + sub;
     float y0 = 0.f, y1 = 0.f;
     if (tile < ntiles) {
-      const int r0 = min(tile * 16 + g, N - 1);
-      const int r1 = min(tile * 16 + g + 8, N - 1);
-      const uint8_t* row0 = W + r0 * RB;
-      const uint8_t* row1 = W + r1 * RB;
+      const uint8_t* row0 = row_ptr(tile, 0);
+      const uint8_t* row1 = row_ptr(tile, 1);
       for (int b = b_begin; b < b_begin + bpw; ++b) {
-        if constexpr (QT == kQ4K)
-          q4k_block(row0 + b * kQ4KBytes, row1 + b * kQ4KBytes, xp + 64 * b, sx16 + 16 * b, tig, y0, y1);
-        else
-          q6k_block(row0 + b * kQ6KBytes, row1 + b * kQ6KBytes, xp + 64 * b, sx16 + 16 * b, tig, y0, y1);
+        BlockRegs<QT> nxt;
+        if (b + 1 < b_begin + bpw) {
+          load_block(nxt, row0 + (b + 1) * kBB, row1 + (b + 1) * kBB, tig);
+        } else if (tile + stride < ntiles) {
+          load_block(nxt, row_ptr(tile + stride, 0) + b_begin * kBB, row_ptr(tile + stride, 1) + b_begin * kBB,
+                     tig);
+        }
+        compute_block(cur, xp + 64 * b, sx16 + 16 * b, tig, y0, y1);
+        cur = nxt;
       }
     }
     y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
@@ -342,14 +389,17 @@ uint32_t gemv_take_status() {
   return v;
 }
 
-// Warps per 16-row tile (ks) divide the K/256 blocks; pick the split that
-// gives about 16 warps per SM over the whole grid.
+// Warps per 16-row tile (ks) divide the K/256 blocks: the smallest split that
+// puts about 32 warps per SM in flight, else the largest available (<= 16).
 static int choose_ks(int64_t N, int nb) {
   const int64_t tiles = (N + 15) / 16;
-  const int64_t want = ((int64_t)sm_count() * 16 + tiles - 1) / tiles;
+  const int64_t target = (int64_t)sm_count() * 32;
   int best = 1;
-  for (int d = 1; d <= 16 && d <= nb; ++d)
-    if (nb % d == 0 && d <= std::max<int64_t>(want, 1)) best = d;
+  for (int d = 1; d <= 16 && d <= nb; ++d) {
+    if (nb % d) continue;
+    best = d;
+    if (tiles * d >= target) break;
+  }
   return best;
 }
 
