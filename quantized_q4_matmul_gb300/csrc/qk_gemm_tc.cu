@@ -42,9 +42,7 @@ namespace {
 constexpr int kBM = 128;               // weight rows per tile (UMMA M)
 constexpr int kBK = 64;                // K per step: one 128-byte swizzle row of fp16
 constexpr int kMaxBN = 256;            // tokens per tile (UMMA N), multiple of 16
-constexpr int kXStageBytes = kMaxBN * kBK * 2;  // 32 KB
 constexpr int kAStageBytes = kBM * kBK * 2;     // 16 KB
-constexpr int kQ6Pitch = 240;          // smem bytes per Q6_K row slot (224 used)
 constexpr uint32_t kH2Magic = 0x64646464u;
 
 template <int QT, bool GATEUP>
@@ -52,38 +50,55 @@ struct Cfg {
   // Dequant warps: two threads per weight row and tensor (each dequantizes
   // half of every K step), i.e. two warps per SM sub-partition per tensor.
   static constexpr int kDqWarps = GATEUP ? 16 : 8;
-  // Arrivals that complete an A stage: Q4_K threads each write half of every
-  // step; Q6_K threads write every other step in full.
-  static constexpr int kAArrivals = QT == kQ4K ? 32 * kDqWarps : 32 * kDqWarps / 2;
   static constexpr int kThreads = 64 + 32 * kDqWarps;
   static constexpr int kNumB = GATEUP ? 2 : 1;  // weight tensors per tile
-  static constexpr int kStages = GATEUP ? 2 : 3;
+  // Arrivals that complete an A stage: Q4_K threads each write half of every
+  // step; Q6_K threads write two of every four steps in full.
+  static constexpr int kAArrivals = QT == kQ4K ? 32 * kDqWarps : 32 * kDqWarps / 2;
   static constexpr int kPStages = 2;
-  static constexpr int kPStageBytes =
-      QT == kQ4K ? kBM * kQ4KBytes : (kBM * kQ6Pitch + 16 + 1023) / 1024 * 1024;
-  static constexpr int kXOff = 0;
-  static constexpr int kAOff = kXOff + kStages * kXStageBytes;
-  static constexpr int kPOff = kAOff + kStages * kNumB * kAStageBytes;
-  static constexpr int kBarOff = kPOff + kPStages * kNumB * ((kPStageBytes + 1023) / 1024 * 1024);
-  static constexpr int kSmemBytes = kBarOff + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : 8 * 4096;  // one tensor, one stage
+  static constexpr int kPBytes = kPStages * kNumB * kPSlotBytes;
+  static constexpr int kMaxStages = 8;
 };
 
+// Shared-memory carve-up for a token tile BN and S K-step stages (all offsets
+// 1024-byte aligned for the 128-byte swizzle atoms).
+struct Layout {
+  uint32_t x_off, x_stage, a_off, p_off, bar_off, total;
+};
+
+template <int QT, bool GATEUP>
+__host__ __device__ inline Layout make_layout(int BN, int S) {
+  using C = Cfg<QT, GATEUP>;
+  Layout L;
+  L.x_stage = (uint32_t)BN * kBK * 2;
+  L.x_off = 0;
+  L.a_off = L.x_off + (uint32_t)S * L.x_stage;
+  L.p_off = L.a_off + (uint32_t)(S * C::kNumB) * kAStageBytes;
+  L.bar_off = L.p_off + (uint32_t)C::kPBytes;
+  L.total = L.bar_off + 256 + 1024;  // barriers + base alignment slack
+  return L;
+}
+
 struct Bars {
-  uint64_t x_full[4];
-  uint64_t a_full[4];
-  uint64_t s_empty[4];
-  uint64_t p_full[4];
-  uint64_t p_empty[4];
+  uint64_t x_full[8];
+  uint64_t a_full[8];
+  uint64_t s_empty[8];
+  uint64_t p_full[2];
+  uint64_t p_empty[2];
   uint64_t acc_full;
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
 
 struct Params {
-  const uint8_t* w[2];  // packed weights (gate, up) -- Q6_K path reads through plain bulk copies
+  const uint8_t* w[2];  // packed weights (gate, up)
   int64_t w_bytes;      // bytes of each weight tensor
   void* y;
   int M, N, K, BN;
+  int stages;           // K-step pipeline depth S
+  int q6_group;         // Q6_K: rows per tensor-map row (g: g * row_bytes % 16 == 0)
+  int q6_rows_tma;      // Q6_K: rows covered by the tensor map, (N / g) * g
 };
 
 __device__ __forceinline__ float h2f(uint32_t bits) {
@@ -179,11 +194,11 @@ __device__ __forceinline__ void lds_vecs(const uint8_t* p, uint32_t (&v)[4 * NV]
   }
 }
 
-// Dequantize K step 2h + side of a Q6_K block (ql bytes 64h..64h+63, qh bytes
-// 128+32h..+31: low nibbles for side 0, high nibbles for side 1) into row r
-// of an A tile.
+// Dequantize K steps 2h (side 0: low nibbles) and 2h+1 (side 1: high nibbles)
+// of a Q6_K block (both read ql bytes 64h..64h+63 and qh bytes 128+32h..+31)
+// into row r of two A tiles.
 template <int MIS>
-__device__ __forceinline__ void q6_half(const uint8_t* slot, int h, int side, uint8_t* a_tile, int r) {
+__device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* a_tile0, uint8_t* a_tile1, int r) {
   uint32_t vl[20], vh[12], vs[8];
   lds_vecs<5>(slot + 64 * h, vl);         // bytes 64h .. 64h+79
   lds_vecs<3>(slot + 128 + 32 * h, vh);   // bytes 128+32h .. +47
@@ -198,7 +213,9 @@ __device__ __forceinline__ void q6_half(const uint8_t* slot, int h, int side, ui
   const uint32_t dw = vs[(16 + MIS) >> 2];
   const float d = h2f(((16 + MIS) & 3) ? (dw >> 16) : dw);
   const __half2 k1056 = __float2half2_rn(1056.0f);  // 1024 + 32
-  {
+#pragma unroll
+  for (int side = 0; side < 2; ++side) {
+    uint8_t* a_tile = side ? a_tile1 : a_tile0;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {  // chunk j: step-local k = 8j .. 8j+7
       const int g = 2 * side + (j >> 2);     // 32-weight group within the half
@@ -225,36 +242,44 @@ __device__ __forceinline__ void q6_half(const uint8_t* slot, int h, int side, ui
   }
 }
 
-__device__ __forceinline__ void q6_half_dispatch(int mis, const uint8_t* slot, int h, int side, uint8_t* t,
+__device__ __forceinline__ void q6_half_dispatch(int mis, const uint8_t* slot, int h, uint8_t* t0, uint8_t* t1,
                                                  int r) {
   switch (mis) {
-    case 0: q6_half<0>(slot, h, side, t, r); break;
-    case 2: q6_half<2>(slot, h, side, t, r); break;
-    case 4: q6_half<4>(slot, h, side, t, r); break;
-    case 6: q6_half<6>(slot, h, side, t, r); break;
-    case 8: q6_half<8>(slot, h, side, t, r); break;
-    case 10: q6_half<10>(slot, h, side, t, r); break;
-    case 12: q6_half<12>(slot, h, side, t, r); break;
-    default: q6_half<14>(slot, h, side, t, r); break;
+    case 0: q6_half<0>(slot, h, t0, t1, r); break;
+    case 2: q6_half<2>(slot, h, t0, t1, r); break;
+    case 4: q6_half<4>(slot, h, t0, t1, r); break;
+    case 6: q6_half<6>(slot, h, t0, t1, r); break;
+    case 8: q6_half<8>(slot, h, t0, t1, r); break;
+    case 10: q6_half<10>(slot, h, t0, t1, r); break;
+    case 12: q6_half<12>(slot, h, t0, t1, r); break;
+    default: q6_half<14>(slot, h, t0, t1, r); break;
   }
 }
 
-// Slot of tile row rho in a Q6_K packed stage: pitch 240 bytes plus a 16-byte
-// skew on every second group of 8 rows, so the 16-byte reads of 8 consecutive
-// threads (rows rho = 2i + p, see dq_row) hit 8 different bank groups:
-// (15*rho + skew) mod 8 = (6i + 7p + skew) mod 8 is distinct for i = 0..7.
-__device__ __forceinline__ uint32_t q6_slot(int rho) { return (uint32_t)(rho * kQ6Pitch + 16 * ((rho >> 3) & 1)); }
+// Q6_K packed stage layout.  The tensor map views the weights as rows of g
+// consecutive weight rows (g * row_bytes is a multiple of 16); box j of a
+// stage holds weight rows n0 + g*i + j (i = 0 .. 128/g - 1) at a 224-byte pitch
+// in region j, so every row of region j has the same misalignment
+// (j * row_bytes + 210 * kb) mod 16 of its block inside its 224-byte window.
+constexpr int kQ6Win = 224;
+__device__ __forceinline__ uint32_t q6_region_stride(int g) {
+  return (uint32_t)(((128 / g) * kQ6Win + 127) / 128 * 128);
+}
+__device__ __forceinline__ uint32_t q6_slot(int rho, int g) {
+  return (uint32_t)(rho % g) * q6_region_stride(g) + (uint32_t)(rho / g) * kQ6Win;
+}
 
-// Row handled by dequant thread t (0..127) of one weight tensor.  Q6_K groups
-// rows of equal parity in a warp so that, for the common K, the misalignment
-// of their blocks is warp-uniform.
+// Row handled by dequant thread t (0..127) of one weight tensor.  Q6_K puts
+// rows of the same residue mod g (same misalignment) in a warp, so the
+// realignment code path is warp-uniform (for g = 8 a warp holds two residues).
 template <int QT>
-__device__ __forceinline__ int dq_row(int t) {
+__device__ __forceinline__ int dq_row(int t, int g) {
   if constexpr (QT == kQ4K) {
     return t;
   } else {
     const int w = t >> 5, i = t & 31;
-    return 2 * i + (w & 1) + 64 * (w >> 1);
+    if (g <= 4) return g * ((w / g) * 32 + i) + (w % g);
+    return 8 * (i & 15) + 2 * w + (i >> 4);
   }
 }
 
@@ -265,7 +290,9 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   using C = Cfg<QT, GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  Bars* bars = reinterpret_cast<Bars*>(smem + C::kBarOff);
+  const int S = p.stages;
+  const Layout L = make_layout<QT, GATEUP>(p.BN, S);
+  Bars* bars = reinterpret_cast<Bars*>(smem + L.bar_off);
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -275,10 +302,10 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   const int nsteps = nb * 4;
   const int BN = p.BN;
   const uint32_t x_bytes = (uint32_t)BN * kBK * 2;
-  constexpr int kPSlotBytes = (C::kPStageBytes + 1023) / 1024 * 1024;
+  constexpr int kPSlotBytes = C::kPSlotBytes;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::kStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&bars->x_full[s], 1);
       mbar_init(&bars->a_full[s], C::kAArrivals);
       mbar_init(&bars->s_empty[s], 1);
@@ -306,10 +333,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
       prefetch_tmap(&tm_x);
-      if (QT == kQ4K) {
-        prefetch_tmap(&tm_w0);
-        if (GATEUP) prefetch_tmap(&tm_w1);
-      }
+      if (QT == kQ4K || p.q6_rows_tma > 0) prefetch_tmap(&tm_w0);
+      if (GATEUP) prefetch_tmap(&tm_w1);
     }
     int step = 0;
     bool ok = true;
@@ -318,7 +343,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       const uint32_t pph = (uint32_t)(kb / C::kPStages) & 1u;
       ok = mbar_wait(&bars->p_empty[ps], pph ^ 1u, abort_flag, &g_gemm_status);
       if (!ok) break;
-      uint8_t* pst = smem + C::kPOff + ps * C::kNumB * kPSlotBytes;
+      uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
       if constexpr (QT == kQ4K) {
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(C::kNumB * kBM * kQ4KBytes));
@@ -326,51 +351,65 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           if (GATEUP) tma_load_2d(pst + kPSlotBytes, &tm_w1, kb * kQ4KBytes, n0, &bars->p_full[ps]);
         }
       } else {
-        // One bulk copy per row of the 16-byte-aligned 224-byte window around
-        // its 210-byte block.  Rows past N are skipped; a window that would run
-        // past the end of the tensor is shortened and its last bytes copied by
-        // plain loads.  Each lane announces its bytes before issuing its copies
-        // and arrives after its plain stores.
+        // Whole tiles inside the tensor map: g TMA boxes (one per residue j).
+        // The last tile, if it holds rows past (N / g) * g, takes one bulk copy
+        // per row of the 16-byte-aligned 224-byte window around its block
+        // instead (a window that would run past the end of the tensor is
+        // shortened and its last bytes copied by plain loads).
+        const int g = p.q6_group;
         const int64_t RB = (int64_t)nb * kQ6KBytes;
-        uint32_t bytes = 0;
-        for (int i = lane; i < kBM; i += 32) {
-          const int n = n0 + i;
-          if (n >= p.N) continue;
-          const int64_t g = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
-          const int64_t lo = g & ~int64_t(15);
-          bytes += (uint32_t)(lo + 224 <= p.w_bytes ? 224 : ((p.w_bytes - lo) & ~int64_t(15)));
+        if (n0 + kBM <= p.q6_rows_tma) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(kBM * kQ6Win));
+            for (int j = 0; j < g; ++j) {
+              const int64_t off = (int64_t)j * RB + (int64_t)kb * kQ6KBytes;
+              tma_load_2d(pst + (uint32_t)j * q6_region_stride(g), &tm_w0, (int32_t)((off & ~int64_t(15)) >> 1),
+                          n0 / g, &bars->p_full[ps]);
+            }
+          } else {
+            mbar_arrive(&bars->p_full[ps]);
+          }
+        } else {
+          uint32_t bytes = 0;
+          for (int i = lane; i < kBM; i += 32) {
+            const int n = n0 + i;
+            if (n >= p.N) continue;
+            const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
+            const int64_t lo = gg & ~int64_t(15);
+            bytes += (uint32_t)(lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15)));
+          }
+          mbar_expect_tx(&bars->p_full[ps], bytes);
+          for (int i = lane; i < kBM; i += 32) {
+            const int n = n0 + i;
+            if (n >= p.N) continue;
+            const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
+            const int64_t lo = gg & ~int64_t(15);
+            const int64_t len = lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15));
+            uint8_t* dst = pst + q6_slot(i, g);
+            bulk_copy_g2s(dst, p.w[0] + lo, (uint32_t)len, &bars->p_full[ps]);
+            for (int64_t b = lo + len; b < gg + kQ6KBytes; b += 2)  // tail bytes (only at the tensor's end)
+              *reinterpret_cast<uint16_t*>(dst + (b - lo)) = *reinterpret_cast<const uint16_t*>(p.w[0] + b);
+          }
+          mbar_arrive(&bars->p_full[ps]);
         }
-        mbar_expect_tx(&bars->p_full[ps], bytes);
-        for (int i = lane; i < kBM; i += 32) {
-          const int n = n0 + i;
-          if (n >= p.N) continue;
-          const int64_t g = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
-          const int64_t lo = g & ~int64_t(15);
-          const int64_t len = lo + 224 <= p.w_bytes ? 224 : ((p.w_bytes - lo) & ~int64_t(15));
-          uint8_t* dst = pst + q6_slot(i);
-          bulk_copy_g2s(dst, p.w[0] + lo, (uint32_t)len, &bars->p_full[ps]);
-          for (int64_t b = lo + len; b < g + kQ6KBytes; b += 2)  // tail bytes (only at the tensor's end)
-            *reinterpret_cast<uint16_t*>(dst + (b - lo)) = *reinterpret_cast<const uint16_t*>(p.w[0] + b);
-        }
-        mbar_arrive(&bars->p_full[ps]);
       }
       for (int c = 0; c < 4 && ok; ++c, ++step) {
-        const int s = step % C::kStages;
-        const uint32_t ph = (uint32_t)(step / C::kStages) & 1u;
+        const int s = step % S;
+        const uint32_t ph = (uint32_t)(step / S) & 1u;
         ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
         if (!ok) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars->x_full[s], x_bytes);
-          tma_load_2d(smem + C::kXOff + s * kXStageBytes, &tm_x, kb * kQK + c * kBK, m0, &bars->x_full[s]);
+          tma_load_2d(smem + L.x_off + s * L.x_stage, &tm_x, kb * kQK + c * kBK, m0, &bars->x_full[s]);
         }
         __syncwarp();
       }
     }
     // Drain: every x copy this warp issued has completed before the CTA exits
     // (the packed-block copies are drained by the dequant warps' waits).
-    for (int i = 0; i < C::kStages && i < step; ++i) {
+    for (int i = 0; i < S && i < step; ++i) {
       const int st = step - 1 - i;
-      mbar_wait(&bars->x_full[st % C::kStages], (uint32_t)(st / C::kStages) & 1u, abort_flag, &g_gemm_status,
+      mbar_wait(&bars->x_full[st % S], (uint32_t)(st / S) & 1u, abort_flag, &g_gemm_status,
                 true);
     }
   } else if (warp == 1) {
@@ -379,18 +418,18 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     bool ok = true;
     int step = 0;
     for (; step < nsteps && ok; ++step) {
-      const int s = step % C::kStages;
-      const uint32_t ph = (uint32_t)(step / C::kStages) & 1u;
+      const int s = step % S;
+      const uint32_t ph = (uint32_t)(step / S) & 1u;
       ok = mbar_wait(&bars->x_full[s], ph, abort_flag, &g_gemm_status) &&
            mbar_wait(&bars->a_full[s], ph, abort_flag, &g_gemm_status);
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t xa = smem_u32(smem + C::kXOff + s * kXStageBytes);
+        const uint32_t xa = smem_u32(smem + L.x_off + s * L.x_stage);
         const uint64_t bdesc = umma_desc_sw128(xa);
 #pragma unroll
         for (int t = 0; t < C::kNumB; ++t) {
-          const uint32_t aa = smem_u32(smem + C::kAOff + (s * C::kNumB + t) * kAStageBytes);
+          const uint32_t aa = smem_u32(smem + L.a_off + (s * C::kNumB + t) * kAStageBytes);
           const uint64_t adesc = umma_desc_sw128(aa);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk) {
@@ -408,7 +447,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     // writing tensor memory before tensor memory is freed.
     if (step > 0) {
       const int st = step - 1;
-      mbar_wait(&bars->s_empty[st % C::kStages], (uint32_t)(st / C::kStages) & 1u, abort_flag, &g_gemm_status,
+      mbar_wait(&bars->s_empty[st % S], (uint32_t)(st / S) & 1u, abort_flag, &g_gemm_status,
                 true);
     }
   } else {
@@ -417,7 +456,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     const int tpt = 32 * C::kDqWarps / C::kNumB;  // threads per weight tensor (256)
     const int which = t / tpt;                    // weight tensor (0 = gate/only, 1 = up)
     const int part = (t % tpt) >> 7;              // which half of the work on this row
-    const int rho = dq_row<QT>(t & 127);          // tile row this thread dequantizes
+    const int rho = dq_row<QT>(t & 127, p.q6_group);  // tile row this thread dequantizes
     const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
     int step = 0;
     bool ok = true;
@@ -426,34 +465,36 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       const uint32_t pph = (uint32_t)(kb / C::kPStages) & 1u;
       ok = mbar_wait(&bars->p_full[ps], pph, abort_flag, &g_gemm_status);
       if (!ok) break;
-      const uint8_t* pst = smem + C::kPOff + (ps * C::kNumB + which) * kPSlotBytes;
+      const uint8_t* pst = smem + L.p_off + (ps * C::kNumB + which) * kPSlotBytes;
       if constexpr (QT == kQ4K) {
         const uint8_t* rowp = pst + rho * kQ4KBytes;
         for (int c = 0; c < 4; ++c, ++step) {
-          const int s = step % C::kStages;
-          const uint32_t ph = (uint32_t)(step / C::kStages) & 1u;
+          const int s = step % S;
+          const uint32_t ph = (uint32_t)(step / S) & 1u;
           ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
           if (!ok) break;
-          uint8_t* a_tile = smem + C::kAOff + (s * C::kNumB + which) * kAStageBytes;
+          uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
           q4_kstep(rowp, c, part, a_tile, rho);
           fence_proxy_async_smem();
           mbar_arrive(&bars->a_full[s]);
         }
       } else {
-        // part p writes K steps 4kb + 2h + p (h = 0, 1).
+        // part h writes K steps 4kb + 2h and 4kb + 2h + 1.
         const int n = min(n0 + rho, p.N - 1);
         const int mis = (int)(((int64_t)n * RB + (int64_t)kb * kQ6KBytes) & 15);
-        const uint8_t* slot = pst + q6_slot(rho);
-        for (int h = 0; h < 2 && ok; ++h) {
-          const int st = step + 2 * h + part;
-          const int s = st % C::kStages;
-          const uint32_t ph = (uint32_t)(st / C::kStages) & 1u;
-          ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
-          if (!ok) break;
-          uint8_t* a_tile = smem + C::kAOff + (s * C::kNumB + which) * kAStageBytes;
-          q6_half_dispatch(mis, slot, h, part, a_tile, rho);
+        const uint8_t* slot = pst + q6_slot(rho, p.q6_group);
+        const int h = part;
+        const int st0 = step + 2 * h, st1 = st0 + 1;
+        const int s0 = st0 % S, s1 = st1 % S;
+        ok = mbar_wait(&bars->s_empty[s0], ((uint32_t)(st0 / S) & 1u) ^ 1u, abort_flag, &g_gemm_status) &&
+             mbar_wait(&bars->s_empty[s1], ((uint32_t)(st1 / S) & 1u) ^ 1u, abort_flag, &g_gemm_status);
+        if (ok) {
+          uint8_t* t0 = smem + L.a_off + (s0 * C::kNumB + which) * kAStageBytes;
+          uint8_t* t1 = smem + L.a_off + (s1 * C::kNumB + which) * kAStageBytes;
+          q6_half_dispatch(mis, slot, h, t0, t1, rho);
           fence_proxy_async_smem();
-          mbar_arrive(&bars->a_full[s]);
+          mbar_arrive(&bars->a_full[s0]);
+          mbar_arrive(&bars->a_full[s1]);
         }
         step += 4;
       }
@@ -563,6 +604,29 @@ bool make_tmap_q4k(CUtensorMap* tm, const void* w, int64_t N, int64_t K) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Q6_K weights as uint16 rows of g consecutive weight rows (g * row_bytes is a
+// multiple of 16, as tensor maps require); one box = the 224-byte window of one
+// residue j's blocks for 128/g such rows.
+int q6_group(int64_t K) {
+  const int64_t rb = (K / kQK) * kQ6KBytes;
+  for (int g = 1; g < 8; g *= 2)
+    if ((g * rb) % 16 == 0) return g;
+  return 8;
+}
+
+bool make_tmap_q6k(CUtensorMap* tm, const void* w, int64_t N, int64_t K, int g) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  const int64_t rb = (K / kQK) * kQ6KBytes;
+  const cuuint64_t dims[2] = {(cuuint64_t)(g * rb / 2), (cuuint64_t)(N / g)};
+  const cuuint64_t strides[1] = {(cuuint64_t)(g * rb)};
+  const cuuint32_t box[2] = {(cuuint32_t)(kQ6Win / 2), (cuuint32_t)(kBM / g)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(w), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int g_sms_tc = 0;
 
 int num_sms() {
@@ -575,16 +639,19 @@ int num_sms() {
   return g_sms_tc;
 }
 
-// Token tile: the multiple of 16 (<= 256) that minimises waves x tile cost.
+// Token tile: the multiple of 16 (<= 256) that minimises waves x tile cost,
+// where a tile costs its MMA time (~BN) plus a per-tile share (dequantizing
+// the 128 x K weight tile and the epilogue) worth about 64 tokens; ties go to
+// the larger tile.
 int choose_bn(int64_t M, int64_t N) {
   const int64_t ntn = (N + kBM - 1) / kBM;
   if (M <= kMaxBN) return (int)((M + 15) / 16 * 16);
   int best = kMaxBN;
   double best_cost = 1e30;
-  for (int bn = 128; bn <= kMaxBN; bn += 16) {
+  for (int bn = kMaxBN; bn >= 128; bn -= 16) {
     const int64_t tiles = ntn * ((M + bn - 1) / bn);
     const int64_t waves = (tiles + num_sms() - 1) / num_sms();
-    const double cost = (double)waves * (bn + 32);
+    const double cost = (double)waves * (bn + 64);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = bn;
@@ -592,6 +659,8 @@ int choose_bn(int64_t M, int64_t N) {
   }
   return best;
 }
+
+constexpr int kSmemLimit = 227 * 1024;
 
 template <int QT, bool GATEUP>
 cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
@@ -602,11 +671,19 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   memset(&tw0, 0, sizeof(tw0));
   memset(&tw1, 0, sizeof(tw1));
   if (!make_tmap_x(&tx, x, M, K, BN)) return cudaErrorInvalidValue;
+  Params p;
+  p.q6_group = 1;
+  p.q6_rows_tma = 0;
   if (QT == kQ4K) {
     if (!make_tmap_q4k(&tw0, W0, N, K)) return cudaErrorInvalidValue;
     if (GATEUP && !make_tmap_q4k(&tw1, W1, N, K)) return cudaErrorInvalidValue;
+  } else {
+    p.q6_group = q6_group(K);
+    if (N / p.q6_group > 0) {
+      if (!make_tmap_q6k(&tw0, W0, N, K, p.q6_group)) return cudaErrorInvalidValue;
+      p.q6_rows_tma = (int)((N / p.q6_group) * p.q6_group);
+    }
   }
-  Params p;
   p.w[0] = static_cast<const uint8_t*>(W0);
   p.w[1] = static_cast<const uint8_t*>(W1);
   p.w_bytes = N * (K / kQK) * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
@@ -615,16 +692,22 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   p.N = (int)N;
   p.K = (int)K;
   p.BN = BN;
+  // As many K-step stages as fit in shared memory (2 .. 8).
+  int S = C::kMaxStages;
+  while (S > 2 && make_layout<QT, GATEUP>(BN, S).total > (uint32_t)kSmemLimit) --S;
+  p.stages = S;
+  const uint32_t smem = make_layout<QT, GATEUP>(BN, S).total;
+  if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         C::kSmemBytes);
+                                         kSmemLimit);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + BN - 1) / BN));
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-  gemm_tc_kernel<QT, GATEUP><<<grid, C::kThreads, C::kSmemBytes, stream>>>(tx, tw0, tw1, p);
+  gemm_tc_kernel<QT, GATEUP><<<grid, C::kThreads, smem, stream>>>(tx, tw0, tw1, p);
   return cudaGetLastError();
 }
 

@@ -298,7 +298,7 @@ __device__ __forceinline__ void compute_block(const BlockRegs<kQ6K>& r, const ui
 // first block) while it computes the current one.  Shared memory: xp (2K
 // bytes), sx16 (K/4 bytes), partial sums (tpc*ks*16 floats).
 template <int QT>
-__global__ void __launch_bounds__(512) gemv_m1_kernel(const uint8_t* __restrict__ W,
+__global__ void __maxnreg__(128) gemv_m1_kernel(const uint8_t* __restrict__ W,
                                                       const uint16_t* __restrict__ x, float* __restrict__ y, int N,
                                                       int K, int ks, int tpc) {
   extern __shared__ __align__(16) uint8_t smem[];
@@ -389,36 +389,47 @@ uint32_t gemv_take_status() {
   return v;
 }
 
-// Warps per 16-row tile (ks) divide the K/256 blocks: the smallest split that
-// puts about 32 warps per SM in flight, else the largest available (<= 16).
-static int choose_ks(int64_t N, int nb) {
+// Launch shape.  ks warps split the K/256 blocks of a 16-row tile (ks divides
+// the block count, ks <= 12); tpc tiles share a CTA when ks is small.  With up
+// to 128 registers a thread, an SM holds 512 threads, so a CTA of T threads
+// gets floor(512 / T) slots per SM.  Prefer the largest ks (shortest per-warp
+// chains, most loads in flight) whose CTAs all fit in one wave.
+struct GemvShape {
+  int ks, tpc, threads;
+  int64_t grid;
+};
+
+static GemvShape choose_shape(int64_t N, int nb) {
   const int64_t tiles = (N + 15) / 16;
-  const int64_t target = (int64_t)sm_count() * 32;
-  int best = 1;
-  for (int d = 1; d <= 16 && d <= nb; ++d) {
+  const int64_t sms = sm_count();
+  GemvShape best{1, 8, 256, 0};
+  for (int d = std::min(nb, 12); d >= 1; --d) {
     if (nb % d) continue;
-    best = d;
-    if (tiles * d >= target) break;
+    const int tpc = std::max(1, 4 / d);
+    const int threads = 32 * d * tpc;
+    const int64_t slots = sms * std::max(1, 512 / threads);
+    const int64_t ctas = (tiles + tpc - 1) / tpc;
+    if (ctas <= slots) return GemvShape{d, tpc, threads, ctas};
   }
+  best.grid = std::min<int64_t>((tiles + best.tpc - 1) / best.tpc, sms * 2);
   return best;
 }
 
 cudaError_t launch_gemv(QType t, const void* W, const uint16_t* x, float* y, int64_t N, int64_t K,
                         cudaStream_t s) {
   const int nb = (int)(K / kQK);
-  const int ks = choose_ks(N, nb);
-  const int tpc = std::max(1, 8 / ks);  // at least 8 warps per CTA
-  const int threads = 32 * ks * tpc;
-  const size_t smem = (size_t)2 * K + (size_t)K / 4 + (size_t)tpc * ks * 16 * sizeof(float);
-  const int64_t tiles = (N + 15) / 16;
-  const int per_sm = std::max(1, 2048 / threads);
-  const int64_t grid = std::min<int64_t>((tiles + tpc - 1) / tpc, (int64_t)sm_count() * per_sm);
+  const GemvShape sh = choose_shape(N, nb);
+  const size_t smem = (size_t)2 * K + (size_t)K / 4 + (size_t)sh.tpc * sh.ks * 16 * sizeof(float);
   if (t == kQ4K) {
-    if (smem > 48 * 1024) cudaFuncSetAttribute(gemv_m1_kernel<kQ4K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    gemv_m1_kernel<kQ4K><<<(int)grid, threads, smem, s>>>(static_cast<const uint8_t*>(W), x, y, (int)N, (int)K, ks, tpc);
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(gemv_m1_kernel<kQ4K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    gemv_m1_kernel<kQ4K><<<(int)sh.grid, sh.threads, smem, s>>>(static_cast<const uint8_t*>(W), x, y, (int)N, (int)K,
+                                                                sh.ks, sh.tpc);
   } else {
-    if (smem > 48 * 1024) cudaFuncSetAttribute(gemv_m1_kernel<kQ6K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    gemv_m1_kernel<kQ6K><<<(int)grid, threads, smem, s>>>(static_cast<const uint8_t*>(W), x, y, (int)N, (int)K, ks, tpc);
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(gemv_m1_kernel<kQ6K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    gemv_m1_kernel<kQ6K><<<(int)sh.grid, sh.threads, smem, s>>>(static_cast<const uint8_t*>(W), x, y, (int)N, (int)K,
+                                                                sh.ks, sh.tpc);
   }
   return cudaGetLastError();
 }
