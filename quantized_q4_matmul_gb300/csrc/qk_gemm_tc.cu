@@ -28,6 +28,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cstring>
 
 #include "qk_device.cuh"
@@ -67,14 +68,14 @@ struct Layout {
   uint32_t x_off, x_stage, a_off, p_off, bar_off, total;
 };
 
-template <int QT, bool GATEUP>
+template <int QT, bool GATEUP, bool AT>
 __host__ __device__ inline Layout make_layout(int BN, int S) {
   using C = Cfg<QT, GATEUP>;
   Layout L;
   L.x_stage = (uint32_t)BN * kBK * 2;
   L.x_off = 0;
   L.a_off = L.x_off + (uint32_t)S * L.x_stage;
-  L.p_off = L.a_off + (uint32_t)(S * C::kNumB) * kAStageBytes;
+  L.p_off = L.a_off + (AT ? 0u : (uint32_t)(S * C::kNumB) * kAStageBytes);
   L.bar_off = L.p_off + (uint32_t)C::kPBytes;
   L.total = L.bar_off + 256 + 1024;  // barriers + base alignment slack
   return L;
@@ -145,9 +146,9 @@ __device__ __forceinline__ void q4_scale_min(uint32_t s03, uint32_t s47, uint32_
 
 // Dequantize half `part` of K step c (0..3) of a Q4_K super-block row held at
 // `rowp` in shared memory: part 0 = the low nibbles (sub-block 2c, step-local
-// k 0..31), part 1 = the high nibbles (sub-block 2c+1, k 32..63).  Writes 32
-// fp16 weights into row r of the swizzled A tile.
-__device__ __forceinline__ void q4_kstep(const uint8_t* rowp, int c, int part, uint8_t* a_tile, int r) {
+// k 0..31), part 1 = the high nibbles (sub-block 2c+1, k 32..63).  r[4j..4j+3]
+// receive the 8 fp16 weights of k = 32*part + 8j .. +7 as four k-ordered pairs.
+__device__ __forceinline__ void q4_kstep_regs(const uint8_t* rowp, int c, int part, uint32_t (&r)[16]) {
   const uint4 hdr = *reinterpret_cast<const uint4*>(rowp);
   const float d = h2f(hdr.x), dmin = h2f(hdr.x >> 16);
   float sc, mn;
@@ -158,16 +159,22 @@ __device__ __forceinline__ void q4_kstep(const uint8_t* rowp, int c, int part, u
   const uint32_t wv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
   const int shift = 4 * part;
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {  // chunk 4*part + j: k = 32*part + 8j .. +7 (words 2j, 2j+1)
-    uint4 o, t;
-    q4_emit4((wv[2 * j] >> shift) & 0x0F0F0F0Fu, dsc, ndmn, t);
-    o.x = t.x;
-    o.y = t.y;
-    q4_emit4((wv[2 * j + 1] >> shift) & 0x0F0F0F0Fu, dsc, ndmn, t);
-    o.z = t.x;
-    o.w = t.y;
-    *reinterpret_cast<uint4*>(a_tile + sw128_off(r, 4 * part + j)) = o;
+  for (int i = 0; i < 8; ++i) {
+    uint4 t;
+    q4_emit4((wv[i] >> shift) & 0x0F0F0F0Fu, dsc, ndmn, t);
+    r[2 * i] = t.x;
+    r[2 * i + 1] = t.y;
   }
+}
+
+// The same 32 weights written into row rr of a swizzled shared-memory A tile.
+__device__ __forceinline__ void q4_kstep(const uint8_t* rowp, int c, int part, uint8_t* a_tile, int rr) {
+  uint32_t r[16];
+  q4_kstep_regs(rowp, c, part, r);
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(a_tile + sw128_off(rr, 4 * part + j)) =
+        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
 }
 
 // Q6_K.  The block of a row sits in its smem slot at byte offset MIS (even,
@@ -283,7 +290,9 @@ __device__ __forceinline__ int dq_row(int t, int g) {
   }
 }
 
-template <int QT, bool GATEUP>
+// AT: the dequantized A tiles live in tensor memory (tcgen05.st from the
+// dequant threads, UMMA reads A from TMEM) instead of shared memory.
+template <int QT, bool GATEUP, bool AT>
 __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
                    const __grid_constant__ CUtensorMap tm_w1, const Params p) {
@@ -291,7 +300,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int S = p.stages;
-  const Layout L = make_layout<QT, GATEUP>(p.BN, S);
+  const Layout L = make_layout<QT, GATEUP, AT>(p.BN, S);
   Bars* bars = reinterpret_cast<Bars*>(smem + L.bar_off);
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
@@ -318,8 +327,12 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  const uint32_t tmem_cols = GATEUP ? (BN <= 64 ? 128 : BN <= 128 ? 256 : 512)
-                                    : (BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256);
+  // Accumulators: kNumB x BN columns; with AT also S x kNumB A tiles of 32
+  // columns (128 rows x 64 fp16) after them.
+  const uint32_t a_col0 = (uint32_t)(C::kNumB * BN);
+  const uint32_t need_cols = a_col0 + (AT ? (uint32_t)(S * C::kNumB * 32) : 0u);
+  const uint32_t tmem_cols = need_cols <= 32 ? 32 : need_cols <= 64 ? 64 : need_cols <= 128 ? 128
+                             : need_cols <= 256 ? 256 : 512;
   if (warp == 1) {
     tmem_alloc(&bars->tmem_base, tmem_cols);
     tmem_relinquish();
@@ -429,13 +442,21 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
         const uint64_t bdesc = umma_desc_sw128(xa);
 #pragma unroll
         for (int t = 0; t < C::kNumB; ++t) {
-          const uint32_t aa = smem_u32(smem + L.a_off + (s * C::kNumB + t) * kAStageBytes);
-          const uint64_t adesc = umma_desc_sw128(aa);
+          if constexpr (AT) {
+            const uint32_t a_tm = tmem + a_col0 + (uint32_t)((s * C::kNumB + t) * 32);
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            // +32 bytes per 16-wide K slice inside the swizzle atom (start address in 16 B units)
-            umma_f16_ss(tmem + (uint32_t)(t * BN), adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
-                        (step > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk)  // 16-wide K slice = 8 TMEM columns of A
+              umma_f16_ts(tmem + (uint32_t)(t * BN), a_tm + (uint32_t)(8 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                          (step > 0 || kk > 0) ? 1u : 0u);
+          } else {
+            const uint32_t aa = smem_u32(smem + L.a_off + (s * C::kNumB + t) * kAStageBytes);
+            const uint64_t adesc = umma_desc_sw128(aa);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              // +32 bytes per 16-wide K slice inside the swizzle atom (start address in 16 B units)
+              umma_f16_ss(tmem + (uint32_t)(t * BN), adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                          (step > 0 || kk > 0) ? 1u : 0u);
+            }
           }
         }
         umma_commit(&bars->s_empty[s]);
@@ -456,7 +477,9 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     const int tpt = 32 * C::kDqWarps / C::kNumB;  // threads per weight tensor (256)
     const int which = t / tpt;                    // weight tensor (0 = gate/only, 1 = up)
     const int part = (t % tpt) >> 7;              // which half of the work on this row
-    const int rho = dq_row<QT>(t & 127, p.q6_group);  // tile row this thread dequantizes
+    // With A in TMEM a warp may only write its own lane quarter (warp % 4).
+    const int rho = AT ? 32 * (warp & 3) + lane : dq_row<QT>(t & 127, p.q6_group);
+    const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
     int step = 0;
     bool ok = true;
@@ -471,11 +494,23 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
         for (int c = 0; c < 4; ++c, ++step) {
           const int s = step % S;
           const uint32_t ph = (uint32_t)(step / S) & 1u;
-          ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
-          if (!ok) break;
-          uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
-          q4_kstep(rowp, c, part, a_tile, rho);
-          fence_proxy_async_smem();
+          if constexpr (AT) {
+            uint32_t r[16];
+            q4_kstep_regs(rowp, c, part, r);  // overlaps the wait below
+            ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
+            ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
+            if (!ok) break;
+            tc_fence_after();
+            tmem_st16(a_lane + a_col0 + (uint32_t)((s * C::kNumB + which) * 32 + 16 * part), r);
+            tmem_wait_st();
+            tc_fence_before();
+          } else {
+            ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
+            if (!ok) break;
+            uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
+            q4_kstep(rowp, c, part, a_tile, rho);
+            fence_proxy_async_smem();
+          }
           mbar_arrive(&bars->a_full[s]);
         }
       } else {
@@ -503,6 +538,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
 
     // -------------------------------------------------------------- epilogue
     if (ok) ok = mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status);
+    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
     if (ok) {
       tc_fence_after();
       const int q = warp & 3;                 // TMEM lane quarter this warp may access
@@ -662,7 +698,7 @@ int choose_bn(int64_t M, int64_t N) {
 
 constexpr int kSmemLimit = 227 * 1024;
 
-template <int QT, bool GATEUP>
+template <int QT, bool GATEUP, bool AT>
 cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
                       cudaStream_t stream) {
   using C = Cfg<QT, GATEUP>;
@@ -694,20 +730,23 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   p.BN = BN;
   // As many K-step stages as fit in shared memory (2 .. 8).
   int S = C::kMaxStages;
-  while (S > 2 && make_layout<QT, GATEUP>(BN, S).total > (uint32_t)kSmemLimit) --S;
+  while (S > 2 && (make_layout<QT, GATEUP, AT>(BN, S).total > (uint32_t)kSmemLimit ||
+                   (AT && C::kNumB * BN + S * C::kNumB * 32 > 512)))
+    --S;
+  if (AT && C::kNumB * BN + S * C::kNumB * 32 > 512) return cudaErrorInvalidConfiguration;
   p.stages = S;
-  const uint32_t smem = make_layout<QT, GATEUP>(BN, S).total;
+  const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, S).total;
   if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemLimit);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   dim3 grid((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + BN - 1) / BN));
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-  gemm_tc_kernel<QT, GATEUP><<<grid, C::kThreads, smem, stream>>>(tx, tw0, tw1, p);
+  gemm_tc_kernel<QT, GATEUP, AT><<<grid, C::kThreads, smem, stream>>>(tx, tw0, tw1, p);
   return cudaGetLastError();
 }
 
@@ -722,9 +761,16 @@ uint32_t gemm_take_status() {
 
 cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N,
                         int64_t K, bool gateup, cudaStream_t s) {
-  if (gateup) return launch_tc<kQ4K, true>(W, W_up, x, y, M, N, K, s);
-  if (t == kQ4K) return launch_tc<kQ4K, false>(W, nullptr, x, y, M, N, K, s);
-  return launch_tc<kQ6K, false>(W, nullptr, x, y, M, N, K, s);
+  static const int a_tmem = [] {
+    const char* e = getenv("QK_A_TMEM");
+    return e ? atoi(e) : 0;
+  }();
+  if (gateup) return launch_tc<kQ4K, true, false>(W, W_up, x, y, M, N, K, s);
+  if (t == kQ4K) {
+    if (a_tmem) return launch_tc<kQ4K, false, true>(W, nullptr, x, y, M, N, K, s);
+    return launch_tc<kQ4K, false, false>(W, nullptr, x, y, M, N, K, s);
+  }
+  return launch_tc<kQ6K, false, false>(W, nullptr, x, y, M, N, K, s);
 }
 
 }  // namespace qk
