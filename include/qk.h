@@ -78,9 +78,11 @@ qk_status qk_dequant_q6k(const void *blocks, int64_t n_blocks, float *out, qk_st
  * y[m][n] = sum_k x[m][k] * w[n][k] for Q4_K weights W (N x K), fp16 x, fp32 y
  * (DAMASCUS project overview, "[01] the thesis" / "[04] one decode step";
  * "Building DAMASCUS", "Prefill and decode need different performance
- * questions").  M = 1 runs the decode GEMV (fp32 weights, fp32 accumulation);
- * larger M runs the tensor-core GEMM (weights dequantized to fp16 in shared
- * memory, never written to device memory; fp32 accumulation in tensor memory),
+ * questions").  M = 1 runs the decode GEMV (products of the integer quants
+ * with fp16 x are exact, sums fp32, block scales applied per sub-block in
+ * fp32); larger M runs the tensor-core GEMM (weights dequantized to fp16 in
+ * shared or tensor memory, never written to device memory; fp32 accumulation
+ * in tensor memory),
  * as the overview's "fused dequant -> matrix unit never materializes FP16
  * weights" describes.  The two paths agree within rounding; results are not
  * bit-identical across M.
@@ -101,6 +103,37 @@ qk_status qk_matmul_q6k(const void *blocks, const uint16_t *x_f16, float *y, int
  */
 qk_status qk_gateup_swiglu_q4k(const void *gate_blocks, const void *up_blocks, const uint16_t *x_f16,
                                uint16_t *y_f16, int64_t M, int64_t N_ff, int64_t K, qk_stream_t stream);
+
+/* Weight formats for qk_matmul_desc.qtype. */
+#define QK_Q4_K 0
+#define QK_Q6_K 1
+
+/*
+ * One problem of a grouped call.  up_blocks == NULL: y[M][N] (fp32) = x . W^T
+ * with W in format `qtype`.  up_blocks != NULL: the fused gate/up + SwiGLU of
+ * qk_gateup_swiglu_q4k (qtype must be QK_Q4_K, blocks = gate, y fp16).
+ */
+typedef struct qk_matmul_desc {
+  int qtype;
+  const void *blocks;
+  const void *up_blocks;
+  const uint16_t *x_f16;
+  void *y;
+  int64_t M, N, K;
+} qk_matmul_desc;
+
+/*
+ * Run `count` independent problems (DAMASCUS project overview, "[04] one
+ * decode step": the QKV projections share x, gate and up share x, and every
+ * decode-step linear is an M = 1 GEMV).  Problems with M = 1 are executed
+ * together, up to 8 per kernel launch, so small GEMVs share one launch and
+ * stream their weights concurrently; other problems run as in
+ * qk_matmul_q4k / qk_matmul_q6k / qk_gateup_swiglu_q4k.  Each entry obeys the
+ * rules of its single-problem entry point; in addition no y may overlap any
+ * input or output of another entry.  count = 0 is a no-op.  Results are
+ * identical to calling the single-problem entry points one by one.
+ */
+qk_status qk_matmul_batch(const qk_matmul_desc *descs, int count, qk_stream_t stream);
 
 /*
  * Synchronise `stream`, then report and clear the device-side status flags

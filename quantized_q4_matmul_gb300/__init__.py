@@ -14,14 +14,24 @@ import os
 
 __all__ = [
     "QKError", "lib", "lib_path", "qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k",
-    "qk_gateup_swiglu_q4k", "qk_get_device_status", "qk_status_string", "qk_version", "QK_BLOCK_BYTES",
+    "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_get_device_status", "qk_status_string", "qk_version",
+    "QK_BLOCK_BYTES", "qk_matmul_desc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 QK_BLOCK_BYTES = {"q4k": 144, "q6k": 210}
 
 SYMBOLS = ("qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k", "qk_gateup_swiglu_q4k",
-           "qk_get_device_status", "qk_status_string", "qk_version")
+           "qk_matmul_batch", "qk_get_device_status", "qk_status_string", "qk_version")
+
+QK_Q4_K, QK_Q6_K = 0, 1
+
+
+class qk_matmul_desc(ctypes.Structure):
+    """Mirror of ``qk_matmul_desc`` in include/qk.h."""
+    _fields_ = [("qtype", ctypes.c_int), ("blocks", ctypes.c_void_p), ("up_blocks", ctypes.c_void_p),
+                ("x_f16", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 class QKError(RuntimeError):
@@ -55,6 +65,8 @@ def lib():
             f.restype, f.argtypes = i32, [vp, vp, vp, i64, i64, i64, vp]
         L.qk_gateup_swiglu_q4k.restype = i32
         L.qk_gateup_swiglu_q4k.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+        L.qk_matmul_batch.restype = i32
+        L.qk_matmul_batch.argtypes = [ctypes.POINTER(qk_matmul_desc), i32, vp]
         L.qk_get_device_status.restype, L.qk_get_device_status.argtypes = i32, [vp]
         L.qk_status_string.restype, L.qk_status_string.argtypes = ctypes.c_char_p, [i32]
         L.qk_version.restype, L.qk_version.argtypes = i32, []
@@ -113,6 +125,19 @@ def qk_matmul_q6k(blocks, x_f16, y, M: int, N: int, K: int, stream=None) -> None
 def qk_gateup_swiglu_q4k(gate_blocks, up_blocks, x_f16, y_f16, M: int, N_ff: int, K: int, stream=None) -> None:
     _check(lib().qk_gateup_swiglu_q4k(_addr(gate_blocks), _addr(up_blocks), _addr(x_f16), _addr(y_f16), int(M),
                                       int(N_ff), int(K), _stream(stream)), "qk_gateup_swiglu_q4k")
+
+
+def qk_matmul_batch(problems, stream=None) -> None:
+    """Run independent problems in as few launches as possible.  Each problem is
+    a dict with keys qtype ("q4k"/"q6k" or 0/1), blocks, x_f16, y, M, N, K and
+    optionally up_blocks (fused gate/up + SwiGLU, fp16 y)."""
+    arr = (qk_matmul_desc * max(1, len(problems)))()
+    for i, p in enumerate(problems):
+        qt = p["qtype"]
+        qt = {"q4k": QK_Q4_K, "q6k": QK_Q6_K}.get(qt, qt)
+        arr[i] = qk_matmul_desc(int(qt), _addr(p["blocks"]), _addr(p.get("up_blocks")), _addr(p["x_f16"]),
+                                _addr(p["y"]), int(p["M"]), int(p["N"]), int(p["K"]))
+    _check(lib().qk_matmul_batch(arr, len(problems), _stream(stream)), "qk_matmul_batch")
 
 
 def qk_get_device_status(stream=None) -> None:

@@ -8,6 +8,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <vector>
 
 #include "../../include/qk.h"
 #include "qk_internal.h"
@@ -84,29 +85,115 @@ qk_status dequant(QType t, const void* blocks, int64_t n_blocks, float* out, cud
   return map_cuda(qk::launch_dequant(t, blocks, n_blocks, out, s));
 }
 
-qk_status matmul(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N,
-                 int64_t K, bool gateup, cudaStream_t s) {
+struct Checked {
+  int64_t w_bytes, x_bytes, y_bytes;
+};
+
+// Host-only checks of one problem (no CUDA call); fills the byte extents.
+qk_status validate_host(QType t, const void* W, const void* W_up, const uint16_t* x, const void* y, int64_t M,
+                        int64_t N, int64_t K, bool gateup, Checked* c) {
   if (M < 0 || N < 0 || K < 0) return QK_ERR_SHAPE;
   if (K == 0 || K % qk::kQK != 0) return QK_ERR_SHAPE;
   if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return QK_ERR_SHAPE;
-  if (M == 0 || N == 0) return QK_OK;
+  if (gateup && t != qk::kQ4K) return QK_ERR_SHAPE;
+  if (M == 0 || N == 0) {
+    c->w_bytes = c->x_bytes = c->y_bytes = 0;
+    return QK_OK;
+  }
   if (!W || !x || !y || (gateup && !W_up)) return QK_ERR_NULL;
   if (!aligned16(W) || !aligned16(x) || !aligned16(y) || (gateup && !aligned16(W_up))) return QK_ERR_ALIGN;
-  int64_t w_bytes, x_elems, x_bytes, y_elems, y_bytes;
-  if (!mul_ok(N, (K / qk::kQK) * qk::block_bytes(t), &w_bytes) || !mul_ok(M, K, &x_elems) ||
-      !mul_ok(x_elems, 2, &x_bytes) || !mul_ok(M, N, &y_elems) || !mul_ok(y_elems, gateup ? 2 : 4, &y_bytes))
+  int64_t x_elems, y_elems;
+  if (!mul_ok(N, (K / qk::kQK) * qk::block_bytes(t), &c->w_bytes) || !mul_ok(M, K, &x_elems) ||
+      !mul_ok(x_elems, 2, &c->x_bytes) || !mul_ok(M, N, &y_elems) || !mul_ok(y_elems, gateup ? 2 : 4, &c->y_bytes))
     return QK_ERR_SHAPE;
+  return QK_OK;
+}
+
+// Device-side checks (architecture, pointer kinds, aliasing) after validate_host.
+qk_status validate_device(const void* W, const void* W_up, const uint16_t* x, const void* y, int64_t M, int64_t N,
+                          bool gateup, const Checked& ck) {
+  if (M == 0 || N == 0) return QK_OK;
+  const Checked* c = &ck;
   qk_status st = check_device();
   if (st != QK_OK) return st;
   if ((st = check_pointer(W)) != QK_OK || (st = check_pointer(x)) != QK_OK || (st = check_pointer(y)) != QK_OK)
     return st;
   if (gateup && (st = check_pointer(W_up)) != QK_OK) return st;
-  if (overlaps(y, y_bytes, x, x_bytes) || overlaps(y, y_bytes, W, w_bytes) ||
-      (gateup && overlaps(y, y_bytes, W_up, w_bytes)))
+  if (overlaps(y, c->y_bytes, x, c->x_bytes) || overlaps(y, c->y_bytes, W, c->w_bytes) ||
+      (gateup && overlaps(y, c->y_bytes, W_up, c->w_bytes)))
     return QK_ERR_ALIAS;
-  if (!gateup && M <= qk::gemv_max_m())
-    return map_cuda(qk::launch_gemv(t, W, x, static_cast<float*>(y), N, K, s));
+  return QK_OK;
+}
+
+// The decode GEMV handles M = 1 (gate/up only when K/256 is a multiple of 4).
+bool use_gemv(int64_t M, int64_t K, bool gateup) {
+  return M <= qk::gemv_max_m() && (!gateup || (K / qk::kQK) % 4 == 0);
+}
+
+qk_status run(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
+              bool gateup, cudaStream_t s) {
+  if (use_gemv(M, K, gateup)) {
+    qk::GemvDesc d{t, W, gateup ? W_up : nullptr, x, y, N, K};
+    return map_cuda(qk::launch_gemv_batch(&d, 1, s));
+  }
   return map_cuda(qk::launch_gemm(t, W, W_up, x, y, M, N, K, gateup, s));
+}
+
+qk_status matmul(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N,
+                 int64_t K, bool gateup, cudaStream_t s) {
+  Checked c;
+  qk_status st = validate_host(t, W, W_up, x, y, M, N, K, gateup, &c);
+  if (st == QK_OK) st = validate_device(W, W_up, x, y, M, N, gateup, c);
+  if (st != QK_OK || M == 0 || N == 0) return st;
+  return run(t, W, W_up, x, y, M, N, K, gateup, s);
+}
+
+qk_status matmul_batch(const qk_matmul_desc* d, int count, cudaStream_t s) {
+  if (count < 0) return QK_ERR_SHAPE;
+  if (count == 0) return QK_OK;
+  if (!d) return QK_ERR_NULL;
+  std::vector<Checked> ck((size_t)count);
+  for (int i = 0; i < count; ++i) {
+    if (d[i].qtype != QK_Q4_K && d[i].qtype != QK_Q6_K) return QK_ERR_SHAPE;
+    const QType t = d[i].qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K;
+    const qk_status st = validate_host(t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].M, d[i].N, d[i].K,
+                                       d[i].up_blocks != nullptr, &ck[(size_t)i]);
+    if (st != QK_OK) return st;
+  }
+  for (int i = 0; i < count; ++i) {
+    const qk_status st = validate_device(d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].M, d[i].N,
+                                         d[i].up_blocks != nullptr, ck[(size_t)i]);
+    if (st != QK_OK) return st;
+  }
+  for (int i = 0; i < count; ++i)
+    for (int j = 0; j < count; ++j) {
+      if (i == j || ck[(size_t)i].y_bytes == 0 || ck[(size_t)j].y_bytes == 0) continue;
+      const int64_t wb = ck[(size_t)j].w_bytes;
+      if (overlaps(d[i].y, ck[(size_t)i].y_bytes, d[j].y, ck[(size_t)j].y_bytes) ||
+          overlaps(d[i].y, ck[(size_t)i].y_bytes, d[j].x_f16, ck[(size_t)j].x_bytes) ||
+          overlaps(d[i].y, ck[(size_t)i].y_bytes, d[j].blocks, wb) ||
+          (d[j].up_blocks && overlaps(d[i].y, ck[(size_t)i].y_bytes, d[j].up_blocks, wb)))
+        return QK_ERR_ALIAS;
+    }
+  std::vector<qk::GemvDesc> group;
+  for (int i = 0; i < count; ++i) {
+    if (d[i].M == 0 || d[i].N == 0) continue;
+    const QType t = d[i].qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K;
+    const bool gu = d[i].up_blocks != nullptr;
+    if (use_gemv(d[i].M, d[i].K, gu)) {
+      group.push_back(qk::GemvDesc{t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].N, d[i].K});
+      if ((int)group.size() == qk::kMaxGemvProbs) {
+        const qk_status st = map_cuda(qk::launch_gemv_batch(group.data(), (int)group.size(), s));
+        if (st != QK_OK) return st;
+        group.clear();
+      }
+    } else {
+      const qk_status st = run(t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].M, d[i].N, d[i].K, gu, s);
+      if (st != QK_OK) return st;
+    }
+  }
+  if (!group.empty()) return map_cuda(qk::launch_gemv_batch(group.data(), (int)group.size(), s));
+  return QK_OK;
 }
 
 }  // namespace
@@ -135,6 +222,10 @@ qk_status qk_gateup_swiglu_q4k(const void* gate_blocks, const void* up_blocks, c
                                uint16_t* y_f16, int64_t M, int64_t N_ff, int64_t K, qk_stream_t stream) {
   return matmul(qk::kQ4K, gate_blocks, up_blocks, x_f16, y_f16, M, N_ff, K, true,
                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+qk_status qk_matmul_batch(const qk_matmul_desc* descs, int count, qk_stream_t stream) {
+  return matmul_batch(descs, count, reinterpret_cast<cudaStream_t>(stream));
 }
 
 qk_status qk_get_device_status(qk_stream_t stream) {

@@ -34,6 +34,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstring>
 
 #include "qk_device.cuh"
 #include "qk_internal.h"
@@ -45,6 +46,20 @@ __device__ uint32_t g_gemv_status = 0;
 namespace {
 
 constexpr uint32_t kMagic = 0x64006400u;  // fp16x2 (1024.0, 1024.0)
+
+struct GemvProb {
+  const uint8_t* w0;  // weights (gate for kind 1)
+  const uint8_t* w1;  // up weights (kind 1), else null
+  const uint16_t* x;
+  void* y;
+  int N, K, qtype, kind;
+  int ks, units, cta_begin, ctas;
+};
+
+struct GemvBatch {
+  GemvProb p[kMaxGemvProbs];
+  int count;
+};
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -289,19 +304,25 @@ __device__ __forceinline__ void compute_block(const BlockRegs<kQ6K>& r, const ui
 }
 
 // ---------------------------------------------------------------------------
-// The kernel: one 16-row tile per CTA iteration, `ks` warps split the K blocks.
-// Shared memory: xp (2K bytes), sx16 (K/4 bytes), partial sums (ks*16 floats).
+// The grouped kernel.  One launch runs up to kMaxGemvProbs independent M = 1
+// problems (e.g. the seven linears of a decoder layer).  Each problem owns a
+// contiguous range of CTAs, sized by its share of the total weight bytes, so
+// every CTA stages one x and the whole launch finishes together.  A CTA has 8
+// warps: `ks` warps split the K blocks of a 16-row tile and `tpc` = 8 / ks
+// tiles are processed side by side; the CTA walks its contiguous range of
+// such units, every warp loading the next block (or the next unit's first
+// block) while it computes the current one.  Partial sums of the ks warps of
+// a tile meet in shared memory in a fixed order (deterministic).
+//
+// Problem kind 1 is the fused gate/up + SwiGLU: sub-tile 0 holds rows of the
+// gate weights, sub-tile 1 the same rows of the up weights, and the epilogue
+// writes fp16(silu(g) * u).
 // ---------------------------------------------------------------------------
-// The kernel: each CTA iteration covers `tpc` 16-row tiles; the `ks` warps of
-// a tile split its K/256 blocks.  Each warp issues the loads of its first
-// block before the CTA stages x, and loads the next block (or the next tile's
-// first block) while it computes the current one.  Shared memory: xp (2K
-// bytes), sx16 (K/4 bytes), partial sums (tpc*ks*16 floats).
+constexpr int kGemvWarps = 8;
+
 template <int QT>
-__global__ void __maxnreg__(128) gemv_m1_kernel(const uint8_t* __restrict__ W,
-                                                      const uint16_t* __restrict__ x, float* __restrict__ y, int N,
-                                                      int K, int ks, int tpc) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uint8_t* smem) {
+  const int K = P.K, N = P.N, ks = P.ks, tpc = kGemvWarps / P.ks;
   uint2* xp = reinterpret_cast<uint2*>(smem);
   float* sx16 = reinterpret_cast<float*>(smem + 2 * K);
   float* red = sx16 + K / 16;
@@ -315,32 +336,39 @@ __global__ void __maxnreg__(128) gemv_m1_kernel(const uint8_t* __restrict__ W,
   constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
   const int64_t RB = (int64_t)nb * kBB;
   const int ntiles = (N + 15) / 16;
-  const int stride = gridDim.x * tpc;
+  // Units of this CTA: [u_begin, u_end).  A unit is tpc tiles (or, for gate/up,
+  // one tile of each weight tensor).
+  const int u_begin = (int)((int64_t)cta * P.units / P.ctas);
+  const int u_end = (int)((int64_t)(cta + 1) * P.units / P.ctas);
+  const bool gu = P.kind == 1;
+  const uint8_t* Wsub = (gu && sub == 1) ? P.w1 : P.w0;
 
+  auto tile_of = [&](int u) { return gu ? u : u * tpc + sub; };
   auto row_ptr = [&](int tile, int which) {
     const int r = min(tile * 16 + g + 8 * which, N - 1);
-    return W + r * RB;
+    return Wsub + r * RB;
   };
 
   BlockRegs<QT> cur;
-  int tile = blockIdx.x * tpc + sub;
-  if (tile < ntiles) load_block(cur, row_ptr(tile, 0) + b_begin * kBB, row_ptr(tile, 1) + b_begin * kBB, tig);
-  stage_x(x, K, xp, sx16);
+  if (u_begin < u_end && tile_of(u_begin) < ntiles)
+    load_block(cur, row_ptr(tile_of(u_begin), 0) + b_begin * kBB, row_ptr(tile_of(u_begin), 1) + b_begin * kBB,
+               tig);
+  stage_x(P.x, K, xp, sx16);
   __syncthreads();
 
-  for (int tile0 = blockIdx.x * tpc; tile0 < ntiles; tile0 += stride) {
-    tile = tile0 + sub;
+  for (int u = u_begin; u < u_end; ++u) {
+    const int tile = tile_of(u);
     float y0 = 0.f, y1 = 0.f;
     if (tile < ntiles) {
       const uint8_t* row0 = row_ptr(tile, 0);
       const uint8_t* row1 = row_ptr(tile, 1);
+      const int tile_next = tile_of(u + 1);
       for (int b = b_begin; b < b_begin + bpw; ++b) {
         BlockRegs<QT> nxt;
         if (b + 1 < b_begin + bpw) {
           load_block(nxt, row0 + (b + 1) * kBB, row1 + (b + 1) * kBB, tig);
-        } else if (tile + stride < ntiles) {
-          load_block(nxt, row_ptr(tile + stride, 0) + b_begin * kBB, row_ptr(tile + stride, 1) + b_begin * kBB,
-                     tig);
+        } else if (u + 1 < u_end && tile_next < ntiles) {
+          load_block(nxt, row_ptr(tile_next, 0) + b_begin * kBB, row_ptr(tile_next, 1) + b_begin * kBB, tig);
         }
         compute_block(cur, xp + 64 * b, sx16 + 16 * b, tig, y0, y1);
         cur = nxt;
@@ -355,15 +383,38 @@ __global__ void __maxnreg__(128) gemv_m1_kernel(const uint8_t* __restrict__ W,
       red[warp * 16 + g + 8] = y1;
     }
     __syncthreads();
-    if (threadIdx.x < 16 * tpc) {
-      const int t = threadIdx.x >> 4, r = threadIdx.x & 15;
-      float acc = 0.f;
-      for (int w = 0; w < ks; ++w) acc += red[(t * ks + w) * 16 + r];
-      const int row = (tile0 + t) * 16 + r;
-      if (row < N) y[row] = acc;
+    if (!gu) {
+      if (threadIdx.x < 16 * tpc) {
+        const int t = threadIdx.x >> 4, r = threadIdx.x & 15;
+        float acc = 0.f;
+        for (int w = 0; w < ks; ++w) acc += red[(t * ks + w) * 16 + r];
+        const int row = (u * tpc + t) * 16 + r;
+        if (row < N) static_cast<float*>(P.y)[row] = acc;
+      }
+    } else if (threadIdx.x < 16) {
+      const int r = threadIdx.x;
+      float gs = 0.f, us = 0.f;
+      for (int w = 0; w < ks; ++w) {
+        gs += red[w * 16 + r];
+        us += red[(ks + w) * 16 + r];
+      }
+      const int row = u * 16 + r;
+      if (row < N) static_cast<__half*>(P.y)[row] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
     }
     __syncthreads();
   }
+}
+
+__global__ void __maxnreg__(128) gemv_batch_kernel(const __grid_constant__ GemvBatch B) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  int i = 0;
+  while (i + 1 < B.count && (int)blockIdx.x >= B.p[i + 1].cta_begin) ++i;
+  const GemvProb& P = B.p[i];
+  const int cta = (int)blockIdx.x - P.cta_begin;
+  if (P.qtype == kQ4K)
+    run_gemv_problem<kQ4K>(P, cta, smem);
+  else
+    run_gemv_problem<kQ6K>(P, cta, smem);
 }
 
 int g_sms = 0;
@@ -389,49 +440,89 @@ uint32_t gemv_take_status() {
   return v;
 }
 
-// Launch shape.  ks warps split the K/256 blocks of a 16-row tile (ks divides
-// the block count, ks <= 12); tpc tiles share a CTA when ks is small.  With up
-// to 128 registers a thread, an SM holds 512 threads, so a CTA of T threads
-// gets floor(512 / T) slots per SM.  Prefer the largest ks (shortest per-warp
-// chains, most loads in flight) whose CTAs all fit in one wave.
-struct GemvShape {
-  int ks, tpc, threads;
-  int64_t grid;
-};
-
-static GemvShape choose_shape(int64_t N, int nb) {
-  const int64_t tiles = (N + 15) / 16;
-  const int64_t sms = sm_count();
-  GemvShape best{1, 8, 256, 0};
-  for (int d = std::min(nb, 12); d >= 1; --d) {
-    if (nb % d) continue;
-    const int tpc = std::max(1, 4 / d);
-    const int threads = 32 * d * tpc;
-    const int64_t slots = sms * std::max(1, 512 / threads);
-    const int64_t ctas = (tiles + tpc - 1) / tpc;
-    if (ctas <= slots) return GemvShape{d, tpc, threads, ctas};
+// Launch one grouped GEMV.  ks = the largest of 8, 4, 2, 1 dividing the block
+// count (gate/up: at most 4, so a CTA holds one gate and one up tile).  CTAs:
+// two per SM (256 threads x 128 registers), split across problems in
+// proportion to their weight bytes.
+cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
+  GemvBatch B;
+  memset(&B, 0, sizeof(B));
+  B.count = count;
+  double total = 0;
+  int64_t bytes[kMaxGemvProbs];
+  size_t smem = 0;
+  for (int i = 0; i < count; ++i) {
+    GemvProb& P = B.p[i];
+    P.w0 = static_cast<const uint8_t*>(d[i].w0);
+    P.w1 = static_cast<const uint8_t*>(d[i].w1);
+    P.x = d[i].x;
+    P.y = d[i].y;
+    P.N = (int)d[i].N;
+    P.K = (int)d[i].K;
+    P.qtype = d[i].qtype;
+    P.kind = d[i].w1 ? 1 : 0;
+    const int nb = P.K / kQK;
+    int ks = 1;
+    for (int c = (P.kind ? 4 : 8); c >= 1; c /= 2)
+      if (nb % c == 0) {
+        ks = c;
+        break;
+      }
+    if (P.kind) {
+      if (nb % 4) return cudaErrorInvalidValue;  // gate/up needs one gate + one up tile per CTA
+      ks = 4;
+    }
+    P.ks = ks;
+    const int tpc = kGemvWarps / ks;
+    const int ntiles = (P.N + 15) / 16;
+    P.units = P.kind ? ntiles : (ntiles + tpc - 1) / tpc;
+    bytes[i] = (int64_t)P.N * nb * (P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes) * (P.kind ? 2 : 1);
+    total += (double)bytes[i];
+    smem = std::max(smem, (size_t)2 * P.K + (size_t)P.K / 4 + (size_t)kGemvWarps * 16 * sizeof(float));
   }
-  best.grid = std::min<int64_t>((tiles + best.tpc - 1) / best.tpc, sms * 2);
-  return best;
+  const int budget = std::max(count, sm_count() * 2);
+  int used = 0;
+  for (int i = 0; i < count; ++i) {
+    int c = (int)((double)budget * (double)bytes[i] / total);
+    c = std::max(1, std::min(c, B.p[i].units));
+    B.p[i].ctas = c;
+    used += c;
+  }
+  // Hand leftover CTAs to the problems with the most units per CTA.
+  for (bool again = true; again && used < budget;) {
+    again = false;
+    int best = -1;
+    double best_load = 1.0;
+    for (int i = 0; i < count; ++i) {
+      const double load = (double)B.p[i].units / B.p[i].ctas;
+      if (B.p[i].ctas < B.p[i].units && load > best_load) {
+        best_load = load;
+        best = i;
+      }
+    }
+    if (best >= 0) {
+      ++B.p[best].ctas;
+      ++used;
+      again = true;
+    }
+  }
+  int begin = 0;
+  for (int i = 0; i < count; ++i) {
+    B.p[i].cta_begin = begin;
+    begin += B.p[i].ctas;
+  }
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  gemv_batch_kernel<<<begin, 32 * kGemvWarps, smem, s>>>(B);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gemv(QType t, const void* W, const uint16_t* x, float* y, int64_t N, int64_t K,
                         cudaStream_t s) {
-  const int nb = (int)(K / kQK);
-  const GemvShape sh = choose_shape(N, nb);
-  const size_t smem = (size_t)2 * K + (size_t)K / 4 + (size_t)sh.tpc * sh.ks * 16 * sizeof(float);
-  if (t == kQ4K) {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(gemv_m1_kernel<kQ4K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    gemv_m1_kernel<kQ4K><<<(int)sh.grid, sh.threads, smem, s>>>(static_cast<const uint8_t*>(W), x, y, (int)N, (int)K,
-                                                                sh.ks, sh.tpc);
-  } else {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(gemv_m1_kernel<kQ6K>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    gemv_m1_kernel<kQ6K><<<(int)sh.grid, sh.threads, smem, s>>>(static_cast<const uint8_t*>(W), x, y, (int)N, (int)K,
-                                                                sh.ks, sh.tpc);
-  }
-  return cudaGetLastError();
+  GemvDesc d{t, W, nullptr, x, y, N, K};
+  return launch_gemv_batch(&d, 1, s);
 }
 
 }  // namespace qk

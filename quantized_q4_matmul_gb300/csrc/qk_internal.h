@@ -33,4 +33,17 @@ cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t
 // Largest M the decode GEMV handles; larger M goes to the tensor-core GEMM.
 int gemv_max_m();
 
+// One M = 1 problem of a grouped decode GEMV launch.  w1 != null makes it the
+// fused gate/up + SwiGLU problem (w0 = gate, w1 = up, y fp16), else y is fp32.
+constexpr int kMaxGemvProbs = 8;
+struct GemvDesc {
+  QType qtype;
+  const void* w0;
+  const void* w1;
+  const uint16_t* x;
+  void* y;
+  int64_t N, K;
+};
+cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s);
+
 }  // namespace qk

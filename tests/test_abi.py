@@ -79,3 +79,19 @@ def test_binding_raises_with_the_status(qk_lib):
     with pytest.raises(qk_lib.QKError) as e:
         qk_lib.qk_matmul_q4k(A16, A16, A16, 4, 8, 300, stream=0)
     assert e.value.status == -3
+
+
+def test_batch_rejects_bad_arguments_on_the_host(qk_lib):
+    L = qk_lib.lib()
+    D = qk_lib.qk_matmul_desc
+    assert L.qk_matmul_batch(None, 0, None) == 0
+    assert L.qk_matmul_batch(None, 2, None) == -1
+    assert L.qk_matmul_batch(None, -1, None) == -3
+    arr = (D * 2)(D(0, A16, None, A16, A16, 1, 8, 256), D(7, A16, None, A16, A16, 1, 8, 256))
+    assert L.qk_matmul_batch(arr, 2, None) == -3                       # unknown qtype
+    arr = (D * 1)(D(1, A16, A16, A16, A16, 1, 8, 256))
+    assert L.qk_matmul_batch(arr, 1, None) == -3                       # gate/up must be Q4_K
+    arr = (D * 1)(D(0, A16, None, A16, A8, 1, 8, 256))
+    assert L.qk_matmul_batch(arr, 1, None) == -2
+    arr = (D * 1)(D(0, A16, None, A16, A16, 1, 8, 300))
+    assert L.qk_matmul_batch(arr, 1, None) == -3

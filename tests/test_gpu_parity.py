@@ -250,3 +250,84 @@ def test_alias_and_host_pointer_rejected(qk_lib, cuda):
     assert L.qk_matmul_q4k(hp, x.data_ptr(), y.data_ptr(), 4, 128, 256, s) == -8  # pageable host memory
     assert L.qk_matmul_q4k(W.data_ptr(), x.data_ptr(), y.data_ptr(), 4, 128, 256, s) == 0
     assert L.qk_get_device_status(s) == 0
+
+
+# ---------------------------------------------------------------------------
+# Grouped calls
+# ---------------------------------------------------------------------------
+def test_batch_decode_layer_matches_single_calls(qk_lib, cuda):
+    """The seven M = 1 linears of a layer in one grouped launch: bit-identical to
+    the single-problem calls, and within the bar of the oracle."""
+    import torch
+    probs, singles, refs = [], [], []
+    for tag, lin, M in synth.workloads()["decode_layer_m1"].linears:
+        rng = synth.rng_for(11, tag)
+        W = synth.weights(rng, lin.qtype, lin.N, lin.K)
+        x = synth.activations(rng, M, lin.K)
+        Wd, xd = _dev(W, cuda), _x_dev(x, cuda)
+        y = torch.full((M, lin.N), float("nan"), device=cuda)
+        probs.append(dict(qtype=lin.qtype, blocks=Wd, x_f16=xd, y=y, M=M, N=lin.N, K=lin.K))
+        refs.append(oracle.matmul(QT[lin.qtype], W, x, lin.N, lin.K))
+        singles.append(gpu_matmul(qk_lib, lin.qtype, W, x, lin.N, lin.K, cuda))
+    qk_lib.qk_matmul_batch(probs)
+    qk_lib.qk_get_device_status()
+    for p, ref, single in zip(probs, refs, singles):
+        got = p["y"].cpu().numpy().astype(np.float64)
+        assert np.array_equal(got, single)
+        check_close(got, ref, "batch N%d K%d" % (p["N"], p["K"]))
+
+
+def test_batch_mixed_and_gateup(qk_lib, cuda):
+    """M = 1 gate/up + SwiGLU, an M > 1 problem, an empty problem and >8 GEMVs in one call."""
+    import torch
+    rng = synth.rng_for(12, 0)
+    K, N = 1024, 256
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    x1 = synth.activations(rng, 1, K)
+    yg = torch.empty(1, N, dtype=torch.float16, device=cuda)
+    probs = [dict(qtype="q4k", blocks=_dev(Wg, cuda), up_blocks=_dev(Wu, cuda), x_f16=_x_dev(x1, cuda), y=yg, M=1,
+                  N=N, K=K)]
+    x40 = synth.activations(rng, 40, K)
+    W6 = synth.q6k_weights(rng, 200, K)
+    y40 = torch.empty(40, 200, device=cuda)
+    probs.append(dict(qtype="q6k", blocks=_dev(W6, cuda), x_f16=_x_dev(x40, cuda), y=y40, M=40, N=200, K=K))
+    probs.append(dict(qtype="q4k", blocks=_dev(Wg, cuda), x_f16=_x_dev(x1, cuda), y=torch.empty(1, 0, device=cuda),
+                      M=1, N=0, K=K))
+    smalls = []
+    for i in range(9):
+        W = synth.weights(rng, "q4k" if i % 2 else "q6k", 48 + 16 * i, K)
+        x = synth.activations(rng, 1, K)
+        y = torch.empty(1, W.shape[0], device=cuda)
+        smalls.append((W, x, y, "q4k" if i % 2 else "q6k"))
+        probs.append(dict(qtype=smalls[-1][3], blocks=_dev(W, cuda), x_f16=_x_dev(x, cuda), y=y, M=1, N=W.shape[0],
+                          K=K))
+    qk_lib.qk_matmul_batch(probs)
+    qk_lib.qk_get_device_status()
+    check_close_f16out(yg.float().cpu().numpy().astype(np.float64), oracle.gateup_swiglu(Wg, Wu, x1, N, K), "gu M1")
+    check_close(y40.cpu().numpy().astype(np.float64), oracle.matmul(oracle.Q6K, W6, x40, 200, K), "q6k M40")
+    for W, x, y, qt in smalls:
+        check_close(y.cpu().numpy().astype(np.float64), oracle.matmul(QT[qt], W, x, W.shape[0], K), "small")
+
+
+def test_batch_alias_between_entries_rejected(qk_lib, cuda):
+    import torch
+    W = torch.zeros(128 * 144, dtype=torch.uint8, device=cuda)
+    x = torch.zeros(256, dtype=torch.float16, device=cuda)
+    y = torch.zeros(128, dtype=torch.float32, device=cuda)
+    p = dict(qtype="q4k", blocks=W, x_f16=x, y=y, M=1, N=128, K=256)
+    with pytest.raises(qk_lib.QKError) as e:
+        qk_lib.qk_matmul_batch([p, dict(p)])  # two entries write the same y
+    assert e.value.status == -7
+
+
+def test_gateup_decode_m1(qk_lib, cuda):
+    """qk_gateup_swiglu_q4k at M = 1 (the grouped-GEMV gate/up path) at full size."""
+    import torch
+    rng = synth.rng_for(13, 0)
+    N, K = 8192, 3072
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, 1, K)
+    y = torch.empty(1, N, dtype=torch.float16, device=cuda)
+    qk_lib.qk_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), y, 1, N, K)
+    qk_lib.qk_get_device_status()
+    check_close_f16out(y.float().cpu().numpy().astype(np.float64), oracle.gateup_swiglu(Wg, Wu, x, N, K), "gu M1")
