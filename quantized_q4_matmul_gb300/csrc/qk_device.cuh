@@ -222,6 +222,18 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// The same for the 64-byte-swizzle canonical layout: rows of 32 fp16 (64 B),
+// 8-row atoms of 512 B stacked at 512 B.
+__device__ __forceinline__ uint64_t umma_desc_sw64(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1u << 16;                         // leading byte offset (unused for swizzled K-major)
+  d |= (uint64_t)(512u >> 4) << 32;                // stride byte offset: next 8-row atom
+  d |= (uint64_t)1u << 46;                         // descriptor version (tcgen05)
+  d |= (uint64_t)4u << 61;                         // swizzle mode: 64 B
+  return d;
+}
+
 // Instruction descriptor, kind::f16: A = B = fp16, D = fp32, both K-major.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(uint32_t M, uint32_t N) {
   return (1u << 4)                // D format: fp32
