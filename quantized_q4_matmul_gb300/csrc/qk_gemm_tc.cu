@@ -41,10 +41,9 @@ __device__ uint32_t g_gemm_status = 0;
 namespace {
 
 constexpr int kBM = 128;               // weight rows per tile (UMMA M)
-constexpr int kBK = 32;                // K per step: one 64-byte swizzle row of fp16 (one Q4_K sub-block)
+constexpr int kBK = 64;                // K per step: one 128-byte swizzle row of fp16
 constexpr int kMaxBN = 256;            // tokens per tile (UMMA N), multiple of 16
-constexpr int kAStageBytes = kBM * kBK * 2;     // 8 KB
-constexpr int kStepsPerBlock = kQK / kBK;       // 8
+constexpr int kAStageBytes = kBM * kBK * 2;     // 16 KB
 constexpr uint32_t kH2Magic = 0x64646464u;
 
 template <int QT, bool GATEUP>
@@ -54,9 +53,9 @@ struct Cfg {
   static constexpr int kDqWarps = GATEUP ? 16 : 8;
   static constexpr int kThreads = 64 + 32 * kDqWarps;
   static constexpr int kNumB = GATEUP ? 2 : 1;  // weight tensors per tile
-  // Every K step is written in full by the 128 threads of one `part` for each
-  // weight tensor.
-  static constexpr int kAArrivals = 128 * kNumB;
+  // Arrivals that complete an A stage: Q4_K threads each write half of every
+  // step; Q6_K threads write two of every four steps in full.
+  static constexpr int kAArrivals = QT == kQ4K ? 32 * kDqWarps : 32 * kDqWarps / 2;
   static constexpr int kPStages = 2;
   static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : 8 * 4096;  // one tensor, one stage
   static constexpr int kPBytes = kPStages * kNumB * kPSlotBytes;
@@ -111,12 +110,9 @@ __device__ __forceinline__ uint32_t h2_bits(__half2 v) { return *reinterpret_cas
 
 __device__ __forceinline__ __half2 bits_h2(uint32_t v) { return *reinterpret_cast<__half2*>(&v); }
 
-// Offset of 16-byte chunk j (k = 8j .. 8j+7, j = 0..3) of row r in a 128 x 32
-// fp16 tile stored in the UMMA 64-byte-swizzle K-major layout (rows of 64 B,
-// 8-row atoms of 512 B, chunk index XOR-ed with bits 1..2 of the row).
-__device__ __forceinline__ uint32_t sw64_off(int r, int j) {
-  return (uint32_t)(r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
-}
+// Offset of 16-byte chunk j (k = 8j .. 8j+7) of row r in a 128 x 64 fp16 tile
+// stored in the UMMA 128-byte-swizzle K-major layout.
+__device__ __forceinline__ uint32_t sw128_off(int r, int j) { return (uint32_t)(r * 128 + ((j ^ (r & 7)) << 4)); }
 
 // Four weights from four quant bytes (each < 16) of `b4`: the byte goes into
 // the mantissa of 1024.0 (exact fp16 1024 + q), 1024 is subtracted exactly,
@@ -171,14 +167,14 @@ __device__ __forceinline__ void q4_kstep_regs(const uint8_t* rowp, int c, int pa
   }
 }
 
-// The same 32 weights (one K step) written into row rr of a swizzled
-// shared-memory A tile.
+// The same 32 weights written into row rr of a swizzled shared-memory A tile.
 __device__ __forceinline__ void q4_kstep(const uint8_t* rowp, int c, int part, uint8_t* a_tile, int rr) {
   uint32_t r[16];
   q4_kstep_regs(rowp, c, part, r);
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    *reinterpret_cast<uint4*>(a_tile + sw64_off(rr, j)) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+    *reinterpret_cast<uint4*>(a_tile + sw128_off(rr, 4 * part + j)) =
+        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
 }
 
 // Q6_K.  The block of a row sits in its smem slot at byte offset MIS (even,
@@ -205,11 +201,11 @@ __device__ __forceinline__ void lds_vecs(const uint8_t* p, uint32_t (&v)[4 * NV]
   }
 }
 
-// Dequantize weights 128h .. 128h+127 of a Q6_K block (side 0: low nibbles of
-// ql bytes 64h..64h+63, side 1: their high nibbles; high bits from qh bytes
-// 128+32h..+31) into row r of the four A tiles of K steps 4h .. 4h+3.
+// Dequantize K steps 2h (side 0: low nibbles) and 2h+1 (side 1: high nibbles)
+// of a Q6_K block (both read ql bytes 64h..64h+63 and qh bytes 128+32h..+31)
+// into row r of two A tiles.
 template <int MIS>
-__device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* const (&tiles)[4], int r) {
+__device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* a_tile0, uint8_t* a_tile1, int r) {
   uint32_t vl[20], vh[12], vs[8];
   lds_vecs<5>(slot + 64 * h, vl);         // bytes 64h .. 64h+79
   lds_vecs<3>(slot + 128 + 32 * h, vh);   // bytes 128+32h .. +47
@@ -226,9 +222,9 @@ __device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* con
   const __half2 k1056 = __float2half2_rn(1056.0f);  // 1024 + 32
 #pragma unroll
   for (int side = 0; side < 2; ++side) {
+    uint8_t* a_tile = side ? a_tile1 : a_tile0;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      uint8_t* a_tile = tiles[2 * side + (j >> 2)];  // chunk j: step-local k = 8j .. 8j+7
+    for (int j = 0; j < 8; ++j) {  // chunk j: step-local k = 8j .. 8j+7
       const int g = 2 * side + (j >> 2);     // 32-weight group within the half
       const int sidx = 4 * side + (j >> 1);  // 16-weight scale group within the half
       const uint32_t scw = sidx < 4 ? scw0 : scw1;
@@ -248,22 +244,22 @@ __device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* con
         o[2 * ww] = h2_bits(__hmul2(p0, dsc2));
         o[2 * ww + 1] = h2_bits(__hmul2(p1, dsc2));
       }
-      *reinterpret_cast<uint4*>(a_tile + sw64_off(r, j & 3)) = make_uint4(o[0], o[1], o[2], o[3]);
+      *reinterpret_cast<uint4*>(a_tile + sw128_off(r, j)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
 }
 
-__device__ __forceinline__ void q6_half_dispatch(int mis, const uint8_t* slot, int h, uint8_t* const (&t)[4],
+__device__ __forceinline__ void q6_half_dispatch(int mis, const uint8_t* slot, int h, uint8_t* t0, uint8_t* t1,
                                                  int r) {
   switch (mis) {
-    case 0: q6_half<0>(slot, h, t, r); break;
-    case 2: q6_half<2>(slot, h, t, r); break;
-    case 4: q6_half<4>(slot, h, t, r); break;
-    case 6: q6_half<6>(slot, h, t, r); break;
-    case 8: q6_half<8>(slot, h, t, r); break;
-    case 10: q6_half<10>(slot, h, t, r); break;
-    case 12: q6_half<12>(slot, h, t, r); break;
-    default: q6_half<14>(slot, h, t, r); break;
+    case 0: q6_half<0>(slot, h, t0, t1, r); break;
+    case 2: q6_half<2>(slot, h, t0, t1, r); break;
+    case 4: q6_half<4>(slot, h, t0, t1, r); break;
+    case 6: q6_half<6>(slot, h, t0, t1, r); break;
+    case 8: q6_half<8>(slot, h, t0, t1, r); break;
+    case 10: q6_half<10>(slot, h, t0, t1, r); break;
+    case 12: q6_half<12>(slot, h, t0, t1, r); break;
+    default: q6_half<14>(slot, h, t0, t1, r); break;
   }
 }
 
@@ -312,7 +308,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   const int n0 = blockIdx.x * kBM;
   const int m0 = blockIdx.y * p.BN;
   const int nb = p.K / kQK;
-  const int nsteps = nb * kStepsPerBlock;
+  const int nsteps = nb * 4;
   const int BN = p.BN;
   const uint32_t x_bytes = (uint32_t)BN * kBK * 2;
   constexpr int kPSlotBytes = C::kPSlotBytes;
@@ -331,10 +327,10 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  // Accumulators: kNumB x BN columns; with AT also S x kNumB A tiles of 16
-  // columns (128 rows x 32 fp16) after them.
+  // Accumulators: kNumB x BN columns; with AT also S x kNumB A tiles of 32
+  // columns (128 rows x 64 fp16) after them.
   const uint32_t a_col0 = (uint32_t)(C::kNumB * BN);
-  const uint32_t need_cols = a_col0 + (AT ? (uint32_t)(S * C::kNumB * (kBK / 2)) : 0u);
+  const uint32_t need_cols = a_col0 + (AT ? (uint32_t)(S * C::kNumB * 32) : 0u);
   const uint32_t tmem_cols = need_cols <= 32 ? 32 : need_cols <= 64 ? 64 : need_cols <= 128 ? 128
                              : need_cols <= 256 ? 256 : 512;
   if (warp == 1) {
@@ -410,7 +406,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           mbar_arrive(&bars->p_full[ps]);
         }
       }
-      for (int c = 0; c < kStepsPerBlock && ok; ++c, ++step) {
+      for (int c = 0; c < 4 && ok; ++c, ++step) {
         const int s = step % S;
         const uint32_t ph = (uint32_t)(step / S) & 1u;
         ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
@@ -443,21 +439,21 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       tc_fence_after();
       if (lane == 0) {
         const uint32_t xa = smem_u32(smem + L.x_off + s * L.x_stage);
-        const uint64_t bdesc = umma_desc_sw64(xa);
+        const uint64_t bdesc = umma_desc_sw128(xa);
 #pragma unroll
         for (int t = 0; t < C::kNumB; ++t) {
           if constexpr (AT) {
-            const uint32_t a_tm = tmem + a_col0 + (uint32_t)((s * C::kNumB + t) * (kBK / 2));
+            const uint32_t a_tm = tmem + a_col0 + (uint32_t)((s * C::kNumB + t) * 32);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)  // 16-wide K slice = 8 TMEM columns of A
               umma_f16_ts(tmem + (uint32_t)(t * BN), a_tm + (uint32_t)(8 * kk), bdesc + (uint64_t)(2 * kk), idesc,
                           (step > 0 || kk > 0) ? 1u : 0u);
           } else {
             const uint32_t aa = smem_u32(smem + L.a_off + (s * C::kNumB + t) * kAStageBytes);
-            const uint64_t adesc = umma_desc_sw64(aa);
+            const uint64_t adesc = umma_desc_sw128(aa);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk) {
-              // +32 bytes per 16-wide K slice inside the 64-byte swizzle row (start address in 16 B units)
+              // +32 bytes per 16-wide K slice inside the swizzle atom (start address in 16 B units)
               umma_f16_ss(tmem + (uint32_t)(t * BN), adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
                           (step > 0 || kk > 0) ? 1u : 0u);
             }
@@ -494,12 +490,10 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       if (!ok) break;
       const uint8_t* pst = smem + L.p_off + (ps * C::kNumB + which) * kPSlotBytes;
       if constexpr (QT == kQ4K) {
-        // part p writes the K steps 8kb + 2c + p (sub-block 2c + p), c = 0..3.
         const uint8_t* rowp = pst + rho * kQ4KBytes;
-        for (int c = 0; c < 4; ++c) {
-          const int st = step + 2 * c + part;
-          const int s = st % S;
-          const uint32_t ph = (uint32_t)(st / S) & 1u;
+        for (int c = 0; c < 4; ++c, ++step) {
+          const int s = step % S;
+          const uint32_t ph = (uint32_t)(step / S) & 1u;
           if constexpr (AT) {
             uint32_t r[16];
             q4_kstep_regs(rowp, c, part, r);  // overlaps the wait below
@@ -507,7 +501,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
             ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
             if (!ok) break;
             tc_fence_after();
-            tmem_st16(a_lane + a_col0 + (uint32_t)((s * C::kNumB + which) * (kBK / 2)), r);
+            tmem_st16(a_lane + a_col0 + (uint32_t)((s * C::kNumB + which) * 32 + 16 * part), r);
             tmem_wait_st();
             tc_fence_before();
           } else {
@@ -519,27 +513,25 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           }
           mbar_arrive(&bars->a_full[s]);
         }
-        step += kStepsPerBlock;
       } else {
-        // part h writes the K steps 8kb + 4h .. 8kb + 4h + 3 (weights 128h ..).
+        // part h writes K steps 4kb + 2h and 4kb + 2h + 1.
         const int n = min(n0 + rho, p.N - 1);
         const int mis = (int)(((int64_t)n * RB + (int64_t)kb * kQ6KBytes) & 15);
         const uint8_t* slot = pst + q6_slot(rho, p.q6_group);
         const int h = part;
-        uint8_t* tiles[4];
-        int sidx[4];
-        for (int i = 0; i < 4 && ok; ++i) {
-          const int st = step + 4 * h + i;
-          sidx[i] = st % S;
-          ok = mbar_wait(&bars->s_empty[sidx[i]], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemm_status);
-          tiles[i] = smem + L.a_off + (sidx[i] * C::kNumB + which) * kAStageBytes;
-        }
+        const int st0 = step + 2 * h, st1 = st0 + 1;
+        const int s0 = st0 % S, s1 = st1 % S;
+        ok = mbar_wait(&bars->s_empty[s0], ((uint32_t)(st0 / S) & 1u) ^ 1u, abort_flag, &g_gemm_status) &&
+             mbar_wait(&bars->s_empty[s1], ((uint32_t)(st1 / S) & 1u) ^ 1u, abort_flag, &g_gemm_status);
         if (ok) {
-          q6_half_dispatch(mis, slot, h, tiles, rho);
+          uint8_t* t0 = smem + L.a_off + (s0 * C::kNumB + which) * kAStageBytes;
+          uint8_t* t1 = smem + L.a_off + (s1 * C::kNumB + which) * kAStageBytes;
+          q6_half_dispatch(mis, slot, h, t0, t1, rho);
           fence_proxy_async_smem();
-          for (int i = 0; i < 4; ++i) mbar_arrive(&bars->a_full[sidx[i]]);
+          mbar_arrive(&bars->a_full[s0]);
+          mbar_arrive(&bars->a_full[s1]);
         }
-        step += kStepsPerBlock;
+        step += 4;
       }
       if (ok) mbar_arrive(&bars->p_empty[ps]);
     }
@@ -629,7 +621,7 @@ bool make_tmap_x(CUtensorMap* tm, const void* x, int64_t M, int64_t K, int BN) {
   const cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)BN};
   const cuuint32_t estr[2] = {1, 1};
   return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -739,11 +731,9 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   // As many K-step stages as fit in shared memory (2 .. 8).
   int S = C::kMaxStages;
   while (S > 2 && (make_layout<QT, GATEUP, AT>(BN, S).total > (uint32_t)kSmemLimit ||
-                   (AT && C::kNumB * BN + S * C::kNumB * (kBK / 2) > 512)))
+                   (AT && C::kNumB * BN + S * C::kNumB * 32 > 512)))
     --S;
-  if (AT && C::kNumB * BN + S * C::kNumB * (kBK / 2) > 512) return cudaErrorInvalidConfiguration;
-  // A Q6_K dequant thread fills four K steps at once: fewer stages would deadlock.
-  if (QT == kQ6K && S < 4) return cudaErrorInvalidConfiguration;
+  if (AT && C::kNumB * BN + S * C::kNumB * 32 > 512) return cudaErrorInvalidConfiguration;
   p.stages = S;
   const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, S).total;
   if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;

@@ -6,37 +6,30 @@
 // "[04] one decode step"; "Building DAMASCUS", "Prefill and decode need
 // different performance questions".
 //
-// The kernel is HBM-bound: every packed weight byte is read once, by TMA, into
-// shared memory, and the arithmetic stays well under the bandwidth budget:
+// The kernel is HBM-bound: every packed weight byte is read once.  To keep
+// the arithmetic well under the bandwidth budget the inner products run on
+// the warp-level tensor instruction mma.sync m16n8k16 (fp16 x fp16, fp32
+// accumulate) used as a dot-product engine, with the block scales applied
+// after each sub-block instead of per weight:
 //
-//   * a warp owns whole 16-row tiles and streams their K slices through a
-//     private two-stage shared-memory pipeline filled by tensor-map TMA loads
-//     (Q4_K: one box of 16 rows x 2 blocks; Q6_K: one box per residue of a
-//     group of g rows whose byte stride is 16-aligned, like the prefill GEMM),
-//     so each weight byte crosses the memory system once, in full sectors;
-//   * the inner products use the warp tensor instruction mma.sync m16n8k16
-//     (fp16 x fp16, fp32 accumulate) as a dot-product engine: a 4-bit quant
-//     OR-ed into the mantissa of fp16 1024.0 is the exact value 1024 + F*q (F =
-//     1 or 16 by nibble position, no shifts), its product with an fp16
-//     activation is exact and the sum fp32;
+//   * a warp owns 16 weight rows (lane g = lane/4 holds rows g and g+8);
+//   * each 4-bit quant q becomes the fp16 value 1024 + F*q by OR-ing the
+//     nibble into the mantissa of 1024.0 (F = 1 or 16 depending on where the
+//     nibble sits, no shifts needed); the product with an fp16 activation is
+//     exact and the sum is fp32;
 //   * x is replicated across the 8 MMA columns, so every lane holds the sum
 //     D = 1024*Sx + F*sum(q*x) of its two rows for the current sub-block, and
-//     sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + dmin*m) (Q4_K) or
-//     (d*sc/F)*D - Sx*(1024*d*sc/F + 32*d*sc) (Q6_K), Sx being the sum of the
-//     sub-block's activations, staged once per CTA with a k-permuted fp16 x;
-//   * lane tig applies the scales of a quarter of the sub-blocks; the two
-//     partial sums of a row meet in two shuffles (deterministic).
-// Q6_K blocks are 210 bytes, so every other block is 2 mod 4 bytes into its
-// window: its words come from two aligned shared-memory loads and a funnel
-// shift.  Shared-memory row pitches (288 B, 432 B) and the Q6_K row order
-// (MMA row r <-> weight row 2r or 2r+1 for g = 2) make the fragment reads of
-// a warp bank-conflict free.
+//     the block math gives  sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + dmin*m)
+//     (Q4_K) or (d*sc/F)*D - Sx*(1024*d*sc/F + 32*d*sc) (Q6_K), Sx being the
+//     sum of the sub-block's activations (computed once per CTA);
+//   * lane tig applies the scales of a quarter of the sub-blocks, so no scale
+//     is decoded twice; partial sums meet in two shuffles and one fixed-order
+//     pass over the warps that split K.  The result is deterministic.
 //
-// One launch runs up to kMaxGemvProbs independent problems (qk_matmul_batch):
-// each owns a contiguous range of CTAs sized by its share of the weight
-// bytes.  Problem kind 1 is the fused gate/up + SwiGLU: a warp streams the gate
-// rows then the up rows of its tile and writes fp16(silu(g) * u).
-#include <cuda.h>
+// Packed rows are read with 8-byte (Q4_K) or 4-byte (Q6_K) loads that each
+// cover whole 32-byte sectors across the warp.  Q6_K blocks are 210 bytes and
+// therefore only 2-byte aligned; their words are assembled from two aligned
+// loads and a funnel shift.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -55,17 +48,12 @@ namespace {
 constexpr uint32_t kMagic = 0x64006400u;  // fp16x2 (1024.0, 1024.0)
 
 struct GemvProb {
-  CUtensorMap tm[2];  // weights (gate for kind 1), up weights (kind 1)
-  const uint8_t* w[2];
+  const uint8_t* w0;  // weights (gate for kind 1)
+  const uint8_t* w1;  // up weights (kind 1), else null
   const uint16_t* x;
   void* y;
   int N, K, qtype, kind;
-  int g;          // Q6_K: weight rows per tensor-map row (1 for Q4_K)
-  int rows_tma;   // rows covered by the tensor map; rows past it are copied by hand
-  int pitch;      // shared-memory bytes per row slot (the box width)
-  int region;     // shared-memory bytes per residue region (128-byte aligned)
-  int stage;      // shared-memory bytes per pipeline stage
-  int tiles, cta_begin, ctas;
+  int ks, units, cta_begin, ctas;
 };
 
 struct GemvBatch {
@@ -84,6 +72,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 
 __device__ __forceinline__ float half_lo(uint32_t v) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+}
+
+// 4-byte little-endian load from a 2-byte-aligned address inside the buffer.
+__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+  const uint32_t odd = (uint32_t)(a >> 1) & 1u;
+  const uint32_t lo = __ldg(w);
+  const uint32_t hi = __ldg(w + odd);  // same word when aligned: never reads past the block
+  return __funnelshift_r(lo, hi, 16u * odd);
 }
 
 __device__ __forceinline__ float pick4(const float (&v)[4], int i) {
@@ -167,15 +165,13 @@ struct BlockRegs<kQ4K> {
   uint2 q0[4], q1[4];  // quant bytes 32G + 8tig .. +7, G = 0..3
 };
 
-// Block registers from shared memory: blk0 / blk1 = the block of the lane's
-// two rows inside their stage slots (16-byte aligned for Q4_K).
 __device__ __forceinline__ void load_block(BlockRegs<kQ4K>& r, const uint8_t* blk0, const uint8_t* blk1, int tig) {
-  r.h0 = *reinterpret_cast<const uint4*>(blk0);
-  r.h1 = *reinterpret_cast<const uint4*>(blk1);
+  r.h0 = __ldg(reinterpret_cast<const uint4*>(blk0));
+  r.h1 = __ldg(reinterpret_cast<const uint4*>(blk1));
 #pragma unroll
   for (int G = 0; G < 4; ++G) {
-    r.q0[G] = *reinterpret_cast<const uint2*>(blk0 + 16 + 32 * G + 8 * tig);
-    r.q1[G] = *reinterpret_cast<const uint2*>(blk1 + 16 + 32 * G + 8 * tig);
+    r.q0[G] = ldg_stream8(blk0 + 16 + 32 * G + 8 * tig);
+    r.q1[G] = ldg_stream8(blk1 + 16 + 32 * G + 8 * tig);
   }
 }
 
@@ -246,37 +242,29 @@ struct BlockRegs<kQ6K> {
   uint32_t d;                               // fp16 d of row g (low half) and row g+8 (high half)
 };
 
-// 4-byte word at a 2-byte-aligned shared-memory address.
-__device__ __forceinline__ uint32_t lds_u32_a2(const uint8_t* p) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-  const uint32_t odd = (uint32_t)(a >> 1) & 1u;
-  return __funnelshift_r(w[0], w[odd], 16u * odd);
-}
-
 __device__ __forceinline__ void load_block(BlockRegs<kQ6K>& r, const uint8_t* blk0, const uint8_t* blk1, int tig) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {  // i = 4h + 2p + s: byte 64h + 32p + 16s + 4tig
     const int off = 64 * (i >> 2) + 32 * ((i >> 1) & 1) + 16 * (i & 1) + 4 * tig;
-    r.ql0[i] = lds_u32_a2(blk0 + off);
-    r.ql1[i] = lds_u32_a2(blk1 + off);
+    r.ql0[i] = ld_u32_a2(blk0 + off);
+    r.ql1[i] = ld_u32_a2(blk1 + off);
   }
 #pragma unroll
   for (int i = 0; i < 4; ++i) {  // i = 2h + s: byte 128 + 32h + 16s + 4tig
     const int off = 128 + 32 * (i >> 1) + 16 * (i & 1) + 4 * tig;
-    r.qh0[i] = lds_u32_a2(blk0 + off);
-    r.qh1[i] = lds_u32_a2(blk1 + off);
+    r.qh0[i] = ld_u32_a2(blk0 + off);
+    r.qh1[i] = ld_u32_a2(blk1 + off);
   }
   uint32_t s0 = 0, s1 = 0;
 #pragma unroll
   for (int u = 0; u < 4; ++u) {
-    s0 |= (uint32_t)blk0[192 + 4 * u + tig] << (8 * u);
-    s1 |= (uint32_t)blk1[192 + 4 * u + tig] << (8 * u);
+    s0 |= (uint32_t)__ldg(blk0 + 192 + 4 * u + tig) << (8 * u);
+    s1 |= (uint32_t)__ldg(blk1 + 192 + 4 * u + tig) << (8 * u);
   }
   r.sc0 = s0;
   r.sc1 = s1;
-  r.d = (uint32_t)*reinterpret_cast<const uint16_t*>(blk0 + 208) |
-        ((uint32_t)*reinterpret_cast<const uint16_t*>(blk1 + 208) << 16);
+  r.d = (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(blk0 + 208)) |
+        ((uint32_t)__ldg(reinterpret_cast<const uint16_t*>(blk1 + 208)) << 16);
 }
 
 __device__ __forceinline__ void compute_block(const BlockRegs<kQ6K>& r, const uint2* xpb, const float* sxb, int tig,
@@ -316,179 +304,117 @@ __device__ __forceinline__ void compute_block(const BlockRegs<kQ6K>& r, const ui
 }
 
 // ---------------------------------------------------------------------------
-// The kernel.
+// The grouped kernel.  One launch runs up to kMaxGemvProbs independent M = 1
+// problems (e.g. the seven linears of a decoder layer).  Each problem owns a
+// contiguous range of CTAs, sized by its share of the total weight bytes, so
+// every CTA stages one x and the whole launch finishes together.  A CTA has 8
+// warps: `ks` warps split the K blocks of a 16-row tile and `tpc` = 8 / ks
+// tiles are processed side by side; the CTA walks its contiguous range of
+// such units, every warp loading the next block (or the next unit's first
+// block) while it computes the current one.  Partial sums of the ks warps of
+// a tile meet in shared memory in a fixed order (deterministic).
+//
+// Problem kind 1 is the fused gate/up + SwiGLU: sub-tile 0 holds rows of the
+// gate weights, sub-tile 1 the same rows of the up weights, and the epilogue
+// writes fp16(silu(g) * u).
 // ---------------------------------------------------------------------------
 constexpr int kGemvWarps = 8;
-constexpr int kSliceBlocks = 2;  // K blocks per pipeline stage
-
-struct GemvShared {
-  uint64_t full[kGemvWarps][2];
-  uint32_t abort_flag;
-};
-
-// Weight row held by MMA row r (0..15) of a tile: identity, except for Q6_K
-// with g = 2, where MMA rows 0..7 take the even rows and 8..15 the odd rows so
-// the eight rows read by one instruction sit in one residue region.
-__device__ __forceinline__ int tile_row(int r, int g) { return g == 2 ? 2 * (r & 7) + (r >> 3) : r; }
-
-// Shared-memory slot of tile row rho (0..15) inside a stage.
-__device__ __forceinline__ uint32_t row_slot(const GemvProb& P, int rho) {
-  return (uint32_t)(rho % P.g) * (uint32_t)P.region + (uint32_t)(rho / P.g) * (uint32_t)P.pitch;
-}
-
-// Byte offset of block b0 of tile row rho inside its slot (the misalignment of
-// the box start: 0 for Q4_K, (n * row_bytes + 210 * b0) mod 16 for Q6_K).
-template <int QT>
-__device__ __forceinline__ int slot_mis(int64_t RB, int n, int b0) {
-  if constexpr (QT == kQ4K) return 0;
-  return (int)(((int64_t)n * RB + (int64_t)b0 * kQ6KBytes) & 15);
-}
 
 template <int QT>
-__device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uint8_t* smem, uint8_t* stages,
-                                                 GemvShared* sh) {
-  const int K = P.K, N = P.N, nb = K / kQK;
-  const uint2* xp = reinterpret_cast<const uint2*>(smem);
-  const float* sx16 = reinterpret_cast<const float*>(smem + 2 * K);
+__device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uint8_t* smem) {
+  const int K = P.K, N = P.N, ks = P.ks, tpc = kGemvWarps / P.ks;
+  uint2* xp = reinterpret_cast<uint2*>(smem);
+  float* sx16 = reinterpret_cast<float*>(smem + 2 * K);
+  float* red = sx16 + K / 16;
+
+  const int nb = K / kQK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tig = lane & 3;
+  const int sub = warp / ks, kslice = warp % ks;
+  const int bpw = nb / ks;
+  const int b_begin = kslice * bpw;
   constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
   const int64_t RB = (int64_t)nb * kBB;
-  const int nten = P.kind == 1 ? 2 : 1;
-  const int nslices = (nb + kSliceBlocks - 1) / kSliceBlocks;
-  // Tiles of this CTA, then of this warp.
-  const int c0 = (int)((int64_t)cta * P.tiles / P.ctas), c1 = (int)((int64_t)(cta + 1) * P.tiles / P.ctas);
-  const int t0 = c0 + (int)((int64_t)warp * (c1 - c0) / kGemvWarps);
-  const int t1 = c0 + (int)((int64_t)(warp + 1) * (c1 - c0) / kGemvWarps);
-  const int steps = (t1 - t0) * nten * nslices;
-  uint8_t* const my_stages = stages + (size_t)(2 * warp) * P.stage;  // this warp's two stages
-  uint64_t* full = sh->full[warp];
-  volatile uint32_t* abort_flag = &sh->abort_flag;
+  const int ntiles = (N + 15) / 16;
+  // Units of this CTA: [u_begin, u_end).  A unit is tpc tiles (or, for gate/up,
+  // one tile of each weight tensor).
+  const int u_begin = (int)((int64_t)cta * P.units / P.ctas);
+  const int u_end = (int)((int64_t)(cta + 1) * P.units / P.ctas);
+  const bool gu = P.kind == 1;
+  const uint8_t* Wsub = (gu && sub == 1) ? P.w1 : P.w0;
 
-  // Issue the TMA boxes of step `st` into stage `b` (lane 0 only).
-  auto issue = [&](int st, int b) {
-    const int slice = st % nslices;
-    const int ten = (st / nslices) % nten;
-    const int tile = t0 + st / (nslices * nten);
-    const int n0 = tile * 16;
-    const int b0 = slice * kSliceBlocks;
-    const bool tma = n0 < P.rows_tma;
-    mbar_arrive_expect_tx(&full[b], tma ? (uint32_t)(16 * P.pitch) : 0u);
-    if (tma) {
-      for (int j = 0; j < P.g; ++j) {
-        const int64_t off = (int64_t)j * RB + (int64_t)b0 * kBB;  // byte offset inside a map row
-        tma_load_2d(my_stages + (size_t)b * P.stage + (uint32_t)j * P.region, &P.tm[ten],
-                    (int32_t)((off & ~int64_t(15)) >> 3),
-                    n0 / P.g, &full[b]);
-      }
-    }
+  auto tile_of = [&](int u) { return gu ? u : u * tpc + sub; };
+  auto row_ptr = [&](int tile, int which) {
+    const int r = min(tile * 16 + g + 8 * which, N - 1);
+    return Wsub + r * RB;
   };
 
-  if (lane == 0 && steps > 0) issue(0, 0);
-  float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
-  bool ok = true;
-  for (int st = 0; st < steps && ok; ++st) {
-    const int b = st & 1;
-    const int slice = st % nslices;
-    const int ten = (st / nslices) % nten;
-    const int tile = t0 + st / (nslices * nten);
-    const int n0 = tile * 16;
-    const int b0 = slice * kSliceBlocks;
-    if (lane == 0 && st + 1 < steps) issue(st + 1, b ^ 1);
-    ok = mbar_wait(&full[b], (uint32_t)(st >> 1) & 1u, abort_flag, &g_gemv_status);
-    ok = __all_sync(0xffffffffu, ok);
-    if (!ok) break;
-    uint8_t* stg = my_stages + (size_t)b * P.stage;
-    // Rows past the tensor map (only the last rows of a Q6_K tensor whose row
-    // count is not a multiple of g): copy their slice bytes by hand.
-    if (QT == kQ6K && n0 + 16 > P.rows_tma) {
-      const uint8_t* W = P.w[ten];
-      for (int rho = 0; rho < 16; ++rho) {
-        const int n = n0 + rho;
-        if (n < P.rows_tma || n >= N) continue;
-        const int64_t src0 = (int64_t)n * RB + (int64_t)b0 * kBB;
-        const int64_t rem = RB - (int64_t)b0 * kBB;
-        const int64_t len = rem < (int64_t)kSliceBlocks * kBB ? rem : (int64_t)kSliceBlocks * kBB;
-        uint8_t* dst = stg + row_slot(P, rho) + slot_mis<QT>(RB, n, b0);
-        for (int64_t i = 2 * lane; i < len; i += 64)
-          *reinterpret_cast<uint16_t*>(dst + i) = *reinterpret_cast<const uint16_t*>(W + src0 + i);
-      }
-      __syncwarp();
-    }
-    const int r0 = tile_row(g, P.g), r1 = tile_row(g + 8, P.g);
-    const uint8_t* s0 = stg + row_slot(P, r0) + slot_mis<QT>(RB, min(n0 + r0, N - 1), b0);
-    const uint8_t* s1 = stg + row_slot(P, r1) + slot_mis<QT>(RB, min(n0 + r1, N - 1), b0);
-    float& a0 = ten ? z0 : y0;
-    float& a1 = ten ? z1 : y1;
-#pragma unroll
-    for (int bb = 0; bb < kSliceBlocks; ++bb) {
-      const int blk = b0 + bb;
-      if (blk < nb) {
-        BlockRegs<QT> r;
-        load_block(r, s0 + bb * kBB, s1 + bb * kBB, tig);
-        compute_block(r, xp + 64 * blk, sx16 + 16 * blk, tig, a0, a1);
-      }
-    }
-    fence_proxy_async_smem();  // our reads of this stage precede the TMA that refills it
-    __syncwarp();
-    if (slice == nslices - 1 && ten == nten - 1) {  // tile done
-      y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
-      y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
-      y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-      y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
-      if (P.kind == 1) {
-        z0 += __shfl_xor_sync(0xffffffffu, z0, 1);
-        z0 += __shfl_xor_sync(0xffffffffu, z0, 2);
-        z1 += __shfl_xor_sync(0xffffffffu, z1, 1);
-        z1 += __shfl_xor_sync(0xffffffffu, z1, 2);
-      }
-      if (tig == 0) {
-        const int n_a = n0 + r0, n_b = n0 + r1;
-        if (P.kind == 1) {
-          __half* y = static_cast<__half*>(P.y);
-          if (n_a < N) y[n_a] = __float2half_rn(y0 / (1.0f + __expf(-y0)) * z0);
-          if (n_b < N) y[n_b] = __float2half_rn(y1 / (1.0f + __expf(-y1)) * z1);
-        } else {
-          float* y = static_cast<float*>(P.y);
-          if (n_a < N) y[n_a] = y0;
-          if (n_b < N) y[n_b] = y1;
+  BlockRegs<QT> cur;
+  if (u_begin < u_end && tile_of(u_begin) < ntiles)
+    load_block(cur, row_ptr(tile_of(u_begin), 0) + b_begin * kBB, row_ptr(tile_of(u_begin), 1) + b_begin * kBB,
+               tig);
+  stage_x(P.x, K, xp, sx16);
+  __syncthreads();
+
+  for (int u = u_begin; u < u_end; ++u) {
+    const int tile = tile_of(u);
+    float y0 = 0.f, y1 = 0.f;
+    if (tile < ntiles) {
+      const uint8_t* row0 = row_ptr(tile, 0);
+      const uint8_t* row1 = row_ptr(tile, 1);
+      const int tile_next = tile_of(u + 1);
+      for (int b = b_begin; b < b_begin + bpw; ++b) {
+        BlockRegs<QT> nxt;
+        if (b + 1 < b_begin + bpw) {
+          load_block(nxt, row0 + (b + 1) * kBB, row1 + (b + 1) * kBB, tig);
+        } else if (u + 1 < u_end && tile_next < ntiles) {
+          load_block(nxt, row_ptr(tile_next, 0) + b_begin * kBB, row_ptr(tile_next, 1) + b_begin * kBB, tig);
         }
+        compute_block(cur, xp + 64 * b, sx16 + 16 * b, tig, y0, y1);
+        cur = nxt;
       }
-      y0 = y1 = z0 = z1 = 0.f;
     }
-  }
-  // Drain: the copy issued for the step after an early exit must land first.
-  if (!ok && lane == 0) {
-    for (int b = 0; b < 2; ++b) mbar_wait(&full[b], 0u, abort_flag, &g_gemv_status, true);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
+    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
+    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
+    if (tig == 0) {
+      red[warp * 16 + g] = y0;
+      red[warp * 16 + g + 8] = y1;
+    }
+    __syncthreads();
+    if (!gu) {
+      if (threadIdx.x < 16 * tpc) {
+        const int t = threadIdx.x >> 4, r = threadIdx.x & 15;
+        float acc = 0.f;
+        for (int w = 0; w < ks; ++w) acc += red[(t * ks + w) * 16 + r];
+        const int row = (u * tpc + t) * 16 + r;
+        if (row < N) static_cast<float*>(P.y)[row] = acc;
+      }
+    } else if (threadIdx.x < 16) {
+      const int r = threadIdx.x;
+      float gs = 0.f, us = 0.f;
+      for (int w = 0; w < ks; ++w) {
+        gs += red[w * 16 + r];
+        us += red[(ks + w) * 16 + r];
+      }
+      const int row = u * 16 + r;
+      if (row < N) static_cast<__half*>(P.y)[row] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
+    }
+    __syncthreads();
   }
 }
 
-__global__ void __launch_bounds__(32 * kGemvWarps) gemv_tma_kernel(const __grid_constant__ GemvBatch B) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+__global__ void __maxnreg__(128) gemv_batch_kernel(const __grid_constant__ GemvBatch B) {
+  extern __shared__ __align__(16) uint8_t smem[];
   int i = 0;
   while (i + 1 < B.count && (int)blockIdx.x >= B.p[i + 1].cta_begin) ++i;
   const GemvProb& P = B.p[i];
   const int cta = (int)blockIdx.x - P.cta_begin;
-  const uint32_t x_bytes = ((uint32_t)(2 * P.K + P.K / 4) + 127u) & ~127u;
-  uint8_t* stages = smem + x_bytes;
-  GemvShared* sh = reinterpret_cast<GemvShared*>(stages + (size_t)(2 * kGemvWarps) * P.stage);
-  if (threadIdx.x < 2 * kGemvWarps) mbar_init(&sh->full[threadIdx.x >> 1][threadIdx.x & 1], 1);
-  if (threadIdx.x == 0) {
-    sh->abort_flag = 0;
-    prefetch_tmap(&P.tm[0]);
-    if (P.kind == 1) prefetch_tmap(&P.tm[1]);
-  }
-  fence_mbar_init();
-  __syncthreads();
-  // The first TMA of each warp could go out before x is staged; staging is
-  // short next to a weight fetch, so it simply comes first.
-  stage_x(P.x, P.K, reinterpret_cast<uint2*>(smem), reinterpret_cast<float*>(smem + 2 * P.K));
-  __syncthreads();
   if (P.qtype == kQ4K)
-    run_gemv_problem<kQ4K>(P, cta, smem, stages, sh);
+    run_gemv_problem<kQ4K>(P, cta, smem);
   else
-    run_gemv_problem<kQ6K>(P, cta, smem, stages, sh);
+    run_gemv_problem<kQ6K>(P, cta, smem);
 }
 
 int g_sms = 0;
@@ -503,37 +429,6 @@ int sm_count() {
   return g_sms;
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-// Weight tensor map: rows of g weight rows (g * row_bytes is 16-aligned) of
-// 8-byte elements; one box = `pitch` bytes of 16/g such rows.
-bool make_weight_map(CUtensorMap* tm, const void* w, int64_t N, int64_t RB, int g, int pitch) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc || N / g <= 0) return false;
-  const cuuint64_t dims[2] = {(cuuint64_t)(g * RB / 8), (cuuint64_t)(N / g)};
-  const cuuint64_t strides[1] = {(cuuint64_t)(g * RB)};
-  const cuuint32_t box[2] = {(cuuint32_t)(pitch / 8), (cuuint32_t)(16 / g)};
-  const cuuint32_t estr[2] = {1, 1};
-  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(w), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace
 
 int gemv_max_m() { return 1; }
@@ -545,11 +440,11 @@ uint32_t gemv_take_status() {
   return v;
 }
 
-// Launch one grouped GEMV: per problem the tensor map(s) and stage geometry;
-// CTAs (one or two per SM, by shared memory) split across problems in
+// Launch one grouped GEMV.  ks = the largest of 8, 4, 2, 1 dividing the block
+// count (gate/up: at most 4, so a CTA holds one gate and one up tile).  CTAs:
+// two per SM (256 threads x 128 registers), split across problems in
 // proportion to their weight bytes.
 cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
-  if (count <= 0 || count > kMaxGemvProbs) return cudaErrorInvalidValue;
   GemvBatch B;
   memset(&B, 0, sizeof(B));
   B.count = count;
@@ -558,8 +453,8 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
   size_t smem = 0;
   for (int i = 0; i < count; ++i) {
     GemvProb& P = B.p[i];
-    P.w[0] = static_cast<const uint8_t*>(d[i].w0);
-    P.w[1] = static_cast<const uint8_t*>(d[i].w1);
+    P.w0 = static_cast<const uint8_t*>(d[i].w0);
+    P.w1 = static_cast<const uint8_t*>(d[i].w1);
     P.x = d[i].x;
     P.y = d[i].y;
     P.N = (int)d[i].N;
@@ -567,49 +462,40 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     P.qtype = d[i].qtype;
     P.kind = d[i].w1 ? 1 : 0;
     const int nb = P.K / kQK;
-    const int64_t RB = (int64_t)nb * (P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes);
-    if (P.qtype == kQ4K) {
-      P.g = 1;
-      P.pitch = kSliceBlocks * kQ4KBytes;  // 288 B: 72 words = 8 mod 32, conflict-free 8-byte reads
-      P.region = 16 * P.pitch;
-    } else {
-      int g = 1;
-      while (g < 8 && (g * RB) % 16) g *= 2;
-      P.g = g;
-      // 2 blocks (420 B) plus the window's misalignment (<= 12 when row_bytes is
-      // a multiple of 4, else <= 14), rounded up to 16 bytes.
-      P.pitch = (RB % 4 == 0) ? 432 : 448;
-      P.region = ((16 / g) * P.pitch + 127) / 128 * 128;
+    int ks = 1;
+    for (int c = (P.kind ? 4 : 8); c >= 1; c /= 2)
+      if (nb % c == 0) {
+        ks = c;
+        break;
+      }
+    if (P.kind) {
+      if (nb % 4) return cudaErrorInvalidValue;  // gate/up needs one gate + one up tile per CTA
+      ks = 4;
     }
-    P.stage = P.g * P.region;
-    P.rows_tma = (P.N / P.g) * P.g;
-    for (int t = 0; t < 1 + P.kind; ++t)
-      if (P.rows_tma > 0 && !make_weight_map(&P.tm[t], P.w[t], P.N, RB, P.g, P.pitch))
-        return cudaErrorInvalidValue;
-    P.tiles = (P.N + 15) / 16;
-    bytes[i] = (int64_t)P.N * RB * (1 + P.kind);
+    P.ks = ks;
+    const int tpc = kGemvWarps / ks;
+    const int ntiles = (P.N + 15) / 16;
+    P.units = P.kind ? ntiles : (ntiles + tpc - 1) / tpc;
+    bytes[i] = (int64_t)P.N * nb * (P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes) * (P.kind ? 2 : 1);
     total += (double)bytes[i];
-    const size_t x_bytes = ((size_t)(2 * P.K + P.K / 4) + 127) / 128 * 128;
-    smem = std::max(smem, x_bytes + (size_t)(2 * kGemvWarps) * P.stage + sizeof(GemvShared) + 128);
+    smem = std::max(smem, (size_t)2 * P.K + (size_t)P.K / 4 + (size_t)kGemvWarps * 16 * sizeof(float));
   }
-  const int per_sm = std::max<int>(1, (int)((227 * 1024) / smem));
-  const int budget = std::max(count, sm_count() * std::min(per_sm, 2));
+  const int budget = std::max(count, sm_count() * 2);
   int used = 0;
   for (int i = 0; i < count; ++i) {
-    const int max_ctas = std::max(1, (B.p[i].tiles + kGemvWarps - 1) / kGemvWarps);
     int c = (int)((double)budget * (double)bytes[i] / total);
-    c = std::max(1, std::min(c, max_ctas));
+    c = std::max(1, std::min(c, B.p[i].units));
     B.p[i].ctas = c;
     used += c;
   }
-  for (bool again = true; again && used < budget;) {  // leftover CTAs to the busiest problems
+  // Hand leftover CTAs to the problems with the most units per CTA.
+  for (bool again = true; again && used < budget;) {
     again = false;
     int best = -1;
-    double best_load = 0.0;
+    double best_load = 1.0;
     for (int i = 0; i < count; ++i) {
-      const int max_ctas = std::max(1, (B.p[i].tiles + kGemvWarps - 1) / kGemvWarps);
-      const double load = (double)bytes[i] / B.p[i].ctas;
-      if (B.p[i].ctas < max_ctas && load > best_load) {
+      const double load = (double)B.p[i].units / B.p[i].ctas;
+      if (B.p[i].ctas < B.p[i].units && load > best_load) {
         best_load = load;
         best = i;
       }
@@ -625,14 +511,11 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     B.p[i].cta_begin = begin;
     begin += B.p[i].ctas;
   }
-  static size_t smem_set = 0;
-  if (smem > 48 * 1024 && smem > smem_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         227 * 1024);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    smem_set = 227 * 1024;
   }
-  gemv_tma_kernel<<<begin, 32 * kGemvWarps, smem, s>>>(B);
+  gemv_batch_kernel<<<begin, 32 * kGemvWarps, smem, s>>>(B);
   return cudaGetLastError();
 }
 
