@@ -131,26 +131,41 @@ class Clocks:
 # CPU baseline: the oracle on a bounded sample
 # ----------------------------------------------------------------------------
 def cpu_baseline(target_s: float = 12.0):
-    """The oracle on host cores: gate/up + SwiGLU at M=1024 for as many output
-    features as take about `target_s` seconds (calibrated on a short run)."""
+    """The oracle on host cores over a bounded sample of the prefill step: the
+    same fraction f of the output features of each of its problems (gate/up +
+    SwiGLU, down, attn_v at M=1024), f grown until one run takes at least half
+    of `target_s` (a short run overestimates the time per feature: fixed costs
+    dominate it)."""
     import oracle
     rng = synth.rng_for(7, 1)
-    K, N = synth.HIDDEN, synth.FFN
-    Wg = synth.q4k_weights(rng, N, K)
-    Wu = synth.q4k_weights(rng, N, K)
-    x = synth.activations(rng, PREFILL_M, K)
-    probe = 4 * oracle.num_threads()
-    t0 = time.perf_counter()
-    oracle.gateup_swiglu(Wg, Wu, x, N, K, rows=np.arange(probe))
-    dt = max(time.perf_counter() - t0, 1e-3)
-    rows = int(min(N, max(probe, probe * target_s / dt)))
-    t0 = time.perf_counter()
-    oracle.gateup_swiglu(Wg, Wu, x, N, K, rows=np.arange(rows))
-    dt = time.perf_counter() - t0
-    flops = 2.0 * 2 * PREFILL_M * K * rows
+    gate, up, down, v = prefill_linears()
+    Wg = synth.q4k_weights(rng, gate.N, gate.K)
+    Wu = synth.q4k_weights(rng, up.N, up.K)
+    Wd = synth.q6k_weights(rng, down.N, down.K)
+    Wv = synth.q6k_weights(rng, v.N, v.K)
+    xg = synth.activations(rng, PREFILL_M, gate.K)
+    xd = synth.swiglu_activations(rng, PREFILL_M, down.K)
+
+    def run(f):
+        rg, rd, rv = (max(1, min(n, int(round(f * n)))) for n in (gate.N, down.N, v.N))
+        t0 = time.perf_counter()
+        oracle.gateup_swiglu(Wg, Wu, xg, gate.N, gate.K, rows=np.arange(rg))
+        oracle.matmul(oracle.Q6K, Wd, xd, down.N, down.K, rows=np.arange(rd))
+        oracle.matmul(oracle.Q6K, Wv, xg, v.N, v.K, rows=np.arange(rv))
+        dt = max(time.perf_counter() - t0, 1e-3)
+        flops = 2.0 * PREFILL_M * (2 * gate.K * rg + down.K * rd + v.K * rv)
+        return dt, flops, (rg, rd, rv)
+
+    f = 8.0 * oracle.num_threads() / gate.N
+    while True:
+        dt, flops, rows = run(f)
+        if dt >= 0.5 * target_s or f >= 1.0:
+            break
+        f = min(1.0, max(2.0 * f, f * target_s / dt))
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": "gate/up + SwiGLU of %d of 8192 output features at M=1024, K=3072 (fp64 oracle, %d "
-                      "threads), %.1f s" % (rows, oracle.num_threads(), dt)}
+            "sample": "prefill step at M=1024, fraction %.3f of the output features of each problem "
+                      "(gate/up+SwiGLU %d of %d, down %d of %d, attn_v %d of %d; fp64 oracle, %d threads), %.1f s"
+                      % (f, rows[0], gate.N, rows[1], down.N, rows[2], v.N, oracle.num_threads(), dt)}
 
 
 # ----------------------------------------------------------------------------
