@@ -13,9 +13,11 @@
 //   warp 0      producer: TMA loads of the x tile (BN x 64 fp16, 128-byte
 //               swizzle) per 64-wide K step, and of the packed blocks of the
 //               128 weight rows per 256-wide super-block.
-//   warp 1      allocates tensor memory; one thread issues tcgen05.mma
-//               (kind::f16, fp32 accumulate in TMEM) and tcgen05.commit.
-//   warps 2..   dequantize the packed blocks into fp16 A tiles written straight
+//   warps 1, 2  UMMA issuers (warp 1 also allocates tensor memory): one thread
+//               of each issues tcgen05.mma (kind::f16, fp32 accumulate in
+//               TMEM) and tcgen05.commit for its own accumulator: the gate
+//               and up tensors, or the even and odd K steps of one tensor.
+//   warps 3..   dequantize the packed blocks into fp16 A tiles written straight
 //               into shared memory in the UMMA 128-byte-swizzle K-major layout
 //               (the fp16 weights never touch device memory), then run the
 //               epilogue: tcgen05.ld of the accumulator, fp32 y stores or
@@ -45,52 +47,64 @@ constexpr int kBK = 64;                // K per step: one 128-byte swizzle row o
 constexpr int kMaxBN = 256;            // tokens per tile (UMMA N), multiple of 16
 constexpr int kAStageBytes = kBM * kBK * 2;     // 16 KB
 constexpr uint32_t kH2Magic = 0x64646464u;
+// UMMA issuer warps.  tcgen05.commit holds its issuing thread until that
+// thread's earlier UMMAs have completed, so a single issuer that commits after
+// every K step leaves the tensor pipe idle for the commit's latency; two
+// issuers, each committing its own steps, keep it fed.  Each issuer owns one
+// accumulator (the gate / up tensor, or the even / odd K steps of a single
+// tensor, summed in a fixed order in the epilogue), so results stay
+// deterministic.
+constexpr int kIssuers = 2;
 
 template <int QT, bool GATEUP>
 struct Cfg {
   // Dequant warps: two threads per weight row and tensor (each dequantizes
   // half of every K step), i.e. two warps per SM sub-partition per tensor.
   static constexpr int kDqWarps = GATEUP ? 16 : 8;
-  static constexpr int kThreads = 64 + 32 * kDqWarps;
+  static constexpr int kThreads = 32 * (1 + kIssuers + kDqWarps);
+  static constexpr int kDqWarp0 = 1 + kIssuers;  // first dequant warp
   static constexpr int kNumB = GATEUP ? 2 : 1;  // weight tensors per tile
   // Arrivals that complete an A stage: Q4_K threads each write half of every
   // step; Q6_K threads write two of every four steps in full.
   static constexpr int kAArrivals = QT == kQ4K ? 32 * kDqWarps : 32 * kDqWarps / 2;
-  static constexpr int kPStages = 2;
-  static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : 8 * 4096;  // one tensor, one stage
-  static constexpr int kPBytes = kPStages * kNumB * kPSlotBytes;
+  // Packed-block stages (one super-block of the tile's rows each): 2 .. 4.
+  static constexpr int kMaxPStages = 4;
+  static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : kBM * 224;  // one tensor, one stage
   static constexpr int kMaxStages = 8;
 };
 
-// Shared-memory carve-up for a token tile BN and S K-step stages (all offsets
-// 1024-byte aligned for the 128-byte swizzle atoms).
+struct Bars {
+  uint64_t x_full[8];
+  uint64_t a_full[8];
+  uint64_t s_empty[8];
+  uint64_t p_full[4];
+  uint64_t p_empty[4];
+  uint64_t acc_full;
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+constexpr uint32_t kBarsBytes = (sizeof(Bars) + 127) / 128 * 128;
+
+// Shared-memory carve-up for a token tile BN, S K-step stages and P packed
+// stages (x and A offsets 1024-byte aligned for the 128-byte swizzle atoms).
 struct Layout {
   uint32_t x_off, x_stage, a_off, p_off, bar_off, total;
 };
 
 template <int QT, bool GATEUP, bool AT>
-__host__ __device__ inline Layout make_layout(int BN, int S) {
+__host__ __device__ inline Layout make_layout(int BN, int S, int P) {
   using C = Cfg<QT, GATEUP>;
   Layout L;
   L.x_stage = (uint32_t)BN * kBK * 2;
   L.x_off = 0;
   L.a_off = L.x_off + (uint32_t)S * L.x_stage;
   L.p_off = L.a_off + (AT ? 0u : (uint32_t)(S * C::kNumB) * kAStageBytes);
-  L.bar_off = L.p_off + (uint32_t)C::kPBytes;
-  L.total = L.bar_off + 256 + 1024;  // barriers + base alignment slack
+  L.bar_off = L.p_off + (uint32_t)(P * C::kNumB * C::kPSlotBytes);
+  L.total = L.bar_off + kBarsBytes + 1024;  // barriers + base alignment slack
   return L;
 }
 
-struct Bars {
-  uint64_t x_full[8];
-  uint64_t a_full[8];
-  uint64_t s_empty[8];
-  uint64_t p_full[2];
-  uint64_t p_empty[2];
-  uint64_t acc_full;
-  uint32_t tmem_base;
-  uint32_t abort_flag;
-};
+
 
 struct Params {
   const uint8_t* w[2];  // packed weights (gate, up)
@@ -98,6 +112,7 @@ struct Params {
   void* y;
   int M, N, K, BN;
   int stages;           // K-step pipeline depth S
+  int pstages;          // packed-block pipeline depth P
   int q6_group;         // Q6_K: rows per tensor-map row (g: g * row_bytes % 16 == 0)
   int q6_rows_tma;      // Q6_K: rows covered by the tensor map, (N / g) * g
 };
@@ -144,37 +159,44 @@ __device__ __forceinline__ void q4_scale_min(uint32_t s03, uint32_t s47, uint32_
   mn = (float)b;
 }
 
-// Dequantize half `part` of K step c (0..3) of a Q4_K super-block row held at
-// `rowp` in shared memory: part 0 = the low nibbles (sub-block 2c, step-local
-// k 0..31), part 1 = the high nibbles (sub-block 2c+1, k 32..63).  r[4j..4j+3]
-// receive the 8 fp16 weights of k = 32*part + 8j .. +7 as four k-ordered pairs.
-__device__ __forceinline__ void q4_kstep_regs(const uint8_t* rowp, int c, int part, uint32_t (&r)[16]) {
+// One thread's share of a Q4_K super-block row, held in registers: the 128
+// quant bytes and, for the sub-blocks 2c + PART (c = 0..3) this thread
+// dequantizes, fp16x2 (d*sc) and -(dmin*m) (products rounded in fp32 first).
+struct Q4Regs {
+  uint4 qv[8];
+  __half2 dsc[4], ndmn[4];
+};
+
+template <int PART>
+__device__ __forceinline__ void q4_load(const uint8_t* rowp, Q4Regs& q) {
   const uint4 hdr = *reinterpret_cast<const uint4*>(rowp);
-  const float d = h2f(hdr.x), dmin = h2f(hdr.x >> 16);
-  float sc, mn;
-  q4_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + part, sc, mn);
-  const __half2 dsc = __float2half2_rn(d * sc), ndmn = __float2half2_rn(-(dmin * mn));
-  const uint4 qa = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * c);
-  const uint4 qb = *reinterpret_cast<const uint4*>(rowp + 16 + 32 * c + 16);
-  const uint32_t wv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-  const int shift = 4 * part;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint4 t;
-    q4_emit4((wv[i] >> shift) & 0x0F0F0F0Fu, dsc, ndmn, t);
-    r[2 * i] = t.x;
-    r[2 * i + 1] = t.y;
+  for (int i = 0; i < 8; ++i) q.qv[i] = *reinterpret_cast<const uint4*>(rowp + 16 + 16 * i);
+  const float d = h2f(hdr.x), dmin = h2f(hdr.x >> 16);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float sc, mn;
+    q4_scale_min(hdr.y, hdr.z, hdr.w, 2 * c + PART, sc, mn);
+    q.dsc[c] = __float2half2_rn(d * sc);
+    q.ndmn[c] = __float2half2_rn(-(dmin * mn));
   }
 }
 
-// The same 32 weights written into row rr of a swizzled shared-memory A tile.
-__device__ __forceinline__ void q4_kstep(const uint8_t* rowp, int c, int part, uint8_t* a_tile, int rr) {
-  uint32_t r[16];
-  q4_kstep_regs(rowp, c, part, r);
+// K step c of the row: PART 0 = the low nibbles of quant bytes 32c .. 32c+31
+// (sub-block 2c, step-local k 0..31), PART 1 = the high nibbles (sub-block
+// 2c+1, k 32..63).  r[4j .. 4j+3] = the 8 fp16 weights of k = 32*PART + 8j ..
+// +7 as four k-ordered pairs.
+template <int PART>
+__device__ __forceinline__ void q4_step(const Q4Regs& q, int c, uint32_t (&r)[16]) {
+  const uint4 qa = q.qv[2 * c], qb = q.qv[2 * c + 1];
+  const uint32_t wv[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-    *reinterpret_cast<uint4*>(a_tile + sw128_off(rr, 4 * part + j)) =
-        make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+  for (int i = 0; i < 8; ++i) {
+    uint4 t;
+    q4_emit4((wv[i] >> (4 * PART)) & 0x0F0F0F0Fu, q.dsc[c], q.ndmn[c], t);
+    r[2 * i] = t.x;
+    r[2 * i + 1] = t.y;
+  }
 }
 
 // Q6_K.  The block of a row sits in its smem slot at byte offset MIS (even,
@@ -201,65 +223,68 @@ __device__ __forceinline__ void lds_vecs(const uint8_t* p, uint32_t (&v)[4 * NV]
   }
 }
 
-// Dequantize K steps 2h (side 0: low nibbles) and 2h+1 (side 1: high nibbles)
-// of a Q6_K block (both read ql bytes 64h..64h+63 and qh bytes 128+32h..+31)
-// into row r of two A tiles.
+// One thread's share of a Q6_K super-block row, K steps 2h and 2h+1 (both read
+// ql bytes 64h .. 64h+63 and qh bytes 128+32h .. +31), held in registers.
+struct Q6Regs {
+  uint32_t ql[16], qh[8];
+  uint32_t scw0, scw1;  // int8 scales 8h .. 8h+3 and 8h+4 .. 8h+7
+  float d;
+};
+
 template <int MIS>
-__device__ __forceinline__ void q6_half(const uint8_t* slot, int h, uint8_t* a_tile0, uint8_t* a_tile1, int r) {
+__device__ __forceinline__ void q6_load(const uint8_t* slot, int h, Q6Regs& q) {
   uint32_t vl[20], vh[12], vs[8];
   lds_vecs<5>(slot + 64 * h, vl);         // bytes 64h .. 64h+79
   lds_vecs<3>(slot + 128 + 32 * h, vh);   // bytes 128+32h .. +47
   lds_vecs<2>(slot + 192, vs);            // bytes 192 .. 223
-  uint32_t ql[16], qh[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) ql[i] = q6_pick<MIS>(vl, MIS + 4 * i);
+  for (int i = 0; i < 16; ++i) q.ql[i] = q6_pick<MIS>(vl, MIS + 4 * i);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) qh[i] = q6_pick<MIS>(vh, MIS + 4 * i);
-  const uint32_t scw0 = h ? q6_pick<MIS>(vs, MIS + 8) : q6_pick<MIS>(vs, MIS);       // scales 8h .. 8h+3
-  const uint32_t scw1 = h ? q6_pick<MIS>(vs, MIS + 12) : q6_pick<MIS>(vs, MIS + 4);  // scales 8h+4 .. 8h+7
+  for (int i = 0; i < 8; ++i) q.qh[i] = q6_pick<MIS>(vh, MIS + 4 * i);
+  q.scw0 = h ? q6_pick<MIS>(vs, MIS + 8) : q6_pick<MIS>(vs, MIS);
+  q.scw1 = h ? q6_pick<MIS>(vs, MIS + 12) : q6_pick<MIS>(vs, MIS + 4);
   const uint32_t dw = vs[(16 + MIS) >> 2];
-  const float d = h2f(((16 + MIS) & 3) ? (dw >> 16) : dw);
-  const __half2 k1056 = __float2half2_rn(1056.0f);  // 1024 + 32
-#pragma unroll
-  for (int side = 0; side < 2; ++side) {
-    uint8_t* a_tile = side ? a_tile1 : a_tile0;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {  // chunk j: step-local k = 8j .. 8j+7
-      const int g = 2 * side + (j >> 2);     // 32-weight group within the half
-      const int sidx = 4 * side + (j >> 1);  // 16-weight scale group within the half
-      const uint32_t scw = sidx < 4 ? scw0 : scw1;
-      const float sc = (float)(int8_t)((scw >> (8 * (sidx & 3))) & 0xFFu);
-      const __half2 dsc2 = __float2half2_rn(d * sc);
-      uint32_t o[4];
-#pragma unroll
-      for (int ww = 0; ww < 2; ++ww) {
-        const int i = 2 * j + ww;  // ql word: bytes 64h + 4i, step-local k = 4i .. 4i+3
-        const uint32_t lo4 = (side ? (ql[i] >> 4) : ql[i]) & 0x0F0F0F0Fu;
-        const uint32_t qhw = qh[i & 7];
-        const int sh = 4 - 2 * g;  // bits 2g..2g+1 of every byte -> bits 4..5
-        const uint32_t hs = sh >= 0 ? (qhw << sh) : (qhw >> (-sh));
-        const uint32_t q6 = lo4 | (hs & 0x30303030u);
-        const __half2 p0 = __hsub2(bits_h2(prmt(q6, kH2Magic, 0x4140u)), k1056);
-        const __half2 p1 = __hsub2(bits_h2(prmt(q6, kH2Magic, 0x4342u)), k1056);
-        o[2 * ww] = h2_bits(__hmul2(p0, dsc2));
-        o[2 * ww + 1] = h2_bits(__hmul2(p1, dsc2));
-      }
-      *reinterpret_cast<uint4*>(a_tile + sw128_off(r, j)) = make_uint4(o[0], o[1], o[2], o[3]);
-    }
+  q.d = h2f(((16 + MIS) & 3) ? (dw >> 16) : dw);
+}
+
+__device__ __forceinline__ void q6_load_dispatch(int mis, const uint8_t* slot, int h, Q6Regs& q) {
+  switch (mis) {
+    case 0: q6_load<0>(slot, h, q); break;
+    case 2: q6_load<2>(slot, h, q); break;
+    case 4: q6_load<4>(slot, h, q); break;
+    case 6: q6_load<6>(slot, h, q); break;
+    case 8: q6_load<8>(slot, h, q); break;
+    case 10: q6_load<10>(slot, h, q); break;
+    case 12: q6_load<12>(slot, h, q); break;
+    default: q6_load<14>(slot, h, q); break;
   }
 }
 
-__device__ __forceinline__ void q6_half_dispatch(int mis, const uint8_t* slot, int h, uint8_t* t0, uint8_t* t1,
-                                                 int r) {
-  switch (mis) {
-    case 0: q6_half<0>(slot, h, t0, t1, r); break;
-    case 2: q6_half<2>(slot, h, t0, t1, r); break;
-    case 4: q6_half<4>(slot, h, t0, t1, r); break;
-    case 6: q6_half<6>(slot, h, t0, t1, r); break;
-    case 8: q6_half<8>(slot, h, t0, t1, r); break;
-    case 10: q6_half<10>(slot, h, t0, t1, r); break;
-    case 12: q6_half<12>(slot, h, t0, t1, r); break;
-    default: q6_half<14>(slot, h, t0, t1, r); break;
+// The 64 fp16 weights of K step 2h + SIDE (SIDE 0: low nibbles of ql, SIDE 1:
+// high nibbles) as 32 k-ordered pairs r[4j .. 4j+3] = chunk j (k = 8j .. 8j+7).
+template <int SIDE>
+__device__ __forceinline__ void q6_side(const Q6Regs& q, uint32_t (&r)[32]) {
+  const __half2 k1056 = __float2half2_rn(1056.0f);  // 1024 + 32
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int g = 2 * SIDE + (j >> 2);     // 32-weight group within the half
+    const int sidx = 4 * SIDE + (j >> 1);  // 16-weight scale group within the half
+    const uint32_t scw = sidx < 4 ? q.scw0 : q.scw1;
+    const float sc = (float)(int8_t)((scw >> (8 * (sidx & 3))) & 0xFFu);
+    const __half2 dsc2 = __float2half2_rn(q.d * sc);
+#pragma unroll
+    for (int ww = 0; ww < 2; ++ww) {
+      const int i = 2 * j + ww;  // ql word: bytes 64h + 4i, step-local k = 4i .. 4i+3
+      const uint32_t lo4 = (SIDE ? (q.ql[i] >> 4) : q.ql[i]) & 0x0F0F0F0Fu;
+      const uint32_t qhw = q.qh[i & 7];
+      const int sh = 4 - 2 * g;  // bits 2g..2g+1 of every byte -> bits 4..5
+      const uint32_t hs = sh >= 0 ? (qhw << sh) : (qhw >> (-sh));
+      const uint32_t q6 = lo4 | (hs & 0x30303030u);
+      const __half2 p0 = __hsub2(bits_h2(prmt(q6, kH2Magic, 0x4140u)), k1056);
+      const __half2 p1 = __hsub2(bits_h2(prmt(q6, kH2Magic, 0x4342u)), k1056);
+      r[4 * j + 2 * ww] = h2_bits(__hmul2(p0, dsc2));
+      r[4 * j + 2 * ww + 1] = h2_bits(__hmul2(p1, dsc2));
+    }
   }
 }
 
@@ -290,6 +315,86 @@ __device__ __forceinline__ int dq_row(int t, int g) {
   }
 }
 
+// The dequant threads' main loop.  Thread (row rho, PART) dequantizes, per
+// K step, half of the step's 64 weights of its row (Q4_K: the nibbles PART of
+// sub-block 2c + PART), or for Q6_K the two whole K steps 2*PART and
+// 2*PART + 1 of every super-block.  A super-block's packed bytes are loaded
+// into registers at once and the packed slot released before any
+// conversion, so the producer can refill it while the A tiles are written.
+template <int QT, bool GATEUP, bool AT, int PART>
+__device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bars* bars, int S, int P, int nb, int which,
+                                             int rho, uint32_t a_lane, uint32_t a_col0, int n0, int N, int q6g,
+                                             volatile uint32_t* abort_flag) {
+  using C = Cfg<QT, GATEUP>;
+  constexpr int kChunks = QT == kQ4K ? 4 : 8;  // 16-byte chunks of an A-tile row written per K step
+  uint32_t off[kChunks];
+#pragma unroll
+  for (int j = 0; j < kChunks; ++j) off[j] = sw128_off(rho, QT == kQ4K ? 4 * PART + j : j);
+  const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
+  int step = 0;
+  bool ok = true;
+  for (int kb = 0; kb < nb && ok; ++kb) {
+    const int ps = kb % P;
+    ok = mbar_wait(&bars->p_full[ps], (uint32_t)(kb / P) & 1u, abort_flag, &g_gemm_status);
+    if (!ok) break;
+    const uint8_t* pst = smem + L.p_off + (ps * C::kNumB + which) * C::kPSlotBytes;
+    if constexpr (QT == kQ4K) {
+      Q4Regs q;
+      q4_load<PART>(pst + rho * kQ4KBytes, q);
+      mbar_arrive(&bars->p_empty[ps]);
+#pragma unroll
+      for (int c = 0; c < 4; ++c, ++step) {
+        const int s = step % S;
+        uint32_t r[16];
+        q4_step<PART>(q, c, r);
+        ok = mbar_wait(&bars->s_empty[s], ((uint32_t)(step / S) & 1u) ^ 1u, abort_flag, &g_gemm_status);
+        if constexpr (AT) {
+          ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
+          if (!ok) break;
+          tc_fence_after();
+          tmem_st16(a_lane + a_col0 + (uint32_t)((s * C::kNumB + which) * 32 + 16 * PART), r);
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          if (!ok) break;
+          uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4*>(a_tile + off[j]) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          fence_proxy_async_smem();
+        }
+        mbar_arrive(&bars->a_full[s]);
+      }
+    } else {
+      const int n = min(n0 + rho, N - 1);
+      const int mis = (int)(((int64_t)n * RB + (int64_t)kb * kQ6KBytes) & 15);
+      Q6Regs q;
+      q6_load_dispatch(mis, pst + q6_slot(rho, q6g), PART, q);
+      mbar_arrive(&bars->p_empty[ps]);
+#pragma unroll
+      for (int side = 0; side < 2; ++side) {
+        const int st = step + 2 * PART + side;
+        const int s = st % S;
+        uint32_t r[32];
+        if (side == 0)
+          q6_side<0>(q, r);
+        else
+          q6_side<1>(q, r);
+        ok = mbar_wait(&bars->s_empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemm_status);
+        if (!ok) break;
+        uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(a_tile + off[j]) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars->a_full[s]);
+      }
+      step += 4;
+    }
+  }
+  return ok;
+}
+
 // AT: the dequantized A tiles live in tensor memory (tcgen05.st from the
 // dequant threads, UMMA reads A from TMEM) instead of shared memory.
 template <int QT, bool GATEUP, bool AT>
@@ -299,8 +404,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   using C = Cfg<QT, GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = p.stages;
-  const Layout L = make_layout<QT, GATEUP, AT>(p.BN, S);
+  const int S = p.stages, P = p.pstages;
+  const Layout L = make_layout<QT, GATEUP, AT>(p.BN, S, P);
   Bars* bars = reinterpret_cast<Bars*>(smem + L.bar_off);
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
@@ -317,19 +422,20 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     for (int s = 0; s < S; ++s) {
       mbar_init(&bars->x_full[s], 1);
       mbar_init(&bars->a_full[s], C::kAArrivals);
-      mbar_init(&bars->s_empty[s], 1);
+      mbar_init(&bars->s_empty[s], GATEUP ? kIssuers : 1);  // one commit per issuer using the stage
     }
-    for (int s = 0; s < C::kPStages; ++s) {
+    for (int s = 0; s < P; ++s) {
       mbar_init(&bars->p_full[s], QT == kQ4K ? 1 : 32);
       mbar_init(&bars->p_empty[s], 32 * C::kDqWarps);
     }
-    mbar_init(&bars->acc_full, 1);
+    mbar_init(&bars->acc_full, kIssuers);
     bars->abort_flag = 0;
     fence_mbar_init();
   }
-  // Accumulators: kNumB x BN columns; with AT also S x kNumB A tiles of 32
-  // columns (128 rows x 64 fp16) after them.
-  const uint32_t a_col0 = (uint32_t)(C::kNumB * BN);
+  // Accumulators: one per issuer, BN columns each (gate / up, or even / odd K
+  // steps); with AT also S x kNumB A tiles of 32 columns (128 rows x 64 fp16)
+  // after them.
+  const uint32_t a_col0 = (uint32_t)(kIssuers * BN);
   const uint32_t need_cols = a_col0 + (AT ? (uint32_t)(S * C::kNumB * 32) : 0u);
   const uint32_t tmem_cols = need_cols <= 32 ? 32 : need_cols <= 64 ? 64 : need_cols <= 128 ? 128
                              : need_cols <= 256 ? 256 : 512;
@@ -352,8 +458,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     int step = 0;
     bool ok = true;
     for (int kb = 0; kb < nb && ok; ++kb) {
-      const int ps = kb % C::kPStages;
-      const uint32_t pph = (uint32_t)(kb / C::kPStages) & 1u;
+      const int ps = kb % P;
+      const uint32_t pph = (uint32_t)(kb / P) & 1u;
       ok = mbar_wait(&bars->p_empty[ps], pph ^ 1u, abort_flag, &g_gemm_status);
       if (!ok) break;
       uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
@@ -425,12 +531,17 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       mbar_wait(&bars->x_full[st % S], (uint32_t)(st / S) & 1u, abort_flag, &g_gemm_status,
                 true);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp <= kIssuers) {
+    // ------------------------------------------------------------------ UMMA issuers
+    // Issuer i accumulates into columns [i*BN, (i+1)*BN): gate/up -> tensor i
+    // in every K step; one tensor -> K steps i, i + kIssuers, ...
+    const int iss = warp - 1;
     const uint32_t idesc = umma_idesc_f16(kBM, (uint32_t)BN);
+    const uint32_t d_tm = tmem + (uint32_t)(iss * BN);
+    const int t_first = GATEUP ? 0 : iss, t_stride = GATEUP ? 1 : kIssuers;
+    const int ten = GATEUP ? iss : 0;
     bool ok = true;
-    int step = 0;
-    for (; step < nsteps && ok; ++step) {
+    for (int step = t_first; step < nsteps && ok; step += t_stride) {
       const int s = step % S;
       const uint32_t ph = (uint32_t)(step / S) & 1u;
       ok = mbar_wait(&bars->x_full[s], ph, abort_flag, &g_gemm_status) &&
@@ -438,103 +549,43 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint32_t xa = smem_u32(smem + L.x_off + s * L.x_stage);
-        const uint64_t bdesc = umma_desc_sw128(xa);
+        const uint64_t bdesc = umma_desc_sw128(smem_u32(smem + L.x_off + s * L.x_stage));
+        if constexpr (AT) {
+          const uint32_t a_tm = tmem + a_col0 + (uint32_t)((s * C::kNumB + ten) * 32);
 #pragma unroll
-        for (int t = 0; t < C::kNumB; ++t) {
-          if constexpr (AT) {
-            const uint32_t a_tm = tmem + a_col0 + (uint32_t)((s * C::kNumB + t) * 32);
+          for (int kk = 0; kk < kBK / 16; ++kk)  // 16-wide K slice = 8 TMEM columns of A
+            umma_f16_ts(d_tm, a_tm + (uint32_t)(8 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                        (step > t_first || kk > 0) ? 1u : 0u);
+        } else {
+          const uint64_t adesc = umma_desc_sw128(smem_u32(smem + L.a_off + (s * C::kNumB + ten) * kAStageBytes));
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)  // 16-wide K slice = 8 TMEM columns of A
-              umma_f16_ts(tmem + (uint32_t)(t * BN), a_tm + (uint32_t)(8 * kk), bdesc + (uint64_t)(2 * kk), idesc,
-                          (step > 0 || kk > 0) ? 1u : 0u);
-          } else {
-            const uint32_t aa = smem_u32(smem + L.a_off + (s * C::kNumB + t) * kAStageBytes);
-            const uint64_t adesc = umma_desc_sw128(aa);
-#pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              // +32 bytes per 16-wide K slice inside the swizzle atom (start address in 16 B units)
-              umma_f16_ss(tmem + (uint32_t)(t * BN), adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
-                          (step > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
+          for (int kk = 0; kk < kBK / 16; ++kk)  // +32 bytes per 16-wide K slice inside the swizzle atom
+            umma_f16_ss(d_tm, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
+                        (step > t_first || kk > 0) ? 1u : 0u);
         }
         umma_commit(&bars->s_empty[s]);
-        if (step == nsteps - 1) umma_commit(&bars->acc_full);
       }
       __syncwarp();
     }
-    // Drain: the UMMAs issued last have finished reading shared memory and
-    // writing tensor memory before tensor memory is freed.
-    if (step > 0) {
-      const int st = step - 1;
-      mbar_wait(&bars->s_empty[st % S], (uint32_t)(st / S) & 1u, abort_flag, &g_gemm_status,
-                true);
-    }
+    // acc_full completes once both issuers' UMMAs have completed (it is also
+    // committed after an abort, so the wait below always ends); waiting for it
+    // here keeps tensor memory allocated until the last UMMA is done.
+    if (lane == 0) umma_commit(&bars->acc_full);
+    __syncwarp();
+    mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status, true);
   } else {
     // ------------------------------------------------------------------ dequant + epilogue
-    const int t = threadIdx.x - 64;               // 0 .. 32*kDqWarps-1
+    const int t = threadIdx.x - 32 * C::kDqWarp0;  // 0 .. 32*kDqWarps-1
     const int tpt = 32 * C::kDqWarps / C::kNumB;  // threads per weight tensor (256)
     const int which = t / tpt;                    // weight tensor (0 = gate/only, 1 = up)
     const int part = (t % tpt) >> 7;              // which half of the work on this row
     // With A in TMEM a warp may only write its own lane quarter (warp % 4).
     const int rho = AT ? 32 * (warp & 3) + lane : dq_row<QT>(t & 127, p.q6_group);
     const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
-    int step = 0;
-    bool ok = true;
-    for (int kb = 0; kb < nb && ok; ++kb) {
-      const int ps = kb % C::kPStages;
-      const uint32_t pph = (uint32_t)(kb / C::kPStages) & 1u;
-      ok = mbar_wait(&bars->p_full[ps], pph, abort_flag, &g_gemm_status);
-      if (!ok) break;
-      const uint8_t* pst = smem + L.p_off + (ps * C::kNumB + which) * kPSlotBytes;
-      if constexpr (QT == kQ4K) {
-        const uint8_t* rowp = pst + rho * kQ4KBytes;
-        for (int c = 0; c < 4; ++c, ++step) {
-          const int s = step % S;
-          const uint32_t ph = (uint32_t)(step / S) & 1u;
-          if constexpr (AT) {
-            uint32_t r[16];
-            q4_kstep_regs(rowp, c, part, r);  // overlaps the wait below
-            ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
-            ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
-            if (!ok) break;
-            tc_fence_after();
-            tmem_st16(a_lane + a_col0 + (uint32_t)((s * C::kNumB + which) * 32 + 16 * part), r);
-            tmem_wait_st();
-            tc_fence_before();
-          } else {
-            ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
-            if (!ok) break;
-            uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
-            q4_kstep(rowp, c, part, a_tile, rho);
-            fence_proxy_async_smem();
-          }
-          mbar_arrive(&bars->a_full[s]);
-        }
-      } else {
-        // part h writes K steps 4kb + 2h and 4kb + 2h + 1.
-        const int n = min(n0 + rho, p.N - 1);
-        const int mis = (int)(((int64_t)n * RB + (int64_t)kb * kQ6KBytes) & 15);
-        const uint8_t* slot = pst + q6_slot(rho, p.q6_group);
-        const int h = part;
-        const int st0 = step + 2 * h, st1 = st0 + 1;
-        const int s0 = st0 % S, s1 = st1 % S;
-        ok = mbar_wait(&bars->s_empty[s0], ((uint32_t)(st0 / S) & 1u) ^ 1u, abort_flag, &g_gemm_status) &&
-             mbar_wait(&bars->s_empty[s1], ((uint32_t)(st1 / S) & 1u) ^ 1u, abort_flag, &g_gemm_status);
-        if (ok) {
-          uint8_t* t0 = smem + L.a_off + (s0 * C::kNumB + which) * kAStageBytes;
-          uint8_t* t1 = smem + L.a_off + (s1 * C::kNumB + which) * kAStageBytes;
-          q6_half_dispatch(mis, slot, h, t0, t1, rho);
-          fence_proxy_async_smem();
-          mbar_arrive(&bars->a_full[s0]);
-          mbar_arrive(&bars->a_full[s1]);
-        }
-        step += 4;
-      }
-      if (ok) mbar_arrive(&bars->p_empty[ps]);
-    }
+    bool ok = part == 0 ? dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, S, P, nb, which, rho, a_lane, a_col0, n0, p.N,
+                                                          p.q6_group, abort_flag)
+                        : dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, S, P, nb, which, rho, a_lane, a_col0, n0, p.N,
+                                                          p.q6_group, abort_flag);
 
     // -------------------------------------------------------------- epilogue
     if (ok) ok = mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status);
@@ -547,20 +598,21 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
       const int nchunks = BN / 16;
       // Warps with the same lane quarter split the columns.
-      const int ngroups = C::kDqWarps / 4, grp = (warp - 2) >> 2;
+      const int ngroups = C::kDqWarps / 4, grp = (warp - C::kDqWarp0) >> 2;
       const int per = (nchunks + ngroups - 1) / ngroups;
       const int c_begin = min(nchunks, grp * per), c_end = min(nchunks, c_begin + per);
       if constexpr (!GATEUP) {
         float* y = static_cast<float*>(p.y);
         for (int cc = c_begin; cc < c_end; ++cc) {
-          uint32_t r[16];
-          tmem_ld16(lane_addr + (uint32_t)(16 * cc), r);
+          uint32_t r0[16], r1[16];  // even / odd K steps
+          tmem_ld16(lane_addr + (uint32_t)(16 * cc), r0);
+          tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), r1);
           tmem_wait_ld();
           if (n < p.N) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int m = m0 + 16 * cc + i;
-              if (m < p.M) y[(int64_t)m * p.N + n] = __uint_as_float(r[i]);
+              if (m < p.M) y[(int64_t)m * p.N + n] = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
             }
           }
         }
@@ -577,7 +629,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
               const int m = m0 + 16 * cc + i;
               const float g = __uint_as_float(rg[i]);
               const float u = __uint_as_float(ru[i]);
-              const float o = g / (1.0f + __expf(-g)) * u;
+              const float o = __fdividef(g, 1.0f + __expf(-g)) * u;  // silu(g) * u
               if (m < p.M) y[(int64_t)m * p.N + n] = __float2half_rn(o);
             }
           }
@@ -728,14 +780,23 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   p.N = (int)N;
   p.K = (int)K;
   p.BN = BN;
-  // As many K-step stages as fit in shared memory (2 .. 8).
+  // Pipeline depths: 2 packed-block stages (measured on GB300: deeper
+  // packed prefetch queues more tall weight boxes ahead of the x tiles in the
+  // SM's TMA unit and slows every shape), then as many K-step stages (2 .. 8)
+  // as fit in shared memory (and, with A in tensor memory, in TMEM).
+  auto fits = [&](int S_, int P_) {
+    return make_layout<QT, GATEUP, AT>(BN, S_, P_).total <= (uint32_t)kSmemLimit &&
+           !(AT && kIssuers * BN + S_ * C::kNumB * 32 > 512);
+  };
+  const int P = 2;
   int S = C::kMaxStages;
-  while (S > 2 && (make_layout<QT, GATEUP, AT>(BN, S).total > (uint32_t)kSmemLimit ||
-                   (AT && C::kNumB * BN + S * C::kNumB * 32 > 512)))
-    --S;
-  if (AT && C::kNumB * BN + S * C::kNumB * 32 > 512) return cudaErrorInvalidConfiguration;
+  while (S > 2 && !fits(S, P)) --S;
+  if constexpr (AT) {  // A tiles do not fit next to the accumulators: keep them in shared memory
+    if (kIssuers * BN + S * C::kNumB * 32 > 512) return launch_tc<QT, GATEUP, false>(W0, W1, x, y, M, N, K, stream);
+  }
   p.stages = S;
-  const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, S).total;
+  p.pstages = P;
+  const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, S, P).total;
   if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   static bool attr_set = false;
   if (!attr_set) {
