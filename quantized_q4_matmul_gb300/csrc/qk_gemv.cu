@@ -1,35 +1,38 @@
 // qk_gemv.cu -- decode GEMV (M = 1): y[n] = sum_k x[k] * w[n][k] for Q4_K and
-// Q6_K weights.
+// Q6_K weights, one or several independent problems per launch.
 //
 // Source: DAMASCUS project overview, "[01] the thesis" (decode is one token at
 // a time, GEMV-heavy and limited by streaming the weights from memory) and
 // "[04] one decode step"; "Building DAMASCUS", "Prefill and decode need
 // different performance questions".
 //
-// The kernel is HBM-bound: every packed weight byte is read once.  To keep
-// the arithmetic well under the bandwidth budget the inner products run on
-// the warp-level tensor instruction mma.sync m16n8k16 (fp16 x fp16, fp32
-// accumulate) used as a dot-product engine, with the block scales applied
-// after each sub-block instead of per weight:
-//
-//   * a warp owns 16 weight rows (lane g = lane/4 holds rows g and g+8);
-//   * each 4-bit quant q becomes the fp16 value 1024 + F*q by OR-ing the
-//     nibble into the mantissa of 1024.0 (F = 1 or 16 depending on where the
-//     nibble sits, no shifts needed); the product with an fp16 activation is
-//     exact and the sum is fp32;
-//   * x is replicated across the 8 MMA columns, so every lane holds the sum
-//     D = 1024*Sx + F*sum(q*x) of its two rows for the current sub-block, and
-//     the block math gives  sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + dmin*m)
-//     (Q4_K) or (d*sc/F)*D - Sx*(1024*d*sc/F + 32*d*sc) (Q6_K), Sx being the
-//     sum of the sub-block's activations (computed once per CTA);
-//   * lane tig applies the scales of a quarter of the sub-blocks, so no scale
-//     is decoded twice; partial sums meet in two shuffles and one fixed-order
-//     pass over the warps that split K.  The result is deterministic.
-//
-// Packed rows are read with 8-byte (Q4_K) or 4-byte (Q6_K) loads that each
-// cover whole 32-byte sectors across the warp.  Q6_K blocks are 210 bytes and
-// therefore only 2-byte aligned; their words are assembled from two aligned
-// loads and a funnel shift.
+// The kernel is HBM-bound: every packed weight byte is read once.
+//   * Streaming: the weights of 16 consecutive rows are contiguous, so one
+//     producer warp fetches a whole 16-row tile (or, for long rows, a 16-row x
+//     cb-block chunk, one copy per row) with bulk asynchronous copies into a
+//     ring of 2..8 shared-memory stages; with 100+ KB in flight per SM the HBM
+//     latency is hidden without holding data in registers.
+//   * Arithmetic: 12 compute warps split a stage into half-blocks (16 rows x
+//     128 weights).  The inner products use the warp tensor instruction
+//     mma.sync m16n8k16 (fp16 x fp16, fp32 accumulate) as a dot-product
+//     engine: a 4-bit quant OR-ed into the mantissa of fp16 1024.0 is the exact
+//     value 1024 + F*q (F = 1 or 16 by nibble position, no shifts), its product
+//     with an fp16 activation is exact and the sum fp32.  x is replicated over
+//     the 8 MMA columns, so every lane holds D = 1024*Sx + F*sum(q*x) of its
+//     rows g and g+8 for each sub-block, and
+//       sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + dmin*m)        (Q4_K)
+//       sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + 32*d*sc)       (Q6_K)
+//     with Sx the sub-block's sum of x.  Lane tig (0..3) applies the scales
+//     of one quarter of the half-block's sub-blocks, so no scale is decoded
+//     twice.  A k-permuted fp16 copy of x and the sums Sx are staged once per
+//     CTA in shared memory.
+//   * Reduction: partial sums meet in two shuffles and one fixed-order pass
+//     over the compute warps per tile (deterministic).
+// Q6_K blocks are 210 bytes, so a block can start 2 mod 4 bytes into shared
+// memory; its words then come from two aligned loads and a funnel shift.
+// Problem kind 1 is the fused gate/up + SwiGLU: a stage holds the gate tile
+// and the up tile of the same rows, and the epilogue writes fp16(silu(g)*u).
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -47,20 +50,6 @@ namespace {
 
 constexpr uint32_t kMagic = 0x64006400u;  // fp16x2 (1024.0, 1024.0)
 
-struct GemvProb {
-  const uint8_t* w0;  // weights (gate for kind 1)
-  const uint8_t* w1;  // up weights (kind 1), else null
-  const uint16_t* x;
-  void* y;
-  int N, K, qtype, kind;
-  int ks, units, cta_begin, ctas;
-};
-
-struct GemvBatch {
-  GemvProb p[kMaxGemvProbs];
-  int count;
-};
-
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -70,157 +59,127 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Shared-memory loads through 32-bit shared-window addresses.
+__device__ __forceinline__ uint4 lds128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds32(a)); }
+__device__ __forceinline__ float2 ldsf2(uint32_t a) {
+  const uint2 v = lds64(a);
+  return make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+}
+
+// 4-byte word at shared address a: 4-byte aligned (A2 = false) or 2 mod 4
+// (A2 = true: two aligned loads and a funnel shift).
+template <bool A2>
+__device__ __forceinline__ uint32_t lds_word(uint32_t a) {
+  if constexpr (!A2) {
+    return lds32(a);
+  } else {
+    return __funnelshift_r(lds32(a - 2), lds32(a + 2), 16);
+  }
+}
+
 __device__ __forceinline__ float half_lo(uint32_t v) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
 }
 
-// 4-byte little-endian load from a 2-byte-aligned address inside the buffer.
-__device__ __forceinline__ uint32_t ld_u32_a2(const uint8_t* p) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-  const uint32_t odd = (uint32_t)(a >> 1) & 1u;
-  const uint32_t lo = __ldg(w);
-  const uint32_t hi = __ldg(w + odd);  // same word when aligned: never reads past the block
-  return __funnelshift_r(lo, hi, 16u * odd);
-}
-
-__device__ __forceinline__ float pick4(const float (&v)[4], int i) {
-  float r = v[0];
-  r = i == 1 ? v[1] : r;
-  r = i == 2 ? v[2] : r;
-  r = i == 3 ? v[3] : r;
-  return r;
+// v[i] for a lane-dependent i in 0..3.
+__device__ __forceinline__ float pick4(float v0, float v1, float v2, float v3, int i) {
+  const float a = (i & 1) ? v1 : v0;
+  const float b = (i & 1) ? v3 : v2;
+  return (i & 2) ? b : a;
 }
 
 // ---------------------------------------------------------------------------
-// x staging: xp[k/4] = { fp16x2(x[k], x[k+2]), fp16x2(x[k+1], x[k+3]) } (the
-// MMA k-slot order used below) and sx16[i] = sum of x[16i .. 16i+15] in fp32.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void stage_x(const uint16_t* __restrict__ x, int K, uint2* xp, float* sx16) {
-  const int nq = K / 4;  // a multiple of 64
-  for (int i = threadIdx.x; i < nq; i += blockDim.x) {
-    const uint2 v = *reinterpret_cast<const uint2*>(x + 4 * i);
-    uint2 o;
-    o.x = prmt(v.x, v.y, 0x5410u);  // x0 | x2 << 16
-    o.y = prmt(v.x, v.y, 0x7632u);  // x1 | x3 << 16
-    xp[i] = o;
-    float s = (half_lo(v.x) + half_lo(v.x >> 16)) + (half_lo(v.y) + half_lo(v.y >> 16));
-    s += __shfl_xor_sync(0xffffffffu, s, 1);
-    s += __shfl_xor_sync(0xffffffffu, s, 2);
-    if ((i & 3) == 0) sx16[i >> 2] = s;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Q4_K: lane (g, tig) handles rows g, g+8.  In 64-weight group G (sub-blocks
-// 2G, 2G+1, quant bytes 32G..32G+31) the lane owns bytes 8*tig .. 8*tig+7,
-// i.e. words hh = 0, 1 at 8*tig + 4*hh.  Word hh feeds one MMA per sub-block:
+// Q4_K half-block U (sub-blocks 4U .. 4U+3, quant bytes 64U .. 64U+63) of the
+// lane's rows g (block at shared address b0) and g+8 (b1).  In 64-weight group
+// G (sub-blocks 2G, 2G+1, quant bytes 32G .. 32G+31) the lane owns bytes
+// 8*tig .. 8*tig+7, i.e. words hh = 0, 1 at 8*tig + 4*hh.  Word hh feeds one
+// MMA per sub-block:
 //   k-slots 2tig, 2tig+1  <- bytes 0, 2 of the word  (k = 8tig+4hh + 0, 2)
 //   k-slots 2tig+8, +9    <- bytes 1, 3              (k = 8tig+4hh + 1, 3)
+// which is the order of the permuted x pairs xp[k/4] = {(x0,x2), (x1,x3)}.
 // Low nibbles (mask 0x000F000F, F = 1) give sub-block 2G, high nibbles (mask
-// 0x00F000F0, F = 16) sub-block 2G+1.
+// 0x00F000F0, F = 16) sub-block 2G+1.  Lane tig then scales sub-block
+// j = 4U + tig of both rows.
 // ---------------------------------------------------------------------------
-struct Q4Scales {
-  float a_lo, c_lo, a_hi, c_hi;
-};
-
-// Scale/min of sub-blocks 2*tig and 2*tig+1 from a block header.
-__device__ __forceinline__ Q4Scales q4k_lane_scales(uint4 hdr, int tig) {
-  const float d = half_lo(hdr.x);
-  const float dmin = half_lo(hdr.x >> 16);
-  Q4Scales r;
+template <int U>
+__device__ __forceinline__ void q4_half(uint32_t b0, uint32_t b1, uint32_t xa, uint32_t sxa, int tig, float& y0,
+                                        float& y1) {
+  float D[2][2][4];  // [G - 2U][lo, hi][mma regs]
 #pragma unroll
-  for (int side = 0; side < 2; ++side) {
-    const int j = 2 * tig + side;
-    const int jj = j & 3;
-    uint32_t sc, mn;
-    if (j < 4) {
-      sc = (hdr.y >> (8 * jj)) & 63u;
-      mn = (hdr.z >> (8 * jj)) & 63u;
-    } else {
-      const uint32_t lo = (hdr.w >> (8 * jj)) & 0xFFu;
-      sc = (lo & 0xFu) | (((hdr.y >> (8 * jj + 6)) & 3u) << 4);
-      mn = (lo >> 4) | (((hdr.z >> (8 * jj + 6)) & 3u) << 4);
-    }
-    const float dsc = d * (float)sc;
-    const float dmn = dmin * (float)mn;
-    if (side == 0) {
-      r.a_lo = dsc;
-      r.c_lo = fmaf(1024.0f, dsc, dmn);
-    } else {
-      r.a_hi = dsc * 0.0625f;
-      r.c_hi = fmaf(64.0f, dsc, dmn);
-    }
-  }
-  return r;
-}
-
-// Registers holding one block of each of the lane's two rows.
-template <int QT>
-struct BlockRegs;
-
-template <>
-struct BlockRegs<kQ4K> {
-  uint4 h0, h1;      // d, dmin, packed scales of rows g, g+8
-  uint2 q0[4], q1[4];  // quant bytes 32G + 8tig .. +7, G = 0..3
-};
-
-__device__ __forceinline__ void load_block(BlockRegs<kQ4K>& r, const uint8_t* blk0, const uint8_t* blk1, int tig) {
-  r.h0 = __ldg(reinterpret_cast<const uint4*>(blk0));
-  r.h1 = __ldg(reinterpret_cast<const uint4*>(blk1));
-#pragma unroll
-  for (int G = 0; G < 4; ++G) {
-    r.q0[G] = ldg_stream8(blk0 + 16 + 32 * G + 8 * tig);
-    r.q1[G] = ldg_stream8(blk1 + 16 + 32 * G + 8 * tig);
-  }
-}
-
-__device__ __forceinline__ void compute_block(const BlockRegs<kQ4K>& r, const uint2* xpb, const float* sxb, int tig,
-                                              float& y0, float& y1) {
-  float dlo0[4], dlo1[4], dhi0[4], dhi1[4];
-#pragma unroll
-  for (int G = 0; G < 4; ++G) {
+  for (int i = 0; i < 2; ++i) {
+    const int G = 2 * U + i;
+    const uint2 w0 = lds64(b0 + 16 + 32 * G + 8 * tig);
+    const uint2 w1 = lds64(b1 + 16 + 32 * G + 8 * tig);
+    const uint4 xlo = lds128(xa + 8 * (16 * G + 2 * tig));      // k = 64G + 8tig + 0..7
+    const uint4 xhi = lds128(xa + 8 * (16 * G + 8 + 2 * tig));  // k + 32
     float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint4 xlo = *reinterpret_cast<const uint4*>(xpb + 16 * G + 2 * tig);      // k = 64G + 8tig + {0..7}
-    const uint4 xhi = *reinterpret_cast<const uint4*>(xpb + 16 * G + 8 + 2 * tig);  // k + 32
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const uint32_t w0 = hh ? r.q0[G].y : r.q0[G].x;
-      const uint32_t w1 = hh ? r.q1[G].y : r.q1[G].x;
-      const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
-      const uint32_t bl0 = hh ? xlo.z : xlo.x, bl1 = hh ? xlo.w : xlo.y;
-      const uint32_t bh0 = hh ? xhi.z : xhi.x, bh1 = hh ? xhi.w : xhi.y;
-      mma16816(c, (w0 & 0x000F000Fu) | kMagic, (w1 & 0x000F000Fu) | kMagic, (s0 & 0x000F000Fu) | kMagic,
-               (s1 & 0x000F000Fu) | kMagic, bl0, bl1);
-      mma16816(e, (w0 & 0x00F000F0u) | kMagic, (w1 & 0x00F000F0u) | kMagic, (s0 & 0x00F000F0u) | kMagic,
-               (s1 & 0x00F000F0u) | kMagic, bh0, bh1);
+      const uint32_t v0 = hh ? w0.y : w0.x, v1 = hh ? w1.y : w1.x;
+      const uint32_t s0 = v0 >> 8, s1 = v1 >> 8;
+      mma16816(c, (v0 & 0x000F000Fu) | kMagic, (v1 & 0x000F000Fu) | kMagic, (s0 & 0x000F000Fu) | kMagic,
+               (s1 & 0x000F000Fu) | kMagic, hh ? xlo.z : xlo.x, hh ? xlo.w : xlo.y);
+      mma16816(e, (v0 & 0x00F000F0u) | kMagic, (v1 & 0x00F000F0u) | kMagic, (s0 & 0x00F000F0u) | kMagic,
+               (s1 & 0x00F000F0u) | kMagic, hh ? xhi.z : xhi.x, hh ? xhi.w : xhi.y);
     }
-    dlo0[G] = c[0];
-    dlo1[G] = c[2];
-    dhi0[G] = e[0];
-    dhi1[G] = e[2];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      D[i][0][r] = c[r];
+      D[i][1][r] = e[r];
+    }
   }
-  // This lane applies the scales of group G = tig (sub-blocks 2tig, 2tig+1).
-  const Q4Scales r0 = q4k_lane_scales(r.h0, tig);
-  const Q4Scales r1 = q4k_lane_scales(r.h1, tig);
-  const float2 sx = make_float2(sxb[4 * tig] + sxb[4 * tig + 1], sxb[4 * tig + 2] + sxb[4 * tig + 3]);
-  y0 = fmaf(r0.a_lo, pick4(dlo0, tig), y0);
-  y0 = fmaf(-r0.c_lo, sx.x, y0);
-  y0 = fmaf(r0.a_hi, pick4(dhi0, tig), y0);
-  y0 = fmaf(-r0.c_hi, sx.y, y0);
-  y1 = fmaf(r1.a_lo, pick4(dlo1, tig), y1);
-  y1 = fmaf(-r1.c_lo, sx.x, y1);
-  y1 = fmaf(r1.a_hi, pick4(dhi1, tig), y1);
-  y1 = fmaf(-r1.c_hi, sx.y, y1);
+  // Sub-block j = 4U + tig: group G = 2U + (tig >> 1), nibble tig & 1.
+  const float d0 = pick4(D[0][0][0], D[0][1][0], D[1][0][0], D[1][1][0], tig);
+  const float d1 = pick4(D[0][0][2], D[0][1][2], D[1][0][2], D[1][1][2], tig);
+  const uint4 h0 = lds128(b0), h1 = lds128(b1);
+  const int sh = 8 * tig;
+  uint32_t sc0, mn0, sc1, mn1;
+  if constexpr (U == 0) {
+    sc0 = (h0.y >> sh) & 63u;
+    mn0 = (h0.z >> sh) & 63u;
+    sc1 = (h1.y >> sh) & 63u;
+    mn1 = (h1.z >> sh) & 63u;
+  } else {
+    const uint32_t l0 = h0.w >> sh, l1 = h1.w >> sh;
+    sc0 = (l0 & 0xFu) | ((h0.y >> (sh + 2)) & 0x30u);
+    mn0 = ((l0 >> 4) & 0xFu) | ((h0.z >> (sh + 2)) & 0x30u);
+    sc1 = (l1 & 0xFu) | ((h1.y >> (sh + 2)) & 0x30u);
+    mn1 = ((l1 >> 4) & 0xFu) | ((h1.z >> (sh + 2)) & 0x30u);
+  }
+  const float inv_f = (tig & 1) ? 0.0625f : 1.0f;
+  const float2 sxp = ldsf2(sxa + 8 * (4 * U + tig));  // 16-wide x sums of sub-block j
+  const float sx = sxp.x + sxp.y;
+  const float dsc0 = half_lo(h0.x) * (float)sc0, dmn0 = half_lo(h0.x >> 16) * (float)mn0;
+  const float dsc1 = half_lo(h1.x) * (float)sc1, dmn1 = half_lo(h1.x >> 16) * (float)mn1;
+  const float a0 = dsc0 * inv_f, a1 = dsc1 * inv_f;
+  y0 = fmaf(a0, d0, fmaf(-fmaf(1024.0f, a0, dmn0), sx, y0));
+  y1 = fmaf(a1, d1, fmaf(-fmaf(1024.0f, a1, dmn1), sx, y1));
 }
 
 // ---------------------------------------------------------------------------
-// Q6_K: scale group t (16 weights, t = 8h + 2*g6 + s) takes its low 4 bits
-// from quant bytes 64h + 32(g6&1) + 16s + l (low nibble if g6 < 2) and its
-// high 2 bits from bits 2*g6 of byte 128 + 32h + 16s + l, l = 0..15.  Lane tig
-// owns l = 4tig .. 4tig+3 (one word of each).  The fp16 operand is 1024 + F*q6
+// Q6_K half H (scale groups 8H .. 8H+7, 128 weights).  Scale group t = 8H + tt
+// (tt = 2*g6 + s, g6 = 0..3) takes its low 4 bits from quant bytes
+// 64H + 32(g6&1) + 16s + l (low nibble if g6 < 2) and its high 2 bits from
+// bits 2*g6 of byte 128 + 32H + 16s + l, l = 0..15.  Lane tig owns
+// l = 4tig .. 4tig+3 (one word of each).  The fp16 operand is 1024 + F*q6
 // with F = 1 (g6 < 2: nibble in bits 0-3, high bits moved to 4-5) or F = 16
-// (g6 >= 2: nibble in bits 4-7, high bits moved to 8-9).
+// (g6 >= 2: nibble in bits 4-7, high bits moved to 8-9).  Lane tig scales
+// groups 8H + tig and 8H + 4 + tig of both rows.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void q6k_operands(uint32_t wl, uint32_t wh, int g6, uint32_t& r0, uint32_t& r2) {
   const uint32_t wl8 = wl >> 8;
@@ -235,186 +194,312 @@ __device__ __forceinline__ void q6k_operands(uint32_t wl, uint32_t wh, int g6, u
   }
 }
 
-template <>
-struct BlockRegs<kQ6K> {
-  uint32_t ql0[8], ql1[8], qh0[4], qh1[4];  // the lane's quant words of rows g, g+8
-  uint32_t sc0, sc1;                        // int8 scales t = 4u + tig, u = 0..3 (byte u)
-  uint32_t d;                               // fp16 d of row g (low half) and row g+8 (high half)
+// The lane's words of one Q6_K half for rows g (block at b0) and g+8 (b1):
+// loads only, so a caller may pick A2 per lane.
+struct Q6Half {
+  uint32_t ql0[4], ql1[4], qh0[2], qh1[2];
+  uint32_t sc0[2], sc1[2];  // int8 scale words 192 + 8H + 4u (u = 0, 1)
+  uint32_t dw0, dw1;        // the words holding d (low half)
 };
 
-__device__ __forceinline__ void load_block(BlockRegs<kQ6K>& r, const uint8_t* blk0, const uint8_t* blk1, int tig) {
+template <int H, bool A2>
+__device__ __forceinline__ void q6_load_half(uint32_t b0, uint32_t b1, int tig, Q6Half& q) {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {  // i = 4h + 2p + s: byte 64h + 32p + 16s + 4tig
-    const int off = 64 * (i >> 2) + 32 * ((i >> 1) & 1) + 16 * (i & 1) + 4 * tig;
-    r.ql0[i] = ld_u32_a2(blk0 + off);
-    r.ql1[i] = ld_u32_a2(blk1 + off);
+  for (int i = 0; i < 4; ++i) {  // i = 2p + s: byte 64H + 32p + 16s + 4tig
+    const uint32_t off = 64 * H + 32 * (i >> 1) + 16 * (i & 1) + 4 * tig;
+    q.ql0[i] = lds_word<A2>(b0 + off);
+    q.ql1[i] = lds_word<A2>(b1 + off);
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // i = 2h + s: byte 128 + 32h + 16s + 4tig
-    const int off = 128 + 32 * (i >> 1) + 16 * (i & 1) + 4 * tig;
-    r.qh0[i] = ld_u32_a2(blk0 + off);
-    r.qh1[i] = ld_u32_a2(blk1 + off);
+  for (int s = 0; s < 2; ++s) {  // byte 128 + 32H + 16s + 4tig
+    const uint32_t off = 128 + 32 * H + 16 * s + 4 * tig;
+    q.qh0[s] = lds_word<A2>(b0 + off);
+    q.qh1[s] = lds_word<A2>(b1 + off);
   }
-  uint32_t s0 = 0, s1 = 0;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    s0 |= (uint32_t)__ldg(blk0 + 192 + 4 * u + tig) << (8 * u);
-    s1 |= (uint32_t)__ldg(blk1 + 192 + 4 * u + tig) << (8 * u);
+  for (int u = 0; u < 2; ++u) {
+    q.sc0[u] = lds_word<A2>(b0 + 192 + 8 * H + 4 * u);
+    q.sc1[u] = lds_word<A2>(b1 + 192 + 8 * H + 4 * u);
   }
-  r.sc0 = s0;
-  r.sc1 = s1;
-  r.d = (uint32_t)__ldg(reinterpret_cast<const uint16_t*>(blk0 + 208)) |
-        ((uint32_t)__ldg(reinterpret_cast<const uint16_t*>(blk1 + 208)) << 16);
+  q.dw0 = lds_word<A2>(b0 + 208);
+  q.dw1 = lds_word<A2>(b1 + 208);
 }
 
-__device__ __forceinline__ void compute_block(const BlockRegs<kQ6K>& r, const uint2* xpb, const float* sxb, int tig,
-                                              float& y0, float& y1) {
-  float d0[16], d1[16];
+template <int H>
+__device__ __forceinline__ void q6_half(const Q6Half& q, uint32_t xa, uint32_t sxa, int tig, float& y0, float& y1) {
+  float d0[8], d1[8];
 #pragma unroll
-  for (int t = 0; t < 16; ++t) {
-    const int h = t >> 3, g6 = (t >> 1) & 3, s = t & 1;
-    const int li = 4 * h + 2 * (g6 & 1) + s, hi = 2 * h + s;
+  for (int tt = 0; tt < 8; ++tt) {
+    const int g6 = (tt >> 1) & 3, s = tt & 1;
+    const int li = 2 * (g6 & 1) + s;
     uint32_t a0, a2, a1, a3;
-    q6k_operands(r.ql0[li], r.qh0[hi], g6, a0, a2);
-    q6k_operands(r.ql1[li], r.qh1[hi], g6, a1, a3);
-    const uint2 b = xpb[4 * t + tig];
+    q6k_operands(q.ql0[li], q.qh0[s], g6, a0, a2);
+    q6k_operands(q.ql1[li], q.qh1[s], g6, a1, a3);
+    const uint2 bx = lds64(xa + 8 * (4 * (8 * H + tt) + tig));
     float c[4] = {0.f, 0.f, 0.f, 0.f};
-    mma16816(c, a0, a1, a2, a3, b.x, b.y);
-    d0[t] = c[0];
-    d1[t] = c[2];
+    mma16816(c, a0, a1, a2, a3, bx.x, bx.y);
+    d0[tt] = c[0];
+    d1[tt] = c[2];
   }
-  // Scales: lane tig applies scale groups t = 4u + tig.
-  const float dA = half_lo(r.d), dB = half_lo(r.d >> 16);
+  // Scale groups 8H + tig (u = 0, F = 1) and 8H + 4 + tig (u = 1, F = 16).
+  const float dA = half_lo(q.dw0), dB = half_lo(q.dw1);
+  const int sh = 8 * tig;
 #pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int t = 4 * u + tig;
-    // 1/F: scale group t = 4u + tig has g6 = (2u + tig/2) & 3, which is >= 2 exactly for odd u.
-    const float inv_f = (u & 1) ? 0.0625f : 1.0f;
-    const float dsc0 = dA * (float)(int8_t)((r.sc0 >> (8 * u)) & 0xFFu);
-    const float dsc1 = dB * (float)(int8_t)((r.sc1 >> (8 * u)) & 0xFFu);
-    float v0[4] = {d0[4 * u], d0[4 * u + 1], d0[4 * u + 2], d0[4 * u + 3]};
-    float v1[4] = {d1[4 * u], d1[4 * u + 1], d1[4 * u + 2], d1[4 * u + 3]};
-    const float sxt = sxb[t];
+  for (int u = 0; u < 2; ++u) {
+    const float inv_f = u ? 0.0625f : 1.0f;
+    const float dsc0 = dA * (float)(int8_t)((q.sc0[u] >> sh) & 0xFFu);
+    const float dsc1 = dB * (float)(int8_t)((q.sc1[u] >> sh) & 0xFFu);
+    const float v0 = pick4(d0[4 * u], d0[4 * u + 1], d0[4 * u + 2], d0[4 * u + 3], tig);
+    const float v1 = pick4(d1[4 * u], d1[4 * u + 1], d1[4 * u + 2], d1[4 * u + 3], tig);
+    const float sx = ldsf(sxa + 4 * (8 * H + 4 * u + tig));
     const float a0 = dsc0 * inv_f, a1 = dsc1 * inv_f;
-    y0 = fmaf(a0, pick4(v0, tig), y0);
-    y0 = fmaf(-fmaf(1024.0f, a0, 32.0f * dsc0), sxt, y0);
-    y1 = fmaf(a1, pick4(v1, tig), y1);
-    y1 = fmaf(-fmaf(1024.0f, a1, 32.0f * dsc1), sxt, y1);
+    y0 = fmaf(a0, v0, fmaf(-fmaf(1024.0f, a0, 32.0f * dsc0), sx, y0));
+    y1 = fmaf(a1, v1, fmaf(-fmaf(1024.0f, a1, 32.0f * dsc1), sx, y1));
   }
 }
 
 // ---------------------------------------------------------------------------
-// The grouped kernel.  One launch runs up to kMaxGemvProbs independent M = 1
-// problems (e.g. the seven linears of a decoder layer).  Each problem owns a
-// contiguous range of CTAs, sized by its share of the total weight bytes, so
-// every CTA stages one x and the whole launch finishes together.  A CTA has 8
-// warps: `ks` warps split the K blocks of a 16-row tile and `tpc` = 8 / ks
-// tiles are processed side by side; the CTA walks its contiguous range of
-// such units, every warp loading the next block (or the next unit's first
-// block) while it computes the current one.  Partial sums of the ks warps of
-// a tile meet in shared memory in a fixed order (deterministic).
-//
-// Problem kind 1 is the fused gate/up + SwiGLU: sub-tile 0 holds rows of the
-// gate weights, sub-tile 1 the same rows of the up weights, and the epilogue
-// writes fp16(silu(g) * u).
+// The kernel
 // ---------------------------------------------------------------------------
-constexpr int kGemvWarps = 8;
+// Compute warps per CTA (measured on GB300: 12 beat 8 and 16 on the decode
+// layer; a K = 3072 tile is 24 half-blocks, two per warp).
+#ifndef QK_GEMV_WARPS
+#define QK_GEMV_WARPS 12
+#endif
+constexpr int kComputeWarps = QK_GEMV_WARPS;
+constexpr int kThreads = 32 * (kComputeWarps + 1);  // + one producer warp
+constexpr int kMaxStages = 8;
+
+struct GemvProb {
+  const uint8_t* w[2];  // weights (gate for kind 1), up weights (kind 1)
+  const uint16_t* x;
+  void* y;
+  int N, K, qtype, kind;
+  int cb;           // K blocks per chunk (a stage holds 16 rows x cb blocks per weight tensor)
+  int tiles, cta_begin, ctas;
+};
+
+struct GemvBatch {
+  GemvProb p[kMaxGemvProbs];
+  int count;
+  int stages;       // pipeline depth (same for every problem of the launch)
+  uint32_t stage_bytes;
+};
+
+struct GemvShared {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  float red[2][kComputeWarps][2][16];  // [tile parity][warp][tensor][row]
+  uint32_t abort_flag;
+};
 
 template <int QT>
-__device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uint8_t* smem) {
-  const int K = P.K, N = P.N, ks = P.ks, tpc = kGemvWarps / P.ks;
-  uint2* xp = reinterpret_cast<uint2*>(smem);
-  float* sx16 = reinterpret_cast<float*>(smem + 2 * K);
-  float* red = sx16 + K / 16;
-
-  const int nb = K / kQK;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = lane >> 2, tig = lane & 3;
-  const int sub = warp / ks, kslice = warp % ks;
-  const int bpw = nb / ks;
-  const int b_begin = kslice * bpw;
+__device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, const GemvBatch& B, uint8_t* smem,
+                                                 uint8_t* stages, GemvShared* sh) {
+  const int K = P.K, N = P.N, nb = K / kQK, cb = P.cb;
   constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
   const int64_t RB = (int64_t)nb * kBB;
-  const int ntiles = (N + 15) / 16;
-  // Units of this CTA: [u_begin, u_end).  A unit is tpc tiles (or, for gate/up,
-  // one tile of each weight tensor).
-  const int u_begin = (int)((int64_t)cta * P.units / P.ctas);
-  const int u_end = (int)((int64_t)(cta + 1) * P.units / P.ctas);
-  const bool gu = P.kind == 1;
-  const uint8_t* Wsub = (gu && sub == 1) ? P.w1 : P.w0;
+  const int nten = P.kind == 1 ? 2 : 1;
+  const int nchunks = nb / cb;  // the host makes cb divide nb
+  const int t0 = (int)((int64_t)cta * P.tiles / P.ctas), t1 = (int)((int64_t)(cta + 1) * P.tiles / P.ctas);
+  const int steps = (t1 - t0) * nchunks;
+  const int S = B.stages;
+  const uint32_t SB = B.stage_bytes;
+  const uint32_t ten_bytes = (uint32_t)(16 * cb * kBB);  // one tensor's share of a stage
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile uint32_t* abort_flag = &sh->abort_flag;
 
-  auto tile_of = [&](int u) { return gu ? u : u * tpc + sub; };
-  auto row_ptr = [&](int tile, int which) {
-    const int r = min(tile * 16 + g + 8 * which, N - 1);
-    return Wsub + r * RB;
-  };
-
-  BlockRegs<QT> cur;
-  if (u_begin < u_end && tile_of(u_begin) < ntiles)
-    load_block(cur, row_ptr(tile_of(u_begin), 0) + b_begin * kBB, row_ptr(tile_of(u_begin), 1) + b_begin * kBB,
-               tig);
-  stage_x(P.x, K, xp, sx16);
-  __syncthreads();
-
-  for (int u = u_begin; u < u_end; ++u) {
-    const int tile = tile_of(u);
-    float y0 = 0.f, y1 = 0.f;
-    if (tile < ntiles) {
-      const uint8_t* row0 = row_ptr(tile, 0);
-      const uint8_t* row1 = row_ptr(tile, 1);
-      const int tile_next = tile_of(u + 1);
-      for (int b = b_begin; b < b_begin + bpw; ++b) {
-        BlockRegs<QT> nxt;
-        if (b + 1 < b_begin + bpw) {
-          load_block(nxt, row0 + (b + 1) * kBB, row1 + (b + 1) * kBB, tig);
-        } else if (u + 1 < u_end && tile_next < ntiles) {
-          load_block(nxt, row_ptr(tile_next, 0) + b_begin * kBB, row_ptr(tile_next, 1) + b_begin * kBB, tig);
+  if (warp == kComputeWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int st = 0;
+      for (; st < steps; ++st) {
+        const int s = st % S;
+        if (!mbar_wait(&sh->empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemv_status)) break;
+        const int tile = t0 + st / nchunks, chunk = st % nchunks;
+        const int n0 = tile * 16, rows = min(16, N - n0);
+        uint8_t* dst = stages + (size_t)s * SB;
+        if (cb == nb) {
+          // The whole tile: rows n0 .. n0+rows-1 are one contiguous span.
+          const int64_t span = (int64_t)rows * RB;
+          const uint32_t bulk = (uint32_t)(span & ~int64_t(15));
+          mbar_expect_tx(&sh->full[s], bulk * (uint32_t)nten);
+          for (int t = 0; t < nten; ++t) {
+            const uint8_t* src = P.w[t] + (int64_t)n0 * RB;
+            uint8_t* d = dst + t * ten_bytes;
+            if (bulk) bulk_copy_g2s(d, src, bulk, &sh->full[s]);
+            for (int64_t b = bulk; b < span; b += 2)  // last bytes of the tensor (span % 16 != 0)
+              *reinterpret_cast<uint16_t*>(d + b) = *reinterpret_cast<const uint16_t*>(src + b);
+          }
+        } else {
+          // A K chunk: one copy per row of cb blocks (16-byte aligned by construction).
+          const uint32_t row_bytes = (uint32_t)(cb * kBB);
+          mbar_expect_tx(&sh->full[s], row_bytes * (uint32_t)(rows * nten));
+          for (int t = 0; t < nten; ++t)
+            for (int r = 0; r < rows; ++r)
+              bulk_copy_g2s(dst + t * ten_bytes + r * row_bytes,
+                            P.w[t] + (int64_t)(n0 + r) * RB + (int64_t)chunk * cb * kBB, row_bytes, &sh->full[s]);
         }
-        compute_block(cur, xp + 64 * b, sx16 + 16 * b, tig, y0, y1);
-        cur = nxt;
+        mbar_arrive(&sh->full[s]);
+      }
+      // Drain: the copies issued last have landed before the CTA can exit.
+      for (int i = 1; i <= S && i <= st; ++i)
+        mbar_wait(&sh->full[(st - i) % S], (uint32_t)((st - i) / S) & 1u, abort_flag, &g_gemv_status, true);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- compute
+  const uint32_t xs = smem_u32(smem);             // permuted x pairs, 8 bytes per 4 k
+  const uint32_t sxs = smem_u32(smem + 2 * K);    // 16-wide sums of x
+  const uint32_t ring = smem_u32(stages);
+  const int g = lane >> 2, tig = lane & 3;
+  const uint32_t pitch = (cb == nb) ? (uint32_t)RB : (uint32_t)(cb * kBB);  // bytes per row inside a stage
+  const int units = 2 * nten * cb;  // half-blocks per stage
+  float ya0 = 0.f, ya1 = 0.f, yb0 = 0.f, yb1 = 0.f;  // rows g, g+8 of tensor 0 (a) and 1 (b)
+  bool ok = true;
+  for (int st = 0; st < steps; ++st) {
+    const int s = st % S;
+    const int tile = t0 + st / nchunks, chunk = st % nchunks;
+    // After a timed-out wait the warp skips the arithmetic but keeps taking
+    // part in the per-tile named barrier below, so no compute warp is left
+    // waiting there for one that gave up.
+    if (ok)
+      ok = __all_sync(0xffffffffu, mbar_wait(&sh->full[s], (uint32_t)(st / S) & 1u, abort_flag, &g_gemv_status));
+    const uint32_t stg = ring + (uint32_t)s * SB + (uint32_t)g * pitch;
+    // Warp w takes half-blocks v = w, w + kComputeWarps, ...: v = (t*cb + b)*2 + U,
+    // walked with (t, rem = 2b + U) counters instead of divisions.
+    int t = 0, rem = warp;
+    while (rem >= 2 * cb) {
+      rem -= 2 * cb;
+      ++t;
+    }
+    for (int v = warp; ok && v < units; v += kComputeWarps) {
+      const int b = rem >> 1;
+      const uint32_t b0 = stg + (uint32_t)t * ten_bytes + (uint32_t)(b * kBB);
+      const uint32_t b1 = b0 + 8 * pitch;
+      const int blk = chunk * cb + b;
+      const uint32_t xa = xs + (uint32_t)blk * 512u, sxa = sxs + (uint32_t)blk * 64u;
+      float y0 = 0.f, y1 = 0.f;
+      if constexpr (QT == kQ4K) {
+        if (rem & 1)
+          q4_half<1>(b0, b1, xa, sxa, tig, y0, y1);
+        else
+          q4_half<0>(b0, b1, xa, sxa, tig, y0, y1);
+      } else {
+        // A block starts 2 mod 4 when b0 does (b1 = b0 + 8*pitch has the same
+        // alignment).  That is uniform over the warp unless K/256 is odd, so
+        // the alignment is picked per lane for the loads only, and the warp
+        // reconverges before the MMAs.
+        const bool a2 = (b0 & 3u) != 0;
+        Q6Half q;
+        if (rem & 1) {
+          if (a2)
+            q6_load_half<1, true>(b0, b1, tig, q);
+          else
+            q6_load_half<1, false>(b0, b1, tig, q);
+          __syncwarp();
+          q6_half<1>(q, xa, sxa, tig, y0, y1);
+        } else {
+          if (a2)
+            q6_load_half<0, true>(b0, b1, tig, q);
+          else
+            q6_load_half<0, false>(b0, b1, tig, q);
+          __syncwarp();
+          q6_half<0>(q, xa, sxa, tig, y0, y1);
+        }
+      }
+      if (t == 0) {
+        ya0 += y0;
+        ya1 += y1;
+      } else {
+        yb0 += y0;
+        yb1 += y1;
+      }
+      rem += kComputeWarps;
+      while (rem >= 2 * cb) {
+        rem -= 2 * cb;
+        ++t;
       }
     }
-    y0 += __shfl_xor_sync(0xffffffffu, y0, 1);
-    y0 += __shfl_xor_sync(0xffffffffu, y0, 2);
-    y1 += __shfl_xor_sync(0xffffffffu, y1, 1);
-    y1 += __shfl_xor_sync(0xffffffffu, y1, 2);
-    if (tig == 0) {
-      red[warp * 16 + g] = y0;
-      red[warp * 16 + g + 8] = y1;
-    }
-    __syncthreads();
-    if (!gu) {
-      if (threadIdx.x < 16 * tpc) {
-        const int t = threadIdx.x >> 4, r = threadIdx.x & 15;
-        float acc = 0.f;
-        for (int w = 0; w < ks; ++w) acc += red[(t * ks + w) * 16 + r];
-        const int row = (u * tpc + t) * 16 + r;
-        if (row < N) static_cast<float*>(P.y)[row] = acc;
+    __syncwarp();
+    if (ok && lane == 0) mbar_arrive(&sh->empty[s]);
+    if (chunk == nchunks - 1) {  // tile done: reduce over lanes, then warps
+      const int par = (st / nchunks) & 1;
+      for (int t = 0; t < nten; ++t) {
+        float a = t ? yb0 : ya0, c = t ? yb1 : ya1;
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        a += __shfl_xor_sync(0xffffffffu, a, 2);
+        c += __shfl_xor_sync(0xffffffffu, c, 1);
+        c += __shfl_xor_sync(0xffffffffu, c, 2);
+        if (tig == 0) {
+          sh->red[par][warp][t][g] = a;
+          sh->red[par][warp][t][g + 8] = c;
+        }
       }
-    } else if (threadIdx.x < 16) {
-      const int r = threadIdx.x;
-      float gs = 0.f, us = 0.f;
-      for (int w = 0; w < ks; ++w) {
-        gs += red[w * 16 + r];
-        us += red[(ks + w) * 16 + r];
+      ya0 = ya1 = yb0 = yb1 = 0.f;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+      if (warp == 0 && lane < 16) {
+        const int n = tile * 16 + lane;
+        float gs = 0.f, us = 0.f;
+        for (int w = 0; w < kComputeWarps; ++w) gs += sh->red[par][w][0][lane];
+        if (n < N) {
+          if (P.kind == 1) {
+            for (int w = 0; w < kComputeWarps; ++w) us += sh->red[par][w][1][lane];
+            static_cast<__half*>(P.y)[n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
+          } else {
+            static_cast<float*>(P.y)[n] = gs;
+          }
+        }
       }
-      const int row = u * 16 + r;
-      if (row < N) static_cast<__half*>(P.y)[row] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
+      // red[par] is reused two tiles later, after the next tile's barrier.
     }
-    __syncthreads();
   }
 }
 
-__global__ void __maxnreg__(128) gemv_batch_kernel(const __grid_constant__ GemvBatch B) {
-  extern __shared__ __align__(16) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_constant__ GemvBatch B) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   int i = 0;
   while (i + 1 < B.count && (int)blockIdx.x >= B.p[i + 1].cta_begin) ++i;
   const GemvProb& P = B.p[i];
   const int cta = (int)blockIdx.x - P.cta_begin;
+  int kmax = 0;
+  for (int j = 0; j < B.count; ++j) kmax = max(kmax, B.p[j].K);
+  const uint32_t x_bytes = ((uint32_t)(2 * kmax + kmax / 4) + 127u) & ~127u;
+  uint8_t* stages = smem + x_bytes;
+  GemvShared* sh = reinterpret_cast<GemvShared*>(stages + (size_t)B.stages * B.stage_bytes);
+  if (threadIdx.x < (unsigned)B.stages) {
+    mbar_init(&sh->full[threadIdx.x], 1);
+    mbar_init(&sh->empty[threadIdx.x], kComputeWarps);
+  }
+  if (threadIdx.x == 0) sh->abort_flag = 0;
+  fence_mbar_init();
+  __syncthreads();
+  // x staging by the compute warps only (the producer starts streaming at once):
+  // xp[k/4] = { fp16x2(x[k], x[k+2]), fp16x2(x[k+1], x[k+3]) }, the MMA k-slot
+  // order of the quant words, and sx16[i] = sum of x[16i .. 16i+15] in fp32.
+  if (threadIdx.x < 32 * kComputeWarps) {
+    const int nq = P.K / 4;
+    uint2* xp = reinterpret_cast<uint2*>(smem);
+    float* sx16 = reinterpret_cast<float*>(smem + 2 * P.K);
+    for (int q = threadIdx.x; q < nq; q += 32 * kComputeWarps) {
+      const uint2 v = *reinterpret_cast<const uint2*>(P.x + 4 * q);
+      uint2 o;
+      o.x = prmt(v.x, v.y, 0x5410u);
+      o.y = prmt(v.x, v.y, 0x7632u);
+      xp[q] = o;
+      float s = (half_lo(v.x) + half_lo(v.x >> 16)) + (half_lo(v.y) + half_lo(v.y >> 16));
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      if ((q & 3) == 0) sx16[q >> 2] = s;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+  }
   if (P.qtype == kQ4K)
-    run_gemv_problem<kQ4K>(P, cta, smem);
+    run_gemv_problem<kQ4K>(P, cta, B, smem, stages, sh);
   else
-    run_gemv_problem<kQ6K>(P, cta, smem);
+    run_gemv_problem<kQ6K>(P, cta, B, smem, stages, sh);
 }
 
 int g_sms = 0;
@@ -440,21 +525,29 @@ uint32_t gemv_take_status() {
   return v;
 }
 
-// Launch one grouped GEMV.  ks = the largest of 8, 4, 2, 1 dividing the block
-// count (gate/up: at most 4, so a CTA holds one gate and one up tile).  CTAs:
-// two per SM (256 threads x 128 registers), split across problems in
+// Launch one grouped GEMV.  Stage = 16 rows x cb blocks per weight tensor: the
+// whole row (cb = K/256) when at least three such stages fit in shared
+// memory, else the largest multiple of 8 blocks (8 x 210 B is 16-byte aligned)
+// dividing K/256 that gives three stages; all problems of a launch share the
+// stage size and depth.  CTAs (one per SM) split across problems in
 // proportion to their weight bytes.
 cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
+  if (count <= 0 || count > kMaxGemvProbs) return cudaErrorInvalidValue;
+  constexpr size_t kSmem = 227 * 1024;
   GemvBatch B;
   memset(&B, 0, sizeof(B));
   B.count = count;
+  int kmax = 0;
+  for (int i = 0; i < count; ++i) kmax = std::max<int>(kmax, (int)d[i].K);
+  const size_t x_bytes = ((size_t)(2 * kmax + kmax / 4) + 127) / 128 * 128;
+  const size_t avail = kSmem - x_bytes - sizeof(GemvShared) - 256;
   double total = 0;
   int64_t bytes[kMaxGemvProbs];
-  size_t smem = 0;
+  size_t stage = 0;
   for (int i = 0; i < count; ++i) {
     GemvProb& P = B.p[i];
-    P.w0 = static_cast<const uint8_t*>(d[i].w0);
-    P.w1 = static_cast<const uint8_t*>(d[i].w1);
+    P.w[0] = static_cast<const uint8_t*>(d[i].w0);
+    P.w[1] = static_cast<const uint8_t*>(d[i].w1);
     P.x = d[i].x;
     P.y = d[i].y;
     P.N = (int)d[i].N;
@@ -462,40 +555,41 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     P.qtype = d[i].qtype;
     P.kind = d[i].w1 ? 1 : 0;
     const int nb = P.K / kQK;
-    int ks = 1;
-    for (int c = (P.kind ? 4 : 8); c >= 1; c /= 2)
-      if (nb % c == 0) {
-        ks = c;
-        break;
-      }
-    if (P.kind) {
-      if (nb % 4) return cudaErrorInvalidValue;  // gate/up needs one gate + one up tile per CTA
-      ks = 4;
+    const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
+    const int nten = 1 + P.kind;
+    const int64_t RB = (int64_t)nb * bb;
+    int cb = nb;
+    if ((size_t)3 * 16 * nten * nb * bb > avail) {
+      cb = 0;
+      for (int c = 8; c <= nb; c += 8)
+        if (nb % c == 0 && (size_t)3 * 16 * nten * c * bb <= avail && (RB % 16) == 0) cb = c;
+      if (cb == 0) cb = nb;  // fall back to whole rows with fewer stages
     }
-    P.ks = ks;
-    const int tpc = kGemvWarps / ks;
-    const int ntiles = (P.N + 15) / 16;
-    P.units = P.kind ? ntiles : (ntiles + tpc - 1) / tpc;
-    bytes[i] = (int64_t)P.N * nb * (P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes) * (P.kind ? 2 : 1);
+    P.cb = cb;
+    stage = std::max(stage, ((size_t)16 * nten * cb * bb + 127) / 128 * 128);
+    P.tiles = (P.N + 15) / 16;
+    bytes[i] = (int64_t)P.N * RB * nten;
     total += (double)bytes[i];
-    smem = std::max(smem, (size_t)2 * P.K + (size_t)P.K / 4 + (size_t)kGemvWarps * 16 * sizeof(float));
   }
-  const int budget = std::max(count, sm_count() * 2);
+  B.stage_bytes = (uint32_t)stage;
+  B.stages = (int)std::min<size_t>(kMaxStages, avail / stage);
+  if (B.stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = x_bytes + (size_t)B.stages * stage + sizeof(GemvShared) + 128;
+  const int budget = std::max(count, sm_count());
   int used = 0;
   for (int i = 0; i < count; ++i) {
     int c = (int)((double)budget * (double)bytes[i] / total);
-    c = std::max(1, std::min(c, B.p[i].units));
+    c = std::max(1, std::min(c, B.p[i].tiles));
     B.p[i].ctas = c;
     used += c;
   }
-  // Hand leftover CTAs to the problems with the most units per CTA.
-  for (bool again = true; again && used < budget;) {
+  for (bool again = true; again && used < budget;) {  // leftover CTAs to the busiest problems
     again = false;
     int best = -1;
-    double best_load = 1.0;
+    double best_load = 0.0;
     for (int i = 0; i < count; ++i) {
-      const double load = (double)B.p[i].units / B.p[i].ctas;
-      if (B.p[i].ctas < B.p[i].units && load > best_load) {
+      const double load = (double)bytes[i] / B.p[i].ctas;
+      if (B.p[i].ctas < B.p[i].tiles && load > best_load) {
         best_load = load;
         best = i;
       }
@@ -511,11 +605,13 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     B.p[i].cta_begin = begin;
     begin += B.p[i].ctas;
   }
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_batch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
+    attr = true;
   }
-  gemv_batch_kernel<<<begin, 32 * kGemvWarps, smem, s>>>(B);
+  gemv_stream_kernel<<<begin, kThreads, smem, s>>>(B);
   return cudaGetLastError();
 }
 
