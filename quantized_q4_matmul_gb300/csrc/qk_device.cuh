@@ -275,8 +275,13 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t mask, uint32_t orv) {
-  return (a & mask) | orv;
+// (a & MASK) | orv in one LOP3 (orv held in a register): written out because
+// the compiler otherwise splits the two 32-bit constants into two logic ops.
+template <uint32_t MASK>
+__device__ __forceinline__ uint32_t lop_and_or(uint32_t a, uint32_t orv) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "r"(orv));
+  return d;
 }
 
 }  // namespace qk

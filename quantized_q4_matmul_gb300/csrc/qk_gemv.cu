@@ -117,8 +117,8 @@ __device__ __forceinline__ float pick4(float v0, float v1, float v2, float v3, i
 // j = 4U + tig of both rows.
 // ---------------------------------------------------------------------------
 template <int U>
-__device__ __forceinline__ void q4_half(uint32_t b0, uint32_t b1, uint32_t xa, uint32_t sxa, int tig, float& y0,
-                                        float& y1) {
+__device__ __forceinline__ void q4_half(uint32_t b0, uint32_t b1, uint32_t xa, uint32_t sxa, int tig, uint32_t magic,
+                                        float& y0, float& y1) {
   float D[2][2][4];  // [G - 2U][lo, hi][mma regs]
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -132,10 +132,12 @@ __device__ __forceinline__ void q4_half(uint32_t b0, uint32_t b1, uint32_t xa, u
     for (int hh = 0; hh < 2; ++hh) {
       const uint32_t v0 = hh ? w0.y : w0.x, v1 = hh ? w1.y : w1.x;
       const uint32_t s0 = v0 >> 8, s1 = v1 >> 8;
-      mma16816(c, (v0 & 0x000F000Fu) | kMagic, (v1 & 0x000F000Fu) | kMagic, (s0 & 0x000F000Fu) | kMagic,
-               (s1 & 0x000F000Fu) | kMagic, hh ? xlo.z : xlo.x, hh ? xlo.w : xlo.y);
-      mma16816(e, (v0 & 0x00F000F0u) | kMagic, (v1 & 0x00F000F0u) | kMagic, (s0 & 0x00F000F0u) | kMagic,
-               (s1 & 0x00F000F0u) | kMagic, hh ? xhi.z : xhi.x, hh ? xhi.w : xhi.y);
+      mma16816(c, lop_and_or<0x000F000Fu>(v0, magic), lop_and_or<0x000F000Fu>(v1, magic),
+               lop_and_or<0x000F000Fu>(s0, magic), lop_and_or<0x000F000Fu>(s1, magic), hh ? xlo.z : xlo.x,
+               hh ? xlo.w : xlo.y);
+      mma16816(e, lop_and_or<0x00F000F0u>(v0, magic), lop_and_or<0x00F000F0u>(v1, magic),
+               lop_and_or<0x00F000F0u>(s0, magic), lop_and_or<0x00F000F0u>(s1, magic), hh ? xhi.z : xhi.x,
+               hh ? xhi.w : xhi.y);
     }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -181,16 +183,17 @@ __device__ __forceinline__ void q4_half(uint32_t b0, uint32_t b1, uint32_t xa, u
 // (g6 >= 2: nibble in bits 4-7, high bits moved to 8-9).  Lane tig scales
 // groups 8H + tig and 8H + 4 + tig of both rows.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void q6k_operands(uint32_t wl, uint32_t wh, int g6, uint32_t& r0, uint32_t& r2) {
+__device__ __forceinline__ void q6k_operands(uint32_t wl, uint32_t wh, int g6, uint32_t magic, uint32_t& r0,
+                                             uint32_t& r2) {
   const uint32_t wl8 = wl >> 8;
   const uint32_t up = (g6 & 1) ? (wh << 2) : (wh << 4);
   const uint32_t dn = (g6 & 1) ? (wh >> 6) : (wh >> 4);
   if (g6 < 2) {
-    r0 = (wl & 0x000F000Fu) | (up & 0x00300030u) | kMagic;
-    r2 = (wl8 & 0x000F000Fu) | (dn & 0x00300030u) | kMagic;
+    r0 = lop_and_or<0x000F000Fu>(wl, lop_and_or<0x00300030u>(up, magic));
+    r2 = lop_and_or<0x000F000Fu>(wl8, lop_and_or<0x00300030u>(dn, magic));
   } else {
-    r0 = (wl & 0x00F000F0u) | (up & 0x03000300u) | kMagic;
-    r2 = (wl8 & 0x00F000F0u) | (dn & 0x03000300u) | kMagic;
+    r0 = lop_and_or<0x00F000F0u>(wl, lop_and_or<0x03000300u>(up, magic));
+    r2 = lop_and_or<0x00F000F0u>(wl8, lop_and_or<0x03000300u>(dn, magic));
   }
 }
 
@@ -226,15 +229,16 @@ __device__ __forceinline__ void q6_load_half(uint32_t b0, uint32_t b1, int tig, 
 }
 
 template <int H>
-__device__ __forceinline__ void q6_half(const Q6Half& q, uint32_t xa, uint32_t sxa, int tig, float& y0, float& y1) {
+__device__ __forceinline__ void q6_half(const Q6Half& q, uint32_t xa, uint32_t sxa, int tig, uint32_t magic, float& y0,
+                                        float& y1) {
   float d0[8], d1[8];
 #pragma unroll
   for (int tt = 0; tt < 8; ++tt) {
     const int g6 = (tt >> 1) & 3, s = tt & 1;
     const int li = 2 * (g6 & 1) + s;
     uint32_t a0, a2, a1, a3;
-    q6k_operands(q.ql0[li], q.qh0[s], g6, a0, a2);
-    q6k_operands(q.ql1[li], q.qh1[s], g6, a1, a3);
+    q6k_operands(q.ql0[li], q.qh0[s], g6, magic, a0, a2);
+    q6k_operands(q.ql1[li], q.qh1[s], g6, magic, a1, a3);
     const uint2 bx = lds64(xa + 8 * (4 * (8 * H + tt) + tig));
     float c[4] = {0.f, 0.f, 0.f, 0.f};
     mma16816(c, a0, a1, a2, a3, bx.x, bx.y);
@@ -267,7 +271,9 @@ __device__ __forceinline__ void q6_half(const Q6Half& q, uint32_t xa, uint32_t s
 #define QK_GEMV_WARPS 12
 #endif
 constexpr int kComputeWarps = QK_GEMV_WARPS;
-constexpr int kThreads = 32 * (kComputeWarps + 1);  // + one producer warp
+constexpr int kProducerWarp = kComputeWarps;      // streams the weights (and x)
+constexpr int kReducerWarp = kComputeWarps + 1;       // sums the compute warps' partials per tile
+constexpr int kThreads = 32 * (kComputeWarps + 2);
 constexpr int kMaxStages = 8;
 
 struct GemvProb {
@@ -289,6 +295,9 @@ struct GemvBatch {
 struct GemvShared {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint64_t x_full;                     // x copied into shared memory
+  uint64_t red_full[2];                // every compute warp wrote its partials of a tile (by parity)
+  uint64_t red_free[2];                // the reducer has consumed them
   float red[2][kComputeWarps][2][16];  // [tile parity][warp][tensor][row]
   uint32_t abort_flag;
 };
@@ -309,7 +318,7 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile uint32_t* abort_flag = &sh->abort_flag;
 
-  if (warp == kComputeWarps) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int st = 0;
@@ -349,18 +358,48 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
     return;
   }
 
+  if (warp == kReducerWarp) {
+    // ------------------------------------------------------------ reducer
+    // Tile i's partials sit in red[i & 1]; sum them over the compute warps in
+    // a fixed order (deterministic) and write y.
+    const int ntiles = t1 - t0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int par = i & 1;
+      if (!mbar_wait(&sh->red_full[par], (uint32_t)(i >> 1) & 1u, abort_flag, &g_gemv_status)) break;
+      if (lane < 16) {
+        const int n = (t0 + i) * 16 + lane;
+        float gs = 0.f, us = 0.f;
+        for (int w = 0; w < kComputeWarps; ++w) gs += sh->red[par][w][0][lane];
+        if (n < N) {
+          if (P.kind == 1) {
+            for (int w = 0; w < kComputeWarps; ++w) us += sh->red[par][w][1][lane];
+            static_cast<__half*>(P.y)[n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
+          } else {
+            static_cast<float*>(P.y)[n] = gs;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->red_free[par]);
+    }
+    return;
+  }
+
   // -------------------------------------------------------------- compute
   const uint32_t xs = smem_u32(smem);             // permuted x pairs, 8 bytes per 4 k
   const uint32_t sxs = smem_u32(smem + 2 * K);    // 16-wide sums of x
   const uint32_t ring = smem_u32(stages);
   const int g = lane >> 2, tig = lane & 3;
+  // fp16x2 (1024, 1024), kept in a register for the LOP3s that build the MMA operands
+  uint32_t magic;
+  asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
   const uint32_t pitch = (cb == nb) ? (uint32_t)RB : (uint32_t)(cb * kBB);  // bytes per row inside a stage
   const int units = 2 * nten * cb;  // half-blocks per stage
   float ya0 = 0.f, ya1 = 0.f, yb0 = 0.f, yb1 = 0.f;  // rows g, g+8 of tensor 0 (a) and 1 (b)
   bool ok = true;
   for (int st = 0; st < steps; ++st) {
     const int s = st % S;
-    const int tile = t0 + st / nchunks, chunk = st % nchunks;
+    const int chunk = st % nchunks;
     // After a timed-out wait the warp skips the arithmetic but keeps taking
     // part in the per-tile named barrier below, so no compute warp is left
     // waiting there for one that gave up.
@@ -383,9 +422,9 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
       float y0 = 0.f, y1 = 0.f;
       if constexpr (QT == kQ4K) {
         if (rem & 1)
-          q4_half<1>(b0, b1, xa, sxa, tig, y0, y1);
+          q4_half<1>(b0, b1, xa, sxa, tig, magic, y0, y1);
         else
-          q4_half<0>(b0, b1, xa, sxa, tig, y0, y1);
+          q4_half<0>(b0, b1, xa, sxa, tig, magic, y0, y1);
       } else {
         // A block starts 2 mod 4 when b0 does (b1 = b0 + 8*pitch has the same
         // alignment).  That is uniform over the warp unless K/256 is odd, so
@@ -399,14 +438,14 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
           else
             q6_load_half<1, false>(b0, b1, tig, q);
           __syncwarp();
-          q6_half<1>(q, xa, sxa, tig, y0, y1);
+          q6_half<1>(q, xa, sxa, tig, magic, y0, y1);
         } else {
           if (a2)
             q6_load_half<0, true>(b0, b1, tig, q);
           else
             q6_load_half<0, false>(b0, b1, tig, q);
           __syncwarp();
-          q6_half<0>(q, xa, sxa, tig, y0, y1);
+          q6_half<0>(q, xa, sxa, tig, magic, y0, y1);
         }
       }
       if (t == 0) {
@@ -424,8 +463,12 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
     }
     __syncwarp();
     if (ok && lane == 0) mbar_arrive(&sh->empty[s]);
-    if (chunk == nchunks - 1) {  // tile done: reduce over lanes, then warps
-      const int par = (st / nchunks) & 1;
+    if (chunk == nchunks - 1) {  // tile done: reduce over lanes, hand the warp's partials to the reducer
+      const int ti = st / nchunks, par = ti & 1;
+      // red[par] was last used by tile ti - 2: wait until the reducer is done with it.
+      if (ti >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(&sh->red_free[par], (uint32_t)((ti >> 1) - 1) & 1u, abort_flag,
+                                               &g_gemv_status)) && ok;
       for (int t = 0; t < nten; ++t) {
         float a = t ? yb0 : ya0, c = t ? yb1 : ya1;
         a += __shfl_xor_sync(0xffffffffu, a, 1);
@@ -438,21 +481,8 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
         }
       }
       ya0 = ya1 = yb0 = yb1 = 0.f;
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
-      if (warp == 0 && lane < 16) {
-        const int n = tile * 16 + lane;
-        float gs = 0.f, us = 0.f;
-        for (int w = 0; w < kComputeWarps; ++w) gs += sh->red[par][w][0][lane];
-        if (n < N) {
-          if (P.kind == 1) {
-            for (int w = 0; w < kComputeWarps; ++w) us += sh->red[par][w][1][lane];
-            static_cast<__half*>(P.y)[n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
-          } else {
-            static_cast<float*>(P.y)[n] = gs;
-          }
-        }
-      }
-      // red[par] is reused two tiles later, after the next tile's barrier.
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh->red_full[par]);
     }
   }
 }
@@ -473,18 +503,31 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     mbar_init(&sh->full[threadIdx.x], 1);
     mbar_init(&sh->empty[threadIdx.x], kComputeWarps);
   }
-  if (threadIdx.x == 0) sh->abort_flag = 0;
+  if (threadIdx.x == 0) {
+    mbar_init(&sh->x_full, 1);
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(&sh->red_full[p], kComputeWarps);
+      mbar_init(&sh->red_free[p], 1);
+    }
+    sh->abort_flag = 0;
+  }
   fence_mbar_init();
   __syncthreads();
-  // x staging by the compute warps only (the producer starts streaming at once):
-  // xp[k/4] = { fp16x2(x[k], x[k+2]), fp16x2(x[k+1], x[k+3]) }, the MMA k-slot
-  // order of the quant words, and sx16[i] = sum of x[16i .. 16i+15] in fp32.
+  // x arrives with one bulk copy (the producer then streams the weights) and
+  // the compute warps rearrange it in place: xp[k/4] = { fp16x2(x[k], x[k+2]),
+  // fp16x2(x[k+1], x[k+3]) }, the MMA k-slot order of the quant words, and
+  // sx16[i] = sum of x[16i .. 16i+15] in fp32.
+  if (threadIdx.x == 32 * kProducerWarp) {
+    mbar_arrive_expect_tx(&sh->x_full, (uint32_t)(2 * P.K));
+    bulk_copy_g2s(smem, P.x, (uint32_t)(2 * P.K), &sh->x_full);
+  }
   if (threadIdx.x < 32 * kComputeWarps) {
+    mbar_wait(&sh->x_full, 0u, &sh->abort_flag, &g_gemv_status);
     const int nq = P.K / 4;
     uint2* xp = reinterpret_cast<uint2*>(smem);
     float* sx16 = reinterpret_cast<float*>(smem + 2 * P.K);
     for (int q = threadIdx.x; q < nq; q += 32 * kComputeWarps) {
-      const uint2 v = *reinterpret_cast<const uint2*>(P.x + 4 * q);
+      const uint2 v = xp[q];
       uint2 o;
       o.x = prmt(v.x, v.y, 0x5410u);
       o.y = prmt(v.x, v.y, 0x7632u);
