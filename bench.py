@@ -59,6 +59,41 @@ def prefill_flops():
     return 2.0 * PREFILL_M * (gate.N * gate.K + up.N * up.K + down.N * down.K + v.N * v.K)
 
 
+def step_config(world):
+    """The workload one step runs (the same for both arms)."""
+    return {"workload": "llama-3.2-3b linears: prefill M=1024 (gate/up+SwiGLU Q4_K, down Q6_K, attn_v Q6_K)"
+                        " + decode M=1 (one layer's 7 linears)",
+            "prefill_tokens": PREFILL_M, "decode_tokens": 1, "replicas": world,
+            "l2": "%d rotating input copies, %.0f MB read per step (> 129 MB L2)"
+                  % (N_COPIES, (decode_bytes() + 51.5e6 + 28e6) / 1e6)}
+
+
+def kernel_sources_sha():
+    """Hash of the CUDA sources, to tell whether stored ncu counters are current."""
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_q4_matmul_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(key):
+    """DRAM bytes per launch from an ncu capture (profiles/traffic.json), or None
+    if there is none or the kernels have changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(key)
+    if not e or d.get("sources_sha256") != kernel_sources_sha():
+        return None
+    return e.get("bytes_per_launch")
+
+
 def decode_linears():
     return synth.layer_linears(0)  # layer 0: down is Q6_K
 
@@ -390,11 +425,7 @@ def run_gpu(args, rank, world, dist):
     gu_flops = 2.0 * 2 * PREFILL_M * gate.N * gate.K
     gu_ms_med = local_res["gu_ms"]
     gu_ach = gu_flops / (gu_ms_med * 1e-3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as f:
-            traffic = json.load(f).get("gateup_swiglu_m1024")
+    traffic = measured_traffic("gateup_swiglu_m1024")
     return {
         "metric": METRIC,
         "value": tflops,
@@ -408,11 +439,7 @@ def run_gpu(args, rank, world, dist):
         "vs_baseline": None,
         "dtype": "f16 (q4_k/q6_k weights, fp32 accumulate)",
         "data": "synthetic (seeded Llama-3.2-3B-shaped Q4_K/Q6_K weights, fp16 N(0,1) activations)",
-        "config": {"workload": "llama-3.2-3b linears: prefill M=1024 (gate/up+SwiGLU Q4_K, down Q6_K, attn_v Q6_K)"
-                               " + decode M=1 (one layer's 7 linears)",
-                   "prefill_tokens": PREFILL_M, "decode_tokens": 1, "replicas": world,
-                   "l2": "%d rotating input copies, %.0f MB read per step (> 129 MB L2)"
-                         % (N_COPIES, (decode_bytes() + 51.5e6 + 28e6) / 1e6)},
+        "config": step_config(world),
         "frac_of_fp16_peak": tflops / world / pk["bf16_tflops"],
         "decode": {"metric": "decode GEMV HBM GB/s", "value": dec_gbs, "unit": "GB/s",
                    "frac_of_hbm": dec_gbs / world / pk["hbm_gbs"], "ms_per_layer": max_dec,
@@ -450,11 +477,36 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 0, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(ts), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
-        "config": {"workload": "llama-3.2-3b gate/up+SwiGLU prefill M=1024 (sampled output features)"},
+        "config": step_config(1),
         "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": r["cores"], "kind": "oracle",
                          "sample": r["sample"]},
         "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
+
+
+def run_profile(args):
+    """Run one call of the step five times on cuda:0 (a target for ncu -k ... -s 4 -c 1)."""
+    import torch
+    import quantized_q4_matmul_gb300 as qk
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    wl = Workload(torch, dev)
+    stream = torch.cuda.Stream(device=dev)
+    s = stream.cuda_stream
+    gate, _, down, v = prefill_linears()
+    d = wl.copies[0]
+    calls = {
+        "gateup": lambda: qk.qk_gateup_swiglu_q4k(d["gate"], d["up"], d["x_gu"], wl.y_gu, PREFILL_M, gate.N, gate.K, s),
+        "down": lambda: qk.qk_matmul_q6k(d["down"], d["x_down"], wl.y_down, PREFILL_M, down.N, down.K, s),
+        "v": lambda: qk.qk_matmul_q6k(d["v"], d["x_v"], wl.y_v, PREFILL_M, v.N, v.K, s),
+        "decode": lambda: wl.decode(qk, 0, s),
+    }
+    with torch.cuda.stream(stream):
+        for _ in range(5):
+            calls[args.profile]()
+    qk.qk_get_device_status(s)
+    torch.cuda.synchronize()
+    print("profiled %s: 5 calls" % args.profile)
 
 
 def main():
@@ -464,7 +516,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", choices=["gateup", "down", "v", "decode"],
+                    help="run one call of the step 5 times on one GPU and exit (for ncu)")
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     args.warmup = max(args.warmup, 3)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
