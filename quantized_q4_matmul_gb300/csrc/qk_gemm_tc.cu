@@ -67,8 +67,7 @@ struct Cfg {
   // Arrivals that complete an A stage: Q4_K threads each write half of every
   // step; Q6_K threads write two of every four steps in full.
   static constexpr int kAArrivals = QT == kQ4K ? 32 * kDqWarps : 32 * kDqWarps / 2;
-  // Packed-block stages (one super-block of the tile's rows each): 2 .. 4.
-  static constexpr int kMaxPStages = 4;
+  // Packed-block stages (one super-block of the tile's rows each): up to 4.
   static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : kBM * 224;  // one tensor, one stage
   static constexpr int kMaxStages = 8;
 };
@@ -113,6 +112,7 @@ struct Params {
   int M, N, K, BN;
   int stages;           // K-step pipeline depth S
   int pstages;          // packed-block pipeline depth P
+  int ksplit;           // CTAs of a cluster that split the K range of one tile (1 = no split)
   int q6_group;         // Q6_K: rows per tensor-map row (g: g * row_bytes % 16 == 0)
   int q6_rows_tma;      // Q6_K: rows covered by the tensor map, (N / g) * g
 };
@@ -315,6 +315,18 @@ __device__ __forceinline__ int dq_row(int t, int g) {
   }
 }
 
+// acc[i] += the 16 fp32 values at shared address src (fp32 bits in acc).
+__device__ __forceinline__ void add_partial16(uint32_t (&acc)[16], uint32_t src) {
+#pragma unroll
+  for (int i = 0; i < 16; i += 4) {
+    const uint4 v = lds128_u(src + 4 * i);
+    acc[i] = __float_as_uint(__uint_as_float(acc[i]) + __uint_as_float(v.x));
+    acc[i + 1] = __float_as_uint(__uint_as_float(acc[i + 1]) + __uint_as_float(v.y));
+    acc[i + 2] = __float_as_uint(__uint_as_float(acc[i + 2]) + __uint_as_float(v.z));
+    acc[i + 3] = __float_as_uint(__uint_as_float(acc[i + 3]) + __uint_as_float(v.w));
+  }
+}
+
 // The dequant threads' main loop.  Thread (row rho, PART) dequantizes, per
 // K step, half of the step's 64 weights of its row (Q4_K: the nibbles PART of
 // sub-block 2c + PART), or for Q6_K the two whole K steps 2*PART and
@@ -322,9 +334,9 @@ __device__ __forceinline__ int dq_row(int t, int g) {
 // into registers at once and the packed slot released before any
 // conversion, so the producer can refill it while the A tiles are written.
 template <int QT, bool GATEUP, bool AT, int PART>
-__device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bars* bars, int S, int P, int nb, int which,
-                                             int rho, uint32_t a_lane, uint32_t a_col0, int n0, int N, int q6g,
-                                             volatile uint32_t* abort_flag) {
+__device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bars* bars, int S, int P, int nb,
+                                             int kb_begin, int nkb, int which, int rho, uint32_t a_lane,
+                                             uint32_t a_col0, int n0, int N, int q6g, volatile uint32_t* abort_flag) {
   using C = Cfg<QT, GATEUP>;
   constexpr int kChunks = QT == kQ4K ? 4 : 8;  // 16-byte chunks of an A-tile row written per K step
   uint32_t off[kChunks];
@@ -333,9 +345,10 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
   const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
   int step = 0;
   bool ok = true;
-  for (int kb = 0; kb < nb && ok; ++kb) {
-    const int ps = kb % P;
-    ok = mbar_wait(&bars->p_full[ps], (uint32_t)(kb / P) & 1u, abort_flag, &g_gemm_status);
+  for (int i = 0; i < nkb && ok; ++i) {
+    const int kb = kb_begin + i;  // super-block of the row; i counts this CTA's pipeline slots
+    const int ps = i % P;
+    ok = mbar_wait(&bars->p_full[ps], (uint32_t)(i / P) & 1u, abort_flag, &g_gemm_status);
     if (!ok) break;
     const uint8_t* pst = smem + L.p_off + (ps * C::kNumB + which) * C::kPSlotBytes;
     if constexpr (QT == kQ4K) {
@@ -413,7 +426,11 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   const int n0 = blockIdx.x * kBM;
   const int m0 = blockIdx.y * p.BN;
   const int nb = p.K / kQK;
-  const int nsteps = nb * 4;
+  // Split K: CTA z of a cluster of p.ksplit takes super-blocks [kb_begin, kb_begin + nkb).
+  const int z = (int)blockIdx.z;
+  const int kb_begin = (int)((int64_t)z * nb / p.ksplit);
+  const int nkb = (int)((int64_t)(z + 1) * nb / p.ksplit) - kb_begin;
+  const int nsteps = nkb * 4;
   const int BN = p.BN;
   const uint32_t x_bytes = (uint32_t)BN * kBK * 2;
   constexpr int kPSlotBytes = C::kPSlotBytes;
@@ -448,6 +465,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
+  bool dq_ok = false;  // dequant warps: the accumulators are complete and readable
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
     if (lane == 0) {
@@ -457,9 +475,10 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     }
     int step = 0;
     bool ok = true;
-    for (int kb = 0; kb < nb && ok; ++kb) {
-      const int ps = kb % P;
-      const uint32_t pph = (uint32_t)(kb / P) & 1u;
+    for (int i = 0; i < nkb && ok; ++i) {
+      const int kb = kb_begin + i;
+      const int ps = i % P;
+      const uint32_t pph = (uint32_t)(i / P) & 1u;
       ok = mbar_wait(&bars->p_empty[ps], pph ^ 1u, abort_flag, &g_gemm_status);
       if (!ok) break;
       uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
@@ -582,56 +601,95 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     // With A in TMEM a warp may only write its own lane quarter (warp % 4).
     const int rho = AT ? 32 * (warp & 3) + lane : dq_row<QT>(t & 127, p.q6_group);
     const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    bool ok = part == 0 ? dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, S, P, nb, which, rho, a_lane, a_col0, n0, p.N,
+    bool ok = part == 0 ? dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, S, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0, p.N,
                                                           p.q6_group, abort_flag)
-                        : dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, S, P, nb, which, rho, a_lane, a_col0, n0, p.N,
+                        : dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, S, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0, p.N,
                                                           p.q6_group, abort_flag);
 
-    // -------------------------------------------------------------- epilogue
     if (ok) ok = mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status);
-    ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
-    if (ok) {
+    dq_ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
+  }
+
+  // ---------------------------------------------------------------- epilogue
+  // Dequant warp w reads TMEM lane quarter w % 4 (rows 32q .. 32q+31); the
+  // warps sharing a quarter split the BN / 16 column chunks.
+  const bool dq_warp = warp >= C::kDqWarp0;
+  const int q = warp & 3;
+  const int row = q * 32 + lane;
+  const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+  const int nchunks = BN / 16;
+  const int ngroups = C::kDqWarps / 4, grp = (warp - C::kDqWarp0) >> 2;
+  const int per = (nchunks + ngroups - 1) / ngroups;
+  const int c_begin = min(nchunks, grp * per), c_end = min(nchunks, c_begin + per);
+  // Split K: the partial tiles of CTAs 1 .. ksplit-1 go to CTA 0's shared
+  // memory ([peer][tensor][row][BN] fp32, in the stage region, free once every
+  // CTA's main loop is done), and CTA 0 adds them in a fixed order.
+  const uint32_t peer_buf = smem_u32(smem);
+  const int ksplit = GATEUP ? 1 : p.ksplit;  // the host splits K for single-tensor problems only
+  if (ksplit > 1) {
+    __syncwarp();        // each warp arrives converged (the cluster barrier is .aligned)
+    cluster_sync_all();  // every CTA of the cluster is past its main loop
+    if (dq_warp && dq_ok && z > 0) {
       tc_fence_after();
-      const int q = warp & 3;                 // TMEM lane quarter this warp may access
-      const int row = q * 32 + lane;
-      const int n = n0 + row;
-      const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-      const int nchunks = BN / 16;
-      // Warps with the same lane quarter split the columns.
-      const int ngroups = C::kDqWarps / 4, grp = (warp - C::kDqWarp0) >> 2;
-      const int per = (nchunks + ngroups - 1) / ngroups;
-      const int c_begin = min(nchunks, grp * per), c_end = min(nchunks, c_begin + per);
-      if constexpr (!GATEUP) {
-        float* y = static_cast<float*>(p.y);
-        for (int cc = c_begin; cc < c_end; ++cc) {
-          uint32_t r0[16], r1[16];  // even / odd K steps
-          tmem_ld16(lane_addr + (uint32_t)(16 * cc), r0);
-          tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), r1);
-          tmem_wait_ld();
-          if (n < p.N) {
+      const uint32_t dst0 = mapa_shared(peer_buf, 0u);
+      for (int cc = c_begin; cc < c_end; ++cc) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(lane_addr + (uint32_t)(16 * cc), r0);
+        tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), r1);
+        tmem_wait_ld();
+        // one tensor: D0 + D1 of the peer's tile; gate/up: g and u side by side
+        const uint32_t a = dst0 + (uint32_t)(((((z - 1) * C::kNumB) * 128 + row) * BN + 16 * cc) * 4);
+        if constexpr (!GATEUP) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int m = m0 + 16 * cc + i;
-              if (m < p.M) y[(int64_t)m * p.N + n] = __uint_as_float(r0[i]) + __uint_as_float(r1[i]);
-            }
-          }
+          for (int i = 0; i < 16; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __uint_as_float(r1[i]));
         }
-      } else {
-        __half* y = static_cast<__half*>(p.y);
-        for (int cc = c_begin; cc < c_end; ++cc) {
-          uint32_t rg[16], ru[16];
-          tmem_ld16(lane_addr + (uint32_t)(16 * cc), rg);
-          tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), ru);
-          tmem_wait_ld();
-          if (n < p.N) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int m = m0 + 16 * cc + i;
-              const float g = __uint_as_float(rg[i]);
-              const float u = __uint_as_float(ru[i]);
-              const float o = __fdividef(g, 1.0f + __expf(-g)) * u;  // silu(g) * u
-              if (m < p.M) y[(int64_t)m * p.N + n] = __float2half_rn(o);
-            }
+        for (int i = 0; i < 4; ++i)
+          st_cluster_v4(a + 16 * i, __uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
+                        __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
+        if constexpr (GATEUP) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            st_cluster_v4(a + (uint32_t)(128 * BN * 4) + 16 * i, __uint_as_float(r1[4 * i]),
+                          __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
+                          __uint_as_float(r1[4 * i + 3]));
+        }
+      }
+    }
+    __syncwarp();
+    cluster_sync_all();  // the partials are in CTA 0's shared memory
+  }
+  if (dq_warp && dq_ok && z == 0) {
+    tc_fence_after();
+    const int n = n0 + row;
+    for (int cc = c_begin; cc < c_end; ++cc) {
+      // ra / rb: one tensor's even / odd K steps, or gate / up (fp32 bits)
+      uint32_t ra[16], rb[16];
+      tmem_ld16(lane_addr + (uint32_t)(16 * cc), ra);
+      tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), rb);
+      tmem_wait_ld();
+#pragma unroll 1
+      for (int zz = 1; zz < ksplit; ++zz) {
+        const uint32_t src = peer_buf + (uint32_t)(((((zz - 1) * C::kNumB) * 128 + row) * BN + 16 * cc) * 4);
+        add_partial16(ra, src);
+        if constexpr (GATEUP) add_partial16(rb, src + (uint32_t)(128 * BN * 4));
+      }
+      if (n < p.N) {
+        if constexpr (!GATEUP) {
+          float* y = static_cast<float*>(p.y);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int m = m0 + 16 * cc + i;
+            if (m < p.M) y[(int64_t)m * p.N + n] = __uint_as_float(ra[i]) + __uint_as_float(rb[i]);
+          }
+        } else {
+          __half* y = static_cast<__half*>(p.y);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int m = m0 + 16 * cc + i;
+            const float g = __uint_as_float(ra[i]), u = __uint_as_float(rb[i]);
+            const float o = __fdividef(g, 1.0f + __expf(-g)) * u;  // silu(g) * u
+            if (m < p.M) y[(int64_t)m * p.N + n] = __float2half_rn(o);
           }
         }
       }
@@ -796,6 +854,7 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   }
   p.stages = S;
   p.pstages = P;
+  p.ksplit = 1;
   const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, S, P).total;
   if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   static bool attr_set = false;
@@ -807,8 +866,39 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   }
   dim3 grid((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + BN - 1) / BN));
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
-  gemm_tc_kernel<QT, GATEUP, AT><<<grid, C::kThreads, smem, stream>>>(tx, tw0, tw1, p);
-  return cudaGetLastError();
+  // Split K across a cluster when the tiles would leave at least half of the
+  // SMs idle (small N or small M): ks CTAs per tile, each with >= 1 super-block,
+  // the peers' fp32 partial tiles fitting in CTA 0's stage region.
+  int ks = 1;
+  if (!GATEUP) {
+    const int64_t tiles = (int64_t)grid.x * grid.y;
+    const Layout L = make_layout<QT, GATEUP, AT>(BN, S, P);
+    for (int c = 8; c >= 2; --c)
+      if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * kBM * BN * 4 <= L.bar_off) {
+        ks = c;
+        break;
+      }
+  }
+  p.ksplit = ks;
+  if (ks == 1) {
+    gemm_tc_kernel<QT, GATEUP, AT><<<grid, C::kThreads, smem, stream>>>(tx, tw0, tw1, p);
+    return cudaGetLastError();
+  }
+  grid.z = (unsigned)ks;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)ks;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<QT, GATEUP, AT>, tx, tw0, tw1, p);
 }
 
 }  // namespace
