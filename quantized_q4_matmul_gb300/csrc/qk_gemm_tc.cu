@@ -327,16 +327,17 @@ __device__ __forceinline__ void add_partial16(uint32_t (&acc)[16], uint32_t src)
   }
 }
 
-// The dequant threads' main loop.  Thread (row rho, PART) dequantizes, per
-// K step, half of the step's 64 weights of its row (Q4_K: the nibbles PART of
-// sub-block 2c + PART), or for Q6_K the two whole K steps 2*PART and
-// 2*PART + 1 of every super-block.  A super-block's packed bytes are loaded
+// The dequant threads' main loop.  Thread (row rho, half PART) dequantizes,
+// per K step, half of the step's 64 weights of its row (Q4_K: the nibbles PART
+// of sub-block 2c + PART), or for Q6_K the two whole K steps 2*part and
+// 2*part + 1 of every super-block (Q6_K uses the runtime `part`; PART is 0).  A super-block's packed bytes are loaded
 // into registers at once and the packed slot released before any
 // conversion, so the producer can refill it while the A tiles are written.
 template <int QT, bool GATEUP, bool AT, int PART>
 __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bars* bars, int S, int P, int nb,
                                              int kb_begin, int nkb, int which, int rho, uint32_t a_lane,
-                                             uint32_t a_col0, int n0, int N, int q6g, volatile uint32_t* abort_flag) {
+                                             uint32_t a_col0, int n0, int N, int q6g, int part,
+                                             volatile uint32_t* abort_flag) {
   using C = Cfg<QT, GATEUP>;
   constexpr int kChunks = QT == kQ4K ? 4 : 8;  // 16-byte chunks of an A-tile row written per K step
   uint32_t off[kChunks];
@@ -382,11 +383,11 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
       const int n = min(n0 + rho, N - 1);
       const int mis = (int)(((int64_t)n * RB + (int64_t)kb * kQ6KBytes) & 15);
       Q6Regs q;
-      q6_load_dispatch(mis, pst + q6_slot(rho, q6g), PART, q);
+      q6_load_dispatch(mis, pst + q6_slot(rho, q6g), part, q);
       mbar_arrive(&bars->p_empty[ps]);
 #pragma unroll
       for (int side = 0; side < 2; ++side) {
-        const int st = step + 2 * PART + side;
+        const int st = step + 2 * part + side;
         const int s = st % S;
         uint32_t r[32];
         if (side == 0)
@@ -601,10 +602,15 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     // With A in TMEM a warp may only write its own lane quarter (warp % 4).
     const int rho = AT ? 32 * (warp & 3) + lane : dq_row<QT>(t & 127, p.q6_group);
     const uint32_t a_lane = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    bool ok = part == 0 ? dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, S, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0, p.N,
-                                                          p.q6_group, abort_flag)
-                        : dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, S, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0, p.N,
-                                                          p.q6_group, abort_flag);
+    // Q4_K specialises on the nibble half (compile-time shifts); Q6_K takes the
+    // half as a runtime value (one copy of its larger code).
+    bool ok;
+    if (QT == kQ6K || part == 0)
+      ok = dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, S, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
+                                           p.N, p.q6_group, part, abort_flag);
+    else
+      ok = dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, S, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
+                                           p.N, p.q6_group, part, abort_flag);
 
     if (ok) ok = mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status);
     dq_ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld is warp-collective
