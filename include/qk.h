@@ -142,6 +142,17 @@ qk_status qk_matmul_batch(const qk_matmul_desc *descs, int count, qk_stream_t st
  */
 qk_status qk_get_device_status(qk_stream_t stream);
 
+/*
+ * Diagnostic for the failure path: enqueue on `stream` a kernel whose only
+ * wait can never complete (an mbarrier nothing arrives on).  Like every wait
+ * in the library's kernels it gives up after a wall-clock limit, here
+ * `limit_ns` (clamped to 1 us .. 1 s), raises the device status word and
+ * returns, so the next qk_get_device_status() reports QK_ERR_TIMEOUT and the
+ * CUDA context stays usable.  No fault, trap or unbounded wait is involved.
+ * Returns QK_ERR_UNSUPPORTED_DEVICE or QK_ERR_CUDA on launch problems.
+ */
+qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream);
+
 /* A static, human-readable name for a status code. */
 const char *qk_status_string(qk_status status);
 

@@ -14,15 +14,15 @@ import os
 
 __all__ = [
     "QKError", "lib", "lib_path", "qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k",
-    "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_get_device_status", "qk_status_string", "qk_version",
-    "QK_BLOCK_BYTES", "qk_matmul_desc",
+    "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout",
+    "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 QK_BLOCK_BYTES = {"q4k": 144, "q6k": 210}
 
 SYMBOLS = ("qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k", "qk_gateup_swiglu_q4k",
-           "qk_matmul_batch", "qk_get_device_status", "qk_status_string", "qk_version")
+           "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout", "qk_status_string", "qk_version")
 
 QK_Q4_K, QK_Q6_K = 0, 1
 
@@ -68,6 +68,7 @@ def lib():
         L.qk_matmul_batch.restype = i32
         L.qk_matmul_batch.argtypes = [ctypes.POINTER(qk_matmul_desc), i32, vp]
         L.qk_get_device_status.restype, L.qk_get_device_status.argtypes = i32, [vp]
+        L.qk_debug_wait_timeout.restype, L.qk_debug_wait_timeout.argtypes = i32, [i64, vp]
         L.qk_status_string.restype, L.qk_status_string.argtypes = ctypes.c_char_p, [i32]
         L.qk_version.restype, L.qk_version.argtypes = i32, []
         _lib = L
@@ -142,3 +143,8 @@ def qk_matmul_batch(problems, stream=None) -> None:
 
 def qk_get_device_status(stream=None) -> None:
     _check(lib().qk_get_device_status(_stream(stream)), "qk_get_device_status")
+
+
+def qk_debug_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Enqueue a kernel whose only wait times out after ``limit_ns`` (see include/qk.h)."""
+    _check(lib().qk_debug_wait_timeout(int(limit_ns), _stream(stream)), "qk_debug_wait_timeout")

@@ -230,6 +230,14 @@ qk_status qk_matmul_batch(const qk_matmul_desc* descs, int count, qk_stream_t st
   return matmul_batch(descs, count, reinterpret_cast<cudaStream_t>(stream));
 }
 
+qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream) {
+  qk_status st = check_device();
+  if (st != QK_OK) return st;
+  if (limit_ns < 1000) limit_ns = 1000;
+  if (limit_ns > 1000000000) limit_ns = 1000000000;
+  return map_cuda(qk::launch_wait_probe((uint64_t)limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 qk_status qk_get_device_status(qk_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QK_ERR_CUDA;
   const uint32_t v = qk::dequant_take_status() | qk::gemv_take_status() | qk::gemm_take_status();

@@ -106,7 +106,27 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) dequant_q6k_kernel(const ui
   }
 }
 
+// Diagnostic: one wait that can never complete (nothing arrives on the
+// barrier), bounded like every wait of the library's kernels.  After
+// `limit_ns` it raises the abort flag and this file's status word and returns.
+__global__ void wait_probe_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0u, &abort_flag, &g_dequant_status, false, limit_ns);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t s) {
+  wait_probe_kernel<<<1, 32, 0, s>>>(limit_ns);
+  return cudaGetLastError();
+}
 
 uint32_t dequant_take_status() {
   uint32_t v = 0, zero = 0;

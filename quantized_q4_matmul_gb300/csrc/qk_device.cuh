@@ -78,14 +78,15 @@ __device__ __forceinline__ uint64_t global_ns() {
 // or early if another thread of the CTA already aborted (unless
 // `ignore_abort`, used when draining copies that are still in flight).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
-                                          uint32_t* dev_status, bool ignore_abort = false) {
+                                          uint32_t* dev_status, bool ignore_abort = false,
+                                          uint64_t limit_ns = QK_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (!ignore_abort && *abort_flag) return false;
-      if (global_ns() - t0 > QK_WAIT_LIMIT_NS) break;
+      if (global_ns() - t0 > limit_ns) break;
     }
   }
   *abort_flag = 1u;

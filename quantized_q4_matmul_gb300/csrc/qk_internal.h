@@ -30,6 +30,9 @@ cudaError_t launch_gemv(QType t, const void* W, const uint16_t* x, float* y, int
 cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M,
                         int64_t N, int64_t K, bool gateup, cudaStream_t s);
 
+// A kernel whose single bounded wait can never complete (see qk_debug_wait_timeout).
+cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t s);
+
 // Largest M the decode GEMV handles; larger M goes to the tensor-core GEMM.
 int gemv_max_m();
 

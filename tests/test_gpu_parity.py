@@ -331,3 +331,28 @@ def test_gateup_decode_m1(qk_lib, cuda):
     qk_lib.qk_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), y, 1, N, K)
     qk_lib.qk_get_device_status()
     check_close_f16out(y.float().cpu().numpy().astype(np.float64), oracle.gateup_swiglu(Wg, Wu, x, N, K), "gu M1")
+
+
+# ---------------------------------------------------------------------------
+# Failure path: a bounded wait that runs out (no fault, no unbounded wait)
+# ---------------------------------------------------------------------------
+def test_wait_timeout_is_reported_and_the_context_stays_usable(qk_lib, cuda):
+    """A kernel whose only mbarrier wait can never complete gives up after its
+    wall-clock limit; the host reads QK_ERR_TIMEOUT, the status is cleared, and
+    the next call runs and checks out."""
+    import time
+    import torch
+    t0 = time.perf_counter()
+    qk_lib.qk_debug_wait_timeout(20_000_000)  # 20 ms
+    with pytest.raises(qk_lib.QKError) as e:
+        qk_lib.qk_get_device_status()
+    assert e.value.status == -5
+    assert time.perf_counter() - t0 >= 0.02
+    qk_lib.qk_get_device_status()  # read once, then cleared
+    rng = synth.rng_for(21, 0)
+    W = synth.q4k_weights(rng, 128, 512)
+    x = synth.activations(rng, 3, 512)
+    y = torch.empty(3, 128, dtype=torch.float32, device=cuda)
+    qk_lib.qk_matmul_q4k(_dev(W, cuda), _x_dev(x, cuda), y, 3, 128, 512)
+    qk_lib.qk_get_device_status()
+    check_close(y.cpu().numpy().astype(np.float64), oracle.matmul(QT["q4k"], W, x, 128, 512), "after timeout")
