@@ -165,6 +165,21 @@ class Clocks:
 # ----------------------------------------------------------------------------
 # CPU baseline: the oracle on a bounded sample
 # ----------------------------------------------------------------------------
+_CPU_INPUTS = []
+
+
+def _cpu_inputs():
+    """The prefill step's inputs for the oracle (generated once per process)."""
+    if not _CPU_INPUTS:
+        rng = synth.rng_for(7, 1)
+        gate, up, down, v = prefill_linears()
+        _CPU_INPUTS.extend([synth.q4k_weights(rng, gate.N, gate.K), synth.q4k_weights(rng, up.N, up.K),
+                            synth.q6k_weights(rng, down.N, down.K), synth.q6k_weights(rng, v.N, v.K),
+                            synth.activations(rng, PREFILL_M, gate.K),
+                            synth.swiglu_activations(rng, PREFILL_M, down.K)])
+    return _CPU_INPUTS
+
+
 def cpu_baseline(target_s: float = 12.0):
     """The oracle on host cores over a bounded sample of the prefill step: the
     same fraction f of the output features of each of its problems (gate/up +
@@ -172,14 +187,8 @@ def cpu_baseline(target_s: float = 12.0):
     of `target_s` (a short run overestimates the time per feature: fixed costs
     dominate it)."""
     import oracle
-    rng = synth.rng_for(7, 1)
     gate, up, down, v = prefill_linears()
-    Wg = synth.q4k_weights(rng, gate.N, gate.K)
-    Wu = synth.q4k_weights(rng, up.N, up.K)
-    Wd = synth.q6k_weights(rng, down.N, down.K)
-    Wv = synth.q6k_weights(rng, v.N, v.K)
-    xg = synth.activations(rng, PREFILL_M, gate.K)
-    xd = synth.swiglu_activations(rng, PREFILL_M, down.K)
+    Wg, Wu, Wd, Wv, xg, xd = _cpu_inputs()
 
     def run(f):
         rg, rd, rv = (max(1, min(n, int(round(f * n)))) for n in (gate.N, down.N, v.N))
