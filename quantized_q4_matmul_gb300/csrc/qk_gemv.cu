@@ -12,8 +12,8 @@
 //     cb-block chunk, one copy per row) with bulk asynchronous copies into a
 //     ring of 2..8 shared-memory stages; with 100+ KB in flight per SM the HBM
 //     latency is hidden without holding data in registers.
-//   * Arithmetic: 12 compute warps split a stage into half-blocks (16 rows x
-//     128 weights).  The inner products use the warp tensor instruction
+//   * Arithmetic: 12 compute warps split a stage into blocks (16 rows x 256
+//     weights; the two 128-weight halves are independent straight-line code).  The inner products use the warp tensor instruction
 //     mma.sync m16n8k16 (fp16 x fp16, fp32 accumulate) as a dot-product
 //     engine: a 4-bit quant OR-ed into the mantissa of fp16 1024.0 is the exact
 //     value 1024 + F*q (F = 1 or 16 by nibble position, no shifts), its product
@@ -23,8 +23,7 @@
 //       sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + dmin*m)        (Q4_K)
 //       sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + 32*d*sc)       (Q6_K)
 //     with Sx the sub-block's sum of x.  Lane tig (0..3) applies the scales
-//     of one quarter of the half-block's sub-blocks, so no scale is decoded
-//     twice.  A k-permuted fp16 copy of x and the sums Sx are staged once per
+//     of one quarter of each half's sub-blocks, so no scale is decoded twice.  A k-permuted fp16 copy of x and the sums Sx are staged once per
 //     CTA in shared memory.
 //   * Reduction: partial sums meet in two shuffles and one fixed-order pass
 //     over the compute warps per tile (deterministic).
@@ -266,7 +265,7 @@ __device__ __forceinline__ void q6_half(const Q6Half& q, uint32_t xa, uint32_t s
 // The kernel
 // ---------------------------------------------------------------------------
 // Compute warps per CTA (measured on GB300: 12 beat 8 and 16 on the decode
-// layer; a K = 3072 tile is 24 half-blocks, two per warp).
+// layer; a K = 3072 tile is 12 blocks, one per warp).
 #ifndef QK_GEMV_WARPS
 #define QK_GEMV_WARPS 12
 #endif
@@ -394,70 +393,56 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
   uint32_t magic;
   asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
   const uint32_t pitch = (cb == nb) ? (uint32_t)RB : (uint32_t)(cb * kBB);  // bytes per row inside a stage
-  const int units = 2 * nten * cb;  // half-blocks per stage
   float ya0 = 0.f, ya1 = 0.f, yb0 = 0.f, yb1 = 0.f;  // rows g, g+8 of tensor 0 (a) and 1 (b)
   bool ok = true;
   for (int st = 0; st < steps; ++st) {
     const int s = st % S;
     const int chunk = st % nchunks;
-    // After a timed-out wait the warp skips the arithmetic but keeps taking
-    // part in the per-tile named barrier below, so no compute warp is left
-    // waiting there for one that gave up.
+    // After a timed-out wait the warp skips the arithmetic but still hands its
+    // partials of every tile to the reducer, so the reducer is not left waiting.
     if (ok)
       ok = __all_sync(0xffffffffu, mbar_wait(&sh->full[s], (uint32_t)(st / S) & 1u, abort_flag, &g_gemv_status));
     const uint32_t stg = ring + (uint32_t)s * SB + (uint32_t)g * pitch;
-    // Warp w takes half-blocks v = w, w + kComputeWarps, ...: v = (t*cb + b)*2 + U,
-    // walked with (t, rem = 2b + U) counters instead of divisions.
-    int t = 0, rem = warp;
-    while (rem >= 2 * cb) {
-      rem -= 2 * cb;
+    // Warp w takes whole blocks v = w, w + kComputeWarps, ...: v = t*cb + b; both
+    // halves of a block are independent straight-line work (more ILP per warp).
+    int t = 0, b = warp;
+    while (b >= cb) {
+      b -= cb;
       ++t;
     }
-    for (int v = warp; ok && v < units; v += kComputeWarps) {
-      const int b = rem >> 1;
+    for (int v = warp; ok && v < nten * cb; v += kComputeWarps) {
       const uint32_t b0 = stg + (uint32_t)t * ten_bytes + (uint32_t)(b * kBB);
       const uint32_t b1 = b0 + 8 * pitch;
       const int blk = chunk * cb + b;
       const uint32_t xa = xs + (uint32_t)blk * 512u, sxa = sxs + (uint32_t)blk * 64u;
-      float y0 = 0.f, y1 = 0.f;
+      float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
       if constexpr (QT == kQ4K) {
-        if (rem & 1)
-          q4_half<1>(b0, b1, xa, sxa, tig, magic, y0, y1);
-        else
-          q4_half<0>(b0, b1, xa, sxa, tig, magic, y0, y1);
+        q4_half<0>(b0, b1, xa, sxa, tig, magic, y0, y1);
+        q4_half<1>(b0, b1, xa, sxa, tig, magic, z0, z1);
       } else {
-        // A block starts 2 mod 4 when b0 does (b1 = b0 + 8*pitch has the same
-        // alignment).  That is uniform over the warp unless K/256 is odd, so
-        // the alignment is picked per lane for the loads only, and the warp
-        // reconverges before the MMAs.
         const bool a2 = (b0 & 3u) != 0;
-        Q6Half q;
-        if (rem & 1) {
-          if (a2)
-            q6_load_half<1, true>(b0, b1, tig, q);
-          else
-            q6_load_half<1, false>(b0, b1, tig, q);
-          __syncwarp();
-          q6_half<1>(q, xa, sxa, tig, magic, y0, y1);
+        Q6Half q, r;
+        if (a2) {
+          q6_load_half<0, true>(b0, b1, tig, q);
+          q6_load_half<1, true>(b0, b1, tig, r);
         } else {
-          if (a2)
-            q6_load_half<0, true>(b0, b1, tig, q);
-          else
-            q6_load_half<0, false>(b0, b1, tig, q);
-          __syncwarp();
-          q6_half<0>(q, xa, sxa, tig, magic, y0, y1);
+          q6_load_half<0, false>(b0, b1, tig, q);
+          q6_load_half<1, false>(b0, b1, tig, r);
         }
+        __syncwarp();
+        q6_half<0>(q, xa, sxa, tig, magic, y0, y1);
+        q6_half<1>(r, xa, sxa, tig, magic, z0, z1);
       }
       if (t == 0) {
-        ya0 += y0;
-        ya1 += y1;
+        ya0 += y0 + z0;
+        ya1 += y1 + z1;
       } else {
-        yb0 += y0;
-        yb1 += y1;
+        yb0 += y0 + z0;
+        yb1 += y1 + z1;
       }
-      rem += kComputeWarps;
-      while (rem >= 2 * cb) {
-        rem -= 2 * cb;
+      b += kComputeWarps;
+      while (b >= cb) {
+        b -= cb;
         ++t;
       }
     }
