@@ -282,15 +282,18 @@ struct GemvProb {
   int N, K, qtype, kind;
   int pair;         // one tensor, whole rows: a stage holds two adjacent 16-row tiles (as two "tensors")
   int cb;           // K blocks per chunk (a stage holds 16 rows x cb blocks per weight tensor)
+  int stages;       // pipeline depth of this problem's CTAs
+  uint32_t stage_bytes;
   int tiles, cta_begin, ctas;
 };
 
 struct GemvBatch {
   GemvProb p[kMaxGemvProbs];
   int count;
-  int stages;       // pipeline depth (same for every problem of the launch)
-  uint32_t stage_bytes;
 };
+
+struct GemvShared;
+constexpr uint32_t round128(size_t v) { return (uint32_t)((v + 127) / 128 * 128); }
 
 struct GemvShared {
   uint64_t full[kMaxStages];
@@ -301,6 +304,8 @@ struct GemvShared {
   float red[2][kComputeWarps][2][16];  // [tile parity][warp][tensor][row]
   uint32_t abort_flag;
 };
+constexpr uint32_t kSharedBytes = round128(sizeof(GemvShared));
+
 
 template <int QT>
 __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, const GemvBatch& B, uint8_t* smem,
@@ -315,8 +320,8 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
   const int nchunks = nb / cb;  // the host makes cb divide nb
   const int t0 = (int)((int64_t)cta * P.tiles / P.ctas), t1 = (int)((int64_t)(cta + 1) * P.tiles / P.ctas);
   const int steps = (t1 - t0) * nchunks;
-  const int S = B.stages;
-  const uint32_t SB = B.stage_bytes;
+  const int S = P.stages;
+  const uint32_t SB = P.stage_bytes;
   const uint32_t ten_bytes = (uint32_t)(16 * cb * kBB);  // one tensor's share of a stage
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   volatile uint32_t* abort_flag = &sh->abort_flag;
@@ -502,9 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
   int kmax = 0;
   for (int j = 0; j < B.count; ++j) kmax = max(kmax, B.p[j].K);
   const uint32_t x_bytes = ((uint32_t)(2 * kmax + kmax / 4) + 127u) & ~127u;
-  uint8_t* stages = smem + x_bytes;
-  GemvShared* sh = reinterpret_cast<GemvShared*>(stages + (size_t)B.stages * B.stage_bytes);
-  if (threadIdx.x < (unsigned)B.stages) {
+  // [x | barriers and partial sums | ring of this problem's stages]
+  GemvShared* sh = reinterpret_cast<GemvShared*>(smem + x_bytes);
+  uint8_t* stages = smem + x_bytes + kSharedBytes;
+  if (threadIdx.x < (unsigned)P.stages) {
     mbar_init(&sh->full[threadIdx.x], 1);
     mbar_init(&sh->empty[threadIdx.x], kComputeWarps);
   }
@@ -573,11 +579,8 @@ uint32_t gemv_take_status() {
   return v;
 }
 
-// Launch one grouped GEMV.  Stage = 16 rows x cb blocks per weight tensor: the
-// whole row (cb = K/256) when at least three such stages fit in shared
-// memory, else the largest multiple of 8 blocks (8 x 210 B is 16-byte aligned)
-// dividing K/256 that gives three stages; all problems of a launch share the
-// stage size and depth.  CTAs (one per SM) split across problems in
+// Launch one grouped GEMV.  Each problem gets its own stage geometry (its
+// CTAs carve their own ring); CTAs (one per SM) split across problems in
 // proportion to their weight bytes.
 cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
   if (count <= 0 || count > kMaxGemvProbs) return cudaErrorInvalidValue;
@@ -588,10 +591,10 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
   int kmax = 0;
   for (int i = 0; i < count; ++i) kmax = std::max<int>(kmax, (int)d[i].K);
   const size_t x_bytes = ((size_t)(2 * kmax + kmax / 4) + 127) / 128 * 128;
-  const size_t avail = kSmem - x_bytes - sizeof(GemvShared) - 256;
+  const size_t avail = kSmem - x_bytes - kSharedBytes - 128;  // for one CTA's ring
   double total = 0;
   int64_t bytes[kMaxGemvProbs];
-  size_t stage = 0;
+  size_t ring = 0;
   for (int i = 0; i < count; ++i) {
     GemvProb& P = B.p[i];
     P.w[0] = static_cast<const uint8_t*>(d[i].w0);
@@ -602,11 +605,13 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     P.K = (int)d[i].K;
     P.qtype = d[i].qtype;
     P.kind = d[i].w1 ? 1 : 0;
-    P.pair = 0;
     const int nb = P.K / kQK;
     const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
     const int nten = 1 + P.kind;
     const int64_t RB = (int64_t)nb * bb;
+    // Stage: whole rows (cb = K/256) when three stages fit, else the largest
+    // multiple of 8 blocks (8 x 210 B is 16-byte aligned) dividing K/256 that
+    // gives three stages.
     int cb = nb;
     if ((size_t)3 * 16 * nten * nb * bb > avail) {
       cb = 0;
@@ -615,32 +620,20 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
       if (cb == 0) cb = nb;  // fall back to whole rows with fewer stages
     }
     P.cb = cb;
-    stage = std::max(stage, ((size_t)16 * nten * cb * bb + 127) / 128 * 128);
+    // One tensor with whole rows: two adjacent tiles per stage (halves the
+    // per-block share of the per-tile reduction) when two such stages fit
+    // (measured on GB300: the Q6_K LM head streams ~15 % faster with two
+    // paired stages than with five single ones).
+    P.pair = (P.kind == 0 && cb == nb && P.N > 16 && 2 * (size_t)round128((size_t)32 * nb * bb) <= avail) ? 1 : 0;
+    P.stage_bytes = round128((size_t)16 * (nten + P.pair) * cb * bb);
+    P.stages = (int)std::min<size_t>(kMaxStages, avail / P.stage_bytes);
+    if (P.stages < 2) return cudaErrorInvalidConfiguration;
+    ring = std::max(ring, (size_t)P.stages * P.stage_bytes);
+    P.tiles = (P.N + 16 * (1 + P.pair) - 1) / (16 * (1 + P.pair));
     bytes[i] = (int64_t)P.N * RB * nten;
     total += (double)bytes[i];
   }
-  // One tensor with whole rows: two adjacent tiles per stage (halves the
-  // per-block share of the per-tile reduction) when that keeps at least three
-  // stages or does not enlarge the launch's stage; for a launch of one
-  // problem two stages suffice (measured on GB300: the Q6_K LM head streams
-  // ~15 % faster with two paired stages than with five single ones).
-  for (int i = 0; i < count; ++i) {
-    GemvProb& P = B.p[i];
-    const int nb = P.K / kQK;
-    const size_t paired = ((size_t)32 * nb * (P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes) + 127) / 128 * 128;
-    if (P.kind == 0 && P.cb == nb && P.N > 16 &&
-        (3 * paired <= avail || paired <= stage || (count == 1 && 2 * paired <= avail)))
-      P.pair = 1;
-  }
-  for (int i = 0; i < count; ++i) {
-    GemvProb& P = B.p[i];
-    if (P.pair) stage = std::max(stage, ((size_t)32 * P.cb * (P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes) + 127) / 128 * 128);
-    P.tiles = (P.N + 16 * (1 + P.pair) - 1) / (16 * (1 + P.pair));
-  }
-  B.stage_bytes = (uint32_t)stage;
-  B.stages = (int)std::min<size_t>(kMaxStages, avail / stage);
-  if (B.stages < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = x_bytes + (size_t)B.stages * stage + sizeof(GemvShared) + 128;
+  const size_t smem = x_bytes + kSharedBytes + ring + 128;
   const int budget = std::max(count, sm_count());
   int used = 0;
   for (int i = 0; i < count; ++i) {
