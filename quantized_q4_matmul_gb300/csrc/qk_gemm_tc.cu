@@ -327,6 +327,20 @@ __device__ __forceinline__ void add_partial16(uint32_t (&acc)[16], uint32_t src)
   }
 }
 
+// Slot and phase parity of a position in a ring of n stages, advanced
+// incrementally (the ring depth is a launch parameter: no division per step).
+struct RingPos {
+  int slot;
+  uint32_t phase;
+};
+__device__ __forceinline__ void ring_advance(RingPos& r, int k, int n) {
+  r.slot += k;
+  while (r.slot >= n) {
+    r.slot -= n;
+    r.phase ^= 1u;
+  }
+}
+
 // The dequant threads' main loop.  Thread (row rho, half PART) dequantizes,
 // per K step, half of the step's 64 weights of its row (Q4_K: the nibbles PART
 // of sub-block 2c + PART), or for Q6_K the two whole K steps 2*part and
@@ -344,12 +358,12 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
 #pragma unroll
   for (int j = 0; j < kChunks; ++j) off[j] = sw128_off(rho, QT == kQ4K ? 4 * PART + j : j);
   const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
-  int step = 0;
+  RingPos pos = {0, 0u};  // K step 4i of this CTA (Q4_K: the current step)
   bool ok = true;
   for (int i = 0; i < nkb && ok; ++i) {
     const int kb = kb_begin + i;  // super-block of the row; i counts this CTA's pipeline slots
-    const int ps = i % P;
-    ok = mbar_wait(&bars->p_full[ps], (uint32_t)(i / P) & 1u, abort_flag, &g_gemm_status);
+    const int ps = i & 1;  // two packed stages
+    ok = mbar_wait(&bars->p_full[ps], (uint32_t)(i >> 1) & 1u, abort_flag, &g_gemm_status);
     if (!ok) break;
     const uint8_t* pst = smem + L.p_off + (ps * C::kNumB + which) * C::kPSlotBytes;
     if constexpr (QT == kQ4K) {
@@ -357,11 +371,11 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
       q4_load<PART>(pst + rho * kQ4KBytes, q);
       mbar_arrive(&bars->p_empty[ps]);
 #pragma unroll
-      for (int c = 0; c < 4; ++c, ++step) {
-        const int s = step % S;
+      for (int c = 0; c < 4; ++c, ring_advance(pos, 1, S)) {
+        const int s = pos.slot;
         uint32_t r[16];
         q4_step<PART>(q, c, r);
-        ok = mbar_wait(&bars->s_empty[s], ((uint32_t)(step / S) & 1u) ^ 1u, abort_flag, &g_gemm_status);
+        ok = mbar_wait(&bars->s_empty[s], pos.phase ^ 1u, abort_flag, &g_gemm_status);
         if constexpr (AT) {
           ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
           if (!ok) break;
@@ -385,16 +399,18 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
       Q6Regs q;
       q6_load_dispatch(mis, pst + q6_slot(rho, q6g), part, q);
       mbar_arrive(&bars->p_empty[ps]);
+      RingPos sp = pos;  // K step 4i + 2*part
+      ring_advance(sp, 2 * part, S);
 #pragma unroll
       for (int side = 0; side < 2; ++side) {
-        const int st = step + 2 * part + side;
-        const int s = st % S;
+        if (side == 1) ring_advance(sp, 1, S);
+        const int s = sp.slot;
         uint32_t r[32];
         if (side == 0)
           q6_side<0>(q, r);
         else
           q6_side<1>(q, r);
-        ok = mbar_wait(&bars->s_empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemm_status);
+        ok = mbar_wait(&bars->s_empty[s], sp.phase ^ 1u, abort_flag, &g_gemm_status);
         if (!ok) break;
         uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
 #pragma unroll
@@ -403,7 +419,7 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
         fence_proxy_async_smem();
         mbar_arrive(&bars->a_full[s]);
       }
-      step += 4;
+      ring_advance(pos, 4, S);
     }
   }
   return ok;
@@ -475,11 +491,12 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       if (GATEUP) prefetch_tmap(&tm_w1);
     }
     int step = 0;
+    RingPos xpos = {0, 0u};  // ring position of `step`
     bool ok = true;
     for (int i = 0; i < nkb && ok; ++i) {
       const int kb = kb_begin + i;
-      const int ps = i % P;
-      const uint32_t pph = (uint32_t)(i / P) & 1u;
+      const int ps = i & 1;  // two packed stages
+      const uint32_t pph = (uint32_t)(i >> 1) & 1u;
       ok = mbar_wait(&bars->p_empty[ps], pph ^ 1u, abort_flag, &g_gemm_status);
       if (!ok) break;
       uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
@@ -532,10 +549,9 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           mbar_arrive(&bars->p_full[ps]);
         }
       }
-      for (int c = 0; c < 4 && ok; ++c, ++step) {
-        const int s = step % S;
-        const uint32_t ph = (uint32_t)(step / S) & 1u;
-        ok = mbar_wait(&bars->s_empty[s], ph ^ 1u, abort_flag, &g_gemm_status);
+      for (int c = 0; c < 4 && ok; ++c, ++step, ring_advance(xpos, 1, S)) {
+        const int s = xpos.slot;
+        ok = mbar_wait(&bars->s_empty[s], xpos.phase ^ 1u, abort_flag, &g_gemm_status);
         if (!ok) break;
         if (lane == 0) {
           mbar_arrive_expect_tx(&bars->x_full[s], x_bytes);
@@ -561,9 +577,11 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     const int t_first = GATEUP ? 0 : iss, t_stride = GATEUP ? 1 : kIssuers;
     const int ten = GATEUP ? iss : 0;
     bool ok = true;
-    for (int step = t_first; step < nsteps && ok; step += t_stride) {
-      const int s = step % S;
-      const uint32_t ph = (uint32_t)(step / S) & 1u;
+    RingPos ipos = {0, 0u};
+    ring_advance(ipos, t_first, S);
+    for (int step = t_first; step < nsteps && ok; step += t_stride, ring_advance(ipos, t_stride, S)) {
+      const int s = ipos.slot;
+      const uint32_t ph = ipos.phase;
       ok = mbar_wait(&bars->x_full[s], ph, abort_flag, &g_gemm_status) &&
            mbar_wait(&bars->a_full[s], ph, abort_flag, &g_gemm_status);
       if (!ok) break;
