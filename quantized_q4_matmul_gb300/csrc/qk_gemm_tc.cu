@@ -12,7 +12,8 @@
 // weights are the UMMA A operand with M = 128 and the tokens are N = BN):
 //   warp 0      producer: TMA loads of the x tile (BN x 64 fp16, 128-byte
 //               swizzle) per 64-wide K step, and of the packed blocks of the
-//               128 weight rows per 256-wide super-block.
+//               128 weight rows per 256-wide super-block (Q4_K: the two
+//               streams from two lanes, each at its own pace).
 //   warps 1, 2  UMMA issuers (warp 1 also allocates tensor memory): one thread
 //               of each issues tcgen05.mma (kind::f16, fp32 accumulate in
 //               TMEM) and tcgen05.commit for its own accumulator: the gate
@@ -22,9 +23,10 @@
 //               (the fp16 weights never touch device memory), then run the
 //               epilogue: tcgen05.ld of the accumulator, fp32 y stores or
 //               silu(g) * u -> fp16.
-// Pipelines: packed blocks (PS stages, one super-block each), and K steps
-// (S stages, each an x tile + an A tile).  All waits are bounded mbarrier
-// waits; a timeout raises a device status flag and the CTA drains and exits.
+// Pipelines: packed blocks (P stages, one super-block each), x tiles (SX
+// stages) and A tiles (SA >= SX stages), the last two released per K step by
+// the step's UMMA commit.  All waits are bounded mbarrier waits; a timeout
+// raises a device status flag and the CTA drains and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -67,15 +69,14 @@ struct Cfg {
   // Arrivals that complete an A stage: Q4_K threads each write half of every
   // step; Q6_K threads write two of every four steps in full.
   static constexpr int kAArrivals = QT == kQ4K ? 32 * kDqWarps : 32 * kDqWarps / 2;
-  // Packed-block stages (one super-block of the tile's rows each): up to 4.
-  static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : kBM * 224;  // one tensor, one stage
-  static constexpr int kMaxStages = 8;
+  // One packed-block stage holds a super-block of the tile's rows per tensor.
+  static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : kBM * 224;
 };
 
-struct Bars {
+struct Bars {  // capacity: 8 x / A stages, 4 packed stages
   uint64_t x_full[8];
   uint64_t a_full[8];
-  uint64_t s_empty[8];
+  uint64_t done[8];  // done[j]: the UMMAs of the K step in A slot j completed (frees that step's A and x slots)
   uint64_t p_full[4];
   uint64_t p_empty[4];
   uint64_t acc_full;
@@ -84,20 +85,21 @@ struct Bars {
 };
 constexpr uint32_t kBarsBytes = (sizeof(Bars) + 127) / 128 * 128;
 
-// Shared-memory carve-up for a token tile BN, S K-step stages and P packed
-// stages (x and A offsets 1024-byte aligned for the 128-byte swizzle atoms).
+// Shared-memory carve-up for a token tile BN, SX x-tile stages, SA A-tile
+// stages and P packed stages (x and A offsets 1024-byte aligned for the
+// 128-byte swizzle atoms).
 struct Layout {
   uint32_t x_off, x_stage, a_off, p_off, bar_off, total;
 };
 
 template <int QT, bool GATEUP, bool AT>
-__host__ __device__ inline Layout make_layout(int BN, int S, int P) {
+__host__ __device__ inline Layout make_layout(int BN, int SX, int SA, int P) {
   using C = Cfg<QT, GATEUP>;
   Layout L;
   L.x_stage = (uint32_t)BN * kBK * 2;
   L.x_off = 0;
-  L.a_off = L.x_off + (uint32_t)S * L.x_stage;
-  L.p_off = L.a_off + (AT ? 0u : (uint32_t)(S * C::kNumB) * kAStageBytes);
+  L.a_off = L.x_off + (uint32_t)SX * L.x_stage;
+  L.p_off = L.a_off + (AT ? 0u : (uint32_t)(SA * C::kNumB) * kAStageBytes);
   L.bar_off = L.p_off + (uint32_t)(P * C::kNumB * C::kPSlotBytes);
   L.total = L.bar_off + kBarsBytes + 1024;  // barriers + base alignment slack
   return L;
@@ -110,7 +112,8 @@ struct Params {
   int64_t w_bytes;      // bytes of each weight tensor
   void* y;
   int M, N, K, BN;
-  int stages;           // K-step pipeline depth S
+  int stages;           // x-tile stages SX
+  int astages;          // A-tile stages SA >= SX (the dequant may run SA steps ahead of the UMMAs)
   int pstages;          // packed-block pipeline depth P
   int ksplit;           // CTAs of a cluster that split the K range of one tile (1 = no split)
   int q6_group;         // Q6_K: rows per tensor-map row (g: g * row_bytes % 16 == 0)
@@ -344,11 +347,12 @@ __device__ __forceinline__ void ring_advance(RingPos& r, int k, int n) {
 // The dequant threads' main loop.  Thread (row rho, half PART) dequantizes,
 // per K step, half of the step's 64 weights of its row (Q4_K: the nibbles PART
 // of sub-block 2c + PART), or for Q6_K the two whole K steps 2*part and
-// 2*part + 1 of every super-block (Q6_K uses the runtime `part`; PART is 0).  A super-block's packed bytes are loaded
-// into registers at once and the packed slot released before any
-// conversion, so the producer can refill it while the A tiles are written.
+// 2*part + 1 of every super-block (Q6_K uses the runtime `part`; PART is 0).
+// A super-block's packed bytes are loaded into registers at once and the
+// packed slot released before any conversion, so the producer can refill it
+// while the A tiles are written.
 template <int QT, bool GATEUP, bool AT, int PART>
-__device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bars* bars, int S, int P, int nb,
+__device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bars* bars, int SA, int P, int nb,
                                              int kb_begin, int nkb, int which, int rho, uint32_t a_lane,
                                              uint32_t a_col0, int n0, int N, int q6g, int part,
                                              volatile uint32_t* abort_flag) {
@@ -358,24 +362,26 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
 #pragma unroll
   for (int j = 0; j < kChunks; ++j) off[j] = sw128_off(rho, QT == kQ4K ? 4 * PART + j : j);
   const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
-  RingPos pos = {0, 0u};  // K step 4i of this CTA (Q4_K: the current step)
+  RingPos pos = {0, 0u};   // A slot of K step 4i of this CTA (Q4_K: the current step)
+  RingPos ppos = {0, 0u};  // packed stage of super-block i
   bool ok = true;
-  for (int i = 0; i < nkb && ok; ++i) {
+  for (int i = 0; i < nkb && ok; ++i, ring_advance(ppos, 1, P)) {
     const int kb = kb_begin + i;  // super-block of the row; i counts this CTA's pipeline slots
-    const int ps = i & 1;  // two packed stages
-    ok = mbar_wait(&bars->p_full[ps], (uint32_t)(i >> 1) & 1u, abort_flag, &g_gemm_status);
+    const int ps = ppos.slot;
+    ok = mbar_wait(&bars->p_full[ps], ppos.phase, abort_flag, &g_gemm_status);
     if (!ok) break;
     const uint8_t* pst = smem + L.p_off + (ps * C::kNumB + which) * C::kPSlotBytes;
     if constexpr (QT == kQ4K) {
       Q4Regs q;
       q4_load<PART>(pst + rho * kQ4KBytes, q);
-      mbar_arrive(&bars->p_empty[ps]);
+      mbar_arrive(&bars->p_empty[ps]);  // the producer fences before it refills the slot
 #pragma unroll
-      for (int c = 0; c < 4; ++c, ring_advance(pos, 1, S)) {
+      for (int c = 0; c < 4; ++c, ring_advance(pos, 1, SA)) {
         const int s = pos.slot;
         uint32_t r[16];
         q4_step<PART>(q, c, r);
-        ok = mbar_wait(&bars->s_empty[s], pos.phase ^ 1u, abort_flag, &g_gemm_status);
+        // A slot s last held step - SA: wait until its UMMAs completed.
+        ok = mbar_wait(&bars->done[s], pos.phase ^ 1u, abort_flag, &g_gemm_status);
         if constexpr (AT) {
           ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
           if (!ok) break;
@@ -400,17 +406,17 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
       q6_load_dispatch(mis, pst + q6_slot(rho, q6g), part, q);
       mbar_arrive(&bars->p_empty[ps]);
       RingPos sp = pos;  // K step 4i + 2*part
-      ring_advance(sp, 2 * part, S);
+      ring_advance(sp, 2 * part, SA);
 #pragma unroll
       for (int side = 0; side < 2; ++side) {
-        if (side == 1) ring_advance(sp, 1, S);
+        if (side == 1) ring_advance(sp, 1, SA);
         const int s = sp.slot;
         uint32_t r[32];
         if (side == 0)
           q6_side<0>(q, r);
         else
           q6_side<1>(q, r);
-        ok = mbar_wait(&bars->s_empty[s], sp.phase ^ 1u, abort_flag, &g_gemm_status);
+        ok = mbar_wait(&bars->done[s], sp.phase ^ 1u, abort_flag, &g_gemm_status);
         if (!ok) break;
         uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
 #pragma unroll
@@ -419,7 +425,7 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
         fence_proxy_async_smem();
         mbar_arrive(&bars->a_full[s]);
       }
-      ring_advance(pos, 4, S);
+      ring_advance(pos, 4, SA);
     }
   }
   return ok;
@@ -434,8 +440,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   using C = Cfg<QT, GATEUP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = p.stages, P = p.pstages;
-  const Layout L = make_layout<QT, GATEUP, AT>(p.BN, S, P);
+  const int SX = p.stages, SA = p.astages, P = p.pstages;
+  const Layout L = make_layout<QT, GATEUP, AT>(p.BN, SX, SA, P);
   Bars* bars = reinterpret_cast<Bars*>(smem + L.bar_off);
   volatile uint32_t* abort_flag = &bars->abort_flag;
 
@@ -451,12 +457,15 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   const int BN = p.BN;
   const uint32_t x_bytes = (uint32_t)BN * kBK * 2;
   constexpr int kPSlotBytes = C::kPSlotBytes;
+  // Gate/up: x tiles and packed blocks from separate producer lanes (measured
+  // faster on GB300); one tensor: one lane issues both, packed block first.
+  constexpr bool kSplitProducer = QT == kQ4K && GATEUP;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(&bars->x_full[s], 1);
+    for (int s = 0; s < SX; ++s) mbar_init(&bars->x_full[s], 1);
+    for (int s = 0; s < SA; ++s) {
       mbar_init(&bars->a_full[s], C::kAArrivals);
-      mbar_init(&bars->s_empty[s], GATEUP ? kIssuers : 1);  // one commit per issuer using the stage
+      mbar_init(&bars->done[s], GATEUP ? kIssuers : 1);  // one commit per issuer of the step
     }
     for (int s = 0; s < P; ++s) {
       mbar_init(&bars->p_full[s], QT == kQ4K ? 1 : 32);
@@ -467,10 +476,10 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     fence_mbar_init();
   }
   // Accumulators: one per issuer, BN columns each (gate / up, or even / odd K
-  // steps); with AT also S x kNumB A tiles of 32 columns (128 rows x 64 fp16)
+  // steps); with AT also SA x kNumB A tiles of 32 columns (128 rows x 64 fp16)
   // after them.
   const uint32_t a_col0 = (uint32_t)(kIssuers * BN);
-  const uint32_t need_cols = a_col0 + (AT ? (uint32_t)(S * C::kNumB * 32) : 0u);
+  const uint32_t need_cols = a_col0 + (AT ? (uint32_t)(SA * C::kNumB * 32) : 0u);
   const uint32_t tmem_cols = need_cols <= 32 ? 32 : need_cols <= 64 ? 64 : need_cols <= 128 ? 128
                              : need_cols <= 256 ? 256 : 512;
   if (warp == 1) {
@@ -490,82 +499,119 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       if (QT == kQ4K || p.q6_rows_tma > 0) prefetch_tmap(&tm_w0);
       if (GATEUP) prefetch_tmap(&tm_w1);
     }
+    // x slot of `step` (ring SX) and the done barrier of step - SX (ring SA,
+    // starting one lap back: the first SX waits return at once).
     int step = 0;
-    RingPos xpos = {0, 0u};  // ring position of `step`
-    bool ok = true;
-    for (int i = 0; i < nkb && ok; ++i) {
-      const int kb = kb_begin + i;
-      const int ps = i & 1;  // two packed stages
-      const uint32_t pph = (uint32_t)(i >> 1) & 1u;
-      ok = mbar_wait(&bars->p_empty[ps], pph ^ 1u, abort_flag, &g_gemm_status);
-      if (!ok) break;
-      uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
-      if constexpr (QT == kQ4K) {
-        if (lane == 0) {
+    RingPos xpos = {0, 0u}, dpos = {SA - SX, 1u};
+    if constexpr (kSplitProducer) {
+      // Lane 0 streams the x tiles, lane 1 the packed blocks, each at its own
+      // pace: a packed stage is refilled as soon as the dequant threads have
+      // released it, whatever the state of the x ring.
+      if (lane == 0) {
+        bool ok = true;
+        for (; step < nsteps && ok; ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, SA)) {
+          ok = mbar_wait(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
+          if (!ok) break;
+          const int kb = kb_begin + (step >> 2), c = step & 3;
+          mbar_arrive_expect_tx(&bars->x_full[xpos.slot], x_bytes);
+          tma_load_2d(smem + L.x_off + xpos.slot * L.x_stage, &tm_x, kb * kQK + c * kBK, m0, &bars->x_full[xpos.slot]);
+        }
+      } else if (lane == 1) {
+        RingPos ppos = {0, 0u};
+        for (int i = 0; i < nkb; ++i, ring_advance(ppos, 1, P)) {
+          const int ps = ppos.slot;
+          if (!mbar_wait(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status)) break;
+          // The dequant threads read the slot with plain loads; the refill is
+          // an async-proxy write.  This proxy fence, after the barrier that
+          // their releases completed, orders those reads before the copy
+          // (without any fence the copy was seen to overwrite unread bytes).
+          fence_proxy_async_smem();
+          const int kb = kb_begin + i;
+          uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
           mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(C::kNumB * kBM * kQ4KBytes));
           tma_load_2d(pst, &tm_w0, kb * kQ4KBytes, n0, &bars->p_full[ps]);
           if (GATEUP) tma_load_2d(pst + kPSlotBytes, &tm_w1, kb * kQ4KBytes, n0, &bars->p_full[ps]);
         }
-      } else {
-        // Whole tiles inside the tensor map: g TMA boxes (one per residue j).
-        // The last tile, if it holds rows past (N / g) * g, takes one bulk copy
-        // per row of the 16-byte-aligned 224-byte window around its block
-        // instead (a window that would run past the end of the tensor is
-        // shortened and its last bytes copied by plain loads).
-        const int g = p.q6_group;
-        const int64_t RB = (int64_t)nb * kQ6KBytes;
-        if (n0 + kBM <= p.q6_rows_tma) {
+      }
+    } else {
+      RingPos ppos = {0, 0u};
+      bool ok = true;
+      for (int i = 0; i < nkb && ok; ++i, ring_advance(ppos, 1, P)) {
+        const int kb = kb_begin + i;
+        const int ps = ppos.slot;
+        ok = mbar_wait(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status);
+        if (!ok) break;
+        fence_proxy_async_smem();  // as in the split producer: plain reads before the refill
+        uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
+        if constexpr (QT == kQ4K) {
           if (lane == 0) {
-            mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(kBM * kQ6Win));
-            for (int j = 0; j < g; ++j) {
-              const int64_t off = (int64_t)j * RB + (int64_t)kb * kQ6KBytes;
-              tma_load_2d(pst + (uint32_t)j * q6_region_stride(g), &tm_w0, (int32_t)((off & ~int64_t(15)) >> 1),
-                          n0 / g, &bars->p_full[ps]);
-            }
-          } else {
-            mbar_arrive(&bars->p_full[ps]);
+            mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(C::kNumB * kBM * kQ4KBytes));
+            tma_load_2d(pst, &tm_w0, kb * kQ4KBytes, n0, &bars->p_full[ps]);
+            if (GATEUP) tma_load_2d(pst + kPSlotBytes, &tm_w1, kb * kQ4KBytes, n0, &bars->p_full[ps]);
           }
         } else {
-          uint32_t bytes = 0;
-          for (int i = lane; i < kBM; i += 32) {
-            const int n = n0 + i;
-            if (n >= p.N) continue;
-            const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
-            const int64_t lo = gg & ~int64_t(15);
-            bytes += (uint32_t)(lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15)));
+          // Whole tiles inside the tensor map: g TMA boxes (one per residue j).
+          // The last tile, if it holds rows past (N / g) * g, takes one bulk copy
+          // per row of the 16-byte-aligned 224-byte window around its block
+          // instead (a window that would run past the end of the tensor is
+          // shortened and its last bytes copied by plain loads).
+          const int g = p.q6_group;
+          const int64_t RB = (int64_t)nb * kQ6KBytes;
+          if (n0 + kBM <= p.q6_rows_tma) {
+            if (lane == 0) {
+              mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(kBM * kQ6Win));
+              for (int j = 0; j < g; ++j) {
+                const int64_t off = (int64_t)j * RB + (int64_t)kb * kQ6KBytes;
+                tma_load_2d(pst + (uint32_t)j * q6_region_stride(g), &tm_w0, (int32_t)((off & ~int64_t(15)) >> 1),
+                            n0 / g, &bars->p_full[ps]);
+              }
+            } else {
+              mbar_arrive(&bars->p_full[ps]);
+            }
+          } else {
+            uint32_t bytes = 0;
+            for (int i = lane; i < kBM; i += 32) {
+              const int n = n0 + i;
+              if (n >= p.N) continue;
+              const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
+              const int64_t lo = gg & ~int64_t(15);
+              bytes += (uint32_t)(lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15)));
+            }
+            mbar_expect_tx(&bars->p_full[ps], bytes);
+            for (int i = lane; i < kBM; i += 32) {
+              const int n = n0 + i;
+              if (n >= p.N) continue;
+              const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
+              const int64_t lo = gg & ~int64_t(15);
+              const int64_t len = lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15));
+              uint8_t* dst = pst + q6_slot(i, g);
+              bulk_copy_g2s(dst, p.w[0] + lo, (uint32_t)len, &bars->p_full[ps]);
+              for (int64_t b = lo + len; b < gg + kQ6KBytes; b += 2)  // tail bytes (only at the tensor's end)
+                *reinterpret_cast<uint16_t*>(dst + (b - lo)) = *reinterpret_cast<const uint16_t*>(p.w[0] + b);
+            }
+            fence_proxy_async_smem();  // plain writes into a slot that later refills write through TMA
+            mbar_arrive(&bars->p_full[ps]);
           }
-          mbar_expect_tx(&bars->p_full[ps], bytes);
-          for (int i = lane; i < kBM; i += 32) {
-            const int n = n0 + i;
-            if (n >= p.N) continue;
-            const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
-            const int64_t lo = gg & ~int64_t(15);
-            const int64_t len = lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15));
-            uint8_t* dst = pst + q6_slot(i, g);
-            bulk_copy_g2s(dst, p.w[0] + lo, (uint32_t)len, &bars->p_full[ps]);
-            for (int64_t b = lo + len; b < gg + kQ6KBytes; b += 2)  // tail bytes (only at the tensor's end)
-              *reinterpret_cast<uint16_t*>(dst + (b - lo)) = *reinterpret_cast<const uint16_t*>(p.w[0] + b);
+        }
+        for (int c = 0; c < 4 && ok; ++c, ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, SA)) {
+          const int s = xpos.slot;
+          ok = mbar_wait(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
+          if (!ok) break;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bars->x_full[s], x_bytes);
+            tma_load_2d(smem + L.x_off + s * L.x_stage, &tm_x, kb * kQK + c * kBK, m0, &bars->x_full[s]);
           }
-          mbar_arrive(&bars->p_full[ps]);
+          __syncwarp();
         }
-      }
-      for (int c = 0; c < 4 && ok; ++c, ++step, ring_advance(xpos, 1, S)) {
-        const int s = xpos.slot;
-        ok = mbar_wait(&bars->s_empty[s], xpos.phase ^ 1u, abort_flag, &g_gemm_status);
-        if (!ok) break;
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&bars->x_full[s], x_bytes);
-          tma_load_2d(smem + L.x_off + s * L.x_stage, &tm_x, kb * kQK + c * kBK, m0, &bars->x_full[s]);
-        }
-        __syncwarp();
       }
     }
-    // Drain: every x copy this warp issued has completed before the CTA exits
-    // (the packed-block copies are drained by the dequant warps' waits).
-    for (int i = 0; i < S && i < step; ++i) {
-      const int st = step - 1 - i;
-      mbar_wait(&bars->x_full[st % S], (uint32_t)(st / S) & 1u, abort_flag, &g_gemm_status,
-                true);
+    // Drain: every x copy issued has completed before the CTA exits (the
+    // packed-block copies are drained by the dequant warps' waits).
+    if (!kSplitProducer || lane == 0) {
+      for (int i = 0; i < SX && i < step; ++i) {
+        const int st = step - 1 - i;
+        mbar_wait(&bars->x_full[st % SX], (uint32_t)(st / SX) & 1u, abort_flag, &g_gemm_status, true);
+      }
     }
   } else if (warp <= kIssuers) {
     // ------------------------------------------------------------------ UMMA issuers
@@ -577,17 +623,18 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     const int t_first = GATEUP ? 0 : iss, t_stride = GATEUP ? 1 : kIssuers;
     const int ten = GATEUP ? iss : 0;
     bool ok = true;
-    RingPos ipos = {0, 0u};
-    ring_advance(ipos, t_first, S);
-    for (int step = t_first; step < nsteps && ok; step += t_stride, ring_advance(ipos, t_stride, S)) {
-      const int s = ipos.slot;
-      const uint32_t ph = ipos.phase;
-      ok = mbar_wait(&bars->x_full[s], ph, abort_flag, &g_gemm_status) &&
-           mbar_wait(&bars->a_full[s], ph, abort_flag, &g_gemm_status);
+    RingPos xs = {0, 0u}, as = {0, 0u};  // x and A slots of `step`
+    ring_advance(xs, t_first, SX);
+    ring_advance(as, t_first, SA);
+    for (int step = t_first; step < nsteps && ok;
+         step += t_stride, ring_advance(xs, t_stride, SX), ring_advance(as, t_stride, SA)) {
+      const int s = as.slot;
+      ok = mbar_wait(&bars->x_full[xs.slot], xs.phase, abort_flag, &g_gemm_status) &&
+           mbar_wait(&bars->a_full[s], as.phase, abort_flag, &g_gemm_status);
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
-        const uint64_t bdesc = umma_desc_sw128(smem_u32(smem + L.x_off + s * L.x_stage));
+        const uint64_t bdesc = umma_desc_sw128(smem_u32(smem + L.x_off + xs.slot * L.x_stage));
         if constexpr (AT) {
           const uint32_t a_tm = tmem + a_col0 + (uint32_t)((s * C::kNumB + ten) * 32);
 #pragma unroll
@@ -601,7 +648,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
             umma_f16_ss(d_tm, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
                         (step > t_first || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&bars->s_empty[s]);
+        umma_commit(&bars->done[s]);
       }
       __syncwarp();
     }
@@ -624,10 +671,10 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     // half as a runtime value (one copy of its larger code).
     bool ok;
     if (QT == kQ6K || part == 0)
-      ok = dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, S, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
+      ok = dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, SA, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
                                            p.N, p.q6_group, part, abort_flag);
     else
-      ok = dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, S, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
+      ok = dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, SA, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
                                            p.N, p.q6_group, part, abort_flag);
 
     if (ok) ok = mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status);
@@ -862,24 +909,54 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   p.N = (int)N;
   p.K = (int)K;
   p.BN = BN;
-  // Pipeline depths: 2 packed-block stages (measured on GB300: deeper
-  // packed prefetch queues more tall weight boxes ahead of the x tiles in the
-  // SM's TMA unit and slows every shape), then as many K-step stages (2 .. 8)
-  // as fit in shared memory (and, with A in tensor memory, in TMEM).
-  auto fits = [&](int S_, int P_) {
-    return make_layout<QT, GATEUP, AT>(BN, S_, P_).total <= (uint32_t)kSmemLimit &&
-           !(AT && kIssuers * BN + S_ * C::kNumB * 32 > 512);
+  // Pipeline depths (all measured on GB300).  The K-step rings come first: a
+  // single-tensor kernel with fewer than 4 x-tile stages ran ~35 % slower.
+  // A-tile and x-tile stages are grown alternately, A first and never fewer
+  // A than x stages (the A tiles wait for the dequant, the x tiles only for a
+  // copy), up to 5 A and 4 x stages (deeper rings were no faster, and slower
+  // for Q6_K attn_v), while shared memory (and, with A in tensor memory,
+  // TMEM) allows.  Two packed-block stages where the rings still reach 4 x
+  // stages next to them (cold-cache Q6_K ran faster with two), else one (the
+  // dequant threads copy a super-block to registers and release its slot at
+  // once, so the refill overlaps the block's four K steps).
+  constexpr int kMaxXStages = 4, kMaxAStages = 5;
+  auto depths = [&](int P_, int& SX_, int& SA_) {
+    auto fits = [&](int sx, int sa) {
+      return make_layout<QT, GATEUP, AT>(BN, sx, sa, P_).total <= (uint32_t)kSmemLimit &&
+             !(AT && kIssuers * BN + sa * C::kNumB * 32 > 512);
+    };
+    SX_ = 2;
+    SA_ = 2;
+    for (bool grew = true; grew;) {
+      grew = false;
+      if (SA_ == SX_ && SA_ < kMaxAStages && fits(SX_, SA_ + 1)) {
+        ++SA_;
+        grew = true;
+      } else if (SX_ < SA_ && SX_ < kMaxXStages && fits(SX_ + 1, SA_)) {
+        ++SX_;
+        grew = true;
+      }
+    }
   };
-  const int P = 2;
-  int S = C::kMaxStages;
-  while (S > 2 && !fits(S, P)) --S;
-  if constexpr (AT) {  // A tiles do not fit next to the accumulators: keep them in shared memory
-    if (kIssuers * BN + S * C::kNumB * 32 > 512) return launch_tc<QT, GATEUP, false>(W0, W1, x, y, M, N, K, stream);
+  int P = 2, SX, SA;
+  depths(P, SX, SA);
+  if (SX < kMaxXStages) {
+    int sx1, sa1;
+    depths(1, sx1, sa1);
+    if (sx1 > SX || (sx1 == SX && sa1 > SA)) {
+      P = 1;
+      SX = sx1;
+      SA = sa1;
+    }
   }
-  p.stages = S;
+  if constexpr (AT) {  // A tiles do not fit next to the accumulators: keep them in shared memory
+    if (kIssuers * BN + SA * C::kNumB * 32 > 512) return launch_tc<QT, GATEUP, false>(W0, W1, x, y, M, N, K, stream);
+  }
+  p.stages = SX;
+  p.astages = SA;
   p.pstages = P;
   p.ksplit = 1;
-  const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, S, P).total;
+  const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, SX, SA, P).total;
   if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   static bool attr_set = false;
   if (!attr_set) {
@@ -896,7 +973,7 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   int ks = 1;
   if (!GATEUP) {
     const int64_t tiles = (int64_t)grid.x * grid.y;
-    const Layout L = make_layout<QT, GATEUP, AT>(BN, S, P);
+    const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
     for (int c = 8; c >= 2; --c)
       if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * kBM * BN * 4 <= L.bar_off) {
         ks = c;

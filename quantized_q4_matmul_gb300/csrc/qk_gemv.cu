@@ -333,6 +333,10 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
       for (; st < steps; ++st) {
         const int s = st % S;
         if (!mbar_wait(&sh->empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemv_status)) break;
+        // The compute warps read the stage with plain loads; the refill is an
+        // async-proxy write.  The proxy fence after the barrier their releases
+        // completed orders those reads before the copy.
+        fence_proxy_async_smem();
         const int tile = t0 + st / nchunks, chunk = st % nchunks;
         const int n0 = tile * tile_rows, rows = min(16, N - n0);
         uint8_t* dst = stages + (size_t)s * SB;

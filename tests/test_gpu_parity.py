@@ -127,6 +127,34 @@ def test_matmul_deterministic(qk_lib, cuda, qtype):
         assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("kind,N,K", [("gateup", 8192, 3072), ("q4k", 8192, 3072), ("q4k", 3072, 3072),
+                                      ("q6k", 3072, 8192), ("q6k", 16384, 3072)])
+def test_full_size_repeatable(qk_lib, cuda, kind, N, K):
+    """Repeated M=1024 launches give bit-identical outputs.  These shapes cover
+    every pipeline configuration of the prefill GEMM (two-tensor split producer,
+    one and two packed stages); a missing ordering between the dequant threads'
+    reads of a packed slot and its refill showed up as run-to-run differences."""
+    import torch
+    rng = synth.rng_for(11, N)
+    M = 1024
+    x = _x_dev(synth.activations(rng, M, K), cuda)
+    if kind == "gateup":
+        Wg, Wu = _dev(synth.q4k_weights(rng, N, K), cuda), _dev(synth.q4k_weights(rng, N, K), cuda)
+        y = torch.empty(M, N, dtype=torch.float16, device=cuda)
+        call = lambda: qk_lib.qk_gateup_swiglu_q4k(Wg, Wu, x, y, M, N, K)
+    else:
+        W = _dev(synth.weights(rng, kind, N, K), cuda)
+        y = torch.empty(M, N, dtype=torch.float32, device=cuda)
+        fn = qk_lib.qk_matmul_q4k if kind == "q4k" else qk_lib.qk_matmul_q6k
+        call = lambda: fn(W, x, y, M, N, K)
+    call()
+    first = y.clone()
+    for _ in range(6):
+        call()
+        assert torch.equal(y, first)
+    qk_lib.qk_get_device_status()
+
+
 @pytest.mark.parametrize("qtype", ["q4k", "q6k"])
 def test_matmul_special_scales(qk_lib, cuda, qtype):
     """Zero, subnormal and large fp16 scale fields (finite)."""
