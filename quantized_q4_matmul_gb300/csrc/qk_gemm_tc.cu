@@ -404,6 +404,7 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
       const int mis = (int)(((int64_t)n * RB + (int64_t)kb * kQ6KBytes) & 15);
       Q6Regs q;
       q6_load_dispatch(mis, pst + q6_slot(rho, q6g), part, q);
+      if constexpr (AT) __syncwarp();  // rows of one warp may differ in alignment (tcgen05.st below is collective)
       mbar_arrive(&bars->p_empty[ps]);
       RingPos sp = pos;  // K step 4i + 2*part
       ring_advance(sp, 2 * part, SA);
@@ -417,12 +418,23 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
         else
           q6_side<1>(q, r);
         ok = mbar_wait(&bars->done[s], sp.phase ^ 1u, abort_flag, &g_gemm_status);
-        if (!ok) break;
-        uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
+        if constexpr (AT) {
+          ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t ta = a_lane + a_col0 + (uint32_t)((s * C::kNumB + which) * 32);
+          tmem_st16(ta, *reinterpret_cast<const uint32_t(*)[16]>(r));
+          tmem_st16(ta + 16, *reinterpret_cast<const uint32_t(*)[16]>(r + 16));
+          tmem_wait_st();
+          tc_fence_before();
+        } else {
+          if (!ok) break;
+          uint8_t* a_tile = smem + L.a_off + (s * C::kNumB + which) * kAStageBytes;
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<uint4*>(a_tile + off[j]) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
-        fence_proxy_async_smem();
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(a_tile + off[j]) = make_uint4(r[4 * j], r[4 * j + 1], r[4 * j + 2], r[4 * j + 3]);
+          fence_proxy_async_smem();
+        }
         mbar_arrive(&bars->a_full[s]);
       }
       ring_advance(pos, 4, SA);
@@ -1013,15 +1025,19 @@ uint32_t gemm_take_status() {
 
 cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N,
                         int64_t K, bool gateup, cudaStream_t s) {
+  // Single-tensor problems keep the dequantized A tiles in tensor memory when
+  // they fit next to the accumulators (measured faster on GB300: no A-tile
+  // shared-memory writes and UMMA reads); QK_A_TMEM=0 selects shared memory.
   static const int a_tmem = [] {
     const char* e = getenv("QK_A_TMEM");
-    return e ? atoi(e) : 0;
+    return e ? atoi(e) : 1;
   }();
   if (gateup) return launch_tc<kQ4K, true, false>(W, W_up, x, y, M, N, K, s);
   if (t == kQ4K) {
     if (a_tmem) return launch_tc<kQ4K, false, true>(W, nullptr, x, y, M, N, K, s);
     return launch_tc<kQ4K, false, false>(W, nullptr, x, y, M, N, K, s);
   }
+  if (a_tmem) return launch_tc<kQ6K, false, true>(W, nullptr, x, y, M, N, K, s);
   return launch_tc<kQ6K, false, false>(W, nullptr, x, y, M, N, K, s);
 }
 

@@ -155,6 +155,42 @@ def test_full_size_repeatable(qk_lib, cuda, kind, N, K):
     qk_lib.qk_get_device_status()
 
 
+_SMEM_A_CHILD = """
+import sys, numpy as np, torch
+sys.path.insert(0, sys.argv[1])
+import oracle, quantized_q4_matmul_gb300 as qk
+from tests import synth
+dev = torch.device("cuda", 0)
+for qtype, M, N, K in [("q4k", 200, 384, 1024), ("q6k", 200, 384, 1024), ("q4k", 37, 200, 768),
+                       ("q6k", 37, 200, 768), ("q6k", 300, 1024, 3072)]:
+    rng = synth.rng_for(31, N)
+    W = synth.weights(rng, qtype, N, K)
+    x = synth.activations(rng, M, K)
+    y = torch.empty(M, N, dtype=torch.float32, device=dev)
+    fn = qk.qk_matmul_q4k if qtype == "q4k" else qk.qk_matmul_q6k
+    fn(torch.from_numpy(W).to(dev), torch.from_numpy(x.view(np.uint16)).to(dev), y, M, N, K)
+    qk.qk_get_device_status()
+    ref = oracle.matmul(oracle.Q4K if qtype == "q4k" else oracle.Q6K, W, x, N, K)
+    err = np.max(np.abs(y.cpu().numpy() - ref)) / np.sqrt(np.mean(ref ** 2))
+    assert err <= 1e-2, (qtype, M, N, K, err)
+print("ok")
+"""
+
+
+def test_shared_memory_a_tiles_path(qk_lib, cuda):
+    """Single-tensor GEMMs keep A tiles in tensor memory by default; the
+    shared-memory A path (QK_A_TMEM=0, read once per process) is checked
+    against the oracle in a child process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, QK_A_TMEM="0")
+    r = subprocess.run([sys.executable, "-c", _SMEM_A_CHILD, root], env=env, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout[-2000:] + r.stderr[-2000:]
+
+
 @pytest.mark.parametrize("qtype", ["q4k", "q6k"])
 def test_matmul_special_scales(qk_lib, cuda, qtype):
     """Zero, subnormal and large fp16 scale fields (finite)."""
