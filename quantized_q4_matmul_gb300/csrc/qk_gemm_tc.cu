@@ -443,6 +443,66 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
   return ok;
 }
 
+// Copies of super-block kb's packed blocks (the CTA's 128 rows) into the
+// packed stage pst, completing on `full`.  Lanes pl = 0 .. np-1 of the calling
+// warp share the work: Q4_K, lane 0 alone (one tensor-map box per tensor);
+// Q6_K, every lane arrives on `full` (np arrivals).  Q6_K tiles inside the
+// tensor map take g boxes (one per residue j); the last tile, if it holds rows
+// past (N / g) * g, takes one bulk copy per row of the 16-byte-aligned
+// 224-byte window around its block instead (a window that would run past the
+// end of the tensor is shortened and its last bytes copied by plain loads).
+template <int QT, bool GATEUP>
+__device__ __forceinline__ void issue_packed(uint8_t* pst, uint64_t* full, const CUtensorMap* tm_w0,
+                                             const CUtensorMap* tm_w1, const Params& p, int kb, int n0, int nb,
+                                             int pl, int np) {
+  using C = Cfg<QT, GATEUP>;
+  if constexpr (QT == kQ4K) {
+    if (pl == 0) {
+      mbar_arrive_expect_tx(full, (uint32_t)(C::kNumB * kBM * kQ4KBytes));
+      tma_load_2d(pst, tm_w0, kb * kQ4KBytes, n0, full);
+      if (GATEUP) tma_load_2d(pst + C::kPSlotBytes, tm_w1, kb * kQ4KBytes, n0, full);
+    }
+  } else {
+    const int g = p.q6_group;
+    const int64_t RB = (int64_t)nb * kQ6KBytes;
+    if (n0 + kBM <= p.q6_rows_tma) {
+      if (pl == 0) {
+        mbar_arrive_expect_tx(full, (uint32_t)(kBM * kQ6Win));
+        for (int j = 0; j < g; ++j) {
+          const int64_t off = (int64_t)j * RB + (int64_t)kb * kQ6KBytes;
+          tma_load_2d(pst + (uint32_t)j * q6_region_stride(g), tm_w0, (int32_t)((off & ~int64_t(15)) >> 1), n0 / g,
+                      full);
+        }
+      } else {
+        mbar_arrive(full);
+      }
+    } else {
+      uint32_t bytes = 0;
+      for (int i = pl; i < kBM; i += np) {
+        const int n = n0 + i;
+        if (n >= p.N) continue;
+        const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
+        const int64_t lo = gg & ~int64_t(15);
+        bytes += (uint32_t)(lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15)));
+      }
+      mbar_expect_tx(full, bytes);
+      for (int i = pl; i < kBM; i += np) {
+        const int n = n0 + i;
+        if (n >= p.N) continue;
+        const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
+        const int64_t lo = gg & ~int64_t(15);
+        const int64_t len = lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15));
+        uint8_t* dst = pst + q6_slot(i, g);
+        bulk_copy_g2s(dst, p.w[0] + lo, (uint32_t)len, full);
+        for (int64_t b = lo + len; b < gg + kQ6KBytes; b += 2)  // tail bytes (only at the tensor's end)
+          *reinterpret_cast<uint16_t*>(dst + (b - lo)) = *reinterpret_cast<const uint16_t*>(p.w[0] + b);
+      }
+      fence_proxy_async_smem();  // plain writes into a slot that later refills write through TMA
+      mbar_arrive(full);
+    }
+  }
+}
+
 // AT: the dequantized A tiles live in tensor memory (tcgen05.st from the
 // dequant threads, UMMA reads A from TMEM) instead of shared memory.
 template <int QT, bool GATEUP, bool AT>
@@ -469,9 +529,11 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   const int BN = p.BN;
   const uint32_t x_bytes = (uint32_t)BN * kBK * 2;
   constexpr int kPSlotBytes = C::kPSlotBytes;
-  // Gate/up: x tiles and packed blocks from separate producer lanes (measured
-  // faster on GB300); one tensor: one lane issues both, packed block first.
-  constexpr bool kSplitProducer = QT == kQ4K && GATEUP;
+  // Gate/up and Q6_K: x tiles and packed blocks from separate producer lanes
+  // (measured faster on GB300: the packed copies no longer wait behind the x
+  // ring); one Q4_K tensor: one loop issues both, packed block first.
+  constexpr bool kSplitProducer = GATEUP || QT == kQ6K;
+  constexpr int kPackedLanes = QT == kQ4K ? 1 : 31;  // split producer: lanes 1 .. kPackedLanes
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SX; ++s) mbar_init(&bars->x_full[s], 1);
@@ -480,7 +542,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       mbar_init(&bars->done[s], GATEUP ? kIssuers : 1);  // one commit per issuer of the step
     }
     for (int s = 0; s < P; ++s) {
-      mbar_init(&bars->p_full[s], QT == kQ4K ? 1 : 32);
+      mbar_init(&bars->p_full[s], QT == kQ4K ? 1 : (kSplitProducer ? kPackedLanes : 32));
       mbar_init(&bars->p_empty[s], 32 * C::kDqWarps);
     }
     mbar_init(&bars->acc_full, kIssuers);
@@ -516,9 +578,9 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     int step = 0;
     RingPos xpos = {0, 0u}, dpos = {SA - SX, 1u};
     if constexpr (kSplitProducer) {
-      // Lane 0 streams the x tiles, lane 1 the packed blocks, each at its own
-      // pace: a packed stage is refilled as soon as the dequant threads have
-      // released it, whatever the state of the x ring.
+      // Lane 0 streams the x tiles, lanes 1 .. kPackedLanes the packed blocks,
+      // each at its own pace: a packed stage is refilled as soon as the
+      // dequant threads have released it, whatever the state of the x ring.
       if (lane == 0) {
         bool ok = true;
         for (; step < nsteps && ok; ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, SA)) {
@@ -528,7 +590,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           mbar_arrive_expect_tx(&bars->x_full[xpos.slot], x_bytes);
           tma_load_2d(smem + L.x_off + xpos.slot * L.x_stage, &tm_x, kb * kQK + c * kBK, m0, &bars->x_full[xpos.slot]);
         }
-      } else if (lane == 1) {
+      } else if (lane <= kPackedLanes) {
         RingPos ppos = {0, 0u};
         for (int i = 0; i < nkb; ++i, ring_advance(ppos, 1, P)) {
           const int ps = ppos.slot;
@@ -538,14 +600,12 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           // their releases completed, orders those reads before the copy
           // (without any fence the copy was seen to overwrite unread bytes).
           fence_proxy_async_smem();
-          const int kb = kb_begin + i;
-          uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
-          mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(C::kNumB * kBM * kQ4KBytes));
-          tma_load_2d(pst, &tm_w0, kb * kQ4KBytes, n0, &bars->p_full[ps]);
-          if (GATEUP) tma_load_2d(pst + kPSlotBytes, &tm_w1, kb * kQ4KBytes, n0, &bars->p_full[ps]);
+          issue_packed<QT, GATEUP>(smem + L.p_off + ps * C::kNumB * kPSlotBytes, &bars->p_full[ps], &tm_w0, &tm_w1, p,
+                                   kb_begin + i, n0, nb, lane - 1, kPackedLanes);
         }
       }
     } else {
+      // One loop for both: the packed block of super-block i, then its four x tiles.
       RingPos ppos = {0, 0u};
       bool ok = true;
       for (int i = 0; i < nkb && ok; ++i, ring_advance(ppos, 1, P)) {
@@ -554,57 +614,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
         ok = mbar_wait(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status);
         if (!ok) break;
         fence_proxy_async_smem();  // as in the split producer: plain reads before the refill
-        uint8_t* pst = smem + L.p_off + ps * C::kNumB * kPSlotBytes;
-        if constexpr (QT == kQ4K) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(C::kNumB * kBM * kQ4KBytes));
-            tma_load_2d(pst, &tm_w0, kb * kQ4KBytes, n0, &bars->p_full[ps]);
-            if (GATEUP) tma_load_2d(pst + kPSlotBytes, &tm_w1, kb * kQ4KBytes, n0, &bars->p_full[ps]);
-          }
-        } else {
-          // Whole tiles inside the tensor map: g TMA boxes (one per residue j).
-          // The last tile, if it holds rows past (N / g) * g, takes one bulk copy
-          // per row of the 16-byte-aligned 224-byte window around its block
-          // instead (a window that would run past the end of the tensor is
-          // shortened and its last bytes copied by plain loads).
-          const int g = p.q6_group;
-          const int64_t RB = (int64_t)nb * kQ6KBytes;
-          if (n0 + kBM <= p.q6_rows_tma) {
-            if (lane == 0) {
-              mbar_arrive_expect_tx(&bars->p_full[ps], (uint32_t)(kBM * kQ6Win));
-              for (int j = 0; j < g; ++j) {
-                const int64_t off = (int64_t)j * RB + (int64_t)kb * kQ6KBytes;
-                tma_load_2d(pst + (uint32_t)j * q6_region_stride(g), &tm_w0, (int32_t)((off & ~int64_t(15)) >> 1),
-                            n0 / g, &bars->p_full[ps]);
-              }
-            } else {
-              mbar_arrive(&bars->p_full[ps]);
-            }
-          } else {
-            uint32_t bytes = 0;
-            for (int i = lane; i < kBM; i += 32) {
-              const int n = n0 + i;
-              if (n >= p.N) continue;
-              const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
-              const int64_t lo = gg & ~int64_t(15);
-              bytes += (uint32_t)(lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15)));
-            }
-            mbar_expect_tx(&bars->p_full[ps], bytes);
-            for (int i = lane; i < kBM; i += 32) {
-              const int n = n0 + i;
-              if (n >= p.N) continue;
-              const int64_t gg = (int64_t)n * RB + (int64_t)kb * kQ6KBytes;
-              const int64_t lo = gg & ~int64_t(15);
-              const int64_t len = lo + kQ6Win <= p.w_bytes ? kQ6Win : ((p.w_bytes - lo) & ~int64_t(15));
-              uint8_t* dst = pst + q6_slot(i, g);
-              bulk_copy_g2s(dst, p.w[0] + lo, (uint32_t)len, &bars->p_full[ps]);
-              for (int64_t b = lo + len; b < gg + kQ6KBytes; b += 2)  // tail bytes (only at the tensor's end)
-                *reinterpret_cast<uint16_t*>(dst + (b - lo)) = *reinterpret_cast<const uint16_t*>(p.w[0] + b);
-            }
-            fence_proxy_async_smem();  // plain writes into a slot that later refills write through TMA
-            mbar_arrive(&bars->p_full[ps]);
-          }
-        }
+        issue_packed<QT, GATEUP>(smem + L.p_off + ps * C::kNumB * kPSlotBytes, &bars->p_full[ps], &tm_w0, &tm_w1, p, kb,
+                                 n0, nb, lane, 32);
         for (int c = 0; c < 4 && ok; ++c, ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, SA)) {
           const int s = xpos.slot;
           ok = mbar_wait(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
@@ -931,7 +942,13 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   // stages next to them (cold-cache Q6_K ran faster with two), else one (the
   // dequant threads copy a super-block to registers and release its slot at
   // once, so the refill overlaps the block's four K steps).
-  constexpr int kMaxXStages = 4, kMaxAStages = 5;
+  // Q6_K takes exactly 4 A stages: its threads write two consecutive K steps
+  // of a super-block and the two halves of a row alternate, so with SA a
+  // multiple of 4 each half owns its A slots and observes every phase of their
+  // done barriers in order (with SA = 2, 3 or 5 a thread could wait on a slot
+  // whose previous phase it never saw, and the parity test then passes a phase
+  // early: seen on GB300 as wrong output with the packed copies running ahead).
+  constexpr int kMaxXStages = 4, kMaxAStages = QT == kQ6K ? 4 : 5;
   auto depths = [&](int P_, int& SX_, int& SA_) {
     auto fits = [&](int sx, int sa) {
       return make_layout<QT, GATEUP, AT>(BN, sx, sa, P_).total <= (uint32_t)kSmemLimit &&
@@ -962,8 +979,10 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
     }
   }
   if constexpr (AT) {  // A tiles do not fit next to the accumulators: keep them in shared memory
-    if (kIssuers * BN + SA * C::kNumB * 32 > 512) return launch_tc<QT, GATEUP, false>(W0, W1, x, y, M, N, K, stream);
+    if (kIssuers * BN + SA * C::kNumB * 32 > 512 || (QT == kQ6K && SA != 4))
+      return launch_tc<QT, GATEUP, false>(W0, W1, x, y, M, N, K, stream);
   }
+  if (QT == kQ6K && SA != 4) return cudaErrorInvalidConfiguration;  // not reached for BN <= 256
   p.stages = SX;
   p.astages = SA;
   p.pstages = P;
