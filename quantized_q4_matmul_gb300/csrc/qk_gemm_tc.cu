@@ -76,7 +76,7 @@ struct Cfg {
 struct Bars {  // capacity: 8 x / A stages, 4 packed stages
   uint64_t x_full[8];
   uint64_t a_full[8];
-  uint64_t done[8];  // done[j]: the UMMAs of the K step in A slot j completed (frees that step's A and x slots)
+  uint64_t done[8];  // done[t % D]: the UMMAs of K step t completed (frees its A and x slots)
   uint64_t p_full[4];
   uint64_t p_empty[4];
   uint64_t acc_full;
@@ -352,7 +352,7 @@ __device__ __forceinline__ void ring_advance(RingPos& r, int k, int n) {
 // packed slot released before any conversion, so the producer can refill it
 // while the A tiles are written.
 template <int QT, bool GATEUP, bool AT, int PART>
-__device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bars* bars, int SA, int P, int nb,
+__device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bars* bars, int SA, int D, int P, int nb,
                                              int kb_begin, int nkb, int which, int rho, uint32_t a_lane,
                                              uint32_t a_col0, int n0, int N, int q6g, int part,
                                              volatile uint32_t* abort_flag) {
@@ -364,6 +364,10 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
   const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
   RingPos pos = {0, 0u};   // A slot of K step 4i of this CTA (Q4_K: the current step)
   RingPos ppos = {0, 0u};  // packed stage of super-block i
+  // Q4_K: done barrier of step - SA (ring D >= SA, one lap back at the start,
+  // so the first SA waits return at once).  Q6_K runs with D == SA and uses
+  // the A slot (phase flipped) directly.
+  RingPos dd = {D - SA, 1u};
   bool ok = true;
   for (int i = 0; i < nkb && ok; ++i, ring_advance(ppos, 1, P)) {
     const int kb = kb_begin + i;  // super-block of the row; i counts this CTA's pipeline slots
@@ -376,12 +380,12 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
       q4_load<PART>(pst + rho * kQ4KBytes, q);
       mbar_arrive(&bars->p_empty[ps]);  // the producer fences before it refills the slot
 #pragma unroll
-      for (int c = 0; c < 4; ++c, ring_advance(pos, 1, SA)) {
+      for (int c = 0; c < 4; ++c, ring_advance(pos, 1, SA), ring_advance(dd, 1, D)) {
         const int s = pos.slot;
         uint32_t r[16];
         q4_step<PART>(q, c, r);
         // A slot s last held step - SA: wait until its UMMAs completed.
-        ok = mbar_wait(&bars->done[s], pos.phase ^ 1u, abort_flag, &g_gemm_status);
+        ok = mbar_wait(&bars->done[dd.slot], dd.phase, abort_flag, &g_gemm_status);
         if constexpr (AT) {
           ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
           if (!ok) break;
@@ -513,6 +517,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int SX = p.stages, SA = p.astages, P = p.pstages;
+  const int D = SX > SA ? SX : SA;  // done-barrier ring
   const Layout L = make_layout<QT, GATEUP, AT>(p.BN, SX, SA, P);
   Bars* bars = reinterpret_cast<Bars*>(smem + L.bar_off);
   volatile uint32_t* abort_flag = &bars->abort_flag;
@@ -537,10 +542,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SX; ++s) mbar_init(&bars->x_full[s], 1);
-    for (int s = 0; s < SA; ++s) {
-      mbar_init(&bars->a_full[s], C::kAArrivals);
-      mbar_init(&bars->done[s], GATEUP ? kIssuers : 1);  // one commit per issuer of the step
-    }
+    for (int s = 0; s < SA; ++s) mbar_init(&bars->a_full[s], C::kAArrivals);
+    for (int s = 0; s < D; ++s) mbar_init(&bars->done[s], GATEUP ? kIssuers : 1);  // one commit per issuer of the step
     for (int s = 0; s < P; ++s) {
       mbar_init(&bars->p_full[s], QT == kQ4K ? 1 : (kSplitProducer ? kPackedLanes : 32));
       mbar_init(&bars->p_empty[s], 32 * C::kDqWarps);
@@ -573,17 +576,17 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       if (QT == kQ4K || p.q6_rows_tma > 0) prefetch_tmap(&tm_w0);
       if (GATEUP) prefetch_tmap(&tm_w1);
     }
-    // x slot of `step` (ring SX) and the done barrier of step - SX (ring SA,
+    // x slot of `step` (ring SX) and the done barrier of step - SX (ring D,
     // starting one lap back: the first SX waits return at once).
     int step = 0;
-    RingPos xpos = {0, 0u}, dpos = {SA - SX, 1u};
+    RingPos xpos = {0, 0u}, dpos = {D - SX, 1u};
     if constexpr (kSplitProducer) {
       // Lane 0 streams the x tiles, lanes 1 .. kPackedLanes the packed blocks,
       // each at its own pace: a packed stage is refilled as soon as the
       // dequant threads have released it, whatever the state of the x ring.
       if (lane == 0) {
         bool ok = true;
-        for (; step < nsteps && ok; ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, SA)) {
+        for (; step < nsteps && ok; ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, D)) {
           ok = mbar_wait(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
           if (!ok) break;
           const int kb = kb_begin + (step >> 2), c = step & 3;
@@ -616,7 +619,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
         fence_proxy_async_smem();  // as in the split producer: plain reads before the refill
         issue_packed<QT, GATEUP>(smem + L.p_off + ps * C::kNumB * kPSlotBytes, &bars->p_full[ps], &tm_w0, &tm_w1, p, kb,
                                  n0, nb, lane, 32);
-        for (int c = 0; c < 4 && ok; ++c, ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, SA)) {
+        for (int c = 0; c < 4 && ok; ++c, ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, D)) {
           const int s = xpos.slot;
           ok = mbar_wait(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
           if (!ok) break;
@@ -646,11 +649,12 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     const int t_first = GATEUP ? 0 : iss, t_stride = GATEUP ? 1 : kIssuers;
     const int ten = GATEUP ? iss : 0;
     bool ok = true;
-    RingPos xs = {0, 0u}, as = {0, 0u};  // x and A slots of `step`
+    RingPos xs = {0, 0u}, as = {0, 0u}, ds = {0, 0u};  // x slot, A slot and done barrier of `step`
     ring_advance(xs, t_first, SX);
     ring_advance(as, t_first, SA);
+    ring_advance(ds, t_first, D);
     for (int step = t_first; step < nsteps && ok;
-         step += t_stride, ring_advance(xs, t_stride, SX), ring_advance(as, t_stride, SA)) {
+         step += t_stride, ring_advance(xs, t_stride, SX), ring_advance(as, t_stride, SA), ring_advance(ds, t_stride, D)) {
       const int s = as.slot;
       ok = mbar_wait(&bars->x_full[xs.slot], xs.phase, abort_flag, &g_gemm_status) &&
            mbar_wait(&bars->a_full[s], as.phase, abort_flag, &g_gemm_status);
@@ -671,7 +675,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
             umma_f16_ss(d_tm, adesc + (uint64_t)(2 * kk), bdesc + (uint64_t)(2 * kk), idesc,
                         (step > t_first || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&bars->done[s]);
+        umma_commit(&bars->done[ds.slot]);
       }
       __syncwarp();
     }
@@ -694,10 +698,10 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     // half as a runtime value (one copy of its larger code).
     bool ok;
     if (QT == kQ6K || part == 0)
-      ok = dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, SA, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
+      ok = dequant_loop<QT, GATEUP, AT, 0>(smem, L, bars, SA, D, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
                                            p.N, p.q6_group, part, abort_flag);
     else
-      ok = dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, SA, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
+      ok = dequant_loop<QT, GATEUP, AT, 1>(smem, L, bars, SA, D, P, nb, kb_begin, nkb, which, rho, a_lane, a_col0, n0,
                                            p.N, p.q6_group, part, abort_flag);
 
     if (ok) ok = mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status);
@@ -934,11 +938,12 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   p.BN = BN;
   // Pipeline depths (all measured on GB300).  The K-step rings come first: a
   // single-tensor kernel with fewer than 4 x-tile stages ran ~35 % slower.
-  // A-tile and x-tile stages are grown alternately, A first and never fewer
-  // A than x stages (the A tiles wait for the dequant, the x tiles only for a
-  // copy), up to 5 A and 4 x stages (deeper rings were no faster, and slower
-  // for Q6_K attn_v), while shared memory (and, with A in tensor memory,
-  // TMEM) allows.  Two packed-block stages where the rings still reach 4 x
+  // Single-tensor problems grow A-tile and x-tile stages alternately, A first
+  // and never fewer A than x stages; gate/up grows x stages first (its issuers
+  // waited on x tiles while its dequant threads had slack: 3 x + 2 A stages
+  // ran 12 % faster than 2 + 3).  Up to 5 A and 4 x stages (deeper rings were
+  // no faster, and slower for Q6_K attn_v), while shared memory (and, with A
+  // in tensor memory, TMEM) allows.  Two packed-block stages where the rings still reach 4 x
   // stages next to them (cold-cache Q6_K ran faster with two), else one (the
   // dequant threads copy a super-block to registers and release its slot at
   // once, so the refill overlaps the block's four K steps).
@@ -958,7 +963,15 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
     SA_ = 2;
     for (bool grew = true; grew;) {
       grew = false;
-      if (SA_ == SX_ && SA_ < kMaxAStages && fits(SX_, SA_ + 1)) {
+      if (GATEUP) {  // x stages first (x_full waits dominated gate/up), then A
+        if (SX_ < kMaxXStages && fits(SX_ + 1, SA_)) {
+          ++SX_;
+          grew = true;
+        } else if (SA_ < kMaxAStages && fits(SX_, SA_ + 1)) {
+          ++SA_;
+          grew = true;
+        }
+      } else if (SA_ == SX_ && SA_ < kMaxAStages && fits(SX_, SA_ + 1)) {
         ++SA_;
         grew = true;
       } else if (SX_ < SA_ && SX_ < kMaxXStages && fits(SX_ + 1, SA_)) {
