@@ -11,22 +11,24 @@
 // Design (one CTA per 128-weight-row x BN-token output tile, swap-AB so the
 // weights are the UMMA A operand with M = 128 and the tokens are N = BN):
 //   warp 0      producer: TMA loads of the x tile (BN x 64 fp16, 128-byte
-//               swizzle) per 64-wide K step, and of the packed blocks of the
-//               128 weight rows per 256-wide super-block (Q4_K: the two
-//               streams from two lanes, each at its own pace).
+//               swizzle) per 64-wide K step, and (one Q4_K tensor) of the
+//               packed blocks of the 128 weight rows per 256-wide super-block.
 //   warps 1, 2  UMMA issuers (warp 1 also allocates tensor memory): one thread
 //               of each issues tcgen05.mma (kind::f16, fp32 accumulate in
 //               TMEM) and tcgen05.commit for its own accumulator: the gate
 //               and up tensors, or the even and odd K steps of one tensor.
-//   warps 3..   dequantize the packed blocks into fp16 A tiles written straight
-//               into shared memory in the UMMA 128-byte-swizzle K-major layout
-//               (the fp16 weights never touch device memory), then run the
-//               epilogue: tcgen05.ld of the accumulator, fp32 y stores or
-//               silu(g) * u -> fp16.
+//   warps 3..   dequantize the packed blocks into fp16 A tiles, written
+//               straight into shared memory in the UMMA 128-byte-swizzle
+//               K-major layout or into tensor memory (the fp16 weights never
+//               touch device memory), then run the epilogue: tcgen05.ld of
+//               the accumulator, fp32 y stores or silu(g) * u -> fp16.
+//   last warp   (gate/up and Q6_K) copies of the packed blocks, at their own
+//               pace.
 // Pipelines: packed blocks (P stages, one super-block each), x tiles (SX
-// stages) and A tiles (SA >= SX stages), the last two released per K step by
-// the step's UMMA commit.  All waits are bounded mbarrier waits; a timeout
-// raises a device status flag and the CTA drains and exits.
+// stages) and A tiles (SA stages), the last two released per K step by the
+// step's UMMA commit (done barriers, a ring of max(SX, SA)).  All waits are
+// bounded mbarrier waits; a timeout raises a device status flag and the CTA
+// drains and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -63,8 +65,14 @@ struct Cfg {
   // Dequant warps: two threads per weight row and tensor (each dequantizes
   // half of every K step), i.e. two warps per SM sub-partition per tensor.
   static constexpr int kDqWarps = GATEUP ? 16 : 8;
-  static constexpr int kThreads = 32 * (1 + kIssuers + kDqWarps);
+  // Gate/up and Q6_K: the packed blocks come from a warp of their own, after
+  // the dequant warps (measured faster on GB300: the packed copies no longer
+  // wait behind the x ring, nor the x copies behind lanes polling for free
+  // packed slots); one Q4_K tensor: warp 0 issues both, packed block first.
+  static constexpr bool kSplit = GATEUP || QT == kQ6K;
+  static constexpr int kThreads = 32 * (1 + kIssuers + kDqWarps + (kSplit ? 1 : 0));
   static constexpr int kDqWarp0 = 1 + kIssuers;  // first dequant warp
+  static constexpr int kPackedWarp = kDqWarp0 + kDqWarps;  // with kSplit
   static constexpr int kNumB = GATEUP ? 2 : 1;  // weight tensors per tile
   // Arrivals that complete an A stage: Q4_K threads each write half of every
   // step; Q6_K threads write two of every four steps in full.
@@ -534,18 +542,15 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   const int BN = p.BN;
   const uint32_t x_bytes = (uint32_t)BN * kBK * 2;
   constexpr int kPSlotBytes = C::kPSlotBytes;
-  // Gate/up and Q6_K: x tiles and packed blocks from separate producer lanes
-  // (measured faster on GB300: the packed copies no longer wait behind the x
-  // ring); one Q4_K tensor: one loop issues both, packed block first.
-  constexpr bool kSplitProducer = GATEUP || QT == kQ6K;
-  constexpr int kPackedLanes = QT == kQ4K ? 1 : 31;  // split producer: lanes 1 .. kPackedLanes
+  constexpr bool kSplitProducer = C::kSplit;
+  constexpr int kPackedLanes = QT == kQ4K ? 1 : 32;  // lanes of the packed warp that issue copies
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SX; ++s) mbar_init(&bars->x_full[s], 1);
     for (int s = 0; s < SA; ++s) mbar_init(&bars->a_full[s], C::kAArrivals);
     for (int s = 0; s < D; ++s) mbar_init(&bars->done[s], GATEUP ? kIssuers : 1);  // one commit per issuer of the step
     for (int s = 0; s < P; ++s) {
-      mbar_init(&bars->p_full[s], QT == kQ4K ? 1 : (kSplitProducer ? kPackedLanes : 32));
+      mbar_init(&bars->p_full[s], QT == kQ4K ? 1 : 32);
       mbar_init(&bars->p_empty[s], 32 * C::kDqWarps);
     }
     mbar_init(&bars->acc_full, kIssuers);
@@ -581,9 +586,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     int step = 0;
     RingPos xpos = {0, 0u}, dpos = {D - SX, 1u};
     if constexpr (kSplitProducer) {
-      // Lane 0 streams the x tiles, lanes 1 .. kPackedLanes the packed blocks,
-      // each at its own pace: a packed stage is refilled as soon as the
-      // dequant threads have released it, whatever the state of the x ring.
+      // Lane 0 streams the x tiles; the packed warp streams the packed blocks,
+      // each at its own pace.
       if (lane == 0) {
         bool ok = true;
         for (; step < nsteps && ok; ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, D)) {
@@ -592,19 +596,6 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           const int kb = kb_begin + (step >> 2), c = step & 3;
           mbar_arrive_expect_tx(&bars->x_full[xpos.slot], x_bytes);
           tma_load_2d(smem + L.x_off + xpos.slot * L.x_stage, &tm_x, kb * kQK + c * kBK, m0, &bars->x_full[xpos.slot]);
-        }
-      } else if (lane <= kPackedLanes) {
-        RingPos ppos = {0, 0u};
-        for (int i = 0; i < nkb; ++i, ring_advance(ppos, 1, P)) {
-          const int ps = ppos.slot;
-          if (!mbar_wait(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status)) break;
-          // The dequant threads read the slot with plain loads; the refill is
-          // an async-proxy write.  This proxy fence, after the barrier that
-          // their releases completed, orders those reads before the copy
-          // (without any fence the copy was seen to overwrite unread bytes).
-          fence_proxy_async_smem();
-          issue_packed<QT, GATEUP>(smem + L.p_off + ps * C::kNumB * kPSlotBytes, &bars->p_full[ps], &tm_w0, &tm_w1, p,
-                                   kb_begin + i, n0, nb, lane - 1, kPackedLanes);
         }
       }
     } else {
@@ -685,6 +676,24 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     if (lane == 0) umma_commit(&bars->acc_full);
     __syncwarp();
     mbar_wait(&bars->acc_full, 0u, abort_flag, &g_gemm_status, true);
+  } else if (warp == C::kPackedWarp) {
+    // ------------------------------------------------------------------ packed blocks (kSplit)
+    // A packed stage is refilled as soon as the dequant threads have released
+    // it, whatever the state of the x ring.
+    if (lane < kPackedLanes) {
+      RingPos ppos = {0, 0u};
+      for (int i = 0; i < nkb; ++i, ring_advance(ppos, 1, P)) {
+        const int ps = ppos.slot;
+        if (!mbar_wait(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status)) break;
+        // The dequant threads read the slot with plain loads; the refill is
+        // an async-proxy write.  This proxy fence, after the barrier that
+        // their releases completed, orders those reads before the copy
+        // (without any fence the copy was seen to overwrite unread bytes).
+        fence_proxy_async_smem();
+        issue_packed<QT, GATEUP>(smem + L.p_off + ps * C::kNumB * kPSlotBytes, &bars->p_full[ps], &tm_w0, &tm_w1, p,
+                                 kb_begin + i, n0, nb, lane, kPackedLanes);
+      }
+    }
   } else {
     // ------------------------------------------------------------------ dequant + epilogue
     const int t = threadIdx.x - 32 * C::kDqWarp0;  // 0 .. 32*kDqWarps-1
@@ -711,7 +720,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   // ---------------------------------------------------------------- epilogue
   // Dequant warp w reads TMEM lane quarter w % 4 (rows 32q .. 32q+31); the
   // warps sharing a quarter split the BN / 16 column chunks.
-  const bool dq_warp = warp >= C::kDqWarp0;
+  const bool dq_warp = warp >= C::kDqWarp0 && warp < C::kDqWarp0 + C::kDqWarps;
   const int q = warp & 3;
   const int row = q * 32 + lane;
   const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
