@@ -728,12 +728,15 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   const int ngroups = C::kDqWarps / 4, grp = (warp - C::kDqWarp0) >> 2;
   const int per = (nchunks + ngroups - 1) / ngroups;
   const int c_begin = min(nchunks, grp * per), c_end = min(nchunks, c_begin + per);
-  // Split K: the partial tiles of CTAs 1 .. ksplit-1 go to CTA 0's shared
-  // memory ([peer][tensor][row][BN] fp32, in the stage region, free once every
-  // CTA's main loop is done), and CTA 0 adds them in a fixed order.
+  // Split K (single-tensor problems only): the partial tiles of CTAs 1 ..
+  // ksplit-1 go to CTA 0's shared memory ([peer][row][BN] fp32 in the stage
+  // region, free once every CTA's main loop is done; rows padded by 16 bytes
+  // so a warp's 16-byte accesses to 32 consecutive rows spread over all
+  // banks), and CTA 0 adds them in a fixed order.
   const uint32_t peer_buf = smem_u32(smem);
-  const int ksplit = GATEUP ? 1 : p.ksplit;  // the host splits K for single-tensor problems only
-  if (ksplit > 1) {
+  const uint32_t peer_pitch = (uint32_t)BN * 4 + 16;
+  const int ksplit = GATEUP ? 1 : p.ksplit;
+  if (!GATEUP && ksplit > 1) {
     __syncwarp();        // each warp arrives converged (the cluster barrier is .aligned)
     cluster_sync_all();  // every CTA of the cluster is past its main loop
     if (dq_warp && dq_ok && z > 0) {
@@ -744,23 +747,14 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
         tmem_ld16(lane_addr + (uint32_t)(16 * cc), r0);
         tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), r1);
         tmem_wait_ld();
-        // one tensor: D0 + D1 of the peer's tile; gate/up: g and u side by side
-        const uint32_t a = dst0 + (uint32_t)(((((z - 1) * C::kNumB) * 128 + row) * BN + 16 * cc) * 4);
-        if constexpr (!GATEUP) {
+        // D0 + D1 of the peer's tile
+        const uint32_t a = dst0 + (uint32_t)((z - 1) * 128 + row) * peer_pitch + (uint32_t)(64 * cc);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __uint_as_float(r1[i]));
-        }
+        for (int i = 0; i < 16; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __uint_as_float(r1[i]));
 #pragma unroll
         for (int i = 0; i < 4; ++i)
           st_cluster_v4(a + 16 * i, __uint_as_float(r0[4 * i]), __uint_as_float(r0[4 * i + 1]),
                         __uint_as_float(r0[4 * i + 2]), __uint_as_float(r0[4 * i + 3]));
-        if constexpr (GATEUP) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-            st_cluster_v4(a + (uint32_t)(128 * BN * 4) + 16 * i, __uint_as_float(r1[4 * i]),
-                          __uint_as_float(r1[4 * i + 1]), __uint_as_float(r1[4 * i + 2]),
-                          __uint_as_float(r1[4 * i + 3]));
-        }
       }
     }
     __syncwarp();
@@ -775,11 +769,10 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       tmem_ld16(lane_addr + (uint32_t)(16 * cc), ra);
       tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), rb);
       tmem_wait_ld();
+      if constexpr (!GATEUP) {
 #pragma unroll 1
-      for (int zz = 1; zz < ksplit; ++zz) {
-        const uint32_t src = peer_buf + (uint32_t)(((((zz - 1) * C::kNumB) * 128 + row) * BN + 16 * cc) * 4);
-        add_partial16(ra, src);
-        if constexpr (GATEUP) add_partial16(rb, src + (uint32_t)(128 * BN * 4));
+        for (int zz = 1; zz < ksplit; ++zz)
+          add_partial16(ra, peer_buf + (uint32_t)((zz - 1) * 128 + row) * peer_pitch + (uint32_t)(64 * cc));
       }
       if (n < p.N) {
         if constexpr (!GATEUP) {
@@ -1028,7 +1021,7 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
     const int64_t tiles = (int64_t)grid.x * grid.y;
     const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
     for (int c = 8; c >= 2; --c)
-      if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * kBM * BN * 4 <= L.bar_off) {
+      if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * kBM * (BN * 4 + 16) <= L.bar_off) {
         ks = c;
         break;
       }
