@@ -150,9 +150,23 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
   return d;
 }
 
-__device__ __forceinline__ void st_cluster_v4(uint32_t a, float x, float y, float z, float w) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(x), "f"(y), "f"(z), "f"(w)
+__device__ __forceinline__ void sts128_u(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+
+// Bulk copy from this CTA's shared memory to another CTA's of the cluster
+// (dst and mbar are shared::cluster addresses from mapa): 16-byte aligned
+// addresses, size a multiple of 16; completes tx bytes on mbar.
+__device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(src), "r"(bytes), "r"(mbar)
                : "memory");
+}
+
+// Named barrier over `count` threads (whole warps).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128_u(uint32_t a) {
