@@ -517,8 +517,11 @@ __device__ __forceinline__ void issue_packed(uint8_t* pst, uint64_t* full, const
 }
 
 // AT: the dequantized A tiles live in tensor memory (tcgen05.st from the
-// dequant threads, UMMA reads A from TMEM) instead of shared memory.
-template <int QT, bool GATEUP, bool AT>
+// dequant threads, UMMA reads A from TMEM) instead of shared memory.  KS: the
+// kernel holds the split-K exchange (gate/up launches without split K use a
+// KS = false instantiation, which would otherwise spill; single-tensor
+// problems always use KS = true, measured faster on GB300 even unsplit).
+template <int QT, bool GATEUP, bool AT, bool KS>
 __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
                    const __grid_constant__ CUtensorMap tm_w1, const Params p) {
@@ -558,8 +561,9 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     mbar_init(&bars->peer_full, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
-    if (!GATEUP && p.ksplit > 1 && z == 0)  // split K: the bytes of the peers' partial tiles
-      mbar_arrive_expect_tx(&bars->peer_full, (uint32_t)(p.ksplit - 1) * 128u * ((uint32_t)BN * 4 + 16));
+    if (p.ksplit > 1 && z == 0)  // split K: the bytes of the peers' partial tiles
+      mbar_arrive_expect_tx(&bars->peer_full,
+                            (uint32_t)((p.ksplit - 1) * C::kNumB) * 128u * ((uint32_t)BN * 4 + 16));
   }
   // Accumulators: one per issuer, BN columns each (gate / up, or even / odd K
   // steps); with AT also SA x kNumB A tiles of 32 columns (128 rows x 64 fp16)
@@ -732,8 +736,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   const int ngroups = C::kDqWarps / 4, grp = (warp - C::kDqWarp0) >> 2;
   const int per = (nchunks + ngroups - 1) / ngroups;
   const int c_begin = min(nchunks, grp * per), c_end = min(nchunks, c_begin + per);
-  // Split K (single-tensor problems only): CTA z > 0 writes its partial tile
-  // (D0 + D1, [row][BN] fp32 with rows padded by 16 bytes so a warp's
+  // Split K: CTA z > 0 writes its partial tile(s) (one tensor: D0 + D1;
+  // gate/up: G and U; [tensor][row][BN] fp32 with rows padded by 16 bytes so a warp's
   // 16-byte accesses to 32 consecutive rows spread over all banks) into its
   // own stage region, free once its main loop is done, and one bulk copy moves
   // it into slot z - 1 of CTA 0's stage region (after the first cluster
@@ -744,8 +748,9 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
   // measured ~3.5 us slower per tile.)
   const uint32_t peer_buf = smem_u32(smem);
   const uint32_t peer_pitch = (uint32_t)BN * 4 + 16;
-  const int ksplit = GATEUP ? 1 : p.ksplit;
-  if (!GATEUP && ksplit > 1) {
+  const uint32_t peer_slot = (uint32_t)C::kNumB * 128 * peer_pitch;  // one peer's partials
+  const int ksplit = KS ? p.ksplit : 1;
+  if (KS && ksplit > 1) {
     __syncwarp();        // each warp arrives converged (the cluster barrier is .aligned)
     cluster_sync_all();  // every CTA of the cluster is past its main loop
     if (dq_warp && z > 0) {
@@ -757,17 +762,24 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), r1);
           tmem_wait_ld();
           const uint32_t a = peer_buf + (uint32_t)row * peer_pitch + (uint32_t)(64 * cc);
+          if constexpr (!GATEUP) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __uint_as_float(r1[i]));
+            for (int i = 0; i < 16; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __uint_as_float(r1[i]));
+          }
 #pragma unroll
           for (int i = 0; i < 4; ++i) sts128_u(a + 16 * i, r0[4 * i], r0[4 * i + 1], r0[4 * i + 2], r0[4 * i + 3]);
+          if constexpr (GATEUP) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              sts128_u(a + 128 * peer_pitch + 16 * i, r1[4 * i], r1[4 * i + 1], r1[4 * i + 2], r1[4 * i + 3]);
+          }
         }
       }
       fence_proxy_async_smem();  // plain writes, read by the bulk copy (async proxy)
       named_bar_sync(1, 32 * C::kDqWarps);
       if (threadIdx.x == 32 * C::kDqWarp0)
-        bulk_copy_s2cluster(mapa_shared(peer_buf + (uint32_t)(z - 1) * 128 * peer_pitch, 0u), peer_buf,
-                            128 * peer_pitch, mapa_shared(smem_u32(&bars->peer_full), 0u));
+        bulk_copy_s2cluster(mapa_shared(peer_buf + (uint32_t)(z - 1) * peer_slot, 0u), peer_buf, peer_slot,
+                            mapa_shared(smem_u32(&bars->peer_full), 0u));
     }
     if (dq_warp && z == 0) {  // the peers always send, so this wait ends (bounded in any case)
       const bool landed = mbar_wait(&bars->peer_full, 0u, abort_flag, &g_gemm_status, true);
@@ -785,10 +797,14 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       tmem_ld16(lane_addr + (uint32_t)(16 * cc), ra);
       tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), rb);
       tmem_wait_ld();
-      if constexpr (!GATEUP) {
+      if constexpr (KS) {
 #pragma unroll 1
-        for (int zz = 1; zz < ksplit; ++zz)
-          add_partial16(ra, peer_buf + ((uint32_t)(zz - 1) * 128 + (uint32_t)row) * peer_pitch + (uint32_t)(64 * cc));
+        for (int zz = 1; zz < ksplit; ++zz) {
+          const uint32_t src =
+              peer_buf + (uint32_t)(zz - 1) * peer_slot + (uint32_t)row * peer_pitch + (uint32_t)(64 * cc);
+          add_partial16(ra, src);
+          if constexpr (GATEUP) add_partial16(rb, src + 128 * peer_pitch);
+        }
       }
       if (n < p.N) {
         if constexpr (!GATEUP) {
@@ -1022,8 +1038,11 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP, AT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmemLimit);
+    cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP, AT, !GATEUP>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP, AT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemLimit);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
@@ -1033,18 +1052,18 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   // SMs idle (small N or small M): ks CTAs per tile, each with >= 1 super-block,
   // the peers' fp32 partial tiles fitting in CTA 0's stage region.
   int ks = 1;
-  if (!GATEUP) {
+  {
     const int64_t tiles = (int64_t)grid.x * grid.y;
     const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
     for (int c = 8; c >= 2; --c)
-      if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * kBM * (BN * 4 + 16) <= L.bar_off) {
+      if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= L.bar_off) {
         ks = c;
         break;
       }
   }
   p.ksplit = ks;
   if (ks == 1) {
-    gemm_tc_kernel<QT, GATEUP, AT><<<grid, C::kThreads, smem, stream>>>(tx, tw0, tw1, p);
+    gemm_tc_kernel<QT, GATEUP, AT, !GATEUP><<<grid, C::kThreads, smem, stream>>>(tx, tw0, tw1, p);
     return cudaGetLastError();
   }
   grid.z = (unsigned)ks;
@@ -1061,7 +1080,7 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   attr[0].val.clusterDim.z = (unsigned)ks;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<QT, GATEUP, AT>, tx, tw0, tw1, p);
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<QT, GATEUP, AT, true>, tx, tw0, tw1, p);
 }
 
 }  // namespace
