@@ -60,6 +60,13 @@ constexpr uint32_t kH2Magic = 0x64646464u;
 // deterministic.
 constexpr int kIssuers = 2;
 
+// Q6_K: bytes of the 16-byte-aligned window staged for each 210-byte block
+// (the block plus its misalignment, up to 14 bytes, fits in 224).  240 rather
+// than 224: at a 60-word pitch the 16-byte loads of 8 consecutive rows cover
+// all 32 shared-memory banks (at 56 words every fourth row collided; ncu
+// counted 74 % of the Q6_K kernel's shared wavefronts as bank conflicts).
+constexpr int kQ6Win = 240;
+
 template <int QT, bool GATEUP>
 struct Cfg {
   // Dequant warps: two threads per weight row and tensor (each dequantizes
@@ -78,7 +85,7 @@ struct Cfg {
   // step; Q6_K threads write two of every four steps in full.
   static constexpr int kAArrivals = QT == kQ4K ? 32 * kDqWarps : 32 * kDqWarps / 2;
   // One packed-block stage holds a super-block of the tile's rows per tensor.
-  static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : kBM * 224;
+  static constexpr int kPSlotBytes = QT == kQ4K ? kBM * kQ4KBytes : kBM * kQ6Win;
 };
 
 struct Bars {  // capacity: 8 x / A stages, 4 packed stages
@@ -302,10 +309,9 @@ __device__ __forceinline__ void q6_side(const Q6Regs& q, uint32_t (&r)[32]) {
 
 // Q6_K packed stage layout.  The tensor map views the weights as rows of g
 // consecutive weight rows (g * row_bytes is a multiple of 16); box j of a
-// stage holds weight rows n0 + g*i + j (i = 0 .. 128/g - 1) at a 224-byte pitch
+// stage holds weight rows n0 + g*i + j (i = 0 .. 128/g - 1) at a kQ6Win-byte pitch
 // in region j, so every row of region j has the same misalignment
-// (j * row_bytes + 210 * kb) mod 16 of its block inside its 224-byte window.
-constexpr int kQ6Win = 224;
+// (j * row_bytes + 210 * kb) mod 16 of its block inside its window.
 __device__ __forceinline__ uint32_t q6_region_stride(int g) {
   return (uint32_t)(((128 / g) * kQ6Win + 127) / 128 * 128);
 }
@@ -462,7 +468,7 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
 // Q6_K, every lane arrives on `full` (np arrivals).  Q6_K tiles inside the
 // tensor map take g boxes (one per residue j); the last tile, if it holds rows
 // past (N / g) * g, takes one bulk copy per row of the 16-byte-aligned
-// 224-byte window around its block instead (a window that would run past the
+// window around its block instead (a window that would run past the
 // end of the tensor is shortened and its last bytes copied by plain loads).
 template <int QT, bool GATEUP>
 __device__ __forceinline__ void issue_packed(uint8_t* pst, uint64_t* full, const CUtensorMap* tm_w0,
@@ -883,7 +889,7 @@ bool make_tmap_q4k(CUtensorMap* tm, const void* w, int64_t N, int64_t K) {
 }
 
 // Q6_K weights as uint16 rows of g consecutive weight rows (g * row_bytes is a
-// multiple of 16, as tensor maps require); one box = the 224-byte window of one
+// multiple of 16, as tensor maps require); one box = the kQ6Win-byte window of one
 // residue j's blocks for 128/g such rows.
 int q6_group(int64_t K) {
   const int64_t rb = (K / kQK) * kQ6KBytes;
