@@ -150,6 +150,14 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t a, uint32_t rank) {
   return d;
 }
 
+// Hardware tanh approximation (one special-function op, relative error
+// about 2^-11).
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ void sts128_u(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
   asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
 }

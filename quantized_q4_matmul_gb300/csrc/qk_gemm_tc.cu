@@ -826,7 +826,11 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
           for (int i = 0; i < 16; ++i) {
             const int m = m0 + 16 * cc + i;
             const float g = __uint_as_float(ra[i]), u = __uint_as_float(rb[i]);
-            const float o = __fdividef(g, 1.0f + __expf(-g)) * u;  // silu(g) * u
+            // silu(g) * u with sigmoid(g) = 0.5 + 0.5 tanh(g / 2): one
+            // special-function op per element instead of two (exp and a
+            // reciprocal); the epilogue was bound by that unit.
+            const float hg = 0.5f * g;
+            const float o = fmaf(hg, tanh_approx(hg), hg) * u;
             if (m < p.M) y[(int64_t)m * p.N + n] = __float2half_rn(o);
           }
         }
