@@ -129,7 +129,7 @@ struct Params {
   void* y;
   int M, N, K, BN;
   int stages;           // x-tile stages SX
-  int astages;          // A-tile stages SA >= SX (the dequant may run SA steps ahead of the UMMAs)
+  int astages;          // A-tile stages SA (the dequant may run SA steps ahead of the UMMAs; Q6_K: 4)
   int pstages;          // packed-block pipeline depth P
   int ksplit;           // CTAs of a cluster that split the K range of one tile (1 = no split)
   int q6_group;         // Q6_K: rows per tensor-map row (g: g * row_bytes % 16 == 0)
