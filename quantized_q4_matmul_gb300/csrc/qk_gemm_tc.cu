@@ -36,6 +36,9 @@
 #include <algorithm>
 #include <cstdlib>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "qk_device.cuh"
 #include "qk_internal.h"
@@ -950,6 +953,42 @@ int choose_bn(int64_t M, int64_t N) {
 
 constexpr int kSmemLimit = 227 * 1024;
 
+template <int QT, bool GATEUP, bool AT, bool KS>
+__global__ void gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
+                               const __grid_constant__ CUtensorMap tm_w1, const Params p);
+
+// Clusters of c CTAs of the split-K kernel that can be resident at once with
+// `smem` bytes of dynamic shared memory each (cached per size; 0 if the query
+// fails, which disables that split).
+template <int QT, bool GATEUP, bool AT>
+int max_active_clusters(int c, uint32_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<int, uint32_t>, int> cache;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(c, smem);
+  const auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(1, 1, (unsigned)c);
+  cfg.blockDim = dim3(Cfg<QT, GATEUP>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = (unsigned)c;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<QT, GATEUP, AT, true>, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // clear the error; this split size is then not used
+    n = 0;
+  }
+  cache[key] = n;
+  return n;
+}
+
 template <int QT, bool GATEUP, bool AT>
 cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
                       cudaStream_t stream) {
@@ -1060,13 +1099,18 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
   // Split K across a cluster when the tiles would leave at least half of the
   // SMs idle (small N or small M): ks CTAs per tile, each with >= 1 super-block,
-  // the peers' fp32 partial tiles fitting in CTA 0's stage region.
+  // the peers' fp32 partial tiles fitting in CTA 0's stage region, and every
+  // tile's cluster resident at once.  The last condition is the device's
+  // answer for this kernel and cluster size: clusters must fit inside one GPC,
+  // and on GB300 24 clusters of 6 one-CTA-per-SM CTAs did not (a second wave
+  // doubled the time of a 24-tile problem).
   int ks = 1;
   {
     const int64_t tiles = (int64_t)grid.x * grid.y;
     const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
     for (int c = 8; c >= 2; --c)
-      if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= L.bar_off) {
+      if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= L.bar_off &&
+          tiles <= max_active_clusters<QT, GATEUP, AT>(c, smem)) {
         ks = c;
         break;
       }
