@@ -1104,15 +1104,24 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   // answer for this kernel and cluster size: clusters must fit inside one GPC,
   // and on GB300 24 clusters of 6 one-CTA-per-SM CTAs did not (a second wave
   // doubled the time of a 24-tile problem).
+  // Among the feasible sizes, the one with the fewest super-blocks per CTA
+  // (ceil(K/256 / ks): the cluster waits for its slowest CTA), then the
+  // smallest (less exchange).
   int ks = 1;
   {
     const int64_t tiles = (int64_t)grid.x * grid.y;
+    const int64_t nb = K / kQK;
     const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
-    for (int c = 8; c >= 2; --c)
-      if (tiles * c <= num_sms() && c <= K / kQK && (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= L.bar_off &&
-          tiles <= max_active_clusters<QT, GATEUP, AT>(c, smem)) {
-        ks = c;
-        break;
+    int64_t best = nb;
+    if (tiles * 2 <= num_sms())
+      for (int c = 2; c <= 8; ++c) {
+        const int64_t per = (nb + c - 1) / c;
+        if (per < best && tiles * c <= num_sms() && c <= nb &&
+            (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= L.bar_off &&
+            tiles <= max_active_clusters<QT, GATEUP, AT>(c, smem)) {
+          ks = c;
+          best = per;
+        }
       }
   }
   p.ksplit = ks;
