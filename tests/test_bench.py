@@ -1,0 +1,74 @@
+"""bench.py's host-side contract, checked on CPU: the algorithmic work units of a
+step, the JSON line of the reference arm (the fp64 oracle on host cores), and
+the multi-process launch (torchrun, gloo, world size 2: rank 0 alone prints)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+ENV = dict(os.environ, QK_REF_STEP_S="0.3", OMP_NUM_THREADS=os.environ.get("OMP_NUM_THREADS", "4"))
+
+
+def test_step_work_units():
+    """Prefill flops of the step (gate/up, down, attn_v at M=1024) and the decode
+    layer's algorithmic bytes (packed weights of one layer's 7 linears, x, y)."""
+    assert bench.prefill_flops() == 2.0 * 1024 * (2 * 8192 * 3072 + 3072 * 8192 + 1024 * 3072)
+    weights = sum(bench.synth.weight_bytes(l.qtype, l.N, l.K) for l in bench.decode_linears())
+    assert weights == 63_922_176
+    x = sum(2 * l.K for l in bench.decode_linears())
+    y = sum(4 * l.N for l in bench.decode_linears())
+    assert bench.decode_bytes() == weights + x + y == 64_086_016
+
+
+def _json_lines(out):
+    return [json.loads(l) for l in out.splitlines() if l.startswith("{")]
+
+
+def _check_reference_line(d):
+    assert d["impl"] == "reference"
+    assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["steps"] == 1 and d["warmup"] >= 3
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["data"] == "synthetic" and "workload" in d["config"]
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "3"], env=ENV, capture_output=True, text=True, timeout=600, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_reference_line(lines[0])
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def test_reference_arm_two_ranks_gloo():
+    """Launched like the multi-GPU bench (torchrun, one process per rank): the
+    ranks join a gloo group, rank 0 alone runs the oracle and prints one line,
+    and every rank exits 0."""
+    pytest.importorskip("torch.distributed")
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2", "--master-addr",
+           "127.0.0.1", "--master-port", str(_free_port()), os.path.join(ROOT, "bench.py"), "--impl", "reference",
+           "--gpus", "2", "--steps", "1", "--warmup", "3"]
+    r = subprocess.run(cmd, env=ENV, capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = _json_lines(r.stdout)
+    assert len(lines) == 1
+    _check_reference_line(lines[0])
