@@ -284,6 +284,26 @@ def test_workload_model_sweep(qk_lib, cuda, qtype, N, K):
 # ---------------------------------------------------------------------------
 # Gate/up + SwiGLU small shapes
 # ---------------------------------------------------------------------------
+def test_gateup_model_sweep(qk_lib, cuda):
+    """Fused gate/up + SwiGLU at the model's shape (N_ff = 8192, K = 3072) over the
+    token counts whose launch configurations differ (split K at small M, token
+    tile and pipeline depths at large M); sampled output features."""
+    import torch
+    rng = synth.rng_for(12, 0)
+    N, K = 8192, 3072
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    Wgd, Wud = _dev(Wg, cuda), _dev(Wu, cuda)
+    for M in (16, 128, 512, 2048):
+        x = synth.activations(rng, M, K)
+        y = torch.empty(M, N, dtype=torch.float16, device=cuda)
+        qk_lib.qk_gateup_swiglu_q4k(Wgd, Wud, _x_dev(x, cuda), y, M, N, K)
+        qk_lib.qk_get_device_status()
+        rows = sample_rows(N, 24, M)
+        ref = oracle.gateup_swiglu(Wg, Wu, x, N, K, rows=rows)
+        check_close_f16out(y.float().cpu().numpy().astype(np.float64)[:, rows], ref, "gate/up M%d" % M)
+        del y
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 128, 256), (16, 256, 512), (37, 200, 768), (300, 384, 1024)])
 def test_gateup_small(qk_lib, cuda, M, N, K):
     import torch
