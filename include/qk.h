@@ -85,7 +85,10 @@ qk_status qk_dequant_q6k(const void *blocks, int64_t n_blocks, float *out, qk_st
  * in tensor memory),
  * as the overview's "fused dequant -> matrix unit never materializes FP16
  * weights" describes.  The two paths agree within rounding; results are not
- * bit-identical across M.
+ * bit-identical across M.  Single-tensor GEMMs keep the dequantized tiles in
+ * tensor memory where they fit; QK_A_TMEM=0 in the environment (read once per
+ * process) selects shared memory instead, with the same results within
+ * rounding.
  */
 qk_status qk_matmul_q4k(const void *blocks, const uint16_t *x_f16, float *y, int64_t M, int64_t N, int64_t K,
                         qk_stream_t stream);
@@ -99,7 +102,11 @@ qk_status qk_matmul_q6k(const void *blocks, const uint16_t *x_f16, float *y, int
  * "[04] one decode step" and "[06] the target": FFN = SwiGLU):
  *   g = x . Wg^T, u = x . Wu^T (both N_ff x K, Q4_K), fp32 accumulation,
  *   y[m][n] = fp16( g / (1 + exp(-g)) * u ), y is [M][N_ff] fp16.
- * Gate and up weights are two separate Q4_K tensors of the same shape.
+ * Gate and up weights are two separate Q4_K tensors of the same shape.  The
+ * tensor-core path (M > 1) evaluates the sigmoid as 0.5 + 0.5 * tanh(g / 2)
+ * with the hardware tanh approximation (relative error about 2^-11); the
+ * result agrees with the definition within the fp16 output's rounding plus
+ * that error.
  */
 qk_status qk_gateup_swiglu_q4k(const void *gate_blocks, const void *up_blocks, const uint16_t *x_f16,
                                uint16_t *y_f16, int64_t M, int64_t N_ff, int64_t K, qk_stream_t stream);
