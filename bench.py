@@ -116,7 +116,11 @@ class Clocks:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+        # Raw samples (the bench line carries their summary); QK_CLOCKS_DIR
+        # keeps them somewhere else than the temporary directory.
+        import tempfile
+        self.path = os.path.join(os.environ.get("QK_CLOCKS_DIR", tempfile.gettempdir()),
+                                 "clocks_bench_%d.csv" % os.getpid())
 
     def __enter__(self):
         try:
