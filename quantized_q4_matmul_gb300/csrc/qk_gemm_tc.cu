@@ -1030,12 +1030,14 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   // stages next to them (cold-cache Q6_K ran faster with two), else one (the
   // dequant threads copy a super-block to registers and release its slot at
   // once, so the refill overlaps the block's four K steps).
-  // Q6_K takes exactly 4 A stages: its threads write two consecutive K steps
-  // of a super-block and the two halves of a row alternate, so with SA a
-  // multiple of 4 each half owns its A slots and observes every phase of their
-  // done barriers in order (with SA = 2, 3 or 5 a thread could wait on a slot
-  // whose previous phase it never saw, and the parity test then passes a phase
-  // early: seen on GB300 as wrong output with the packed copies running ahead).
+  // Q6_K takes 4 A stages.  Its threads write two consecutive K steps of a
+  // super-block and the two halves of a row alternate.  With SA = 2 a half
+  // waits on a slot whose previous phase (the other half's step) it never
+  // saw, so the parity test can pass a phase early (seen on GB300 as wrong
+  // output once the packed copies ran ahead).  From SA = 3 on, the phase a
+  // half skips belongs to an earlier step of the same issuer, whose UMMAs
+  // complete in order, so it has always completed.  Q6_K keeps SX <= SA (its
+  // done ring is indexed by A slot), and its x ring wants 4 stages.
   constexpr int kMaxXStages = 4, kMaxAStages = QT == kQ6K ? 4 : 5;
   auto depths = [&](int P_, int& SX_, int& SA_) {
     auto fits = [&](int sx, int sa) {
