@@ -26,6 +26,11 @@ test then passes early.  With SA >= 3 the phase a half did not wait for always
 belongs to an earlier step of the same issuer as the phase it does wait for.
 That issuer's UMMAs complete in order, so the phase has completed before the
 awaited one.
+
+A second model checks Q4_K with an x ring and an A ring of different depths.
+The two rings share one done ring of max(SX, SA) barriers, indexed by K step.
+It covers gate/up, where both issuers take every step and a phase needs both
+commits, and single-tensor problems, where the issuers alternate.
 """
 import random
 
@@ -119,3 +124,71 @@ def test_q6k_two_stages_can_pass_early():
     """The failure seen on the GPU (wrong output and a wait timeout once the
     packed copies ran ahead) at SA = 2."""
     assert fooled_in_any(2, q6k=True)
+
+
+def simulate_xa(sx, sa, gateup, blocks=5, seed=0):
+    """x ring (SX) and A ring (SA) with done barriers indexed by K step modulo
+    D = max(SX, SA), as the kernel runs Q4_K: the x producer loads step t after
+    waiting for done(t - SX); the (Q4_K, in-order) dequant writes step t after
+    waiting for done(t - SA); an issuer needs both tiles.  Gate/up: both
+    issuers take every step and a done phase needs both commits; one tensor:
+    the issuers alternate and one commit completes a phase.  Returns True if a
+    wait passed before its phase completed."""
+    rng = random.Random(seed)
+    d = max(sx, sa)
+    steps = 4 * blocks
+    need = 2 if gateup else 1
+    done_c = [0] * d   # completed phases of done[slot]
+    done_n = [0] * d   # commits toward the current phase
+    x_ready = [False] * steps
+    a_ready = [False] * steps
+    issued = [[False] * steps for _ in range(2)]
+    xp = ap = 0        # next step of the x producer and of the dequant
+    fooled = False
+
+    def may_pass(t, lag):  # wait on done(t - lag): phase k of slot (t - lag) % d
+        if t < lag:
+            return True, False
+        u = t - lag
+        k, c = u // d, done_c[u % d]
+        return (c & 1) != (k & 1), c <= k
+
+    while True:
+        acts = []
+        if xp < steps and may_pass(xp, sx)[0]:
+            acts.append(("x", None))
+        if ap < steps and may_pass(ap, sa)[0]:
+            acts.append(("a", None))
+        for e in range(2):
+            order = range(steps) if gateup else range(e, steps, 2)
+            nxt = next((t for t in order if not issued[e][t]), None)
+            if nxt is not None and x_ready[nxt] and a_ready[nxt]:
+                acts.append(("issue", (e, nxt)))
+        if not acts:
+            break
+        kind, arg = rng.choice(acts)
+        if kind == "x":
+            fooled |= may_pass(xp, sx)[1]
+            x_ready[xp] = True
+            xp += 1
+        elif kind == "a":
+            fooled |= may_pass(ap, sa)[1]
+            a_ready[ap] = True
+            ap += 1
+        else:
+            e, t = arg
+            issued[e][t] = True
+            done_n[t % d] += 1
+            if done_n[t % d] == need:
+                done_n[t % d] = 0
+                done_c[t % d] += 1
+    assert xp == steps and ap == steps  # no deadlock
+    return fooled
+
+
+@pytest.mark.parametrize("gateup", [True, False])
+@pytest.mark.parametrize("sx,sa", [(2, 2), (2, 3), (3, 2), (4, 2), (3, 3), (4, 4), (4, 5)])
+def test_q4k_x_and_a_rings_never_pass_early(sx, sa, gateup):
+    """Separate x and A ring depths over one done ring of max(SX, SA): no wait
+    passes early and nothing deadlocks (gate/up runs 3 x + 2 A stages)."""
+    assert not any(simulate_xa(sx, sa, gateup, seed=s) for s in range(800))
