@@ -90,8 +90,8 @@ def _f16(b2):
     return np.ascontiguousarray(b2).view(np.float16).astype(np.float32).reshape(-1)
 
 
-@np.errstate(invalid="ignore", over="ignore")
-def table_decode_q4k(blocks):
+def table_fields_q4k(blocks):
+    """(d, dmin, sc[nb, 256], m[nb, 256], q[nb, 256]) per weight, via the tables."""
     blocks = np.asarray(blocks, dtype=np.uint8).reshape(-1, 144)
     nb = blocks.shape[0]
     d = _f16(blocks[:, 0:2])
@@ -105,35 +105,47 @@ def table_decode_q4k(blocks):
             sc[:, j] |= v
         else:
             mn[:, j] |= v
-    q = np.zeros((nb, 256), np.int16)
-    qs = blocks[:, 16:144].astype(np.int16)
+    # weight-major work arrays (one contiguous row per byte / weight), transposed at the end
+    q = np.zeros((256, nb), np.int16)
+    qs = np.ascontiguousarray(blocks[:, 16:144].T).astype(np.int16)
     for byte, shift, w in q4k_quant_table():
-        q[:, w] = (qs[:, byte] >> shift) & 0xF
+        q[w] = (qs[byte] >> shift) & 0xF
     j = np.arange(256) // 32
-    dsc = (d[:, None] * sc[:, j].astype(np.float32)).astype(np.float32)
-    dmn = (dmin[:, None] * mn[:, j].astype(np.float32)).astype(np.float32)
+    return d, dmin, sc[:, j], mn[:, j], np.ascontiguousarray(q.T)
+
+
+@np.errstate(invalid="ignore", over="ignore")
+def table_decode_q4k(blocks):
+    d, dmin, sc, mn, q = table_fields_q4k(blocks)
+    dsc = (d[:, None] * sc.astype(np.float32)).astype(np.float32)
+    dmn = (dmin[:, None] * mn.astype(np.float32)).astype(np.float32)
     t = (dsc * q.astype(np.float32)).astype(np.float32)
     return (t - dmn).astype(np.float32).reshape(-1)
 
 
-@np.errstate(invalid="ignore", over="ignore")
-def table_decode_q6k(blocks):
+def table_fields_q6k(blocks):
+    """(d, sc[nb, 256], q[nb, 256]) per weight, q already minus 32, via the tables."""
     blocks = np.asarray(blocks, dtype=np.uint8).reshape(-1, 210)
     nb = blocks.shape[0]
-    ql_b = blocks[:, 0:128].astype(np.int16)
-    qh_b = blocks[:, 128:192].astype(np.int16)
+    ql_b = np.ascontiguousarray(blocks[:, 0:128].T).astype(np.int16)
+    qh_b = np.ascontiguousarray(blocks[:, 128:192].T).astype(np.int16)
     sc = blocks[:, 192:208].view(np.int8).astype(np.float32)
     d = _f16(blocks[:, 208:210])
-    lo = np.zeros((nb, 256), np.int16)
-    hi = np.zeros((nb, 256), np.int16)
+    lo = np.zeros((256, nb), np.int16)
+    hi = np.zeros((256, nb), np.int16)
     ql_t, qh_t = q6k_quant_table()
     for byte, shift, w in ql_t:
-        lo[:, w] = (ql_b[:, byte] >> shift) & 0xF
+        lo[w] = (ql_b[byte] >> shift) & 0xF
     for byte, shift, w in qh_t:
-        hi[:, w] = (qh_b[:, byte] >> shift) & 0x3
-    q = (lo | (hi << 4)) - 32
-    t = np.arange(256) // 16
-    dsc = (d[:, None] * sc[:, t]).astype(np.float32)
+        hi[w] = (qh_b[byte] >> shift) & 0x3
+    q = np.ascontiguousarray(((lo | (hi << 4)) - 32).T)
+    return d, sc[:, np.arange(256) // 16], q
+
+
+@np.errstate(invalid="ignore", over="ignore")
+def table_decode_q6k(blocks):
+    d, sc, q = table_fields_q6k(blocks)
+    dsc = (d[:, None] * sc).astype(np.float32)
     return (dsc * q.astype(np.float32)).astype(np.float32).reshape(-1)
 
 
@@ -310,10 +322,40 @@ def random_blocks(qtype, n, seed):
     return np.concatenate([a, b])
 
 
-def pin_bruteforce_vs_table_decoder(O, n=100_000, seed=7):
+def pin_bruteforce_vs_table_decoder(O, n=100_000, seed=7, chunk=4096):
+    """The oracle against the table decoder, bit for bit, on n random blocks
+    (decoded in chunks: a few small working arrays instead of several
+    hundred MB of fresh memory)."""
     for qtype, dec in ((Q4K, table_decode_q4k), (Q6K, table_decode_q6k)):
         blocks = random_blocks(qtype, n, seed + qtype)
-        assert same_bits(O.dequant(qtype, blocks), dec(blocks)), qtype
+        for c in range(0, n, chunk):
+            part = blocks[c:c + chunk]
+            assert same_bits(O.dequant(qtype, part), dec(part)), (qtype, c)
+
+
+@np.errstate(invalid="ignore", over="ignore")
+def pin_dequant_correctly_rounded(O, n=8192, seed=3):
+    """Every weight is the exact real value of its formula, rounded once to fp32.
+
+    The products are exact in fp32: an fp16 scale has 11 significant bits, a
+    Q4_K scale or min 6 and a quant 4 (21 bits in all); a Q6_K int8 scale has
+    at most 7 significant bits and |q - 32| <= 32 at most 5 (23 bits).  So a
+    Q6_K weight is exact, and a Q4_K weight has a single rounding, at the
+    subtraction.  The reference value is computed in fp64 (exact for the
+    products; fp64 to fp32 double rounding is innocuous for one subtraction of
+    fp32 values, 53 >= 2*24 + 2) and compared bit for bit.  The order in which
+    the products are formed, or a fused multiply-add at the subtraction,
+    therefore cannot change a bit."""
+    b4 = random_blocks(Q4K, n, seed)
+    d, dmin, sc, mn, q = table_fields_q4k(b4)
+    exact = (d[:, None].astype(np.float64) * sc * q - dmin[:, None].astype(np.float64) * mn)
+    assert same_bits(O.dequant(Q4K, b4), exact.astype(np.float32).reshape(-1))
+    b6 = random_blocks(Q6K, n, seed + 1)
+    d, sc, q = table_fields_q6k(b6)
+    exact = d[:, None].astype(np.float64) * sc.astype(np.float64) * q
+    finite = np.isfinite(exact)
+    assert (exact[finite] == exact[finite].astype(np.float32)).all()  # no rounding at all
+    assert same_bits(O.dequant(Q6K, b6), exact.astype(np.float32).reshape(-1))
 
 
 def _mat(qtype, N, K, seed):
@@ -424,6 +466,7 @@ ALL_PINS = [
     pin_q6k_worked_block,
     pin_q6k_closed_forms,
     pin_bruteforce_vs_table_decoder,
+    pin_dequant_correctly_rounded,
     pin_matmul_onehot,
     pin_matmul_ones_rowsum,
     pin_matmul_vs_numpy_f64,

@@ -3,6 +3,12 @@
 Each mutant is the oracle's C source with one textual change, compiled into a
 temporary directory; the real oracle is never modified.  A mutant that passed
 every pin would mean the pins leave that part of the oracle unchecked.
+
+Reordering the dequant's multiplications, e.g. d*(sc*q) for (d*sc)*q, is not
+a mutant: every product of an fp16 scale, a 6-bit (Q4_K) or int8 (Q6_K)
+scale and a quant is exact in fp32 (21 and 23 significant bits).  Any order
+gives the same bits; the pin that every weight is its exact value rounded
+once to fp32 states that directly.
 """
 import os
 
@@ -43,6 +49,16 @@ MUTANTS = [
      "g += xm[k] * (double)wu[k];\n                    u += xm[k] * (double)wg[k];"),
     ("silu_sign", "g / (1.0 + exp(-g))", "g / (1.0 + exp(g))"),
     ("swiglu_times_gate", "out[m * n_rows + r] = silu * u;", "out[m * n_rows + r] = silu * g;"),
+    ("silu_of_up", "const double silu = g / (1.0 + exp(-g));", "const double silu = u / (1.0 + exp(-u));"),
+    # field offsets inside a block
+    ("q4k_dmin_offset", "rd16(blk + 2)", "rd16(blk)"),
+    ("q4k_scales_offset", "const uint8_t *s = blk + 4;", "const uint8_t *s = blk + 3;"),
+    ("q4k_quants_offset", "const uint8_t *qs = blk + 16;", "const uint8_t *qs = blk + 15;"),
+    ("q6k_qh_offset", "const uint8_t *qh = blk + 128;", "const uint8_t *qh = blk + 64;"),
+    ("q6k_scales_unsigned", "const int8_t *sc = (const int8_t *)(blk + 192);",
+     "const uint8_t *sc = (const uint8_t *)(blk + 192);"),
+    ("q6k_lane_of_16", "l = i % 32;", "l = i % 16;"),
+    ("half_sign_dropped", "return sign ? -v : v;", "return v;"),
 ]
 
 
