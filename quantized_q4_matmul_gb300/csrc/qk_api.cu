@@ -6,6 +6,7 @@
 // overflow), output aliasing an input, and the device architecture.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <vector>
@@ -21,18 +22,20 @@ constexpr int64_t kMaxDim = (int64_t)1 << 31;  // M, N, K each below 2^31
 
 // sm_103 check, cached per device.
 qk_status check_device() {
-  static int checked[64] = {0};  // 0 unknown, 1 ok, 2 unsupported
+  static std::atomic<int> checked[qk::kMaxDevices];  // 0 unknown, 1 ok, 2 unsupported
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return QK_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return QK_ERR_UNSUPPORTED_DEVICE;
-  if (!checked[dev]) {
+  if (dev < 0 || dev >= qk::kMaxDevices) return QK_ERR_UNSUPPORTED_DEVICE;
+  int v = checked[dev].load(std::memory_order_relaxed);
+  if (!v) {
     int major = 0, minor = 0;
     if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
       return QK_ERR_CUDA;
-    checked[dev] = (major == 10 && minor == 3) ? 1 : 2;
+    v = (major == 10 && minor == 3) ? 1 : 2;
+    checked[dev].store(v, std::memory_order_relaxed);
   }
-  return checked[dev] == 1 ? QK_OK : QK_ERR_UNSUPPORTED_DEVICE;
+  return v == 1 ? QK_OK : QK_ERR_UNSUPPORTED_DEVICE;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -199,6 +202,28 @@ qk_status matmul_batch(const qk_matmul_desc* d, int count, cudaStream_t s) {
 }
 
 }  // namespace
+
+namespace qk {
+
+int current_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  return dev;
+}
+
+int device_sms() {
+  static std::atomic<int> sms[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return 152;
+  int v = sms[dev].load(std::memory_order_relaxed);
+  if (v <= 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0) v = 152;
+    sms[dev].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
+}  // namespace qk
 
 extern "C" {
 

@@ -38,6 +38,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <utility>
 
 #include "qk_device.cuh"
@@ -918,18 +919,6 @@ bool make_tmap_q6k(CUtensorMap* tm, const void* w, int64_t N, int64_t K, int g) 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int g_sms_tc = 0;
-
-int num_sms() {
-  if (!g_sms_tc) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms_tc, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms_tc <= 0) g_sms_tc = 148;
-  }
-  return g_sms_tc;
-}
-
 // Token tile: the multiple of 16 (<= 256) that minimises waves x tile cost,
 // where a tile costs its MMA time (~BN) plus a per-tile share (dequantizing
 // the 128 x K weight tile and the epilogue) worth about 64 tokens; ties go to
@@ -937,11 +926,12 @@ int num_sms() {
 int choose_bn(int64_t M, int64_t N) {
   const int64_t ntn = (N + kBM - 1) / kBM;
   if (M <= kMaxBN) return (int)((M + 15) / 16 * 16);
+  const int64_t sms = device_sms();
   int best = kMaxBN;
   double best_cost = 1e30;
   for (int bn = kMaxBN; bn >= 128; bn -= 16) {
     const int64_t tiles = ntn * ((M + bn - 1) / bn);
-    const int64_t waves = (tiles + num_sms() - 1) / num_sms();
+    const int64_t waves = (tiles + sms - 1) / sms;
     const double cost = (double)waves * (bn + 64);
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
@@ -958,14 +948,14 @@ __global__ void gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const _
                                const __grid_constant__ CUtensorMap tm_w1, const Params p);
 
 // Clusters of c CTAs of the split-K kernel that can be resident at once with
-// `smem` bytes of dynamic shared memory each (cached per size; 0 if the query
-// fails, which disables that split).
+// `smem` bytes of dynamic shared memory each (cached per device and size; 0 if
+// the query fails, which disables that split).
 template <int QT, bool GATEUP, bool AT>
 int max_active_clusters(int c, uint32_t smem) {
   static std::mutex mu;
-  static std::map<std::pair<int, uint32_t>, int> cache;
+  static std::map<std::tuple<int, int, uint32_t>, int> cache;
   std::lock_guard<std::mutex> lock(mu);
-  const auto key = std::make_pair(c, smem);
+  const auto key = std::make_tuple(current_device(), c, smem);
   const auto it = cache.find(key);
   if (it != cache.end()) return it->second;
   cudaLaunchConfig_t cfg;
@@ -1087,15 +1077,16 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   p.ksplit = 1;
   const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, SX, SA, P).total;
   if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static PerDeviceFlag attr_set;  // the shared-memory limit is a per-device function attribute
+  const int dev = current_device();
+  if (!attr_set.done(dev)) {
     cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP, AT, !GATEUP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemLimit);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(gemm_tc_kernel<QT, GATEUP, AT, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemLimit);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set.mark(dev);
   }
   dim3 grid((unsigned)((N + kBM - 1) / kBM), (unsigned)((M + BN - 1) / BN));
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
@@ -1115,10 +1106,11 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
     const int64_t nb = K / kQK;
     const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
     int64_t best = nb;
-    if (tiles * 2 <= num_sms())
+    const int64_t sms = device_sms();
+    if (tiles * 2 <= sms)
       for (int c = 2; c <= 8; ++c) {
         const int64_t per = (nb + c - 1) / c;
-        if (per < best && tiles * c <= num_sms() && c <= nb &&
+        if (per < best && tiles * c <= sms && c <= nb &&
             (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= L.bar_off &&
             tiles <= max_active_clusters<QT, GATEUP, AT>(c, smem)) {
           ks = c;

@@ -560,18 +560,6 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     run_gemv_problem<kQ6K>(P, cta, B, smem, stages, sh);
 }
 
-int g_sms = 0;
-
-int sm_count() {
-  if (!g_sms) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms <= 0) g_sms = 148;
-  }
-  return g_sms;
-}
-
 }  // namespace
 
 int gemv_max_m() { return 1; }
@@ -638,7 +626,7 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     total += (double)bytes[i];
   }
   const size_t smem = x_bytes + kSharedBytes + ring + 128;
-  const int budget = std::max(count, sm_count());
+  const int budget = std::max(count, device_sms());
   int used = 0;
   for (int i = 0; i < count; ++i) {
     int c = (int)((double)budget * (double)bytes[i] / total);
@@ -668,11 +656,12 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     B.p[i].cta_begin = begin;
     begin += B.p[i].ctas;
   }
-  static bool attr = false;
-  if (!attr) {
+  static PerDeviceFlag attr;  // the shared-memory limit is a per-device function attribute
+  const int dev = current_device();
+  if (!attr.done(dev)) {
     cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
     if (e != cudaSuccess) return e;
-    attr = true;
+    attr.mark(dev);
   }
   gemv_stream_kernel<<<begin, kThreads, smem, s>>>(B);
   return cudaGetLastError();

@@ -2,6 +2,7 @@
 // units (launchers, status words).  Not part of the public C ABI.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -16,6 +17,30 @@ constexpr int kQ4KBytes = 144;
 constexpr int kQ6KBytes = 210;
 
 inline int64_t block_bytes(QType t) { return t == kQ4K ? kQ4KBytes : kQ6KBytes; }
+
+// Host state that CUDA keeps per device (function attributes, SM counts,
+// occupancy answers) is cached per device index, for processes that drive
+// several GPUs.
+constexpr int kMaxDevices = 64;
+
+// The calling thread's current device, or -1 if it cannot be read or is out
+// of range.
+int current_device();
+
+// The current device's SM count (queried once per device).
+int device_sms();
+
+// One bit per device: set once that device's one-time setup has succeeded.
+class PerDeviceFlag {
+ public:
+  bool done(int dev) const { return dev >= 0 && ((bits_.load(std::memory_order_acquire) >> dev) & 1u); }
+  void mark(int dev) {
+    if (dev >= 0) bits_.fetch_or(uint64_t(1) << dev, std::memory_order_release);
+  }
+
+ private:
+  std::atomic<uint64_t> bits_{0};
+};
 
 // Each translation unit with kernels that can time out owns one device status
 // word; these read it (after the stream has been synchronised) and clear it.
