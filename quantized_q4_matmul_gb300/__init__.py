@@ -4,7 +4,10 @@ This module only marshals arguments: every step of the computation runs in the
 CUDA kernels behind the C ABI declared in ``include/qk.h``.  Functions take
 torch tensors (device memory) or raw integer addresses, plus an optional CUDA
 stream (default: torch's current stream), and raise ``QKError`` on any non-zero
-status.  There is no CPU fallback: if ``libqk.so`` is missing or cannot be
+status.  A tensor argument must be contiguous and large enough for the call
+(x and fp16 outputs fp16, or its bits as int16 / uint16; fp32 outputs
+float32), else ``ValueError`` is raised before the library is called; raw
+addresses are the caller's responsibility.  There is no CPU fallback: if ``libqk.so`` is missing or cannot be
 loaded, every call raises.
 """
 from __future__ import annotations
@@ -75,12 +78,38 @@ def lib():
     return _lib
 
 
-def _addr(t) -> int:
+# dtypes accepted for fp16 buffers (x, the SwiGLU output): fp16 itself or its bits
+_F16 = ("torch.float16", "torch.uint16", "torch.int16")
+_F32 = ("torch.float32",)
+
+
+def _buf(t, nbytes: int, what: str, dtypes=None) -> int:
+    """The address of a buffer argument.  A raw integer address (or None) is
+    passed through unchecked.  A tensor must be contiguous, of one of `dtypes`
+    (any dtype if None), and hold at least `nbytes` bytes: the C ABI takes
+    plain pointers and cannot see how large a buffer is."""
     if t is None:
         return 0
     if isinstance(t, int):
         return t
+    if dtypes is not None and str(t.dtype) not in dtypes:
+        raise ValueError("%s: dtype %s, expected one of %s" % (what, t.dtype, ", ".join(dtypes)))
+    if not t.is_contiguous():
+        raise ValueError("%s: the tensor is not contiguous" % what)
+    have = t.numel() * t.element_size()
+    if have < nbytes:
+        raise ValueError("%s: holds %d bytes, the call needs %d" % (what, have, nbytes))
     return int(t.data_ptr())
+
+
+def _n(v) -> int:
+    return max(int(v), 0)
+
+
+def _weight_bytes(qtype, N, K) -> int:
+    """Bytes of N rows of K/256 super-blocks (0 for shapes the library rejects)."""
+    bb = {QK_Q4_K: 144, QK_Q6_K: 210}.get(qtype, 0)
+    return _n(N) * (_n(K) // 256) * bb
 
 
 def _stream(stream) -> int:
@@ -105,27 +134,44 @@ def qk_version() -> int:
     return int(lib().qk_version())
 
 
+def _dequant(name, qtype, blocks, n_blocks, out, stream):
+    nb = _n(n_blocks)
+    w = _buf(blocks, nb * (144 if qtype == QK_Q4_K else 210), name + ": blocks")
+    o = _buf(out, nb * 256 * 4, name + ": out", _F32)
+    _check(getattr(lib(), name)(w, int(n_blocks), o, _stream(stream)), name)
+
+
 def qk_dequant_q4k(blocks, n_blocks: int, out, stream=None) -> None:
-    _check(lib().qk_dequant_q4k(_addr(blocks), int(n_blocks), _addr(out), _stream(stream)), "qk_dequant_q4k")
+    _dequant("qk_dequant_q4k", QK_Q4_K, blocks, n_blocks, out, stream)
 
 
 def qk_dequant_q6k(blocks, n_blocks: int, out, stream=None) -> None:
-    _check(lib().qk_dequant_q6k(_addr(blocks), int(n_blocks), _addr(out), _stream(stream)), "qk_dequant_q6k")
+    _dequant("qk_dequant_q6k", QK_Q6_K, blocks, n_blocks, out, stream)
+
+
+def _matmul(name, qtype, blocks, x_f16, y, M, N, K, stream):
+    w = _buf(blocks, _weight_bytes(qtype, N, K), name + ": blocks")
+    x = _buf(x_f16, _n(M) * _n(K) * 2, name + ": x_f16", _F16)
+    o = _buf(y, _n(M) * _n(N) * 4, name + ": y", _F32)
+    _check(getattr(lib(), name)(w, x, o, int(M), int(N), int(K), _stream(stream)), name)
 
 
 def qk_matmul_q4k(blocks, x_f16, y, M: int, N: int, K: int, stream=None) -> None:
-    _check(lib().qk_matmul_q4k(_addr(blocks), _addr(x_f16), _addr(y), int(M), int(N), int(K), _stream(stream)),
-           "qk_matmul_q4k")
+    _matmul("qk_matmul_q4k", QK_Q4_K, blocks, x_f16, y, M, N, K, stream)
 
 
 def qk_matmul_q6k(blocks, x_f16, y, M: int, N: int, K: int, stream=None) -> None:
-    _check(lib().qk_matmul_q6k(_addr(blocks), _addr(x_f16), _addr(y), int(M), int(N), int(K), _stream(stream)),
-           "qk_matmul_q6k")
+    _matmul("qk_matmul_q6k", QK_Q6_K, blocks, x_f16, y, M, N, K, stream)
 
 
 def qk_gateup_swiglu_q4k(gate_blocks, up_blocks, x_f16, y_f16, M: int, N_ff: int, K: int, stream=None) -> None:
-    _check(lib().qk_gateup_swiglu_q4k(_addr(gate_blocks), _addr(up_blocks), _addr(x_f16), _addr(y_f16), int(M),
-                                      int(N_ff), int(K), _stream(stream)), "qk_gateup_swiglu_q4k")
+    name = "qk_gateup_swiglu_q4k"
+    wb = _weight_bytes(QK_Q4_K, N_ff, K)
+    g = _buf(gate_blocks, wb, name + ": gate_blocks")
+    u = _buf(up_blocks, wb, name + ": up_blocks")
+    x = _buf(x_f16, _n(M) * _n(K) * 2, name + ": x_f16", _F16)
+    o = _buf(y_f16, _n(M) * _n(N_ff) * 2, name + ": y_f16", _F16)
+    _check(lib().qk_gateup_swiglu_q4k(g, u, x, o, int(M), int(N_ff), int(K), _stream(stream)), name)
 
 
 def qk_matmul_batch(problems, stream=None) -> None:
@@ -135,9 +181,16 @@ def qk_matmul_batch(problems, stream=None) -> None:
     arr = (qk_matmul_desc * max(1, len(problems)))()
     for i, p in enumerate(problems):
         qt = p["qtype"]
-        qt = {"q4k": QK_Q4_K, "q6k": QK_Q6_K}.get(qt, qt)
-        arr[i] = qk_matmul_desc(int(qt), _addr(p["blocks"]), _addr(p.get("up_blocks")), _addr(p["x_f16"]),
-                                _addr(p["y"]), int(p["M"]), int(p["N"]), int(p["K"]))
+        qt = int({"q4k": QK_Q4_K, "q6k": QK_Q6_K}.get(qt, qt))
+        M, N, K = int(p["M"]), int(p["N"]), int(p["K"])
+        what = "qk_matmul_batch[%d]" % i
+        gu = p.get("up_blocks") is not None
+        wb = _weight_bytes(qt, N, K)
+        arr[i] = qk_matmul_desc(qt, _buf(p["blocks"], wb, what + ": blocks"),
+                                _buf(p.get("up_blocks"), wb, what + ": up_blocks"),
+                                _buf(p["x_f16"], _n(M) * _n(K) * 2, what + ": x_f16", _F16),
+                                _buf(p["y"], _n(M) * _n(N) * (2 if gu else 4), what + ": y", _F16 if gu else _F32),
+                                M, N, K)
     _check(lib().qk_matmul_batch(arr, len(problems), _stream(stream)), "qk_matmul_batch")
 
 

@@ -95,3 +95,43 @@ def test_batch_rejects_bad_arguments_on_the_host(qk_lib):
     assert L.qk_matmul_batch(arr, 1, None) == -2
     arr = (D * 1)(D(0, A16, None, A16, A16, 1, 8, 300))
     assert L.qk_matmul_batch(arr, 1, None) == -3
+
+
+def test_binding_checks_tensor_buffers_before_the_call(qk_lib):
+    """Tensor arguments are checked for dtype, contiguity and size in the
+    binding (the C ABI sees only pointers), before the library is called."""
+    torch = pytest.importorskip("torch")
+    M, N, K = 4, 8, 256
+    W = torch.zeros(N * 144, dtype=torch.uint8)
+    x = torch.zeros(M, K, dtype=torch.float16)
+    y = torch.zeros(M, N, dtype=torch.float32)
+    bad = [
+        lambda: qk_lib.qk_matmul_q4k(W, x.float(), y, M, N, K, stream=0),             # x not fp16
+        lambda: qk_lib.qk_matmul_q4k(W, x.t().contiguous().t(), y, M, N, K, stream=0),  # x not contiguous
+        lambda: qk_lib.qk_matmul_q4k(W, x, y[:, :4], M, N, K, stream=0),               # y not contiguous
+        lambda: qk_lib.qk_matmul_q4k(W, x, y.half(), M, N, K, stream=0),               # y not fp32
+        lambda: qk_lib.qk_matmul_q4k(W, x, y[:3], M, N, K, stream=0),                  # y too small
+        lambda: qk_lib.qk_matmul_q4k(W[:-1], x, y, M, N, K, stream=0),                 # weights too small
+        lambda: qk_lib.qk_matmul_q6k(W, x, y, M, N, K, stream=0),                      # 144 B < 210 B blocks
+        lambda: qk_lib.qk_matmul_q4k(W, x[:, :128], y, M, N, K, stream=0),             # x not contiguous
+        lambda: qk_lib.qk_gateup_swiglu_q4k(W, W, x, y, M, N, K, stream=0),            # SwiGLU output is fp16
+        lambda: qk_lib.qk_gateup_swiglu_q4k(W, W[:10], x, y.half(), M, N, K, stream=0),  # up too small
+        lambda: qk_lib.qk_dequant_q4k(W, N, torch.zeros(N * 256, dtype=torch.float16), stream=0),
+        lambda: qk_lib.qk_dequant_q6k(W, N, torch.zeros(N * 256), stream=0),          # 8 x 210 B > W
+        lambda: qk_lib.qk_matmul_batch([dict(qtype="q4k", blocks=W, x_f16=x, y=y[:2], M=M, N=N, K=K)], stream=0),
+        lambda: qk_lib.qk_matmul_batch([dict(qtype="q4k", blocks=W, up_blocks=W, x_f16=x, y=y, M=M, N=N, K=K)],
+                                       stream=0),                                       # gate/up y is fp16
+    ]
+    for i, call in enumerate(bad):
+        with pytest.raises(ValueError):
+            call()
+    # Well-formed host tensors pass the binding and reach the library, which
+    # rejects them (no device here, or host memory on a GPU machine).
+    for call in (lambda: qk_lib.qk_matmul_q4k(W, x, y, M, N, K, stream=0),
+                 lambda: qk_lib.qk_matmul_q4k(W, x.view(torch.int16), y, M, N, K, stream=0),
+                 lambda: qk_lib.qk_gateup_swiglu_q4k(W, W, x, y.half(), M, N, K, stream=0),
+                 lambda: qk_lib.qk_matmul_batch([dict(qtype="q4k", blocks=W, up_blocks=W, x_f16=x, y=y.half(), M=M,
+                                                      N=N, K=K)], stream=0)):
+        with pytest.raises(qk_lib.QKError) as e:
+            call()
+        assert e.value.status in (-4, -6, -8)  # CUDA error, unsupported device, inaccessible pointer
