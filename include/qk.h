@@ -80,7 +80,10 @@ qk_status qk_dequant_q6k(const void *blocks, int64_t n_blocks, float *out, qk_st
  * "Building DAMASCUS", "Prefill and decode need different performance
  * questions").  M = 1 runs the decode GEMV (products of the integer quants
  * with fp16 x are exact, sums fp32, block scales applied per sub-block in
- * fp32); larger M runs the tensor-core GEMM (weights dequantized to fp16 in
+ * fp32) where its shared-memory plan fits K (see qk_decode_uses_gemv: every
+ * K up to 6144 and K = 8192 do, in both formats and for gate/up); larger M,
+ * and an M = 1 problem whose K the GEMV cannot stage, runs the tensor-core
+ * GEMM (weights dequantized to fp16 in
  * shared or tensor memory, never written to device memory; fp32 accumulation
  * in tensor memory),
  * as the overview's "fused dequant -> matrix unit never materializes FP16
@@ -159,6 +162,17 @@ qk_status qk_get_device_status(qk_stream_t stream);
  * Returns QK_ERR_UNSUPPORTED_DEVICE or QK_ERR_CUDA on launch problems.
  */
 qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream);
+
+/*
+ * Host-only query (no CUDA call): 1 if an M = 1 problem in format `qtype`
+ * (QK_Q4_K / QK_Q6_K; with gateup != 0 the fused gate/up + SwiGLU, Q4_K only)
+ * and inner size K runs on the decode GEMV, 0 if it runs on the tensor-core
+ * GEMM because the GEMV cannot stage it (x of K plus two weight stages must
+ * fit in shared memory), -1 for an invalid qtype or K.  The answer depends
+ * only on these arguments; grouped calls (qk_matmul_batch) launch problems
+ * together only while their joint plan fits.
+ */
+int qk_decode_uses_gemv(int qtype, int gateup, int64_t K);
 
 /* A static, human-readable name for a status code. */
 const char *qk_status_string(qk_status status);

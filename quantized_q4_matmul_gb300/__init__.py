@@ -18,14 +18,15 @@ import os
 __all__ = [
     "QKError", "lib", "lib_path", "qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k",
     "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout",
-    "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
+    "qk_decode_uses_gemv", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 QK_BLOCK_BYTES = {"q4k": 144, "q6k": 210}
 
 SYMBOLS = ("qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k", "qk_gateup_swiglu_q4k",
-           "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout", "qk_status_string", "qk_version")
+           "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout", "qk_decode_uses_gemv",
+           "qk_status_string", "qk_version")
 
 QK_Q4_K, QK_Q6_K = 0, 1
 
@@ -72,6 +73,7 @@ def lib():
         L.qk_matmul_batch.argtypes = [ctypes.POINTER(qk_matmul_desc), i32, vp]
         L.qk_get_device_status.restype, L.qk_get_device_status.argtypes = i32, [vp]
         L.qk_debug_wait_timeout.restype, L.qk_debug_wait_timeout.argtypes = i32, [i64, vp]
+        L.qk_decode_uses_gemv.restype, L.qk_decode_uses_gemv.argtypes = i32, [i32, i32, i64]
         L.qk_status_string.restype, L.qk_status_string.argtypes = ctypes.c_char_p, [i32]
         L.qk_version.restype, L.qk_version.argtypes = i32, []
         _lib = L
@@ -192,6 +194,16 @@ def qk_matmul_batch(problems, stream=None) -> None:
                                 _buf(p["y"], _n(M) * _n(N) * (2 if gu else 4), what + ": y", _F16 if gu else _F32),
                                 M, N, K)
     _check(lib().qk_matmul_batch(arr, len(problems), _stream(stream)), "qk_matmul_batch")
+
+
+def qk_decode_uses_gemv(qtype, K: int, gateup: bool = False) -> bool:
+    """Whether an M = 1 problem of this format and K runs on the decode GEMV
+    (True) or on the tensor-core GEMM (False); host only."""
+    qt = {"q4k": QK_Q4_K, "q6k": QK_Q6_K}.get(qtype, qtype)
+    r = int(lib().qk_decode_uses_gemv(int(qt), int(bool(gateup)), int(K)))
+    if r < 0:
+        raise ValueError("qk_decode_uses_gemv: invalid qtype %r or K %d" % (qtype, K))
+    return bool(r)
 
 
 def qk_get_device_status(stream=None) -> None:

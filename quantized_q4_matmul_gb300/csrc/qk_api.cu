@@ -128,19 +128,14 @@ qk_status validate_device(const void* W, const void* W_up, const uint16_t* x, co
   return QK_OK;
 }
 
-// The decode GEMV handles M = 1.
-bool use_gemv(int64_t M, int64_t K, bool gateup) {
-  (void)K;
-  (void)gateup;
-  return M <= qk::gemv_max_m();
-}
+// The decode GEMV handles M = 1 when its shared-memory plan fits K; the
+// tensor-core GEMM takes everything else (M = 1 as a one-token tile).
+bool use_gemv(const qk::GemvDesc& d, int64_t M) { return M <= qk::gemv_max_m() && qk::gemv_plan_fits(&d, 1); }
 
 qk_status run(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
               bool gateup, cudaStream_t s) {
-  if (use_gemv(M, K, gateup)) {
-    qk::GemvDesc d{t, W, gateup ? W_up : nullptr, x, y, N, K};
-    return map_cuda(qk::launch_gemv_batch(&d, 1, s));
-  }
+  const qk::GemvDesc d{t, W, gateup ? W_up : nullptr, x, y, N, K};
+  if (use_gemv(d, M)) return map_cuda(qk::launch_gemv_batch(&d, 1, s));
   return map_cuda(qk::launch_gemm(t, W, W_up, x, y, M, N, K, gateup, s));
 }
 
@@ -180,25 +175,39 @@ qk_status matmul_batch(const qk_matmul_desc* d, int count, cudaStream_t s) {
           (d[j].up_blocks && overlaps(d[i].y, ck[(size_t)i].y_bytes, d[j].up_blocks, wb)))
         return QK_ERR_ALIAS;
     }
+  // M = 1 problems share GEMV launches: a problem joins the current group if
+  // the group's plan still fits with it (x of the largest K is staged once per
+  // CTA), else the group is launched first.
   std::vector<qk::GemvDesc> group;
+  auto flush = [&]() -> qk_status {
+    if (group.empty()) return QK_OK;
+    const qk_status st = map_cuda(qk::launch_gemv_batch(group.data(), (int)group.size(), s));
+    group.clear();
+    return st;
+  };
   for (int i = 0; i < count; ++i) {
     if (d[i].M == 0 || d[i].N == 0) continue;
     const QType t = d[i].qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K;
     const bool gu = d[i].up_blocks != nullptr;
-    if (use_gemv(d[i].M, d[i].K, gu)) {
-      group.push_back(qk::GemvDesc{t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].N, d[i].K});
-      if ((int)group.size() == qk::kMaxGemvProbs) {
-        const qk_status st = map_cuda(qk::launch_gemv_batch(group.data(), (int)group.size(), s));
+    const qk::GemvDesc g{t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].N, d[i].K};
+    if (use_gemv(g, d[i].M)) {
+      group.push_back(g);
+      if (group.size() > 1 && !qk::gemv_plan_fits(group.data(), (int)group.size())) {
+        group.pop_back();
+        const qk_status st = flush();
         if (st != QK_OK) return st;
-        group.clear();
+        group.push_back(g);
+      }
+      if ((int)group.size() == qk::kMaxGemvProbs) {
+        const qk_status st = flush();
+        if (st != QK_OK) return st;
       }
     } else {
       const qk_status st = run(t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].M, d[i].N, d[i].K, gu, s);
       if (st != QK_OK) return st;
     }
   }
-  if (!group.empty()) return map_cuda(qk::launch_gemv_batch(group.data(), (int)group.size(), s));
-  return QK_OK;
+  return flush();
 }
 
 }  // namespace
@@ -267,6 +276,16 @@ qk_status qk_get_device_status(qk_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QK_ERR_CUDA;
   const uint32_t v = qk::dequant_take_status() | qk::gemv_take_status() | qk::gemm_take_status();
   return v ? QK_ERR_TIMEOUT : QK_OK;
+}
+
+int qk_decode_uses_gemv(int qtype, int gateup, int64_t K) {
+  if ((qtype != QK_Q4_K && qtype != QK_Q6_K) || (gateup && qtype != QK_Q4_K)) return -1;
+  if (K <= 0 || K % qk::kQK != 0 || K >= kMaxDim) return -1;
+  // The weight and activation pointers are not dereferenced by the plan; the
+  // up pointer only marks the problem as gate/up.
+  const void* up = gateup ? reinterpret_cast<const void*>(uintptr_t(16)) : nullptr;
+  const qk::GemvDesc d{qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K, nullptr, up, nullptr, nullptr, 1, K};
+  return qk::gemv_plan_fits(&d, 1) ? 1 : 0;
 }
 
 const char* qk_status_string(qk_status status) {

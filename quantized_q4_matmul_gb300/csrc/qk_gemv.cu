@@ -571,19 +571,25 @@ uint32_t gemv_take_status() {
   return v;
 }
 
-// Launch one grouped GEMV.  Each problem gets its own stage geometry (its
-// CTAs carve their own ring); CTAs (one per SM) split across problems in
-// proportion to their weight bytes.
-cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
-  if (count <= 0 || count > kMaxGemvProbs) return cudaErrorInvalidValue;
-  constexpr size_t kSmem = 227 * 1024;
-  GemvBatch B;
+namespace {
+
+constexpr size_t kGemvSmem = 227 * 1024;
+
+// The stage geometry of one grouped GEMV launch (host only, no CUDA call):
+// each problem gets its own stages (its CTAs carve their own ring), and the
+// CTAs (one per SM, `sms` of them) split across problems in proportion to
+// their weight bytes.  False if some problem has no plan that fits shared
+// memory (x of the largest K plus at least two stages).
+bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* smem_out) {
+  if (count <= 0 || count > kMaxGemvProbs) return false;
+  GemvBatch& B = *out;
   memset(&B, 0, sizeof(B));
   B.count = count;
-  int kmax = 0;
-  for (int i = 0; i < count; ++i) kmax = std::max<int>(kmax, (int)d[i].K);
+  int64_t kmax = 0;
+  for (int i = 0; i < count; ++i) kmax = std::max<int64_t>(kmax, d[i].K);
   const size_t x_bytes = ((size_t)(2 * kmax + kmax / 4) + 127) / 128 * 128;
-  const size_t avail = kSmem - x_bytes - kSharedBytes - 128;  // for one CTA's ring
+  if (x_bytes + kSharedBytes + 128 >= kGemvSmem) return false;
+  const size_t avail = kGemvSmem - x_bytes - kSharedBytes - 128;  // for one CTA's ring
   double total = 0;
   int64_t bytes[kMaxGemvProbs];
   size_t ring = 0;
@@ -619,14 +625,14 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     P.pair = (P.kind == 0 && cb == nb && P.N > 16 && 2 * (size_t)round128((size_t)32 * nb * bb) <= avail) ? 1 : 0;
     P.stage_bytes = round128((size_t)16 * (nten + P.pair) * cb * bb);
     P.stages = (int)std::min<size_t>(kMaxStages, avail / P.stage_bytes);
-    if (P.stages < 2) return cudaErrorInvalidConfiguration;
+    if (P.stages < 2) return false;
     ring = std::max(ring, (size_t)P.stages * P.stage_bytes);
     P.tiles = (P.N + 16 * (1 + P.pair) - 1) / (16 * (1 + P.pair));
     bytes[i] = (int64_t)P.N * RB * nten;
     total += (double)bytes[i];
   }
-  const size_t smem = x_bytes + kSharedBytes + ring + 128;
-  const int budget = std::max(count, device_sms());
+  *smem_out = x_bytes + kSharedBytes + ring + 128;
+  const int budget = std::max(count, sms);
   int used = 0;
   for (int i = 0; i < count; ++i) {
     int c = (int)((double)budget * (double)bytes[i] / total);
@@ -656,14 +662,33 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
     B.p[i].cta_begin = begin;
     begin += B.p[i].ctas;
   }
+  return *smem_out <= kGemvSmem;
+}
+
+}  // namespace
+
+bool gemv_plan_fits(const GemvDesc* d, int count) {
+  GemvBatch B;
+  size_t smem = 0;
+  return plan_gemv(d, count, 152, &B, &smem);  // the SM count splits CTAs; it does not decide the fit
+}
+
+// Launch one grouped GEMV (see plan_gemv).
+cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
+  GemvBatch B;
+  size_t smem = 0;
+  if (!plan_gemv(d, count, device_sms(), &B, &smem)) return cudaErrorInvalidConfiguration;
   static PerDeviceFlag attr;  // the shared-memory limit is a per-device function attribute
   const int dev = current_device();
   if (!attr.done(dev)) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
+    cudaError_t e =
+        cudaFuncSetAttribute(gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
     if (e != cudaSuccess) return e;
     attr.mark(dev);
   }
-  gemv_stream_kernel<<<begin, kThreads, smem, s>>>(B);
+  int ctas = 0;
+  for (int i = 0; i < B.count; ++i) ctas += B.p[i].ctas;
+  gemv_stream_kernel<<<ctas, kThreads, smem, s>>>(B);
   return cudaGetLastError();
 }
 

@@ -74,4 +74,9 @@ struct GemvDesc {
 };
 cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s);
 
+// Whether one grouped GEMV launch can run these problems: x of the largest K
+// and at least two weight stages of every problem must fit in shared memory.
+// Host only (no CUDA call).  Problems that do not fit run on the GEMM.
+bool gemv_plan_fits(const GemvDesc* d, int count);
+
 }  // namespace qk

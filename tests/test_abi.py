@@ -135,3 +135,27 @@ def test_binding_checks_tensor_buffers_before_the_call(qk_lib):
         with pytest.raises(qk_lib.QKError) as e:
             call()
         assert e.value.status in (-4, -6, -8)  # CUDA error, unsupported device, inaccessible pointer
+
+
+def test_decode_kernel_choice_on_the_host(qk_lib):
+    """Which kernel an M = 1 problem runs on is decided on the host from the
+    GEMV's shared-memory plan (x of K plus two weight stages).  The model's
+    inner sizes stay on the GEMV; K values it cannot stage go to the GEMM."""
+    use = qk_lib.qk_decode_uses_gemv
+    for qt, gu in (("q4k", False), ("q6k", False), ("q4k", True)):
+        for K in range(256, 6144 + 1, 256):
+            assert use(qt, K, gu), (qt, gu, K)
+        assert use(qt, 8192, gu)
+        # x alone (fp16 copy plus 16-wide sums, 2.25 bytes per k) exceeds 227 KB
+        assert not use(qt, 131072, gu)
+    # Q6_K rows of an odd number of 8-block groups cannot be chunked 16-byte
+    # aligned, and whole 16-row tiles no longer fit three times
+    assert not use("q6k", 8448)
+    assert not use("q4k", 6400, True)   # gate/up: two tensors per stage
+    assert not use("q4k", 11520)
+    assert use("q6k", 16384) and use("q4k", 16384, True)  # 64 blocks: chunks of 8 fit
+    L = qk_lib.lib()
+    assert L.qk_decode_uses_gemv(2, 0, 3072) == -1      # unknown format
+    assert L.qk_decode_uses_gemv(1, 1, 3072) == -1      # gate/up is Q4_K only
+    assert L.qk_decode_uses_gemv(0, 0, 300) == -1       # K % 256
+    assert L.qk_decode_uses_gemv(0, 0, 0) == -1

@@ -440,3 +440,57 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable(qk_lib, cuda):
     qk_lib.qk_matmul_q4k(_dev(W, cuda), _x_dev(x, cuda), y, 3, 128, 512)
     qk_lib.qk_get_device_status()
     check_close(y.cpu().numpy().astype(np.float64), oracle.matmul(QT["q4k"], W, x, 128, 512), "after timeout")
+
+
+# ---------------------------------------------------------------------------
+# M = 1 problems whose K the GEMV cannot stage run on the tensor-core GEMM
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("qtype,N,K", [("q6k", 200, 8448), ("q4k", 130, 11520)])
+def test_decode_fallback_to_gemm(qk_lib, cuda, qtype, N, K):
+    assert not qk_lib.qk_decode_uses_gemv(qtype, K)
+    rng = synth.rng_for(41, K)
+    W = synth.weights(rng, qtype, N, K)
+    x = synth.activations(rng, 1, K)
+    ref = oracle.matmul(QT[qtype], W, x, N, K)
+    check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "%s M1 K%d on the GEMM" % (qtype, K))
+
+
+def test_decode_gateup_fallback_to_gemm(qk_lib, cuda):
+    import torch
+    N, K = 192, 6400
+    assert not qk_lib.qk_decode_uses_gemv("q4k", K, gateup=True)
+    rng = synth.rng_for(42, K)
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, 1, K)
+    y = torch.empty(1, N, dtype=torch.float16, device=cuda)
+    qk_lib.qk_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), y, 1, N, K)
+    qk_lib.qk_get_device_status()
+    check_close_f16out(y.float().cpu().numpy().astype(np.float64), oracle.gateup_swiglu(Wg, Wu, x, N, K),
+                       "gate/up M1 K%d on the GEMM" % K)
+
+
+def test_batch_launches_groups_whose_plans_fit(qk_lib, cuda):
+    """A gate/up at K = 6144 and a Q6_K at K = 65536 each fit a GEMV launch but
+    not one together (x of the larger K leaves too little room for the gate/up
+    stages); a Q6_K at K = 8448 fits none and runs on the GEMM."""
+    import torch
+    assert qk_lib.qk_decode_uses_gemv("q4k", 6144, gateup=True) and qk_lib.qk_decode_uses_gemv("q6k", 65536)
+    rng = synth.rng_for(43, 0)
+    probs, checks = [], []
+    Wg, Wu = synth.q4k_weights(rng, 128, 6144), synth.q4k_weights(rng, 128, 6144)
+    xg = synth.activations(rng, 1, 6144)
+    yg = torch.empty(1, 128, dtype=torch.float16, device=cuda)
+    probs.append(dict(qtype="q4k", blocks=_dev(Wg, cuda), up_blocks=_dev(Wu, cuda), x_f16=_x_dev(xg, cuda), y=yg,
+                      M=1, N=128, K=6144))
+    for qt, N, K in (("q6k", 64, 65536), ("q6k", 64, 8448), ("q4k", 256, 3072)):
+        W = synth.weights(rng, qt, N, K)
+        x = synth.activations(rng, 1, K)
+        y = torch.empty(1, N, dtype=torch.float32, device=cuda)
+        probs.append(dict(qtype=qt, blocks=_dev(W, cuda), x_f16=_x_dev(x, cuda), y=y, M=1, N=N, K=K))
+        checks.append((y, oracle.matmul(QT[qt], W, x, N, K), "%s K%d" % (qt, K)))
+    qk_lib.qk_matmul_batch(probs)
+    qk_lib.qk_get_device_status()
+    check_close_f16out(yg.float().cpu().numpy().astype(np.float64), oracle.gateup_swiglu(Wg, Wu, xg, 128, 6144),
+                       "gate/up K6144")
+    for y, ref, what in checks:
+        check_close(y.cpu().numpy().astype(np.float64), ref, what)
