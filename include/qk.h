@@ -28,7 +28,8 @@
  *   - All pointers are DEVICE pointers of the current CUDA device (or mapped
  *     host memory the device can read), 16-byte aligned.  The caller owns every
  *     buffer; the library allocates no device memory on any call.
- *   - K must be a positive multiple of 256.  M = 0 or N = 0 is a no-op.
+ *   - K must be a positive multiple of 256 and N, K below 2^31; M is at most
+ *     8,388,480 (65535 token tiles of 128).  M = 0 or N = 0 is a no-op.
  *   - y must not overlap x or the weights.
  *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
  *     stream).  The return value reports argument and launch errors only; a
@@ -51,7 +52,7 @@ typedef int qk_status;
 #define QK_OK 0
 #define QK_ERR_NULL (-1)               /* a required pointer is NULL */
 #define QK_ERR_ALIGN (-2)              /* a pointer is not 16-byte aligned */
-#define QK_ERR_SHAPE (-3)              /* K % 256 != 0, a negative size, or sizes that overflow */
+#define QK_ERR_SHAPE (-3)              /* K % 256 != 0, a negative size, or a size beyond the limits */
 #define QK_ERR_CUDA (-4)               /* a CUDA runtime call or kernel launch failed */
 #define QK_ERR_TIMEOUT (-5)            /* a kernel gave up on a bounded wait (see qk_get_device_status) */
 #define QK_ERR_UNSUPPORTED_DEVICE (-6) /* the current device is not an sm_103 GPU */

@@ -19,6 +19,9 @@ namespace {
 using qk::QType;
 
 constexpr int64_t kMaxDim = (int64_t)1 << 31;  // M, N, K each below 2^31
+// The GEMM puts token tiles (at least 128 tokens each for M > 256) on the
+// grid's y dimension, which holds at most 65535 blocks.
+constexpr int64_t kMaxM = (int64_t)65535 * 128;
 
 // sm_103 check, cached per device.
 qk_status check_device() {
@@ -97,7 +100,7 @@ qk_status validate_host(QType t, const void* W, const void* W_up, const uint16_t
                         int64_t N, int64_t K, bool gateup, Checked* c) {
   if (M < 0 || N < 0 || K < 0) return QK_ERR_SHAPE;
   if (K == 0 || K % qk::kQK != 0) return QK_ERR_SHAPE;
-  if (M >= kMaxDim || N >= kMaxDim || K >= kMaxDim) return QK_ERR_SHAPE;
+  if (M > kMaxM || N >= kMaxDim || K >= kMaxDim) return QK_ERR_SHAPE;
   if (gateup && t != qk::kQ4K) return QK_ERR_SHAPE;
   if (M == 0 || N == 0) {
     c->w_bytes = c->x_bytes = c->y_bytes = 0;

@@ -50,6 +50,11 @@ def test_matmul_rejects_bad_arguments_on_the_host(qk_lib, fn):
     assert f(A16, A16, A16, -1, 8, 256, None) == -3       # negative M
     assert f(A16, A16, A16, 4, -8, 256, None) == -3       # negative N
     assert f(A16, A16, A16, 1 << 31, 8, 256, None) == -3  # too large
+    assert f(A16, A16, A16, 65535 * 128 + 1, 8, 256, None) == -3  # more token tiles than the grid holds
+    assert f(A16, A16, A16, 4, 1 << 31, 256, None) == -3
+    assert f(A16, A16, A16, 4, 8, 1 << 31, None) == -3
+    # the largest M passes the host checks (then the fake pointers are refused)
+    assert f(A16, A16, A16, 65535 * 128, 8, 256, None) in (-4, -6, -8)
     assert f(None, A16, A16, 4, 8, 256, None) == -1       # NULL weights
     assert f(A16, None, A16, 4, 8, 256, None) == -1
     assert f(A16, A16, None, 4, 8, 256, None) == -1
