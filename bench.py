@@ -298,6 +298,59 @@ def chain_bytes():
     return tot
 
 
+def dequant_bytes():
+    """Bytes the dequant export moves for one layer's seven weight tensors:
+    the packed blocks in, 4 bytes per weight out."""
+    return sum(synth.weight_bytes(l.qtype, l.N, l.K) + 4 * l.N * l.K for l in decode_linears())
+
+
+def measure_dequant(torch, qk, wl, stream, dev, reps):
+    """The dequant export (bit-exact fp32 weights) of one layer's seven weight
+    tensors, captured as one CUDA graph per rotating copy and timed with CUDA
+    events around each replay (weights ~64 MB in, ~403 MB out: beyond L2)."""
+    s = stream.cuda_stream
+    lins = decode_linears()
+    outs = [torch.empty(l.N * l.K, dtype=torch.float32, device=dev) for l in lins]
+    fns = {"q4k": qk.qk_dequant_q4k, "q6k": qk.qk_dequant_q6k}
+
+    def one(c):
+        for (lin, Wd, _), out in zip(wl.copies[c]["decode"], outs):
+            fns[lin.qtype](Wd, lin.N * lin.K // 256, out, s)
+        return len(lins)
+
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            one(i % N_COPIES)
+    qk.qk_get_device_status(s)
+    torch.cuda.synchronize()
+    graphs = []
+    for c in range(N_COPIES):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            one(c)
+        graphs.append(g)
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(3 + reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graphs[i % N_COPIES].replay()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                ms.append(e0.elapsed_time(e1))
+    qk.qk_get_device_status(s)
+    med = statistics.median(ms)
+    nbytes = dequant_bytes()
+    pk = peaks()
+    gbs = nbytes / (med * 1e-3) / 1e9
+    del graphs, outs
+    return {"metric": "dequant export HBM GB/s", "value": gbs, "unit": "GB/s", "frac_of_hbm": gbs / pk["hbm_gbs"],
+            "ms_per_layer": med, "bytes_per_layer": nbytes, "launches_per_layer": len(lins),
+            "note": "qk_dequant_q4k/q6k over one layer's 7 weight tensors (packed in, fp32 out), "
+                    "one CUDA graph per rotating copy, %d replays" % reps}
+
+
 def run_gpu(args, rank, world, dist):
     import torch
     import quantized_q4_matmul_gb300 as qk
@@ -451,7 +504,7 @@ def run_gpu(args, rank, world, dist):
     gu_ms_med = local_res["gu_ms"]
     gu_ach = gu_flops / (gu_ms_med * 1e-3) / 1e12
     traffic = measured_traffic("gateup_swiglu_m1024")
-    return {
+    res = {
         "metric": METRIC,
         "value": tflops,
         "unit": "TFLOP/s",
@@ -482,6 +535,13 @@ def run_gpu(args, rank, world, dist):
         "gpu_launches": sum(r["launches"] for r in allr),
         "clocks": local_res["clocks"],
     }
+    # The dequant export (not part of the step) last, on rank 0, after every
+    # number above is final: whatever happens here only affects this field.
+    try:
+        res["dequant"] = measure_dequant(torch, qk, wl, stream, dev, max(5, args.steps))
+    except Exception as e:  # noqa: BLE001 -- reported in the line, not fatal
+        res["dequant"] = {"error": ("%s: %s" % (type(e).__name__, e))[:300]}
+    return res
 
 
 def run_reference(args, rank):

@@ -136,9 +136,7 @@ uint32_t dequant_take_status() {
 }
 
 cudaError_t launch_dequant(QType t, const void* blocks, int64_t n_blocks, float* out, cudaStream_t s) {
-  int dev = 0, sms = 148;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int sms = device_sms();
   const int64_t ctas_needed = (n_blocks + kWarpsPerCta - 1) / kWarpsPerCta;
   const int64_t cap = (int64_t)sms * 16;
   const int grid = (int)(ctas_needed < cap ? ctas_needed : cap);

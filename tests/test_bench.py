@@ -18,14 +18,18 @@ ENV = dict(os.environ, QK_REF_STEP_S="0.3", OMP_NUM_THREADS=os.environ.get("OMP_
 
 
 def test_step_work_units():
-    """Prefill flops of the step (gate/up, down, attn_v at M=1024) and the decode
-    layer's algorithmic bytes (packed weights of one layer's 7 linears, x, y)."""
+    """Prefill flops of the step (gate/up, down, attn_v at M=1024), the decode
+    layer's algorithmic bytes (packed weights of one layer's 7 linears, x, y)
+    and the dequant export's (packed weights in, fp32 weights out)."""
     assert bench.prefill_flops() == 2.0 * 1024 * (2 * 8192 * 3072 + 3072 * 8192 + 1024 * 3072)
     weights = sum(bench.synth.weight_bytes(l.qtype, l.N, l.K) for l in bench.decode_linears())
     assert weights == 63_922_176
     x = sum(2 * l.K for l in bench.decode_linears())
     y = sum(4 * l.N for l in bench.decode_linears())
     assert bench.decode_bytes() == weights + x + y == 64_086_016
+    # dequant export of the same seven tensors: packed in, fp32 out (100,663,296 weights)
+    assert sum(l.N * l.K for l in bench.decode_linears()) == 100_663_296
+    assert bench.dequant_bytes() == weights + 4 * 100_663_296 == 466_575_360
 
 
 def _json_lines(out):
