@@ -137,8 +137,10 @@ typedef struct qk_matmul_desc {
  * Run `count` independent problems (DAMASCUS project overview, "[04] one
  * decode step": the QKV projections share x, gate and up share x, and every
  * decode-step linear is an M = 1 GEMV).  Problems with M = 1 are executed
- * together, up to 8 per kernel launch, so small GEMVs share one launch and
- * stream their weights concurrently; other problems run as in
+ * together, up to 8 per kernel launch and as long as their joint
+ * shared-memory plan fits (x is staged for the largest K of a launch), so
+ * small GEMVs share one launch and stream their weights concurrently; other
+ * problems, and M = 1 problems the GEMV cannot stage at all, run as in
  * qk_matmul_q4k / qk_matmul_q6k / qk_gateup_swiglu_q4k.  Each entry obeys the
  * rules of its single-problem entry point; in addition no y may overlap any
  * input or output of another entry.  count = 0 is a no-op.  Results are
