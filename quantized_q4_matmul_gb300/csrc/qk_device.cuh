@@ -77,12 +77,17 @@ __device__ __forceinline__ uint64_t global_ns() {
 // abort flag and the device status word) once QK_WAIT_LIMIT_NS has passed,
 // or early if another thread of the CTA already aborted (unless
 // `ignore_abort`, used when draining copies that are still in flight).
+// kSleepNs > 0 sleeps that long between polls after the first miss, for
+// waits whose latency is hidden anyway, so that the polling warp leaves
+// issue slots to the warps sharing its scheduler.
+template <uint32_t kSleepNs = 0>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile uint32_t* abort_flag,
                                           uint32_t* dev_status, bool ignore_abort = false,
                                           uint64_t limit_ns = QK_WAIT_LIMIT_NS) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   for (uint32_t i = 1;; ++i) {
+    if constexpr (kSleepNs > 0) __nanosleep(kSleepNs);
     if (mbar_try_wait(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (!ignore_abort && *abort_flag) return false;

@@ -270,6 +270,13 @@ __device__ __forceinline__ void q6_half(const Q6Half& q, uint32_t xa, uint32_t s
 #define QK_GEMV_WARPS 12
 #endif
 constexpr int kComputeWarps = QK_GEMV_WARPS;
+// Sleep between polls of the producer's and the reducer's waits, in ns (0:
+// poll back to back).  Those two warps share schedulers with compute warps;
+// their waits are hidden by the ring and by the double-buffered partials.
+#ifndef QK_GEMV_BACKOFF_NS
+#define QK_GEMV_BACKOFF_NS 0
+#endif
+constexpr uint32_t kBackoffNs = QK_GEMV_BACKOFF_NS;
 constexpr int kProducerWarp = kComputeWarps;      // streams the weights (and x)
 constexpr int kReducerWarp = kComputeWarps + 1;       // sums the compute warps' partials per tile
 constexpr int kThreads = 32 * (kComputeWarps + 2);
@@ -332,7 +339,8 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
       int st = 0;
       for (; st < steps; ++st) {
         const int s = st % S;
-        if (!mbar_wait(&sh->empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemv_status)) break;
+        if (!mbar_wait<kBackoffNs>(&sh->empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemv_status))
+          break;
         // The compute warps read the stage with plain loads; the refill is an
         // async-proxy write.  The proxy fence after the barrier their releases
         // completed orders those reads before the copy.
@@ -391,7 +399,7 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
     const int ntiles = t1 - t0;
     for (int i = 0; i < ntiles; ++i) {
       const int par = i & 1;
-      if (!mbar_wait(&sh->red_full[par], (uint32_t)(i >> 1) & 1u, abort_flag, &g_gemv_status)) break;
+      if (!mbar_wait<kBackoffNs>(&sh->red_full[par], (uint32_t)(i >> 1) & 1u, abort_flag, &g_gemv_status)) break;
       if (P.kind == 1) {
         if (lane < 16) {
           const int n = (t0 + i) * 16 + lane;
