@@ -31,6 +31,11 @@ A second model checks Q4_K with an x ring and an A ring of different depths.
 The two rings share one done ring of max(SX, SA) barriers, indexed by K step.
 It covers gate/up, where both issuers take every step and a phase needs both
 commits, and single-tensor problems, where the issuers alternate.
+
+A third model checks the decode GEMV's hand-off of per-tile partial sums. The
+compute warps and the reducer warp use double-buffered red_full / red_free
+barriers. A control drops one wait and shows that the model then catches the
+overwrite.
 """
 import random
 
@@ -192,3 +197,85 @@ def test_q4k_x_and_a_rings_never_pass_early(sx, sa, gateup):
     """Separate x and A ring depths over one done ring of max(SX, SA): no wait
     passes early and nothing deadlocks (gate/up runs 3 x + 2 A stages)."""
     assert not any(simulate_xa(sx, sa, gateup, seed=s) for s in range(800))
+
+
+class Bar:
+    """An mbarrier: `count` arrivals complete a phase; a parity wait for phase k
+    passes while the number of completed phases has the other parity than k."""
+
+    def __init__(self, count):
+        self.count, self.pending, self.done = count, 0, 0
+
+    def arrive(self):
+        self.pending += 1
+        if self.pending == self.count:
+            self.pending = 0
+            self.done += 1
+
+    def passes(self, k):
+        return (self.done & 1) != (k & 1)
+
+    def early(self, k):
+        return self.done <= k  # passed although phase k has not completed
+
+
+def simulate_gemv_reduction(warps, tiles, seed, free_wait=True):
+    """The decode GEMV's per-tile hand-off: each compute warp finishes tile ti,
+    waits (from ti = 2 on) for red_free[ti & 1] phase (ti >> 1) - 1, writes its
+    partials into red[ti & 1] and arrives on red_full[ti & 1] (count = warps);
+    the reducer waits for red_full[i & 1] phase i >> 1, reads all partials and
+    arrives on red_free[i & 1] (count 1).  Returns (fooled, overwritten): a
+    wait that passed early, or a partial overwritten before the reducer read it.
+    free_wait=False drops the compute warps' red_free wait (a control)."""
+    rng = random.Random(seed)
+    full, free = [Bar(warps), Bar(warps)], [Bar(1), Bar(1)]
+    slot = [[None] * warps for _ in range(2)]  # tile whose partial sits in red[par][w]
+    nxt = [0] * warps   # next tile of each compute warp
+    red_i = 0           # next tile of the reducer
+    fooled = overwritten = False
+    while True:
+        acts = []
+        for w in range(warps):
+            ti = nxt[w]
+            if ti < tiles and (ti < 2 or not free_wait or free[ti & 1].passes((ti >> 1) - 1)):
+                acts.append(w)
+        if red_i < tiles and full[red_i & 1].passes(red_i >> 1):
+            acts.append("r")
+        if not acts:
+            break
+        a = rng.choice(acts)
+        if a == "r":
+            i, par = red_i, red_i & 1
+            fooled |= full[par].early(i >> 1)
+            if any(t != i for t in slot[par]):
+                overwritten = True  # a partial of another tile (missing or already replaced)
+            free[par].arrive()
+            red_i += 1
+        else:
+            w, ti = a, nxt[a]
+            par = ti & 1
+            if ti >= 2 and free_wait:
+                fooled |= free[par].early((ti >> 1) - 1)
+            if slot[par][w] is not None and slot[par][w] != ti - 2:
+                overwritten = True
+            if ti >= 2 and red_i <= ti - 2:
+                overwritten = True  # tile ti - 2 not yet reduced
+            slot[par][w] = ti
+            full[par].arrive()
+            nxt[w] += 1
+    assert red_i == tiles and all(n == tiles for n in nxt), "deadlock"
+    return fooled, overwritten
+
+
+@pytest.mark.parametrize("warps,tiles", [(1, 5), (3, 7), (12, 9)])
+def test_gemv_partials_handoff(warps, tiles):
+    """The double-buffered partials of the decode GEMV: no wait passes early, no
+    partial is overwritten before the reducer has read it, nothing deadlocks."""
+    for seed in range(600):
+        assert simulate_gemv_reduction(warps, tiles, seed) == (False, False)
+
+
+def test_gemv_partials_without_the_free_wait_can_race():
+    """Control: without the red_free wait a fast warp can overwrite a partial the
+    reducer has not read yet, and the model sees it (so it can fail)."""
+    assert any(simulate_gemv_reduction(3, 7, seed, free_wait=False)[1] for seed in range(600))
