@@ -33,6 +33,7 @@ from tests import synth  # noqa: E402
 METRIC = "prefill GEMM TFLOP/s (% FP16 tensor peak) at M=1024; decode GEMV HBM GB/s"
 PREFILL_M = 1024
 N_COPIES = 3  # rotating input copies: ~3 x 230 MB per cycle, well above L2
+CLOCK_SOAK_S = 0.5  # untimed replay of the step after the timed region, for the clock samples
 
 
 def peaks():
@@ -163,7 +164,9 @@ class Clocks:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm),
+                "window": "every 100 ms over the timed steps and %.1f s of untimed replays of the same step "
+                          "graphs right after them" % CLOCK_SOAK_S}
 
 
 # ----------------------------------------------------------------------------
@@ -417,6 +420,18 @@ def run_gpu(args, rank, world, dist):
                 launches += n_pre + n_dec
             t_end.record(stream)
         t_end.synchronize()
+        # nvidia-smi samples every 100 ms, far longer than the timed steps: the
+        # same step graphs keep replaying (untimed, after t_end) for ~0.5 s so
+        # that the samples see the GPU under this load.
+        soak_end = time.perf_counter() + CLOCK_SOAK_S
+        with torch.cuda.stream(stream):
+            i = 0
+            while time.perf_counter() < soak_end:
+                for _ in range(16):
+                    g_pre[i % N_COPIES].replay()
+                    g_dec[i % N_COPIES].replay()
+                    i += 1
+                stream.synchronize()
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()

@@ -76,3 +76,22 @@ def test_reference_arm_two_ranks_gloo():
     lines = _json_lines(r.stdout)
     assert len(lines) == 1
     _check_reference_line(lines[0])
+
+
+def test_clock_summary_parsing(tmp_path, monkeypatch):
+    """The clocks object of the bench line: median SM clock, max clock and the
+    throttle reasons seen active, from nvidia-smi's CSV samples."""
+    monkeypatch.setenv("QK_CLOCKS_DIR", str(tmp_path))
+    c = bench.Clocks(0)
+    c.proc = object()  # as if the sampler had run
+    with open(c.path, "w") as f:
+        f.write("0, 2070, 2070, 900.5, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                "0, 1980, 2070, 1390.0, 0x4, Not Active, Not Active, Not Active, Active\n"
+                "0, 2070, 2070, 1200.0, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+                "garbage line\n")
+    d = c.summary()
+    assert d["sm_mhz"] == 2070.0 and d["sm_max_mhz"] == 2070.0 and d["samples"] == 3
+    assert d["reasons"] == ["sw_power_cap"]
+    assert "untimed replays" in d["window"]
+    c.proc = None
+    assert c.summary()["reasons"] == ["nvidia-smi unavailable"]
