@@ -71,6 +71,14 @@ constexpr int kIssuers = 2;
 // counted 74 % of the Q6_K kernel's shared wavefronts as bank conflicts).
 constexpr int kQ6Win = 240;
 
+// Sleep between polls of the copy warps' waits (x tiles and packed blocks),
+// in ns; 0 polls back to back.  Those warps share schedulers with dequant
+// warps, and their waits are hidden by the rings.
+#ifndef QK_GEMM_BACKOFF_NS
+#define QK_GEMM_BACKOFF_NS 0
+#endif
+constexpr uint32_t kCopyBackoffNs = QK_GEMM_BACKOFF_NS;
+
 template <int QT, bool GATEUP>
 struct Cfg {
   // Dequant warps: two threads per weight row and tensor (each dequantizes
@@ -609,7 +617,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       if (lane == 0) {
         bool ok = true;
         for (; step < nsteps && ok; ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, D)) {
-          ok = mbar_wait(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
+          ok = mbar_wait<kCopyBackoffNs>(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
           if (!ok) break;
           const int kb = kb_begin + (step >> 2), c = step & 3;
           mbar_arrive_expect_tx(&bars->x_full[xpos.slot], x_bytes);
@@ -623,14 +631,14 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       for (int i = 0; i < nkb && ok; ++i, ring_advance(ppos, 1, P)) {
         const int kb = kb_begin + i;
         const int ps = ppos.slot;
-        ok = mbar_wait(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status);
+        ok = mbar_wait<kCopyBackoffNs>(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status);
         if (!ok) break;
         fence_proxy_async_smem();  // as in the split producer: plain reads before the refill
         issue_packed<QT, GATEUP>(smem + L.p_off + ps * C::kNumB * kPSlotBytes, &bars->p_full[ps], &tm_w0, &tm_w1, p, kb,
                                  n0, nb, lane, 32);
         for (int c = 0; c < 4 && ok; ++c, ++step, ring_advance(xpos, 1, SX), ring_advance(dpos, 1, D)) {
           const int s = xpos.slot;
-          ok = mbar_wait(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
+          ok = mbar_wait<kCopyBackoffNs>(&bars->done[dpos.slot], dpos.phase, abort_flag, &g_gemm_status);
           if (!ok) break;
           if (lane == 0) {
             mbar_arrive_expect_tx(&bars->x_full[s], x_bytes);
@@ -702,7 +710,7 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
       RingPos ppos = {0, 0u};
       for (int i = 0; i < nkb; ++i, ring_advance(ppos, 1, P)) {
         const int ps = ppos.slot;
-        if (!mbar_wait(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status)) break;
+        if (!mbar_wait<kCopyBackoffNs>(&bars->p_empty[ps], ppos.phase ^ 1u, abort_flag, &g_gemm_status)) break;
         // The dequant threads read the slot with plain loads; the refill is
         // an async-proxy write.  This proxy fence, after the barrier that
         // their releases completed, orders those reads before the copy
