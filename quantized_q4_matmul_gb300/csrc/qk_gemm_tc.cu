@@ -26,9 +26,12 @@
 //               pace.
 // Pipelines: packed blocks (P stages, one super-block each), x tiles (SX
 // stages) and A tiles (SA stages), the last two released per K step by the
-// step's UMMA commit (done barriers, a ring of max(SX, SA)).  All waits are
-// bounded mbarrier waits; a timeout raises a device status flag and the CTA
-// drains and exits.
+// step's UMMA commit (done barriers, a ring of max(SX, SA)).  Grids that
+// would leave half of the SMs idle split K across a thread-block cluster of
+// 2..8 CTAs per tile: each peer sends its fp32 partial tile to CTA 0 with one
+// bulk shared::cluster copy, and CTA 0 adds them in a fixed order (no global
+// scratch, deterministic).  All waits are bounded mbarrier waits; a timeout
+// raises a device status flag and the CTA drains and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
