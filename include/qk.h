@@ -87,8 +87,8 @@ qk_status qk_dequant_q6k(const void *blocks, int64_t n_blocks, float *out, qk_st
  * GEMM (weights dequantized to fp16 in
  * shared or tensor memory, never written to device memory; fp32 accumulation
  * in tensor memory),
- * as the overview's "fused dequant -> matrix unit never materializes FP16
- * weights" describes.  The two paths agree within rounding; results are not
+ * the overview's prefill plan in which dequantized weights feed the matrix
+ * unit directly and no fp16 copy of them is stored.  The two paths agree within rounding; results are not
  * bit-identical across M.  Single-tensor GEMMs keep the dequantized tiles in
  * tensor memory where they fit; QK_A_TMEM=0 in the environment (read once per
  * process) selects shared memory instead, with the same results within
@@ -176,6 +176,29 @@ qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream);
  * together only while their joint plan fits.
  */
 int qk_decode_uses_gemv(int qtype, int gateup, int64_t K);
+
+/*
+ * Host-only query: the launch plan the tensor-core GEMM (M > 1, and M = 1
+ * problems the GEMV cannot stage) uses for an M x N problem of format
+ * `qtype` (gateup != 0: the fused gate/up + SwiGLU, Q4_K only).  Needs no GPU;
+ * with one present, the current device's shared-memory limits are used.
+ * tcgen05.alloc waits without a time limit until tensor-memory columns are
+ * free, so the plan pads a CTA's shared memory until the CTAs that can share
+ * an SM fit in its 512 columns together: max_ctas_per_sm * tmem_cols <= 512.
+ * Returns QK_ERR_SHAPE for invalid arguments (as qk_matmul_q4k), else QK_OK.
+ */
+typedef struct qk_gemm_plan_info {
+  int token_tile;      /* tokens per CTA tile (the UMMA N dimension), a multiple of 16 */
+  int x_stages;        /* activation-tile ring depth */
+  int a_stages;        /* dequantized weight-tile ring depth */
+  int packed_stages;   /* packed super-block ring depth */
+  int a_in_tmem;       /* 1: dequantized weight tiles live in tensor memory, 0: in shared memory */
+  int tmem_cols;       /* tensor-memory columns one CTA allocates */
+  int smem_bytes;      /* dynamic shared memory per CTA */
+  int max_ctas_per_sm; /* CTAs that fit on one SM by shared memory */
+} qk_gemm_plan_info;
+
+qk_status qk_gemm_plan(int qtype, int gateup, int64_t M, int64_t N, int64_t K, qk_gemm_plan_info *out);
 
 /* A static, human-readable name for a status code. */
 const char *qk_status_string(qk_status status);

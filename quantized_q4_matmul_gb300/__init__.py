@@ -18,7 +18,8 @@ import os
 __all__ = [
     "QKError", "lib", "lib_path", "qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k",
     "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout",
-    "qk_decode_uses_gemv", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
+    "qk_decode_uses_gemv", "qk_gemm_plan", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
+    "qk_gemm_plan_info",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +27,7 @@ QK_BLOCK_BYTES = {"q4k": 144, "q6k": 210}
 
 SYMBOLS = ("qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k", "qk_gateup_swiglu_q4k",
            "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout", "qk_decode_uses_gemv",
-           "qk_status_string", "qk_version")
+           "qk_gemm_plan", "qk_status_string", "qk_version")
 
 QK_Q4_K, QK_Q6_K = 0, 1
 
@@ -36,6 +37,12 @@ class qk_matmul_desc(ctypes.Structure):
     _fields_ = [("qtype", ctypes.c_int), ("blocks", ctypes.c_void_p), ("up_blocks", ctypes.c_void_p),
                 ("x_f16", ctypes.c_void_p), ("y", ctypes.c_void_p), ("M", ctypes.c_int64),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class qk_gemm_plan_info(ctypes.Structure):
+    """Mirror of ``qk_gemm_plan_info`` in include/qk.h."""
+    _fields_ = [(n, ctypes.c_int) for n in ("token_tile", "x_stages", "a_stages", "packed_stages", "a_in_tmem",
+                                             "tmem_cols", "smem_bytes", "max_ctas_per_sm")]
 
 
 class QKError(RuntimeError):
@@ -74,6 +81,8 @@ def lib():
         L.qk_get_device_status.restype, L.qk_get_device_status.argtypes = i32, [vp]
         L.qk_debug_wait_timeout.restype, L.qk_debug_wait_timeout.argtypes = i32, [i64, vp]
         L.qk_decode_uses_gemv.restype, L.qk_decode_uses_gemv.argtypes = i32, [i32, i32, i64]
+        L.qk_gemm_plan.restype = i32
+        L.qk_gemm_plan.argtypes = [i32, i32, i64, i64, i64, ctypes.POINTER(qk_gemm_plan_info)]
         L.qk_status_string.restype, L.qk_status_string.argtypes = ctypes.c_char_p, [i32]
         L.qk_version.restype, L.qk_version.argtypes = i32, []
         _lib = L
@@ -204,6 +213,15 @@ def qk_decode_uses_gemv(qtype, K: int, gateup: bool = False) -> bool:
     if r < 0:
         raise ValueError("qk_decode_uses_gemv: invalid qtype %r or K %d" % (qtype, K))
     return bool(r)
+
+
+def qk_gemm_plan(qtype, M: int, N: int, K: int, gateup: bool = False) -> dict:
+    """The tensor-core GEMM's launch plan for an M x N x K problem (host only)."""
+    qt = {"q4k": QK_Q4_K, "q6k": QK_Q6_K}.get(qtype, qtype)
+    info = qk_gemm_plan_info()
+    _check(lib().qk_gemm_plan(int(qt), int(bool(gateup)), int(M), int(N), int(K), ctypes.byref(info)),
+           "qk_gemm_plan")
+    return {n: getattr(info, n) for n, _ in qk_gemm_plan_info._fields_}
 
 
 def qk_get_device_status(stream=None) -> None:

@@ -291,6 +291,24 @@ int qk_decode_uses_gemv(int qtype, int gateup, int64_t K) {
   return qk::gemv_plan_fits(&d, 1) ? 1 : 0;
 }
 
+qk_status qk_gemm_plan(int qtype, int gateup, int64_t M, int64_t N, int64_t K, qk_gemm_plan_info* out) {
+  if (!out) return QK_ERR_NULL;
+  if ((qtype != QK_Q4_K && qtype != QK_Q6_K) || (gateup && qtype != QK_Q4_K)) return QK_ERR_SHAPE;
+  if (M <= 0 || N <= 0 || K <= 0 || K % qk::kQK != 0 || M > kMaxM || N >= kMaxDim || K >= kMaxDim)
+    return QK_ERR_SHAPE;
+  qk::GemmPlanInfo g;
+  if (!qk::gemm_plan(qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K, gateup != 0, M, N, &g)) return QK_ERR_SHAPE;
+  out->token_tile = g.token_tile;
+  out->x_stages = g.x_stages;
+  out->a_stages = g.a_stages;
+  out->packed_stages = g.packed_stages;
+  out->a_in_tmem = g.a_in_tmem;
+  out->tmem_cols = g.tmem_cols;
+  out->smem_bytes = g.smem_bytes;
+  out->max_ctas_per_sm = g.max_ctas_per_sm;
+  return QK_OK;
+}
+
 const char* qk_status_string(qk_status status) {
   switch (status) {
     case QK_OK: return "QK_OK";

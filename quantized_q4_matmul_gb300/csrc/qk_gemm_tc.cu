@@ -2,9 +2,10 @@
 // y[m][n] = sum_k x[m][k] * w[n][k] with Q4_K / Q6_K weights dequantized on
 // the fly, plus the fused gate/up + SwiGLU variant.
 //
-// Source: DAMASCUS project overview, "[01] the thesis" (prefill is the whole
-// prompt at once, GEMM-heavy and compute-bound; fused dequant feeding the
-// matrix unit never materializes fp16 weights) and "[04] one decode step"
+// Source: DAMASCUS project overview, "[01] the thesis" (prefill takes every
+// prompt token in one pass as matrix-matrix products bound by arithmetic, and
+// the dequantized weights go straight to the matrix unit, so no fp16 copy of
+// them is ever stored) and "[04] one decode step"
 // (QKV, SwiGLU FFN, LM head over every prompt position); "Building DAMASCUS",
 // "Prefill and decode need different performance questions".
 //
@@ -37,6 +38,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <map>
@@ -993,55 +995,87 @@ int max_active_clusters(int c, uint32_t smem) {
   return n;
 }
 
+// Tensor-memory columns one CTA allocates: one BN-column accumulator per
+// issuer and, with A tiles in tensor memory, SA x kNumB tiles of 32 columns,
+// rounded up to the power of two tcgen05.alloc takes (the kernel computes the
+// same value).
+inline uint32_t tmem_cols_for(int BN, int SA, int num_b, bool at) {
+  const uint32_t need = (uint32_t)(kIssuers * BN) + (at ? (uint32_t)(SA * num_b * 32) : 0u);
+  return need <= 32 ? 32 : need <= 64 ? 64 : need <= 128 ? 128 : need <= 256 ? 256 : 512;
+}
+
+// tcgen05.alloc waits until enough tensor-memory columns are free, with no
+// time limit, so the CTAs that share an SM must fit in its 512 columns
+// together; otherwise one of them can wait forever (in a split-K cluster,
+// while its peers hold theirs at the cluster barrier).  Shared memory bounds
+// how many CTAs share an SM: `sm_smem` per SM, `reserved` per CTA.  This
+// returns the dynamic shared-memory request, at least `smem`, for which at
+// most 512 / cols CTAs fit (host only; registers can only lower the count).
+uint32_t smem_for_tmem(uint32_t smem, uint32_t cols, uint32_t sm_smem, uint32_t reserved) {
+  const uint32_t max_ctas = 512u / cols;
+  if (sm_smem / (smem + reserved) <= max_ctas) return smem;
+  uint32_t need = sm_smem / (max_ctas + 1) - reserved + 1;
+  need = (need + 127u) & ~127u;
+  return need > smem ? need : smem;
+}
+
+// Shared memory per SM and the per-CTA reservation (the GB300 values when no
+// device can be queried).
+void sm_smem_limits(uint32_t* sm_smem, uint32_t* reserved) {
+  static std::atomic<int64_t> cache[kMaxDevices];
+  *sm_smem = 233472;
+  *reserved = 1024;
+  const int dev = current_device();
+  if (dev < 0) return;
+  int64_t v = cache[dev].load(std::memory_order_relaxed);
+  if (v == 0) {
+    int a = 0, b = 0;
+    if (cudaDeviceGetAttribute(&a, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&b, cudaDevAttrReservedSharedMemoryPerBlock, dev) == cudaSuccess && a > 0) {
+      v = ((int64_t)a << 20) | (int64_t)b;
+    } else {
+      cudaGetLastError();
+      v = ((int64_t)233472 << 20) | 1024;
+    }
+    cache[dev].store(v, std::memory_order_relaxed);
+  }
+  *sm_smem = (uint32_t)(v >> 20);
+  *reserved = (uint32_t)(v & 0xFFFFF);
+}
+
+// The launch plan of one GEMM problem (host only, no kernel launch).
+struct TcPlan {
+  int BN, SX, SA, P;
+  uint32_t smem;       // dynamic shared memory requested per CTA
+  uint32_t tmem_cols;  // tensor-memory columns per CTA
+  uint32_t bar_off;    // offset of the barrier block (bounds the split-K partials)
+};
+
+// Pipeline depths (all measured on GB300).  The K-step rings come first: a
+// single-tensor kernel with fewer than 4 x-tile stages ran ~35 % slower.
+// Single-tensor problems grow A-tile and x-tile stages alternately, A first
+// and never fewer A than x stages; gate/up grows x stages first (its issuers
+// waited on x tiles while its dequant threads had slack: 3 x + 2 A stages
+// ran 12 % faster than 2 + 3).  Up to 5 A and 4 x stages (deeper rings were
+// no faster, and slower for Q6_K attn_v), while shared memory (and, with A
+// in tensor memory, TMEM) allows.  Two packed-block stages where the rings still reach 4 x
+// stages next to them (cold-cache Q6_K ran faster with two), else one (the
+// dequant threads copy a super-block to registers and release its slot at
+// once, so the refill overlaps the block's four K steps).
+// Q6_K takes 4 A stages.  Its threads write two consecutive K steps of a
+// super-block and the two halves of a row alternate.  With SA = 2 a half
+// waits on a slot whose previous phase (the other half's step) it never
+// saw, so the parity test can pass a phase early (seen on GB300 as wrong
+// output once the packed copies ran ahead).  From SA = 3 on, the phase a
+// half skips belongs to an earlier step of the same issuer, whose UMMAs
+// complete in order, so it has always completed.  Q6_K keeps SX <= SA (its
+// done ring is indexed by A slot), and its x ring wants 4 stages.
+// Returns false when the A tiles do not fit in tensor memory next to the
+// accumulators (the caller then keeps them in shared memory).
 template <int QT, bool GATEUP, bool AT>
-cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
-                      cudaStream_t stream) {
+bool plan_tc(int64_t M, int64_t N, TcPlan* out) {
   using C = Cfg<QT, GATEUP>;
   const int BN = choose_bn(M, N);
-  CUtensorMap tx, tw0, tw1;
-  memset(&tw0, 0, sizeof(tw0));
-  memset(&tw1, 0, sizeof(tw1));
-  if (!make_tmap_x(&tx, x, M, K, BN)) return cudaErrorInvalidValue;
-  Params p;
-  p.q6_group = 1;
-  p.q6_rows_tma = 0;
-  if (QT == kQ4K) {
-    if (!make_tmap_q4k(&tw0, W0, N, K)) return cudaErrorInvalidValue;
-    if (GATEUP && !make_tmap_q4k(&tw1, W1, N, K)) return cudaErrorInvalidValue;
-  } else {
-    p.q6_group = q6_group(K);
-    if (N / p.q6_group > 0) {
-      if (!make_tmap_q6k(&tw0, W0, N, K, p.q6_group)) return cudaErrorInvalidValue;
-      p.q6_rows_tma = (int)((N / p.q6_group) * p.q6_group);
-    }
-  }
-  p.w[0] = static_cast<const uint8_t*>(W0);
-  p.w[1] = static_cast<const uint8_t*>(W1);
-  p.w_bytes = N * (K / kQK) * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
-  p.y = y;
-  p.M = (int)M;
-  p.N = (int)N;
-  p.K = (int)K;
-  p.BN = BN;
-  // Pipeline depths (all measured on GB300).  The K-step rings come first: a
-  // single-tensor kernel with fewer than 4 x-tile stages ran ~35 % slower.
-  // Single-tensor problems grow A-tile and x-tile stages alternately, A first
-  // and never fewer A than x stages; gate/up grows x stages first (its issuers
-  // waited on x tiles while its dequant threads had slack: 3 x + 2 A stages
-  // ran 12 % faster than 2 + 3).  Up to 5 A and 4 x stages (deeper rings were
-  // no faster, and slower for Q6_K attn_v), while shared memory (and, with A
-  // in tensor memory, TMEM) allows.  Two packed-block stages where the rings still reach 4 x
-  // stages next to them (cold-cache Q6_K ran faster with two), else one (the
-  // dequant threads copy a super-block to registers and release its slot at
-  // once, so the refill overlaps the block's four K steps).
-  // Q6_K takes 4 A stages.  Its threads write two consecutive K steps of a
-  // super-block and the two halves of a row alternate.  With SA = 2 a half
-  // waits on a slot whose previous phase (the other half's step) it never
-  // saw, so the parity test can pass a phase early (seen on GB300 as wrong
-  // output once the packed copies ran ahead).  From SA = 3 on, the phase a
-  // half skips belongs to an earlier step of the same issuer, whose UMMAs
-  // complete in order, so it has always completed.  Q6_K keeps SX <= SA (its
-  // done ring is indexed by A slot), and its x ring wants 4 stages.
   constexpr int kMaxXStages = 4, kMaxAStages = QT == kQ6K ? 4 : 5;
   auto depths = [&](int P_, int& SX_, int& SA_) {
     auto fits = [&](int sx, int sa) {
@@ -1080,16 +1114,61 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
       SA = sa1;
     }
   }
-  if constexpr (AT) {  // A tiles do not fit next to the accumulators: keep them in shared memory
-    if (kIssuers * BN + SA * C::kNumB * 32 > 512 || (QT == kQ6K && SA != 4))
-      return launch_tc<QT, GATEUP, false>(W0, W1, x, y, M, N, K, stream);
+  if (AT && (kIssuers * BN + SA * C::kNumB * 32 > 512 || (QT == kQ6K && SA != 4))) return false;
+  const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
+  uint32_t sm_smem, reserved;
+  sm_smem_limits(&sm_smem, &reserved);
+  out->BN = BN;
+  out->SX = SX;
+  out->SA = SA;
+  out->P = P;
+  out->tmem_cols = tmem_cols_for(BN, SA, C::kNumB, AT);
+  out->smem = smem_for_tmem(L.total, out->tmem_cols, sm_smem, reserved);
+  out->bar_off = L.bar_off;
+  return true;
+}
+
+template <int QT, bool GATEUP, bool AT>
+cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
+                      cudaStream_t stream) {
+  using C = Cfg<QT, GATEUP>;
+  TcPlan pl;
+  if (!plan_tc<QT, GATEUP, AT>(M, N, &pl)) {
+    if constexpr (AT) return launch_tc<QT, GATEUP, false>(W0, W1, x, y, M, N, K, stream);
+    return cudaErrorInvalidConfiguration;
   }
+  const int BN = pl.BN, SX = pl.SX, SA = pl.SA, P = pl.P;
   if (QT == kQ6K && SA != 4) return cudaErrorInvalidConfiguration;  // not reached for BN <= 256
+  CUtensorMap tx, tw0, tw1;
+  memset(&tw0, 0, sizeof(tw0));
+  memset(&tw1, 0, sizeof(tw1));
+  if (!make_tmap_x(&tx, x, M, K, BN)) return cudaErrorInvalidValue;
+  Params p;
+  p.q6_group = 1;
+  p.q6_rows_tma = 0;
+  if (QT == kQ4K) {
+    if (!make_tmap_q4k(&tw0, W0, N, K)) return cudaErrorInvalidValue;
+    if (GATEUP && !make_tmap_q4k(&tw1, W1, N, K)) return cudaErrorInvalidValue;
+  } else {
+    p.q6_group = q6_group(K);
+    if (N / p.q6_group > 0) {
+      if (!make_tmap_q6k(&tw0, W0, N, K, p.q6_group)) return cudaErrorInvalidValue;
+      p.q6_rows_tma = (int)((N / p.q6_group) * p.q6_group);
+    }
+  }
+  p.w[0] = static_cast<const uint8_t*>(W0);
+  p.w[1] = static_cast<const uint8_t*>(W1);
+  p.w_bytes = N * (K / kQK) * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
+  p.y = y;
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.BN = BN;
   p.stages = SX;
   p.astages = SA;
   p.pstages = P;
   p.ksplit = 1;
-  const uint32_t smem = make_layout<QT, GATEUP, AT>(BN, SX, SA, P).total;
+  const uint32_t smem = pl.smem;
   if (smem > (uint32_t)kSmemLimit) return cudaErrorInvalidConfiguration;
   static PerDeviceFlag attr_set;  // the shared-memory limit is a per-device function attribute
   const int dev = current_device();
@@ -1118,14 +1197,13 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   {
     const int64_t tiles = (int64_t)grid.x * grid.y;
     const int64_t nb = K / kQK;
-    const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
     int64_t best = nb;
     const int64_t sms = device_sms();
     if (tiles * 2 <= sms)
       for (int c = 2; c <= 8; ++c) {
         const int64_t per = (nb + c - 1) / c;
         if (per < best && tiles * c <= sms && c <= nb &&
-            (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= L.bar_off &&
+            (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= pl.bar_off &&
             tiles <= max_active_clusters<QT, GATEUP, AT>(c, smem)) {
           ks = c;
           best = per;
@@ -1154,6 +1232,25 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<QT, GATEUP, AT, true>, tx, tw0, tw1, p);
 }
 
+// The plan of the instantiation launch_gemm picks (host only).
+template <int QT, bool GATEUP, bool AT>
+bool plan_for(int64_t M, int64_t N, TcPlan* pl, int* a_in_tmem) {
+  if (plan_tc<QT, GATEUP, AT>(M, N, pl)) {
+    *a_in_tmem = AT ? 1 : 0;
+    return true;
+  }
+  if constexpr (AT) return plan_for<QT, GATEUP, false>(M, N, pl, a_in_tmem);
+  return false;
+}
+
+int a_tmem_default() {
+  static const int a_tmem = [] {
+    const char* e = getenv("QK_A_TMEM");
+    return e ? atoi(e) : 1;
+  }();
+  return a_tmem;
+}
+
 }  // namespace
 
 uint32_t gemm_take_status() {
@@ -1168,10 +1265,7 @@ cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t
   // Single-tensor problems keep the dequantized A tiles in tensor memory when
   // they fit next to the accumulators (measured faster on GB300: no A-tile
   // shared-memory writes and UMMA reads); QK_A_TMEM=0 selects shared memory.
-  static const int a_tmem = [] {
-    const char* e = getenv("QK_A_TMEM");
-    return e ? atoi(e) : 1;
-  }();
+  const int a_tmem = a_tmem_default();
   if (gateup) return launch_tc<kQ4K, true, false>(W, W_up, x, y, M, N, K, s);
   if (t == kQ4K) {
     if (a_tmem) return launch_tc<kQ4K, false, true>(W, nullptr, x, y, M, N, K, s);
@@ -1179,6 +1273,31 @@ cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t
   }
   if (a_tmem) return launch_tc<kQ6K, false, true>(W, nullptr, x, y, M, N, K, s);
   return launch_tc<kQ6K, false, false>(W, nullptr, x, y, M, N, K, s);
+}
+
+bool gemm_plan(QType t, bool gateup, int64_t M, int64_t N, GemmPlanInfo* info) {
+  TcPlan pl;
+  int at = 0;
+  bool ok;
+  const int a_tmem = a_tmem_default();
+  if (gateup)
+    ok = plan_for<kQ4K, true, false>(M, N, &pl, &at);
+  else if (t == kQ4K)
+    ok = a_tmem ? plan_for<kQ4K, false, true>(M, N, &pl, &at) : plan_for<kQ4K, false, false>(M, N, &pl, &at);
+  else
+    ok = a_tmem ? plan_for<kQ6K, false, true>(M, N, &pl, &at) : plan_for<kQ6K, false, false>(M, N, &pl, &at);
+  if (!ok) return false;
+  uint32_t sm_smem, reserved;
+  sm_smem_limits(&sm_smem, &reserved);
+  info->token_tile = pl.BN;
+  info->x_stages = pl.SX;
+  info->a_stages = pl.SA;
+  info->packed_stages = pl.P;
+  info->a_in_tmem = at;
+  info->tmem_cols = (int)pl.tmem_cols;
+  info->smem_bytes = (int)pl.smem;
+  info->max_ctas_per_sm = (int)(sm_smem / (pl.smem + reserved));
+  return true;
 }
 
 }  // namespace qk

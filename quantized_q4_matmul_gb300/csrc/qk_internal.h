@@ -55,6 +55,13 @@ cudaError_t launch_gemv(QType t, const void* W, const uint16_t* x, float* y, int
 cudaError_t launch_gemm(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M,
                         int64_t N, int64_t K, bool gateup, cudaStream_t s);
 
+// The tensor-core GEMM's launch plan for an M x N problem (host only; the
+// fields mirror qk_gemm_plan_info).  False if no plan exists.
+struct GemmPlanInfo {
+  int token_tile, x_stages, a_stages, packed_stages, a_in_tmem, tmem_cols, smem_bytes, max_ctas_per_sm;
+};
+bool gemm_plan(QType t, bool gateup, int64_t M, int64_t N, GemmPlanInfo* info);
+
 // A kernel whose single bounded wait can never complete (see qk_debug_wait_timeout).
 cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t s);
 

@@ -164,3 +164,53 @@ def test_decode_kernel_choice_on_the_host(qk_lib):
     assert L.qk_decode_uses_gemv(1, 1, 3072) == -1      # gate/up is Q4_K only
     assert L.qk_decode_uses_gemv(0, 0, 300) == -1       # K % 256
     assert L.qk_decode_uses_gemv(0, 0, 0) == -1
+
+
+def test_gemm_plans_fit_tensor_memory_on_a_shared_sm(qk_lib):
+    """tcgen05.alloc waits without a time limit for free tensor-memory columns,
+    so the CTAs that can share an SM must fit in its 512 columns together.
+    Checked on the host for every linear of the model at every swept M (and the
+    small-M shapes that pick narrow token tiles), for both A-tile placements."""
+    import subprocess
+    import sys
+    from tests import synth
+    shapes = sorted({(lin.qtype, lin.N, lin.K) for _, lin in synth.model_linears()})
+    Ms = sorted(set(synth.SWEEP_M) | {2, 17, 33, 48, 64, 100, 200, 300, 513, 4096})
+    seen_tmem = set()
+    for qt, N, K in shapes:
+        for M in Ms:
+            p = qk_lib.qk_gemm_plan(qt, M, N, K)
+            assert p["max_ctas_per_sm"] >= 1
+            assert p["max_ctas_per_sm"] * p["tmem_cols"] <= 512, (qt, N, K, M, p)
+            assert p["smem_bytes"] <= 227 * 1024
+            seen_tmem.add(p["a_in_tmem"])
+    for M in Ms:
+        p = qk_lib.qk_gemm_plan("q4k", M, synth.FFN, synth.HIDDEN, gateup=True)
+        assert p["max_ctas_per_sm"] * p["tmem_cols"] <= 512, (M, p)
+    assert seen_tmem == {0, 1}
+    # A narrow token tile with A tiles in tensor memory needs 2*64 + 5*32 = 288
+    # columns (allocated as 512) in ~70 KB of shared memory: padded to one CTA.
+    p = qk_lib.qk_gemm_plan("q4k", 64, 4096, 4096)
+    assert p["token_tile"] == 64 and p["a_in_tmem"] == 1 and p["tmem_cols"] == 512
+    assert p["max_ctas_per_sm"] == 1
+    # The shared-memory A path (QK_A_TMEM=0) in a child process: same rule.
+    code = ("import sys; sys.path.insert(0, %r); import quantized_q4_matmul_gb300 as qk\n"
+            "for M in (16, 64, 128, 1024):\n"
+            "    p = qk.qk_gemm_plan('q6k', M, 3072, 8192)\n"
+            "    assert p['a_in_tmem'] == 0 and p['max_ctas_per_sm'] * p['tmem_cols'] <= 512, p\n"
+            "print('ok')" % ROOT)
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, QK_A_TMEM="0"), capture_output=True,
+                       text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
+
+
+def test_gemm_plan_rejects_bad_arguments(qk_lib):
+    L = qk_lib.lib()
+    info = qk_lib.qk_gemm_plan_info()
+    import ctypes as C
+    assert L.qk_gemm_plan(0, 0, 16, 3072, 3072, None) == -1
+    assert L.qk_gemm_plan(2, 0, 16, 3072, 3072, C.byref(info)) == -3
+    assert L.qk_gemm_plan(1, 1, 16, 3072, 3072, C.byref(info)) == -3
+    assert L.qk_gemm_plan(0, 0, 16, 3072, 300, C.byref(info)) == -3
+    assert L.qk_gemm_plan(0, 0, 0, 3072, 3072, C.byref(info)) == -3
+    assert L.qk_gemm_plan(0, 0, 16, 3072, 3072, C.byref(info)) == 0 and info.token_tile == 16
