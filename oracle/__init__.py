@@ -5,7 +5,8 @@ the benchmark's CPU-baseline leg may import this package.  The CUDA library and
 its Python binding never import it.
 
 ``qk_oracle.c`` holds the arithmetic (GGUF Q4_K / Q6_K block decoding in fp32,
-fp64-accumulated matmul, fp64 SwiGLU); this module only builds it with gcc and
+fp64-accumulated matmul, fp64 SwiGLU, fp64 RMSNorm in front of a linear); this
+module only builds it with gcc and
 marshals numpy arrays through ctypes.
 """
 from __future__ import annotations
@@ -63,6 +64,18 @@ class Oracle:
                                                 ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
                                                 ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                                 ctypes.c_void_p]
+        L.oracle_rmsnorm.restype = ctypes.c_int
+        L.oracle_rmsnorm.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_double, ctypes.c_void_p]
+        L.oracle_rmsnorm_matmul_rows.restype = ctypes.c_int
+        L.oracle_rmsnorm_matmul_rows.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                 ctypes.c_double, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                                 ctypes.c_int64, ctypes.c_void_p]
+        L.oracle_rmsnorm_gateup_swiglu_rows.restype = ctypes.c_int
+        L.oracle_rmsnorm_gateup_swiglu_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                                        ctypes.c_void_p, ctypes.c_double, ctypes.c_int64,
+                                                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
+                                                        ctypes.c_void_p]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.L = L
@@ -111,6 +124,46 @@ class Oracle:
         assert rc == 0, rc
         return (out, g, u) if return_gu else out
 
+    def rmsnorm(self, x, gamma, eps: float) -> np.ndarray:
+        """fp64 x / sqrt(mean(x^2) + eps) * gamma per row; x fp16 [M][K], gamma fp16 [K]."""
+        g = np.ascontiguousarray(gamma, dtype=np.float16).reshape(-1)
+        x = np.ascontiguousarray(x, dtype=np.float16).reshape(-1, g.size)
+        out = np.empty(x.shape, dtype=np.float64)
+        rc = self.L.oracle_rmsnorm(_ptr(x.view(np.uint16)), _ptr(g.view(np.uint16)), x.shape[0], g.size,
+                                   float(eps), _ptr(out))
+        assert rc == 0, rc
+        return out
+
+    def rmsnorm_matmul(self, qtype: int, W, x, gamma, eps: float, N: int, K: int, rows=None) -> np.ndarray:
+        """fp64 y[M][len(rows)] = (RMSNorm(x) * gamma) . W[rows]^T."""
+        W = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)
+        assert W.size == N * (K // QK) * BLOCK_BYTES[qtype]
+        g = np.ascontiguousarray(gamma, dtype=np.float16).reshape(-1)
+        assert g.size == K
+        x = np.ascontiguousarray(x, dtype=np.float16).reshape(-1, K)
+        r = _rows(N, rows)
+        y = np.empty((x.shape[0], r.size), dtype=np.float64)
+        rc = self.L.oracle_rmsnorm_matmul_rows(qtype, _ptr(W), _ptr(x.view(np.uint16)), _ptr(g.view(np.uint16)),
+                                               float(eps), x.shape[0], K, _ptr(r), r.size, _ptr(y))
+        assert rc == 0, rc
+        return y
+
+    def rmsnorm_gateup_swiglu(self, Wg, Wu, x, gamma, eps: float, N_ff: int, K: int, rows=None) -> np.ndarray:
+        """fp64 silu(xhat.Wg^T) * (xhat.Wu^T) with xhat = RMSNorm(x) * gamma."""
+        Wg = np.ascontiguousarray(Wg, dtype=np.uint8).reshape(-1)
+        Wu = np.ascontiguousarray(Wu, dtype=np.uint8).reshape(-1)
+        assert Wg.size == Wu.size == N_ff * (K // QK) * BLOCK_BYTES[Q4K]
+        g = np.ascontiguousarray(gamma, dtype=np.float16).reshape(-1)
+        assert g.size == K
+        x = np.ascontiguousarray(x, dtype=np.float16).reshape(-1, K)
+        r = _rows(N_ff, rows)
+        out = np.empty((x.shape[0], r.size), dtype=np.float64)
+        rc = self.L.oracle_rmsnorm_gateup_swiglu_rows(_ptr(Wg), _ptr(Wu), _ptr(x.view(np.uint16)),
+                                                      _ptr(g.view(np.uint16)), float(eps), x.shape[0], K, _ptr(r),
+                                                      r.size, _ptr(out))
+        assert rc == 0, rc
+        return out
+
     def num_threads(self) -> int:
         return int(self.L.oracle_num_threads())
 
@@ -142,6 +195,18 @@ def matmul(qtype, W, x, N, K, rows=None):
 
 def gateup_swiglu(Wg, Wu, x, N_ff, K, rows=None, return_gu=False):
     return default().gateup_swiglu(Wg, Wu, x, N_ff, K, rows, return_gu)
+
+
+def rmsnorm(x, gamma, eps):
+    return default().rmsnorm(x, gamma, eps)
+
+
+def rmsnorm_matmul(qtype, W, x, gamma, eps, N, K, rows=None):
+    return default().rmsnorm_matmul(qtype, W, x, gamma, eps, N, K, rows)
+
+
+def rmsnorm_gateup_swiglu(Wg, Wu, x, gamma, eps, N_ff, K, rows=None):
+    return default().rmsnorm_gateup_swiglu(Wg, Wu, x, gamma, eps, N_ff, K, rows)
 
 
 def num_threads():

@@ -28,6 +28,8 @@
  *  - matmul: y[m][n] = sum_k x[m][k] * w[n][k], summed in fp64 in k order;
  *    x is fp16 widened exactly, w is the fp32 dequantized weight.
  *  - SwiGLU: out = g / (1 + exp(-g)) * u with g, u the fp64 sums above.
+ *  - RMSNorm in front of a linear: xhat = x / sqrt(mean(x^2) + eps) * gamma
+ *    in fp64, then the matmul above over xhat (not rounded to fp16).
  *
  * Parity pins live in the test suite (hand-built blocks with closed forms,
  * bit-placement tables, an independent bit-level decoder, one-hot and all-ones
@@ -194,14 +196,10 @@ static void dequant_row(int qtype, const uint8_t *W, int64_t n, int64_t K, float
         dequant_block(qtype, W + (n * nb + b) * bb, w + b * ORACLE_QK);
 }
 
-int oracle_matmul_rows(int qtype, const uint8_t *W, const uint16_t *x, int64_t M, int64_t K,
+/* The matmul over activations already widened to fp64 (xd is [M][K]). */
+static int matmul_core(int qtype, const uint8_t *W, const double *xd, int64_t M, int64_t K,
                        const int64_t *rows, int64_t n_rows, double *y)
 {
-    if (!block_bytes(qtype) || M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
-        return -1;
-    double *xd = widen_x(x, M, K);
-    if (!xd)
-        return -2;
     int failed = 0;
 #pragma omp parallel
     {
@@ -225,22 +223,28 @@ int oracle_matmul_rows(int qtype, const uint8_t *W, const uint16_t *x, int64_t M
         }
         free(w);
     }
-    free(xd);
     return failed ? -2 : 0;
+}
+
+int oracle_matmul_rows(int qtype, const uint8_t *W, const uint16_t *x, int64_t M, int64_t K,
+                       const int64_t *rows, int64_t n_rows, double *y)
+{
+    if (!block_bytes(qtype) || M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
+        return -1;
+    double *xd = widen_x(x, M, K);
+    if (!xd)
+        return -2;
+    const int rc = matmul_core(qtype, W, xd, M, K, rows, n_rows, y);
+    free(xd);
+    return rc;
 }
 
 /* SwiGLU over two Q4_K weight sets with the same x:
  * out[m][r] = silu(g) * u, g = x[m] . wg[rows[r]], u = x[m] . wu[rows[r]],
  * silu(g) = g / (1 + exp(-g)), all in fp64.  Optionally also returns g and u. */
-int oracle_gateup_swiglu_rows(const uint8_t *Wg, const uint8_t *Wu, const uint16_t *x, int64_t M,
-                              int64_t K, const int64_t *rows, int64_t n_rows, double *out,
-                              double *g_out, double *u_out)
+static int gateup_core(const uint8_t *Wg, const uint8_t *Wu, const double *xd, int64_t M, int64_t K,
+                       const int64_t *rows, int64_t n_rows, double *out, double *g_out, double *u_out)
 {
-    if (M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
-        return -1;
-    double *xd = widen_x(x, M, K);
-    if (!xd)
-        return -2;
     int failed = 0;
 #pragma omp parallel
     {
@@ -274,8 +278,82 @@ int oracle_gateup_swiglu_rows(const uint8_t *Wg, const uint8_t *Wu, const uint16
         free(wg);
         free(wu);
     }
-    free(xd);
     return failed ? -2 : 0;
+}
+
+int oracle_gateup_swiglu_rows(const uint8_t *Wg, const uint8_t *Wu, const uint16_t *x, int64_t M,
+                              int64_t K, const int64_t *rows, int64_t n_rows, double *out,
+                              double *g_out, double *u_out)
+{
+    if (M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
+        return -1;
+    double *xd = widen_x(x, M, K);
+    if (!xd)
+        return -2;
+    const int rc = gateup_core(Wg, Wu, xd, M, K, rows, n_rows, out, g_out, u_out);
+    free(xd);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* RMSNorm in front of a linear (DAMASCUS project overview, "[04] one decode  */
+/* step": an RMSNorm comes before the QKV projections and before the SwiGLU  */
+/* FFN; "Building DAMASCUS", "Read the model, then reproduce its             */
+/* operations").  The pages give no formula or epsilon; the reading taken is */
+/* the standard RMSNorm of the Llama family:                                  */
+/*   xhat[m][k] = x[m][k] / sqrt(mean_k(x[m][k]^2) + eps) * gamma[k],         */
+/* all in fp64, with x and gamma fp16 widened exactly.                        */
+/* ------------------------------------------------------------------------ */
+int oracle_rmsnorm(const uint16_t *x, const uint16_t *gamma, int64_t M, int64_t K, double eps, double *out)
+{
+    if (M < 0 || K <= 0 || !(eps >= 0.0))
+        return -1;
+    for (int64_t m = 0; m < M; ++m) {
+        const uint16_t *xm = x + m * K;
+        double ss = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double v = (double)oracle_half_to_float(xm[k]);
+            ss += v * v;
+        }
+        const double inv = 1.0 / sqrt(ss / (double)K + eps);
+        for (int64_t k = 0; k < K; ++k)
+            out[m * K + k] = (double)oracle_half_to_float(xm[k]) * inv * (double)oracle_half_to_float(gamma[k]);
+    }
+    return 0;
+}
+
+/* y[m][r] = sum_k xhat[m][k] * w[rows[r]][k] with xhat = RMSNorm(x) * gamma. */
+int oracle_rmsnorm_matmul_rows(int qtype, const uint8_t *W, const uint16_t *x, const uint16_t *gamma,
+                               double eps, int64_t M, int64_t K, const int64_t *rows, int64_t n_rows,
+                               double *y)
+{
+    if (!block_bytes(qtype) || M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
+        return -1;
+    double *xn = (double *)malloc((size_t)(M * K) * sizeof(double) + 1);
+    if (!xn)
+        return -2;
+    int rc = oracle_rmsnorm(x, gamma, M, K, eps, xn);
+    if (rc == 0)
+        rc = matmul_core(qtype, W, xn, M, K, rows, n_rows, y);
+    free(xn);
+    return rc;
+}
+
+/* The fused gate/up + SwiGLU of RMSNorm(x) * gamma. */
+int oracle_rmsnorm_gateup_swiglu_rows(const uint8_t *Wg, const uint8_t *Wu, const uint16_t *x,
+                                      const uint16_t *gamma, double eps, int64_t M, int64_t K,
+                                      const int64_t *rows, int64_t n_rows, double *out)
+{
+    if (M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
+        return -1;
+    double *xn = (double *)malloc((size_t)(M * K) * sizeof(double) + 1);
+    if (!xn)
+        return -2;
+    int rc = oracle_rmsnorm(x, gamma, M, K, eps, xn);
+    if (rc == 0)
+        rc = gateup_core(Wg, Wu, xn, M, K, rows, n_rows, out, NULL, NULL);
+    free(xn);
+    return rc;
 }
 
 int oracle_num_threads(void)

@@ -15,6 +15,10 @@ What the pins rest on:
 * Worked blocks with hand-derived scales, closed forms (all-zero / all-max
   quants), one-hot and all-ones activations, a float64 library matmul,
   linearity, row permutation and the SwiGLU closed form via scipy's expit.
+* RMSNorm: hand-worked examples (tests/golden/rmsnorm_worked.txt), the closed
+  form of a constant vector, unit mean square and exact invariance to scaling
+  x by a power of two, a one-hot gamma, and the composition with the matmul
+  and the SwiGLU against float64 library routines.
 """
 from __future__ import annotations
 
@@ -455,7 +459,82 @@ def pin_gateup_swiglu(O):
     assert not np.allclose(sw, out)
 
 
+# ---------------------------------------------------------------------------
+# RMSNorm in front of a linear
+# ---------------------------------------------------------------------------
+def pin_rmsnorm_worked(O):
+    for ln in _lines("rmsnorm_worked.txt"):
+        eps, xs, gs, want = (p.split() for p in ln.split("|"))
+        x = np.array([float(v) for v in xs], np.float16)
+        g = np.array([float(v) for v in gs], np.float16)
+        got = O.rmsnorm(x.reshape(1, -1), g, float(eps[0]))[0]
+        exp = np.array([float(v) for v in want])
+        assert np.allclose(got, exp, rtol=1e-15, atol=0), (ln, got)
+
+
+def pin_rmsnorm_constant_vector(O):
+    """x = c everywhere, gamma = 1: xhat = sign(c) / sqrt(1 + eps / c^2)."""
+    K = 3072
+    for c in (0.5, -2.0, 0.0009765625, 100.0):
+        for eps in (0.0, 1e-5, 1e-2):
+            x = np.full((1, K), c, np.float16)
+            got = O.rmsnorm(x, np.ones(K, np.float16), eps)[0]
+            want = np.sign(c) / np.sqrt(1.0 + eps / (c * c))
+            assert np.allclose(got, want, rtol=1e-14, atol=0), (c, eps, got[0], want)
+
+
+def pin_rmsnorm_unit_mean_square_and_scale_invariance(O):
+    rng = synth.rng_for(61, 0)
+    K = 3072
+    x = synth.activations(rng, 3, K)
+    one = np.ones(K, np.float16)
+    a = O.rmsnorm(x, one, 0.0)
+    assert np.allclose((a ** 2).mean(axis=1), 1.0, rtol=1e-12)
+    # scaling x by 4 scales the sum of squares by 16 and the root by 4, all
+    # exactly: the output is bit-identical
+    b = O.rmsnorm((x.astype(np.float32) * 4).astype(np.float16), one, 0.0)
+    assert np.array_equal(a, b)
+
+
+def pin_rmsnorm_gamma_onehot(O):
+    rng = synth.rng_for(62, 0)
+    K = 512
+    x = synth.activations(rng, 2, K)
+    rms = np.sqrt((x.astype(np.float64) ** 2).mean(axis=1) + 1e-5)
+    for k in (0, 7, K - 1):
+        g = np.zeros(K, np.float16)
+        g[k] = 1
+        out = O.rmsnorm(x, g, 1e-5)
+        assert np.count_nonzero(out[:, np.arange(K) != k]) == 0
+        assert np.allclose(out[:, k], x[:, k].astype(np.float64) / rms, rtol=1e-14)
+
+
+def pin_rmsnorm_matmul_composition(O):
+    """The normalized linear equals a float64 library matmul of the oracle's
+    dequantized weights with its normalized activations (and the SwiGLU of two
+    such, through scipy's expit), with eps large enough to matter."""
+    from scipy.special import expit
+    rng = synth.rng_for(63, 0)
+    K, N, eps = 512, 40, 1e-2
+    x = (synth.activations(rng, 3, K).astype(np.float32) * 0.05).astype(np.float16)
+    g = (1.0 + 0.1 * rng.standard_normal(K)).astype(np.float16)
+    xn = O.rmsnorm(x, g, eps)
+    for qt in (Q4K, Q6K):
+        W = synth.weights(rng, "q4k" if qt == Q4K else "q6k", N, K)
+        w = O.dequant(qt, W).astype(np.float64).reshape(N, K)
+        got = O.rmsnorm_matmul(qt, W, x, g, eps, N, K)
+        ref = xn @ w.T
+        assert np.all(np.abs(got - ref) <= 1e-13 * (np.abs(xn) @ np.abs(w).T))
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    G = xn @ O.dequant(Q4K, Wg).astype(np.float64).reshape(N, K).T
+    U = xn @ O.dequant(Q4K, Wu).astype(np.float64).reshape(N, K).T
+    got = O.rmsnorm_gateup_swiglu(Wg, Wu, x, g, eps, N, K)
+    assert np.allclose(got, G * expit(G) * U, rtol=1e-10, atol=1e-12 * np.abs(G * U).max())
+
+
 ALL_PINS = [
+    pin_rmsnorm_worked, pin_rmsnorm_constant_vector, pin_rmsnorm_unit_mean_square_and_scale_invariance,
+    pin_rmsnorm_gamma_onehot, pin_rmsnorm_matmul_composition,
     pin_half_to_float,
     pin_q4k_scale_bits,
     pin_q4k_quant_map,

@@ -59,6 +59,15 @@ MUTANTS = [
      "const uint8_t *sc = (const uint8_t *)(blk + 192);"),
     ("q6k_lane_of_16", "l = i % 32;", "l = i % 16;"),
     ("half_sign_dropped", "return sign ? -v : v;", "return v;"),
+    # RMSNorm in front of a linear
+    ("rms_eps_outside_sqrt", "1.0 / sqrt(ss / (double)K + eps)", "1.0 / (sqrt(ss / (double)K) + eps)"),
+    ("rms_mean_of_x", "ss += v * v;", "ss += v;"),
+    ("rms_sum_not_mean", "sqrt(ss / (double)K + eps)", "sqrt(ss + eps)"),
+    ("rms_gamma_dropped", "* inv * (double)oracle_half_to_float(gamma[k]);", "* inv;"),
+    ("rms_gamma_reversed", "oracle_half_to_float(gamma[k])", "oracle_half_to_float(gamma[K - 1 - k])"),
+    ("rms_matmul_eps_ignored", "int rc = oracle_rmsnorm(x, gamma, M, K, eps, xn);\n    if (rc == 0)\n        rc = matmul_core",
+     "int rc = oracle_rmsnorm(x, gamma, M, K, 0.0, xn);\n    if (rc == 0)\n        rc = matmul_core"),
+    ("rms_gateup_up_as_gate", "rc = gateup_core(Wg, Wu, xn", "rc = gateup_core(Wg, Wg, xn"),
 ]
 
 
