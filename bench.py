@@ -187,6 +187,37 @@ def _cpu_inputs():
     return _CPU_INPUTS
 
 
+def cpu_single_thread():
+    """The oracle on one host thread over configs 0 and 1 in full: the attn_q
+    matmul at M = 16 (0.30 GFLOP) and the decode layer's seven linears at M = 1
+    (63.9 MB of weights), each timed once after a warm-up call."""
+    import oracle
+    rng = synth.rng_for(7, 2)
+    n0 = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        q = synth.Linear("attn_q", synth.Q4K, synth.HIDDEN, synth.HIDDEN)
+        W = synth.q4k_weights(rng, q.N, q.K)
+        x = synth.activations(rng, 16, q.K)
+        oracle.matmul(oracle.Q4K, W, x[:1], q.N, q.K, rows=np.arange(64))
+        t0 = time.perf_counter()
+        oracle.matmul(oracle.Q4K, W, x, q.N, q.K)
+        t_q = time.perf_counter() - t0
+        lins = synth.layer_linears(0)
+        data = [(l, synth.weights(rng, l.qtype, l.N, l.K), synth.activations(rng, 1, l.K)) for l in lins]
+        t0 = time.perf_counter()
+        for l, W, x in data:
+            oracle.matmul(oracle.Q4K if l.qtype == "q4k" else oracle.Q6K, W, x, l.N, l.K)
+        t_d = time.perf_counter() - t0
+    finally:
+        oracle.set_num_threads(n0)
+    dbytes = sum(synth.weight_bytes(l.qtype, l.N, l.K) + 2 * l.K + 4 * l.N for l in lins)
+    return {"attn_q_m16": {"ms": 1e3 * t_q, "tflops": 2.0 * 16 * q.N * q.K / t_q / 1e12, "cores": 1,
+                           "sample": "full problem (M=16, N=K=3072), fp64 oracle, 1 thread"},
+            "decode_layer_m1": {"ms": 1e3 * t_d, "gbs": dbytes / t_d / 1e9, "cores": 1,
+                                "sample": "one layer's 7 linears at M=1 in full, fp64 oracle, 1 thread"}}
+
+
 def cpu_baseline(target_s: float = 12.0):
     """The oracle on host cores over a bounded sample of the prefill step: the
     same fraction f of the output features of each of its problems (gate/up +
@@ -248,7 +279,7 @@ class Workload:
             d["v"] = torch.from_numpy(synth.q6k_weights(rng, v.N, v.K)).to(dev)
             d["x_gu"] = torch.from_numpy(synth.activations(rng, PREFILL_M, gate.K).view(np.uint16)).to(dev)
             d["x_down"] = torch.from_numpy(synth.swiglu_activations(rng, PREFILL_M, down.K).view(np.uint16)).to(dev)
-            d["x_v"] = torch.from_numpy(synth.activations(rng, PREFILL_M, v.K).view(np.uint16)).to(dev)
+            d["x_v"] = torch.from_numpy(synth.swiglu_activations(rng, PREFILL_M, v.K).view(np.uint16)).to(dev)
             dec = []
             for lin in decode_linears():
                 Wd = torch.from_numpy(synth.weights(rng, lin.qtype, lin.N, lin.K)).to(dev)
@@ -352,6 +383,214 @@ def measure_dequant(torch, qk, wl, stream, dev, reps):
             "ms_per_layer": med, "bytes_per_layer": nbytes, "launches_per_layer": len(lins),
             "note": "qk_dequant_q4k/q6k over one layer's 7 weight tensors (packed in, fp32 out), "
                     "one CUDA graph per rotating copy, %d replays" % reps}
+
+
+# ----------------------------------------------------------------------------
+# Per-configuration measurements (each kernel timed alone, L2 flushed first)
+# ----------------------------------------------------------------------------
+L2_FLUSH_BYTES = 512 << 20  # written before every timed launch: more than the 129 MB L2
+
+
+def stats(ms):
+    """Median, p95 and spread of per-run times (ms)."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "p95": float(np.percentile(a, 95)), "min": float(a.min()),
+            "max": float(a.max()), "runs": int(a.size)}
+
+
+def roof(flops, nbytes, ms, pk):
+    """Achieved rates and the fraction of the attainable rate min(peak, AI x BW)."""
+    s = ms * 1e-3
+    tflops, gbs = flops / s / 1e12, nbytes / s / 1e9
+    ai = flops / nbytes
+    att = min(pk["bf16_tflops"], ai * pk["hbm_gbs"] / 1e3)
+    bound = "tensor" if att >= pk["bf16_tflops"] else "hbm"
+    return {"tflops": tflops, "gbs": gbs, "intensity_flop_per_byte": ai, "bound": bound,
+            "attainable_tflops": att, "frac_of_attainable": tflops / att}
+
+
+def timed(torch, stream, fn, reps, flush):
+    """CUDA-event time of fn() on `stream`, each run after an L2 flush."""
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(reps + 2):
+            flush.fill_(i & 0xFF)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 2:
+                ms.append(e0.elapsed_time(e1))
+    return ms
+
+
+def lin_bytes(lin, M, gateup=False):
+    """Packed weight bytes + fp16 x + output bytes of one linear at M tokens."""
+    w = synth.weight_bytes(lin.qtype, lin.N, lin.K) * (2 if gateup else 1)
+    return w + 2 * M * lin.K + (2 if gateup else 4) * M * lin.N
+
+
+def device_weights(torch, gen, qtype, N, K, dev):
+    """Seeded random blocks drawn on the device with the recipe of tests/synth.py
+    (uniform quant and scale bytes, fp16 |N(0,1)|*1e-4 scales; Q6_K int8 scales
+    uniform on -32..63), for the sweep's 1.9 GiB of weights."""
+    nb = N * (K // 256)
+    bb = 144 if qtype == "q4k" else 210
+    blk = torch.randint(0, 256, (nb, bb), dtype=torch.uint8, device=dev, generator=gen)
+
+    def f16(n):
+        return (torch.randn(n, device=dev, generator=gen).abs() * 1e-4).half().view(torch.uint8).view(n, 2)
+
+    if qtype == "q4k":
+        blk[:, 0:2] = f16(nb)
+        blk[:, 2:4] = f16(nb)
+    else:
+        blk[:, 192:208] = torch.randint(-32, 64, (nb, 16), dtype=torch.int8, device=dev, generator=gen).view(
+            torch.uint8)
+        blk[:, 208:210] = f16(nb)
+    return blk.view(-1)
+
+
+def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
+    """Every workload configuration with its own roofline fraction:
+    config 0 (attn_q M=16), config 1 (the decode layer: grouped, chained and per
+    linear), config 2 (gate/up + SwiGLU M=1024), config 3 (down and attn_v
+    M=1024, separately) and config 4 (every linear of the model plus the LM head
+    at M in 1..2048)."""
+    s = stream.cuda_stream
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    out = {}
+    rng = synth.rng_for(0, 900)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    def x16(M, K, swiglu=False):
+        x = synth.swiglu_activations(rng, M, K) if swiglu else synth.activations(rng, M, K)
+        return up(x.view(np.uint16))
+
+    def entry(name, flops, nbytes, ms, kernel, extra=None):
+        st = stats(ms)
+        r = {"kernel": kernel, "ms": st, "flops": flops, "bytes": nbytes}
+        r.update(roof(flops, nbytes, st["median"], pk))
+        if extra:
+            r.update(extra)
+        log("  %-28s %8.4f ms  %8.1f GB/s  %7.1f TFLOP/s  %5.1f%% of attainable (%s)" % (
+            name, st["median"], r["gbs"], r["tflops"], 100 * r["frac_of_attainable"], r["bound"]))
+        return r
+
+    fns = {"q4k": qk.qk_matmul_q4k, "q6k": qk.qk_matmul_q6k}
+
+    def kernel_of(qtype, M, K, gateup=False):
+        if M == 1 and qk.qk_decode_uses_gemv(qtype, K, gateup):
+            return "gemv_stream_kernel (decode GEMV)"
+        return "gemm_tc_kernel (tcgen05 GEMM)"
+
+    # config 0: attn_q, M = 16
+    q = synth.Linear("attn_q", synth.Q4K, synth.HIDDEN, synth.HIDDEN)
+    W = up(synth.q4k_weights(rng, q.N, q.K))
+    x = x16(16, q.K)
+    y = torch.empty(16, q.N, dtype=torch.float32, device=dev)
+    ms = timed(torch, stream, lambda: qk.qk_matmul_q4k(W, x, y, 16, q.N, q.K, s), reps, flush)
+    out["attn_q_m16"] = entry("attn_q M=16", 2.0 * 16 * q.N * q.K, lin_bytes(q, 16), ms, kernel_of("q4k", 16, q.K))
+    del W, x, y
+
+    # config 1: one layer's seven linears at M = 1
+    lins = synth.layer_linears(0)
+    Ws = [up(synth.weights(rng, l.qtype, l.N, l.K)) for l in lins]
+    xs = [x16(1, l.K) for l in lins]
+    ys = [torch.empty(1, l.N, dtype=torch.float32, device=dev) for l in lins]
+    y_gu = torch.empty(1, synth.FFN, dtype=torch.float16, device=dev)
+    per = {}
+    for l, W, x, y in zip(lins, Ws, xs, ys):
+        ms = timed(torch, stream, lambda: fns[l.qtype](W, x, y, 1, l.N, l.K, s), reps, flush)
+        per[l.name] = entry("decode " + l.name, 2.0 * l.N * l.K, lin_bytes(l, 1), ms, kernel_of(l.qtype, 1, l.K))
+    probs = [dict(qtype=l.qtype, blocks=W, x_f16=x, y=y, M=1, N=l.N, K=l.K) for l, W, x, y in zip(lins, Ws, xs, ys)]
+    layer_bytes = sum(lin_bytes(l, 1) for l in lins)
+    layer_flops = sum(2.0 * l.N * l.K for l in lins)
+    ms = timed(torch, stream, lambda: qk.qk_matmul_batch(probs, s), reps, flush)
+    grouped = entry("decode layer, grouped", layer_flops, layer_bytes, ms, "gemv_stream_kernel, one launch")
+
+    def chain():
+        qk.qk_matmul_batch(probs[0:3], s)
+        qk.qk_matmul_batch(probs[3:4], s)
+        qk.qk_gateup_swiglu_q4k(Ws[4], Ws[5], xs[4], y_gu, 1, lins[4].N, lins[4].K, s)
+        qk.qk_matmul_batch(probs[6:7], s)
+
+    cbytes = layer_bytes - lin_bytes(lins[5], 1) - lin_bytes(lins[4], 1) + lin_bytes(lins[4], 1, gateup=True)
+    ms = timed(torch, stream, chain, reps, flush)
+    chained = entry("decode layer, chained", layer_flops, cbytes, ms,
+                    "gemv_stream_kernel, 4 launches: {q,k,v} -> o -> gate/up+SwiGLU -> down")
+    out["decode_layer_m1"] = {"grouped": grouped, "chained": chained, "per_linear": per}
+    del Ws, xs, ys, probs
+
+    # config 2: fused gate/up + SwiGLU at M = 1024
+    g = synth.Linear("ffn_gate", synth.Q4K, synth.FFN, synth.HIDDEN)
+    Wg, Wu = up(synth.q4k_weights(rng, g.N, g.K)), up(synth.q4k_weights(rng, g.N, g.K))
+    x = x16(PREFILL_M, g.K)
+    y = torch.empty(PREFILL_M, g.N, dtype=torch.float16, device=dev)
+    ms = timed(torch, stream, lambda: qk.qk_gateup_swiglu_q4k(Wg, Wu, x, y, PREFILL_M, g.N, g.K, s), reps, flush)
+    out["prefill_gateup_swiglu_m1024"] = entry("gate/up+SwiGLU M=1024", 2.0 * 2 * PREFILL_M * g.N * g.K,
+                                               lin_bytes(g, PREFILL_M, gateup=True), ms,
+                                               kernel_of("q4k", PREFILL_M, g.K, True))
+    del Wg, Wu, x, y
+
+    # config 3: down (Q6_K, K 8192) and attn_v (Q6_K, 3072 -> 1024) at M = 1024, x = silu(z1) z2
+    c3 = {}
+    for l in (synth.Linear("ffn_down", synth.Q6K, synth.HIDDEN, synth.FFN),
+              synth.Linear("attn_v", synth.Q6K, synth.KV_DIM, synth.HIDDEN)):
+        W = up(synth.q6k_weights(rng, l.N, l.K))
+        x = x16(PREFILL_M, l.K, swiglu=True)
+        y = torch.empty(PREFILL_M, l.N, dtype=torch.float32, device=dev)
+        ms = timed(torch, stream, lambda: qk.qk_matmul_q6k(W, x, y, PREFILL_M, l.N, l.K, s), reps, flush)
+        c3[l.name] = entry(l.name + " M=1024", 2.0 * PREFILL_M * l.N * l.K, lin_bytes(l, PREFILL_M), ms,
+                           kernel_of("q6k", PREFILL_M, l.K))
+        del W, x, y
+    out["prefill_down_v_m1024"] = c3
+    del flush
+    torch.cuda.empty_cache()
+
+    # config 4: every linear of the 28 layers plus the LM head, one call each, at each M
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    model = synth.model_linears()
+    Wm = [device_weights(torch, gen, l.qtype, l.N, l.K, dev) for _, l in model]
+    wbytes = sum(synth.weight_bytes(l.qtype, l.N, l.K) for _, l in model)
+    sweep = {}
+    for M in synth.SWEEP_M:
+        xk = {K: x16(M, K) for K in sorted({l.K for _, l in model})}
+        yn = {N: torch.empty(M, N, dtype=torch.float32, device=dev) for N in sorted({l.N for _, l in model})}
+
+        def one_pass():
+            for (_, l), W in zip(model, Wm):
+                fns[l.qtype](W, xk[l.K], yn[l.N], M, l.N, l.K, s)
+
+        with torch.cuda.stream(stream):
+            one_pass()
+        torch.cuda.synchronize()
+        ms = []
+        with torch.cuda.stream(stream):
+            for i in range(max(3, reps // 2)):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                one_pass()
+                e1.record(stream)
+                e1.synchronize()
+                ms.append(e0.elapsed_time(e1))
+        flops = sum(2.0 * M * l.N * l.K for _, l in model)
+        nbytes = sum(lin_bytes(l, M) for _, l in model)
+        sweep[str(M)] = entry("model sweep M=%d" % M, flops, nbytes, ms,
+                              "%s, %d launches per pass" % (kernel_of("q4k", M, 3072), len(model)),
+                              {"weight_bytes": wbytes})
+        del xk, yn
+    out["model_sweep"] = sweep
+    out["note"] = ("each kernel timed alone with CUDA events, a %d MB write flushing L2 before every run "
+                   "(the sweep's 1.9 GiB of weights exceed L2); attainable = min(bf16 peak, intensity x HBM)"
+                   % (L2_FLUSH_BYTES >> 20))
+    del Wm
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_gpu(args, rank, world, dist):
@@ -550,6 +789,11 @@ def run_gpu(args, rank, world, dist):
         "gpu_launches": sum(r["launches"] for r in allr),
         "clocks": local_res["clocks"],
     }
+    # Every workload configuration timed alone (rank 0), after the step's
+    # numbers are final.
+    if not args.no_configs:
+        res["configs"] = measure_configs(torch, qk, dev, stream, max(10, args.steps), pk,
+                                         log=lambda m: print(m, file=sys.stderr))
     # The dequant export (not part of the step) last, on rank 0, after every
     # number above is final: whatever happens here only affects this field.
     try:
@@ -616,6 +860,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration measurements")
     ap.add_argument("--profile", choices=["gateup", "down", "v", "decode"],
                     help="run one call of the step 5 times on one GPU and exit (for ncu)")
     args = ap.parse_args()
@@ -626,6 +871,9 @@ def main():
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.gpus != world:
+        sys.exit("bench.py: --gpus %d but WORLD_SIZE is %d: launch N > 1 ranks with torchrun "
+                 "(python -m torch.distributed.run --nproc-per-node N bench.py --gpus N ...)" % (args.gpus, world))
     dist = None
     if world > 1:
         import torch.distributed as dist_mod
@@ -639,6 +887,7 @@ def main():
         res = run_gpu(args, rank, world, dist)
         if res is not None and not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_baseline()
+            res["cpu_baseline"]["single_thread"] = cpu_single_thread()
     if res is not None:
         print(json.dumps(res), flush=True)
     if dist is not None:

@@ -149,6 +149,46 @@ typedef struct qk_matmul_desc {
 qk_status qk_matmul_batch(const qk_matmul_desc *descs, int count, qk_stream_t stream);
 
 /*
+ * RMSNorm in front of the linears (DAMASCUS project overview, "[04] one decode
+ * step": an RMSNorm comes before the QKV projections and before the SwiGLU
+ * FFN; "Building DAMASCUS", "Read the model, then reproduce its operations").
+ * Every problem's x is replaced by
+ *   xhat[m][k] = fp16( x[m][k] / sqrt(mean_k x[m][k]^2 + eps) * gamma[k] )
+ * (sum of squares, scale and products in fp32; gamma is fp16[K], the same K
+ * for every problem of the call; eps finite and >= 0) and the problems then
+ * run as in qk_matmul_batch.  Problems the GEMV runs (M <= 16, see
+ * qk_uses_gemv) normalize inside its x staging: no extra pass, no scratch.
+ * Problems the tensor-core GEMM runs first have their xhat written to
+ * `scratch`, a caller-owned device buffer of at least qk_rmsnorm_scratch_bytes
+ * (the largest M * K * 2 over those problems; NULL is allowed when no problem
+ * needs it); problems run in order on `stream` and share it.  scratch must
+ * not overlap gamma or any input or output; the library cannot check its
+ * size.  Returns QK_ERR_NULL (gamma, or scratch when needed), QK_ERR_ALIGN,
+ * QK_ERR_SHAPE (eps negative or not finite, problems of different K), and the
+ * codes of qk_matmul_batch.
+ */
+qk_status qk_rmsnorm_matmul_batch(const qk_matmul_desc *descs, int count, const uint16_t *gamma_f16, float eps,
+                                  void *scratch, qk_stream_t stream);
+
+/* One problem of qk_rmsnorm_matmul_batch: y = (RMSNorm(x) * gamma) . W^T, Q4_K or Q6_K weights. */
+qk_status qk_rmsnorm_matmul_q4k(const void *blocks, const uint16_t *x_f16, const uint16_t *gamma_f16, float eps,
+                                void *scratch, float *y, int64_t M, int64_t N, int64_t K, qk_stream_t stream);
+qk_status qk_rmsnorm_matmul_q6k(const void *blocks, const uint16_t *x_f16, const uint16_t *gamma_f16, float eps,
+                                void *scratch, float *y, int64_t M, int64_t N, int64_t K, qk_stream_t stream);
+
+/* The fused gate/up + SwiGLU of qk_gateup_swiglu_q4k over RMSNorm(x) * gamma. */
+qk_status qk_rmsnorm_gateup_swiglu_q4k(const void *gate_blocks, const void *up_blocks, const uint16_t *x_f16,
+                                       const uint16_t *gamma_f16, float eps, void *scratch, uint16_t *y_f16,
+                                       int64_t M, int64_t N_ff, int64_t K, qk_stream_t stream);
+
+/*
+ * Host-only query: bytes of scratch an M-token problem of this format and K
+ * needs under qk_rmsnorm_matmul_batch (0 when the GEMV fuses the norm, else
+ * M * K * 2), or -1 for invalid arguments.
+ */
+int64_t qk_rmsnorm_scratch_bytes(int qtype, int gateup, int64_t M, int64_t K);
+
+/*
  * Synchronise `stream`, then report and clear the device-side status flags
  * that the library's kernels set when a bounded wait expires.  Returns QK_OK,
  * QK_ERR_TIMEOUT, or QK_ERR_CUDA if the synchronisation itself failed.
@@ -176,6 +216,16 @@ qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream);
  * together only while their joint plan fits.
  */
 int qk_decode_uses_gemv(int qtype, int gateup, int64_t K);
+
+/*
+ * Host-only query (no CUDA call), for any M: 1 if an M x N x K problem in
+ * format `qtype` (gateup != 0: the fused gate/up + SwiGLU) runs on the
+ * CUDA-core-fed GEMV (M <= 16: M = 1 in the decode layout, 2..16 with the
+ * tokens in the MMA columns; the x table of M tokens plus two weight stages
+ * must fit in shared memory), 0 if it runs on the tensor-core GEMM, -1 for
+ * invalid arguments.  qk_decode_uses_gemv(q, g, K) is qk_uses_gemv(q, g, 1, K).
+ */
+int qk_uses_gemv(int qtype, int gateup, int64_t M, int64_t K);
 
 /*
  * Host-only query: the launch plan the tensor-core GEMM (M > 1, and M = 1

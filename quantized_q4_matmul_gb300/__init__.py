@@ -18,7 +18,8 @@ import os
 __all__ = [
     "QKError", "lib", "lib_path", "qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k",
     "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout",
-    "qk_decode_uses_gemv", "qk_gemm_plan", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
+    "qk_decode_uses_gemv", "qk_uses_gemv", "qk_gemm_plan", "qk_rmsnorm_matmul_batch", "qk_rmsnorm_matmul_q4k",
+    "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
     "qk_gemm_plan_info",
 ]
 
@@ -27,7 +28,9 @@ QK_BLOCK_BYTES = {"q4k": 144, "q6k": 210}
 
 SYMBOLS = ("qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k", "qk_gateup_swiglu_q4k",
            "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout", "qk_decode_uses_gemv",
-           "qk_gemm_plan", "qk_status_string", "qk_version")
+           "qk_uses_gemv", "qk_gemm_plan", "qk_rmsnorm_matmul_batch", "qk_rmsnorm_matmul_q4k",
+           "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes", "qk_status_string",
+           "qk_version")
 
 QK_Q4_K, QK_Q6_K = 0, 1
 
@@ -81,6 +84,16 @@ def lib():
         L.qk_get_device_status.restype, L.qk_get_device_status.argtypes = i32, [vp]
         L.qk_debug_wait_timeout.restype, L.qk_debug_wait_timeout.argtypes = i32, [i64, vp]
         L.qk_decode_uses_gemv.restype, L.qk_decode_uses_gemv.argtypes = i32, [i32, i32, i64]
+        L.qk_uses_gemv.restype, L.qk_uses_gemv.argtypes = i32, [i32, i32, i64, i64]
+        f32 = ctypes.c_float
+        L.qk_rmsnorm_matmul_batch.restype = i32
+        L.qk_rmsnorm_matmul_batch.argtypes = [ctypes.POINTER(qk_matmul_desc), i32, vp, f32, vp, vp]
+        for name in ("qk_rmsnorm_matmul_q4k", "qk_rmsnorm_matmul_q6k"):
+            f = getattr(L, name)
+            f.restype, f.argtypes = i32, [vp, vp, vp, f32, vp, vp, i64, i64, i64, vp]
+        L.qk_rmsnorm_gateup_swiglu_q4k.restype = i32
+        L.qk_rmsnorm_gateup_swiglu_q4k.argtypes = [vp, vp, vp, vp, f32, vp, vp, i64, i64, i64, vp]
+        L.qk_rmsnorm_scratch_bytes.restype, L.qk_rmsnorm_scratch_bytes.argtypes = i64, [i32, i32, i64, i64]
         L.qk_gemm_plan.restype = i32
         L.qk_gemm_plan.argtypes = [i32, i32, i64, i64, i64, ctypes.POINTER(qk_gemm_plan_info)]
         L.qk_status_string.restype, L.qk_status_string.argtypes = ctypes.c_char_p, [i32]
@@ -185,10 +198,7 @@ def qk_gateup_swiglu_q4k(gate_blocks, up_blocks, x_f16, y_f16, M: int, N_ff: int
     _check(lib().qk_gateup_swiglu_q4k(g, u, x, o, int(M), int(N_ff), int(K), _stream(stream)), name)
 
 
-def qk_matmul_batch(problems, stream=None) -> None:
-    """Run independent problems in as few launches as possible.  Each problem is
-    a dict with keys qtype ("q4k"/"q6k" or 0/1), blocks, x_f16, y, M, N, K and
-    optionally up_blocks (fused gate/up + SwiGLU, fp16 y)."""
+def _descs(problems):
     arr = (qk_matmul_desc * max(1, len(problems)))()
     for i, p in enumerate(problems):
         qt = p["qtype"]
@@ -202,7 +212,77 @@ def qk_matmul_batch(problems, stream=None) -> None:
                                 _buf(p["x_f16"], _n(M) * _n(K) * 2, what + ": x_f16", _F16),
                                 _buf(p["y"], _n(M) * _n(N) * (2 if gu else 4), what + ": y", _F16 if gu else _F32),
                                 M, N, K)
+    return arr
+
+
+def qk_matmul_batch(problems, stream=None) -> None:
+    """Run independent problems in as few launches as possible.  Each problem is
+    a dict with keys qtype ("q4k"/"q6k" or 0/1), blocks, x_f16, y, M, N, K and
+    optionally up_blocks (fused gate/up + SwiGLU, fp16 y)."""
+    arr = _descs(problems)
     _check(lib().qk_matmul_batch(arr, len(problems), _stream(stream)), "qk_matmul_batch")
+
+
+def qk_rmsnorm_scratch_bytes(qtype, M: int, K: int, gateup: bool = False) -> int:
+    """Scratch bytes an M-token problem needs under the RMSNorm entry points
+    (0 when the GEMV fuses the norm); host only."""
+    qt = {"q4k": QK_Q4_K, "q6k": QK_Q6_K}.get(qtype, qtype)
+    r = int(lib().qk_rmsnorm_scratch_bytes(int(qt), int(bool(gateup)), int(M), int(K)))
+    if r < 0:
+        raise ValueError("qk_rmsnorm_scratch_bytes: invalid qtype %r, M %d or K %d" % (qtype, M, K))
+    return r
+
+
+def _scratch(problems, scratch, what):
+    need = 0
+    for p in problems:
+        qt = {"q4k": QK_Q4_K, "q6k": QK_Q6_K}.get(p["qtype"], p["qtype"])
+        if int(p["M"]) > 0 and int(p["N"]) > 0:
+            need = max(need, qk_rmsnorm_scratch_bytes(qt, p["M"], p["K"], p.get("up_blocks") is not None))
+    return _buf(scratch, need, what + ": scratch", _F16 + ("torch.uint8",))
+
+
+def qk_rmsnorm_matmul_batch(problems, gamma_f16, eps: float, scratch=None, stream=None) -> None:
+    """qk_matmul_batch over RMSNorm(x) * gamma (see include/qk.h); `scratch` is
+    needed for problems the tensor-core GEMM runs (qk_rmsnorm_scratch_bytes)."""
+    what = "qk_rmsnorm_matmul_batch"
+    arr = _descs(problems)
+    K = max([int(p["K"]) for p in problems] or [0])
+    g = _buf(gamma_f16, 2 * K, what + ": gamma_f16", _F16)
+    sc = _scratch(problems, scratch, what)
+    _check(lib().qk_rmsnorm_matmul_batch(arr, len(problems), g, float(eps), sc, _stream(stream)), what)
+
+
+def _rms_single(name, qtype, blocks, up_blocks, x_f16, gamma_f16, eps, scratch, y, M, N, K, stream):
+    gu = up_blocks is not None
+    wb = _weight_bytes(qtype, N, K)
+    w = _buf(blocks, wb, name + ": blocks")
+    x = _buf(x_f16, _n(M) * _n(K) * 2, name + ": x_f16", _F16)
+    g = _buf(gamma_f16, 2 * _n(K), name + ": gamma_f16", _F16)
+    need = qk_rmsnorm_scratch_bytes(qtype, max(0, int(M)), K, gu) if int(K) > 0 and int(K) % 256 == 0 else 0
+    sc = _buf(scratch, need, name + ": scratch", _F16 + ("torch.uint8",))
+    if gu:
+        u = _buf(up_blocks, wb, name + ": up_blocks")
+        o = _buf(y, _n(M) * _n(N) * 2, name + ": y_f16", _F16)
+        rc = lib().qk_rmsnorm_gateup_swiglu_q4k(w, u, x, g, float(eps), sc, o, int(M), int(N), int(K), _stream(stream))
+    else:
+        o = _buf(y, _n(M) * _n(N) * 4, name + ": y", _F32)
+        rc = getattr(lib(), name)(w, x, g, float(eps), sc, o, int(M), int(N), int(K), _stream(stream))
+    _check(rc, name)
+
+
+def qk_rmsnorm_matmul_q4k(blocks, x_f16, gamma_f16, eps, y, M, N, K, scratch=None, stream=None) -> None:
+    _rms_single("qk_rmsnorm_matmul_q4k", QK_Q4_K, blocks, None, x_f16, gamma_f16, eps, scratch, y, M, N, K, stream)
+
+
+def qk_rmsnorm_matmul_q6k(blocks, x_f16, gamma_f16, eps, y, M, N, K, scratch=None, stream=None) -> None:
+    _rms_single("qk_rmsnorm_matmul_q6k", QK_Q6_K, blocks, None, x_f16, gamma_f16, eps, scratch, y, M, N, K, stream)
+
+
+def qk_rmsnorm_gateup_swiglu_q4k(gate_blocks, up_blocks, x_f16, gamma_f16, eps, y_f16, M, N_ff, K, scratch=None,
+                                 stream=None) -> None:
+    _rms_single("qk_rmsnorm_gateup_swiglu_q4k", QK_Q4_K, gate_blocks, up_blocks, x_f16, gamma_f16, eps, scratch,
+                y_f16, M, N_ff, K, stream)
 
 
 def qk_decode_uses_gemv(qtype, K: int, gateup: bool = False) -> bool:
@@ -212,6 +292,16 @@ def qk_decode_uses_gemv(qtype, K: int, gateup: bool = False) -> bool:
     r = int(lib().qk_decode_uses_gemv(int(qt), int(bool(gateup)), int(K)))
     if r < 0:
         raise ValueError("qk_decode_uses_gemv: invalid qtype %r or K %d" % (qtype, K))
+    return bool(r)
+
+
+def qk_uses_gemv(qtype, M: int, K: int, gateup: bool = False) -> bool:
+    """Whether an M-token problem of this format and K runs on the GEMV (True)
+    or on the tensor-core GEMM (False); host only."""
+    qt = {"q4k": QK_Q4_K, "q6k": QK_Q6_K}.get(qtype, qtype)
+    r = int(lib().qk_uses_gemv(int(qt), int(bool(gateup)), int(M), int(K)))
+    if r < 0:
+        raise ValueError("qk_uses_gemv: invalid qtype %r, M %d or K %d" % (qtype, M, K))
     return bool(r)
 
 

@@ -9,6 +9,7 @@
 #include <atomic>
 #include <cstdint>
 #include <cstdlib>
+#include <algorithm>
 #include <vector>
 
 #include "../../include/qk.h"
@@ -131,14 +132,15 @@ qk_status validate_device(const void* W, const void* W_up, const uint16_t* x, co
   return QK_OK;
 }
 
-// The decode GEMV handles M = 1 when its shared-memory plan fits K; the
-// tensor-core GEMM takes everything else (M = 1 as a one-token tile).
-bool use_gemv(const qk::GemvDesc& d, int64_t M) { return M <= qk::gemv_max_m() && qk::gemv_plan_fits(&d, 1); }
+// The GEMV handles M <= 16 when its shared-memory plan fits (the x table of
+// M tokens and K plus two weight stages); the tensor-core GEMM takes
+// everything else.
+bool use_gemv(const qk::GemvDesc& d) { return d.M <= qk::gemv_max_m() && qk::gemv_plan_fits(&d, 1); }
 
 qk_status run(QType t, const void* W, const void* W_up, const uint16_t* x, void* y, int64_t M, int64_t N, int64_t K,
               bool gateup, cudaStream_t s) {
-  const qk::GemvDesc d{t, W, gateup ? W_up : nullptr, x, y, N, K};
-  if (use_gemv(d, M)) return map_cuda(qk::launch_gemv_batch(&d, 1, s));
+  const qk::GemvDesc d{t, W, gateup ? W_up : nullptr, x, y, M, N, K, nullptr, 0.f};
+  if (use_gemv(d)) return map_cuda(qk::launch_gemv_batch(&d, 1, s));
   return map_cuda(qk::launch_gemm(t, W, W_up, x, y, M, N, K, gateup, s));
 }
 
@@ -151,11 +153,10 @@ qk_status matmul(QType t, const void* W, const void* W_up, const uint16_t* x, vo
   return run(t, W, W_up, x, y, M, N, K, gateup, s);
 }
 
-qk_status matmul_batch(const qk_matmul_desc* d, int count, cudaStream_t s) {
-  if (count < 0) return QK_ERR_SHAPE;
-  if (count == 0) return QK_OK;
-  if (!d) return QK_ERR_NULL;
-  std::vector<Checked> ck((size_t)count);
+// Host and device checks of a grouped call, including that no y overlaps
+// another entry's input or output.
+qk_status validate_batch(const qk_matmul_desc* d, int count, std::vector<Checked>& ck) {
+  ck.assign((size_t)count, Checked{});
   for (int i = 0; i < count; ++i) {
     if (d[i].qtype != QK_Q4_K && d[i].qtype != QK_Q6_K) return QK_ERR_SHAPE;
     const QType t = d[i].qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K;
@@ -178,39 +179,118 @@ qk_status matmul_batch(const qk_matmul_desc* d, int count, cudaStream_t s) {
           (d[j].up_blocks && overlaps(d[i].y, ck[(size_t)i].y_bytes, d[j].up_blocks, wb)))
         return QK_ERR_ALIAS;
     }
-  // M = 1 problems share GEMV launches: a problem joins the current group if
-  // the group's plan still fits with it (x of the largest K is staged once per
-  // CTA), else the group is launched first.
-  std::vector<qk::GemvDesc> group;
-  auto flush = [&]() -> qk_status {
-    if (group.empty()) return QK_OK;
-    const qk_status st = map_cuda(qk::launch_gemv_batch(group.data(), (int)group.size(), s));
-    group.clear();
+  return QK_OK;
+}
+
+// Run validated problems.  GEMV problems share launches, up to 8 per launch,
+// with the problems of the same token-slot count (M = 1; 2..8; 9..16); each
+// keeps its own plan, so a problem's result does not depend on its group.
+// With gamma, every problem's x passes through RMSNorm * gamma first: inside
+// the GEMV's x staging, or for GEMM problems into `scratch` (M * K fp16),
+// which the GEMM then reads (problems run in order on one stream, so they can
+// share the scratch; one x is normalized once for consecutive problems).
+qk_status run_batch(const qk_matmul_desc* d, int count, const uint16_t* gamma, float eps, uint16_t* scratch,
+                    cudaStream_t s) {
+  std::vector<qk::GemvDesc> groups[3];
+  auto slot_index = [](int64_t M) { const int k = qk::gemv_slots(M); return k == 1 ? 0 : k == 8 ? 1 : 2; };
+  auto flush = [&](int gi) -> qk_status {
+    if (groups[gi].empty()) return QK_OK;
+    const qk_status st = map_cuda(qk::launch_gemv_batch(groups[gi].data(), (int)groups[gi].size(), s));
+    groups[gi].clear();
     return st;
   };
+  const uint16_t* normalized = nullptr;  // the x whose rows the scratch holds
+  int64_t normalized_m = 0;
   for (int i = 0; i < count; ++i) {
     if (d[i].M == 0 || d[i].N == 0) continue;
     const QType t = d[i].qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K;
     const bool gu = d[i].up_blocks != nullptr;
-    const qk::GemvDesc g{t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].N, d[i].K};
-    if (use_gemv(g, d[i].M)) {
-      group.push_back(g);
-      if (group.size() > 1 && !qk::gemv_plan_fits(group.data(), (int)group.size())) {
-        group.pop_back();
-        const qk_status st = flush();
-        if (st != QK_OK) return st;
-        group.push_back(g);
-      }
-      if ((int)group.size() == qk::kMaxGemvProbs) {
-        const qk_status st = flush();
+    const qk::GemvDesc g{t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].M, d[i].N, d[i].K, gamma, eps};
+    if (use_gemv(g)) {
+      const int gi = slot_index(d[i].M);
+      groups[gi].push_back(g);
+      if ((int)groups[gi].size() == qk::kMaxGemvProbs) {
+        const qk_status st = flush(gi);
         if (st != QK_OK) return st;
       }
-    } else {
-      const qk_status st = run(t, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y, d[i].M, d[i].N, d[i].K, gu, s);
-      if (st != QK_OK) return st;
+      continue;
+    }
+    const uint16_t* x = d[i].x_f16;
+    if (gamma) {
+      if (normalized != d[i].x_f16 || normalized_m != d[i].M) {
+        const qk_status st = map_cuda(qk::launch_rmsnorm_rows(d[i].x_f16, gamma, eps, scratch, d[i].M, d[i].K, s));
+        if (st != QK_OK) return st;
+        normalized = d[i].x_f16;
+        normalized_m = d[i].M;
+      }
+      x = scratch;
+    }
+    const qk_status st = map_cuda(qk::launch_gemm(t, d[i].blocks, d[i].up_blocks, x, d[i].y, d[i].M, d[i].N, d[i].K,
+                                                  gu, s));
+    if (st != QK_OK) return st;
+  }
+  for (int gi = 0; gi < 3; ++gi) {
+    const qk_status st = flush(gi);
+    if (st != QK_OK) return st;
+  }
+  return QK_OK;
+}
+
+qk_status matmul_batch(const qk_matmul_desc* d, int count, cudaStream_t s) {
+  if (count < 0) return QK_ERR_SHAPE;
+  if (count == 0) return QK_OK;
+  if (!d) return QK_ERR_NULL;
+  std::vector<Checked> ck;
+  const qk_status st = validate_batch(d, count, ck);
+  if (st != QK_OK) return st;
+  return run_batch(d, count, nullptr, 0.f, nullptr, s);
+}
+
+// Bytes of RMSNorm scratch one problem needs: 0 when the GEMV runs it (the
+// norm is fused into its x staging), else M * K fp16.
+int64_t norm_scratch_bytes(const qk_matmul_desc& d) {
+  if (d.M == 0 || d.N == 0) return 0;
+  const QType t = d.qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K;
+  const qk::GemvDesc g{t, d.blocks, d.up_blocks, d.x_f16, d.y, d.M, d.N, d.K, nullptr, 0.f};
+  return use_gemv(g) ? 0 : d.M * d.K * 2;
+}
+
+qk_status rmsnorm_matmul_batch(const qk_matmul_desc* d, int count, const uint16_t* gamma, float eps, void* scratch,
+                               cudaStream_t s) {
+  if (count < 0) return QK_ERR_SHAPE;
+  if (count == 0) return QK_OK;
+  if (!d || !gamma) return QK_ERR_NULL;
+  if (!(eps >= 0.0f) || !(eps <= 3.0e38f)) return QK_ERR_SHAPE;  // finite, non-negative
+  if (!aligned16(gamma)) return QK_ERR_ALIGN;
+  std::vector<Checked> ck;
+  qk_status st = validate_batch(d, count, ck);
+  if (st != QK_OK) return st;
+  int64_t K0 = -1, need = 0;
+  for (int i = 0; i < count; ++i) {
+    if (d[i].M == 0 || d[i].N == 0) continue;
+    if (K0 >= 0 && d[i].K != K0) return QK_ERR_SHAPE;  // one gamma of K values for every problem
+    K0 = d[i].K;
+    need = std::max(need, norm_scratch_bytes(d[i]));
+  }
+  if (K0 < 0) return QK_OK;
+  if ((st = check_pointer(gamma)) != QK_OK) return st;
+  for (int i = 0; i < count; ++i)
+    if (ck[(size_t)i].y_bytes && overlaps(d[i].y, ck[(size_t)i].y_bytes, gamma, K0 * 2)) return QK_ERR_ALIAS;
+  if (need > 0) {
+    if (!scratch) return QK_ERR_NULL;
+    if (!aligned16(scratch)) return QK_ERR_ALIGN;
+    if ((st = check_pointer(scratch)) != QK_OK) return st;
+    if (overlaps(scratch, need, gamma, K0 * 2)) return QK_ERR_ALIAS;
+    for (int i = 0; i < count; ++i) {
+      const Checked& c = ck[(size_t)i];
+      if (c.y_bytes == 0) continue;
+      if (overlaps(scratch, need, d[i].x_f16, c.x_bytes) || overlaps(scratch, need, d[i].y, c.y_bytes) ||
+          overlaps(scratch, need, d[i].blocks, c.w_bytes) ||
+          (d[i].up_blocks && overlaps(scratch, need, d[i].up_blocks, c.w_bytes)))
+        return QK_ERR_ALIAS;
     }
   }
-  return flush();
+  return run_batch(d, count, gamma, eps, static_cast<uint16_t*>(scratch), s);
 }
 
 }  // namespace
@@ -267,6 +347,39 @@ qk_status qk_matmul_batch(const qk_matmul_desc* descs, int count, qk_stream_t st
   return matmul_batch(descs, count, reinterpret_cast<cudaStream_t>(stream));
 }
 
+qk_status qk_rmsnorm_matmul_batch(const qk_matmul_desc* descs, int count, const uint16_t* gamma_f16, float eps,
+                                  void* scratch, qk_stream_t stream) {
+  return rmsnorm_matmul_batch(descs, count, gamma_f16, eps, scratch, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qk_status qk_rmsnorm_matmul_q4k(const void* blocks, const uint16_t* x_f16, const uint16_t* gamma_f16, float eps,
+                                void* scratch, float* y, int64_t M, int64_t N, int64_t K, qk_stream_t stream) {
+  const qk_matmul_desc d{QK_Q4_K, blocks, nullptr, x_f16, y, M, N, K};
+  return qk_rmsnorm_matmul_batch(&d, 1, gamma_f16, eps, scratch, stream);
+}
+
+qk_status qk_rmsnorm_matmul_q6k(const void* blocks, const uint16_t* x_f16, const uint16_t* gamma_f16, float eps,
+                                void* scratch, float* y, int64_t M, int64_t N, int64_t K, qk_stream_t stream) {
+  const qk_matmul_desc d{QK_Q6_K, blocks, nullptr, x_f16, y, M, N, K};
+  return qk_rmsnorm_matmul_batch(&d, 1, gamma_f16, eps, scratch, stream);
+}
+
+qk_status qk_rmsnorm_gateup_swiglu_q4k(const void* gate_blocks, const void* up_blocks, const uint16_t* x_f16,
+                                       const uint16_t* gamma_f16, float eps, void* scratch, uint16_t* y_f16,
+                                       int64_t M, int64_t N_ff, int64_t K, qk_stream_t stream) {
+  if (!up_blocks && M > 0 && N_ff > 0) return QK_ERR_NULL;
+  const qk_matmul_desc d{QK_Q4_K, gate_blocks, up_blocks, x_f16, y_f16, M, N_ff, K};
+  return qk_rmsnorm_matmul_batch(&d, 1, gamma_f16, eps, scratch, stream);
+}
+
+int64_t qk_rmsnorm_scratch_bytes(int qtype, int gateup, int64_t M, int64_t K) {
+  if ((qtype != QK_Q4_K && qtype != QK_Q6_K) || (gateup && qtype != QK_Q4_K)) return -1;
+  if (K <= 0 || K % qk::kQK != 0 || K >= kMaxDim || M < 0 || M > kMaxM) return -1;
+  const void* up = gateup ? reinterpret_cast<const void*>(uintptr_t(16)) : nullptr;
+  const qk_matmul_desc d{qtype, nullptr, up, nullptr, nullptr, M, 1, K};
+  return norm_scratch_bytes(d);
+}
+
 qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream) {
   qk_status st = check_device();
   if (st != QK_OK) return st;
@@ -281,15 +394,17 @@ qk_status qk_get_device_status(qk_stream_t stream) {
   return v ? QK_ERR_TIMEOUT : QK_OK;
 }
 
-int qk_decode_uses_gemv(int qtype, int gateup, int64_t K) {
+int qk_uses_gemv(int qtype, int gateup, int64_t M, int64_t K) {
   if ((qtype != QK_Q4_K && qtype != QK_Q6_K) || (gateup && qtype != QK_Q4_K)) return -1;
-  if (K <= 0 || K % qk::kQK != 0 || K >= kMaxDim) return -1;
+  if (K <= 0 || K % qk::kQK != 0 || K >= kMaxDim || M <= 0 || M > kMaxM) return -1;
   // The weight and activation pointers are not dereferenced by the plan; the
   // up pointer only marks the problem as gate/up.
   const void* up = gateup ? reinterpret_cast<const void*>(uintptr_t(16)) : nullptr;
-  const qk::GemvDesc d{qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K, nullptr, up, nullptr, nullptr, 1, K};
-  return qk::gemv_plan_fits(&d, 1) ? 1 : 0;
+  const qk::GemvDesc d{qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K, nullptr, up, nullptr, nullptr, M, 1, K, nullptr, 0.f};
+  return use_gemv(d) ? 1 : 0;
 }
+
+int qk_decode_uses_gemv(int qtype, int gateup, int64_t K) { return qk_uses_gemv(qtype, gateup, 1, K); }
 
 qk_status qk_gemm_plan(int qtype, int gateup, int64_t M, int64_t N, int64_t K, qk_gemm_plan_info* out) {
   if (!out) return QK_ERR_NULL;

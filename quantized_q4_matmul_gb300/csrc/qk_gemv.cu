@@ -1,36 +1,42 @@
 // qk_gemv.cu -- decode GEMV (M = 1): y[n] = sum_k x[k] * w[n][k] for Q4_K and
 // Q6_K weights, one or several independent problems per launch.
 //
-// Source: DAMASCUS project overview, "[01] the thesis" (decode is one token at
-// a time, GEMV-heavy and limited by streaming the weights from memory) and
-// "[04] one decode step"; "Building DAMASCUS", "Prefill and decode need
-// different performance questions".
+// Source: DAMASCUS project overview, "[01] the thesis" (decode handles one
+// token at a time with matrix-vector products whose speed is set by streaming
+// the weights from memory) and "[04] one decode step"; "Building DAMASCUS",
+// "Prefill and decode need different performance questions".
 //
-// The kernel is HBM-bound: every packed weight byte is read once.
+// The kernel is HBM-bound by design: every packed weight byte is read once.
 //   * Streaming: the weights of 16 consecutive rows are contiguous, so one
 //     producer warp fetches a whole 16-row tile (or, for long rows, a 16-row x
 //     cb-block chunk, one copy per row) with bulk asynchronous copies into a
-//     ring of 2..8 shared-memory stages; with 100+ KB in flight per SM the HBM
-//     latency is hidden without holding data in registers.
-//   * Arithmetic: 12 compute warps split a stage into blocks (16 rows x 256
-//     weights; the two 128-weight halves are independent straight-line code).  The inner products use the warp tensor instruction
-//     mma.sync m16n8k16 (fp16 x fp16, fp32 accumulate) as a dot-product
-//     engine: a 4-bit quant OR-ed into the mantissa of fp16 1024.0 is the exact
-//     value 1024 + F*q (F = 1 or 16 by nibble position, no shifts), its product
-//     with an fp16 activation is exact and the sum fp32.  x is replicated over
-//     the 8 MMA columns, so every lane holds D = 1024*Sx + F*sum(q*x) of its
-//     rows g and g+8 for each sub-block, and
-//       sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + dmin*m)        (Q4_K)
-//       sum(w*x) = (d*sc/F)*D - Sx*(1024*d*sc/F + 32*d*sc)       (Q6_K)
-//     with Sx the sub-block's sum of x.  Lane tig (0..3) applies the scales
-//     of one quarter of each half's sub-blocks, so no scale is decoded twice.  A k-permuted fp16 copy of x and the sums Sx are staged once per
-//     CTA in shared memory.
-//   * Reduction: partial sums meet in two shuffles and one fixed-order pass
-//     over the compute warps per tile (deterministic).
+//     ring of shared-memory stages.
+//   * Arithmetic: the warp tensor instruction mma.sync m16n8k16 (fp16 x fp16,
+//     fp32 accumulate) multiplies raw quants: a 4-bit quant OR-ed into the
+//     mantissa of fp16 1024.0 is the exact value 1024 + F*q (F = 1 or 16 by
+//     nibble position; Q6_K: the 6-bit quant, F = 1 or 16), and its product
+//     with an fp16 activation is exact.
+//   * Column layout: with one token, the MMA's 8 columns do not hold copies of
+//     x.  Lane (g, t) of the warp feeds the 4 k-slots it owns in every MMA
+//     from one byte group of the block: the slots of its B half 0 belong to
+//     one sub-block (Q4_K low nibbles; Q6_K one scale group), those of half 1
+//     to another.  Column 2t holds x only at lane t's half-0 slots and column
+//     2t+1 only at its half-1 slots (every other B entry is zero), so the
+//     accumulator lane (g, t) receives, D[g][2t] and D[g][2t+1], is the sum over
+//     exactly its own two sub-blocks, for rows g and g+8.  Each lane then
+//     applies the scales of those two sub-blocks: no value is selected across
+//     lanes and no scale is decoded twice.  The zero B entries come from a
+//     zero region: a lane whose column takes no x reads zeros.
+//   * Per sub-block, with Sx the sum of x over the lane's k-slots of it:
+//       Q4_K: sum(w*x) = (d*sc/F) * (D - 1024*Sx) - (dmin*m) * Sx
+//       Q6_K: sum(w*x) = (d*sc/F) * (D - (1024 + 32F)*Sx)
+//   * Reduction: each warp sums its lanes' partials of a tile (two shuffles)
+//     and the last warp to finish the tile adds the warps' partials in a fixed
+//     order (deterministic) and writes y.
 // Q6_K blocks are 210 bytes, so a block can start 2 mod 4 bytes into shared
-// memory; its words then come from two aligned loads and a funnel shift.
-// Problem kind 1 is the fused gate/up + SwiGLU: a stage holds the gate tile
-// and the up tile of the same rows, and the epilogue writes fp16(silu(g)*u).
+// memory; its words then come from aligned loads and funnel shifts.  Problem
+// kind 1 is the fused gate/up + SwiGLU: a stage holds the gate tile and the up
+// tile of the same rows, and the epilogue writes fp16(silu(g)*u).
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -47,7 +53,8 @@ __device__ uint32_t g_gemv_status = 0;
 
 namespace {
 
-constexpr uint32_t kMagic = 0x64006400u;  // fp16x2 (1024.0, 1024.0)
+constexpr uint32_t kMagic = 0x64006400u;   // fp16x2 (1024.0, 1024.0)
+constexpr uint32_t kFMagic = 0x4B000000u;  // fp32 2^23: 0x4B0000XX is 2^23 + XX
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -74,14 +81,322 @@ __device__ __forceinline__ uint32_t lds32(uint32_t a) {
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
-__device__ __forceinline__ float ldsf(uint32_t a) { return __uint_as_float(lds32(a)); }
-__device__ __forceinline__ float2 ldsf2(uint32_t a) {
-  const uint2 v = lds64(a);
-  return make_float2(__uint_as_float(v.x), __uint_as_float(v.y));
+__device__ __forceinline__ float4 ldsf4(uint32_t a) {
+  const uint4 v = lds128(a);
+  return make_float4(__uint_as_float(v.x), __uint_as_float(v.y), __uint_as_float(v.z), __uint_as_float(v.w));
 }
 
-// 4-byte word at shared address a: 4-byte aligned (A2 = false) or 2 mod 4
-// (A2 = true: two aligned loads and a funnel shift).
+__device__ __forceinline__ float half_lo(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+}
+
+// Two consecutive 4-byte words starting at shared address a, which is 4-byte
+// aligned (A2 = false) or 2 mod 4 (A2 = true: three aligned loads, two funnel
+// shifts).
+template <bool A2>
+__device__ __forceinline__ void lds_run2(uint32_t a, uint32_t& w0, uint32_t& w1) {
+  if constexpr (!A2) {
+    w0 = lds32(a);
+    w1 = lds32(a + 4);
+  } else {
+    const uint32_t t0 = lds32(a - 2), t1 = lds32(a + 2), t2 = lds32(a + 6);
+    w0 = __funnelshift_r(t0, t1, 16);
+    w1 = __funnelshift_r(t1, t2, 16);
+  }
+}
+
+// Per-lane constants of the decode layout.
+struct Lane {
+  int g, tig;
+  uint32_t xt_off;     // offset of the lane's x-table entry inside a block's table, or its zero-region offset
+  uint32_t xt_stride;  // bytes per block for lanes that read x, 0 for lanes that read zeros
+  // Q4_K scale decode (sub-blocks 2t, 2t+1): shifts for the packed 6-bit fields
+  uint32_t sh, shA, shL;
+  bool hi;             // sub-blocks 4..7
+  // Q6_K scale group offset s = t >> 1 and the byte selectors of its two scales per word
+  uint32_t sel0, sel1;
+};
+
+// ---------------------------------------------------------------------------
+// Q4_K, one 256-weight block of rows g (row address r0) and g+8 (r1).
+// Lane t owns byte group t (quant bytes 32t .. 32t+31: low nibbles are
+// sub-block 2t, high nibbles sub-block 2t+1).  Word v (bytes 4v .. 4v+3) feeds
+// two MMAs: p = 0 the bytes 0 and 2, p = 1 the bytes 1 and 3 (shifted down by
+// 8).  In each, a0/a1 (k-slots 2t, 2t+1) carry the low nibbles (F = 1) and
+// a2/a3 (k-slots 2t+8, 2t+9) the high nibbles (F = 16) of the same two bytes.
+// The x-table entry of word v holds the B operands of both MMAs.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void q4_row_scales(uint4 h, float c0, float c1, float4 sx, const Lane& L, uint32_t fmagic,
+                                              float& y) {
+  const uint32_t A = h.y, B = h.z, C = h.w;
+  const uint32_t L1 = L.hi ? C : A, L2 = L.hi ? C : B;
+  // bytes 0, 1: the 6-bit scale (min) of sub-blocks 2t and 2t+1
+  const uint32_t sc2 = ((L1 >> L.sh) & 0x0F0Fu) | ((A >> L.shA) & 0x3030u);
+  const uint32_t mn2 = ((L2 >> L.shL) & 0x0F0Fu) | ((B >> L.shA) & 0x3030u);
+  // 2^23 + v as fp32 bit patterns; fma(d, 2^23 + v, -d * 2^23) = d * v exactly
+  const float fs0 = __uint_as_float(prmt(sc2, fmagic, 0x7440u)), fs1 = __uint_as_float(prmt(sc2, fmagic, 0x7441u));
+  const float fm0 = __uint_as_float(prmt(mn2, fmagic, 0x7440u)), fm1 = __uint_as_float(prmt(mn2, fmagic, 0x7441u));
+  const float d = half_lo(h.x), dmin = half_lo(h.x >> 16);
+  const float d16 = d * 0.0625f;
+  const float a0 = fmaf(d, fs0, d * -8388608.0f);          // d*sc0
+  const float a1 = fmaf(d16, fs1, d16 * -8388608.0f);      // d*sc1/16
+  const float m0 = fmaf(dmin, fm0, dmin * -8388608.0f);    // dmin*m0
+  const float m1 = fmaf(dmin, fm1, dmin * -8388608.0f);    // dmin*m1
+  y = fmaf(a0, c0 + sx.y, y);
+  y = fmaf(a1, c1 + sx.w, y);
+  y = fmaf(-m0, sx.x, y);
+  y = fmaf(-m1, sx.z, y);
+}
+
+__device__ __forceinline__ void q4_block(uint32_t r0, uint32_t r1, uint32_t xa, uint32_t sxa, const Lane& L,
+                                         uint32_t magic, uint32_t fmagic, float& y0, float& y1) {
+  // Every load of the block first (the loads and MMAs keep their source
+  // order), so that their latencies overlap.
+  const uint32_t o = 16u + 32u * (uint32_t)L.tig;
+  const uint4 qa = lds128(r0 + o), qb = lds128(r0 + o + 16), qc = lds128(r1 + o), qd = lds128(r1 + o + 16);
+  uint4 xb[8];
+#pragma unroll
+  for (int v = 0; v < 8; ++v) xb[v] = lds128(xa + 128u * (uint32_t)v);
+  const float4 sx = ldsf4(sxa);  // (Sx, -1024 Sx) of sub-blocks 2t and 2t+1
+  const uint4 h0 = lds128(r0), h1 = lds128(r1);
+  const uint32_t w0[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+  const uint32_t w1[8] = {qc.x, qc.y, qc.z, qc.w, qd.x, qd.y, qd.z, qd.w};
+  // four independent accumulation chains (MMA m = 2v + p goes to chain m % 4)
+  float acc[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[c][i] = 0.f;
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const uint32_t s0 = w0[v] >> 8, s1 = w1[v] >> 8;
+    mma16816(acc[(2 * v) & 3], lop_and_or<0x000F000Fu>(w0[v], magic), lop_and_or<0x000F000Fu>(w1[v], magic),
+             lop_and_or<0x00F000F0u>(w0[v], magic), lop_and_or<0x00F000F0u>(w1[v], magic), xb[v].x, xb[v].y);
+    mma16816(acc[(2 * v + 1) & 3], lop_and_or<0x000F000Fu>(s0, magic), lop_and_or<0x000F000Fu>(s1, magic),
+             lop_and_or<0x00F000F0u>(s0, magic), lop_and_or<0x00F000F0u>(s1, magic), xb[v].z, xb[v].w);
+  }
+  float c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = (acc[0][i] + acc[1][i]) + (acc[2][i] + acc[3][i]);
+  q4_row_scales(h0, c[0], c[1], sx, L, fmagic, y0);
+  q4_row_scales(h1, c[2], c[3], sx, L, fmagic, y1);
+}
+
+// ---------------------------------------------------------------------------
+// Q6_K, one block of rows g (r0) and g+8 (r1).  Weight 128h + 32j + l (half
+// h, field j = 0..3, l = 0..31) takes its low 4 bits from byte
+// 64h + 32(j & 1) + l (low nibble for j < 2, high for j >= 2) and its high 2
+// bits from bits 2j of byte 128 + 32h + l; its scale group is 8h + 2j +
+// (l >= 16).  Lane t owns l = 8t .. 8t+7 of every half and field, so all its
+// weights of a (half, field) share the scale group 8h + 2j + (t >> 1).  Pass
+// P = 0 takes fields j = 0 (B half 0, F = 1) and 1 (B half 1, F = 1), pass
+// P = 1 fields 2 and 3 (F = 16).  Word u (l = 8t + 4u .. 8t + 4u + 3) feeds two
+// MMAs, p = 0 (bytes 0 and 2) and p = 1 (bytes 1 and 3).
+// ---------------------------------------------------------------------------
+struct Q6Row {
+  uint32_t ql0[2][2], ql1[2][2], qh[2][2];  // [h][u]
+  uint32_t S[4];                            // the 16 int8 scales
+  uint32_t dw;                              // low half: d
+};
+
+template <bool A2>
+__device__ __forceinline__ void q6_load_row(uint32_t b, int tig, Q6Row& q) {
+  const uint32_t o = 8u * (uint32_t)tig;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    lds_run2<A2>(b + 64u * h + o, q.ql0[h][0], q.ql0[h][1]);
+    lds_run2<A2>(b + 64u * h + 32u + o, q.ql1[h][0], q.ql1[h][1]);
+    lds_run2<A2>(b + 128u + 32u * h + o, q.qh[h][0], q.qh[h][1]);
+  }
+  if constexpr (!A2) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q.S[i] = lds32(b + 192u + 4u * i);
+    q.dw = lds32(b + 208);
+  } else {
+    uint32_t t[6];
+#pragma unroll
+    for (int i = 0; i < 6; ++i) t[i] = lds32(b + 190u + 4u * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q.S[i] = __funnelshift_r(t[i], t[i + 1], 16);
+    q.dw = __funnelshift_r(t[4], t[5], 16);
+  }
+}
+
+// (X & lo_mask) | (H & hi_mask) | magic in two LOP3s.
+template <uint32_t LO, uint32_t HI>
+__device__ __forceinline__ uint32_t q6op(uint32_t X, uint32_t H, uint32_t magic) {
+  return lop_and_or<LO>(X, lop_and_or<HI>(H, magic));
+}
+
+// Scales of one row for pass (h, P): y += (d*sc/F) * (c + nS) for the lane's
+// two fields j = 2P (c_a) and 2P + 1 (c_b).
+__device__ __forceinline__ void q6_row_scales(uint32_t Sw, float dF, float c_a, float c_b, float ns_a, float ns_b,
+                                              const Lane& L, uint32_t fmagic, float& y) {
+  const uint32_t u = Sw ^ 0x80808080u;  // int8 + 128 as unsigned bytes
+  const float f0 = __uint_as_float(prmt(u, fmagic, L.sel0)), f1 = __uint_as_float(prmt(u, fmagic, L.sel1));
+  const float ndF = dF * -8388608.0f;
+  const float a0 = fmaf(-128.0f, dF, fmaf(dF, f0, ndF));  // dF * sc exactly
+  const float a1 = fmaf(-128.0f, dF, fmaf(dF, f1, ndF));
+  y = fmaf(a0, c_a + ns_a, y);
+  y = fmaf(a1, c_b + ns_b, y);
+}
+
+__device__ __forceinline__ void q6_block(uint32_t r0, uint32_t r1, uint32_t xa, uint32_t sxa, const Lane& L,
+                                         uint32_t magic, uint32_t fmagic, float& y0, float& y1) {
+  // The loads branch per lane on the block's alignment (rows g and g+8 share
+  // it); the warp reconverges before the MMAs, which need every lane.
+  Q6Row q, r;
+  if ((r0 & 3u) == 0) {
+    q6_load_row<false>(r0, L.tig, q);
+    q6_load_row<false>(r1, L.tig, r);
+  } else {
+    q6_load_row<true>(r0, L.tig, q);
+    q6_load_row<true>(r1, L.tig, r);
+  }
+  __syncwarp();
+  uint4 xb[8];  // entry v = 4h + 2P + u
+#pragma unroll
+  for (int v = 0; v < 8; ++v) xb[v] = lds128(xa + 128u * (uint32_t)v);
+  const float4 ns0 = ldsf4(sxa), ns1 = ldsf4(sxa + 64u);  // -(1024 + 32F) * Sx of fields 0..3, per half
+  float acc[2][2][4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int P = 0; P < 2; ++P)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[h][P][i] = 0.f;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint4 xb0 = xb[4 * h + u];      // P = 0
+      const uint4 xb1 = xb[4 * h + 2 + u];  // P = 1
+#pragma unroll
+      for (int p = 0; p < 2; ++p) {
+        const int sh = 8 * p;
+        const uint32_t X0 = q.ql0[h][u] >> sh, X1 = q.ql1[h][u] >> sh, H = q.qh[h][u] >> sh;
+        const uint32_t Y0 = r.ql0[h][u] >> sh, Y1 = r.ql1[h][u] >> sh, G = r.qh[h][u] >> sh;
+        const uint32_t H4 = H << 4, H2 = H << 2, G4 = G << 4, G2 = G << 2;
+        const uint32_t b0a = p ? xb0.z : xb0.x, b1a = p ? xb0.w : xb0.y;
+        const uint32_t b0b = p ? xb1.z : xb1.x, b1b = p ? xb1.w : xb1.y;
+        // P = 0: fields 0 (low nibble of ql0, qh bits 0-1) and 1 (low nibble of ql1, qh bits 2-3)
+        mma16816(acc[h][0], q6op<0x000F000Fu, 0x00300030u>(X0, H4, magic),
+                 q6op<0x000F000Fu, 0x00300030u>(Y0, G4, magic), q6op<0x000F000Fu, 0x00300030u>(X1, H2, magic),
+                 q6op<0x000F000Fu, 0x00300030u>(Y1, G2, magic), b0a, b1a);
+        // P = 1: fields 2 (high nibble of ql0, qh bits 4-5) and 3 (high nibble of ql1, qh bits 6-7)
+        mma16816(acc[h][1], q6op<0x00F000F0u, 0x03000300u>(X0, H4, magic),
+                 q6op<0x00F000F0u, 0x03000300u>(Y0, G4, magic), q6op<0x00F000F0u, 0x03000300u>(X1, H2, magic),
+                 q6op<0x00F000F0u, 0x03000300u>(Y1, G2, magic), b0b, b1b);
+      }
+    }
+  }
+  const float dq = half_lo(q.dw), dr = half_lo(r.dw);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float4 ns = h ? ns1 : ns0;
+#pragma unroll
+    for (int P = 0; P < 2; ++P) {
+      const float fq = P ? dq * 0.0625f : dq, fr = P ? dr * 0.0625f : dr;
+      const float na = P ? ns.z : ns.x, nb = P ? ns.w : ns.y;
+      q6_row_scales(q.S[2 * h + P], fq, acc[h][P][0], acc[h][P][1], na, nb, L, fmagic, y0);
+      q6_row_scales(r.S[2 * h + P], fr, acc[h][P][2], acc[h][P][3], na, nb, L, fmagic, y1);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Several tokens (2 <= M <= 16): the MMA columns carry tokens.  Lane (g, t)
+// supplies B for token 8*nt + g of n-tile nt from that token's k-permuted x
+// (or from the zero region for a token beyond M).  Every k-slot of one MMA
+// lies in one sub-block (Q4_K) or scale group (Q6_K), so after its MMAs lane
+// (g, t) holds that sub-block's sums for rows g, g+8 and tokens 8nt + 2t,
+// 8nt + 2t + 1, and adds scale * D - k * Sx for each:
+//   Q4_K: scale = d*sc/F, k = 1024*scale + dmin*m
+//   Q6_K: scale = d*sc/F, k = (1024 + 32F)*scale
+// Each lane decodes the scales of two sub-blocks (Q4_K) or four groups (Q6_K)
+// of its two rows, and the others reach it through shuffles within the
+// lane's quad.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void q4_row_decode(uint4 h, const Lane& L, uint32_t fmagic, float& a0, float& a1,
+                                              float& k0, float& k1) {
+  const uint32_t A = h.y, B = h.z, C = h.w;
+  const uint32_t L1 = L.hi ? C : A, L2 = L.hi ? C : B;
+  const uint32_t sc2 = ((L1 >> L.sh) & 0x0F0Fu) | ((A >> L.shA) & 0x3030u);
+  const uint32_t mn2 = ((L2 >> L.shL) & 0x0F0Fu) | ((B >> L.shA) & 0x3030u);
+  const float fs0 = __uint_as_float(prmt(sc2, fmagic, 0x7440u)), fs1 = __uint_as_float(prmt(sc2, fmagic, 0x7441u));
+  const float fm0 = __uint_as_float(prmt(mn2, fmagic, 0x7440u)), fm1 = __uint_as_float(prmt(mn2, fmagic, 0x7441u));
+  const float d = half_lo(h.x), dmin = half_lo(h.x >> 16);
+  const float d16 = d * 0.0625f;
+  a0 = fmaf(d, fs0, d * -8388608.0f);                                // d*sc0
+  a1 = fmaf(d16, fs1, d16 * -8388608.0f);                            // d*sc1/16
+  k0 = fmaf(1024.0f, a0, fmaf(dmin, fm0, dmin * -8388608.0f));       // 1024*a0 + dmin*m0
+  k1 = fmaf(1024.0f, a1, fmaf(dmin, fm1, dmin * -8388608.0f));       // 1024*a1 + dmin*m1
+}
+
+template <int NT>
+__device__ __forceinline__ void q4_block_tn(uint32_t r0, uint32_t r1, const uint32_t (&xa)[NT], uint32_t sxa,
+                                            const Lane& L, int lane, uint32_t magic, uint32_t fmagic,
+                                            float (&y)[NT][4]) {
+  constexpr int MT = 8 * NT;
+  float a0[2], a1[2], k0[2], k1[2];  // [row g / g+8]: the lane's sub-blocks 2t, 2t+1
+  q4_row_decode(lds128(r0), L, fmagic, a0[0], a1[0], k0[0], k1[0]);
+  q4_row_decode(lds128(r1), L, fmagic, a0[1], a1[1], k0[1], k1[1]);
+  const int quad = lane & ~3;
+  const uint32_t o = 16u + 8u * (uint32_t)L.tig;
+#pragma unroll
+  for (int G = 0; G < 4; ++G) {
+    const uint2 wa = lds64(r0 + o + 32u * G), wb = lds64(r1 + o + 32u * G);
+#pragma unroll
+    for (int sb = 0; sb < 2; ++sb) {
+      const int j = 2 * G + sb;
+      float acc[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t w0 = hh ? wa.y : wa.x, w1 = hh ? wb.y : wb.x;
+        const uint32_t s0 = w0 >> 8, s1 = w1 >> 8;
+        uint32_t A0, A1, A2, A3;
+        if (sb == 0) {
+          A0 = lop_and_or<0x000F000Fu>(w0, magic);
+          A1 = lop_and_or<0x000F000Fu>(w1, magic);
+          A2 = lop_and_or<0x000F000Fu>(s0, magic);
+          A3 = lop_and_or<0x000F000Fu>(s1, magic);
+        } else {
+          A0 = lop_and_or<0x00F000F0u>(w0, magic);
+          A1 = lop_and_or<0x00F000F0u>(w1, magic);
+          A2 = lop_and_or<0x00F000F0u>(s0, magic);
+          A3 = lop_and_or<0x00F000F0u>(s1, magic);
+        }
+        const uint32_t koff = 2u * (uint32_t)(64 * G + 32 * sb + 4 * hh) + 16u * (uint32_t)L.tig;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint2 b = lds64(xa[nt] + koff);
+          mma16816(acc[nt], A0, A1, A2, A3, b.x, b.y);
+        }
+      }
+      // the scale and offset of sub-block j for rows g and g+8, from lane t = j / 2 of the quad
+      const int src = quad | (j >> 1);
+      const float sa0 = __shfl_sync(0xffffffffu, (j & 1) ? a1[0] : a0[0], src);
+      const float sa1 = __shfl_sync(0xffffffffu, (j & 1) ? a1[1] : a0[1], src);
+      const float sk0 = __shfl_sync(0xffffffffu, (j & 1) ? k1[0] : k0[0], src);
+      const float sk1 = __shfl_sync(0xffffffffu, (j & 1) ? k1[1] : k0[1], src);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const uint2 sxw = lds64(sxa + 4u * (uint32_t)(j * MT + 8 * nt + 2 * L.tig));
+        const float sx0 = __uint_as_float(sxw.x), sx1 = __uint_as_float(sxw.y);
+        y[nt][0] = fmaf(sa0, acc[nt][0], fmaf(-sk0, sx0, y[nt][0]));
+        y[nt][1] = fmaf(sa0, acc[nt][1], fmaf(-sk0, sx1, y[nt][1]));
+        y[nt][2] = fmaf(sa1, acc[nt][2], fmaf(-sk1, sx0, y[nt][2]));
+        y[nt][3] = fmaf(sa1, acc[nt][3], fmaf(-sk1, sx1, y[nt][3]));
+      }
+    }
+  }
+}
+
+// A 4-byte word at shared address a: 4-byte aligned (A2 = false) or 2 mod 4.
 template <bool A2>
 __device__ __forceinline__ uint32_t lds_word(uint32_t a) {
   if constexpr (!A2) {
@@ -91,206 +406,159 @@ __device__ __forceinline__ uint32_t lds_word(uint32_t a) {
   }
 }
 
-__device__ __forceinline__ float half_lo(uint32_t v) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
-}
-
-// v[i] for a lane-dependent i in 0..3.
-__device__ __forceinline__ float pick4(float v0, float v1, float v2, float v3, int i) {
-  const float a = (i & 1) ? v1 : v0;
-  const float b = (i & 1) ? v3 : v2;
-  return (i & 2) ? b : a;
-}
-
-// ---------------------------------------------------------------------------
-// Q4_K half-block U (sub-blocks 4U .. 4U+3, quant bytes 64U .. 64U+63) of the
-// lane's rows g (block at shared address b0) and g+8 (b1).  In 64-weight group
-// G (sub-blocks 2G, 2G+1, quant bytes 32G .. 32G+31) the lane owns bytes
-// 8*tig .. 8*tig+7, i.e. words hh = 0, 1 at 8*tig + 4*hh.  Word hh feeds one
-// MMA per sub-block:
-//   k-slots 2tig, 2tig+1  <- bytes 0, 2 of the word  (k = 8tig+4hh + 0, 2)
-//   k-slots 2tig+8, +9    <- bytes 1, 3              (k = 8tig+4hh + 1, 3)
-// which is the order of the permuted x pairs xp[k/4] = {(x0,x2), (x1,x3)}.
-// Low nibbles (mask 0x000F000F, F = 1) give sub-block 2G, high nibbles (mask
-// 0x00F000F0, F = 16) sub-block 2G+1.  Lane tig then scales sub-block
-// j = 4U + tig of both rows.
-// ---------------------------------------------------------------------------
-template <int U>
-__device__ __forceinline__ void q4_half(uint32_t b0, uint32_t b1, uint32_t xa, uint32_t sxa, int tig, uint32_t magic,
-                                        float& y0, float& y1) {
-  float D[2][2][4];  // [G - 2U][lo, hi][mma regs]
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const int G = 2 * U + i;
-    const uint2 w0 = lds64(b0 + 16 + 32 * G + 8 * tig);
-    const uint2 w1 = lds64(b1 + 16 + 32 * G + 8 * tig);
-    const uint4 xlo = lds128(xa + 8 * (16 * G + 2 * tig));      // k = 64G + 8tig + 0..7
-    const uint4 xhi = lds128(xa + 8 * (16 * G + 8 + 2 * tig));  // k + 32
-    float c[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      const uint32_t v0 = hh ? w0.y : w0.x, v1 = hh ? w1.y : w1.x;
-      const uint32_t s0 = v0 >> 8, s1 = v1 >> 8;
-      mma16816(c, lop_and_or<0x000F000Fu>(v0, magic), lop_and_or<0x000F000Fu>(v1, magic),
-               lop_and_or<0x000F000Fu>(s0, magic), lop_and_or<0x000F000Fu>(s1, magic), hh ? xlo.z : xlo.x,
-               hh ? xlo.w : xlo.y);
-      mma16816(e, lop_and_or<0x00F000F0u>(v0, magic), lop_and_or<0x00F000F0u>(v1, magic),
-               lop_and_or<0x00F000F0u>(s0, magic), lop_and_or<0x00F000F0u>(s1, magic), hh ? xhi.z : xhi.x,
-               hh ? xhi.w : xhi.y);
-    }
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      D[i][0][r] = c[r];
-      D[i][1][r] = e[r];
-    }
-  }
-  // Sub-block j = 4U + tig: group G = 2U + (tig >> 1), nibble tig & 1.
-  const float d0 = pick4(D[0][0][0], D[0][1][0], D[1][0][0], D[1][1][0], tig);
-  const float d1 = pick4(D[0][0][2], D[0][1][2], D[1][0][2], D[1][1][2], tig);
-  const uint4 h0 = lds128(b0), h1 = lds128(b1);
-  const int sh = 8 * tig;
-  uint32_t sc0, mn0, sc1, mn1;
-  if constexpr (U == 0) {
-    sc0 = (h0.y >> sh) & 63u;
-    mn0 = (h0.z >> sh) & 63u;
-    sc1 = (h1.y >> sh) & 63u;
-    mn1 = (h1.z >> sh) & 63u;
-  } else {
-    const uint32_t l0 = h0.w >> sh, l1 = h1.w >> sh;
-    sc0 = (l0 & 0xFu) | ((h0.y >> (sh + 2)) & 0x30u);
-    mn0 = ((l0 >> 4) & 0xFu) | ((h0.z >> (sh + 2)) & 0x30u);
-    sc1 = (l1 & 0xFu) | ((h1.y >> (sh + 2)) & 0x30u);
-    mn1 = ((l1 >> 4) & 0xFu) | ((h1.z >> (sh + 2)) & 0x30u);
-  }
-  const float inv_f = (tig & 1) ? 0.0625f : 1.0f;
-  const float2 sxp = ldsf2(sxa + 8 * (4 * U + tig));  // 16-wide x sums of sub-block j
-  const float sx = sxp.x + sxp.y;
-  const float dsc0 = half_lo(h0.x) * (float)sc0, dmn0 = half_lo(h0.x >> 16) * (float)mn0;
-  const float dsc1 = half_lo(h1.x) * (float)sc1, dmn1 = half_lo(h1.x >> 16) * (float)mn1;
-  const float a0 = dsc0 * inv_f, a1 = dsc1 * inv_f;
-  y0 = fmaf(a0, d0, fmaf(-fmaf(1024.0f, a0, dmn0), sx, y0));
-  y1 = fmaf(a1, d1, fmaf(-fmaf(1024.0f, a1, dmn1), sx, y1));
-}
-
-// ---------------------------------------------------------------------------
-// Q6_K half H (scale groups 8H .. 8H+7, 128 weights).  Scale group t = 8H + tt
-// (tt = 2*g6 + s, g6 = 0..3) takes its low 4 bits from quant bytes
-// 64H + 32(g6&1) + 16s + l (low nibble if g6 < 2) and its high 2 bits from
-// bits 2*g6 of byte 128 + 32H + 16s + l, l = 0..15.  Lane tig owns
-// l = 4tig .. 4tig+3 (one word of each).  The fp16 operand is 1024 + F*q6
-// with F = 1 (g6 < 2: nibble in bits 0-3, high bits moved to 4-5) or F = 16
-// (g6 >= 2: nibble in bits 4-7, high bits moved to 8-9).  Lane tig scales
-// groups 8H + tig and 8H + 4 + tig of both rows.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void q6k_operands(uint32_t wl, uint32_t wh, int g6, uint32_t magic, uint32_t& r0,
-                                             uint32_t& r2) {
-  const uint32_t wl8 = wl >> 8;
-  const uint32_t up = (g6 & 1) ? (wh << 2) : (wh << 4);
-  const uint32_t dn = (g6 & 1) ? (wh >> 6) : (wh >> 4);
-  if (g6 < 2) {
-    r0 = lop_and_or<0x000F000Fu>(wl, lop_and_or<0x00300030u>(up, magic));
-    r2 = lop_and_or<0x000F000Fu>(wl8, lop_and_or<0x00300030u>(dn, magic));
-  } else {
-    r0 = lop_and_or<0x00F000F0u>(wl, lop_and_or<0x03000300u>(up, magic));
-    r2 = lop_and_or<0x00F000F0u>(wl8, lop_and_or<0x03000300u>(dn, magic));
-  }
-}
-
-// The lane's words of one Q6_K half for rows g (block at b0) and g+8 (b1):
-// loads only, so a caller may pick A2 per lane.
-struct Q6Half {
-  uint32_t ql0[4], ql1[4], qh0[2], qh1[2];
-  uint32_t sc0[2], sc1[2];  // int8 scale words 192 + 8H + 4u (u = 0, 1)
-  uint32_t dw0, dw1;        // the words holding d (low half)
+// The lane's words of one Q6_K row for the multi-token layout: for half h and
+// 16-weight column s, ql words of fields 0/2 (c = 0) and 1/3 (c = 1) and the qh
+// word at l = 16s + 4t; the lane's four scales (groups 4t .. 4t+3) and d.
+struct Q6RowTn {
+  uint32_t x0[2][2], x1[2][2], qh[2][2];  // [h][s]
+  uint32_t sc;                            // int8 scales of groups 4t .. 4t+3
+  uint32_t dw;
 };
 
-template <int H, bool A2>
-__device__ __forceinline__ void q6_load_half(uint32_t b0, uint32_t b1, int tig, Q6Half& q) {
+template <bool A2>
+__device__ __forceinline__ void q6_load_row_tn(uint32_t b, int tig, Q6RowTn& q) {
+  const uint32_t o = 4u * (uint32_t)tig;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {  // i = 2p + s: byte 64H + 32p + 16s + 4tig
-    const uint32_t off = 64 * H + 32 * (i >> 1) + 16 * (i & 1) + 4 * tig;
-    q.ql0[i] = lds_word<A2>(b0 + off);
-    q.ql1[i] = lds_word<A2>(b1 + off);
-  }
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
-  for (int s = 0; s < 2; ++s) {  // byte 128 + 32H + 16s + 4tig
-    const uint32_t off = 128 + 32 * H + 16 * s + 4 * tig;
-    q.qh0[s] = lds_word<A2>(b0 + off);
-    q.qh1[s] = lds_word<A2>(b1 + off);
-  }
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    q.sc0[u] = lds_word<A2>(b0 + 192 + 8 * H + 4 * u);
-    q.sc1[u] = lds_word<A2>(b1 + 192 + 8 * H + 4 * u);
-  }
-  q.dw0 = lds_word<A2>(b0 + 208);
-  q.dw1 = lds_word<A2>(b1 + 208);
+    for (int s = 0; s < 2; ++s) {
+      q.x0[h][s] = lds_word<A2>(b + 64u * h + 16u * s + o);
+      q.x1[h][s] = lds_word<A2>(b + 64u * h + 32u + 16u * s + o);
+      q.qh[h][s] = lds_word<A2>(b + 128u + 32u * h + 16u * s + o);
+    }
+  q.sc = lds_word<A2>(b + 192u + o);
+  q.dw = lds_word<A2>(b + 208u);
 }
 
-template <int H>
-__device__ __forceinline__ void q6_half(const Q6Half& q, uint32_t xa, uint32_t sxa, int tig, uint32_t magic, float& y0,
-                                        float& y1) {
-  float d0[8], d1[8];
+// The lane's four scales as fp32 d*sc/F: groups 4t + i, i = 0..3, share the
+// field parity (t odd: fields 2, 3, F = 16).
+__device__ __forceinline__ void q6_decode_tn(const Q6RowTn& q, int tig, float (&a)[4]) {
+  const float dF = (tig & 1) ? half_lo(q.dw) * 0.0625f : half_lo(q.dw);
 #pragma unroll
-  for (int tt = 0; tt < 8; ++tt) {
-    const int g6 = (tt >> 1) & 3, s = tt & 1;
-    const int li = 2 * (g6 & 1) + s;
-    uint32_t a0, a2, a1, a3;
-    q6k_operands(q.ql0[li], q.qh0[s], g6, magic, a0, a2);
-    q6k_operands(q.ql1[li], q.qh1[s], g6, magic, a1, a3);
-    const uint2 bx = lds64(xa + 8 * (4 * (8 * H + tt) + tig));
-    float c[4] = {0.f, 0.f, 0.f, 0.f};
-    mma16816(c, a0, a1, a2, a3, bx.x, bx.y);
-    d0[tt] = c[0];
-    d1[tt] = c[2];
+  for (int i = 0; i < 4; ++i) a[i] = dF * (float)(int8_t)((q.sc >> (8 * i)) & 0xFFu);
+}
+
+template <int NT>
+__device__ __forceinline__ void q6_block_tn(uint32_t r0, uint32_t r1, const uint32_t (&xa)[NT], uint32_t sxa,
+                                            const Lane& L, int lane, uint32_t magic, float (&y)[NT][4]) {
+  constexpr int MT = 8 * NT;
+  Q6RowTn q, r;
+  if ((r0 & 3u) == 0) {
+    q6_load_row_tn<false>(r0, L.tig, q);
+    q6_load_row_tn<false>(r1, L.tig, r);
+  } else {
+    q6_load_row_tn<true>(r0, L.tig, q);
+    q6_load_row_tn<true>(r1, L.tig, r);
   }
-  // Scale groups 8H + tig (u = 0, F = 1) and 8H + 4 + tig (u = 1, F = 16).
-  const float dA = half_lo(q.dw0), dB = half_lo(q.dw1);
-  const int sh = 8 * tig;
+  __syncwarp();
+  float aq[4], ar[4];
+  q6_decode_tn(q, L.tig, aq);
+  q6_decode_tn(r, L.tig, ar);
+  const int quad = lane & ~3;
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const float inv_f = u ? 0.0625f : 1.0f;
-    const float dsc0 = dA * (float)(int8_t)((q.sc0[u] >> sh) & 0xFFu);
-    const float dsc1 = dB * (float)(int8_t)((q.sc1[u] >> sh) & 0xFFu);
-    const float v0 = pick4(d0[4 * u], d0[4 * u + 1], d0[4 * u + 2], d0[4 * u + 3], tig);
-    const float v1 = pick4(d1[4 * u], d1[4 * u + 1], d1[4 * u + 2], d1[4 * u + 3], tig);
-    const float sx = ldsf(sxa + 4 * (8 * H + 4 * u + tig));
-    const float a0 = dsc0 * inv_f, a1 = dsc1 * inv_f;
-    y0 = fmaf(a0, v0, fmaf(-fmaf(1024.0f, a0, 32.0f * dsc0), sx, y0));
-    y1 = fmaf(a1, v1, fmaf(-fmaf(1024.0f, a1, 32.0f * dsc1), sx, y1));
+  for (int h = 0; h < 2; ++h) {
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int grp = 8 * h + 2 * j + s;
+        const uint32_t X = (j & 1) ? q.x1[h][s] : q.x0[h][s], Y = (j & 1) ? r.x1[h][s] : r.x0[h][s];
+        const uint32_t H = q.qh[h][s], G = r.qh[h][s];
+        const uint32_t X8 = X >> 8, Y8 = Y >> 8, H8 = H >> 8, G8 = G >> 8;
+        uint32_t A0, A1, A2, A3;
+        if (j == 0) {
+          A0 = q6op<0x000F000Fu, 0x00300030u>(X, H << 4, magic);
+          A1 = q6op<0x000F000Fu, 0x00300030u>(Y, G << 4, magic);
+          A2 = q6op<0x000F000Fu, 0x00300030u>(X8, H8 << 4, magic);
+          A3 = q6op<0x000F000Fu, 0x00300030u>(Y8, G8 << 4, magic);
+        } else if (j == 1) {
+          A0 = q6op<0x000F000Fu, 0x00300030u>(X, H << 2, magic);
+          A1 = q6op<0x000F000Fu, 0x00300030u>(Y, G << 2, magic);
+          A2 = q6op<0x000F000Fu, 0x00300030u>(X8, H8 << 2, magic);
+          A3 = q6op<0x000F000Fu, 0x00300030u>(Y8, G8 << 2, magic);
+        } else if (j == 2) {
+          A0 = q6op<0x00F000F0u, 0x03000300u>(X, H << 4, magic);
+          A1 = q6op<0x00F000F0u, 0x03000300u>(Y, G << 4, magic);
+          A2 = q6op<0x00F000F0u, 0x03000300u>(X8, H8 << 4, magic);
+          A3 = q6op<0x00F000F0u, 0x03000300u>(Y8, G8 << 4, magic);
+        } else {
+          A0 = q6op<0x00F000F0u, 0x03000300u>(X, H << 2, magic);
+          A1 = q6op<0x00F000F0u, 0x03000300u>(Y, G << 2, magic);
+          A2 = q6op<0x00F000F0u, 0x03000300u>(X8, H8 << 2, magic);
+          A3 = q6op<0x00F000F0u, 0x03000300u>(Y8, G8 << 2, magic);
+        }
+        const uint32_t koff = 2u * (uint32_t)(128 * h + 32 * j + 16 * s) + 8u * (uint32_t)L.tig;
+        float acc[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
+          const uint2 b = lds64(xa[nt] + koff);
+          mma16816(acc[nt], A0, A1, A2, A3, b.x, b.y);
+        }
+        // the scale of group grp (rows g, g+8) from lane t = grp / 4 of the quad
+        const int src = quad | (grp >> 2);
+        const float sa0 = __shfl_sync(0xffffffffu, aq[grp & 3], src);
+        const float sa1 = __shfl_sync(0xffffffffu, ar[grp & 3], src);
+        const float kf = j >= 2 ? 1024.0f + 32.0f * 16.0f : 1024.0f + 32.0f;
+        const float sk0 = sa0 * kf, sk1 = sa1 * kf;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint2 sxw = lds64(sxa + 4u * (uint32_t)(grp * MT + 8 * nt + 2 * L.tig));
+          const float sx0 = __uint_as_float(sxw.x), sx1 = __uint_as_float(sxw.y);
+          y[nt][0] = fmaf(sa0, acc[nt][0], fmaf(-sk0, sx0, y[nt][0]));
+          y[nt][1] = fmaf(sa0, acc[nt][1], fmaf(-sk0, sx1, y[nt][1]));
+          y[nt][2] = fmaf(sa1, acc[nt][2], fmaf(-sk1, sx0, y[nt][2]));
+          y[nt][3] = fmaf(sa1, acc[nt][3], fmaf(-sk1, sx1, y[nt][3]));
+        }
+      }
+    }
   }
 }
 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-// Compute warps per CTA (measured on GB300: 12 beat 8 and 16 on the decode
-// layer; a K = 3072 tile is 12 blocks, one per warp).
 #ifndef QK_GEMV_WARPS
 #define QK_GEMV_WARPS 12
 #endif
-constexpr int kComputeWarps = QK_GEMV_WARPS;
-// Sleep between polls of the producer's and the reducer's waits, in ns (0:
-// poll back to back).  Those two warps share schedulers with compute warps;
-// their waits are hidden by the ring and by the double-buffered partials.
+constexpr int kW = QK_GEMV_WARPS;  // compute warps per CTA
+// Sleep between polls of the producer's waits, in ns (0: poll back to back).
 #ifndef QK_GEMV_BACKOFF_NS
 #define QK_GEMV_BACKOFF_NS 0
 #endif
 constexpr uint32_t kBackoffNs = QK_GEMV_BACKOFF_NS;
-constexpr int kProducerWarp = kComputeWarps;      // streams the weights (and x)
-constexpr int kReducerWarp = kComputeWarps + 1;       // sums the compute warps' partials per tile
-constexpr int kThreads = 32 * (kComputeWarps + 2);
+// 1: the producer waits for a CTA's first stage to land before queueing the
+// others; 0: it queues every stage at once.
+#ifndef QK_GEMV_FIRST_WAIT
+#define QK_GEMV_FIRST_WAIT 1
+#endif
+constexpr bool kFirstWait = QK_GEMV_FIRST_WAIT != 0;
+constexpr int kProducerWarp = kW;
+constexpr int kThreads = 32 * (kW + 1);
 constexpr int kMaxStages = 8;
+constexpr uint32_t kXtBlock = 1024;  // x-table bytes per 256-weight block
+constexpr uint32_t kZeroBytes = 1024;
+
+constexpr uint32_t round128(size_t v) { return (uint32_t)((v + 127) / 128 * 128); }
+// Sums table bytes per block: Q4_K [t][Sx, -1024 Sx, Sx', -1024 Sx'], Q6_K [h][t][4 fields].
+constexpr uint32_t sx_block_bytes(int qtype) { return qtype == kQ4K ? 64u : 128u; }
+constexpr uint32_t red_slot_bytes() { return (uint32_t)(kW * 2 * 16 * sizeof(float)); }
 
 struct GemvProb {
   const uint8_t* w[2];  // weights (gate for kind 1), up weights (kind 1)
   const uint16_t* x;
   void* y;
+  int M;                // tokens (1 for the decode layout)
+  const uint16_t* gamma;  // RMSNorm prologue: fp16 gamma[K], or null for none
+  float eps;
   int N, K, qtype, kind;
-  int pair;         // one tensor, whole rows: a stage holds two adjacent 16-row tiles (as two "tensors")
-  int cb;           // K blocks per chunk (a stage holds 16 rows x cb blocks per weight tensor)
-  int stages;       // pipeline depth of this problem's CTAs
+  int pair;             // one tensor, whole rows: a stage holds two adjacent 16-row tiles (as two "tensors")
+  int cb;               // K blocks per chunk (a stage holds 16 rows x cb blocks per weight tensor)
+  int stages;           // pipeline depth of this problem's CTAs
   uint32_t stage_bytes;
+  uint32_t ctl_off, red_off, ring_off;  // shared-memory layout of this problem's CTAs
+  uint32_t red_bytes;                   // several tokens: bytes of one partials buffer (of two)
   int tiles, cta_begin, ctas;
 };
 
@@ -299,31 +567,315 @@ struct GemvBatch {
   int count;
 };
 
-struct GemvShared;
-constexpr uint32_t round128(size_t v) { return (uint32_t)((v + 127) / 128 * 128); }
-
-struct GemvShared {
+struct Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  uint64_t x_full;                     // x copied into shared memory
-  uint64_t red_full[2];                // every compute warp wrote its partials of a tile (by parity)
-  uint64_t red_free[2];                // the reducer has consumed them
-  float red[2][kComputeWarps][2][16];  // [tile parity][warp][tensor][row]
+  uint64_t red_free[2];       // several tokens: the partials buffer of tile parity p has been summed
+  uint32_t done[kMaxStages];  // warps that finished the tile whose last chunk used this stage (or parity)
   uint32_t abort_flag;
+  float rnorm[kMaxGemvM];     // RMSNorm prologue: 1 / sqrt(mean(x^2) + eps) per token
+  float rss[kMaxGemvM][kW];   // its per-warp sums of squares
 };
-constexpr uint32_t kSharedBytes = round128(sizeof(GemvShared));
+constexpr uint32_t kCtlBytes = round128(sizeof(Ctl));
 
+// RMSNorm prologue (DAMASCUS project overview, "[04] one decode step": an
+// RMSNorm comes before the QKV projections and the SwiGLU FFN).  Every
+// compute thread sums the squares of its 8-value chunks c = tid, tid + 32kW,
+// ... of every token (loads of all tokens issued together), the warps reduce
+// them in a fixed shuffle tree into rss[m][warp], and after a barrier thread m
+// adds the warps in order: rnorm[m] = 1 / sqrt(mean_k x[m][k]^2 + eps), fp32.
+__device__ void rms_partials(const uint16_t* __restrict__ x, int M, int K, float (*rss)[kW], int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int nc = K / 8;
+  float ss[kMaxGemvM];
+#pragma unroll
+  for (int m = 0; m < kMaxGemvM; ++m) ss[m] = 0.f;
+  for (int c = tid; c < nc; c += 32 * kW) {
+    uint4 v[kMaxGemvM];
+#pragma unroll
+    for (int m = 0; m < kMaxGemvM; ++m)
+      if (m < M) v[m] = ldg_stream16(x + (size_t)m * K + 8 * c);
+#pragma unroll
+    for (int m = 0; m < kMaxGemvM; ++m) {
+      if (m < M) {
+        const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = half_lo(w[i]), b = half_lo(w[i] >> 16);
+          ss[m] = fmaf(b, b, fmaf(a, a, ss[m]));
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int m = 0; m < kMaxGemvM; ++m) {
+    if (m < M) {
+      float t = ss[m];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if (lane == 0) rss[m][warp] = t;
+    }
+  }
+}
 
+// Four fp16 values of x (two words) times r * gamma, rounded to fp16.
+__device__ __forceinline__ uint2 norm4(uint2 v, uint2 g, float r) {
+  uint2 o;
+  const __half2 a = __floats2half2_rn(half_lo(v.x) * r * half_lo(g.x), half_lo(v.x >> 16) * r * half_lo(g.x >> 16));
+  const __half2 b = __floats2half2_rn(half_lo(v.y) * r * half_lo(g.y), half_lo(v.y >> 16) * r * half_lo(g.y >> 16));
+  o.x = *reinterpret_cast<const uint32_t*>(&a);
+  o.y = *reinterpret_cast<const uint32_t*>(&b);
+  return o;
+}
+
+// Build the x table and the sums table of one problem from x in device memory
+// (all compute threads; the caller synchronises them afterwards).
+//   Q4_K entry (block, word v, lane group t, e): base k = 64t + 32e + 4v.
+//   Q6_K entry (block, v = 4h + 2P + u, t, e):   base k = 128h + 64P + 32e + 8t + 4u.
+// An entry holds x[k], x[k+2] / x[k+1], x[k+3] as fp16 pairs: for e = 0 in
+// words 0 and 2 (B half 0 of the MMAs p = 0, 1), for e = 1 in words 1 and 3.
 template <int QT>
-__device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, const GemvBatch& B, uint8_t* smem,
-                                                 uint8_t* stages, GemvShared* sh) {
+__device__ void build_x_table(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, const float* rnorm,
+                              int K, uint32_t xt, uint32_t sx, uint32_t zero, int tid) {
+  const int nb = K / kQK;
+  const int nent = nb * 64;  // entries, each from 4 consecutive x values
+  for (int i = tid; i < nent; i += 32 * kW) {
+    int blk, t, e, v, k;
+    uint32_t dst;
+    if constexpr (QT == kQ4K) {
+      // i = ((blk * 4 + t) * 2 + e) * 8 + v: the 8 entries of one sub-block are adjacent lanes
+      v = i & 7;
+      e = (i >> 3) & 1;
+      t = (i >> 4) & 3;
+      blk = i >> 6;
+      k = 64 * t + 32 * e + 4 * v;
+      dst = xt + (uint32_t)blk * kXtBlock + 128u * v + 32u * t + 16u * e;
+    } else {
+      // i = ((((blk * 2 + h) * 2 + P) * 4 + t) * 2 + e) * 2 + u: the two entries of a field sum are adjacent
+      const int u = i & 1;
+      e = (i >> 1) & 1;
+      t = (i >> 2) & 3;
+      const int P = (i >> 4) & 1, h = (i >> 5) & 1;
+      blk = i >> 6;
+      v = 4 * h + 2 * P + u;
+      k = 128 * h + 64 * P + 32 * e + 8 * t + 4 * u;
+      dst = xt + (uint32_t)blk * kXtBlock + 128u * v + 32u * t + 16u * e;
+    }
+    uint2 q = ldg_stream8(x + (size_t)blk * kQK + k);
+    if (gamma) q = norm4(q, ldg_stream8(gamma + (size_t)blk * kQK + k), rnorm[0]);
+    const uint32_t p0 = prmt(q.x, q.y, 0x5410u), p1 = prmt(q.x, q.y, 0x7632u);  // (x0, x2), (x1, x3)
+    if (e == 0)
+      sts128_u(dst, p0, 0u, p1, 0u);
+    else
+      sts128_u(dst, 0u, p0, 0u, p1);
+    float s = (half_lo(q.x) + half_lo(q.x >> 16)) + (half_lo(q.y) + half_lo(q.y >> 16));
+    if constexpr (QT == kQ4K) {
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      s += __shfl_xor_sync(0xffffffffu, s, 4);
+      if (v == 0) {
+        const uint32_t a = sx + (uint32_t)blk * 64u + 16u * t + 8u * e;
+        asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(a), "f"(s), "f"(-1024.0f * s) : "memory");
+      }
+    } else {
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      if ((i & 1) == 0) {
+        const int P = (i >> 4) & 1, h = (i >> 5) & 1;
+        const float c = P ? -(1024.0f + 32.0f * 16.0f) : -(1024.0f + 32.0f);
+        const uint32_t a = sx + (uint32_t)blk * 128u + 64u * h + 16u * t + 4u * (2 * P + e);
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(c * s) : "memory");
+      }
+    }
+  }
+  for (int i = tid; i < (int)(kZeroBytes / 16); i += 32 * kW) sts128_u(zero + 16u * i, 0u, 0u, 0u, 0u);
+}
+
+// Several tokens: token m's x as k-permuted fp16 pairs, xp_m[k/4] = { (x[k],
+// x[k+2]), (x[k+1], x[k+3]) } (2K bytes per token), and the sums table
+// [block][sub-block (Q4_K, 32 weights) or scale group (Q6_K, 16)][MT tokens]
+// (zero for tokens beyond M).
+template <int QT, int MT>
+__device__ void build_x_table_tn(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
+                                 const float* rnorm, int M, int K, uint32_t xt, uint32_t sx, uint32_t zero, int tid) {
+  constexpr int kSub = QT == kQ4K ? 8 : 16;      // sums per block
+  constexpr int kPer = QT == kQ4K ? 8 : 4;       // 4-value groups per sum
+  const int nq = K / 4;
+  for (int i = tid; i < M * nq; i += 32 * kW) {  // nq is a multiple of 64: a warp never straddles tokens
+    const int m = i / nq, q = i - m * nq;
+    uint2 v = ldg_stream8(x + (size_t)m * K + 4 * q);
+    if (gamma) v = norm4(v, ldg_stream8(gamma + 4 * q), rnorm[m]);
+    const uint32_t a = xt + (uint32_t)m * (uint32_t)(2 * K) + 8u * q;  // 8-byte entries
+    asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(prmt(v.x, v.y, 0x5410u)),
+                 "r"(prmt(v.x, v.y, 0x7632u))
+                 : "memory");
+    float s = (half_lo(v.x) + half_lo(v.x >> 16)) + (half_lo(v.y) + half_lo(v.y >> 16));
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    if (kPer == 8) s += __shfl_xor_sync(0xffffffffu, s, 4);
+    if ((q & (kPer - 1)) == 0) {
+      const int sub = q / kPer;  // global sub-block / group index: block sub / kSub, slot sub % kSub
+      asm volatile("st.shared.f32 [%0], %1;" ::"r"(sx + 4u * (uint32_t)(sub * MT + m)), "f"(s) : "memory");
+    }
+  }
+  const int nsums = (K / kQK) * kSub;
+  for (int i = tid; i < nsums * (MT - M); i += 32 * kW) {
+    const int sub = i / (MT - M), m = M + i % (MT - M);
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(sx + 4u * (uint32_t)(sub * MT + m)), "f"(0.0f) : "memory");
+  }
+  for (int i = tid; i < (int)(kZeroBytes / 16); i += 32 * kW) sts128_u(zero + 16u * i, 0u, 0u, 0u, 0u);
+}
+
+constexpr uint32_t red_tn_bytes(int mt, int nten) { return (uint32_t)(kW * nten * 16 * mt * sizeof(float)); }
+
+// The compute warps of the several-token layout: round-robin units as in the
+// decode layout, partials of every (row, token) handed over per tile through
+// two buffers (tile parity), the last warp of a tile adding them in warp order.
+template <int QT, int MT>
+__device__ __forceinline__ void compute_tn(const GemvProb& P, uint8_t* smem, int t0, int t1, int steps, int nchunks,
+                                           int nten, int tile_rows, uint32_t ten_bytes, int64_t RB) {
+  constexpr int NT = MT / 8;
+  constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
+  constexpr int kSub = QT == kQ4K ? 8 : 16;
+  const int K = P.K, N = P.N, M = P.M, nb = K / kQK, cb = P.cb, kind = P.kind, S = P.stages;
+  const uint32_t SB = P.stage_bytes;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  void* const yout = P.y;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + P.ctl_off);
+  volatile uint32_t* abort_flag = &ctl->abort_flag;
+  Lane L;
+  L.g = lane >> 2;
+  L.tig = lane & 3;
+  L.hi = L.tig >= 2;
+  L.sh = 16u * (uint32_t)(L.tig & 1);
+  L.shA = L.sh + (L.hi ? 2u : 0u);
+  L.shL = L.sh + (L.hi ? 4u : 0u);
+  const uint32_t base = smem_u32(smem);
+  const uint32_t zero = base + P.ctl_off - kZeroBytes;
+  uint32_t xbase[NT], xstride[NT];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int tok = 8 * nt + L.g;
+    xbase[nt] = tok < M ? base + (uint32_t)tok * (uint32_t)(2 * K) : zero;
+    xstride[nt] = tok < M ? 2u * kQK : 0u;
+  }
+  const uint32_t sx_base = base + (uint32_t)MT * (uint32_t)(2 * K);
+  const uint32_t ring_s = base + P.ring_off;
+  uint32_t magic, fmagic;
+  asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
+  asm volatile("mov.b32 %0, %1;" : "=r"(fmagic) : "n"(kFMagic));
+  const uint32_t pitch = (cb == nb) ? (uint32_t)RB : (uint32_t)(cb * kBB);
+  const int upt = nten * nb, ups = nten * cb;
+  float ya[NT][4], yb[NT][4];  // rows g, g+8 x tokens 8nt + 2t, +1 of tensor 0 (a) and 1 (b)
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ya[nt][i] = yb[nt][i] = 0.f;
+  bool ok = true;
+  for (int st = 0; st < steps; ++st) {
+    const int s = st % S;
+    const int tl = st / nchunks, chunk = st % nchunks;
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, abort_flag, &g_gemv_status));
+    const uint32_t stg = ring_s + (uint32_t)s * SB + (uint32_t)L.g * pitch;
+    const int U0 = (int)(((int64_t)(t0 + tl) * upt + (int64_t)chunk * ups) % kW);
+    int v = (warp - U0 + kW) % kW;
+    for (; ok && v < ups; v += kW) {
+      const int t = v >= cb ? 1 : 0, b = v - t * cb;
+      const uint32_t r0 = stg + (uint32_t)t * ten_bytes + (uint32_t)(b * kBB);
+      const uint32_t r1 = r0 + 8u * pitch;
+      const int blk = chunk * cb + b;
+      uint32_t xa[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) xa[nt] = xbase[nt] + (uint32_t)blk * xstride[nt];
+      const uint32_t sxa = sx_base + (uint32_t)blk * (uint32_t)(kSub * MT * 4);
+      if (t == 0) {
+        if constexpr (QT == kQ4K)
+          q4_block_tn<NT>(r0, r1, xa, sxa, L, lane, magic, fmagic, ya);
+        else
+          q6_block_tn<NT>(r0, r1, xa, sxa, L, lane, magic, ya);
+      } else {
+        if constexpr (QT == kQ4K)
+          q4_block_tn<NT>(r0, r1, xa, sxa, L, lane, magic, fmagic, yb);
+        else
+          q6_block_tn<NT>(r0, r1, xa, sxa, L, lane, magic, yb);
+      }
+    }
+    __syncwarp();
+    if (chunk == nchunks - 1) {
+      const int par = tl & 1;
+      // The buffer of this parity was last used by tile tl - 2: wait until its
+      // partials have been summed.
+      if (tl >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->red_free[par], (uint32_t)((tl >> 1) - 1) & 1u, abort_flag,
+                                               &g_gemv_status)) && ok;
+      float* red = reinterpret_cast<float*>(smem + P.red_off + (size_t)par * P.red_bytes);
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        if (t < nten) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int row = L.g + 8 * (i >> 1), tok = 8 * nt + 2 * L.tig + (i & 1);
+              red[((warp * nten + t) * 16 + row) * MT + tok] = t ? yb[nt][i] : ya[nt][i];
+            }
+        }
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) ya[nt][i] = yb[nt][i] = 0.f;
+      __threadfence_block();
+      __syncwarp();
+      uint32_t prev = 0;
+      if (lane == 0) {
+        prev = atomicAdd(&ctl->done[par], 1u);
+        __threadfence_block();
+      }
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      __syncwarp();
+      if (prev == (uint32_t)(kW - 1)) {
+        const int tile = t0 + tl;
+        if (kind == 1) {
+          for (int idx = lane; idx < 16 * M; idx += 32) {
+            const int row = idx & 15, tok = idx >> 4;
+            const int n = tile * 16 + row;
+            float gs = 0.f, us = 0.f;
+            for (int w = 0; w < kW; ++w) gs += red[((w * 2 + 0) * 16 + row) * MT + tok];  // kind 1: nten = 2
+            for (int w = 0; w < kW; ++w) us += red[((w * 2 + 1) * 16 + row) * MT + tok];
+            if (n < N) static_cast<__half*>(yout)[(size_t)tok * N + n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
+          }
+        } else {
+          for (int idx = lane; idx < nten * 16 * M; idx += 32) {
+            const int t = idx / (16 * M), rem = idx - t * 16 * M;
+            const int row = rem & 15, tok = rem >> 4;
+            const int n = tile * tile_rows + 16 * t + row;
+            float gs = 0.f;
+            for (int w = 0; w < kW; ++w) gs += red[((w * nten + t) * 16 + row) * MT + tok];
+            if (n < N) static_cast<float*>(yout)[(size_t)tok * N + n] = gs;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) {
+          ctl->done[par] = 0u;
+          mbar_arrive(&ctl->red_free[par]);
+        }
+      }
+      __syncwarp();
+    }
+    if (lane == 0) mbar_arrive(&ctl->empty[s]);
+  }
+}
+
+template <int QT, int MT>
+__device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uint8_t* smem) {
   const int K = P.K, N = P.N, nb = K / kQK, cb = P.cb;
   constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
   const int64_t RB = (int64_t)nb * kBB;
+  const int kind = P.kind, pair = P.pair;
   // Tiles of a stage: gate and up (kind 1), two adjacent 16-row tiles of one
   // tensor (pair), or one tile.  "tile" below is a stage's worth of rows.
-  const int nten = (P.kind == 1 || P.pair) ? 2 : 1;
-  const int tile_rows = P.pair ? 32 : 16;
+  const int nten = (kind == 1 || pair) ? 2 : 1;
+  const int tile_rows = pair ? 32 : 16;
   const int nchunks = nb / cb;  // the host makes cb divide nb
   const int t0 = (int)((int64_t)cta * P.tiles / P.ctas), t1 = (int)((int64_t)(cta + 1) * P.tiles / P.ctas);
   const int steps = (t1 - t0) * nchunks;
@@ -331,7 +883,12 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
   const uint32_t SB = P.stage_bytes;
   const uint32_t ten_bytes = (uint32_t)(16 * cb * kBB);  // one tensor's share of a stage
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  volatile uint32_t* abort_flag = &sh->abort_flag;
+  const uint8_t* const w0 = P.w[0];
+  const uint8_t* const w1 = P.w[1];
+  void* const yout = P.y;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + P.ctl_off);
+  volatile uint32_t* abort_flag = &ctl->abort_flag;
+  uint8_t* ring = smem + P.ring_off;
 
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
@@ -339,7 +896,7 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
       int st = 0;
       for (; st < steps; ++st) {
         const int s = st % S;
-        if (!mbar_wait<kBackoffNs>(&sh->empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemv_status))
+        if (!mbar_wait<kBackoffNs>(&ctl->empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemv_status))
           break;
         // The compute warps read the stage with plain loads; the refill is an
         // async-proxy write.  The proxy fence after the barrier their releases
@@ -347,168 +904,179 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, con
         fence_proxy_async_smem();
         const int tile = t0 + st / nchunks, chunk = st % nchunks;
         const int n0 = tile * tile_rows, rows = min(16, N - n0);
-        uint8_t* dst = stages + (size_t)s * SB;
+        uint8_t* dst = ring + (size_t)s * SB;
         if (cb == nb) {
           // Whole 16-row tiles: rows nt .. nt+rows_t-1 of a tensor are one
           // contiguous span (pair: tile t starts 16 rows further).
           uint32_t total = 0;
           for (int t = 0; t < nten; ++t) {
-            const int rows_t = min(16, N - (n0 + (P.pair ? 16 * t : 0)));
+            const int rows_t = min(16, N - (n0 + (pair ? 16 * t : 0)));
             if (rows_t > 0) total += (uint32_t)(((int64_t)rows_t * RB) & ~int64_t(15));
           }
-          mbar_expect_tx(&sh->full[s], total);
+          mbar_expect_tx(&ctl->full[s], total);
           for (int t = 0; t < nten; ++t) {
-            const int nt = n0 + (P.pair ? 16 * t : 0), rows_t = min(16, N - nt);
+            const int nt = n0 + (pair ? 16 * t : 0), rows_t = min(16, N - nt);
             if (rows_t <= 0) continue;
             const int64_t span = (int64_t)rows_t * RB;
             const uint32_t bulk = (uint32_t)(span & ~int64_t(15));
-            const uint8_t* src = P.w[P.pair ? 0 : t] + (int64_t)nt * RB;
+            const uint8_t* src = (pair || t == 0 ? w0 : w1) + (int64_t)nt * RB;
             uint8_t* d = dst + t * ten_bytes;
-            if (bulk) bulk_copy_g2s(d, src, bulk, &sh->full[s]);
+            if (bulk) bulk_copy_g2s(d, src, bulk, &ctl->full[s]);
             for (int64_t b = bulk; b < span; b += 2)  // last bytes of the tensor (span % 16 != 0)
               *reinterpret_cast<uint16_t*>(d + b) = *reinterpret_cast<const uint16_t*>(src + b);
           }
         } else {
           // A K chunk: one copy per row of cb blocks (16-byte aligned by construction).
           const uint32_t row_bytes = (uint32_t)(cb * kBB);
-          mbar_expect_tx(&sh->full[s], row_bytes * (uint32_t)(rows * nten));
+          mbar_expect_tx(&ctl->full[s], row_bytes * (uint32_t)(rows * nten));
           for (int t = 0; t < nten; ++t)
             for (int r = 0; r < rows; ++r)
               bulk_copy_g2s(dst + t * ten_bytes + r * row_bytes,
-                            P.w[t] + (int64_t)(n0 + r) * RB + (int64_t)chunk * cb * kBB, row_bytes, &sh->full[s]);
+                            (t ? w1 : w0) + (int64_t)(n0 + r) * RB + (int64_t)chunk * cb * kBB, row_bytes,
+                            &ctl->full[s]);
         }
-        mbar_arrive(&sh->full[s]);
+        mbar_arrive(&ctl->full[s]);
         // Let the first stage of every CTA land before queueing the rest, so
         // the compute warps start while the other stages stream in.
-        if (st == 0 && steps > 1 && !mbar_wait(&sh->full[0], 0u, abort_flag, &g_gemv_status)) {
+        if (kFirstWait && st == 0 && steps > 1 && !mbar_wait(&ctl->full[0], 0u, abort_flag, &g_gemv_status)) {
           ++st;
           break;
         }
       }
       // Drain: the copies issued last have landed before the CTA can exit.
       for (int i = 1; i <= S && i <= st; ++i)
-        mbar_wait(&sh->full[(st - i) % S], (uint32_t)((st - i) / S) & 1u, abort_flag, &g_gemv_status, true);
-    }
-    return;
-  }
-
-  if (warp == kReducerWarp) {
-    // ------------------------------------------------------------ reducer
-    // Tile i's partials sit in red[i & 1]; sum them over the compute warps in
-    // a fixed order (deterministic) and write y.
-    const int ntiles = t1 - t0;
-    for (int i = 0; i < ntiles; ++i) {
-      const int par = i & 1;
-      if (!mbar_wait<kBackoffNs>(&sh->red_full[par], (uint32_t)(i >> 1) & 1u, abort_flag, &g_gemv_status)) break;
-      if (P.kind == 1) {
-        if (lane < 16) {
-          const int n = (t0 + i) * 16 + lane;
-          float gs = 0.f, us = 0.f;
-          for (int w = 0; w < kComputeWarps; ++w) gs += sh->red[par][w][0][lane];
-          for (int w = 0; w < kComputeWarps; ++w) us += sh->red[par][w][1][lane];
-          if (n < N) static_cast<__half*>(P.y)[n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
-        }
-      } else if (lane < 16 * nten) {  // lane 16t + r: row r of tile t of the stage
-        const int t = lane >> 4, r = lane & 15;
-        const int n = (t0 + i) * tile_rows + 16 * t + r;
-        float gs = 0.f;
-        for (int w = 0; w < kComputeWarps; ++w) gs += sh->red[par][w][t][r];
-        if (n < N) static_cast<float*>(P.y)[n] = gs;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->red_free[par]);
+        mbar_wait(&ctl->full[(st - i) % S], (uint32_t)((st - i) / S) & 1u, abort_flag, &g_gemv_status, true);
     }
     return;
   }
 
   // -------------------------------------------------------------- compute
-  const uint32_t xs = smem_u32(smem);             // permuted x pairs, 8 bytes per 4 k
-  const uint32_t sxs = smem_u32(smem + 2 * K);    // 16-wide sums of x
-  const uint32_t ring = smem_u32(stages);
-  const int g = lane >> 2, tig = lane & 3;
-  // fp16x2 (1024, 1024), kept in a register for the LOP3s that build the MMA operands
-  uint32_t magic;
+  if constexpr (MT > 1) {
+    compute_tn<QT, MT>(P, smem, t0, t1, steps, nchunks, nten, tile_rows, ten_bytes, RB);
+    return;
+  }
+  Lane L;
+  L.g = lane >> 2;
+  L.tig = lane & 3;
+  {
+    const int e = L.g & 1;
+    const bool reads_x = (L.g >> 1) == L.tig;  // column g takes x from lane group t = g >> 1 only
+    // Zero-region offset: a 16-byte chunk of the 128-byte line other than the
+    // two the x-reading lanes of this lane's quarter-warp use (no bank conflict).
+    L.xt_off = reads_x ? 32u * (uint32_t)L.tig + 16u * (uint32_t)e : 32u * (uint32_t)(((L.g >> 1) + 2) & 3);
+    L.xt_stride = reads_x ? kXtBlock : 0u;
+  }
+  L.hi = L.tig >= 2;
+  L.sh = 16u * (uint32_t)(L.tig & 1);
+  L.shA = L.sh + (L.hi ? 2u : 0u);
+  L.shL = L.sh + (L.hi ? 4u : 0u);
+  {
+    const uint32_t s = (uint32_t)(L.tig >> 1);
+    L.sel0 = 0x7440u | s;        // byte s: the scale of field 2P
+    L.sel1 = 0x7440u | (s + 2);  // byte s + 2: the scale of field 2P + 1
+  }
+  const uint32_t base = smem_u32(smem);
+  const bool reads_x = L.xt_stride != 0;
+  const uint32_t xt_lane = (reads_x ? base : base + P.ctl_off - kZeroBytes) + L.xt_off;
+  const uint32_t sx_base = base + (uint32_t)nb * kXtBlock + 16u * (uint32_t)L.tig;
+  const uint32_t ring_s = base + P.ring_off;
+  uint32_t magic, fmagic;
   asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
+  asm volatile("mov.b32 %0, %1;" : "=r"(fmagic) : "n"(kFMagic));
   const uint32_t pitch = (cb == nb) ? (uint32_t)RB : (uint32_t)(cb * kBB);  // bytes per row inside a stage
+  const int upt = nten * nb;        // units (one tensor's 16 rows x one block) per tile
+  const int ups = nten * cb;        // units per stage
   float ya0 = 0.f, ya1 = 0.f, yb0 = 0.f, yb1 = 0.f;  // rows g, g+8 of tensor 0 (a) and 1 (b)
   bool ok = true;
   for (int st = 0; st < steps; ++st) {
     const int s = st % S;
-    const int chunk = st % nchunks;
-    // After a timed-out wait the warp skips the arithmetic but still hands its
-    // partials of every tile to the reducer, so the reducer is not left waiting.
-    if (ok)
-      ok = __all_sync(0xffffffffu, mbar_wait(&sh->full[s], (uint32_t)(st / S) & 1u, abort_flag, &g_gemv_status));
-    const uint32_t stg = ring + (uint32_t)s * SB + (uint32_t)g * pitch;
-    // Warp w takes whole blocks v = w, w + kComputeWarps, ...: v = t*cb + b; both
-    // halves of a block are independent straight-line work (more ILP per warp).
-    int t = 0, b = warp;
-    while (b >= cb) {
-      b -= cb;
-      ++t;
-    }
-    for (int v = warp; ok && v < nten * cb; v += kComputeWarps) {
-      const uint32_t b0 = stg + (uint32_t)t * ten_bytes + (uint32_t)(b * kBB);
-      const uint32_t b1 = b0 + 8 * pitch;
+    const int tl = st / nchunks, chunk = st % nchunks;
+    // After a timed-out wait the warp skips the arithmetic but still takes
+    // part in every tile's hand-off, so no other warp is left waiting.
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, abort_flag, &g_gemv_status));
+    const uint32_t stg = ring_s + (uint32_t)s * SB + (uint32_t)L.g * pitch;
+    // Units are dealt to the warps round robin over the problem's tiles:
+    // U = tile * upt + chunk * ups + (t * cb + b), warp w takes U = w mod kW.
+    // The global tile index makes a tile's split over warps (and so its
+    // rounding) independent of how tiles are spread over CTAs.
+    const int U0 = (int)(((int64_t)(t0 + tl) * upt + (int64_t)chunk * ups) % kW);
+    int v = (warp - U0 + kW) % kW;
+    for (; ok && v < ups; v += kW) {
+      const int t = v >= cb ? 1 : 0, b = v - t * cb;
+      const uint32_t r0 = stg + (uint32_t)t * ten_bytes + (uint32_t)(b * kBB);
+      const uint32_t r1 = r0 + 8u * pitch;
       const int blk = chunk * cb + b;
-      const uint32_t xa = xs + (uint32_t)blk * 512u, sxa = sxs + (uint32_t)blk * 64u;
-      float y0 = 0.f, y1 = 0.f, z0 = 0.f, z1 = 0.f;
+      const uint32_t xa = xt_lane + (uint32_t)blk * L.xt_stride;
+      const uint32_t sxa = sx_base + (uint32_t)blk * sx_block_bytes(QT);
+      float y0 = 0.f, y1 = 0.f;
       if constexpr (QT == kQ4K) {
-        q4_half<0>(b0, b1, xa, sxa, tig, magic, y0, y1);
-        q4_half<1>(b0, b1, xa, sxa, tig, magic, z0, z1);
+        q4_block(r0, r1, xa, sxa, L, magic, fmagic, y0, y1);
       } else {
-        const bool a2 = (b0 & 3u) != 0;
-        Q6Half q, r;
-        if (a2) {
-          q6_load_half<0, true>(b0, b1, tig, q);
-          q6_load_half<1, true>(b0, b1, tig, r);
-        } else {
-          q6_load_half<0, false>(b0, b1, tig, q);
-          q6_load_half<1, false>(b0, b1, tig, r);
-        }
-        __syncwarp();
-        q6_half<0>(q, xa, sxa, tig, magic, y0, y1);
-        q6_half<1>(r, xa, sxa, tig, magic, z0, z1);
+        q6_block(r0, r1, xa, sxa, L, magic, fmagic, y0, y1);
       }
       if (t == 0) {
-        ya0 += y0 + z0;
-        ya1 += y1 + z1;
+        ya0 += y0;
+        ya1 += y1;
       } else {
-        yb0 += y0 + z0;
-        yb1 += y1 + z1;
-      }
-      b += kComputeWarps;
-      while (b >= cb) {
-        b -= cb;
-        ++t;
+        yb0 += y0;
+        yb1 += y1;
       }
     }
     __syncwarp();
-    if (ok && lane == 0) mbar_arrive(&sh->empty[s]);
-    if (chunk == nchunks - 1) {  // tile done: reduce over lanes, hand the warp's partials to the reducer
-      const int ti = st / nchunks, par = ti & 1;
-      // red[par] was last used by tile ti - 2: wait until the reducer is done with it.
-      if (ti >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(&sh->red_free[par], (uint32_t)((ti >> 1) - 1) & 1u, abort_flag,
-                                               &g_gemv_status)) && ok;
+    if (chunk == nchunks - 1) {
+      // Tile done: sum the four lanes of each row, hand the warp's partials to
+      // the last warp to finish the tile, which adds them in warp order.
+      float* red = reinterpret_cast<float*>(smem + P.red_off + (size_t)s * red_slot_bytes());
       for (int t = 0; t < nten; ++t) {
         float a = t ? yb0 : ya0, c = t ? yb1 : ya1;
         a += __shfl_xor_sync(0xffffffffu, a, 1);
         a += __shfl_xor_sync(0xffffffffu, a, 2);
         c += __shfl_xor_sync(0xffffffffu, c, 1);
         c += __shfl_xor_sync(0xffffffffu, c, 2);
-        if (tig == 0) {
-          sh->red[par][warp][t][g] = a;
-          sh->red[par][warp][t][g + 8] = c;
+        if (L.tig == 0) {
+          red[(warp * 2 + t) * 16 + L.g] = a;
+          red[(warp * 2 + t) * 16 + L.g + 8] = c;
         }
       }
       ya0 = ya1 = yb0 = yb1 = 0.f;
+      __threadfence_block();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh->red_full[par]);
+      uint32_t prev = 0;
+      if (lane == 0) {
+        prev = atomicAdd(&ctl->done[s], 1u);
+        __threadfence_block();
+      }
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      __syncwarp();
+      if (prev == (uint32_t)(kW - 1)) {
+        const int tile = t0 + tl;
+        if (kind == 1) {
+          if (lane < 16) {
+            const int n = tile * 16 + lane;
+            float gs = 0.f, us = 0.f;
+            for (int w = 0; w < kW; ++w) gs += red[(w * 2 + 0) * 16 + lane];
+            for (int w = 0; w < kW; ++w) us += red[(w * 2 + 1) * 16 + lane];
+            if (n < N) static_cast<__half*>(yout)[n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
+          }
+        } else if (lane < 16 * nten) {  // lane 16t + r: row r of tile t of the stage
+          const int t = lane >> 4, r = lane & 15;
+          const int n = tile * tile_rows + 16 * t + r;
+          float gs = 0.f;
+          for (int w = 0; w < kW; ++w) gs += red[(w * 2 + t) * 16 + r];
+          if (n < N) static_cast<float*>(yout)[n] = gs;
+        }
+        __syncwarp();
+        if (lane == 0) ctl->done[s] = 0u;
+      }
+      __syncwarp();
     }
+    // Release the stage (after the reduction: its partials slot is reused
+    // only once the producer has refilled this stage).
+    if (lane == 0) mbar_arrive(&ctl->empty[s]);
   }
 }
 
+template <int MT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_constant__ GemvBatch B) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -516,61 +1084,57 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
   while (i + 1 < B.count && (int)blockIdx.x >= B.p[i + 1].cta_begin) ++i;
   const GemvProb& P = B.p[i];
   const int cta = (int)blockIdx.x - P.cta_begin;
-  int kmax = 0;
-  for (int j = 0; j < B.count; ++j) kmax = max(kmax, B.p[j].K);
-  const uint32_t x_bytes = ((uint32_t)(2 * kmax + kmax / 4) + 127u) & ~127u;
-  // [x | barriers and partial sums | ring of this problem's stages]
-  GemvShared* sh = reinterpret_cast<GemvShared*>(smem + x_bytes);
-  uint8_t* stages = smem + x_bytes + kSharedBytes;
+  Ctl* ctl = reinterpret_cast<Ctl*>(smem + P.ctl_off);
   if (threadIdx.x < (unsigned)P.stages) {
-    mbar_init(&sh->full[threadIdx.x], 1);
-    mbar_init(&sh->empty[threadIdx.x], kComputeWarps);
+    mbar_init(&ctl->full[threadIdx.x], 1);
+    mbar_init(&ctl->empty[threadIdx.x], kW);
+    ctl->done[threadIdx.x] = 0u;
   }
   if (threadIdx.x == 0) {
-    mbar_init(&sh->x_full, 1);
-    for (int p = 0; p < 2; ++p) {
-      mbar_init(&sh->red_full[p], kComputeWarps);
-      mbar_init(&sh->red_free[p], 1);
-    }
-    sh->abort_flag = 0;
+    ctl->abort_flag = 0;
+    mbar_init(&ctl->red_free[0], 1);
+    mbar_init(&ctl->red_free[1], 1);
+    ctl->done[0] = ctl->done[1] = 0u;  // several tokens: counters by tile parity
   }
   fence_mbar_init();
   __syncthreads();
-  // x arrives with one bulk copy (the producer then streams the weights) and
-  // the compute warps rearrange it in place: xp[k/4] = { fp16x2(x[k], x[k+2]),
-  // fp16x2(x[k+1], x[k+3]) }, the MMA k-slot order of the quant words, and
-  // sx16[i] = sum of x[16i .. 16i+15] in fp32.
-  if (threadIdx.x == 32 * kProducerWarp) {
-    mbar_arrive_expect_tx(&sh->x_full, (uint32_t)(2 * P.K));
-    bulk_copy_g2s(smem, P.x, (uint32_t)(2 * P.K), &sh->x_full);
-  }
-  if (threadIdx.x < 32 * kComputeWarps) {
-    mbar_wait(&sh->x_full, 0u, &sh->abort_flag, &g_gemv_status);
-    const int nq = P.K / 4;
-    uint2* xp = reinterpret_cast<uint2*>(smem);
-    float* sx16 = reinterpret_cast<float*>(smem + 2 * P.K);
-    for (int q = threadIdx.x; q < nq; q += 32 * kComputeWarps) {
-      const uint2 v = xp[q];
-      uint2 o;
-      o.x = prmt(v.x, v.y, 0x5410u);
-      o.y = prmt(v.x, v.y, 0x7632u);
-      xp[q] = o;
-      float s = (half_lo(v.x) + half_lo(v.x >> 16)) + (half_lo(v.y) + half_lo(v.y >> 16));
-      s += __shfl_xor_sync(0xffffffffu, s, 1);
-      s += __shfl_xor_sync(0xffffffffu, s, 2);
-      if ((q & 3) == 0) sx16[q >> 2] = s;
+  if (threadIdx.x < 32 * kW) {
+    const uint32_t base = smem_u32(smem);
+    const uint32_t zero = base + P.ctl_off - kZeroBytes;
+    if (P.gamma) {
+      rms_partials(P.x, P.M, P.K, ctl->rss, threadIdx.x);
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
+      if ((int)threadIdx.x < P.M) {
+        float t = 0.f;
+        for (int w = 0; w < kW; ++w) t += ctl->rss[threadIdx.x][w];
+        ctl->rnorm[threadIdx.x] = 1.0f / sqrtf(t / (float)P.K + P.eps);
+      }
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kComputeWarps) : "memory");
+    if constexpr (MT == 1) {
+      const uint32_t sx = base + (uint32_t)(P.K / kQK) * kXtBlock;
+      if (P.qtype == kQ4K)
+        build_x_table<kQ4K>(P.x, P.gamma, ctl->rnorm, P.K, base, sx, zero, threadIdx.x);
+      else
+        build_x_table<kQ6K>(P.x, P.gamma, ctl->rnorm, P.K, base, sx, zero, threadIdx.x);
+    } else {
+      const uint32_t sx = base + (uint32_t)MT * (uint32_t)(2 * P.K);
+      if (P.qtype == kQ4K)
+        build_x_table_tn<kQ4K, MT>(P.x, P.gamma, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
+      else
+        build_x_table_tn<kQ6K, MT>(P.x, P.gamma, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
   }
   if (P.qtype == kQ4K)
-    run_gemv_problem<kQ4K>(P, cta, B, smem, stages, sh);
+    run_gemv_problem<kQ4K, MT>(P, cta, smem);
   else
-    run_gemv_problem<kQ6K>(P, cta, B, smem, stages, sh);
+    run_gemv_problem<kQ6K, MT>(P, cta, smem);
 }
 
 }  // namespace
 
-int gemv_max_m() { return 1; }
+int gemv_max_m() { return kMaxGemvM; }
 
 uint32_t gemv_take_status() {
   uint32_t v = 0, zero = 0;
@@ -583,63 +1147,102 @@ namespace {
 
 constexpr size_t kGemvSmem = 227 * 1024;
 
-// The stage geometry of one grouped GEMV launch (host only, no CUDA call):
-// each problem gets its own stages (its CTAs carve their own ring), and the
-// CTAs (one per SM, `sms` of them) split across problems in proportion to
-// their weight bytes.  False if some problem has no plan that fits shared
-// memory (x of the largest K plus at least two stages).
+// The token slots of the kernel that runs M tokens: 1 (decode layout), 8 or 16.
+int slots_for(int64_t M) { return M <= 1 ? 1 : M <= 8 ? 8 : 16; }
+
+// The stage geometry of one problem, from its own shape only (so grouping
+// problems never changes how one of them is computed).  False if no plan with
+// at least two stages fits.
+//   Layout: [x table | sums | zero region | control | partials | ring[S]].
+bool plan_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
+  memset(&P, 0, sizeof(P));
+  P.w[0] = static_cast<const uint8_t*>(d.w0);
+  P.w[1] = static_cast<const uint8_t*>(d.w1);
+  P.x = d.x;
+  P.y = d.y;
+  if (d.M < 1 || d.M > kMaxGemvM || d.N <= 0 || d.N >= ((int64_t)1 << 31) || d.K <= 0 || d.K % kQK != 0 ||
+      d.K >= ((int64_t)1 << 31))
+    return false;
+  P.M = (int)d.M;
+  P.gamma = d.gamma;
+  P.eps = d.eps;
+  P.N = (int)d.N;
+  P.K = (int)d.K;
+  P.qtype = d.qtype;
+  P.kind = d.w1 ? 1 : 0;
+  const int mt = slots_for(d.M);
+  const int nb = P.K / kQK;
+  const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
+  const int nten = 1 + P.kind;
+  const int64_t RB = (int64_t)nb * bb;
+  const size_t xt = mt == 1 ? round128((size_t)nb * (kXtBlock + sx_block_bytes(P.qtype)))
+                            : round128((size_t)mt * 2 * P.K + (size_t)nb * (P.qtype == kQ4K ? 8 : 16) * mt * 4);
+  P.ctl_off = (uint32_t)(xt + kZeroBytes);
+  P.red_off = P.ctl_off + kCtlBytes;
+  // The decode layout keeps a partials slot per stage; several tokens keep
+  // two buffers (tile parity) sized for the stage's tensors.
+  const size_t red_stage = mt == 1 ? red_slot_bytes() : 0;
+  auto red_fixed_for = [&](int ten) { return mt == 1 ? (size_t)0 : round128((size_t)2 * red_tn_bytes(mt, ten)); };
+  auto avail_for = [&](int ten) -> size_t {
+    const size_t fixed = (size_t)P.red_off + red_fixed_for(ten) + 128 + 128;  // + slack past the last block
+    return fixed >= kGemvSmem ? 0 : kGemvSmem - fixed;
+  };
+  size_t avail = avail_for(nten);
+  if (avail == 0) return false;
+  auto per_stage = [&](size_t stage_bytes) { return stage_bytes + red_stage; };
+  // Stage: whole rows (cb = K/256) when three stages fit, else the largest
+  // chunk of cb blocks dividing K/256 (rows 16-byte aligned in device memory,
+  // cb blocks a multiple of 16 bytes: any cb for Q4_K, multiples of 8 for
+  // Q6_K) that gives three stages, else two.
+  int cb = nb;
+  if (3 * per_stage(round128((size_t)16 * nten * nb * bb)) > avail) {
+    cb = 0;
+    for (int want = 3; want >= 2 && cb == 0; --want)
+      for (int c = 1; c <= nb; ++c)
+        if (nb % c == 0 && (c * bb) % 16 == 0 && (RB % 16) == 0 &&
+            (size_t)want * per_stage(round128((size_t)16 * nten * c * bb)) <= avail)
+          cb = c;
+    if (cb == 0) cb = nb;  // whole rows with fewer stages (checked below)
+  }
+  P.cb = cb;
+  // One tensor with whole rows: two adjacent tiles per stage (halves the
+  // per-block share of the per-tile reduction) when two such stages fit.
+  P.pair = (P.kind == 0 && cb == nb && P.N > 16 && 2 * per_stage(round128((size_t)32 * nb * bb)) <= avail_for(2))
+               ? 1
+               : 0;
+  if (P.pair) avail = avail_for(2);
+  P.stage_bytes = round128((size_t)16 * (nten + P.pair) * cb * bb);
+  P.stages = (int)std::min<size_t>(kMaxStages, avail / per_stage(P.stage_bytes));
+  if (P.stages < 2) return false;
+  P.red_bytes = mt == 1 ? 0u : red_tn_bytes(mt, nten + P.pair);
+  P.ring_off = P.red_off + (uint32_t)(mt == 1 ? round128((size_t)P.stages * red_stage) : red_fixed_for(nten + P.pair));
+  P.tiles = (P.N + 16 * (1 + P.pair) - 1) / (16 * (1 + P.pair));
+  *smem_out = (size_t)P.ring_off + (size_t)P.stages * P.stage_bytes + 128 + 128;  // + base alignment + slack
+  return *smem_out <= kGemvSmem;
+}
+
+// One grouped GEMV launch (problems of the same token-slot count): every
+// problem keeps its own plan, the launch takes the largest shared-memory size,
+// and the CTAs (one per SM, `sms` of them) split across problems in proportion
+// to their weight bytes.
 bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* smem_out) {
   if (count <= 0 || count > kMaxGemvProbs) return false;
   GemvBatch& B = *out;
   memset(&B, 0, sizeof(B));
   B.count = count;
-  int64_t kmax = 0;
-  for (int i = 0; i < count; ++i) kmax = std::max<int64_t>(kmax, d[i].K);
-  const size_t x_bytes = ((size_t)(2 * kmax + kmax / 4) + 127) / 128 * 128;
-  if (x_bytes + kSharedBytes + 128 >= kGemvSmem) return false;
-  const size_t avail = kGemvSmem - x_bytes - kSharedBytes - 128;  // for one CTA's ring
   double total = 0;
   int64_t bytes[kMaxGemvProbs];
-  size_t ring = 0;
+  size_t smem = 0;
   for (int i = 0; i < count; ++i) {
-    GemvProb& P = B.p[i];
-    P.w[0] = static_cast<const uint8_t*>(d[i].w0);
-    P.w[1] = static_cast<const uint8_t*>(d[i].w1);
-    P.x = d[i].x;
-    P.y = d[i].y;
-    P.N = (int)d[i].N;
-    P.K = (int)d[i].K;
-    P.qtype = d[i].qtype;
-    P.kind = d[i].w1 ? 1 : 0;
-    const int nb = P.K / kQK;
-    const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
-    const int nten = 1 + P.kind;
-    const int64_t RB = (int64_t)nb * bb;
-    // Stage: whole rows (cb = K/256) when three stages fit, else the largest
-    // multiple of 8 blocks (8 x 210 B is 16-byte aligned) dividing K/256 that
-    // gives three stages.
-    int cb = nb;
-    if ((size_t)3 * 16 * nten * nb * bb > avail) {
-      cb = 0;
-      for (int c = 8; c <= nb; c += 8)
-        if (nb % c == 0 && (size_t)3 * 16 * nten * c * bb <= avail && (RB % 16) == 0) cb = c;
-      if (cb == 0) cb = nb;  // fall back to whole rows with fewer stages
-    }
-    P.cb = cb;
-    // One tensor with whole rows: two adjacent tiles per stage (halves the
-    // per-block share of the per-tile reduction) when two such stages fit
-    // (measured on GB300: the Q6_K LM head streams ~15 % faster with two
-    // paired stages than with five single ones).
-    P.pair = (P.kind == 0 && cb == nb && P.N > 16 && 2 * (size_t)round128((size_t)32 * nb * bb) <= avail) ? 1 : 0;
-    P.stage_bytes = round128((size_t)16 * (nten + P.pair) * cb * bb);
-    P.stages = (int)std::min<size_t>(kMaxStages, avail / P.stage_bytes);
-    if (P.stages < 2) return false;
-    ring = std::max(ring, (size_t)P.stages * P.stage_bytes);
-    P.tiles = (P.N + 16 * (1 + P.pair) - 1) / (16 * (1 + P.pair));
-    bytes[i] = (int64_t)P.N * RB * nten;
+    size_t s = 0;
+    if (slots_for(d[i].M) != slots_for(d[0].M)) return false;
+    if (!plan_problem(d[i], B.p[i], &s)) return false;
+    smem = std::max(smem, s);
+    const int bb = B.p[i].qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
+    bytes[i] = (int64_t)B.p[i].N * (B.p[i].K / kQK) * bb * (1 + B.p[i].kind);
     total += (double)bytes[i];
   }
-  *smem_out = x_bytes + kSharedBytes + ring + 128;
+  *smem_out = smem;
   const int budget = std::max(count, sms);
   int used = 0;
   for (int i = 0; i < count; ++i) {
@@ -670,7 +1273,23 @@ bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* sm
     B.p[i].cta_begin = begin;
     begin += B.p[i].ctas;
   }
-  return *smem_out <= kGemvSmem;
+  return true;
+}
+
+template <int MT>
+cudaError_t launch_mt(const GemvBatch& B, size_t smem, cudaStream_t s) {
+  static PerDeviceFlag attr;  // the shared-memory limit is a per-device function attribute
+  const int dev = current_device();
+  if (!attr.done(dev)) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemv_stream_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
+    if (e != cudaSuccess) return e;
+    attr.mark(dev);
+  }
+  int ctas = 0;
+  for (int i = 0; i < B.count; ++i) ctas += B.p[i].ctas;
+  gemv_stream_kernel<MT><<<ctas, kThreads, smem, s>>>(B);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -681,28 +1300,23 @@ bool gemv_plan_fits(const GemvDesc* d, int count) {
   return plan_gemv(d, count, 152, &B, &smem);  // the SM count splits CTAs; it does not decide the fit
 }
 
+int gemv_slots(int64_t M) { return slots_for(M); }
+
 // Launch one grouped GEMV (see plan_gemv).
 cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
   GemvBatch B;
   size_t smem = 0;
   if (!plan_gemv(d, count, device_sms(), &B, &smem)) return cudaErrorInvalidConfiguration;
-  static PerDeviceFlag attr;  // the shared-memory limit is a per-device function attribute
-  const int dev = current_device();
-  if (!attr.done(dev)) {
-    cudaError_t e =
-        cudaFuncSetAttribute(gemv_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
-    if (e != cudaSuccess) return e;
-    attr.mark(dev);
+  switch (slots_for(d[0].M)) {
+    case 1: return launch_mt<1>(B, smem, s);
+    case 8: return launch_mt<8>(B, smem, s);
+    default: return launch_mt<16>(B, smem, s);
   }
-  int ctas = 0;
-  for (int i = 0; i < B.count; ++i) ctas += B.p[i].ctas;
-  gemv_stream_kernel<<<ctas, kThreads, smem, s>>>(B);
-  return cudaGetLastError();
 }
 
 cudaError_t launch_gemv(QType t, const void* W, const uint16_t* x, float* y, int64_t N, int64_t K,
                         cudaStream_t s) {
-  GemvDesc d{t, W, nullptr, x, y, N, K};
+  GemvDesc d{t, W, nullptr, x, y, 1, N, K, nullptr, 0.f};
   return launch_gemv_batch(&d, 1, s);
 }
 

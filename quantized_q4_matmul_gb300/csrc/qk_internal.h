@@ -62,14 +62,24 @@ struct GemmPlanInfo {
 };
 bool gemm_plan(QType t, bool gateup, int64_t M, int64_t N, GemmPlanInfo* info);
 
+// RMSNorm rows into an fp16 buffer (problems the GEMV does not take):
+// out[m][k] = fp16(x[m][k] / sqrt(mean_k x[m][k]^2 + eps) * gamma[k]).
+cudaError_t launch_rmsnorm_rows(const uint16_t* x, const uint16_t* gamma, float eps, uint16_t* out, int64_t M,
+                                int64_t K, cudaStream_t s);
+
 // A kernel whose single bounded wait can never complete (see qk_debug_wait_timeout).
 cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t s);
 
-// Largest M the decode GEMV handles; larger M goes to the tensor-core GEMM.
+// Largest M the GEMV handles (M = 1 in the decode layout, 2..16 with the
+// tokens in the MMA columns); larger M goes to the tensor-core GEMM.
+constexpr int kMaxGemvM = 16;
 int gemv_max_m();
+// The kernel's token-slot count for M tokens (1, 8 or 16): problems share a
+// launch only with problems of the same count.
+int gemv_slots(int64_t M);
 
-// One M = 1 problem of a grouped decode GEMV launch.  w1 != null makes it the
-// fused gate/up + SwiGLU problem (w0 = gate, w1 = up, y fp16), else y is fp32.
+// One problem of a grouped GEMV launch.  w1 != null makes it the fused
+// gate/up + SwiGLU problem (w0 = gate, w1 = up, y fp16), else y is fp32.
 constexpr int kMaxGemvProbs = 8;
 struct GemvDesc {
   QType qtype;
@@ -77,13 +87,16 @@ struct GemvDesc {
   const void* w1;
   const uint16_t* x;
   void* y;
-  int64_t N, K;
+  int64_t M, N, K;
+  const uint16_t* gamma;  // RMSNorm prologue over x (fp16 gamma[K]), or null
+  float eps;
 };
 cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s);
 
-// Whether one grouped GEMV launch can run these problems: x of the largest K
-// and at least two weight stages of every problem must fit in shared memory.
-// Host only (no CUDA call).  Problems that do not fit run on the GEMM.
+// Whether one grouped GEMV launch can run these problems: each problem's own
+// plan (its x table and at least two weight stages) must fit in shared memory
+// and all must have the same token-slot count.  Host only (no CUDA call).
+// Problems that do not fit run on the GEMM.
 bool gemv_plan_fits(const GemvDesc* d, int count);
 
 }  // namespace qk

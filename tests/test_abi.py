@@ -144,73 +144,56 @@ def test_binding_checks_tensor_buffers_before_the_call(qk_lib):
 
 def test_decode_kernel_choice_on_the_host(qk_lib):
     """Which kernel an M = 1 problem runs on is decided on the host from the
-    GEMV's shared-memory plan (x of K plus two weight stages).  The model's
-    inner sizes stay on the GEMV; K values it cannot stage go to the GEMM."""
+    GEMV's shared-memory plan (the x table of K plus two weight stages).  The
+    model's inner sizes stay on the GEMV; K values it cannot stage go to the
+    GEMM."""
     use = qk_lib.qk_decode_uses_gemv
     for qt, gu in (("q4k", False), ("q6k", False), ("q4k", True)):
-        for K in range(256, 6144 + 1, 256):
+        for K in range(256, 5632 + 1, 256):
             assert use(qt, K, gu), (qt, gu, K)
-        assert use(qt, 8192, gu)
-        # x alone (fp16 copy plus 16-wide sums, 2.25 bytes per k) exceeds 227 KB
-        assert not use(qt, 131072, gu)
+        for K in (6144, 8192, 16384):
+            assert use(qt, K, gu), (qt, gu, K)
+        # the x table alone (4.25-4.5 bytes per k) exceeds 227 KB
+        assert not use(qt, 65536, gu)
     # Q6_K rows of an odd number of 8-block groups cannot be chunked 16-byte
-    # aligned, and whole 16-row tiles no longer fit three times
-    assert not use("q6k", 8448)
-    assert not use("q4k", 6400, True)   # gate/up: two tensors per stage
-    assert not use("q4k", 11520)
-    assert use("q6k", 16384) and use("q4k", 16384, True)  # 64 blocks: chunks of 8 fit
+    # aligned, and whole 16-row tiles no longer fit three times; Q4_K blocks
+    # (144 bytes) chunk at any block count
+    assert not use("q6k", 7424) and not use("q6k", 8448)
+    assert use("q4k", 5888, True) and use("q4k", 10496) and use("q4k", 32768)
+    assert use("q6k", 32768)
     L = qk_lib.lib()
+    # several tokens (2 <= M <= 16) run on the GEMV too while the x table of M
+    # tokens fits: the model's K = 3072 up to 16 tokens, K = 8192 up to 8
+    uses = qk_lib.qk_uses_gemv
+    for qt, gu in (("q4k", False), ("q6k", False), ("q4k", True)):
+        for M in (1, 2, 5, 8, 9, 16):
+            assert uses(qt, M, 3072, gu), (qt, M)
+        for M in (2, 8):
+            assert uses(qt, M, 8192, gu), (qt, M)
+        assert not uses(qt, 9, 8192, gu) and not uses(qt, 17, 3072, gu)
+        assert uses(qt, 1, 8192, gu) == use(qt, 8192, gu)
+    assert L.qk_uses_gemv(0, 0, 0, 3072) == -1 and L.qk_uses_gemv(0, 0, 4, 300) == -1
     assert L.qk_decode_uses_gemv(2, 0, 3072) == -1      # unknown format
     assert L.qk_decode_uses_gemv(1, 1, 3072) == -1      # gate/up is Q4_K only
     assert L.qk_decode_uses_gemv(0, 0, 300) == -1       # K % 256
     assert L.qk_decode_uses_gemv(0, 0, 0) == -1
 
 
-def test_gemm_plans_fit_tensor_memory_on_a_shared_sm(qk_lib):
-    """tcgen05.alloc waits without a time limit for free tensor-memory columns,
-    so the CTAs that can share an SM must fit in its 512 columns together.
-    Checked on the host for every linear of the model at every swept M (and the
-    small-M shapes that pick narrow token tiles), for both A-tile placements."""
-    import subprocess
-    import sys
-    from tests import synth
-    shapes = sorted({(lin.qtype, lin.N, lin.K) for _, lin in synth.model_linears()})
-    Ms = sorted(set(synth.SWEEP_M) | {2, 17, 33, 48, 64, 100, 200, 300, 513, 4096})
-    seen_tmem = set()
-    for qt, N, K in shapes:
-        for M in Ms:
-            p = qk_lib.qk_gemm_plan(qt, M, N, K)
-            assert p["max_ctas_per_sm"] >= 1
-            assert p["max_ctas_per_sm"] * p["tmem_cols"] <= 512, (qt, N, K, M, p)
-            assert p["smem_bytes"] <= 227 * 1024
-            seen_tmem.add(p["a_in_tmem"])
-    for M in Ms:
-        p = qk_lib.qk_gemm_plan("q4k", M, synth.FFN, synth.HIDDEN, gateup=True)
-        assert p["max_ctas_per_sm"] * p["tmem_cols"] <= 512, (M, p)
-    assert seen_tmem == {0, 1}
-    # A narrow token tile with A tiles in tensor memory needs 2*64 + 5*32 = 288
-    # columns (allocated as 512) in ~70 KB of shared memory: padded to one CTA.
-    p = qk_lib.qk_gemm_plan("q4k", 64, 4096, 4096)
-    assert p["token_tile"] == 64 and p["a_in_tmem"] == 1 and p["tmem_cols"] == 512
-    assert p["max_ctas_per_sm"] == 1
-    # The shared-memory A path (QK_A_TMEM=0) in a child process: same rule.
-    code = ("import sys; sys.path.insert(0, %r); import quantized_q4_matmul_gb300 as qk\n"
-            "for M in (16, 64, 128, 1024):\n"
-            "    p = qk.qk_gemm_plan('q6k', M, 3072, 8192)\n"
-            "    assert p['a_in_tmem'] == 0 and p['max_ctas_per_sm'] * p['tmem_cols'] <= 512, p\n"
-            "print('ok')" % ROOT)
-    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, QK_A_TMEM="0"), capture_output=True,
-                       text=True, timeout=300)
-    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
-
-
-def test_gemm_plan_rejects_bad_arguments(qk_lib):
+def test_rmsnorm_rejects_bad_arguments_on_the_host(qk_lib):
     L = qk_lib.lib()
-    info = qk_lib.qk_gemm_plan_info()
-    import ctypes as C
-    assert L.qk_gemm_plan(0, 0, 16, 3072, 3072, None) == -1
-    assert L.qk_gemm_plan(2, 0, 16, 3072, 3072, C.byref(info)) == -3
-    assert L.qk_gemm_plan(1, 1, 16, 3072, 3072, C.byref(info)) == -3
-    assert L.qk_gemm_plan(0, 0, 16, 3072, 300, C.byref(info)) == -3
-    assert L.qk_gemm_plan(0, 0, 0, 3072, 3072, C.byref(info)) == -3
-    assert L.qk_gemm_plan(0, 0, 16, 3072, 3072, C.byref(info)) == 0 and info.token_tile == 16
+    f = L.qk_rmsnorm_matmul_q4k
+    assert f(A16, A16, None, 1e-5, A16, A16, 4, 8, 256, None) == -1          # gamma NULL
+    assert f(A16, A16, A16, -1.0, A16, A16, 4, 8, 256, None) == -3           # eps < 0
+    assert f(A16, A16, A16, float("inf"), A16, A16, 4, 8, 256, None) == -3   # eps not finite
+    assert f(A16, A16, A8, 1e-5, A16, A16, 4, 8, 256, None) == -2            # gamma misaligned
+    assert f(A16, A16, A16, 1e-5, A16, A16, 4, 8, 300, None) == -3           # K % 256
+    assert f(None, None, A16, 1e-5, None, None, 0, 8, 256, None) == 0        # M = 0: no-op
+    D = qk_lib.qk_matmul_desc
+    arr = (D * 2)(D(0, A16, None, A16, A16, 1, 8, 256), D(0, A16, None, A16, A16, 1, 8, 512))
+    assert L.qk_rmsnorm_matmul_batch(arr, 2, A16, 1e-5, None, None) in (-3, -4, -6, -8)
+    assert L.qk_rmsnorm_gateup_swiglu_q4k(A16, None, A16, A16, 1e-5, A16, A16, 4, 8, 256, None) == -1
+    # the scratch an M-token problem needs: none where the GEMV fuses the norm
+    sb = qk_lib.qk_rmsnorm_scratch_bytes
+    assert sb("q4k", 1, 3072) == 0 and sb("q6k", 16, 3072) == 0 and sb("q4k", 8, 8192, True) == 0
+    assert sb("q4k", 17, 3072) == 17 * 3072 * 2 and sb("q6k", 1024, 8192) == 1024 * 8192 * 2
+    assert L.qk_rmsnorm_scratch_bytes(1, 1, 4, 256) == -1 and L.qk_rmsnorm_scratch_bytes(0, 0, 4, 300) == -1

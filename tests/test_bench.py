@@ -95,3 +95,41 @@ def test_clock_summary_parsing(tmp_path, monkeypatch):
     assert "untimed replays" in d["window"]
     c.proc = None
     assert c.summary()["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_roofline_fraction_uses_the_attainable_rate():
+    """Each configuration reports its fraction of min(peak, intensity x HBM):
+    an HBM-bound decode GEMV against the copy bandwidth, a tensor-bound GEMM
+    against the tensor peak."""
+    pk = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+    # decode: 64 MB moved for 63 MFLOP in 0.016 ms -> 4 TB/s, HBM-bound
+    r = bench.roof(63e6, 64e6, 0.016, pk)
+    assert r["bound"] == "hbm"
+    assert abs(r["gbs"] - 4000.0) < 1e-6
+    assert abs(r["frac_of_attainable"] - 4000.0 / 6800.0) < 1e-9
+    # prefill: 103 GFLOP over 35 MB in 0.1 ms -> 1030 TFLOP/s, tensor-bound
+    r = bench.roof(103e9, 35e6, 0.1, pk)
+    assert r["bound"] == "tensor" and abs(r["frac_of_attainable"] - 1030.0 / 1900.0) < 1e-9
+    s = bench.stats([1.0, 2.0, 3.0, 4.0, 100.0])
+    assert s["median"] == 3.0 and s["min"] == 1.0 and s["max"] == 100.0 and s["runs"] == 5
+    assert 4.0 < s["p95"] <= 100.0
+
+
+def test_lin_bytes_and_sweep_totals():
+    """Config 4's weights: the 28 layers' linears under the Q4_K_M mix plus the
+    tied LM head, 2,022,193,152 bytes (1.883 GiB, the pages' 1.9 GiB)."""
+    model = bench.synth.model_linears()
+    assert sum(bench.synth.weight_bytes(l.qtype, l.N, l.K) for _, l in model) == 2_022_193_152
+    q = bench.synth.Linear("attn_q", "q4k", 3072, 3072)
+    assert bench.lin_bytes(q, 16) == 3072 * 12 * 144 + 2 * 16 * 3072 + 4 * 16 * 3072
+    g = bench.synth.Linear("ffn_gate", "q4k", 8192, 3072)
+    assert bench.lin_bytes(g, 1, gateup=True) == 2 * 8192 * 12 * 144 + 2 * 3072 + 2 * 8192
+
+
+def test_gpus_flag_must_match_the_launcher():
+    """--gpus N without a launcher that starts N ranks is an error, not a
+    silent single replica."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--steps", "1"],
+                       env={k: v for k, v in ENV.items() if k not in ("WORLD_SIZE", "RANK")}, capture_output=True,
+                       text=True, timeout=300, cwd=ROOT)
+    assert r.returncode != 0 and "torchrun" in r.stderr

@@ -116,6 +116,56 @@ def test_matmul_small(qk_lib, cuda, qtype, M, N, K):
     check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "%s M%d N%d K%d" % (qtype, M, N, K))
 
 
+# Several tokens on the GEMV (tokens in the MMA columns): every M of one and
+# two token tiles, ragged N, both K of the model (M <= 8 at K = 8192).
+SMALL_M = [(M, N, K) for M in (2, 3, 7, 8, 9, 12, 16) for N, K in ((200, 3072), (48, 1024))] + \
+          [(M, 80, 8192) for M in (2, 5, 8)]
+
+
+@pytest.mark.parametrize("qtype", ["q4k", "q6k"])
+@pytest.mark.parametrize("M,N,K", SMALL_M)
+def test_matmul_small_m_gemv(qk_lib, cuda, qtype, M, N, K):
+    assert qk_lib.qk_uses_gemv(qtype, M, K)
+    rng = synth.rng_for(M * 13 + N, K + 1)
+    W = synth.weights(rng, qtype, N, K)
+    x = synth.activations(rng, M, K)
+    ref = oracle.matmul(QT[qtype], W, x, N, K)
+    check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "%s M%d N%d K%d" % (qtype, M, N, K))
+
+
+@pytest.mark.parametrize("M", [2, 8, 16])
+def test_gateup_small_m_gemv(qk_lib, cuda, M):
+    import torch
+    N, K = 144, 3072
+    assert qk_lib.qk_uses_gemv("q4k", M, K, gateup=True)
+    rng = synth.rng_for(M, 77)
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, M, K)
+    y = torch.empty(M, N, dtype=torch.float16, device=cuda)
+    qk_lib.qk_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), y, M, N, K)
+    qk_lib.qk_get_device_status()
+    check_close_f16out(y.float().cpu().numpy().astype(np.float64), oracle.gateup_swiglu(Wg, Wu, x, N, K),
+                       "gate/up M%d" % M)
+
+
+def test_batch_small_m_matches_single_calls(qk_lib, cuda):
+    """QKV-shaped problems at M = 16 in one grouped launch: bit-identical to the
+    single calls (each keeps its own plan and split over warps)."""
+    import torch
+    probs, singles = [], []
+    for i, (qt, N) in enumerate((("q4k", 3072), ("q4k", 1024), ("q6k", 1024))):
+        rng = synth.rng_for(81, i)
+        W = synth.weights(rng, qt, N, 3072)
+        x = synth.activations(rng, 16, 3072)
+        y = torch.full((16, N), float("nan"), device=cuda)
+        probs.append(dict(qtype=qt, blocks=_dev(W, cuda), x_f16=_x_dev(x, cuda), y=y, M=16, N=N, K=3072))
+        singles.append(gpu_matmul(qk_lib, qt, W, x, N, 3072, cuda))
+    qk_lib.qk_matmul_batch(probs)
+    qk_lib.qk_get_device_status()
+    for p, single in zip(probs, singles):
+        assert np.array_equal(p["y"].cpu().numpy().astype(np.float64), single)
+
+
 @pytest.mark.parametrize("qtype", ["q4k", "q6k"])
 def test_matmul_deterministic(qk_lib, cuda, qtype):
     rng = synth.rng_for(3, 3)
@@ -445,7 +495,7 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable(qk_lib, cuda):
 # ---------------------------------------------------------------------------
 # M = 1 problems whose K the GEMV cannot stage run on the tensor-core GEMM
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("qtype,N,K", [("q6k", 200, 8448), ("q4k", 130, 11520)])
+@pytest.mark.parametrize("qtype,N,K", [("q6k", 200, 8448), ("q4k", 130, 65536)])
 def test_decode_fallback_to_gemm(qk_lib, cuda, qtype, N, K):
     assert not qk_lib.qk_decode_uses_gemv(qtype, K)
     rng = synth.rng_for(41, K)
@@ -457,7 +507,7 @@ def test_decode_fallback_to_gemm(qk_lib, cuda, qtype, N, K):
 
 def test_decode_gateup_fallback_to_gemm(qk_lib, cuda):
     import torch
-    N, K = 192, 6400
+    N, K = 192, 65536
     assert not qk_lib.qk_decode_uses_gemv("q4k", K, gateup=True)
     rng = synth.rng_for(42, K)
     Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
@@ -469,28 +519,184 @@ def test_decode_gateup_fallback_to_gemm(qk_lib, cuda):
                        "gate/up M1 K%d on the GEMM" % K)
 
 
-def test_batch_launches_groups_whose_plans_fit(qk_lib, cuda):
-    """A gate/up at K = 6144 and a Q6_K at K = 65536 each fit a GEMV launch but
-    not one together (x of the larger K leaves too little room for the gate/up
-    stages); a Q6_K at K = 8448 fits none and runs on the GEMM."""
+def test_batch_mixed_k_group(qk_lib, cuda):
+    """M = 1 problems of different K share one launch (each keeps its own plan,
+    the launch takes the largest shared-memory size); a Q6_K at K = 8448 fits
+    no GEMV plan and runs on the GEMM.  Every result is bit-identical to its
+    single-problem call, since grouping never changes a problem's plan."""
     import torch
-    assert qk_lib.qk_decode_uses_gemv("q4k", 6144, gateup=True) and qk_lib.qk_decode_uses_gemv("q6k", 65536)
+    assert qk_lib.qk_decode_uses_gemv("q4k", 6144, gateup=True) and qk_lib.qk_decode_uses_gemv("q6k", 16384)
+    assert not qk_lib.qk_decode_uses_gemv("q6k", 8448)
     rng = synth.rng_for(43, 0)
     probs, checks = [], []
     Wg, Wu = synth.q4k_weights(rng, 128, 6144), synth.q4k_weights(rng, 128, 6144)
     xg = synth.activations(rng, 1, 6144)
     yg = torch.empty(1, 128, dtype=torch.float16, device=cuda)
-    probs.append(dict(qtype="q4k", blocks=_dev(Wg, cuda), up_blocks=_dev(Wu, cuda), x_f16=_x_dev(xg, cuda), y=yg,
-                      M=1, N=128, K=6144))
-    for qt, N, K in (("q6k", 64, 65536), ("q6k", 64, 8448), ("q4k", 256, 3072)):
+    Wgd, Wud, xgd = _dev(Wg, cuda), _dev(Wu, cuda), _x_dev(xg, cuda)
+    probs.append(dict(qtype="q4k", blocks=Wgd, up_blocks=Wud, x_f16=xgd, y=yg, M=1, N=128, K=6144))
+    singles = []
+    for qt, N, K in (("q6k", 64, 16384), ("q6k", 64, 8448), ("q4k", 256, 3072), ("q4k", 48, 32768)):
         W = synth.weights(rng, qt, N, K)
         x = synth.activations(rng, 1, K)
         y = torch.empty(1, N, dtype=torch.float32, device=cuda)
         probs.append(dict(qtype=qt, blocks=_dev(W, cuda), x_f16=_x_dev(x, cuda), y=y, M=1, N=N, K=K))
         checks.append((y, oracle.matmul(QT[qt], W, x, N, K), "%s K%d" % (qt, K)))
+        singles.append(gpu_matmul(qk_lib, qt, W, x, N, K, cuda))
+    ys = torch.empty(1, 128, dtype=torch.float16, device=cuda)
+    qk_lib.qk_gateup_swiglu_q4k(Wgd, Wud, xgd, ys, 1, 128, 6144)
     qk_lib.qk_matmul_batch(probs)
     qk_lib.qk_get_device_status()
+    assert torch.equal(yg, ys)
     check_close_f16out(yg.float().cpu().numpy().astype(np.float64), oracle.gateup_swiglu(Wg, Wu, xg, 128, 6144),
                        "gate/up K6144")
-    for y, ref, what in checks:
-        check_close(y.cpu().numpy().astype(np.float64), ref, what)
+    for (y, ref, what), single in zip(checks, singles):
+        got = y.cpu().numpy().astype(np.float64)
+        assert np.array_equal(got, single), what
+        check_close(got, ref, what)
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm in front of the linears
+# ---------------------------------------------------------------------------
+EPS = 1e-5
+
+
+def gamma_vec(rng, K):
+    """Norm weights fp16(1 + 0.1 N(0,1)): the synthetic recipe of this suite."""
+    return (1.0 + 0.1 * rng.standard_normal(K)).astype(np.float16)
+
+
+def scratch_for(qk, problems, cuda):
+    import torch
+    need = 0
+    for qt, M, K, gu in problems:
+        need = max(need, qk.qk_rmsnorm_scratch_bytes(qt, M, K, gu))
+    return torch.empty(max(need // 2, 1), dtype=torch.float16, device=cuda) if need else None
+
+
+@pytest.mark.parametrize("qtype", ["q4k", "q6k"])
+@pytest.mark.parametrize("M,N,K", [(1, 200, 3072), (1, 64, 8192), (5, 130, 1024), (16, 96, 3072), (40, 160, 1024),
+                                   (300, 128, 512), (12, 64, 8192)])
+def test_rmsnorm_matmul(qk_lib, cuda, qtype, M, N, K):
+    """y = (RMSNorm(x) * gamma) . W^T: fused into the GEMV's x staging for
+    M <= 16 where it fits, through the scratch buffer and the GEMM otherwise."""
+    import torch
+    rng = synth.rng_for(M + 3 * N, K + 7)
+    W = synth.weights(rng, qtype, N, K)
+    x = synth.activations(rng, M, K)
+    g = gamma_vec(rng, K)
+    sc = scratch_for(qk_lib, [(qtype, M, K, False)], cuda)
+    assert (sc is None) == qk_lib.qk_uses_gemv(qtype, M, K)
+    y = torch.empty(M, N, dtype=torch.float32, device=cuda)
+    fn = qk_lib.qk_rmsnorm_matmul_q4k if qtype == "q4k" else qk_lib.qk_rmsnorm_matmul_q6k
+    fn(_dev(W, cuda), _x_dev(x, cuda), _x_dev(g, cuda), EPS, y, M, N, K, scratch=sc)
+    qk_lib.qk_get_device_status()
+    ref = oracle.rmsnorm_matmul(QT[qtype], W, x, g, EPS, N, K)
+    check_close(y.cpu().numpy().astype(np.float64), ref, "rmsnorm %s M%d N%d K%d" % (qtype, M, N, K))
+
+
+@pytest.mark.parametrize("M", [1, 8, 16, 100])
+def test_rmsnorm_gateup(qk_lib, cuda, M):
+    import torch
+    N, K = 160, 3072
+    rng = synth.rng_for(M, 91)
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, M, K)
+    g = gamma_vec(rng, K)
+    sc = scratch_for(qk_lib, [("q4k", M, K, True)], cuda)
+    y = torch.empty(M, N, dtype=torch.float16, device=cuda)
+    qk_lib.qk_rmsnorm_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), _x_dev(g, cuda), EPS, y, M,
+                                        N, K, scratch=sc)
+    qk_lib.qk_get_device_status()
+    ref = oracle.rmsnorm_gateup_swiglu(Wg, Wu, x, g, EPS, N, K)
+    check_close_f16out(y.float().cpu().numpy().astype(np.float64), ref, "rmsnorm gate/up M%d" % M)
+
+
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_rmsnorm_batch_qkv(qk_lib, cuda, M):
+    """q, k, v share x and one RMSNorm: grouped on the GEMV (M <= 16), or
+    normalized once into the scratch for the three GEMMs (M = 64)."""
+    import torch
+    rng = synth.rng_for(M, 92)
+    K = 3072
+    x = synth.activations(rng, M, K)
+    g = gamma_vec(rng, K)
+    xd, gd = _x_dev(x, cuda), _x_dev(g, cuda)
+    probs, refs = [], []
+    for qt, N in (("q4k", 256), ("q4k", 128), ("q6k", 128)):
+        W = synth.weights(rng, qt, N, K)
+        y = torch.full((M, N), float("nan"), device=cuda)
+        probs.append(dict(qtype=qt, blocks=_dev(W, cuda), x_f16=xd, y=y, M=M, N=N, K=K))
+        refs.append(oracle.rmsnorm_matmul(QT[qt], W, x, g, EPS, N, K))
+    sc = scratch_for(qk_lib, [(p["qtype"], M, K, False) for p in probs], cuda)
+    qk_lib.qk_rmsnorm_matmul_batch(probs, gd, EPS, scratch=sc)
+    qk_lib.qk_get_device_status()
+    for p, ref in zip(probs, refs):
+        check_close(p["y"].cpu().numpy().astype(np.float64), ref, "rmsnorm batch %s M%d" % (p["qtype"], M))
+
+
+def test_rmsnorm_decode_layer(qk_lib, cuda):
+    """The decode layer's linears with their norms (config 1 at M = 1): q, k, v
+    behind one RMSNorm, the fused gate/up behind another; checked in full."""
+    import torch
+    rng = synth.rng_for(93, 0)
+    K = synth.HIDDEN
+    x1, x2 = synth.activations(rng, 1, K), synth.activations(rng, 1, K)
+    g1, g2 = gamma_vec(rng, K), gamma_vec(rng, K)
+    lins = synth.layer_linears(0)
+    probs, refs = [], []
+    for lin in lins[:3]:
+        W = synth.weights(rng, lin.qtype, lin.N, lin.K)
+        y = torch.empty(1, lin.N, device=cuda)
+        probs.append(dict(qtype=lin.qtype, blocks=_dev(W, cuda), x_f16=_x_dev(x1, cuda), y=y, M=1, N=lin.N, K=K))
+        refs.append(oracle.rmsnorm_matmul(QT[lin.qtype], W, x1, g1, EPS, lin.N, K))
+    qk_lib.qk_rmsnorm_matmul_batch(probs, _x_dev(g1, cuda), EPS)
+    Wg, Wu = synth.q4k_weights(rng, synth.FFN, K), synth.q4k_weights(rng, synth.FFN, K)
+    yg = torch.empty(1, synth.FFN, dtype=torch.float16, device=cuda)
+    qk_lib.qk_rmsnorm_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x2, cuda), _x_dev(g2, cuda), EPS, yg,
+                                        1, synth.FFN, K)
+    qk_lib.qk_get_device_status()
+    for p, ref in zip(probs, refs):
+        check_close(p["y"].cpu().numpy().astype(np.float64), ref, "rmsnorm " + p["qtype"])
+    check_close_f16out(yg.float().cpu().numpy().astype(np.float64),
+                       oracle.rmsnorm_gateup_swiglu(Wg, Wu, x2, g2, EPS, synth.FFN, K), "rmsnorm gate/up M1")
+
+
+def test_rmsnorm_prefill_gateup_m1024(qk_lib, cuda):
+    """Config 2 behind its RMSNorm: M = 1024 through the scratch and the GEMM
+    (sampled output features)."""
+    import torch
+    rng = synth.rng_for(94, 0)
+    M, N, K = 1024, synth.FFN, synth.HIDDEN
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, M, K)
+    g = gamma_vec(rng, K)
+    sc = scratch_for(qk_lib, [("q4k", M, K, True)], cuda)
+    assert sc is not None and sc.numel() * 2 == M * K * 2
+    y = torch.empty(M, N, dtype=torch.float16, device=cuda)
+    qk_lib.qk_rmsnorm_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), _x_dev(g, cuda), EPS, y, M,
+                                        N, K, scratch=sc)
+    qk_lib.qk_get_device_status()
+    rows = sample_rows(N, 48, 94)
+    ref = oracle.rmsnorm_gateup_swiglu(Wg, Wu, x, g, EPS, N, K, rows=rows)
+    check_close_f16out(y.float().cpu().numpy().astype(np.float64)[:, rows], ref, "rmsnorm gate/up M1024")
+
+
+def test_rmsnorm_rejects_missing_scratch_and_bad_arguments(qk_lib, cuda):
+    import torch
+    L = qk_lib.lib()
+    M, N, K = 64, 128, 512
+    W = torch.zeros(N * 2 * 144, dtype=torch.uint8, device=cuda)
+    x = torch.zeros(M * K, dtype=torch.float16, device=cuda)
+    g = torch.ones(K, dtype=torch.float16, device=cuda)
+    y = torch.zeros(M * N, dtype=torch.float32, device=cuda)
+    sc = torch.zeros(M * K, dtype=torch.float16, device=cuda)
+    s = torch.cuda.current_stream().cuda_stream
+    args = lambda gm, eps, scr, yy: (W.data_ptr(), x.data_ptr(), gm, eps, scr, yy, M, N, K, s)
+    assert L.qk_rmsnorm_matmul_q4k(*args(g.data_ptr(), 1e-5, None, y.data_ptr())) == -1      # GEMM needs scratch
+    assert L.qk_rmsnorm_matmul_q4k(*args(None, 1e-5, sc.data_ptr(), y.data_ptr())) == -1     # no gamma
+    assert L.qk_rmsnorm_matmul_q4k(*args(g.data_ptr(), -1.0, sc.data_ptr(), y.data_ptr())) == -3
+    assert L.qk_rmsnorm_matmul_q4k(*args(g.data_ptr(), float("nan"), sc.data_ptr(), y.data_ptr())) == -3
+    assert L.qk_rmsnorm_matmul_q4k(*args(g.data_ptr(), 1e-5, x.data_ptr(), y.data_ptr())) == -7  # scratch = x
+    assert L.qk_rmsnorm_matmul_q4k(*args(g.data_ptr(), 1e-5, sc.data_ptr(), y.data_ptr())) == 0
+    assert L.qk_get_device_status(s) == 0
