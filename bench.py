@@ -410,11 +410,16 @@ def roof(flops, nbytes, ms, pk):
 
 
 def timed(torch, stream, fn, reps, flush):
-    """CUDA-event time of fn() on `stream`, each run after an L2 flush."""
+    """CUDA-event time of fn() on `stream`, each run after an L2 flush: a write
+    of the whole flush buffer, then a read of its first half, so that L2 holds
+    clean lines (write-backs of a dirty L2 would otherwise load the timed
+    kernel's first microseconds)."""
     ms = []
+    half = flush[: flush.numel() // 2].view(torch.int32)
     with torch.cuda.stream(stream):
         for i in range(reps + 2):
             flush.fill_(i & 0xFF)
+            half.sum()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             fn()
@@ -585,9 +590,10 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
                               {"weight_bytes": wbytes})
         del xk, yn
     out["model_sweep"] = sweep
-    out["note"] = ("each kernel timed alone with CUDA events, a %d MB write flushing L2 before every run "
-                   "(the sweep's 1.9 GiB of weights exceed L2); attainable = min(bf16 peak, intensity x HBM)"
-                   % (L2_FLUSH_BYTES >> 20))
+    out["note"] = ("each kernel timed alone with CUDA events; before every run L2 is flushed by a %d MB write "
+                   "followed by a %d MB read (so it holds clean lines); the sweep's 1.9 GiB of weights exceed L2 "
+                   "(one pass per run, 197 launches); attainable = min(bf16 peak, intensity x HBM)"
+                   % (L2_FLUSH_BYTES >> 20, L2_FLUSH_BYTES >> 21))
     del Wm
     torch.cuda.empty_cache()
     return out

@@ -76,15 +76,23 @@ qk_status qk_dequant_q4k(const void *blocks, int64_t n_blocks, float *out, qk_st
 qk_status qk_dequant_q6k(const void *blocks, int64_t n_blocks, float *out, qk_stream_t stream);
 
 /*
+ * Number range of the two paths.  The GEMV (M <= 16) applies the block scales
+ * in fp32.  The tensor-core GEMM forms every weight in fp16: fp16(d*sc),
+ * fp16(dmin*m) and fp16(q*d*sc - dmin*m), each rounded from fp32; a block
+ * whose |d*sc*q| or |dmin*m| exceeds 65504 gives +-inf weights there (the
+ * synthetic and real Llama scales are near 1e-4).  A non-finite d or dmin
+ * makes its row's outputs non-finite on every path, as in the fp32 definition.
+ */
+
+/*
  * y[m][n] = sum_k x[m][k] * w[n][k] for Q4_K weights W (N x K), fp16 x, fp32 y
  * (DAMASCUS project overview, "[01] the thesis" / "[04] one decode step";
  * "Building DAMASCUS", "Prefill and decode need different performance
- * questions").  M = 1 runs the decode GEMV (products of the integer quants
- * with fp16 x are exact, sums fp32, block scales applied per sub-block in
- * fp32) where its shared-memory plan fits K (see qk_decode_uses_gemv: every
- * K up to 6144 and K = 8192 do, in both formats and for gate/up); larger M,
- * and an M = 1 problem whose K the GEMV cannot stage, runs the tensor-core
- * GEMM (weights dequantized to fp16 in
+ * questions").  M <= 16 runs the GEMV (products of the integer quants with
+ * fp16 x are exact, sums fp32, block scales applied per sub-block in fp32)
+ * where its shared-memory plan fits (see qk_uses_gemv: the model's K = 3072
+ * up to M = 16, K = 8192 up to M = 8); larger M, and problems the GEMV cannot
+ * stage, run the tensor-core GEMM (weights dequantized to fp16 in
  * shared or tensor memory, never written to device memory; fp32 accumulation
  * in tensor memory),
  * the overview's prefill plan in which dequantized weights feed the matrix
@@ -136,15 +144,15 @@ typedef struct qk_matmul_desc {
 /*
  * Run `count` independent problems (DAMASCUS project overview, "[04] one
  * decode step": the QKV projections share x, gate and up share x, and every
- * decode-step linear is an M = 1 GEMV).  Problems with M = 1 are executed
- * together, up to 8 per kernel launch and as long as their joint
- * shared-memory plan fits (x is staged for the largest K of a launch), so
- * small GEMVs share one launch and stream their weights concurrently; other
- * problems, and M = 1 problems the GEMV cannot stage at all, run as in
- * qk_matmul_q4k / qk_matmul_q6k / qk_gateup_swiglu_q4k.  Each entry obeys the
- * rules of its single-problem entry point; in addition no y may overlap any
- * input or output of another entry.  count = 0 is a no-op.  Results are
- * identical to calling the single-problem entry points one by one.
+ * decode-step linear is an M = 1 GEMV).  Problems the GEMV runs (M <= 16)
+ * share launches, up to 8 per launch, with the problems of the same
+ * token-slot class (M = 1; 2..8; 9..16), so small GEMVs stream their weights
+ * concurrently; each keeps its own shared-memory plan and split over warps.
+ * Other problems run as in qk_matmul_q4k / qk_matmul_q6k /
+ * qk_gateup_swiglu_q4k.  Each entry obeys the rules of its single-problem
+ * entry point; in addition no y may overlap any input or output of another
+ * entry.  count = 0 is a no-op.  Results are bit-identical to calling the
+ * single-problem entry points one by one.
  */
 qk_status qk_matmul_batch(const qk_matmul_desc *descs, int count, qk_stream_t stream);
 
@@ -210,10 +218,9 @@ qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream);
  * Host-only query (no CUDA call): 1 if an M = 1 problem in format `qtype`
  * (QK_Q4_K / QK_Q6_K; with gateup != 0 the fused gate/up + SwiGLU, Q4_K only)
  * and inner size K runs on the decode GEMV, 0 if it runs on the tensor-core
- * GEMM because the GEMV cannot stage it (x of K plus two weight stages must
- * fit in shared memory), -1 for an invalid qtype or K.  The answer depends
- * only on these arguments; grouped calls (qk_matmul_batch) launch problems
- * together only while their joint plan fits.
+ * GEMM because the GEMV cannot stage it (the x table of K plus two weight
+ * stages must fit in shared memory), -1 for an invalid qtype or K.  The
+ * answer depends only on these arguments.
  */
 int qk_decode_uses_gemv(int qtype, int gateup, int64_t K);
 

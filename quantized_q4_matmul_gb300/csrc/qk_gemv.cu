@@ -559,6 +559,7 @@ struct GemvProb {
   uint32_t stage_bytes;
   uint32_t ctl_off, red_off, ring_off;  // shared-memory layout of this problem's CTAs
   uint32_t red_bytes;                   // several tokens: bytes of one partials buffer (of two)
+  uint32_t rawx_off, gamma_off;         // where the bulk copies of x and gamma land
   int tiles, cta_begin, ctas;
 };
 
@@ -571,6 +572,7 @@ struct Ctl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint64_t red_free[2];       // several tokens: the partials buffer of tile parity p has been summed
+  uint64_t x_full;            // x (and gamma) copied into shared memory
   uint32_t done[kMaxStages];  // warps that finished the tile whose last chunk used this stage (or parity)
   uint32_t abort_flag;
   float rnorm[kMaxGemvM];     // RMSNorm prologue: 1 / sqrt(mean(x^2) + eps) per token
@@ -579,42 +581,28 @@ struct Ctl {
 constexpr uint32_t kCtlBytes = round128(sizeof(Ctl));
 
 // RMSNorm prologue (DAMASCUS project overview, "[04] one decode step": an
-// RMSNorm comes before the QKV projections and the SwiGLU FFN).  Every
-// compute thread sums the squares of its 8-value chunks c = tid, tid + 32kW,
-// ... of every token (loads of all tokens issued together), the warps reduce
-// them in a fixed shuffle tree into rss[m][warp], and after a barrier thread m
-// adds the warps in order: rnorm[m] = 1 / sqrt(mean_k x[m][k]^2 + eps), fp32.
-__device__ void rms_partials(const uint16_t* __restrict__ x, int M, int K, float (*rss)[kW], int tid) {
+// RMSNorm comes before the QKV projections and the SwiGLU FFN), over x staged
+// in shared memory at xs: every compute thread sums the squares of its 8-value
+// chunks c = tid, tid + 32kW, ... of each token, the warps reduce them in a
+// fixed shuffle tree into rss[m][warp], and after a barrier thread m adds the
+// warps in order: rnorm[m] = 1 / sqrt(mean_k x[m][k]^2 + eps), fp32.
+__device__ void rms_partials(uint32_t xs, int M, int K, float (*rss)[kW], int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   const int nc = K / 8;
-  float ss[kMaxGemvM];
+  for (int m = 0; m < M; ++m) {
+    float ss = 0.f;
+    for (int c = tid; c < nc; c += 32 * kW) {
+      const uint4 v = lds128(xs + (uint32_t)m * (uint32_t)(2 * K) + 16u * c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-  for (int m = 0; m < kMaxGemvM; ++m) ss[m] = 0.f;
-  for (int c = tid; c < nc; c += 32 * kW) {
-    uint4 v[kMaxGemvM];
-#pragma unroll
-    for (int m = 0; m < kMaxGemvM; ++m)
-      if (m < M) v[m] = ldg_stream16(x + (size_t)m * K + 8 * c);
-#pragma unroll
-    for (int m = 0; m < kMaxGemvM; ++m) {
-      if (m < M) {
-        const uint32_t w[4] = {v[m].x, v[m].y, v[m].z, v[m].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float a = half_lo(w[i]), b = half_lo(w[i] >> 16);
-          ss[m] = fmaf(b, b, fmaf(a, a, ss[m]));
-        }
+      for (int i = 0; i < 4; ++i) {
+        const float a = half_lo(w[i]), b = half_lo(w[i] >> 16);
+        ss = fmaf(b, b, fmaf(a, a, ss));
       }
     }
-  }
 #pragma unroll
-  for (int m = 0; m < kMaxGemvM; ++m) {
-    if (m < M) {
-      float t = ss[m];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-      if (lane == 0) rss[m][warp] = t;
-    }
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) rss[m][warp] = ss;
   }
 }
 
@@ -628,15 +616,16 @@ __device__ __forceinline__ uint2 norm4(uint2 v, uint2 g, float r) {
   return o;
 }
 
-// Build the x table and the sums table of one problem from x in device memory
-// (all compute threads; the caller synchronises them afterwards).
+// Build the x table and the sums table of one problem from x staged in shared
+// memory at xs (gs: gamma staged there too, or 0 for no RMSNorm prologue; all
+// compute threads; the caller synchronises them afterwards).
 //   Q4_K entry (block, word v, lane group t, e): base k = 64t + 32e + 4v.
 //   Q6_K entry (block, v = 4h + 2P + u, t, e):   base k = 128h + 64P + 32e + 8t + 4u.
 // An entry holds x[k], x[k+2] / x[k+1], x[k+3] as fp16 pairs: for e = 0 in
 // words 0 and 2 (B half 0 of the MMAs p = 0, 1), for e = 1 in words 1 and 3.
 template <int QT>
-__device__ void build_x_table(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma, const float* rnorm,
-                              int K, uint32_t xt, uint32_t sx, uint32_t zero, int tid) {
+__device__ void build_x_table(uint32_t xs, uint32_t gs, const float* rnorm, int K, uint32_t xt, uint32_t sx,
+                              uint32_t zero, int tid) {
   const int nb = K / kQK;
   const int nent = nb * 64;  // entries, each from 4 consecutive x values
   for (int i = tid; i < nent; i += 32 * kW) {
@@ -661,8 +650,9 @@ __device__ void build_x_table(const uint16_t* __restrict__ x, const uint16_t* __
       k = 128 * h + 64 * P + 32 * e + 8 * t + 4 * u;
       dst = xt + (uint32_t)blk * kXtBlock + 128u * v + 32u * t + 16u * e;
     }
-    uint2 q = ldg_stream8(x + (size_t)blk * kQK + k);
-    if (gamma) q = norm4(q, ldg_stream8(gamma + (size_t)blk * kQK + k), rnorm[0]);
+    const uint32_t off = 2u * (uint32_t)(blk * kQK + k);
+    uint2 q = lds64(xs + off);
+    if (gs) q = norm4(q, lds64(gs + off), rnorm[0]);
     const uint32_t p0 = prmt(q.x, q.y, 0x5410u), p1 = prmt(q.x, q.y, 0x7632u);  // (x0, x2), (x1, x3)
     if (e == 0)
       sts128_u(dst, p0, 0u, p1, 0u);
@@ -690,21 +680,22 @@ __device__ void build_x_table(const uint16_t* __restrict__ x, const uint16_t* __
   for (int i = tid; i < (int)(kZeroBytes / 16); i += 32 * kW) sts128_u(zero + 16u * i, 0u, 0u, 0u, 0u);
 }
 
-// Several tokens: token m's x as k-permuted fp16 pairs, xp_m[k/4] = { (x[k],
-// x[k+2]), (x[k+1], x[k+3]) } (2K bytes per token), and the sums table
+// Several tokens: token m's x (bulk-copied to xt + 2K m) rearranged in place
+// into k-permuted fp16 pairs, xp_m[k/4] = { (x[k], x[k+2]), (x[k+1], x[k+3]) },
+// and the sums table
 // [block][sub-block (Q4_K, 32 weights) or scale group (Q6_K, 16)][MT tokens]
 // (zero for tokens beyond M).
 template <int QT, int MT>
-__device__ void build_x_table_tn(const uint16_t* __restrict__ x, const uint16_t* __restrict__ gamma,
-                                 const float* rnorm, int M, int K, uint32_t xt, uint32_t sx, uint32_t zero, int tid) {
+__device__ void build_x_table_tn(uint32_t gs, const float* rnorm, int M, int K, uint32_t xt, uint32_t sx,
+                                 uint32_t zero, int tid) {
   constexpr int kSub = QT == kQ4K ? 8 : 16;      // sums per block
   constexpr int kPer = QT == kQ4K ? 8 : 4;       // 4-value groups per sum
   const int nq = K / 4;
   for (int i = tid; i < M * nq; i += 32 * kW) {  // nq is a multiple of 64: a warp never straddles tokens
     const int m = i / nq, q = i - m * nq;
-    uint2 v = ldg_stream8(x + (size_t)m * K + 4 * q);
-    if (gamma) v = norm4(v, ldg_stream8(gamma + 4 * q), rnorm[m]);
-    const uint32_t a = xt + (uint32_t)m * (uint32_t)(2 * K) + 8u * q;  // 8-byte entries
+    const uint32_t a = xt + (uint32_t)m * (uint32_t)(2 * K) + 8u * q;  // x copied here; rearranged in place
+    uint2 v = lds64(a);
+    if (gs) v = norm4(v, lds64(gs + 8u * q), rnorm[m]);
     asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(prmt(v.x, v.y, 0x5410u)),
                  "r"(prmt(v.x, v.y, 0x7632u))
                  : "memory");
@@ -893,6 +884,11 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uin
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // x (and gamma) first: one bulk copy each into shared memory
+      const uint32_t xbytes = (uint32_t)P.M * (uint32_t)(2 * K), gbytes = P.gamma ? (uint32_t)(2 * K) : 0u;
+      mbar_arrive_expect_tx(&ctl->x_full, xbytes + gbytes);
+      bulk_copy_g2s(smem + P.rawx_off, P.x, xbytes, &ctl->x_full);
+      if (gbytes) bulk_copy_g2s(smem + P.gamma_off, P.gamma, gbytes, &ctl->x_full);
       int st = 0;
       for (; st < steps; ++st) {
         const int s = st % S;
@@ -1092,6 +1088,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
   }
   if (threadIdx.x == 0) {
     ctl->abort_flag = 0;
+    mbar_init(&ctl->x_full, 1);
     mbar_init(&ctl->red_free[0], 1);
     mbar_init(&ctl->red_free[1], 1);
     ctl->done[0] = ctl->done[1] = 0u;  // several tokens: counters by tile parity
@@ -1101,8 +1098,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
   if (threadIdx.x < 32 * kW) {
     const uint32_t base = smem_u32(smem);
     const uint32_t zero = base + P.ctl_off - kZeroBytes;
+    const uint32_t xs = base + P.rawx_off, gs = P.gamma ? base + P.gamma_off : 0u;
+    mbar_wait(&ctl->x_full, 0u, &ctl->abort_flag, &g_gemv_status);
     if (P.gamma) {
-      rms_partials(P.x, P.M, P.K, ctl->rss, threadIdx.x);
+      rms_partials(xs, P.M, P.K, ctl->rss, threadIdx.x);
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
       if ((int)threadIdx.x < P.M) {
         float t = 0.f;
@@ -1114,15 +1113,15 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     if constexpr (MT == 1) {
       const uint32_t sx = base + (uint32_t)(P.K / kQK) * kXtBlock;
       if (P.qtype == kQ4K)
-        build_x_table<kQ4K>(P.x, P.gamma, ctl->rnorm, P.K, base, sx, zero, threadIdx.x);
+        build_x_table<kQ4K>(xs, gs, ctl->rnorm, P.K, base, sx, zero, threadIdx.x);
       else
-        build_x_table<kQ6K>(P.x, P.gamma, ctl->rnorm, P.K, base, sx, zero, threadIdx.x);
+        build_x_table<kQ6K>(xs, gs, ctl->rnorm, P.K, base, sx, zero, threadIdx.x);
     } else {
       const uint32_t sx = base + (uint32_t)MT * (uint32_t)(2 * P.K);
       if (P.qtype == kQ4K)
-        build_x_table_tn<kQ4K, MT>(P.x, P.gamma, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
+        build_x_table_tn<kQ4K, MT>(gs, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
       else
-        build_x_table_tn<kQ6K, MT>(P.x, P.gamma, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
+        build_x_table_tn<kQ6K, MT>(gs, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
   }
@@ -1146,6 +1145,16 @@ uint32_t gemv_take_status() {
 namespace {
 
 constexpr size_t kGemvSmem = 227 * 1024;
+// Stages the plan aims for before it grows a stage (see plan_problem).
+#ifndef QK_GEMV_MIN_STAGES
+#define QK_GEMV_MIN_STAGES 6
+#endif
+constexpr int kMinStages = QK_GEMV_MIN_STAGES;
+// Relative compute cost per packed byte, for splitting CTAs among the problems
+// of a grouped launch: a Q6_K byte carries 1.2 weights (a Q4_K byte 1.8) but
+// its 6-bit assembly and 16 scale groups cost ~1.4x the instructions per byte
+// (counted from the source of the two decode paths).
+constexpr double kQ6CostPerByte = 1.4;
 
 // The token slots of the kernel that runs M tokens: 1 (decode layout), 8 or 16.
 int slots_for(int64_t M) { return M <= 1 ? 1 : M <= 8 ? 8 : 16; }
@@ -1175,56 +1184,61 @@ bool plan_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
   const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
   const int nten = 1 + P.kind;
   const int64_t RB = (int64_t)nb * bb;
+  // Layout: [x table | sums | zero region | control | partials | x | gamma | ring].
+  // Several tokens copy x straight into the x table's rows (rearranged in place).
   const size_t xt = mt == 1 ? round128((size_t)nb * (kXtBlock + sx_block_bytes(P.qtype)))
                             : round128((size_t)mt * 2 * P.K + (size_t)nb * (P.qtype == kQ4K ? 8 : 16) * mt * 4);
   P.ctl_off = (uint32_t)(xt + kZeroBytes);
   P.red_off = P.ctl_off + kCtlBytes;
-  // The decode layout keeps a partials slot per stage; several tokens keep
-  // two buffers (tile parity) sized for the stage's tensors.
+  const size_t rawx = mt == 1 ? round128((size_t)2 * P.K) : 0;
+  const size_t gam = P.gamma ? round128((size_t)2 * P.K) : 0;
+  // the decode layout keeps a partials slot per stage; several tokens keep two
+  // buffers (tile parity) sized for the stage's tensors
   const size_t red_stage = mt == 1 ? red_slot_bytes() : 0;
-  auto red_fixed_for = [&](int ten) { return mt == 1 ? (size_t)0 : round128((size_t)2 * red_tn_bytes(mt, ten)); };
-  auto avail_for = [&](int ten) -> size_t {
-    const size_t fixed = (size_t)P.red_off + red_fixed_for(ten) + 128 + 128;  // + slack past the last block
-    return fixed >= kGemvSmem ? 0 : kGemvSmem - fixed;
+  const size_t red_fixed = mt == 1 ? 0 : round128((size_t)2 * red_tn_bytes(mt, nten));
+  const size_t fixed = (size_t)P.red_off + red_fixed + rawx + gam + 128 + 128;  // + rounding, + slack past a block
+  if (fixed >= kGemvSmem) return false;
+  const size_t avail = kGemvSmem - fixed;
+  auto stages_for = [&](size_t stage_bytes) {
+    return (int)std::min<size_t>(kMaxStages, avail / (stage_bytes + red_stage));
   };
-  size_t avail = avail_for(nten);
-  if (avail == 0) return false;
-  auto per_stage = [&](size_t stage_bytes) { return stage_bytes + red_stage; };
-  // Stage: whole rows (cb = K/256) when three stages fit, else the largest
-  // chunk of cb blocks dividing K/256 (rows 16-byte aligned in device memory,
-  // cb blocks a multiple of 16 bytes: any cb for Q4_K, multiples of 8 for
-  // Q6_K) that gives three stages, else two.
-  int cb = nb;
-  if (3 * per_stage(round128((size_t)16 * nten * nb * bb)) > avail) {
-    cb = 0;
-    for (int want = 3; want >= 2 && cb == 0; --want)
-      for (int c = 1; c <= nb; ++c)
-        if (nb % c == 0 && (c * bb) % 16 == 0 && (RB % 16) == 0 &&
-            (size_t)want * per_stage(round128((size_t)16 * nten * c * bb)) <= avail)
-          cb = c;
-    if (cb == 0) cb = nb;  // whole rows with fewer stages (checked below)
+  // Stage geometry: 16 rows x cb blocks per tensor.  Bytes in flight per SM
+  // hide the HBM latency only when several stages stream while the warps work
+  // on one or two, so the stage is the largest chunk (cb dividing K/256, rows
+  // 16-byte aligned in device memory and cb blocks a multiple of 16 bytes:
+  // any cb for Q4_K, multiples of 8 for Q6_K, or whole rows) that still gives
+  // six stages, else three, else two.
+  int cb = 0, S = 0;
+  for (int want : {kMinStages, 3, 2}) {
+    for (int c = nb; c >= 1 && cb == 0; --c) {
+      if (nb % c != 0) continue;
+      if (c != nb && ((c * bb) % 16 != 0 || (RB % 16) != 0)) continue;
+      const int st = stages_for(round128((size_t)16 * nten * c * bb));
+      if (st >= want) {
+        cb = c;
+        S = st;
+      }
+    }
+    if (cb) break;
   }
+  if (cb == 0) return false;
   P.cb = cb;
-  // One tensor with whole rows: two adjacent tiles per stage (halves the
-  // per-block share of the per-tile reduction) when two such stages fit.
-  P.pair = (P.kind == 0 && cb == nb && P.N > 16 && 2 * per_stage(round128((size_t)32 * nb * bb)) <= avail_for(2))
-               ? 1
-               : 0;
-  if (P.pair) avail = avail_for(2);
-  P.stage_bytes = round128((size_t)16 * (nten + P.pair) * cb * bb);
-  P.stages = (int)std::min<size_t>(kMaxStages, avail / per_stage(P.stage_bytes));
-  if (P.stages < 2) return false;
-  P.red_bytes = mt == 1 ? 0u : red_tn_bytes(mt, nten + P.pair);
-  P.ring_off = P.red_off + (uint32_t)(mt == 1 ? round128((size_t)P.stages * red_stage) : red_fixed_for(nten + P.pair));
-  P.tiles = (P.N + 16 * (1 + P.pair) - 1) / (16 * (1 + P.pair));
-  *smem_out = (size_t)P.ring_off + (size_t)P.stages * P.stage_bytes + 128 + 128;  // + base alignment + slack
+  P.pair = 0;
+  P.stage_bytes = round128((size_t)16 * nten * cb * bb);
+  P.stages = S;
+  P.red_bytes = mt == 1 ? 0u : red_tn_bytes(mt, nten);
+  P.rawx_off = mt == 1 ? (uint32_t)(P.red_off + round128((size_t)S * red_stage)) : 0u;
+  P.gamma_off = (uint32_t)(P.red_off + (mt == 1 ? round128((size_t)S * red_stage) + rawx : red_fixed));
+  P.ring_off = (uint32_t)(P.gamma_off + gam);
+  P.tiles = (P.N + 15) / 16;
+  *smem_out = (size_t)P.ring_off + (size_t)S * P.stage_bytes + 128 + 128;  // + base alignment + slack
   return *smem_out <= kGemvSmem;
 }
 
 // One grouped GEMV launch (problems of the same token-slot count): every
 // problem keeps its own plan, the launch takes the largest shared-memory size,
 // and the CTAs (one per SM, `sms` of them) split across problems in proportion
-// to their weight bytes.
+// to their weight bytes times the format's compute cost per byte.
 bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* smem_out) {
   if (count <= 0 || count > kMaxGemvProbs) return false;
   GemvBatch& B = *out;
@@ -1239,7 +1253,8 @@ bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* sm
     if (!plan_problem(d[i], B.p[i], &s)) return false;
     smem = std::max(smem, s);
     const int bb = B.p[i].qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
-    bytes[i] = (int64_t)B.p[i].N * (B.p[i].K / kQK) * bb * (1 + B.p[i].kind);
+    const double cost = B.p[i].qtype == kQ4K ? 1.0 : kQ6CostPerByte;
+    bytes[i] = (int64_t)((double)B.p[i].N * (B.p[i].K / kQK) * bb * (1 + B.p[i].kind) * cost);
     total += (double)bytes[i];
   }
   *smem_out = smem;

@@ -28,3 +28,20 @@ def cuda(qk_lib):
         pytest.skip("no CUDA device")
     torch.cuda.set_device(0)
     return torch.device("cuda:0")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """The achieved max|err| / rms of every parity check of the session, worst
+    first (the bar is 1e-2)."""
+    try:
+        from tests import test_gpu_parity
+    except Exception:
+        return
+    margins = getattr(test_gpu_parity, "MARGINS", [])
+    if not margins:
+        return
+    worst = sorted(margins, key=lambda m: -m[1])
+    terminalreporter.write_line("parity margins: %d checks, max|err|/rms worst %.2e, median %.2e (bar 1e-2)" % (
+        len(margins), worst[0][1], sorted(m[1] for m in margins)[len(margins) // 2]))
+    for what, r in worst[:12]:
+        terminalreporter.write_line("  %.2e  %s" % (r, what))

@@ -160,7 +160,7 @@ def test_decode_kernel_choice_on_the_host(qk_lib):
     # (144 bytes) chunk at any block count
     assert not use("q6k", 7424) and not use("q6k", 8448)
     assert use("q4k", 5888, True) and use("q4k", 10496) and use("q4k", 32768)
-    assert use("q6k", 32768)
+    assert not use("q6k", 32768) and use("q6k", 16384)
     L = qk_lib.lib()
     # several tokens (2 <= M <= 16) run on the GEMV too while the x table of M
     # tokens fits: the model's K = 3072 up to 16 tokens, K = 8192 up to 8
