@@ -58,6 +58,7 @@ typedef int qk_status;
 #define QK_ERR_UNSUPPORTED_DEVICE (-6) /* the current device is not an sm_103 GPU */
 #define QK_ERR_ALIAS (-7)              /* the output overlaps an input */
 #define QK_ERR_POINTER (-8)            /* a pointer is not accessible from the current device */
+#define QK_ERR_SCRATCH (-9)            /* the built-in scratch of qk_rmsnorm_matmul_batch_static is too small */
 
 /* A cudaStream_t, spelled without CUDA headers. */
 typedef struct CUstream_st *qk_stream_t;
@@ -188,6 +189,31 @@ qk_status qk_rmsnorm_matmul_q6k(const void *blocks, const uint16_t *x_f16, const
 qk_status qk_rmsnorm_gateup_swiglu_q4k(const void *gate_blocks, const void *up_blocks, const uint16_t *x_f16,
                                        const uint16_t *gamma_f16, float eps, void *scratch, uint16_t *y_f16,
                                        int64_t M, int64_t N_ff, int64_t K, qk_stream_t stream);
+
+/*
+ * qk_rmsnorm_matmul_batch without a scratch argument, for callers that cannot
+ * allocate device memory: code running while a CUDA graph is being captured
+ * (an allocation there is not recorded into the graph), callers inside a
+ * framework whose memory pool owns the GPU's memory, and real-time loops that
+ * allocate nothing after start-up because cudaMalloc can block and
+ * synchronise the device.  The paper has no counterpart of this entry point:
+ * it is a convenience of this library, not part of the method.
+ *
+ * The normalized activations of problems the tensor-core GEMM runs go to a
+ * fixed 8 MiB array inside the library instead (every GPU that loads the
+ * library holds it until the process exits): the largest M * K over those
+ * problems must be at most 4,194,304 (M * K * 2 bytes <= 8 MiB), else the call
+ * returns QK_ERR_SCRATCH and enqueues nothing.  The call allocates nothing and
+ * calls no allocating routine.  Every call shares the array and it keeps the
+ * last call's contents (each call overwrites what it reads), so calls whose
+ * work may overlap on the GPU -- on different streams, or from several host
+ * threads -- race on it; serialise them.  The first call on a device that
+ * needs the array looks up its device address (cudaGetSymbolAddress, with
+ * that device current) and keeps it; make that first call before capturing
+ * any stream.  Otherwise as qk_rmsnorm_matmul_batch.
+ */
+qk_status qk_rmsnorm_matmul_batch_static(const qk_matmul_desc *descs, int count, const uint16_t *gamma_f16, float eps,
+                                         qk_stream_t stream);
 
 /*
  * Host-only query: bytes of scratch an M-token problem of this format and K

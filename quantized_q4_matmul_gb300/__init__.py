@@ -19,7 +19,8 @@ __all__ = [
     "QKError", "lib", "lib_path", "qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k",
     "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout",
     "qk_decode_uses_gemv", "qk_uses_gemv", "qk_gemm_plan", "qk_rmsnorm_matmul_batch", "qk_rmsnorm_matmul_q4k",
-    "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
+    "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes",
+    "qk_rmsnorm_matmul_batch_static", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
     "qk_gemm_plan_info",
 ]
 
@@ -29,7 +30,8 @@ QK_BLOCK_BYTES = {"q4k": 144, "q6k": 210}
 SYMBOLS = ("qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k", "qk_gateup_swiglu_q4k",
            "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout", "qk_decode_uses_gemv",
            "qk_uses_gemv", "qk_gemm_plan", "qk_rmsnorm_matmul_batch", "qk_rmsnorm_matmul_q4k",
-           "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes", "qk_status_string",
+           "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes",
+    "qk_rmsnorm_matmul_batch_static", "qk_status_string",
            "qk_version")
 
 QK_Q4_K, QK_Q6_K = 0, 1
@@ -94,6 +96,8 @@ def lib():
         L.qk_rmsnorm_gateup_swiglu_q4k.restype = i32
         L.qk_rmsnorm_gateup_swiglu_q4k.argtypes = [vp, vp, vp, vp, f32, vp, vp, i64, i64, i64, vp]
         L.qk_rmsnorm_scratch_bytes.restype, L.qk_rmsnorm_scratch_bytes.argtypes = i64, [i32, i32, i64, i64]
+        L.qk_rmsnorm_matmul_batch_static.restype = i32
+        L.qk_rmsnorm_matmul_batch_static.argtypes = [ctypes.POINTER(qk_matmul_desc), i32, vp, f32, vp]
         L.qk_gemm_plan.restype = i32
         L.qk_gemm_plan.argtypes = [i32, i32, i64, i64, i64, ctypes.POINTER(qk_gemm_plan_info)]
         L.qk_status_string.restype, L.qk_status_string.argtypes = ctypes.c_char_p, [i32]
@@ -251,6 +255,19 @@ def qk_rmsnorm_matmul_batch(problems, gamma_f16, eps: float, scratch=None, strea
     g = _buf(gamma_f16, 2 * K, what + ": gamma_f16", _F16)
     sc = _scratch(problems, scratch, what)
     _check(lib().qk_rmsnorm_matmul_batch(arr, len(problems), g, float(eps), sc, _stream(stream)), what)
+
+
+def qk_rmsnorm_matmul_batch_static(problems, gamma_f16, eps: float, stream=None) -> None:
+    """qk_rmsnorm_matmul_batch for callers that cannot allocate device memory
+    (a CUDA graph being captured, a framework whose pool owns the GPU, a loop
+    that must not block in cudaMalloc): the scratch is a fixed 8 MiB array in
+    the library, shared by every call, so calls that may overlap on the GPU
+    race on it.  Problems needing more scratch raise QKError (QK_ERR_SCRATCH)."""
+    what = "qk_rmsnorm_matmul_batch_static"
+    arr = _descs(problems)
+    K = max([int(p["K"]) for p in problems] or [0])
+    g = _buf(gamma_f16, 2 * K, what + ": gamma_f16", _F16)
+    _check(lib().qk_rmsnorm_matmul_batch_static(arr, len(problems), g, float(eps), _stream(stream)), what)
 
 
 def _rms_single(name, qtype, blocks, up_blocks, x_f16, gamma_f16, eps, scratch, y, M, N, K, stream):

@@ -372,6 +372,32 @@ qk_status qk_rmsnorm_gateup_swiglu_q4k(const void* gate_blocks, const void* up_b
   return qk_rmsnorm_matmul_batch(&d, 1, gamma_f16, eps, scratch, stream);
 }
 
+qk_status qk_rmsnorm_matmul_batch_static(const qk_matmul_desc* descs, int count, const uint16_t* gamma_f16, float eps,
+                                         qk_stream_t stream) {
+  if (count < 0) return QK_ERR_SHAPE;
+  if (count == 0) return QK_OK;
+  if (!descs) return QK_ERR_NULL;
+  int64_t need = 0;
+  for (int i = 0; i < count; ++i) {
+    if (descs[i].qtype != QK_Q4_K && descs[i].qtype != QK_Q6_K) return QK_ERR_SHAPE;
+    if (descs[i].M < 0 || descs[i].N < 0 || descs[i].K <= 0 || descs[i].K % qk::kQK != 0 ||
+        descs[i].M > kMaxM || descs[i].N >= kMaxDim || descs[i].K >= kMaxDim)
+      return QK_ERR_SHAPE;
+    need = std::max(need, norm_scratch_bytes(descs[i]));
+  }
+  if (need > (int64_t)qk::kStaticScratchBytes) return QK_ERR_SCRATCH;
+  void* scratch = nullptr;
+  if (need > 0) {
+    const qk_status st = check_device();
+    if (st != QK_OK) return st;
+    if (qk::static_scratch_address(&scratch) != cudaSuccess) {
+      cudaGetLastError();
+      return QK_ERR_CUDA;
+    }
+  }
+  return rmsnorm_matmul_batch(descs, count, gamma_f16, eps, scratch, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int64_t qk_rmsnorm_scratch_bytes(int qtype, int gateup, int64_t M, int64_t K) {
   if ((qtype != QK_Q4_K && qtype != QK_Q6_K) || (gateup && qtype != QK_Q4_K)) return -1;
   if (K <= 0 || K % qk::kQK != 0 || K >= kMaxDim || M < 0 || M > kMaxM) return -1;
@@ -435,6 +461,7 @@ const char* qk_status_string(qk_status status) {
     case QK_ERR_UNSUPPORTED_DEVICE: return "QK_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
     case QK_ERR_ALIAS: return "QK_ERR_ALIAS: the output overlaps an input";
     case QK_ERR_POINTER: return "QK_ERR_POINTER: a pointer is not accessible from the current device";
+    case QK_ERR_SCRATCH: return "QK_ERR_SCRATCH: the problems need more than the library's 8 MiB built-in scratch";
     default: return "unknown qk_status";
   }
 }

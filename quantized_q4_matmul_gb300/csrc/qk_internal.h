@@ -67,6 +67,11 @@ bool gemm_plan(QType t, bool gateup, int64_t M, int64_t N, GemmPlanInfo* info);
 cudaError_t launch_rmsnorm_rows(const uint16_t* x, const uint16_t* gamma, float eps, uint16_t* out, int64_t M,
                                 int64_t K, cudaStream_t s);
 
+// The built-in scratch of qk_rmsnorm_matmul_batch_static (bytes) and its
+// device address on the current device (looked up once per device).
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+cudaError_t static_scratch_address(void** out);
+
 // A kernel whose single bounded wait can never complete (see qk_debug_wait_timeout).
 cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t s);
 

@@ -14,6 +14,8 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "qk_device.cuh"
 #include "qk_internal.h"
 
@@ -96,6 +98,29 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_rows_kernel(const uint16
 }
 
 }  // namespace
+
+// Scratch of qk_rmsnorm_matmul_batch_static, the entry point that allocates
+// nothing: the normalized activations of the problems the tensor-core GEMM
+// runs.  A file-scope array of fixed size that every GPU loading the library
+// holds until the process exits; every call shares it.
+static __device__ __align__(256) uint16_t g_static_scratch[kStaticScratchBytes / 2];
+
+// The device address of g_static_scratch on the current device.  In host code
+// the array's name is only a host-side stand-in, so its address comes from
+// cudaGetSymbolAddress, once per device with that device current, and is kept.
+cudaError_t static_scratch_address(void** out) {
+  static std::atomic<void*> cache[kMaxDevices];
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  void* p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return e;
+    cache[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return cudaSuccess;
+}
 
 cudaError_t launch_rmsnorm_rows(const uint16_t* x, const uint16_t* gamma, float eps, uint16_t* out, int64_t M,
                                 int64_t K, cudaStream_t s) {
