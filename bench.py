@@ -488,8 +488,8 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
     fns = {"q4k": qk.qk_matmul_q4k, "q6k": qk.qk_matmul_q6k}
 
     def kernel_of(qtype, M, K, gateup=False):
-        if M == 1 and qk.qk_decode_uses_gemv(qtype, K, gateup):
-            return "gemv_stream_kernel (decode GEMV)"
+        if qk.qk_uses_gemv(qtype, M, K, gateup):
+            return "gemv_decode_kernel (decode GEMV)" if M == 1 else "gemv_stream_kernel (several-token GEMV)"
         return "gemm_tc_kernel (tcgen05 GEMM)"
 
     # config 0: attn_q, M = 16
@@ -515,7 +515,7 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
     layer_bytes = sum(lin_bytes(l, 1) for l in lins)
     layer_flops = sum(2.0 * l.N * l.K for l in lins)
     ms = timed(torch, stream, lambda: qk.qk_matmul_batch(probs, s), reps, flush)
-    grouped = entry("decode layer, grouped", layer_flops, layer_bytes, ms, "gemv_stream_kernel, one launch")
+    grouped = entry("decode layer, grouped", layer_flops, layer_bytes, ms, "gemv_decode_kernel, one launch")
 
     def chain():
         qk.qk_matmul_batch(probs[0:3], s)
@@ -526,7 +526,7 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
     cbytes = layer_bytes - lin_bytes(lins[5], 1) - lin_bytes(lins[4], 1) + lin_bytes(lins[4], 1, gateup=True)
     ms = timed(torch, stream, chain, reps, flush)
     chained = entry("decode layer, chained", layer_flops, cbytes, ms,
-                    "gemv_stream_kernel, 4 launches: {q,k,v} -> o -> gate/up+SwiGLU -> down")
+                    "gemv_decode_kernel, 4 launches: {q,k,v} -> o -> gate/up+SwiGLU -> down")
     out["decode_layer_m1"] = {"grouped": grouped, "chained": chained, "per_linear": per}
     del Ws, xs, ys, probs
 

@@ -535,6 +535,13 @@ constexpr uint32_t kBackoffNs = QK_GEMV_BACKOFF_NS;
 #endif
 constexpr bool kFirstWait = QK_GEMV_FIRST_WAIT != 0;
 constexpr int kProducerWarp = kW;
+// Compute warps per CTA of the decode (M = 1) kernel; one more warp streams.
+#ifndef QK_DECODE_WARPS
+#define QK_DECODE_WARPS 12
+#endif
+constexpr int kDW = QK_DECODE_WARPS;
+constexpr int kDCompute = 32 * kDW;
+constexpr int kDThreads = 32 * (kDW + 1);
 constexpr int kThreads = 32 * (kW + 1);
 constexpr int kMaxStages = 8;
 constexpr uint32_t kXtBlock = 1024;  // x-table bytes per 256-weight block
@@ -586,12 +593,13 @@ constexpr uint32_t kCtlBytes = round128(sizeof(Ctl));
 // chunks c = tid, tid + 32kW, ... of each token, the warps reduce them in a
 // fixed shuffle tree into rss[m][warp], and after a barrier thread m adds the
 // warps in order: rnorm[m] = 1 / sqrt(mean_k x[m][k]^2 + eps), fp32.
-__device__ void rms_partials(uint32_t xs, int M, int K, float (*rss)[kW], int tid) {
+template <int NW>
+__device__ void rms_partials(uint32_t xs, int M, int K, float* rss, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   const int nc = K / 8;
   for (int m = 0; m < M; ++m) {
     float ss = 0.f;
-    for (int c = tid; c < nc; c += 32 * kW) {
+    for (int c = tid; c < nc; c += 32 * NW) {
       const uint4 v = lds128(xs + (uint32_t)m * (uint32_t)(2 * K) + 16u * c);
       const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -602,7 +610,7 @@ __device__ void rms_partials(uint32_t xs, int M, int K, float (*rss)[kW], int ti
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) rss[m][warp] = ss;
+    if (lane == 0) rss[m * NW + warp] = ss;
   }
 }
 
@@ -628,7 +636,7 @@ __device__ void build_x_table(uint32_t xs, uint32_t gs, const float* rnorm, int 
                               uint32_t zero, int tid) {
   const int nb = K / kQK;
   const int nent = nb * 64;  // entries, each from 4 consecutive x values
-  for (int i = tid; i < nent; i += 32 * kW) {
+  for (int i = tid; i < nent; i += kDCompute) {
     int blk, t, e, v, k;
     uint32_t dst;
     if constexpr (QT == kQ4K) {
@@ -677,7 +685,7 @@ __device__ void build_x_table(uint32_t xs, uint32_t gs, const float* rnorm, int 
       }
     }
   }
-  for (int i = tid; i < (int)(kZeroBytes / 16); i += 32 * kW) sts128_u(zero + 16u * i, 0u, 0u, 0u, 0u);
+  for (int i = tid; i < (int)(kZeroBytes / 16); i += kDCompute) sts128_u(zero + 16u * i, 0u, 0u, 0u, 0u);
 }
 
 // Several tokens: token m's x (bulk-copied to xt + 2K m) rearranged in place
@@ -876,7 +884,6 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uin
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint8_t* const w0 = P.w[0];
   const uint8_t* const w1 = P.w[1];
-  void* const yout = P.y;
   Ctl* ctl = reinterpret_cast<Ctl*>(smem + P.ctl_off);
   volatile uint32_t* abort_flag = &ctl->abort_flag;
   uint8_t* ring = smem + P.ring_off;
@@ -947,129 +954,7 @@ __device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uin
   }
 
   // -------------------------------------------------------------- compute
-  if constexpr (MT > 1) {
-    compute_tn<QT, MT>(P, smem, t0, t1, steps, nchunks, nten, tile_rows, ten_bytes, RB);
-    return;
-  }
-  Lane L;
-  L.g = lane >> 2;
-  L.tig = lane & 3;
-  {
-    const int e = L.g & 1;
-    const bool reads_x = (L.g >> 1) == L.tig;  // column g takes x from lane group t = g >> 1 only
-    // Zero-region offset: a 16-byte chunk of the 128-byte line other than the
-    // two the x-reading lanes of this lane's quarter-warp use (no bank conflict).
-    L.xt_off = reads_x ? 32u * (uint32_t)L.tig + 16u * (uint32_t)e : 32u * (uint32_t)(((L.g >> 1) + 2) & 3);
-    L.xt_stride = reads_x ? kXtBlock : 0u;
-  }
-  L.hi = L.tig >= 2;
-  L.sh = 16u * (uint32_t)(L.tig & 1);
-  L.shA = L.sh + (L.hi ? 2u : 0u);
-  L.shL = L.sh + (L.hi ? 4u : 0u);
-  {
-    const uint32_t s = (uint32_t)(L.tig >> 1);
-    L.sel0 = 0x7440u | s;        // byte s: the scale of field 2P
-    L.sel1 = 0x7440u | (s + 2);  // byte s + 2: the scale of field 2P + 1
-  }
-  const uint32_t base = smem_u32(smem);
-  const bool reads_x = L.xt_stride != 0;
-  const uint32_t xt_lane = (reads_x ? base : base + P.ctl_off - kZeroBytes) + L.xt_off;
-  const uint32_t sx_base = base + (uint32_t)nb * kXtBlock + 16u * (uint32_t)L.tig;
-  const uint32_t ring_s = base + P.ring_off;
-  uint32_t magic, fmagic;
-  asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
-  asm volatile("mov.b32 %0, %1;" : "=r"(fmagic) : "n"(kFMagic));
-  const uint32_t pitch = (cb == nb) ? (uint32_t)RB : (uint32_t)(cb * kBB);  // bytes per row inside a stage
-  const int upt = nten * nb;        // units (one tensor's 16 rows x one block) per tile
-  const int ups = nten * cb;        // units per stage
-  float ya0 = 0.f, ya1 = 0.f, yb0 = 0.f, yb1 = 0.f;  // rows g, g+8 of tensor 0 (a) and 1 (b)
-  bool ok = true;
-  for (int st = 0; st < steps; ++st) {
-    const int s = st % S;
-    const int tl = st / nchunks, chunk = st % nchunks;
-    // After a timed-out wait the warp skips the arithmetic but still takes
-    // part in every tile's hand-off, so no other warp is left waiting.
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, abort_flag, &g_gemv_status));
-    const uint32_t stg = ring_s + (uint32_t)s * SB + (uint32_t)L.g * pitch;
-    // Units are dealt to the warps round robin over the problem's tiles:
-    // U = tile * upt + chunk * ups + (t * cb + b), warp w takes U = w mod kW.
-    // The global tile index makes a tile's split over warps (and so its
-    // rounding) independent of how tiles are spread over CTAs.
-    const int U0 = (int)(((int64_t)(t0 + tl) * upt + (int64_t)chunk * ups) % kW);
-    int v = (warp - U0 + kW) % kW;
-    for (; ok && v < ups; v += kW) {
-      const int t = v >= cb ? 1 : 0, b = v - t * cb;
-      const uint32_t r0 = stg + (uint32_t)t * ten_bytes + (uint32_t)(b * kBB);
-      const uint32_t r1 = r0 + 8u * pitch;
-      const int blk = chunk * cb + b;
-      const uint32_t xa = xt_lane + (uint32_t)blk * L.xt_stride;
-      const uint32_t sxa = sx_base + (uint32_t)blk * sx_block_bytes(QT);
-      float y0 = 0.f, y1 = 0.f;
-      if constexpr (QT == kQ4K) {
-        q4_block(r0, r1, xa, sxa, L, magic, fmagic, y0, y1);
-      } else {
-        q6_block(r0, r1, xa, sxa, L, magic, fmagic, y0, y1);
-      }
-      if (t == 0) {
-        ya0 += y0;
-        ya1 += y1;
-      } else {
-        yb0 += y0;
-        yb1 += y1;
-      }
-    }
-    __syncwarp();
-    if (chunk == nchunks - 1) {
-      // Tile done: sum the four lanes of each row, hand the warp's partials to
-      // the last warp to finish the tile, which adds them in warp order.
-      float* red = reinterpret_cast<float*>(smem + P.red_off + (size_t)s * red_slot_bytes());
-      for (int t = 0; t < nten; ++t) {
-        float a = t ? yb0 : ya0, c = t ? yb1 : ya1;
-        a += __shfl_xor_sync(0xffffffffu, a, 1);
-        a += __shfl_xor_sync(0xffffffffu, a, 2);
-        c += __shfl_xor_sync(0xffffffffu, c, 1);
-        c += __shfl_xor_sync(0xffffffffu, c, 2);
-        if (L.tig == 0) {
-          red[(warp * 2 + t) * 16 + L.g] = a;
-          red[(warp * 2 + t) * 16 + L.g + 8] = c;
-        }
-      }
-      ya0 = ya1 = yb0 = yb1 = 0.f;
-      __threadfence_block();
-      __syncwarp();
-      uint32_t prev = 0;
-      if (lane == 0) {
-        prev = atomicAdd(&ctl->done[s], 1u);
-        __threadfence_block();
-      }
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      __syncwarp();
-      if (prev == (uint32_t)(kW - 1)) {
-        const int tile = t0 + tl;
-        if (kind == 1) {
-          if (lane < 16) {
-            const int n = tile * 16 + lane;
-            float gs = 0.f, us = 0.f;
-            for (int w = 0; w < kW; ++w) gs += red[(w * 2 + 0) * 16 + lane];
-            for (int w = 0; w < kW; ++w) us += red[(w * 2 + 1) * 16 + lane];
-            if (n < N) static_cast<__half*>(yout)[n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
-          }
-        } else if (lane < 16 * nten) {  // lane 16t + r: row r of tile t of the stage
-          const int t = lane >> 4, r = lane & 15;
-          const int n = tile * tile_rows + 16 * t + r;
-          float gs = 0.f;
-          for (int w = 0; w < kW; ++w) gs += red[(w * 2 + t) * 16 + r];
-          if (n < N) static_cast<float*>(yout)[n] = gs;
-        }
-        __syncwarp();
-        if (lane == 0) ctl->done[s] = 0u;
-      }
-      __syncwarp();
-    }
-    // Release the stage (after the reduction: its partials slot is reused
-    // only once the producer has refilled this stage).
-    if (lane == 0) mbar_arrive(&ctl->empty[s]);
-  }
+  compute_tn<QT, MT>(P, smem, t0, t1, steps, nchunks, nten, tile_rows, ten_bytes, RB);
 }
 
 template <int MT>
@@ -1101,7 +986,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     const uint32_t xs = base + P.rawx_off, gs = P.gamma ? base + P.gamma_off : 0u;
     mbar_wait(&ctl->x_full, 0u, &ctl->abort_flag, &g_gemv_status);
     if (P.gamma) {
-      rms_partials(xs, P.M, P.K, ctl->rss, threadIdx.x);
+      rms_partials<kW>(xs, P.M, P.K, &ctl->rss[0][0], threadIdx.x);
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
       if ((int)threadIdx.x < P.M) {
         float t = 0.f;
@@ -1110,13 +995,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
       }
       asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
     }
-    if constexpr (MT == 1) {
-      const uint32_t sx = base + (uint32_t)(P.K / kQK) * kXtBlock;
-      if (P.qtype == kQ4K)
-        build_x_table<kQ4K>(xs, gs, ctl->rnorm, P.K, base, sx, zero, threadIdx.x);
-      else
-        build_x_table<kQ6K>(xs, gs, ctl->rnorm, P.K, base, sx, zero, threadIdx.x);
-    } else {
+    {
       const uint32_t sx = base + (uint32_t)MT * (uint32_t)(2 * P.K);
       if (P.qtype == kQ4K)
         build_x_table_tn<kQ4K, MT>(gs, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
@@ -1129,6 +1008,260 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
     run_gemv_problem<kQ4K, MT>(P, cta, smem);
   else
     run_gemv_problem<kQ6K, MT>(P, cta, smem);
+}
+
+// ---------------------------------------------------------------------------
+// Decode (M = 1)
+// ---------------------------------------------------------------------------
+// A producer warp streams stages into a ring with bulk copies of whole
+// 16-row tiles (two adjacent tiles of one tensor, or the gate and the up tile,
+// per stage), or of 16-row x cb-block chunks with one copy per row: a few
+// large copies per stage keep the copy engine and DRAM efficient.  A unit is
+// 16 rows x one 256-weight block of one tensor; compute warp w takes the
+// units of block j = w, w + kDW, ... of every tile, so each warp's share of a
+// tile is fixed by j alone.  A warp adds its units in j order, leaves its 16
+// row sums of a finished tile in the stage's partials slot, and releases the
+// stage.  Before refilling a stage the producer adds the kDW warps' sums of
+// the tile(s) it held, in warp order, and writes y (fp32, or fp16
+// silu(gate) * up).  No atomic and no barrier among compute warps: each only
+// waits for its stage to land.  The order of every addition depends on the
+// problem's shape only, so a problem launched alone or grouped gives the same
+// bits.
+constexpr int kDMaxStages = 8;
+
+struct DecodeCtl {
+  uint64_t full[kDMaxStages];   // stage landed (producer arrival + copy bytes)
+  uint64_t empty[kDMaxStages];  // stage released by the kDW compute warps
+  uint64_t x_full;              // x (and gamma) copied into shared memory
+  uint32_t abort_flag;
+  float rnorm;
+  float rss[kDW];
+};
+
+__device__ __forceinline__ float quad_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v + __shfl_xor_sync(0xffffffffu, v, 2);
+}
+
+// Stage geometry of a decode problem (P.pair: two tiles of one tensor per
+// stage; P.cb: blocks per stage and row, nb for whole rows).
+template <int QT>
+__device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8_t* smem) {
+  constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
+  const int K = P.K, N = P.N, nb = K / kQK, cb = P.cb, S = P.stages;
+  const int nten = 1 + P.kind, pair = P.pair;
+  const int ncomb = pair ? 2 : nten;  // row sets per stage: two tiles, or gate and up
+  const int64_t RB = (int64_t)nb * kBB;
+  const int nchunks = nb / cb;
+  const uint32_t SB = P.stage_bytes;
+  const uint32_t comb_bytes = (uint32_t)(16 * cb * kBB);  // one row set's share of a stage
+  const uint32_t pitch = cb == nb ? (uint32_t)RB : (uint32_t)(cb * kBB);
+  const int tps = pair ? 2 : 1;  // tiles per stage
+  const int t0 = (int)((int64_t)cta * P.tiles / P.ctas), t1 = (int)((int64_t)(cta + 1) * P.tiles / P.ctas);
+  const int groups = (t1 - t0 + tps - 1) / tps;  // stages' worth of tiles
+  const int steps = groups * nchunks;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  DecodeCtl* ctl = reinterpret_cast<DecodeCtl*>(smem + P.ctl_off);
+  const uint32_t base = smem_u32(smem);
+  uint8_t* const ring = smem + P.ring_off;
+  float* const red = reinterpret_cast<float*>(smem + P.red_off);  // [S][kDW][2][16]
+  void* const yout = P.y;
+
+  if (tid < S) {
+    mbar_init(&ctl->full[tid], 1);
+    mbar_init(&ctl->empty[tid], kDW);
+  }
+  if (tid == 0) {
+    ctl->abort_flag = 0u;
+    mbar_init(&ctl->x_full, 1);
+  }
+  fence_mbar_init();
+  __syncthreads();
+
+  if (warp == kDW) {
+    // ------------------------------------------------------------ producer
+    // Lane 0 copies; all lanes add the partial sums of finished tiles.
+    auto finish = [&](int st) {  // the tile(s) of step st, if its chunk was the last
+      const int s = st % S, g = st / nchunks;
+      if (st % nchunks != nchunks - 1) return;
+      const float* q = red + (size_t)s * (kDW * 32);
+      const int c = lane >> 4, r = lane & 15;
+      const int tile = t0 + g * tps + (pair ? c : 0);
+      const int n = tile * 16 + r;
+      if (nten == 2) {
+        if (lane < 16 && n < N) {
+          float gs = 0.f, us = 0.f;
+          for (int w = 0; w < kDW; ++w) gs += q[w * 32 + r];
+          for (int w = 0; w < kDW; ++w) us += q[w * 32 + 16 + r];
+          static_cast<__half*>(yout)[n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
+        }
+      } else if ((pair || c == 0) && tile < t1 && n < N) {
+        float v = 0.f;
+        for (int w = 0; w < kDW; ++w) v += q[w * 32 + c * 16 + r];
+        static_cast<float*>(yout)[n] = v;
+      }
+    };
+    bool ok = true;
+    if (lane == 0) {
+      const uint32_t xbytes = (uint32_t)(2 * K), gbytes = P.gamma ? (uint32_t)(2 * K) : 0u;
+      mbar_arrive_expect_tx(&ctl->x_full, xbytes + gbytes);
+      bulk_copy_g2s(smem + P.rawx_off, P.x, xbytes, &ctl->x_full);
+      if (gbytes) bulk_copy_g2s(smem + P.gamma_off, P.gamma, gbytes, &ctl->x_full);
+    }
+    for (int st = 0; st < steps; ++st) {
+      const int s = st % S;
+      if (st >= S) {
+        ok = ok && mbar_wait<kBackoffNs>(&ctl->empty[s], (uint32_t)((st / S) - 1) & 1u, &ctl->abort_flag,
+                                          &g_gemv_status);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        finish(st - S);
+        __syncwarp();
+      }
+      if (lane == 0) {
+        // The compute warps read the stage with plain loads; the refill is an
+        // async-proxy write, ordered after their reads by this fence.
+        fence_proxy_async_smem();
+        const int g = st / nchunks, chunk = st % nchunks;
+        const int n0 = (t0 + g * tps) * 16;
+        uint8_t* dst = ring + (size_t)s * SB;
+        if (cb == nb) {
+          // whole rows: a tensor's rows n0 .. n0 + rows - 1 are one span
+          const int rows = min(16 * tps, min(t1 * 16, N) - n0);
+          const int64_t span = (int64_t)rows * RB;
+          const uint32_t bulk = (uint32_t)(span & ~int64_t(15));
+          mbar_expect_tx(&ctl->full[s], bulk * (uint32_t)nten);
+          for (int t = 0; t < nten; ++t) {
+            const uint8_t* src = (t ? P.w[1] : P.w[0]) + (int64_t)n0 * RB;
+            uint8_t* d = dst + (size_t)t * comb_bytes;
+            if (bulk) bulk_copy_g2s(d, src, bulk, &ctl->full[s]);
+            for (int64_t b = bulk; b < span; b += 2)  // the tensor's last bytes (span % 16 != 0)
+              *reinterpret_cast<uint16_t*>(d + b) = *reinterpret_cast<const uint16_t*>(src + b);
+          }
+        } else {
+          // a K chunk: one copy per row of cb blocks (16-byte aligned by construction)
+          const int rows = min(16, N - n0);
+          const uint32_t row_bytes = (uint32_t)(cb * kBB);
+          mbar_expect_tx(&ctl->full[s], row_bytes * (uint32_t)(rows * nten));
+          for (int t = 0; t < nten; ++t)
+            for (int r = 0; r < rows; ++r)
+              bulk_copy_g2s(dst + (size_t)t * comb_bytes + (size_t)r * row_bytes,
+                            (t ? P.w[1] : P.w[0]) + (int64_t)(n0 + r) * RB + (int64_t)chunk * cb * kBB, row_bytes,
+                            &ctl->full[s]);
+        }
+        mbar_arrive(&ctl->full[s]);
+      }
+      __syncwarp();
+    }
+    // the last stages: wait for their release, then finish their tiles
+    for (int st = max(0, steps - S); ok && st < steps; ++st) {
+      ok = ok && mbar_wait<kBackoffNs>(&ctl->empty[st % S], (uint32_t)(st / S) & 1u, &ctl->abort_flag,
+                                        &g_gemv_status);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) finish(st);
+      __syncwarp();
+    }
+    if (lane == 0 && !ok) {
+      // drain: copies still in flight land before the CTA exits
+      for (int i = 1; i <= S && i <= steps; ++i)
+        mbar_wait(&ctl->full[(steps - i) % S], (uint32_t)((steps - i) / S) & 1u, &ctl->abort_flag, &g_gemv_status,
+                  true);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- compute
+  const uint32_t xs = base + P.rawx_off, gs = P.gamma ? base + P.gamma_off : 0u;
+  const uint32_t zero = base + P.ctl_off - kZeroBytes;
+  const uint32_t sxt = base + (uint32_t)nb * kXtBlock;
+  bool ok = mbar_wait(&ctl->x_full, 0u, &ctl->abort_flag, &g_gemv_status);
+  if (P.gamma) {
+    rms_partials<kDW>(xs, 1, K, ctl->rss, tid);
+    asm volatile("bar.sync 1, %0;" ::"n"(kDCompute) : "memory");
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < kDW; ++w) t += ctl->rss[w];
+      ctl->rnorm = 1.0f / sqrtf(t / (float)K + P.eps);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(kDCompute) : "memory");
+  }
+  build_x_table<QT>(xs, gs, &ctl->rnorm, K, base, sxt, zero, tid);
+  asm volatile("bar.sync 1, %0;" ::"n"(kDCompute) : "memory");
+
+  Lane L;
+  L.g = lane >> 2;
+  L.tig = lane & 3;
+  {
+    const int e = L.g & 1;
+    const bool reads_x = (L.g >> 1) == L.tig;
+    L.xt_off = reads_x ? 32u * (uint32_t)L.tig + 16u * (uint32_t)e : 32u * (uint32_t)(((L.g >> 1) + 2) & 3);
+    L.xt_stride = reads_x ? kXtBlock : 0u;
+  }
+  L.hi = L.tig >= 2;
+  L.sh = 16u * (uint32_t)(L.tig & 1);
+  L.shA = L.sh + (L.hi ? 2u : 0u);
+  L.shL = L.sh + (L.hi ? 4u : 0u);
+  {
+    const uint32_t sv = (uint32_t)(L.tig >> 1);
+    L.sel0 = 0x7440u | sv;
+    L.sel1 = 0x7440u | (sv + 2);
+  }
+  const uint32_t xt_lane = (L.xt_stride ? base : zero) + L.xt_off;
+  const uint32_t sx_lane = sxt + 16u * (uint32_t)L.tig;
+  uint32_t magic, fmagic;
+  asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
+  asm volatile("mov.b32 %0, %1;" : "=r"(fmagic) : "n"(kFMagic));
+  const uint32_t ring_s = base + P.ring_off + (uint32_t)L.g * pitch;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // rows g, g+8 of row set 0, then of row set 1
+  for (int st = 0; st < steps; ++st) {
+    const int s = st % S, chunk = st % nchunks;
+    if (ok) ok = mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, &ctl->abort_flag, &g_gemv_status);
+    // this warp's blocks of the chunk: j = chunk * cb + b with j mod kDW = warp
+    const int j0 = chunk * cb;
+    int b = warp - j0 % kDW;
+    if (b < 0) b += kDW;
+    const uint32_t stg = ring_s + (uint32_t)s * SB;
+    for (; ok && b < cb; b += kDW) {
+      const int j = j0 + b;
+      const uint32_t r0 = stg + (uint32_t)(b * kBB);
+      const uint32_t xa = xt_lane + (uint32_t)j * L.xt_stride;
+      const uint32_t sxa = sx_lane + (uint32_t)j * sx_block_bytes(QT);
+      if constexpr (QT == kQ4K) {
+        q4_block(r0, r0 + 8u * pitch, xa, sxa, L, magic, fmagic, a0, a1);
+        if (ncomb == 2) q4_block(r0 + comb_bytes, r0 + comb_bytes + 8u * pitch, xa, sxa, L, magic, fmagic, a2, a3);
+      } else {
+        q6_block(r0, r0 + 8u * pitch, xa, sxa, L, magic, fmagic, a0, a1);
+        if (ncomb == 2) q6_block(r0 + comb_bytes, r0 + comb_bytes + 8u * pitch, xa, sxa, L, magic, fmagic, a2, a3);
+      }
+    }
+    if (chunk == nchunks - 1) {
+      // tile(s) done: this warp's row sums to the stage's partials slot
+      const float p0 = quad_sum(a0), p1 = quad_sum(a1), p2 = quad_sum(a2), p3 = quad_sum(a3);
+      if (L.tig == 0) {
+        float* q = red + ((size_t)s * kDW + warp) * 32;
+        q[L.g] = p0;
+        q[L.g + 8] = p1;
+        q[16 + L.g] = p2;
+        q[16 + L.g + 8] = p3;
+      }
+      a0 = a1 = a2 = a3 = 0.f;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ctl->empty[s]);
+  }
+}
+
+__global__ void __launch_bounds__(kDThreads, 1) gemv_decode_kernel(const __grid_constant__ GemvBatch B) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  int i = 0;
+  while (i + 1 < B.count && (int)blockIdx.x >= B.p[i + 1].cta_begin) ++i;
+  const GemvProb& P = B.p[i];
+  const int cta = (int)blockIdx.x - P.cta_begin;
+  if (P.qtype == kQ4K)
+    decode_problem<kQ4K>(P, cta, smem);
+  else
+    decode_problem<kQ6K>(P, cta, smem);
 }
 
 }  // namespace
@@ -1147,7 +1280,7 @@ namespace {
 constexpr size_t kGemvSmem = 227 * 1024;
 // Stages the plan aims for before it grows a stage (see plan_problem).
 #ifndef QK_GEMV_MIN_STAGES
-#define QK_GEMV_MIN_STAGES 6
+#define QK_GEMV_MIN_STAGES 3
 #endif
 constexpr int kMinStages = QK_GEMV_MIN_STAGES;
 // Relative compute cost per packed byte, for splitting CTAs among the problems
@@ -1235,10 +1368,84 @@ bool plan_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
   return *smem_out <= kGemvSmem;
 }
 
+// The decode kernel's plan of one M = 1 problem, from its shape only.
+// Layout: [x table | sums | zero region | control | x | gamma | partials[S] |
+// ring[S]].  Stage geometry, first that fits: two adjacent whole tiles of one
+// tensor per stage with at least 3 stages; whole tiles (gate and up together)
+// with 3; the largest 16-byte-aligned chunk of cb blocks with 4, then 3; then
+// the same with 2 stages.
+bool plan_decode_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
+  memset(&P, 0, sizeof(P));
+  if (d.M != 1 || d.N <= 0 || d.N >= ((int64_t)1 << 31) || d.K <= 0 || d.K % kQK != 0 || d.K >= ((int64_t)1 << 31))
+    return false;
+  P.w[0] = static_cast<const uint8_t*>(d.w0);
+  P.w[1] = static_cast<const uint8_t*>(d.w1);
+  P.x = d.x;
+  P.y = d.y;
+  P.M = 1;
+  P.gamma = d.gamma;
+  P.eps = d.eps;
+  P.N = (int)d.N;
+  P.K = (int)d.K;
+  P.qtype = d.qtype;
+  P.kind = d.w1 ? 1 : 0;
+  const int nb = P.K / kQK, nten = 1 + P.kind;
+  const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
+  const int64_t RB = (int64_t)nb * bb;
+  P.tiles = (P.N + 15) / 16;
+  const size_t xt = round128((size_t)nb * (kXtBlock + sx_block_bytes(P.qtype)));
+  P.ctl_off = (uint32_t)(xt + kZeroBytes);
+  P.rawx_off = P.ctl_off + round128(sizeof(DecodeCtl));
+  P.gamma_off = P.rawx_off + round128((size_t)2 * P.K);
+  P.red_off = P.gamma_off + (P.gamma ? round128((size_t)2 * P.K) : 0);
+  const size_t red_stage = (size_t)kDW * 32 * sizeof(float);
+  const size_t fixed = (size_t)P.red_off + 128;  // + base alignment
+  if (fixed >= kGemvSmem) return false;
+  const size_t avail = kGemvSmem - fixed;
+  auto stages_for = [&](size_t stage_bytes) {
+    return (int)std::min<size_t>(kDMaxStages, avail / (round128(stage_bytes) + red_stage));
+  };
+  int cb = 0, S = 0, pair = 0;
+#ifndef QK_DECODE_PAIR
+#define QK_DECODE_PAIR 1
+#endif
+#ifndef QK_DECODE_MAXCB
+#define QK_DECODE_MAXCB 0
+#endif
+  for (int want : {3, 2}) {
+    if (QK_DECODE_MAXCB == 0 && QK_DECODE_PAIR && !P.kind && P.tiles >= 2 && stages_for((size_t)32 * RB) >= want) {
+      cb = nb, pair = 1, S = stages_for((size_t)32 * RB);
+      break;
+    }
+    if (QK_DECODE_MAXCB == 0 && stages_for((size_t)16 * RB * nten) >= want) {
+      cb = nb, S = stages_for((size_t)16 * RB * nten);
+      break;
+    }
+    for (int w2 : {want + 1, want}) {
+      for (int c = QK_DECODE_MAXCB ? std::min(nb - 1, QK_DECODE_MAXCB) : nb - 1; c >= 1 && !cb; --c) {
+        if (nb % c != 0 || (c * bb) % 16 != 0 || RB % 16 != 0) continue;
+        if (stages_for((size_t)16 * c * bb * nten) >= w2) cb = c, S = stages_for((size_t)16 * c * bb * nten);
+      }
+      if (cb) break;
+    }
+    if (cb) break;
+  }
+  if (!cb) return false;
+  P.cb = cb;
+  P.pair = pair;
+  P.stages = S;
+  P.stage_bytes = round128((size_t)16 * cb * bb * (pair ? 2 : nten));
+  P.ring_off = (uint32_t)(P.red_off + round128((size_t)S * red_stage));
+  *smem_out = (size_t)P.ring_off + (size_t)S * P.stage_bytes + 128;
+  return *smem_out <= kGemvSmem;
+}
+
 // One grouped GEMV launch (problems of the same token-slot count): every
-// problem keeps its own plan, the launch takes the largest shared-memory size,
-// and the CTAs (one per SM, `sms` of them) split across problems in proportion
-// to their weight bytes times the format's compute cost per byte.
+// problem keeps its own plan and the launch takes the largest shared-memory
+// size.  Decode: the CTAs (one per SM, `sms` of them) go one at a time to
+// the problem whose busiest CTA has the most work (tiles times tile bytes
+// times the format's compute cost per byte).  Several tokens: in proportion
+// to the weight bytes times that cost.
 bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* smem_out) {
   if (count <= 0 || count > kMaxGemvProbs) return false;
   GemvBatch& B = *out;
@@ -1247,10 +1454,11 @@ bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* sm
   double total = 0;
   int64_t bytes[kMaxGemvProbs];
   size_t smem = 0;
+  const bool decode = slots_for(d[0].M) == 1;
   for (int i = 0; i < count; ++i) {
     size_t s = 0;
     if (slots_for(d[i].M) != slots_for(d[0].M)) return false;
-    if (!plan_problem(d[i], B.p[i], &s)) return false;
+    if (decode ? !plan_decode_problem(d[i], B.p[i], &s) : !plan_problem(d[i], B.p[i], &s)) return false;
     smem = std::max(smem, s);
     const int bb = B.p[i].qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
     const double cost = B.p[i].qtype == kQ4K ? 1.0 : kQ6CostPerByte;
@@ -1259,6 +1467,33 @@ bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* sm
   }
   *smem_out = smem;
   const int budget = std::max(count, sms);
+  if (decode) {
+    double tile_cost[kMaxGemvProbs];
+    for (int i = 0; i < count; ++i) {
+      B.p[i].ctas = 1;
+      tile_cost[i] = (double)bytes[i] / B.p[i].tiles;
+    }
+    for (int used = count; used < budget; ++used) {
+      int best = -1;
+      double best_load = 0.0;
+      for (int i = 0; i < count; ++i) {
+        if (B.p[i].ctas >= B.p[i].tiles) continue;
+        const double load = (double)((B.p[i].tiles + B.p[i].ctas - 1) / B.p[i].ctas) * tile_cost[i];
+        if (load > best_load) {
+          best_load = load;
+          best = i;
+        }
+      }
+      if (best < 0) break;
+      ++B.p[best].ctas;
+    }
+    int begin = 0;
+    for (int i = 0; i < count; ++i) {
+      B.p[i].cta_begin = begin;
+      begin += B.p[i].ctas;
+    }
+    return true;
+  }
   int used = 0;
   for (int i = 0; i < count; ++i) {
     int c = (int)((double)budget * (double)bytes[i] / total);
@@ -1307,6 +1542,20 @@ cudaError_t launch_mt(const GemvBatch& B, size_t smem, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+cudaError_t launch_decode(const GemvBatch& B, size_t smem, cudaStream_t s) {
+  static PerDeviceFlag attr;
+  const int dev = current_device();
+  if (!attr.done(dev)) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
+    if (e != cudaSuccess) return e;
+    attr.mark(dev);
+  }
+  int ctas = 0;
+  for (int i = 0; i < B.count; ++i) ctas += B.p[i].ctas;
+  gemv_decode_kernel<<<ctas, kDThreads, smem, s>>>(B);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 bool gemv_plan_fits(const GemvDesc* d, int count) {
@@ -1323,7 +1572,7 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
   size_t smem = 0;
   if (!plan_gemv(d, count, device_sms(), &B, &smem)) return cudaErrorInvalidConfiguration;
   switch (slots_for(d[0].M)) {
-    case 1: return launch_mt<1>(B, smem, s);
+    case 1: return launch_decode(B, smem, s);
     case 8: return launch_mt<8>(B, smem, s);
     default: return launch_mt<16>(B, smem, s);
   }

@@ -144,23 +144,24 @@ def test_binding_checks_tensor_buffers_before_the_call(qk_lib):
 
 def test_decode_kernel_choice_on_the_host(qk_lib):
     """Which kernel an M = 1 problem runs on is decided on the host from the
-    GEMV's shared-memory plan (the x table of K plus two weight stages).  The
-    model's inner sizes stay on the GEMV; K values it cannot stage go to the
-    GEMM."""
+    decode GEMV's shared-memory plan: the x table and its sums (1088 bytes per
+    Q4_K block, 1152 per Q6_K block), x itself, and at least two stages of 16
+    rows, either whole rows (one bulk copy per tensor) or a chunk of cb blocks
+    per row whose copies start on 16-byte boundaries, in 227 KB.  Q4_K rows
+    chunk at any block count: K <= 35584 (gate/up 34816).  Q6_K blocks are 210
+    bytes, so a Q6_K row chunks only when its block count is a multiple of 8;
+    other Q6_K rows run on the GEMV while two whole 16-row tiles fit (up to
+    K = 6912) and on the GEMM beyond."""
     use = qk_lib.qk_decode_uses_gemv
-    for qt, gu in (("q4k", False), ("q6k", False), ("q4k", True)):
-        for K in range(256, 5632 + 1, 256):
+    for qt, gu, kmax in (("q4k", False, 35584), ("q4k", True, 34816)):
+        for K in list(range(256, 8192 + 1, 256)) + [kmax - 256, kmax]:
             assert use(qt, K, gu), (qt, gu, K)
-        for K in (6144, 8192, 16384):
-            assert use(qt, K, gu), (qt, gu, K)
-        # the x table alone (4.25-4.5 bytes per k) exceeds 227 KB
-        assert not use(qt, 65536, gu)
-    # Q6_K rows of an odd number of 8-block groups cannot be chunked 16-byte
-    # aligned, and whole 16-row tiles no longer fit three times; Q4_K blocks
-    # (144 bytes) chunk at any block count
-    assert not use("q6k", 7424) and not use("q6k", 8448)
-    assert use("q4k", 5888, True) and use("q4k", 10496) and use("q4k", 32768)
-    assert not use("q6k", 32768) and use("q6k", 16384)
+        for K in (kmax + 256, kmax + 512, 65536):
+            assert not use(qt, K, gu), (qt, gu, K)
+    for K in list(range(256, 6912 + 1, 256)) + [8192, 16384, 26624]:
+        assert use("q6k", K), K
+    for K in (7168, 8448, 9472, 16640, 28672, 65536):
+        assert not use("q6k", K), K
     L = qk_lib.lib()
     # several tokens (2 <= M <= 16) run on the GEMV too while the x table of M
     # tokens fits: the model's K = 3072 up to 16 tokens, K = 8192 up to 8

@@ -61,8 +61,11 @@ def check_close_f16out(got, ref, what):
     """As check_close for an fp16 output, with two bars:
     * the output format's own rounding (half an fp16 ulp of the value) allowed on
       top of the 1e-2 * rms bar, against the exact (fp64) oracle;
-    * 1e-2 * rms against the oracle rounded to fp16 itself, which leaves the
-      kernel's own arithmetic error (e.g. a fast sigmoid) nowhere to hide."""
+    * against the oracle rounded to fp16 itself: each output within 1e-2 * rms
+      or, where an fp16 ulp of the value is larger than that, within one ulp (an
+      exact value next to a rounding midpoint may round either way after the
+      kernel's fp32 sums).  A kernel arithmetic error such as a coarse sigmoid
+      shows as several ulps at the large outputs and fails it."""
     rms = float(np.sqrt(np.mean(ref ** 2)))
     mag = np.maximum(np.abs(ref), np.abs(got))
     half_ulp = np.ldexp(0.5, np.floor(np.log2(np.maximum(mag, 2.0 ** -14))).astype(np.int64) - 10)
@@ -71,9 +74,13 @@ def check_close_f16out(got, ref, what):
     worst = float(np.max(err - half_ulp)) if ref.size else 0.0
     assert worst <= TOL * rms, "%s: max(|err| - half_ulp) %.3e > %.0e * rms %.3e" % (what, worst, TOL, rms)
     ref16 = ref.astype(np.float16).astype(np.float64)
-    err16 = float(np.max(np.abs(got - ref16))) if ref.size else 0.0
-    assert err16 <= TOL * rms, "%s: max|err vs fp16(oracle)| %.3e > %.0e * rms %.3e" % (what, err16, TOL, rms)
-    MARGINS.append((what + " (vs fp16 oracle)", err16 / rms if rms else 0.0))
+    err16 = np.abs(got - ref16)
+    bar16 = np.maximum(TOL * rms, 2.0 * half_ulp)
+    over = float(np.max(err16 - bar16)) if ref.size else 0.0
+    assert over <= 0.0, "%s: |err vs fp16(oracle)| above max(%.0e * rms, 1 ulp) by %.3e (rms %.3e)" % (
+        what, TOL, over, rms)
+    small = err16[bar16 <= TOL * rms]
+    MARGINS.append((what + " (vs fp16 oracle)", float(np.max(small)) / rms if rms and small.size else 0.0))
 
 
 def sample_rows(N, n, seed):
@@ -507,6 +514,19 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable(qk_lib, cuda):
 # ---------------------------------------------------------------------------
 # M = 1 problems whose K the GEMV cannot stage run on the tensor-core GEMM
 # ---------------------------------------------------------------------------
+@pytest.mark.parametrize("qtype,N,K", [("q6k", 200, 6912), ("q6k", 70, 26624), ("q4k", 50, 35584), ("q4k", 33, 2304)])
+def test_decode_largest_k_on_the_gemv(qk_lib, cuda, qtype, N, K):
+    """K at the decode GEMV's limits: whole Q6_K rows of an odd block count
+    (rows 2 mod 4 bytes aligned), 8-block Q6_K chunks, 5-block Q4_K chunks,
+    and two-tile stages with an odd last tile."""
+    assert qk_lib.qk_decode_uses_gemv(qtype, K)
+    rng = synth.rng_for(43, K)
+    W = synth.weights(rng, qtype, N, K)
+    x = synth.activations(rng, 1, K)
+    ref = oracle.matmul(QT[qtype], W, x, N, K)
+    check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "%s M1 N%d K%d on the GEMV" % (qtype, N, K))
+
+
 @pytest.mark.parametrize("qtype,N,K", [("q6k", 200, 8448), ("q4k", 130, 65536)])
 def test_decode_fallback_to_gemm(qk_lib, cuda, qtype, N, K):
     assert not qk_lib.qk_decode_uses_gemv(qtype, K)
@@ -533,12 +553,13 @@ def test_decode_gateup_fallback_to_gemm(qk_lib, cuda):
 
 def test_batch_mixed_k_group(qk_lib, cuda):
     """M = 1 problems of different K share one launch (each keeps its own plan,
-    the launch takes the largest shared-memory size); a Q6_K at K = 8448 fits
-    no GEMV plan and runs on the GEMM.  Every result is bit-identical to its
-    single-problem call, since grouping never changes a problem's plan."""
+    the launch takes the largest shared-memory size); a Q6_K at K = 16640 and
+    a Q4_K at K = 36864 fit no GEMV plan and run on the GEMM.  Every result is
+    bit-identical to its single-problem call: the order of every addition
+    depends on the problem's shape only."""
     import torch
     assert qk_lib.qk_decode_uses_gemv("q4k", 6144, gateup=True) and qk_lib.qk_decode_uses_gemv("q6k", 16384)
-    assert not qk_lib.qk_decode_uses_gemv("q6k", 8448)
+    assert not qk_lib.qk_decode_uses_gemv("q6k", 16640) and not qk_lib.qk_decode_uses_gemv("q4k", 36864)
     rng = synth.rng_for(43, 0)
     probs, checks = [], []
     Wg, Wu = synth.q4k_weights(rng, 128, 6144), synth.q4k_weights(rng, 128, 6144)
@@ -547,7 +568,7 @@ def test_batch_mixed_k_group(qk_lib, cuda):
     Wgd, Wud, xgd = _dev(Wg, cuda), _dev(Wu, cuda), _x_dev(xg, cuda)
     probs.append(dict(qtype="q4k", blocks=Wgd, up_blocks=Wud, x_f16=xgd, y=yg, M=1, N=128, K=6144))
     singles = []
-    for qt, N, K in (("q6k", 64, 16384), ("q6k", 64, 8448), ("q4k", 256, 3072), ("q4k", 48, 32768)):
+    for qt, N, K in (("q6k", 64, 16384), ("q6k", 64, 16640), ("q4k", 256, 3072), ("q4k", 48, 36864)):
         W = synth.weights(rng, qt, N, K)
         x = synth.activations(rng, 1, K)
         y = torch.empty(1, N, dtype=torch.float32, device=cuda)
