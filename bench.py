@@ -430,6 +430,34 @@ def timed(torch, stream, fn, reps, flush):
     return ms
 
 
+L2_BYTES = 129 << 20
+
+
+def graph_steady(torch, stream, fns, R, reps):
+    """Per-call time of R calls (cycling over fns) captured in one CUDA graph,
+    one sample per replay: launch gaps as a captured decode loop sees them."""
+    with torch.cuda.stream(stream):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+        for i in range(R):
+            fns[i % len(fns)]()
+    ms = []
+    with torch.cuda.stream(stream):
+        for i in range(reps + 1):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            if i:
+                ms.append(e0.elapsed_time(e1) / R)
+    del g
+    return ms
+
+
 def lin_bytes(lin, M, gateup=False):
     """Packed weight bytes + fp16 x + output bytes of one linear at M tokens."""
     w = synth.weight_bytes(lin.qtype, lin.N, lin.K) * (2 if gateup else 1)
@@ -527,8 +555,37 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
     ms = timed(torch, stream, chain, reps, flush)
     chained = entry("decode layer, chained", layer_flops, cbytes, ms,
                     "gemv_decode_kernel, 4 launches: {q,k,v} -> o -> gate/up+SwiGLU -> down")
-    out["decode_layer_m1"] = {"grouped": grouped, "chained": chained, "per_linear": per}
-    del Ws, xs, ys, probs
+    # Steady state: R layers back to back in one CUDA graph over copies of the
+    # layer's weights that together exceed L2 (each layer reads its own copy),
+    # as a captured decode loop runs them.
+    ncopy = max(2, int(-(-2.5 * L2_BYTES // layer_bytes)))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(901)
+    sets = [[dict(p, blocks=device_weights(torch, gen, l.qtype, l.N, l.K, dev)) for p, l in zip(probs, lins)]
+            for _ in range(ncopy - 1)] + [probs]
+    ups = [device_weights(torch, gen, "q4k", lins[5].N, lins[5].K, dev) for _ in range(ncopy - 1)] + [Ws[5]]
+
+    def grouped_of(ps):
+        return lambda: qk.qk_matmul_batch(ps, s)
+
+    def chain_of(ps, wu):
+        gu = [dict(ps[4], up_blocks=wu, y=y_gu)]
+
+        def f():
+            qk.qk_matmul_batch(ps[0:3], s)
+            qk.qk_matmul_batch(ps[3:4], s)
+            qk.qk_matmul_batch(gu, s)
+            qk.qk_matmul_batch(ps[6:7], s)
+        return f
+
+    steady = {}
+    for name, mk, nbytes in (("grouped", lambda ps, wu: grouped_of(ps), layer_bytes), ("chained", chain_of, cbytes)):
+        ms = graph_steady(torch, stream, [mk(ps, wu) for ps, wu in zip(sets, ups)], 4 * ncopy, reps)
+        steady[name] = entry("decode layer, %s, steady" % name, layer_flops, nbytes, ms,
+                             "gemv_decode_kernel, %d layers per CUDA graph over %d weight copies (%d MB > L2)" % (
+                                 4 * ncopy, ncopy, ncopy * layer_bytes >> 20))
+    out["decode_layer_m1"] = {"grouped": grouped, "chained": chained, "per_linear": per, "steady": steady}
+    del Ws, xs, ys, probs, sets, ups
 
     # config 2: fused gate/up + SwiGLU at M = 1024
     g = synth.Linear("ffn_gate", synth.Q4K, synth.FFN, synth.HIDDEN)
@@ -571,22 +628,14 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
             for (_, l), W in zip(model, Wm):
                 fns[l.qtype](W, xk[l.K], yn[l.N], M, l.N, l.K, s)
 
-        with torch.cuda.stream(stream):
-            one_pass()
-        torch.cuda.synchronize()
-        ms = []
-        with torch.cuda.stream(stream):
-            for i in range(max(3, reps // 2)):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                one_pass()
-                e1.record(stream)
-                e1.synchronize()
-                ms.append(e0.elapsed_time(e1))
+        # one pass = 197 launches captured in a CUDA graph (2 GB of weights, far
+        # more than L2, so no flush is needed); the host's per-call cost would
+        # otherwise set the time at small M
+        ms = graph_steady(torch, stream, [one_pass], 1, max(3, reps // 2))
         flops = sum(2.0 * M * l.N * l.K for _, l in model)
         nbytes = sum(lin_bytes(l, M) for _, l in model)
         sweep[str(M)] = entry("model sweep M=%d" % M, flops, nbytes, ms,
-                              "%s, %d launches per pass" % (kernel_of("q4k", M, 3072), len(model)),
+                              "%s, %d launches per pass, one CUDA graph" % (kernel_of("q4k", M, 3072), len(model)),
                               {"weight_bytes": wbytes})
         del xk, yn
     out["model_sweep"] = sweep

@@ -1028,6 +1028,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
 // problem's shape only, so a problem launched alone or grouped gives the same
 // bits.
 constexpr int kDMaxStages = 8;
+#ifndef QK_DECODE_PDL
+#define QK_DECODE_PDL 1
+#endif
+#ifndef QK_DECODE_PIECE
+#define QK_DECODE_PIECE 8192
+#endif
+constexpr uint32_t kDPiece = QK_DECODE_PIECE;  // bytes per bulk copy of a whole-row stage
 
 struct DecodeCtl {
   uint64_t full[kDMaxStages];   // stage landed (producer arrival + copy bytes)
@@ -1102,6 +1109,63 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
       }
     };
     bool ok = true;
+    // Copies of step st into stage st % S, issued from several lanes at once
+    // (the copy engine works on several requests in parallel): whole rows as
+    // pieces of at most kDPiece bytes of each tensor's span, chunks as one row
+    // per lane.  The compute warps read a stage with plain loads; its refill
+    // is an async-proxy write, ordered after their reads by the proxy fence.
+    auto issue = [&](int st) {
+      const int s = st % S;
+      const int g = st / nchunks, chunk = st % nchunks;
+      const int n0 = (t0 + g * tps) * 16;
+      uint8_t* dst = ring + (size_t)s * SB;
+      if (cb == nb) {
+        // whole rows: a tensor's rows n0 .. n0 + rows - 1 are one span
+        const int rows = min(16 * tps, min(t1 * 16, N) - n0);
+        const int64_t span = (int64_t)rows * RB;
+        const uint32_t bulk = (uint32_t)(span & ~int64_t(15));
+        const int np = (int)((bulk + kDPiece - 1) / kDPiece);  // pieces per tensor
+        if (lane == 0) {
+          for (int t = 0; t < nten; ++t) {
+            const uint8_t* src = (t ? P.w[1] : P.w[0]) + (int64_t)n0 * RB;
+            uint8_t* d = dst + (size_t)t * comb_bytes;
+            for (int64_t b = bulk; b < span; b += 2)  // the tensor's last bytes (span % 16 != 0)
+              *reinterpret_cast<uint16_t*>(d + b) = *reinterpret_cast<const uint16_t*>(src + b);
+          }
+          mbar_arrive_expect_tx(&ctl->full[s], bulk * (uint32_t)nten);
+        }
+        __syncwarp();
+        for (int i = lane; i < np * nten; i += 32) {
+          const int t = i / np, pc = i - t * np;
+          const uint32_t o = (uint32_t)pc * kDPiece, len = min(kDPiece, bulk - o);
+          fence_proxy_async_smem();
+          bulk_copy_g2s(dst + (size_t)t * comb_bytes + o, (t ? P.w[1] : P.w[0]) + (int64_t)n0 * RB + o, len,
+                        &ctl->full[s]);
+        }
+      } else {
+        // a K chunk: one copy per row of cb blocks (16-byte aligned by construction)
+        const int rows = min(16, N - n0);
+        const uint32_t row_bytes = (uint32_t)(cb * kBB);
+        if (lane == 0) mbar_arrive_expect_tx(&ctl->full[s], row_bytes * (uint32_t)(rows * nten));
+        __syncwarp();
+        for (int i = lane; i < rows * nten; i += 32) {
+          const int t = i / rows, r = i - t * rows;
+          fence_proxy_async_smem();
+          bulk_copy_g2s(dst + (size_t)t * comb_bytes + (size_t)r * row_bytes,
+                        (t ? P.w[1] : P.w[0]) + (int64_t)(n0 + r) * RB + (int64_t)chunk * cb * kBB, row_bytes,
+                        &ctl->full[s]);
+        }
+      }
+    };
+    int issued = 0;
+#if QK_DECODE_PDL
+    // Launched as a programmatic dependent: the next kernel may be scheduled
+    // now (it waits for this grid before touching memory), and this warp, the
+    // only one that touches global memory, reads weights, x and gamma and
+    // writes y only after the grids this one depends on have finished.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
     if (lane == 0) {
       const uint32_t xbytes = (uint32_t)(2 * K), gbytes = P.gamma ? (uint32_t)(2 * K) : 0u;
       mbar_arrive_expect_tx(&ctl->x_full, xbytes + gbytes);
@@ -1118,39 +1182,8 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
         finish(st - S);
         __syncwarp();
       }
-      if (lane == 0) {
-        // The compute warps read the stage with plain loads; the refill is an
-        // async-proxy write, ordered after their reads by this fence.
-        fence_proxy_async_smem();
-        const int g = st / nchunks, chunk = st % nchunks;
-        const int n0 = (t0 + g * tps) * 16;
-        uint8_t* dst = ring + (size_t)s * SB;
-        if (cb == nb) {
-          // whole rows: a tensor's rows n0 .. n0 + rows - 1 are one span
-          const int rows = min(16 * tps, min(t1 * 16, N) - n0);
-          const int64_t span = (int64_t)rows * RB;
-          const uint32_t bulk = (uint32_t)(span & ~int64_t(15));
-          mbar_expect_tx(&ctl->full[s], bulk * (uint32_t)nten);
-          for (int t = 0; t < nten; ++t) {
-            const uint8_t* src = (t ? P.w[1] : P.w[0]) + (int64_t)n0 * RB;
-            uint8_t* d = dst + (size_t)t * comb_bytes;
-            if (bulk) bulk_copy_g2s(d, src, bulk, &ctl->full[s]);
-            for (int64_t b = bulk; b < span; b += 2)  // the tensor's last bytes (span % 16 != 0)
-              *reinterpret_cast<uint16_t*>(d + b) = *reinterpret_cast<const uint16_t*>(src + b);
-          }
-        } else {
-          // a K chunk: one copy per row of cb blocks (16-byte aligned by construction)
-          const int rows = min(16, N - n0);
-          const uint32_t row_bytes = (uint32_t)(cb * kBB);
-          mbar_expect_tx(&ctl->full[s], row_bytes * (uint32_t)(rows * nten));
-          for (int t = 0; t < nten; ++t)
-            for (int r = 0; r < rows; ++r)
-              bulk_copy_g2s(dst + (size_t)t * comb_bytes + (size_t)r * row_bytes,
-                            (t ? P.w[1] : P.w[0]) + (int64_t)(n0 + r) * RB + (int64_t)chunk * cb * kBB, row_bytes,
-                            &ctl->full[s]);
-        }
-        mbar_arrive(&ctl->full[s]);
-      }
+      issue(st);
+      ++issued;
       __syncwarp();
     }
     // the last stages: wait for their release, then finish their tiles
@@ -1163,8 +1196,8 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
     }
     if (lane == 0 && !ok) {
       // drain: copies still in flight land before the CTA exits
-      for (int i = 1; i <= S && i <= steps; ++i)
-        mbar_wait(&ctl->full[(steps - i) % S], (uint32_t)((steps - i) / S) & 1u, &ctl->abort_flag, &g_gemv_status,
+      for (int i = 1; i <= S && i <= issued; ++i)
+        mbar_wait(&ctl->full[(issued - i) % S], (uint32_t)((issued - i) / S) & 1u, &ctl->abort_flag, &g_gemv_status,
                   true);
     }
     return;
@@ -1284,10 +1317,14 @@ constexpr size_t kGemvSmem = 227 * 1024;
 #endif
 constexpr int kMinStages = QK_GEMV_MIN_STAGES;
 // Relative compute cost per packed byte, for splitting CTAs among the problems
-// of a grouped launch: a Q6_K byte carries 1.2 weights (a Q4_K byte 1.8) but
-// its 6-bit assembly and 16 scale groups cost ~1.4x the instructions per byte
-// (counted from the source of the two decode paths).
-constexpr double kQ6CostPerByte = 1.4;
+// of a grouped launch: a Q6_K block's 6-bit assembly takes ~1.4x the logic
+// instructions per byte of a Q4_K block, and a decode CTA streams Q6_K at
+// 0.5-0.75x its Q4_K rate (per-CTA timelines on GB300: 18-26 vs 34 GB/s);
+// 1.7 balanced the grouped decode layer best.
+#ifndef QK_Q6_COST
+#define QK_Q6_COST 1.7
+#endif
+constexpr double kQ6CostPerByte = QK_Q6_COST;
 
 // The token slots of the kernel that runs M tokens: 1 (decode layout), 8 or 16.
 int slots_for(int64_t M) { return M <= 1 ? 1 : M <= 8 ? 8 : 16; }
@@ -1552,8 +1589,27 @@ cudaError_t launch_decode(const GemvBatch& B, size_t smem, cudaStream_t s) {
   }
   int ctas = 0;
   for (int i = 0; i < B.count; ++i) ctas += B.p[i].ctas;
+#if QK_DECODE_PDL
+  // Programmatic dependent launch: the CTAs of this grid may be scheduled
+  // while the previous kernel on the stream finishes (they wait for it in
+  // griddepcontrol.wait before reading anything), which hides the launch
+  // and the set-up of consecutive decode calls.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ctas);
+  cfg.blockDim = dim3(kDThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_decode_kernel, B);
+  return e != cudaSuccess ? e : cudaGetLastError();
+#else
   gemv_decode_kernel<<<ctas, kDThreads, smem, s>>>(B);
   return cudaGetLastError();
+#endif
 }
 
 }  // namespace

@@ -77,7 +77,10 @@ cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t s);
 
 // Largest M the GEMV handles (M = 1 in the decode layout, 2..16 with the
 // tokens in the MMA columns); larger M goes to the tensor-core GEMM.
-constexpr int kMaxGemvM = 16;
+#ifndef QK_GEMV_MAX_M
+#define QK_GEMV_MAX_M 16
+#endif
+constexpr int kMaxGemvM = QK_GEMV_MAX_M;
 int gemv_max_m();
 // The kernel's token-slot count for M tokens (1, 8 or 16): problems share a
 // launch only with problems of the same count.

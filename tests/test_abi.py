@@ -198,3 +198,4 @@ def test_rmsnorm_rejects_bad_arguments_on_the_host(qk_lib):
     assert sb("q4k", 1, 3072) == 0 and sb("q6k", 16, 3072) == 0 and sb("q4k", 8, 8192, True) == 0
     assert sb("q4k", 17, 3072) == 17 * 3072 * 2 and sb("q6k", 1024, 8192) == 1024 * 8192 * 2
     assert L.qk_rmsnorm_scratch_bytes(1, 1, 4, 256) == -1 and L.qk_rmsnorm_scratch_bytes(0, 0, 4, 300) == -1
+

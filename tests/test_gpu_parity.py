@@ -589,6 +589,87 @@ def test_batch_mixed_k_group(qk_lib, cuda):
 
 
 # ---------------------------------------------------------------------------
+# Stream order around the decode kernel's programmatic dependent launch
+# ---------------------------------------------------------------------------
+def _long_kernel(cuda):
+    """A few hundred microseconds of unrelated work on the current stream."""
+    import torch
+    buf = torch.empty(256 << 20, dtype=torch.uint8, device=cuda)
+    return lambda: buf.fill_(7)
+
+
+def test_decode_reads_x_written_just_before(qk_lib, cuda):
+    """x written by the kernel right before a decode call is the x it reads:
+    the decode kernel may be scheduled while that kernel runs (programmatic
+    dependent launch) but reads memory only after it has finished.  x starts
+    as NaN, so reading it early would show."""
+    import torch
+    rng = synth.rng_for(51, 0)
+    probs, refs, xs_new = [], [], []
+    for qt, N, K in (("q4k", 200, 3072), ("q6k", 96, 8192)):
+        W = synth.weights(rng, qt, N, K)
+        x = synth.activations(rng, 1, K)
+        xd = torch.full((1, K), float("nan"), dtype=torch.float16, device=cuda)
+        xs_new.append((xd, _x_dev(x, cuda).view(torch.float16)))
+        y = torch.full((1, N), float("nan"), device=cuda)
+        probs.append(dict(qtype=qt, blocks=_dev(W, cuda), x_f16=xd, y=y, M=1, N=N, K=K))
+        refs.append(oracle.matmul(QT[qt], W, x, N, K))
+    longk = _long_kernel(cuda)
+    torch.cuda.synchronize()
+    longk()
+    for xd, xn in xs_new:
+        xd.copy_(xn)
+    qk_lib.qk_matmul_batch(probs)
+    qk_lib.qk_get_device_status()
+    for p, ref in zip(probs, refs):
+        check_close(p["y"].cpu().numpy().astype(np.float64), ref, "x after a kernel, %s" % p["qtype"])
+
+
+def test_decode_reads_weights_written_just_before(qk_lib, cuda):
+    """Weights written by the kernel right before the call are the ones the
+    decode kernel reads (they start as zeros, which would give y = 0)."""
+    import torch
+    rng = synth.rng_for(52, 0)
+    N, K = 256, 3072
+    W = synth.weights(rng, "q4k", N, K)
+    x = synth.activations(rng, 1, K)
+    Wn = _dev(W, cuda)
+    Wd = torch.zeros_like(Wn)
+    y = torch.full((1, N), float("nan"), device=cuda)
+    longk = _long_kernel(cuda)
+    torch.cuda.synchronize()
+    longk()
+    Wd.copy_(Wn)
+    qk_lib.qk_matmul_batch([dict(qtype="q4k", blocks=Wd, x_f16=_x_dev(x, cuda), y=y, M=1, N=N, K=K)])
+    qk_lib.qk_get_device_status()
+    check_close(y.cpu().numpy().astype(np.float64), oracle.matmul(QT["q4k"], W, x, N, K), "weights after a kernel")
+
+
+def test_decode_chain_back_to_back(qk_lib, cuda):
+    """The decode layer's linears launched back to back, each reading an x
+    written by a copy kernel right before it: every result matches the
+    oracle."""
+    import torch
+    rng = synth.rng_for(53, 0)
+    K = synth.HIDDEN
+    steps = []
+    for lin in synth.layer_linears(0):
+        W = synth.weights(rng, lin.qtype, lin.N, lin.K)
+        x = synth.activations(rng, 1, lin.K)
+        xd = torch.full((1, lin.K), float("nan"), dtype=torch.float16, device=cuda)
+        y = torch.full((1, lin.N), float("nan"), device=cuda)
+        steps.append((dict(qtype=lin.qtype, blocks=_dev(W, cuda), x_f16=xd, y=y, M=1, N=lin.N, K=lin.K),
+                      _x_dev(x, cuda).view(torch.float16), oracle.matmul(QT[lin.qtype], W, x, lin.N, lin.K), lin.name))
+    torch.cuda.synchronize()
+    for p, xn, _, _ in steps:
+        p["x_f16"].copy_(xn)
+        qk_lib.qk_matmul_batch([p])
+    qk_lib.qk_get_device_status()
+    for p, _, ref, name in steps:
+        check_close(p["y"].cpu().numpy().astype(np.float64), ref, "back-to-back chain " + name)
+
+
+# ---------------------------------------------------------------------------
 # RMSNorm in front of the linears
 # ---------------------------------------------------------------------------
 EPS = 1e-5

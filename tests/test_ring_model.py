@@ -279,3 +279,107 @@ def test_gemv_partials_without_the_free_wait_can_race():
     """Control: without the red_free wait a fast warp can overwrite a partial the
     reducer has not read yet, and the model sees it (so it can fail)."""
     assert any(simulate_gemv_reduction(3, 7, seed, free_wait=False)[1] for seed in range(600))
+
+
+def simulate_decode_ring(warps, stages, steps, nchunks, seed, empty_wait=True):
+    """The decode GEMV's producer/consumer ring.  The producer runs, in order,
+    for every step st: (st >= S) wait for empty[s] phase st / S - 1 (every
+    compute warp released step st - S), add the warps' partials of step st - S
+    if that step ended a tile, then issue the copy of step st into stage
+    st % S; at the end it waits for and adds the last S steps.  A copy lands
+    later and completes full[s].  Each compute warp waits for full[s] phase
+    st / S, reads the stage (start and end are separate events), writes its
+    partial into the stage's slot at a tile's last chunk and arrives on
+    empty[s].  Returns (fooled, overwritten): a wait that passed early, or a
+    stage refilled while a warp read it, a warp reading stale bytes, or a
+    partial missing or replaced when the producer adds it, or a hang (counted
+    as overwritten).  empty_wait=False drops the producer's empty wait (a
+    control)."""
+    rng = random.Random(seed)
+    full = [Bar(1) for _ in range(stages)]
+    empty = [Bar(warps) for _ in range(stages)]
+    ops = []
+    for st in range(steps):
+        if st >= stages:
+            ops += [("wait", st - stages), ("finish", st - stages)]
+        ops.append(("issue", st))
+    for st in range(max(0, steps - stages), steps):
+        ops += [("wait", st), ("finish", st)]
+    pc = 0
+    content = [None] * stages
+    part = [[None] * warps for _ in range(stages)]
+    inflight = []
+    w_next = [0] * warps
+    reading = [None] * warps
+    fooled = overwritten = False
+    while True:
+        acts = []
+        if pc < len(ops):
+            kind, st = ops[pc]
+            if kind != "wait" or not empty_wait or empty[st % stages].passes(st // stages):
+                acts.append("p")
+        if inflight:
+            acts.append("land")
+        for w in range(warps):
+            st = w_next[w]
+            if reading[w] is not None:
+                acts.append(("end", w))
+            elif st < steps and full[st % stages].passes(st // stages):
+                acts.append(("start", w))
+        if not acts:
+            break
+        a = rng.choice(acts)
+        if a == "p":
+            kind, st = ops[pc]
+            s = st % stages
+            if kind == "wait" and empty_wait:
+                fooled |= empty[s].early(st // stages)
+            elif kind == "finish" and st % nchunks == nchunks - 1:
+                if any(p != st for p in part[s]):
+                    overwritten = True
+            elif kind == "issue":
+                inflight.append((s, st))
+            pc += 1
+        elif a == "land":
+            s, st = inflight.pop(rng.randrange(len(inflight)))
+            if any(r is not None and r % stages == s for r in reading):
+                overwritten = True  # bytes of a stage a warp is still reading
+            content[s] = st
+            full[s].arrive()
+        elif a[0] == "start":
+            w = a[1]
+            st = w_next[w]
+            fooled |= full[st % stages].early(st // stages)
+            if content[st % stages] != st:
+                overwritten = True
+            reading[w] = st
+        else:
+            w = a[1]
+            st = reading[w]
+            s = st % stages
+            if content[s] != st:
+                overwritten = True
+            if st % nchunks == nchunks - 1:
+                part[s][w] = st
+            reading[w] = None
+            w_next[w] += 1
+            empty[s].arrive()
+    if pc < len(ops) or inflight or any(n != steps for n in w_next):
+        overwritten = True  # stuck: a warp or the producer never finished
+    return fooled, overwritten
+
+
+@pytest.mark.parametrize("warps,stages,steps,nchunks", [(1, 2, 7, 1), (3, 3, 10, 1), (4, 3, 12, 4), (12, 6, 13, 2)])
+def test_decode_ring(warps, stages, steps, nchunks):
+    """The decode GEMV's ring: no wait passes early, no stage is refilled while
+    a warp reads it, no partial is replaced before the producer adds it, and
+    nothing deadlocks."""
+    for seed in range(400):
+        assert simulate_decode_ring(warps, stages, steps, nchunks, seed) == (False, False)
+
+
+def test_decode_ring_without_the_empty_wait_can_race():
+    """Control: a producer that refills without waiting for the warps' release
+    overwrites a stage in use or adds partials not yet written, and the model
+    sees it."""
+    assert any(simulate_decode_ring(3, 2, 9, 1, seed, empty_wait=False)[1] for seed in range(400))
