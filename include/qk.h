@@ -77,7 +77,7 @@ qk_status qk_dequant_q4k(const void *blocks, int64_t n_blocks, float *out, qk_st
 qk_status qk_dequant_q6k(const void *blocks, int64_t n_blocks, float *out, qk_stream_t stream);
 
 /*
- * Number range of the two paths.  The GEMV (M <= 16) applies the block scales
+ * Number range of the two paths.  The GEMV (M <= 8) applies the block scales
  * in fp32.  The tensor-core GEMM forms every weight in fp16: fp16(d*sc),
  * fp16(dmin*m) and fp16(q*d*sc - dmin*m), each rounded from fp32; a block
  * whose |d*sc*q| or |dmin*m| exceeds 65504 gives +-inf weights there (the
@@ -89,10 +89,10 @@ qk_status qk_dequant_q6k(const void *blocks, int64_t n_blocks, float *out, qk_st
  * y[m][n] = sum_k x[m][k] * w[n][k] for Q4_K weights W (N x K), fp16 x, fp32 y
  * (DAMASCUS project overview, "[01] the thesis" / "[04] one decode step";
  * "Building DAMASCUS", "Prefill and decode need different performance
- * questions").  M <= 16 runs the GEMV (products of the integer quants with
+ * questions").  M <= 8 runs the GEMV (products of the integer quants with
  * fp16 x are exact, sums fp32, block scales applied per sub-block in fp32)
  * where its shared-memory plan fits (see qk_uses_gemv: the model's K = 3072
- * up to M = 16, K = 8192 up to M = 8); larger M, and problems the GEMV cannot
+ * and K = 8192 up to M = 8); larger M, and problems the GEMV cannot
  * stage, run the tensor-core GEMM (weights dequantized to fp16 in
  * shared or tensor memory, never written to device memory; fp32 accumulation
  * in tensor memory),
@@ -145,9 +145,9 @@ typedef struct qk_matmul_desc {
 /*
  * Run `count` independent problems (DAMASCUS project overview, "[04] one
  * decode step": the QKV projections share x, gate and up share x, and every
- * decode-step linear is an M = 1 GEMV).  Problems the GEMV runs (M <= 16)
+ * decode-step linear is an M = 1 GEMV).  Problems the GEMV runs (M <= 8)
  * share launches, up to 8 per launch, with the problems of the same
- * token-slot class (M = 1; 2..8; 9..16), so small GEMVs stream their weights
+ * token-slot class (M = 1; 2..8), so small GEMVs stream their weights
  * concurrently; each keeps its own shared-memory plan and split over warps.
  * Other problems run as in qk_matmul_q4k / qk_matmul_q6k /
  * qk_gateup_swiglu_q4k.  Each entry obeys the rules of its single-problem
@@ -165,7 +165,7 @@ qk_status qk_matmul_batch(const qk_matmul_desc *descs, int count, qk_stream_t st
  *   xhat[m][k] = fp16( x[m][k] / sqrt(mean_k x[m][k]^2 + eps) * gamma[k] )
  * (sum of squares, scale and products in fp32; gamma is fp16[K], the same K
  * for every problem of the call; eps finite and >= 0) and the problems then
- * run as in qk_matmul_batch.  Problems the GEMV runs (M <= 16, see
+ * run as in qk_matmul_batch.  Problems the GEMV runs (M <= 8, see
  * qk_uses_gemv) normalize inside its x staging: no extra pass, no scratch.
  * Problems the tensor-core GEMM runs first have their xhat written to
  * `scratch`, a caller-owned device buffer of at least qk_rmsnorm_scratch_bytes
@@ -245,7 +245,7 @@ qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream);
  * (QK_Q4_K / QK_Q6_K; with gateup != 0 the fused gate/up + SwiGLU, Q4_K only)
  * and inner size K runs on the decode GEMV, 0 if it runs on the tensor-core
  * GEMM because the GEMV cannot stage it (the x table of K plus two weight
- * stages must fit in shared memory: K <= 35584 for Q4_K, 34816 for gate/up;
+ * stages must fit in shared memory: K <= 35840 for Q4_K, 34816 for gate/up;
  * Q6_K up to K = 26624 when K / 256 is a multiple of 8, else up to 6912),
  * -1 for an invalid qtype or K.  The answer depends only on these arguments.
  */
@@ -254,7 +254,7 @@ int qk_decode_uses_gemv(int qtype, int gateup, int64_t K);
 /*
  * Host-only query (no CUDA call), for any M: 1 if an M x N x K problem in
  * format `qtype` (gateup != 0: the fused gate/up + SwiGLU) runs on the
- * CUDA-core-fed GEMV (M <= 16: M = 1 in the decode layout, 2..16 with the
+ * CUDA-core-fed GEMV (M <= 8: M = 1 in the decode layout, 2..8 with the
  * tokens in the MMA columns; the x table of M tokens plus two weight stages
  * must fit in shared memory), 0 if it runs on the tensor-core GEMM, -1 for
  * invalid arguments.  qk_decode_uses_gemv(q, g, K) is qk_uses_gemv(q, g, 1, K).

@@ -132,7 +132,7 @@ qk_status validate_device(const void* W, const void* W_up, const uint16_t* x, co
   return QK_OK;
 }
 
-// The GEMV handles M <= 16 when its shared-memory plan fits (the x table of
+// The GEMV handles M <= 8 when its shared-memory plan fits (the x table of
 // M tokens and K plus two weight stages); the tensor-core GEMM takes
 // everything else.
 bool use_gemv(const qk::GemvDesc& d) { return d.M <= qk::gemv_max_m() && qk::gemv_plan_fits(&d, 1); }
@@ -183,7 +183,7 @@ qk_status validate_batch(const qk_matmul_desc* d, int count, std::vector<Checked
 }
 
 // Run validated problems.  GEMV problems share launches, up to 8 per launch,
-// with the problems of the same token-slot count (M = 1; 2..8; 9..16); each
+// with the problems of the same token-slot count (M = 1; 2..8); each
 // keeps its own plan, so a problem's result does not depend on its group.
 // With gamma, every problem's x passes through RMSNorm * gamma first: inside
 // the GEMV's x staging, or for GEMM problems into `scratch` (M * K fp16),

@@ -1,5 +1,5 @@
-// qk_gemv.cu -- decode GEMV (M = 1): y[n] = sum_k x[k] * w[n][k] for Q4_K and
-// Q6_K weights, one or several independent problems per launch.
+// qk_gemv.cu -- the GEMV for M <= 8 tokens: y[m][n] = sum_k x[m][k] * w[n][k]
+// for Q4_K and Q6_K weights, one or several independent problems per launch.
 //
 // Source: DAMASCUS project overview, "[01] the thesis" (decode handles one
 // token at a time with matrix-vector products whose speed is set by streaming
@@ -7,32 +7,35 @@
 // "Prefill and decode need different performance questions".
 //
 // The kernel is HBM-bound by design: every packed weight byte is read once.
-//   * Streaming: the weights of 16 consecutive rows are contiguous, so one
-//     producer warp fetches a whole 16-row tile (or, for long rows, a 16-row x
-//     cb-block chunk, one copy per row) with bulk asynchronous copies into a
-//     ring of shared-memory stages.
+//   * Streaming: the weights of 16 consecutive rows are contiguous, so a
+//     producer warp copies whole 16-row tiles (two adjacent tiles, or the
+//     gate and the up tile, per stage; for long rows 16-row x cb-block chunks,
+//     one copy per row) with bulk asynchronous copies into a ring of
+//     shared-memory stages.
 //   * Arithmetic: the warp tensor instruction mma.sync m16n8k16 (fp16 x fp16,
 //     fp32 accumulate) multiplies raw quants: a 4-bit quant OR-ed into the
 //     mantissa of fp16 1024.0 is the exact value 1024 + F*q (F = 1 or 16 by
 //     nibble position; Q6_K: the 6-bit quant, F = 1 or 16), and its product
 //     with an fp16 activation is exact.
-//   * Column layout: with one token, the MMA's 8 columns do not hold copies of
-//     x.  Lane (g, t) of the warp feeds the 4 k-slots it owns in every MMA
-//     from one byte group of the block: the slots of its B half 0 belong to
-//     one sub-block (Q4_K low nibbles; Q6_K one scale group), those of half 1
-//     to another.  Column 2t holds x only at lane t's half-0 slots and column
+//   * One token, column layout: the MMA's 8 columns do not hold copies of x.
+//     Lane (g, t) of the warp feeds the 4 k-slots it owns in every MMA from
+//     one byte group of the block: the slots of its B half 0 belong to one
+//     sub-block (Q4_K low nibbles; Q6_K one scale group), those of half 1 to
+//     another.  Column 2t holds x only at lane t's half-0 slots and column
 //     2t+1 only at its half-1 slots (every other B entry is zero), so the
-//     accumulator lane (g, t) receives, D[g][2t] and D[g][2t+1], is the sum over
-//     exactly its own two sub-blocks, for rows g and g+8.  Each lane then
-//     applies the scales of those two sub-blocks: no value is selected across
-//     lanes and no scale is decoded twice.  The zero B entries come from a
-//     zero region: a lane whose column takes no x reads zeros.
+//     accumulator lane (g, t) receives, D[g][2t] and D[g][2t+1], is the sum
+//     over exactly its own two sub-blocks, for rows g and g+8.  Each lane then
+//     applies the scales of those two sub-blocks.  The zero B entries come
+//     from a zero region: a lane whose column takes no x reads zeros.
+//   * Several tokens: the MMA columns carry tokens (see q4_block_tn).
 //   * Per sub-block, with Sx the sum of x over the lane's k-slots of it:
 //       Q4_K: sum(w*x) = (d*sc/F) * (D - 1024*Sx) - (dmin*m) * Sx
 //       Q6_K: sum(w*x) = (d*sc/F) * (D - (1024 + 32F)*Sx)
-//   * Reduction: each warp sums its lanes' partials of a tile (two shuffles)
-//     and the last warp to finish the tile adds the warps' partials in a fixed
-//     order (deterministic) and writes y.
+//   * Reduction: compute warp w takes the blocks j = w mod 12 of every tile
+//     and leaves its sums of a finished tile in the stage's partials slot;
+//     the producer adds the 12 warps' sums in warp order before it refills
+//     the stage and writes y.  The order of every addition depends on the
+//     problem's shape only (deterministic, and the same alone or grouped).
 // Q6_K blocks are 210 bytes, so a block can start 2 mod 4 bytes into shared
 // memory; its words then come from aligned loads and funnel shifts.  Problem
 // kind 1 is the fused gate/up + SwiGLU: a stage holds the gate tile and the up
@@ -305,7 +308,7 @@ __device__ __forceinline__ void q6_block(uint32_t r0, uint32_t r1, uint32_t xa, 
 }
 
 // ---------------------------------------------------------------------------
-// Several tokens (2 <= M <= 16): the MMA columns carry tokens.  Lane (g, t)
+// Several tokens (2 <= M <= 8): the MMA columns carry tokens.  Lane (g, t)
 // supplies B for token 8*nt + g of n-tile nt from that token's k-permuted x
 // (or from the zero region for a token beyond M).  Every k-slot of one MMA
 // lies in one sub-block (Q4_K) or scale group (Q6_K), so after its MMAs lane
@@ -519,38 +522,24 @@ __device__ __forceinline__ void q6_block_tn(uint32_t r0, uint32_t r1, const uint
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-#ifndef QK_GEMV_WARPS
-#define QK_GEMV_WARPS 12
-#endif
-constexpr int kW = QK_GEMV_WARPS;  // compute warps per CTA
 // Sleep between polls of the producer's waits, in ns (0: poll back to back).
 #ifndef QK_GEMV_BACKOFF_NS
 #define QK_GEMV_BACKOFF_NS 0
 #endif
 constexpr uint32_t kBackoffNs = QK_GEMV_BACKOFF_NS;
-// 1: the producer waits for a CTA's first stage to land before queueing the
-// others; 0: it queues every stage at once.
-#ifndef QK_GEMV_FIRST_WAIT
-#define QK_GEMV_FIRST_WAIT 1
-#endif
-constexpr bool kFirstWait = QK_GEMV_FIRST_WAIT != 0;
-constexpr int kProducerWarp = kW;
-// Compute warps per CTA of the decode (M = 1) kernel; one more warp streams.
+// Compute warps per CTA; one more warp streams.
 #ifndef QK_DECODE_WARPS
 #define QK_DECODE_WARPS 12
 #endif
 constexpr int kDW = QK_DECODE_WARPS;
 constexpr int kDCompute = 32 * kDW;
 constexpr int kDThreads = 32 * (kDW + 1);
-constexpr int kThreads = 32 * (kW + 1);
-constexpr int kMaxStages = 8;
 constexpr uint32_t kXtBlock = 1024;  // x-table bytes per 256-weight block
 constexpr uint32_t kZeroBytes = 1024;
 
 constexpr uint32_t round128(size_t v) { return (uint32_t)((v + 127) / 128 * 128); }
 // Sums table bytes per block: Q4_K [t][Sx, -1024 Sx, Sx', -1024 Sx'], Q6_K [h][t][4 fields].
 constexpr uint32_t sx_block_bytes(int qtype) { return qtype == kQ4K ? 64u : 128u; }
-constexpr uint32_t red_slot_bytes() { return (uint32_t)(kW * 2 * 16 * sizeof(float)); }
 
 struct GemvProb {
   const uint8_t* w[2];  // weights (gate for kind 1), up weights (kind 1)
@@ -560,12 +549,11 @@ struct GemvProb {
   const uint16_t* gamma;  // RMSNorm prologue: fp16 gamma[K], or null for none
   float eps;
   int N, K, qtype, kind;
-  int pair;             // one tensor, whole rows: a stage holds two adjacent 16-row tiles (as two "tensors")
+  int pair;             // one tensor, whole rows: a stage holds two adjacent 16-row tiles
   int cb;               // K blocks per chunk (a stage holds 16 rows x cb blocks per weight tensor)
   int stages;           // pipeline depth of this problem's CTAs
   uint32_t stage_bytes;
   uint32_t ctl_off, red_off, ring_off;  // shared-memory layout of this problem's CTAs
-  uint32_t red_bytes;                   // several tokens: bytes of one partials buffer (of two)
   uint32_t rawx_off, gamma_off;         // where the bulk copies of x and gamma land
   int tiles, cta_begin, ctas;
 };
@@ -575,22 +563,10 @@ struct GemvBatch {
   int count;
 };
 
-struct Ctl {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  uint64_t red_free[2];       // several tokens: the partials buffer of tile parity p has been summed
-  uint64_t x_full;            // x (and gamma) copied into shared memory
-  uint32_t done[kMaxStages];  // warps that finished the tile whose last chunk used this stage (or parity)
-  uint32_t abort_flag;
-  float rnorm[kMaxGemvM];     // RMSNorm prologue: 1 / sqrt(mean(x^2) + eps) per token
-  float rss[kMaxGemvM][kW];   // its per-warp sums of squares
-};
-constexpr uint32_t kCtlBytes = round128(sizeof(Ctl));
-
 // RMSNorm prologue (DAMASCUS project overview, "[04] one decode step": an
 // RMSNorm comes before the QKV projections and the SwiGLU FFN), over x staged
 // in shared memory at xs: every compute thread sums the squares of its 8-value
-// chunks c = tid, tid + 32kW, ... of each token, the warps reduce them in a
+// chunks c = tid, tid + 32 NW, ... of each token, the warps reduce them in a
 // fixed shuffle tree into rss[m][warp], and after a barrier thread m adds the
 // warps in order: rnorm[m] = 1 / sqrt(mean_k x[m][k]^2 + eps), fp32.
 template <int NW>
@@ -699,7 +675,7 @@ __device__ void build_x_table_tn(uint32_t gs, const float* rnorm, int M, int K, 
   constexpr int kSub = QT == kQ4K ? 8 : 16;      // sums per block
   constexpr int kPer = QT == kQ4K ? 8 : 4;       // 4-value groups per sum
   const int nq = K / 4;
-  for (int i = tid; i < M * nq; i += 32 * kW) {  // nq is a multiple of 64: a warp never straddles tokens
+  for (int i = tid; i < M * nq; i += kDCompute) {  // nq is a multiple of 64: a warp never straddles tokens
     const int m = i / nq, q = i - m * nq;
     const uint32_t a = xt + (uint32_t)m * (uint32_t)(2 * K) + 8u * q;  // x copied here; rearranged in place
     uint2 v = lds64(a);
@@ -717,301 +693,15 @@ __device__ void build_x_table_tn(uint32_t gs, const float* rnorm, int M, int K, 
     }
   }
   const int nsums = (K / kQK) * kSub;
-  for (int i = tid; i < nsums * (MT - M); i += 32 * kW) {
+  for (int i = tid; i < nsums * (MT - M); i += kDCompute) {
     const int sub = i / (MT - M), m = M + i % (MT - M);
     asm volatile("st.shared.f32 [%0], %1;" ::"r"(sx + 4u * (uint32_t)(sub * MT + m)), "f"(0.0f) : "memory");
   }
-  for (int i = tid; i < (int)(kZeroBytes / 16); i += 32 * kW) sts128_u(zero + 16u * i, 0u, 0u, 0u, 0u);
-}
-
-constexpr uint32_t red_tn_bytes(int mt, int nten) { return (uint32_t)(kW * nten * 16 * mt * sizeof(float)); }
-
-// The compute warps of the several-token layout: round-robin units as in the
-// decode layout, partials of every (row, token) handed over per tile through
-// two buffers (tile parity), the last warp of a tile adding them in warp order.
-template <int QT, int MT>
-__device__ __forceinline__ void compute_tn(const GemvProb& P, uint8_t* smem, int t0, int t1, int steps, int nchunks,
-                                           int nten, int tile_rows, uint32_t ten_bytes, int64_t RB) {
-  constexpr int NT = MT / 8;
-  constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
-  constexpr int kSub = QT == kQ4K ? 8 : 16;
-  const int K = P.K, N = P.N, M = P.M, nb = K / kQK, cb = P.cb, kind = P.kind, S = P.stages;
-  const uint32_t SB = P.stage_bytes;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  void* const yout = P.y;
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + P.ctl_off);
-  volatile uint32_t* abort_flag = &ctl->abort_flag;
-  Lane L;
-  L.g = lane >> 2;
-  L.tig = lane & 3;
-  L.hi = L.tig >= 2;
-  L.sh = 16u * (uint32_t)(L.tig & 1);
-  L.shA = L.sh + (L.hi ? 2u : 0u);
-  L.shL = L.sh + (L.hi ? 4u : 0u);
-  const uint32_t base = smem_u32(smem);
-  const uint32_t zero = base + P.ctl_off - kZeroBytes;
-  uint32_t xbase[NT], xstride[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int tok = 8 * nt + L.g;
-    xbase[nt] = tok < M ? base + (uint32_t)tok * (uint32_t)(2 * K) : zero;
-    xstride[nt] = tok < M ? 2u * kQK : 0u;
-  }
-  const uint32_t sx_base = base + (uint32_t)MT * (uint32_t)(2 * K);
-  const uint32_t ring_s = base + P.ring_off;
-  uint32_t magic, fmagic;
-  asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
-  asm volatile("mov.b32 %0, %1;" : "=r"(fmagic) : "n"(kFMagic));
-  const uint32_t pitch = (cb == nb) ? (uint32_t)RB : (uint32_t)(cb * kBB);
-  const int upt = nten * nb, ups = nten * cb;
-  float ya[NT][4], yb[NT][4];  // rows g, g+8 x tokens 8nt + 2t, +1 of tensor 0 (a) and 1 (b)
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ya[nt][i] = yb[nt][i] = 0.f;
-  bool ok = true;
-  for (int st = 0; st < steps; ++st) {
-    const int s = st % S;
-    const int tl = st / nchunks, chunk = st % nchunks;
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, abort_flag, &g_gemv_status));
-    const uint32_t stg = ring_s + (uint32_t)s * SB + (uint32_t)L.g * pitch;
-    const int U0 = (int)(((int64_t)(t0 + tl) * upt + (int64_t)chunk * ups) % kW);
-    int v = (warp - U0 + kW) % kW;
-    for (; ok && v < ups; v += kW) {
-      const int t = v >= cb ? 1 : 0, b = v - t * cb;
-      const uint32_t r0 = stg + (uint32_t)t * ten_bytes + (uint32_t)(b * kBB);
-      const uint32_t r1 = r0 + 8u * pitch;
-      const int blk = chunk * cb + b;
-      uint32_t xa[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) xa[nt] = xbase[nt] + (uint32_t)blk * xstride[nt];
-      const uint32_t sxa = sx_base + (uint32_t)blk * (uint32_t)(kSub * MT * 4);
-      if (t == 0) {
-        if constexpr (QT == kQ4K)
-          q4_block_tn<NT>(r0, r1, xa, sxa, L, lane, magic, fmagic, ya);
-        else
-          q6_block_tn<NT>(r0, r1, xa, sxa, L, lane, magic, ya);
-      } else {
-        if constexpr (QT == kQ4K)
-          q4_block_tn<NT>(r0, r1, xa, sxa, L, lane, magic, fmagic, yb);
-        else
-          q6_block_tn<NT>(r0, r1, xa, sxa, L, lane, magic, yb);
-      }
-    }
-    __syncwarp();
-    if (chunk == nchunks - 1) {
-      const int par = tl & 1;
-      // The buffer of this parity was last used by tile tl - 2: wait until its
-      // partials have been summed.
-      if (tl >= 2)
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->red_free[par], (uint32_t)((tl >> 1) - 1) & 1u, abort_flag,
-                                               &g_gemv_status)) && ok;
-      float* red = reinterpret_cast<float*>(smem + P.red_off + (size_t)par * P.red_bytes);
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        if (t < nten) {
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int row = L.g + 8 * (i >> 1), tok = 8 * nt + 2 * L.tig + (i & 1);
-              red[((warp * nten + t) * 16 + row) * MT + tok] = t ? yb[nt][i] : ya[nt][i];
-            }
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) ya[nt][i] = yb[nt][i] = 0.f;
-      __threadfence_block();
-      __syncwarp();
-      uint32_t prev = 0;
-      if (lane == 0) {
-        prev = atomicAdd(&ctl->done[par], 1u);
-        __threadfence_block();
-      }
-      prev = __shfl_sync(0xffffffffu, prev, 0);
-      __syncwarp();
-      if (prev == (uint32_t)(kW - 1)) {
-        const int tile = t0 + tl;
-        if (kind == 1) {
-          for (int idx = lane; idx < 16 * M; idx += 32) {
-            const int row = idx & 15, tok = idx >> 4;
-            const int n = tile * 16 + row;
-            float gs = 0.f, us = 0.f;
-            for (int w = 0; w < kW; ++w) gs += red[((w * 2 + 0) * 16 + row) * MT + tok];  // kind 1: nten = 2
-            for (int w = 0; w < kW; ++w) us += red[((w * 2 + 1) * 16 + row) * MT + tok];
-            if (n < N) static_cast<__half*>(yout)[(size_t)tok * N + n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
-          }
-        } else {
-          for (int idx = lane; idx < nten * 16 * M; idx += 32) {
-            const int t = idx / (16 * M), rem = idx - t * 16 * M;
-            const int row = rem & 15, tok = rem >> 4;
-            const int n = tile * tile_rows + 16 * t + row;
-            float gs = 0.f;
-            for (int w = 0; w < kW; ++w) gs += red[((w * nten + t) * 16 + row) * MT + tok];
-            if (n < N) static_cast<float*>(yout)[(size_t)tok * N + n] = gs;
-          }
-        }
-        __syncwarp();
-        if (lane == 0) {
-          ctl->done[par] = 0u;
-          mbar_arrive(&ctl->red_free[par]);
-        }
-      }
-      __syncwarp();
-    }
-    if (lane == 0) mbar_arrive(&ctl->empty[s]);
-  }
-}
-
-template <int QT, int MT>
-__device__ __forceinline__ void run_gemv_problem(const GemvProb& P, int cta, uint8_t* smem) {
-  const int K = P.K, N = P.N, nb = K / kQK, cb = P.cb;
-  constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
-  const int64_t RB = (int64_t)nb * kBB;
-  const int kind = P.kind, pair = P.pair;
-  // Tiles of a stage: gate and up (kind 1), two adjacent 16-row tiles of one
-  // tensor (pair), or one tile.  "tile" below is a stage's worth of rows.
-  const int nten = (kind == 1 || pair) ? 2 : 1;
-  const int tile_rows = pair ? 32 : 16;
-  const int nchunks = nb / cb;  // the host makes cb divide nb
-  const int t0 = (int)((int64_t)cta * P.tiles / P.ctas), t1 = (int)((int64_t)(cta + 1) * P.tiles / P.ctas);
-  const int steps = (t1 - t0) * nchunks;
-  const int S = P.stages;
-  const uint32_t SB = P.stage_bytes;
-  const uint32_t ten_bytes = (uint32_t)(16 * cb * kBB);  // one tensor's share of a stage
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint8_t* const w0 = P.w[0];
-  const uint8_t* const w1 = P.w[1];
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + P.ctl_off);
-  volatile uint32_t* abort_flag = &ctl->abort_flag;
-  uint8_t* ring = smem + P.ring_off;
-
-  if (warp == kProducerWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      // x (and gamma) first: one bulk copy each into shared memory
-      const uint32_t xbytes = (uint32_t)P.M * (uint32_t)(2 * K), gbytes = P.gamma ? (uint32_t)(2 * K) : 0u;
-      mbar_arrive_expect_tx(&ctl->x_full, xbytes + gbytes);
-      bulk_copy_g2s(smem + P.rawx_off, P.x, xbytes, &ctl->x_full);
-      if (gbytes) bulk_copy_g2s(smem + P.gamma_off, P.gamma, gbytes, &ctl->x_full);
-      int st = 0;
-      for (; st < steps; ++st) {
-        const int s = st % S;
-        if (!mbar_wait<kBackoffNs>(&ctl->empty[s], ((uint32_t)(st / S) & 1u) ^ 1u, abort_flag, &g_gemv_status))
-          break;
-        // The compute warps read the stage with plain loads; the refill is an
-        // async-proxy write.  The proxy fence after the barrier their releases
-        // completed orders those reads before the copy.
-        fence_proxy_async_smem();
-        const int tile = t0 + st / nchunks, chunk = st % nchunks;
-        const int n0 = tile * tile_rows, rows = min(16, N - n0);
-        uint8_t* dst = ring + (size_t)s * SB;
-        if (cb == nb) {
-          // Whole 16-row tiles: rows nt .. nt+rows_t-1 of a tensor are one
-          // contiguous span (pair: tile t starts 16 rows further).
-          uint32_t total = 0;
-          for (int t = 0; t < nten; ++t) {
-            const int rows_t = min(16, N - (n0 + (pair ? 16 * t : 0)));
-            if (rows_t > 0) total += (uint32_t)(((int64_t)rows_t * RB) & ~int64_t(15));
-          }
-          mbar_expect_tx(&ctl->full[s], total);
-          for (int t = 0; t < nten; ++t) {
-            const int nt = n0 + (pair ? 16 * t : 0), rows_t = min(16, N - nt);
-            if (rows_t <= 0) continue;
-            const int64_t span = (int64_t)rows_t * RB;
-            const uint32_t bulk = (uint32_t)(span & ~int64_t(15));
-            const uint8_t* src = (pair || t == 0 ? w0 : w1) + (int64_t)nt * RB;
-            uint8_t* d = dst + t * ten_bytes;
-            if (bulk) bulk_copy_g2s(d, src, bulk, &ctl->full[s]);
-            for (int64_t b = bulk; b < span; b += 2)  // last bytes of the tensor (span % 16 != 0)
-              *reinterpret_cast<uint16_t*>(d + b) = *reinterpret_cast<const uint16_t*>(src + b);
-          }
-        } else {
-          // A K chunk: one copy per row of cb blocks (16-byte aligned by construction).
-          const uint32_t row_bytes = (uint32_t)(cb * kBB);
-          mbar_expect_tx(&ctl->full[s], row_bytes * (uint32_t)(rows * nten));
-          for (int t = 0; t < nten; ++t)
-            for (int r = 0; r < rows; ++r)
-              bulk_copy_g2s(dst + t * ten_bytes + r * row_bytes,
-                            (t ? w1 : w0) + (int64_t)(n0 + r) * RB + (int64_t)chunk * cb * kBB, row_bytes,
-                            &ctl->full[s]);
-        }
-        mbar_arrive(&ctl->full[s]);
-        // Let the first stage of every CTA land before queueing the rest, so
-        // the compute warps start while the other stages stream in.
-        if (kFirstWait && st == 0 && steps > 1 && !mbar_wait(&ctl->full[0], 0u, abort_flag, &g_gemv_status)) {
-          ++st;
-          break;
-        }
-      }
-      // Drain: the copies issued last have landed before the CTA can exit.
-      for (int i = 1; i <= S && i <= st; ++i)
-        mbar_wait(&ctl->full[(st - i) % S], (uint32_t)((st - i) / S) & 1u, abort_flag, &g_gemv_status, true);
-    }
-    return;
-  }
-
-  // -------------------------------------------------------------- compute
-  compute_tn<QT, MT>(P, smem, t0, t1, steps, nchunks, nten, tile_rows, ten_bytes, RB);
-}
-
-template <int MT>
-__global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_constant__ GemvBatch B) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  int i = 0;
-  while (i + 1 < B.count && (int)blockIdx.x >= B.p[i + 1].cta_begin) ++i;
-  const GemvProb& P = B.p[i];
-  const int cta = (int)blockIdx.x - P.cta_begin;
-  Ctl* ctl = reinterpret_cast<Ctl*>(smem + P.ctl_off);
-  if (threadIdx.x < (unsigned)P.stages) {
-    mbar_init(&ctl->full[threadIdx.x], 1);
-    mbar_init(&ctl->empty[threadIdx.x], kW);
-    ctl->done[threadIdx.x] = 0u;
-  }
-  if (threadIdx.x == 0) {
-    ctl->abort_flag = 0;
-    mbar_init(&ctl->x_full, 1);
-    mbar_init(&ctl->red_free[0], 1);
-    mbar_init(&ctl->red_free[1], 1);
-    ctl->done[0] = ctl->done[1] = 0u;  // several tokens: counters by tile parity
-  }
-  fence_mbar_init();
-  __syncthreads();
-  if (threadIdx.x < 32 * kW) {
-    const uint32_t base = smem_u32(smem);
-    const uint32_t zero = base + P.ctl_off - kZeroBytes;
-    const uint32_t xs = base + P.rawx_off, gs = P.gamma ? base + P.gamma_off : 0u;
-    mbar_wait(&ctl->x_full, 0u, &ctl->abort_flag, &g_gemv_status);
-    if (P.gamma) {
-      rms_partials<kW>(xs, P.M, P.K, &ctl->rss[0][0], threadIdx.x);
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
-      if ((int)threadIdx.x < P.M) {
-        float t = 0.f;
-        for (int w = 0; w < kW; ++w) t += ctl->rss[threadIdx.x][w];
-        ctl->rnorm[threadIdx.x] = 1.0f / sqrtf(t / (float)P.K + P.eps);
-      }
-      asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
-    }
-    {
-      const uint32_t sx = base + (uint32_t)MT * (uint32_t)(2 * P.K);
-      if (P.qtype == kQ4K)
-        build_x_table_tn<kQ4K, MT>(gs, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
-      else
-        build_x_table_tn<kQ6K, MT>(gs, ctl->rnorm, P.M, P.K, base, sx, zero, threadIdx.x);
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(32 * kW) : "memory");
-  }
-  if (P.qtype == kQ4K)
-    run_gemv_problem<kQ4K, MT>(P, cta, smem);
-  else
-    run_gemv_problem<kQ6K, MT>(P, cta, smem);
+  for (int i = tid; i < (int)(kZeroBytes / 16); i += kDCompute) sts128_u(zero + 16u * i, 0u, 0u, 0u, 0u);
 }
 
 // ---------------------------------------------------------------------------
-// Decode (M = 1)
+// The kernel (MT token slots: 1 or 8)
 // ---------------------------------------------------------------------------
 // A producer warp streams stages into a ring with bulk copies of whole
 // 16-row tiles (two adjacent tiles of one tensor, or the gate and the up tile,
@@ -1019,9 +709,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_stream_kernel(const __grid_c
 // large copies per stage keep the copy engine and DRAM efficient.  A unit is
 // 16 rows x one 256-weight block of one tensor; compute warp w takes the
 // units of block j = w, w + kDW, ... of every tile, so each warp's share of a
-// tile is fixed by j alone.  A warp adds its units in j order, leaves its 16
-// row sums of a finished tile in the stage's partials slot, and releases the
-// stage.  Before refilling a stage the producer adds the kDW warps' sums of
+// tile is fixed by j alone.  A warp adds its units in j order, leaves its row
+// (x token) sums of a finished tile in the stage's partials slot, and
+// releases the stage.  Before refilling a stage the producer adds the kDW warps' sums of
 // the tile(s) it held, in warp order, and writes y (fp32, or fp16
 // silu(gate) * up).  No atomic and no barrier among compute warps: each only
 // waits for its stage to land.  The order of every addition depends on the
@@ -1041,8 +731,8 @@ struct DecodeCtl {
   uint64_t empty[kDMaxStages];  // stage released by the kDW compute warps
   uint64_t x_full;              // x (and gamma) copied into shared memory
   uint32_t abort_flag;
-  float rnorm;
-  float rss[kDW];
+  float rnorm[kMaxGemvM];       // RMSNorm prologue: 1 / sqrt(mean(x^2) + eps) per token
+  float rss[kMaxGemvM][kDW];    // its per-warp sums of squares
 };
 
 __device__ __forceinline__ float quad_sum(float v) {
@@ -1052,12 +742,14 @@ __device__ __forceinline__ float quad_sum(float v) {
 
 // Stage geometry of a decode problem (P.pair: two tiles of one tensor per
 // stage; P.cb: blocks per stage and row, nb for whole rows).
-template <int QT>
+template <int QT, int MT>
 __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8_t* smem) {
   constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
+  constexpr int NT = MT / 8;  // several tokens: 8-token n-tiles of the MMA
   const int K = P.K, N = P.N, nb = K / kQK, cb = P.cb, S = P.stages;
   const int nten = 1 + P.kind, pair = P.pair;
   const int ncomb = pair ? 2 : nten;  // row sets per stage: two tiles, or gate and up
+  const int redw = ncomb * 16 * MT;   // partial floats per warp and stage
   const int64_t RB = (int64_t)nb * kBB;
   const int nchunks = nb / cb;
   const uint32_t SB = P.stage_bytes;
@@ -1071,7 +763,9 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
   DecodeCtl* ctl = reinterpret_cast<DecodeCtl*>(smem + P.ctl_off);
   const uint32_t base = smem_u32(smem);
   uint8_t* const ring = smem + P.ring_off;
-  float* const red = reinterpret_cast<float*>(smem + P.red_off);  // [S][kDW][2][16]
+  // partials: [S][kDW][row set (ncomb)][16 rows][MT tokens], as the plan sizes them
+  float* const red = reinterpret_cast<float*>(smem + P.red_off);
+  const int M = P.M;
   void* const yout = P.y;
 
   if (tid < S) {
@@ -1091,21 +785,22 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
     auto finish = [&](int st) {  // the tile(s) of step st, if its chunk was the last
       const int s = st % S, g = st / nchunks;
       if (st % nchunks != nchunks - 1) return;
-      const float* q = red + (size_t)s * (kDW * 32);
-      const int c = lane >> 4, r = lane & 15;
-      const int tile = t0 + g * tps + (pair ? c : 0);
-      const int n = tile * 16 + r;
-      if (nten == 2) {
-        if (lane < 16 && n < N) {
-          float gs = 0.f, us = 0.f;
-          for (int w = 0; w < kDW; ++w) gs += q[w * 32 + r];
-          for (int w = 0; w < kDW; ++w) us += q[w * 32 + 16 + r];
-          static_cast<__half*>(yout)[n] = __float2half_rn(gs / (1.0f + __expf(-gs)) * us);
-        }
-      } else if ((pair || c == 0) && tile < t1 && n < N) {
+      const float* q = red + (size_t)s * (kDW * redw);
+      // output (row set c, row r, token m) at lane + 32 i
+      for (int o = lane; o < ncomb * 16 * MT; o += 32) {
+        const int c = o / (16 * MT), r = (o / MT) % 16, m = o % MT;
+        const int tile = t0 + g * tps + (pair ? c : 0);
+        const int n = tile * 16 + r;
+        if (m >= M || n >= N || tile >= t1 || (nten == 2 && c == 1)) continue;
         float v = 0.f;
-        for (int w = 0; w < kDW; ++w) v += q[w * 32 + c * 16 + r];
-        static_cast<float*>(yout)[n] = v;
+        for (int w = 0; w < kDW; ++w) v += q[w * redw + o];
+        if (nten == 2) {
+          float u = 0.f;
+          for (int w = 0; w < kDW; ++w) u += q[w * redw + 16 * MT + o];
+          static_cast<__half*>(yout)[(size_t)m * N + n] = __float2half_rn(v / (1.0f + __expf(-v)) * u);
+        } else {
+          static_cast<float*>(yout)[(size_t)m * N + n] = v;
+        }
       }
     };
     bool ok = true;
@@ -1167,7 +862,9 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
     asm volatile("griddepcontrol.wait;" ::: "memory");
 #endif
     if (lane == 0) {
-      const uint32_t xbytes = (uint32_t)(2 * K), gbytes = P.gamma ? (uint32_t)(2 * K) : 0u;
+      // one token: x lands in its own buffer for the x-table build; several:
+      // x lands in the table area and is rearranged in place
+      const uint32_t xbytes = (uint32_t)(2 * K) * (uint32_t)M, gbytes = P.gamma ? (uint32_t)(2 * K) : 0u;
       mbar_arrive_expect_tx(&ctl->x_full, xbytes + gbytes);
       bulk_copy_g2s(smem + P.rawx_off, P.x, xbytes, &ctl->x_full);
       if (gbytes) bulk_copy_g2s(smem + P.gamma_off, P.gamma, gbytes, &ctl->x_full);
@@ -1206,84 +903,151 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
   // -------------------------------------------------------------- compute
   const uint32_t xs = base + P.rawx_off, gs = P.gamma ? base + P.gamma_off : 0u;
   const uint32_t zero = base + P.ctl_off - kZeroBytes;
-  const uint32_t sxt = base + (uint32_t)nb * kXtBlock;
+  // the sums table follows the x table: nb KB of B operands (one token), or
+  // the k-permuted x of MT tokens
+  const uint32_t sxt = base + (MT == 1 ? (uint32_t)nb * kXtBlock : (uint32_t)MT * (uint32_t)(2 * K));
   bool ok = mbar_wait(&ctl->x_full, 0u, &ctl->abort_flag, &g_gemv_status);
   if (P.gamma) {
-    rms_partials<kDW>(xs, 1, K, ctl->rss, tid);
+    rms_partials<kDW>(xs, M, K, &ctl->rss[0][0], tid);
     asm volatile("bar.sync 1, %0;" ::"n"(kDCompute) : "memory");
-    if (tid == 0) {
+    if (tid < M) {
       float t = 0.f;
-      for (int w = 0; w < kDW; ++w) t += ctl->rss[w];
-      ctl->rnorm = 1.0f / sqrtf(t / (float)K + P.eps);
+      for (int w = 0; w < kDW; ++w) t += ctl->rss[tid][w];
+      ctl->rnorm[tid] = 1.0f / sqrtf(t / (float)K + P.eps);
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kDCompute) : "memory");
   }
-  build_x_table<QT>(xs, gs, &ctl->rnorm, K, base, sxt, zero, tid);
+  if constexpr (MT == 1)
+    build_x_table<QT>(xs, gs, ctl->rnorm, K, base, sxt, zero, tid);
+  else
+    build_x_table_tn<QT, MT>(gs, ctl->rnorm, M, K, base, sxt, zero, tid);
   asm volatile("bar.sync 1, %0;" ::"n"(kDCompute) : "memory");
 
   Lane L;
   L.g = lane >> 2;
   L.tig = lane & 3;
-  {
-    const int e = L.g & 1;
-    const bool reads_x = (L.g >> 1) == L.tig;
-    L.xt_off = reads_x ? 32u * (uint32_t)L.tig + 16u * (uint32_t)e : 32u * (uint32_t)(((L.g >> 1) + 2) & 3);
-    L.xt_stride = reads_x ? kXtBlock : 0u;
-  }
   L.hi = L.tig >= 2;
   L.sh = 16u * (uint32_t)(L.tig & 1);
   L.shA = L.sh + (L.hi ? 2u : 0u);
   L.shL = L.sh + (L.hi ? 4u : 0u);
-  {
-    const uint32_t sv = (uint32_t)(L.tig >> 1);
-    L.sel0 = 0x7440u | sv;
-    L.sel1 = 0x7440u | (sv + 2);
-  }
-  const uint32_t xt_lane = (L.xt_stride ? base : zero) + L.xt_off;
-  const uint32_t sx_lane = sxt + 16u * (uint32_t)L.tig;
   uint32_t magic, fmagic;
   asm volatile("mov.b32 %0, %1;" : "=r"(magic) : "n"(kMagic));
   asm volatile("mov.b32 %0, %1;" : "=r"(fmagic) : "n"(kFMagic));
   const uint32_t ring_s = base + P.ring_off + (uint32_t)L.g * pitch;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // rows g, g+8 of row set 0, then of row set 1
-  for (int st = 0; st < steps; ++st) {
-    const int s = st % S, chunk = st % nchunks;
-    if (ok) ok = mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, &ctl->abort_flag, &g_gemv_status);
-    // this warp's blocks of the chunk: j = chunk * cb + b with j mod kDW = warp
-    const int j0 = chunk * cb;
-    int b = warp - j0 % kDW;
-    if (b < 0) b += kDW;
-    const uint32_t stg = ring_s + (uint32_t)s * SB;
-    for (; ok && b < cb; b += kDW) {
-      const int j = j0 + b;
-      const uint32_t r0 = stg + (uint32_t)(b * kBB);
-      const uint32_t xa = xt_lane + (uint32_t)j * L.xt_stride;
-      const uint32_t sxa = sx_lane + (uint32_t)j * sx_block_bytes(QT);
-      if constexpr (QT == kQ4K) {
-        q4_block(r0, r0 + 8u * pitch, xa, sxa, L, magic, fmagic, a0, a1);
-        if (ncomb == 2) q4_block(r0 + comb_bytes, r0 + comb_bytes + 8u * pitch, xa, sxa, L, magic, fmagic, a2, a3);
-      } else {
-        q6_block(r0, r0 + 8u * pitch, xa, sxa, L, magic, fmagic, a0, a1);
-        if (ncomb == 2) q6_block(r0 + comb_bytes, r0 + comb_bytes + 8u * pitch, xa, sxa, L, magic, fmagic, a2, a3);
-      }
+
+  if constexpr (MT == 1) {
+    {
+      const int e = L.g & 1;
+      const bool reads_x = (L.g >> 1) == L.tig;
+      L.xt_off = reads_x ? 32u * (uint32_t)L.tig + 16u * (uint32_t)e : 32u * (uint32_t)(((L.g >> 1) + 2) & 3);
+      L.xt_stride = reads_x ? kXtBlock : 0u;
     }
-    if (chunk == nchunks - 1) {
-      // tile(s) done: this warp's row sums to the stage's partials slot
-      const float p0 = quad_sum(a0), p1 = quad_sum(a1), p2 = quad_sum(a2), p3 = quad_sum(a3);
-      if (L.tig == 0) {
-        float* q = red + ((size_t)s * kDW + warp) * 32;
-        q[L.g] = p0;
-        q[L.g + 8] = p1;
-        q[16 + L.g] = p2;
-        q[16 + L.g + 8] = p3;
-      }
-      a0 = a1 = a2 = a3 = 0.f;
+    {
+      const uint32_t sv = (uint32_t)(L.tig >> 1);
+      L.sel0 = 0x7440u | sv;
+      L.sel1 = 0x7440u | (sv + 2);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&ctl->empty[s]);
+    const uint32_t xt_lane = (L.xt_stride ? base : zero) + L.xt_off;
+    const uint32_t sx_lane = sxt + 16u * (uint32_t)L.tig;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;  // rows g, g+8 of row set 0, then of row set 1
+    for (int st = 0; st < steps; ++st) {
+      const int s = st % S, chunk = st % nchunks;
+      if (ok) ok = mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, &ctl->abort_flag, &g_gemv_status);
+      // this warp's blocks of the chunk: j = chunk * cb + b with j mod kDW = warp
+      const int j0 = chunk * cb;
+      int b = warp - j0 % kDW;
+      if (b < 0) b += kDW;
+      const uint32_t stg = ring_s + (uint32_t)s * SB;
+      for (; ok && b < cb; b += kDW) {
+        const int j = j0 + b;
+        const uint32_t r0 = stg + (uint32_t)(b * kBB);
+        const uint32_t xa = xt_lane + (uint32_t)j * L.xt_stride;
+        const uint32_t sxa = sx_lane + (uint32_t)j * sx_block_bytes(QT);
+        if constexpr (QT == kQ4K) {
+          q4_block(r0, r0 + 8u * pitch, xa, sxa, L, magic, fmagic, a0, a1);
+          if (ncomb == 2) q4_block(r0 + comb_bytes, r0 + comb_bytes + 8u * pitch, xa, sxa, L, magic, fmagic, a2, a3);
+        } else {
+          q6_block(r0, r0 + 8u * pitch, xa, sxa, L, magic, fmagic, a0, a1);
+          if (ncomb == 2) q6_block(r0 + comb_bytes, r0 + comb_bytes + 8u * pitch, xa, sxa, L, magic, fmagic, a2, a3);
+        }
+      }
+      if (chunk == nchunks - 1) {
+        // tile(s) done: this warp's row sums to the stage's partials slot
+        const float p0 = quad_sum(a0), p1 = quad_sum(a1), p2 = quad_sum(a2), p3 = quad_sum(a3);
+        if (L.tig == 0) {
+          float* q = red + ((size_t)s * kDW + warp) * redw;
+          q[L.g] = p0;
+          q[L.g + 8] = p1;
+          if (ncomb == 2) {
+            q[16 + L.g] = p2;
+            q[16 + L.g + 8] = p3;
+          }
+        }
+        a0 = a1 = a2 = a3 = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->empty[s]);
+    }
+  } else {
+    // Several tokens: lane (g, t) supplies B for token 8 nt + g of n-tile nt
+    // (the zero region for a token beyond M) and accumulates rows g, g+8 x
+    // tokens 8 nt + 2t, 8 nt + 2t + 1 of each row set; every k-slot of an MMA
+    // lies in one sub-block, so no lanes are summed afterwards.
+    uint32_t xbase[NT], xstride[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int tok = 8 * nt + L.g;
+      xbase[nt] = tok < M ? base + (uint32_t)tok * (uint32_t)(2 * K) : zero;
+      xstride[nt] = tok < M ? 2u * kQK : 0u;
+    }
+    constexpr int kSub = QT == kQ4K ? 8 : 16;
+    float ya[NT][4], yb[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ya[nt][i] = yb[nt][i] = 0.f;
+    for (int st = 0; st < steps; ++st) {
+      const int s = st % S, chunk = st % nchunks;
+      if (ok) ok = mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, &ctl->abort_flag, &g_gemv_status);
+      const int j0 = chunk * cb;
+      int b = warp - j0 % kDW;
+      if (b < 0) b += kDW;
+      const uint32_t stg = ring_s + (uint32_t)s * SB;
+      for (; ok && b < cb; b += kDW) {
+        const int j = j0 + b;
+        const uint32_t r0 = stg + (uint32_t)(b * kBB);
+        uint32_t xa[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) xa[nt] = xbase[nt] + (uint32_t)j * xstride[nt];
+        const uint32_t sxa = sxt + (uint32_t)j * (uint32_t)(kSub * MT * 4);
+        if constexpr (QT == kQ4K) {
+          q4_block_tn<NT>(r0, r0 + 8u * pitch, xa, sxa, L, lane, magic, fmagic, ya);
+          if (ncomb == 2)
+            q4_block_tn<NT>(r0 + comb_bytes, r0 + comb_bytes + 8u * pitch, xa, sxa, L, lane, magic, fmagic, yb);
+        } else {
+          q6_block_tn<NT>(r0, r0 + 8u * pitch, xa, sxa, L, lane, magic, ya);
+          if (ncomb == 2) q6_block_tn<NT>(r0 + comb_bytes, r0 + comb_bytes + 8u * pitch, xa, sxa, L, lane, magic, yb);
+        }
+      }
+      if (chunk == nchunks - 1) {
+        float* q = red + ((size_t)s * kDW + warp) * redw;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int row = L.g + 8 * (i >> 1), tok = 8 * nt + 2 * L.tig + (i & 1);
+            q[row * MT + tok] = ya[nt][i];
+            if (ncomb == 2) q[16 * MT + row * MT + tok] = yb[nt][i];
+            ya[nt][i] = yb[nt][i] = 0.f;
+          }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->empty[s]);
+    }
   }
 }
 
+template <int MT>
 __global__ void __launch_bounds__(kDThreads, 1) gemv_decode_kernel(const __grid_constant__ GemvBatch B) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -1292,9 +1056,9 @@ __global__ void __launch_bounds__(kDThreads, 1) gemv_decode_kernel(const __grid_
   const GemvProb& P = B.p[i];
   const int cta = (int)blockIdx.x - P.cta_begin;
   if (P.qtype == kQ4K)
-    decode_problem<kQ4K>(P, cta, smem);
+    decode_problem<kQ4K, MT>(P, cta, smem);
   else
-    decode_problem<kQ6K>(P, cta, smem);
+    decode_problem<kQ6K, MT>(P, cta, smem);
 }
 
 }  // namespace
@@ -1311,11 +1075,6 @@ uint32_t gemv_take_status() {
 namespace {
 
 constexpr size_t kGemvSmem = 227 * 1024;
-// Stages the plan aims for before it grows a stage (see plan_problem).
-#ifndef QK_GEMV_MIN_STAGES
-#define QK_GEMV_MIN_STAGES 3
-#endif
-constexpr int kMinStages = QK_GEMV_MIN_STAGES;
 // Relative compute cost per packed byte, for splitting CTAs among the problems
 // of a grouped launch: a Q6_K block's 6-bit assembly takes ~1.4x the logic
 // instructions per byte of a Q4_K block, and a decode CTA streams Q6_K at
@@ -1327,21 +1086,27 @@ constexpr int kMinStages = QK_GEMV_MIN_STAGES;
 constexpr double kQ6CostPerByte = QK_Q6_COST;
 
 // The token slots of the kernel that runs M tokens: 1 (decode layout), 8 or 16.
-int slots_for(int64_t M) { return M <= 1 ? 1 : M <= 8 ? 8 : 16; }
+int slots_for(int64_t M) { return M <= 1 ? 1 : 8; }
 
-// The stage geometry of one problem, from its own shape only (so grouping
-// problems never changes how one of them is computed).  False if no plan with
-// at least two stages fits.
-//   Layout: [x table | sums | zero region | control | partials | ring[S]].
-bool plan_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
+// The plan of one problem, from its shape only (so grouping problems never
+// changes how one of them is computed).  Layout:
+//   one token:     [x table | sums | zero region | control | x | gamma | partials[S] | ring[S]]
+//   several (MT):  [k-permuted x of MT tokens | sums | zero region | control | gamma | partials[S] | ring[S]]
+// (several tokens: x is copied straight into the table area and rearranged
+// in place).  Stage geometry, first that fits: two adjacent whole tiles of
+// one tensor per stage (one token only) with at least 3 stages; whole tiles
+// (gate and up together) with 3; the largest 16-byte-aligned chunk of cb
+// blocks with 4, then 3; then the same with 2 stages (several tokens: with 2
+// stages from the start).
+bool plan_decode_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
   memset(&P, 0, sizeof(P));
+  if (d.M < 1 || d.M > kMaxGemvM || d.N <= 0 || d.N >= ((int64_t)1 << 31) || d.K <= 0 || d.K % kQK != 0 ||
+      d.K >= ((int64_t)1 << 31))
+    return false;
   P.w[0] = static_cast<const uint8_t*>(d.w0);
   P.w[1] = static_cast<const uint8_t*>(d.w1);
   P.x = d.x;
   P.y = d.y;
-  if (d.M < 1 || d.M > kMaxGemvM || d.N <= 0 || d.N >= ((int64_t)1 << 31) || d.K <= 0 || d.K % kQK != 0 ||
-      d.K >= ((int64_t)1 << 31))
-    return false;
   P.M = (int)d.M;
   P.gamma = d.gamma;
   P.eps = d.eps;
@@ -1350,118 +1115,42 @@ bool plan_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
   P.qtype = d.qtype;
   P.kind = d.w1 ? 1 : 0;
   const int mt = slots_for(d.M);
-  const int nb = P.K / kQK;
-  const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
-  const int nten = 1 + P.kind;
-  const int64_t RB = (int64_t)nb * bb;
-  // Layout: [x table | sums | zero region | control | partials | x | gamma | ring].
-  // Several tokens copy x straight into the x table's rows (rearranged in place).
-  const size_t xt = mt == 1 ? round128((size_t)nb * (kXtBlock + sx_block_bytes(P.qtype)))
-                            : round128((size_t)mt * 2 * P.K + (size_t)nb * (P.qtype == kQ4K ? 8 : 16) * mt * 4);
-  P.ctl_off = (uint32_t)(xt + kZeroBytes);
-  P.red_off = P.ctl_off + kCtlBytes;
-  const size_t rawx = mt == 1 ? round128((size_t)2 * P.K) : 0;
-  const size_t gam = P.gamma ? round128((size_t)2 * P.K) : 0;
-  // the decode layout keeps a partials slot per stage; several tokens keep two
-  // buffers (tile parity) sized for the stage's tensors
-  const size_t red_stage = mt == 1 ? red_slot_bytes() : 0;
-  const size_t red_fixed = mt == 1 ? 0 : round128((size_t)2 * red_tn_bytes(mt, nten));
-  const size_t fixed = (size_t)P.red_off + red_fixed + rawx + gam + 128 + 128;  // + rounding, + slack past a block
-  if (fixed >= kGemvSmem) return false;
-  const size_t avail = kGemvSmem - fixed;
-  auto stages_for = [&](size_t stage_bytes) {
-    return (int)std::min<size_t>(kMaxStages, avail / (stage_bytes + red_stage));
-  };
-  // Stage geometry: 16 rows x cb blocks per tensor.  Bytes in flight per SM
-  // hide the HBM latency only when several stages stream while the warps work
-  // on one or two, so the stage is the largest chunk (cb dividing K/256, rows
-  // 16-byte aligned in device memory and cb blocks a multiple of 16 bytes:
-  // any cb for Q4_K, multiples of 8 for Q6_K, or whole rows) that still gives
-  // six stages, else three, else two.
-  int cb = 0, S = 0;
-  for (int want : {kMinStages, 3, 2}) {
-    for (int c = nb; c >= 1 && cb == 0; --c) {
-      if (nb % c != 0) continue;
-      if (c != nb && ((c * bb) % 16 != 0 || (RB % 16) != 0)) continue;
-      const int st = stages_for(round128((size_t)16 * nten * c * bb));
-      if (st >= want) {
-        cb = c;
-        S = st;
-      }
-    }
-    if (cb) break;
-  }
-  if (cb == 0) return false;
-  P.cb = cb;
-  P.pair = 0;
-  P.stage_bytes = round128((size_t)16 * nten * cb * bb);
-  P.stages = S;
-  P.red_bytes = mt == 1 ? 0u : red_tn_bytes(mt, nten);
-  P.rawx_off = mt == 1 ? (uint32_t)(P.red_off + round128((size_t)S * red_stage)) : 0u;
-  P.gamma_off = (uint32_t)(P.red_off + (mt == 1 ? round128((size_t)S * red_stage) + rawx : red_fixed));
-  P.ring_off = (uint32_t)(P.gamma_off + gam);
-  P.tiles = (P.N + 15) / 16;
-  *smem_out = (size_t)P.ring_off + (size_t)S * P.stage_bytes + 128 + 128;  // + base alignment + slack
-  return *smem_out <= kGemvSmem;
-}
-
-// The decode kernel's plan of one M = 1 problem, from its shape only.
-// Layout: [x table | sums | zero region | control | x | gamma | partials[S] |
-// ring[S]].  Stage geometry, first that fits: two adjacent whole tiles of one
-// tensor per stage with at least 3 stages; whole tiles (gate and up together)
-// with 3; the largest 16-byte-aligned chunk of cb blocks with 4, then 3; then
-// the same with 2 stages.
-bool plan_decode_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
-  memset(&P, 0, sizeof(P));
-  if (d.M != 1 || d.N <= 0 || d.N >= ((int64_t)1 << 31) || d.K <= 0 || d.K % kQK != 0 || d.K >= ((int64_t)1 << 31))
-    return false;
-  P.w[0] = static_cast<const uint8_t*>(d.w0);
-  P.w[1] = static_cast<const uint8_t*>(d.w1);
-  P.x = d.x;
-  P.y = d.y;
-  P.M = 1;
-  P.gamma = d.gamma;
-  P.eps = d.eps;
-  P.N = (int)d.N;
-  P.K = (int)d.K;
-  P.qtype = d.qtype;
-  P.kind = d.w1 ? 1 : 0;
   const int nb = P.K / kQK, nten = 1 + P.kind;
   const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
   const int64_t RB = (int64_t)nb * bb;
   P.tiles = (P.N + 15) / 16;
-  const size_t xt = round128((size_t)nb * (kXtBlock + sx_block_bytes(P.qtype)));
+  const size_t xt = mt == 1 ? round128((size_t)nb * (kXtBlock + sx_block_bytes(P.qtype)))
+                            : round128((size_t)mt * 2 * P.K + (size_t)nb * (P.qtype == kQ4K ? 8 : 16) * mt * 4);
   P.ctl_off = (uint32_t)(xt + kZeroBytes);
-  P.rawx_off = P.ctl_off + round128(sizeof(DecodeCtl));
-  P.gamma_off = P.rawx_off + round128((size_t)2 * P.K);
+  const uint32_t after_ctl = P.ctl_off + round128(sizeof(DecodeCtl));
+  P.rawx_off = mt == 1 ? after_ctl : 0u;
+  P.gamma_off = mt == 1 ? after_ctl + round128((size_t)2 * P.K) : after_ctl;
   P.red_off = P.gamma_off + (P.gamma ? round128((size_t)2 * P.K) : 0);
-  const size_t red_stage = (size_t)kDW * 32 * sizeof(float);
+  const bool can_pair = mt == 1 && !P.kind && P.tiles >= 2;
+  auto red_stage = [&](bool two) { return round128((size_t)kDW * (two ? 2 : nten) * 16 * mt * sizeof(float)); };
   const size_t fixed = (size_t)P.red_off + 128;  // + base alignment
   if (fixed >= kGemvSmem) return false;
   const size_t avail = kGemvSmem - fixed;
-  auto stages_for = [&](size_t stage_bytes) {
-    return (int)std::min<size_t>(kDMaxStages, avail / (round128(stage_bytes) + red_stage));
+  auto stages_for = [&](size_t stage_bytes, bool two) {
+    return (int)std::min<size_t>(kDMaxStages, avail / (round128(stage_bytes) + red_stage(two)));
   };
   int cb = 0, S = 0, pair = 0;
-#ifndef QK_DECODE_PAIR
-#define QK_DECODE_PAIR 1
-#endif
-#ifndef QK_DECODE_MAXCB
-#define QK_DECODE_MAXCB 0
-#endif
-  for (int want : {3, 2}) {
-    if (QK_DECODE_MAXCB == 0 && QK_DECODE_PAIR && !P.kind && P.tiles >= 2 && stages_for((size_t)32 * RB) >= want) {
-      cb = nb, pair = 1, S = stages_for((size_t)32 * RB);
+  // Several tokens keep large partials per stage and a large x table: there
+  // two big stages beat more small ones (copies below ~1 KB stream slowly).
+  for (int want : {mt == 1 ? 3 : 2, 2}) {
+    if (can_pair && stages_for((size_t)32 * RB, true) >= want) {
+      cb = nb, pair = 1, S = stages_for((size_t)32 * RB, true);
       break;
     }
-    if (QK_DECODE_MAXCB == 0 && stages_for((size_t)16 * RB * nten) >= want) {
-      cb = nb, S = stages_for((size_t)16 * RB * nten);
+    if (stages_for((size_t)16 * RB * nten, false) >= want) {
+      cb = nb, S = stages_for((size_t)16 * RB * nten, false);
       break;
     }
-    for (int w2 : {want + 1, want}) {
-      for (int c = QK_DECODE_MAXCB ? std::min(nb - 1, QK_DECODE_MAXCB) : nb - 1; c >= 1 && !cb; --c) {
+    for (int w2 : {want + (mt == 1 ? 1 : 0), want}) {
+      for (int c = nb - 1; c >= 1 && !cb; --c) {
         if (nb % c != 0 || (c * bb) % 16 != 0 || RB % 16 != 0) continue;
-        if (stages_for((size_t)16 * c * bb * nten) >= w2) cb = c, S = stages_for((size_t)16 * c * bb * nten);
+        if (stages_for((size_t)16 * c * bb * nten, false) >= w2)
+          cb = c, S = stages_for((size_t)16 * c * bb * nten, false);
       }
       if (cb) break;
     }
@@ -1472,88 +1161,48 @@ bool plan_decode_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
   P.pair = pair;
   P.stages = S;
   P.stage_bytes = round128((size_t)16 * cb * bb * (pair ? 2 : nten));
-  P.ring_off = (uint32_t)(P.red_off + round128((size_t)S * red_stage));
+  P.ring_off = (uint32_t)(P.red_off + (size_t)S * red_stage(pair != 0));
   *smem_out = (size_t)P.ring_off + (size_t)S * P.stage_bytes + 128;
   return *smem_out <= kGemvSmem;
 }
 
 // One grouped GEMV launch (problems of the same token-slot count): every
 // problem keeps its own plan and the launch takes the largest shared-memory
-// size.  Decode: the CTAs (one per SM, `sms` of them) go one at a time to
-// the problem whose busiest CTA has the most work (tiles times tile bytes
-// times the format's compute cost per byte).  Several tokens: in proportion
-// to the weight bytes times that cost.
+// size.  The CTAs (one per SM, `sms` of them) go one at a time to the
+// problem whose busiest CTA has the most work (tiles times tile bytes times
+// the format's compute cost per byte).
 bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* smem_out) {
   if (count <= 0 || count > kMaxGemvProbs) return false;
   GemvBatch& B = *out;
   memset(&B, 0, sizeof(B));
   B.count = count;
-  double total = 0;
-  int64_t bytes[kMaxGemvProbs];
+  double tile_cost[kMaxGemvProbs];
   size_t smem = 0;
-  const bool decode = slots_for(d[0].M) == 1;
   for (int i = 0; i < count; ++i) {
     size_t s = 0;
     if (slots_for(d[i].M) != slots_for(d[0].M)) return false;
-    if (decode ? !plan_decode_problem(d[i], B.p[i], &s) : !plan_problem(d[i], B.p[i], &s)) return false;
+    if (!plan_decode_problem(d[i], B.p[i], &s)) return false;
     smem = std::max(smem, s);
     const int bb = B.p[i].qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
     const double cost = B.p[i].qtype == kQ4K ? 1.0 : kQ6CostPerByte;
-    bytes[i] = (int64_t)((double)B.p[i].N * (B.p[i].K / kQK) * bb * (1 + B.p[i].kind) * cost);
-    total += (double)bytes[i];
+    tile_cost[i] = 16.0 * (B.p[i].K / kQK) * bb * (1 + B.p[i].kind) * cost;
+    B.p[i].ctas = 1;
   }
   *smem_out = smem;
   const int budget = std::max(count, sms);
-  if (decode) {
-    double tile_cost[kMaxGemvProbs];
-    for (int i = 0; i < count; ++i) {
-      B.p[i].ctas = 1;
-      tile_cost[i] = (double)bytes[i] / B.p[i].tiles;
-    }
-    for (int used = count; used < budget; ++used) {
-      int best = -1;
-      double best_load = 0.0;
-      for (int i = 0; i < count; ++i) {
-        if (B.p[i].ctas >= B.p[i].tiles) continue;
-        const double load = (double)((B.p[i].tiles + B.p[i].ctas - 1) / B.p[i].ctas) * tile_cost[i];
-        if (load > best_load) {
-          best_load = load;
-          best = i;
-        }
-      }
-      if (best < 0) break;
-      ++B.p[best].ctas;
-    }
-    int begin = 0;
-    for (int i = 0; i < count; ++i) {
-      B.p[i].cta_begin = begin;
-      begin += B.p[i].ctas;
-    }
-    return true;
-  }
-  int used = 0;
-  for (int i = 0; i < count; ++i) {
-    int c = (int)((double)budget * (double)bytes[i] / total);
-    c = std::max(1, std::min(c, B.p[i].tiles));
-    B.p[i].ctas = c;
-    used += c;
-  }
-  for (bool again = true; again && used < budget;) {  // leftover CTAs to the busiest problems
-    again = false;
+  for (int used = count; used < budget; ++used) {
     int best = -1;
     double best_load = 0.0;
     for (int i = 0; i < count; ++i) {
-      const double load = (double)bytes[i] / B.p[i].ctas;
-      if (B.p[i].ctas < B.p[i].tiles && load > best_load) {
+      if (B.p[i].ctas >= B.p[i].tiles) continue;
+      const double load = (double)((B.p[i].tiles + B.p[i].ctas - 1) / B.p[i].ctas) * tile_cost[i];
+      if (load > best_load) {
         best_load = load;
         best = i;
       }
     }
-    if (best >= 0) {
-      ++B.p[best].ctas;
-      ++used;
-      again = true;
-    }
+    if (best < 0) break;
+    ++B.p[best].ctas;
   }
   int begin = 0;
   for (int i = 0; i < count; ++i) {
@@ -1564,26 +1213,12 @@ bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* sm
 }
 
 template <int MT>
-cudaError_t launch_mt(const GemvBatch& B, size_t smem, cudaStream_t s) {
+cudaError_t launch_decode(const GemvBatch& B, size_t smem, cudaStream_t s) {
   static PerDeviceFlag attr;  // the shared-memory limit is a per-device function attribute
   const int dev = current_device();
   if (!attr.done(dev)) {
     cudaError_t e =
-        cudaFuncSetAttribute(gemv_stream_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
-    if (e != cudaSuccess) return e;
-    attr.mark(dev);
-  }
-  int ctas = 0;
-  for (int i = 0; i < B.count; ++i) ctas += B.p[i].ctas;
-  gemv_stream_kernel<MT><<<ctas, kThreads, smem, s>>>(B);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_decode(const GemvBatch& B, size_t smem, cudaStream_t s) {
-  static PerDeviceFlag attr;
-  const int dev = current_device();
-  if (!attr.done(dev)) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
+        cudaFuncSetAttribute(gemv_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
     if (e != cudaSuccess) return e;
     attr.mark(dev);
   }
@@ -1593,7 +1228,7 @@ cudaError_t launch_decode(const GemvBatch& B, size_t smem, cudaStream_t s) {
   // Programmatic dependent launch: the CTAs of this grid may be scheduled
   // while the previous kernel on the stream finishes (they wait for it in
   // griddepcontrol.wait before reading anything), which hides the launch
-  // and the set-up of consecutive decode calls.
+  // and the set-up of consecutive calls.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)ctas);
   cfg.blockDim = dim3(kDThreads);
@@ -1604,10 +1239,10 @@ cudaError_t launch_decode(const GemvBatch& B, size_t smem, cudaStream_t s) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_decode_kernel, B);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_decode_kernel<MT>, B);
   return e != cudaSuccess ? e : cudaGetLastError();
 #else
-  gemv_decode_kernel<<<ctas, kDThreads, smem, s>>>(B);
+  gemv_decode_kernel<MT><<<ctas, kDThreads, smem, s>>>(B);
   return cudaGetLastError();
 #endif
 }
@@ -1628,9 +1263,8 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
   size_t smem = 0;
   if (!plan_gemv(d, count, device_sms(), &B, &smem)) return cudaErrorInvalidConfiguration;
   switch (slots_for(d[0].M)) {
-    case 1: return launch_decode(B, smem, s);
-    case 8: return launch_mt<8>(B, smem, s);
-    default: return launch_mt<16>(B, smem, s);
+    case 1: return launch_decode<1>(B, smem, s);
+    default: return launch_decode<8>(B, smem, s);
   }
 }
 

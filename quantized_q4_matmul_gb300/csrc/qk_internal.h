@@ -75,14 +75,12 @@ cudaError_t static_scratch_address(void** out);
 // A kernel whose single bounded wait can never complete (see qk_debug_wait_timeout).
 cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t s);
 
-// Largest M the GEMV handles (M = 1 in the decode layout, 2..16 with the
-// tokens in the MMA columns); larger M goes to the tensor-core GEMM.
-#ifndef QK_GEMV_MAX_M
-#define QK_GEMV_MAX_M 16
-#endif
-constexpr int kMaxGemvM = QK_GEMV_MAX_M;
+// Largest M the GEMV handles (M = 1 in the decode layout, 2..8 with the
+// tokens in the MMA columns); larger M goes to the tensor-core GEMM, which
+// measured faster there on GB300 (Q4_K 3072 x 3072 at M = 16: 15 vs 24 us).
+constexpr int kMaxGemvM = 8;
 int gemv_max_m();
-// The kernel's token-slot count for M tokens (1, 8 or 16): problems share a
+// The kernel's token-slot count for M tokens (1 or 8): problems share a
 // launch only with problems of the same count.
 int gemv_slots(int64_t M);
 

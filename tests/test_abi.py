@@ -148,12 +148,12 @@ def test_decode_kernel_choice_on_the_host(qk_lib):
     Q4_K block, 1152 per Q6_K block), x itself, and at least two stages of 16
     rows, either whole rows (one bulk copy per tensor) or a chunk of cb blocks
     per row whose copies start on 16-byte boundaries, in 227 KB.  Q4_K rows
-    chunk at any block count: K <= 35584 (gate/up 34816).  Q6_K blocks are 210
+    chunk at any block count: K <= 35840 (gate/up 34816).  Q6_K blocks are 210
     bytes, so a Q6_K row chunks only when its block count is a multiple of 8;
     other Q6_K rows run on the GEMV while two whole 16-row tiles fit (up to
     K = 6912) and on the GEMM beyond."""
     use = qk_lib.qk_decode_uses_gemv
-    for qt, gu, kmax in (("q4k", False, 35584), ("q4k", True, 34816)):
+    for qt, gu, kmax in (("q4k", False, 35840), ("q4k", True, 34816)):
         for K in list(range(256, 8192 + 1, 256)) + [kmax - 256, kmax]:
             assert use(qt, K, gu), (qt, gu, K)
         for K in (kmax + 256, kmax + 512, 65536):
@@ -163,15 +163,16 @@ def test_decode_kernel_choice_on_the_host(qk_lib):
     for K in (7168, 8448, 9472, 16640, 28672, 65536):
         assert not use("q6k", K), K
     L = qk_lib.lib()
-    # several tokens (2 <= M <= 16) run on the GEMV too while the x table of M
-    # tokens fits: the model's K = 3072 up to 16 tokens, K = 8192 up to 8
+    # several tokens (2 <= M <= 8) run on the GEMV too while the x table of M
+    # tokens fits: the model's K = 3072 and K = 8192; from M = 9 on the GEMM
     uses = qk_lib.qk_uses_gemv
     for qt, gu in (("q4k", False), ("q6k", False), ("q4k", True)):
-        for M in (1, 2, 5, 8, 9, 16):
+        for M in (1, 2, 5, 8):
             assert uses(qt, M, 3072, gu), (qt, M)
         for M in (2, 8):
             assert uses(qt, M, 8192, gu), (qt, M)
-        assert not uses(qt, 9, 8192, gu) and not uses(qt, 17, 3072, gu)
+        for M in (9, 16, 17):
+            assert not uses(qt, M, 3072, gu) and not uses(qt, M, 8192, gu), (qt, M)
         assert uses(qt, 1, 8192, gu) == use(qt, 8192, gu)
     assert L.qk_uses_gemv(0, 0, 0, 3072) == -1 and L.qk_uses_gemv(0, 0, 4, 300) == -1
     assert L.qk_decode_uses_gemv(2, 0, 3072) == -1      # unknown format
@@ -195,7 +196,8 @@ def test_rmsnorm_rejects_bad_arguments_on_the_host(qk_lib):
     assert L.qk_rmsnorm_gateup_swiglu_q4k(A16, None, A16, A16, 1e-5, A16, A16, 4, 8, 256, None) == -1
     # the scratch an M-token problem needs: none where the GEMV fuses the norm
     sb = qk_lib.qk_rmsnorm_scratch_bytes
-    assert sb("q4k", 1, 3072) == 0 and sb("q6k", 16, 3072) == 0 and sb("q4k", 8, 8192, True) == 0
+    assert sb("q4k", 1, 3072) == 0 and sb("q6k", 8, 3072) == 0 and sb("q4k", 8, 8192, True) == 0
+    assert sb("q6k", 16, 3072) == 16 * 3072 * 2  # M > 8: the GEMM, through the scratch
     assert sb("q4k", 17, 3072) == 17 * 3072 * 2 and sb("q6k", 1024, 8192) == 1024 * 8192 * 2
     assert L.qk_rmsnorm_scratch_bytes(1, 1, 4, 256) == -1 and L.qk_rmsnorm_scratch_bytes(0, 0, 4, 300) == -1
 

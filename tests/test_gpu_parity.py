@@ -135,16 +135,16 @@ def test_matmul_small(qk_lib, cuda, qtype, M, N, K):
     check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "%s M%d N%d K%d" % (qtype, M, N, K))
 
 
-# Several tokens on the GEMV (tokens in the MMA columns): every M of one and
-# two token tiles, ragged N, both K of the model (M <= 8 at K = 8192).
+# Several tokens on the GEMV (tokens in the MMA columns) for M <= 8, ragged N,
+# both K of the model; M = 9..16 on the tensor-core GEMM, next to them.
 SMALL_M = [(M, N, K) for M in (2, 3, 7, 8, 9, 12, 16) for N, K in ((200, 3072), (48, 1024))] + \
-          [(M, 80, 8192) for M in (2, 5, 8)]
+          [(M, 80, 8192) for M in (2, 5, 8, 16)]
 
 
 @pytest.mark.parametrize("qtype", ["q4k", "q6k"])
 @pytest.mark.parametrize("M,N,K", SMALL_M)
 def test_matmul_small_m_gemv(qk_lib, cuda, qtype, M, N, K):
-    assert qk_lib.qk_uses_gemv(qtype, M, K)
+    assert qk_lib.qk_uses_gemv(qtype, M, K) == (M <= 8)
     rng = synth.rng_for(M * 13 + N, K + 1)
     W = synth.weights(rng, qtype, N, K)
     x = synth.activations(rng, M, K)
@@ -156,7 +156,7 @@ def test_matmul_small_m_gemv(qk_lib, cuda, qtype, M, N, K):
 def test_gateup_small_m_gemv(qk_lib, cuda, M):
     import torch
     N, K = 144, 3072
-    assert qk_lib.qk_uses_gemv("q4k", M, K, gateup=True)
+    assert qk_lib.qk_uses_gemv("q4k", M, K, gateup=True) == (M <= 8)
     rng = synth.rng_for(M, 77)
     Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
     x = synth.activations(rng, M, K)
@@ -168,16 +168,16 @@ def test_gateup_small_m_gemv(qk_lib, cuda, M):
 
 
 def test_batch_small_m_matches_single_calls(qk_lib, cuda):
-    """QKV-shaped problems at M = 16 in one grouped launch: bit-identical to the
+    """QKV-shaped problems at M = 8 in one grouped launch: bit-identical to the
     single calls (each keeps its own plan and split over warps)."""
     import torch
     probs, singles = [], []
     for i, (qt, N) in enumerate((("q4k", 3072), ("q4k", 1024), ("q6k", 1024))):
         rng = synth.rng_for(81, i)
         W = synth.weights(rng, qt, N, 3072)
-        x = synth.activations(rng, 16, 3072)
-        y = torch.full((16, N), float("nan"), device=cuda)
-        probs.append(dict(qtype=qt, blocks=_dev(W, cuda), x_f16=_x_dev(x, cuda), y=y, M=16, N=N, K=3072))
+        x = synth.activations(rng, 8, 3072)
+        y = torch.full((8, N), float("nan"), device=cuda)
+        probs.append(dict(qtype=qt, blocks=_dev(W, cuda), x_f16=_x_dev(x, cuda), y=y, M=8, N=N, K=3072))
         singles.append(gpu_matmul(qk_lib, qt, W, x, N, 3072, cuda))
     qk_lib.qk_matmul_batch(probs)
     qk_lib.qk_get_device_status()
@@ -514,7 +514,7 @@ def test_wait_timeout_is_reported_and_the_context_stays_usable(qk_lib, cuda):
 # ---------------------------------------------------------------------------
 # M = 1 problems whose K the GEMV cannot stage run on the tensor-core GEMM
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("qtype,N,K", [("q6k", 200, 6912), ("q6k", 70, 26624), ("q4k", 50, 35584), ("q4k", 33, 2304)])
+@pytest.mark.parametrize("qtype,N,K", [("q6k", 200, 6912), ("q6k", 70, 26624), ("q4k", 50, 35840), ("q4k", 33, 2304)])
 def test_decode_largest_k_on_the_gemv(qk_lib, cuda, qtype, N, K):
     """K at the decode GEMV's limits: whole Q6_K rows of an odd block count
     (rows 2 mod 4 bytes aligned), 8-block Q6_K chunks, 5-block Q4_K chunks,
@@ -693,7 +693,7 @@ def scratch_for(qk, problems, cuda):
                                    (300, 128, 512), (12, 64, 8192)])
 def test_rmsnorm_matmul(qk_lib, cuda, qtype, M, N, K):
     """y = (RMSNorm(x) * gamma) . W^T: fused into the GEMV's x staging for
-    M <= 16 where it fits, through the scratch buffer and the GEMM otherwise."""
+    M <= 8 where it fits, through the scratch buffer and the GEMM otherwise."""
     import torch
     rng = synth.rng_for(M + 3 * N, K + 7)
     W = synth.weights(rng, qtype, N, K)

@@ -32,9 +32,10 @@ The two rings share one done ring of max(SX, SA) barriers, indexed by K step.
 It covers gate/up, where both issuers take every step and a phase needs both
 commits, and single-tensor problems, where the issuers alternate.
 
-A third model checks the decode GEMV's hand-off of per-tile partial sums. The
-compute warps and the reducer warp use double-buffered red_full / red_free
-barriers. A control drops one wait and shows that the model then catches the
+A third model checks the GEMV's ring: a producer warp that refills a stage
+after the compute warps release it and first adds their per-tile partial
+sums, and compute warps that read stages and leave partials in them.  A
+control drops the producer's wait and shows that the model then catches the
 overwrite.
 """
 import random
@@ -217,68 +218,6 @@ class Bar:
 
     def early(self, k):
         return self.done <= k  # passed although phase k has not completed
-
-
-def simulate_gemv_reduction(warps, tiles, seed, free_wait=True):
-    """The decode GEMV's per-tile hand-off: each compute warp finishes tile ti,
-    waits (from ti = 2 on) for red_free[ti & 1] phase (ti >> 1) - 1, writes its
-    partials into red[ti & 1] and arrives on red_full[ti & 1] (count = warps);
-    the reducer waits for red_full[i & 1] phase i >> 1, reads all partials and
-    arrives on red_free[i & 1] (count 1).  Returns (fooled, overwritten): a
-    wait that passed early, or a partial overwritten before the reducer read it.
-    free_wait=False drops the compute warps' red_free wait (a control)."""
-    rng = random.Random(seed)
-    full, free = [Bar(warps), Bar(warps)], [Bar(1), Bar(1)]
-    slot = [[None] * warps for _ in range(2)]  # tile whose partial sits in red[par][w]
-    nxt = [0] * warps   # next tile of each compute warp
-    red_i = 0           # next tile of the reducer
-    fooled = overwritten = False
-    while True:
-        acts = []
-        for w in range(warps):
-            ti = nxt[w]
-            if ti < tiles and (ti < 2 or not free_wait or free[ti & 1].passes((ti >> 1) - 1)):
-                acts.append(w)
-        if red_i < tiles and full[red_i & 1].passes(red_i >> 1):
-            acts.append("r")
-        if not acts:
-            break
-        a = rng.choice(acts)
-        if a == "r":
-            i, par = red_i, red_i & 1
-            fooled |= full[par].early(i >> 1)
-            if any(t != i for t in slot[par]):
-                overwritten = True  # a partial of another tile (missing or already replaced)
-            free[par].arrive()
-            red_i += 1
-        else:
-            w, ti = a, nxt[a]
-            par = ti & 1
-            if ti >= 2 and free_wait:
-                fooled |= free[par].early((ti >> 1) - 1)
-            if slot[par][w] is not None and slot[par][w] != ti - 2:
-                overwritten = True
-            if ti >= 2 and red_i <= ti - 2:
-                overwritten = True  # tile ti - 2 not yet reduced
-            slot[par][w] = ti
-            full[par].arrive()
-            nxt[w] += 1
-    assert red_i == tiles and all(n == tiles for n in nxt), "deadlock"
-    return fooled, overwritten
-
-
-@pytest.mark.parametrize("warps,tiles", [(1, 5), (3, 7), (12, 9)])
-def test_gemv_partials_handoff(warps, tiles):
-    """The double-buffered partials of the decode GEMV: no wait passes early, no
-    partial is overwritten before the reducer has read it, nothing deadlocks."""
-    for seed in range(600):
-        assert simulate_gemv_reduction(warps, tiles, seed) == (False, False)
-
-
-def test_gemv_partials_without_the_free_wait_can_race():
-    """Control: without the red_free wait a fast warp can overwrite a partial the
-    reducer has not read yet, and the model sees it (so it can fail)."""
-    assert any(simulate_gemv_reduction(3, 7, seed, free_wait=False)[1] for seed in range(600))
 
 
 def simulate_decode_ring(warps, stages, steps, nchunks, seed, empty_wait=True):
