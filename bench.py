@@ -637,6 +637,25 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
         sweep[str(M)] = entry("model sweep M=%d" % M, flops, nbytes, ms,
                               "%s, %d launches per pass, one CUDA graph" % (kernel_of("q4k", M, 3072), len(model)),
                               {"weight_bytes": wbytes})
+        if M == 1:
+            # the decode step as an engine runs it: each layer's linears in one
+            # grouped launch (qk_matmul_batch), the LM head on its own
+            by_layer = {}
+            ysl = {}  # one output per position in a layer: a grouped launch's outputs must not overlap
+            for ((li, l), W) in zip(model, Wm):
+                pos = len(by_layer.setdefault(li, []))
+                y = ysl.setdefault((pos, l.N), torch.empty(1, l.N, dtype=torch.float32, device=dev))
+                by_layer[li].append(dict(qtype=l.qtype, blocks=W, x_f16=xk[l.K], y=y, M=1, N=l.N, K=l.K))
+            groups = [probs for _, probs in sorted(by_layer.items(), key=lambda kv: str(kv[0]))]
+
+            def grouped_pass():
+                for probs in groups:
+                    qk.qk_matmul_batch(probs, s)
+
+            ms = graph_steady(torch, stream, [grouped_pass], 1, max(3, reps // 2))
+            sweep["1_grouped"] = entry("model sweep M=1, grouped", flops, nbytes, ms,
+                                       "gemv_decode_kernel, %d grouped launches per pass, one CUDA graph" % len(groups),
+                                       {"weight_bytes": wbytes})
         del xk, yn
     out["model_sweep"] = sweep
     out["note"] = ("each kernel timed alone with CUDA events; before every run L2 is flushed by a %d MB write "

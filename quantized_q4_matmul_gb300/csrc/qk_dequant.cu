@@ -4,9 +4,10 @@
 // operations" (the Q4_K / Q6_K dequantizers are checked before anything else
 // uses them).  Block layouts are the public GGUF definitions.
 //
-// Each warp decodes one 256-weight block; lane t produces weights 8t..8t+7
-// and stores them as two 16-byte vectors, so a warp writes one contiguous
-// 1 KB span.  Arithmetic uses __fmul_rn / __fsub_rn, which the compiler never
+// Each warp decodes groups of 4 consecutive 256-weight blocks (their loads
+// issued together); lane t produces weights 8t..8t+7 of each block and
+// stores them as two 16-byte streaming vectors, so a warp writes contiguous
+// 1 KB spans.  Arithmetic uses __fmul_rn / __fsub_rn, which the compiler never
 // fuses, in the order (d*sc)*q - (dmin*m), matching the fp32 expression
 // exactly.  The kernels are HBM-bound: 144 (210) bytes in, 1024 bytes out per
 // block.
@@ -23,92 +24,132 @@ __device__ uint32_t g_dequant_status = 0;
 namespace {
 
 constexpr int kWarpsPerCta = 8;
+constexpr int kGroup = 4;  // consecutive blocks per warp and iteration: their loads go out together
 
 __device__ __forceinline__ float half_bits_to_float(uint32_t bits16) {
   return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }
 
-// Q4_K: lane t covers weights 8t..8t+7 of the block.  Those 8 weights lie in
-// sub-block j = t/4 and in the 64-weight group t/8; they are the low nibbles
-// (t%8 < 4) or high nibbles of quant bytes 32*(t/8) + 8*(t%4) .. +7.
+// Streaming 16-byte store: the output is written once and not read back here.
+__device__ __forceinline__ void st_stream16(float* p, float a, float b, float c, float d) {
+  asm volatile("st.global.cs.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+
+// One Q4_K block's 8 weights of lane `lane` (weights 8*lane .. 8*lane+7).
+__device__ __forceinline__ void q4k_lane(uint4 hdr, uint2 q8, int lane, float* out) {
+  const int j = lane >> 2;
+  const uint32_t s03 = hdr.y, s47 = hdr.z, s811 = hdr.w;
+  uint32_t sc, mn;
+  if (j < 4) {
+    sc = (s03 >> (8 * j)) & 63u;
+    mn = (s47 >> (8 * j)) & 63u;
+  } else {
+    const int jj = j - 4;
+    const uint32_t lo = (s811 >> (8 * jj)) & 0xFFu;
+    sc = (lo & 0x0Fu) | (((s03 >> (8 * jj + 6)) & 3u) << 4);
+    mn = (lo >> 4) | (((s47 >> (8 * jj + 6)) & 3u) << 4);
+  }
+  const float d = half_bits_to_float(hdr.x);
+  const float dmin = half_bits_to_float(hdr.x >> 16);
+  const float dsc = __fmul_rn(d, (float)sc);
+  const float dmn = __fmul_rn(dmin, (float)mn);
+  const int shift = ((lane & 7) < 4) ? 0 : 4;
+  float w[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint32_t word = e < 4 ? q8.x : q8.y;
+    const uint32_t q = (word >> (8 * (e & 3) + shift)) & 0xFu;
+    w[e] = __fsub_rn(__fmul_rn(dsc, (float)q), dmn);
+  }
+  st_stream16(out + 8 * lane, w[0], w[1], w[2], w[3]);
+  st_stream16(out + 8 * lane + 4, w[4], w[5], w[6], w[7]);
+}
+
+// One Q6_K block (staged in shared memory at sb): lane's 8 weights.
+__device__ __forceinline__ void q6k_lane(const uint8_t* sb, int lane, float* out) {
+  const int h = lane >> 4, g = (lane & 15) >> 2, l0 = 8 * (lane & 3);
+  const float d = half_bits_to_float((uint32_t)sb[208] | ((uint32_t)sb[209] << 8));
+  const float dsc = __fmul_rn(d, (float)(int8_t)sb[192 + (lane >> 1)]);
+  float w[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const int l = l0 + e;
+    const uint32_t lb = sb[64 * h + 32 * (g & 1) + l];
+    const uint32_t lo = g < 2 ? (lb & 0xFu) : (lb >> 4);
+    const uint32_t hi = (sb[128 + 32 * h + l] >> (2 * g)) & 3u;
+    const int q = (int)(lo | (hi << 4)) - 32;
+    w[e] = __fmul_rn(dsc, (float)q);
+  }
+  st_stream16(out + 8 * lane, w[0], w[1], w[2], w[3]);
+  st_stream16(out + 8 * lane + 4, w[4], w[5], w[6], w[7]);
+}
+
+// Warp w takes the groups of kGroup consecutive blocks g = w, w + warps, ...
+// and issues every load of a group before it converts and stores.
 __global__ void __launch_bounds__(kWarpsPerCta * 32) dequant_q4k_kernel(const uint8_t* __restrict__ blocks,
                                                                         int64_t n_blocks, float* __restrict__ out) {
   const int lane = threadIdx.x & 31;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + (threadIdx.x >> 5);
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
-  for (int64_t b = warp0; b < n_blocks; b += nwarps) {
-    const uint8_t* blk = blocks + b * kQ4KBytes;
-    const uint4 hdr = *reinterpret_cast<const uint4*>(blk);  // d, dmin, scales[0..11]
-    const int j = lane >> 2;
-    const uint32_t s03 = hdr.y, s47 = hdr.z, s811 = hdr.w;
-    uint32_t sc, mn;
-    if (j < 4) {
-      sc = (s03 >> (8 * j)) & 63u;
-      mn = (s47 >> (8 * j)) & 63u;
-    } else {
-      const int jj = j - 4;
-      const uint32_t lo = (s811 >> (8 * jj)) & 0xFFu;
-      sc = (lo & 0x0Fu) | (((s03 >> (8 * jj + 6)) & 3u) << 4);
-      mn = (lo >> 4) | (((s47 >> (8 * jj + 6)) & 3u) << 4);
-    }
-    const float d = half_bits_to_float(hdr.x);
-    const float dmin = half_bits_to_float(hdr.x >> 16);
-    const float dsc = __fmul_rn(d, (float)sc);
-    const float dmn = __fmul_rn(dmin, (float)mn);
-    const uint2 q8 = *reinterpret_cast<const uint2*>(blk + 16 + 32 * (lane >> 3) + 8 * (lane & 3));
-    const int shift = ((lane & 7) < 4) ? 0 : 4;
-    float w[8];
+  const int64_t groups = (n_blocks + kGroup - 1) / kGroup;
+  for (int64_t gi = warp0; gi < groups; gi += nwarps) {
+    const int64_t b0 = gi * kGroup;
+    const int nbk = (int)(n_blocks - b0 < kGroup ? n_blocks - b0 : kGroup);
+    uint4 hdr[kGroup];
+    uint2 q8[kGroup];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const uint32_t word = e < 4 ? q8.x : q8.y;
-      const uint32_t q = (word >> (8 * (e & 3) + shift)) & 0xFu;
-      w[e] = __fsub_rn(__fmul_rn(dsc, (float)q), dmn);
+    for (int i = 0; i < kGroup; ++i) {
+      if (i < nbk) {
+        const uint8_t* blk = blocks + (b0 + i) * kQ4KBytes;
+        hdr[i] = ldg_stream16(blk);  // d, dmin, scales[0..11]
+        q8[i] = ldg_stream8(blk + 16 + 32 * (lane >> 3) + 8 * (lane & 3));
+      }
     }
-    float4* dst = reinterpret_cast<float4*>(out + b * kQK + 8 * lane);
-    dst[0] = make_float4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_float4(w[4], w[5], w[6], w[7]);
+#pragma unroll
+    for (int i = 0; i < kGroup; ++i)
+      if (i < nbk) q4k_lane(hdr[i], q8[i], lane, out + (b0 + i) * kQK);
   }
 }
 
-// Q6_K blocks are 210 bytes, so consecutive blocks are only 2-byte aligned.
-// Each warp first copies its block into shared memory with 16-bit loads (the
-// block start is always even), then lane t decodes weights 8t..8t+7: all in
-// scale group t/2, half h = t/16, 32-group g = (t%16)/4, l = 8*(t%4) + e.
 __global__ void __launch_bounds__(kWarpsPerCta * 32) dequant_q6k_kernel(const uint8_t* __restrict__ blocks,
                                                                         int64_t n_blocks, float* __restrict__ out) {
-  __shared__ __align__(16) uint16_t stage[kWarpsPerCta][112];  // 224 bytes per warp
+  // kGroup consecutive blocks (840 bytes, 8-byte aligned: 4 * 210 = 8 * 105)
+  __shared__ __align__(16) uint2 stage[kWarpsPerCta][kGroup * kQ6KBytes / 8];
   const int lane = threadIdx.x & 31;
   const int wid = threadIdx.x >> 5;
   const int64_t warp0 = (int64_t)blockIdx.x * kWarpsPerCta + wid;
   const int64_t nwarps = (int64_t)gridDim.x * kWarpsPerCta;
-  uint8_t* sb = reinterpret_cast<uint8_t*>(stage[wid]);
-  for (int64_t b = warp0; b < n_blocks; b += nwarps) {
-    const uint16_t* src = reinterpret_cast<const uint16_t*>(blocks + b * kQ6KBytes);
-    for (int i = lane; i < kQ6KBytes / 2; i += 32) stage[wid][i] = src[i];
-    __syncwarp();
-    const int h = lane >> 4, g = (lane & 15) >> 2, l0 = 8 * (lane & 3);
-    const float d = half_bits_to_float((uint32_t)sb[208] | ((uint32_t)sb[209] << 8));
-    const float dsc = __fmul_rn(d, (float)(int8_t)sb[192 + (lane >> 1)]);
-    float w[8];
+  const int64_t groups = (n_blocks + kGroup - 1) / kGroup;
+  const uint8_t* sb = reinterpret_cast<const uint8_t*>(stage[wid]);
+  for (int64_t gi = warp0; gi < groups; gi += nwarps) {
+    const int64_t b0 = gi * kGroup;
+    const int nbk = (int)(n_blocks - b0 < kGroup ? n_blocks - b0 : kGroup);
+    const uint8_t* src = blocks + b0 * kQ6KBytes;
+    if (nbk == kGroup) {
+      const uint2* s8 = reinterpret_cast<const uint2*>(src);
+      uint2 v[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      const int l = l0 + e;
-      const uint32_t lb = sb[64 * h + 32 * (g & 1) + l];
-      const uint32_t lo = g < 2 ? (lb & 0xFu) : (lb >> 4);
-      const uint32_t hi = (sb[128 + 32 * h + l] >> (2 * g)) & 3u;
-      const int q = (int)(lo | (hi << 4)) - 32;
-      w[e] = __fmul_rn(dsc, (float)q);
+      for (int k = 0; k < 4; ++k) {
+        const int i = lane + 32 * k;
+        if (i < kGroup * kQ6KBytes / 8) v[k] = ldg_stream8(s8 + i);
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = lane + 32 * k;
+        if (i < kGroup * kQ6KBytes / 8) stage[wid][i] = v[k];
+      }
+    } else {
+      // the tensor's last, partial group: 2-byte copies of the blocks that exist
+      const uint16_t* s2 = reinterpret_cast<const uint16_t*>(src);
+      uint16_t* d2 = reinterpret_cast<uint16_t*>(stage[wid]);
+      for (int i = lane; i < nbk * kQ6KBytes / 2; i += 32) d2[i] = s2[i];
     }
     __syncwarp();
-    float4* dst = reinterpret_cast<float4*>(out + b * kQK + 8 * lane);
-    dst[0] = make_float4(w[0], w[1], w[2], w[3]);
-    dst[1] = make_float4(w[4], w[5], w[6], w[7]);
+    for (int i = 0; i < nbk; ++i) q6k_lane(sb + i * kQ6KBytes, lane, out + (b0 + i) * kQK);
+    __syncwarp();
   }
 }
 
-// Diagnostic: one wait that can never complete (nothing arrives on the
-// barrier), bounded like every wait of the library's kernels.  After
-// `limit_ns` it raises the abort flag and this file's status word and returns.
 __global__ void wait_probe_kernel(uint64_t limit_ns) {
   __shared__ uint64_t bar;
   __shared__ uint32_t abort_flag;
@@ -137,8 +178,9 @@ uint32_t dequant_take_status() {
 
 cudaError_t launch_dequant(QType t, const void* blocks, int64_t n_blocks, float* out, cudaStream_t s) {
   const int sms = device_sms();
-  const int64_t ctas_needed = (n_blocks + kWarpsPerCta - 1) / kWarpsPerCta;
-  const int64_t cap = (int64_t)sms * 16;
+  const int64_t groups = (n_blocks + kGroup - 1) / kGroup;
+  const int64_t ctas_needed = (groups + kWarpsPerCta - 1) / kWarpsPerCta;
+  const int64_t cap = (int64_t)sms * 8;  // the CTAs that fit at once (256 threads each)
   const int grid = (int)(ctas_needed < cap ? ctas_needed : cap);
   if (t == kQ4K)
     dequant_q4k_kernel<<<grid, kWarpsPerCta * 32, 0, s>>>(static_cast<const uint8_t*>(blocks), n_blocks, out);
