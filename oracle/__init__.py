@@ -5,7 +5,8 @@ the benchmark's CPU-baseline leg may import this package.  The CUDA library and
 its Python binding never import it.
 
 ``qk_oracle.c`` holds the arithmetic (GGUF Q4_K / Q6_K block decoding in fp32,
-fp64-accumulated matmul, fp64 SwiGLU, fp64 RMSNorm in front of a linear); this
+fp64-accumulated matmul, fp64 SwiGLU, fp64 RMSNorm in front of a linear, int8
+activations per block of 32); this
 module only builds it with gcc and
 marshals numpy arrays through ctypes.
 """
@@ -76,6 +77,12 @@ class Oracle:
                                                         ctypes.c_void_p, ctypes.c_double, ctypes.c_int64,
                                                         ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64,
                                                         ctypes.c_void_p]
+        L.oracle_quantize_q8.restype = ctypes.c_int
+        L.oracle_quantize_q8.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p,
+                                         ctypes.c_void_p]
+        L.oracle_q8_matmul_rows.restype = ctypes.c_int
+        L.oracle_q8_matmul_rows.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.L = L
@@ -170,6 +177,29 @@ class Oracle:
     def set_num_threads(self, n: int) -> None:
         self.L.oracle_set_num_threads(int(n))
 
+    def quantize_q8(self, x):
+        """(q int8 [M][K], d fp32 [M][K/32]): x per block of 32 as int8 with one scale."""
+        x = np.ascontiguousarray(x, dtype=np.float16)
+        x = x.reshape(-1, x.shape[-1])
+        M, K = x.shape
+        q = np.empty((M, K), dtype=np.int8)
+        d = np.empty((M, K // 32), dtype=np.float32)
+        rc = self.L.oracle_quantize_q8(_ptr(x.view(np.uint16)), M, K, _ptr(q), _ptr(d))
+        assert rc == 0, rc
+        return q, d
+
+    def q8_matmul(self, qtype: int, W, x, N: int, K: int, rows=None) -> np.ndarray:
+        """fp64 y[M][len(rows)] = (d * q)(x) . W[rows]^T with x quantized as in quantize_q8."""
+        W = np.ascontiguousarray(W, dtype=np.uint8).reshape(-1)
+        assert W.size == N * (K // QK) * BLOCK_BYTES[qtype]
+        x = np.ascontiguousarray(x, dtype=np.float16).reshape(-1, K)
+        r = _rows(N, rows)
+        y = np.empty((x.shape[0], r.size), dtype=np.float64)
+        rc = self.L.oracle_q8_matmul_rows(qtype, _ptr(W), _ptr(x.view(np.uint16)), x.shape[0], K, _ptr(r), r.size,
+                                          _ptr(y))
+        assert rc == 0, rc
+        return y
+
 
 _default = None
 
@@ -215,3 +245,11 @@ def num_threads():
 
 def set_num_threads(n):
     default().set_num_threads(n)
+
+
+def quantize_q8(x):
+    return default().quantize_q8(x)
+
+
+def q8_matmul(qtype, W, x, N, K, rows=None):
+    return default().q8_matmul(qtype, W, x, N, K, rows)

@@ -30,6 +30,8 @@
  *  - SwiGLU: out = g / (1 + exp(-g)) * u with g, u the fp64 sums above.
  *  - RMSNorm in front of a linear: xhat = x / sqrt(mean(x^2) + eps) * gamma
  *    in fp64, then the matmul above over xhat (not rounded to fp16).
+ *  - Q8 activations (no counterpart in the pages): x quantized to int8 per
+ *    block of 32 with one fp32 scale, then the matmul above over d * q.
  *
  * Parity pins live in the test suite (hand-built blocks with closed forms,
  * bit-placement tables, an independent bit-level decoder, one-hot and all-ones
@@ -353,6 +355,68 @@ int oracle_rmsnorm_gateup_swiglu_rows(const uint8_t *Wg, const uint8_t *Wu, cons
     if (rc == 0)
         rc = gateup_core(Wg, Wu, xn, M, K, rows, n_rows, out, NULL, NULL);
     free(xn);
+    return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q8 activations.  The pages do not describe an integer-activation variant;  */
+/* this is the reading this project takes (per-32 int8 quantization of x, as  */
+/* the GGUF 8-bit activation formats do):                                     */
+/*   for each token, each block of 32 consecutive k:                          */
+/*     amax = max |x| (fp32; x widened exactly from fp16),                    */
+/*     d    = amax / 127            (one fp32 division),                      */
+/*     q    = round(x / d)          (fp32 division, ties away from zero),     */
+/*            clamped to [-127, 127];  d = 0 (and q = 0) when amax = 0;       */
+/*   x~ = d * q, and the matmul is the one above over x~ (fp64 sums).         */
+/* Finite x only.                                                             */
+/* ------------------------------------------------------------------------ */
+int oracle_quantize_q8(const uint16_t *x, int64_t M, int64_t K, int8_t *q, float *d)
+{
+    if (M < 0 || K <= 0 || K % 32)
+        return -1;
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t b = 0; b < K / 32; ++b) {
+            const uint16_t *xb = x + m * K + 32 * b;
+            float amax = 0.0f;
+            for (int i = 0; i < 32; ++i) {
+                const float v = fabsf(oracle_half_to_float(xb[i]));
+                if (v > amax)
+                    amax = v;
+            }
+            volatile float db = amax / 127.0f;
+            d[m * (K / 32) + b] = db;
+            for (int i = 0; i < 32; ++i) {
+                int qi = 0;
+                if (db != 0.0f) {
+                    volatile float r = oracle_half_to_float(xb[i]) / db;
+                    const float t = roundf(r);
+                    qi = t > 127.0f ? 127 : t < -127.0f ? -127 : (int)t;
+                }
+                q[m * K + 32 * b + i] = (int8_t)qi;
+            }
+        }
+    return 0;
+}
+
+int oracle_q8_matmul_rows(int qtype, const uint8_t *W, const uint16_t *x, int64_t M, int64_t K,
+                          const int64_t *rows, int64_t n_rows, double *y)
+{
+    if (!block_bytes(qtype) || M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
+        return -1;
+    int8_t *q = (int8_t *)malloc((size_t)(M * K) + 1);
+    float *d = (float *)malloc((size_t)(M * (K / 32)) * sizeof(float) + 1);
+    double *xq = (double *)malloc((size_t)(M * K) * sizeof(double) + 1);
+    int rc = -2;
+    if (q && d && xq) {
+        rc = oracle_quantize_q8(x, M, K, q, d);
+        for (int64_t i = 0; rc == 0 && i < M * K; ++i)
+            xq[i] = (double)d[(i / K) * (K / 32) + (i % K) / 32] * (double)q[i];
+        if (rc == 0)
+            rc = matmul_core(qtype, W, xq, M, K, rows, n_rows, y);
+    }
+    free(q);
+    free(d);
+    free(xq);
     return rc;
 }
 

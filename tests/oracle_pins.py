@@ -532,7 +532,88 @@ def pin_rmsnorm_matmul_composition(O):
     assert np.allclose(got, G * expit(G) * U, rtol=1e-10, atol=1e-12 * np.abs(G * U).max())
 
 
+# ---------------------------------------------------------------------------
+# Q8 activations (int8 per block of 32 with one fp32 scale; the reading this
+# project takes, the pages have no such variant)
+# ---------------------------------------------------------------------------
+def pin_q8_worked_block(O):
+    """A hand-worked block: amax 127/128 gives d = 1/128 exactly, so x / d is
+    exact and ties round away from zero; an all-zero block has d = 0, q = 0."""
+    x = np.zeros((1, 64), np.float16)
+    vals = {0: 127 / 128, 1: 5 / 256, 2: -5 / 256, 3: 1 / 256, 4: -1 / 256, 5: 3 / 256, 6: 64 / 128,
+            7: -127 / 128, 8: 1 / 1024}
+    for i, v in vals.items():
+        x[0, i] = v
+    q, d = O.quantize_q8(x)
+    assert d[0, 0] == np.float32(1 / 128) and d[0, 1] == 0.0
+    want = {0: 127, 1: 3, 2: -3, 3: 1, 4: -1, 5: 2, 6: 64, 7: -127, 8: 0}
+    for i in range(32):
+        assert q[0, i] == want.get(i, 0), (i, q[0, i])
+    assert not q[0, 32:].any()
+
+
+def _grid_x(rng, M, K, e):
+    """x = 2^-e * q with q integer in [-127, 127] and |q| = 127 somewhere in
+    every block of 32: exactly representable in fp16 and on its own int8 grid."""
+    q = rng.integers(-127, 128, size=(M, K))
+    for m in range(M):
+        for b in range(K // 32):
+            q[m, 32 * b + rng.integers(0, 32)] = 127 if rng.integers(0, 2) else -127
+    return (q * 2.0 ** -e).astype(np.float16), q
+
+
+def pin_q8_grid_reproduces_fp16(O):
+    """x already on its int8 grid: the Q8 matmul is the fp16 matmul, bit for bit."""
+    rng = synth.rng_for(71, 0)
+    K, N = 512, 24
+    x, qx = _grid_x(rng, 3, K, 9)
+    q, d = O.quantize_q8(x)
+    assert np.array_equal(q, qx) and np.all(d == np.float32(2.0 ** -9))
+    for qt in (Q4K, Q6K):
+        W = synth.weights(rng, "q4k" if qt == Q4K else "q6k", N, K)
+        assert np.array_equal(O.q8_matmul(qt, W, x, N, K), O.matmul(qt, W, x, N, K))
+
+
+def pin_q8_error_bound_and_composition(O):
+    """Random activations: every element within half a step of its int8 value
+    (|x - d q| <= d / 2), the matmul equal to a float64 library product of the
+    dequantized weights with d * q, and within sum_b (d_b / 2) sum_k |w_k| of
+    the fp16 matmul."""
+    rng = synth.rng_for(72, 0)
+    K, N = 768, 40
+    x = synth.activations(rng, 4, K)
+    q, d = O.quantize_q8(x)
+    dk = np.repeat(d.astype(np.float64), 32, axis=1)
+    xq = dk * q
+    xf = x.astype(np.float64)
+    assert np.all(np.abs(xf - xq) <= dk / 2 * (1 + 1e-6))
+    assert np.all(np.abs(q) <= 127)
+    for qt in (Q4K, Q6K):
+        W = synth.weights(rng, "q4k" if qt == Q4K else "q6k", N, K)
+        w = O.dequant(qt, W).astype(np.float64).reshape(N, K)
+        got = O.q8_matmul(qt, W, x, N, K)
+        ref = xq @ w.T
+        assert np.all(np.abs(got - ref) <= 1e-13 * (np.abs(xq) @ np.abs(w).T))
+        bound = (dk / 2) @ np.abs(w).T
+        assert np.all(np.abs(got - O.matmul(qt, W, x, N, K)) <= bound * (1 + 1e-9) + 1e-300)
+
+
+def pin_q8_power_of_two_scaling(O):
+    """Doubling x keeps every q and doubles every d exactly, so y doubles exactly."""
+    rng = synth.rng_for(73, 0)
+    K, N = 256, 16
+    x = (synth.activations(rng, 2, K).astype(np.float32) * 0.25).astype(np.float16)
+    x2 = (x.astype(np.float32) * 2).astype(np.float16)
+    q1, d1 = O.quantize_q8(x)
+    q2, d2 = O.quantize_q8(x2)
+    assert np.array_equal(q1, q2) and np.array_equal(d2, d1 * 2)
+    W = synth.weights(rng, "q6k", N, K)
+    assert np.array_equal(O.q8_matmul(Q6K, W, x2, N, K), 2 * O.q8_matmul(Q6K, W, x, N, K))
+
+
 ALL_PINS = [
+    pin_q8_worked_block, pin_q8_grid_reproduces_fp16, pin_q8_error_bound_and_composition,
+    pin_q8_power_of_two_scaling,
     pin_rmsnorm_worked, pin_rmsnorm_constant_vector, pin_rmsnorm_unit_mean_square_and_scale_invariance,
     pin_rmsnorm_gamma_onehot, pin_rmsnorm_matmul_composition,
     pin_half_to_float,

@@ -68,6 +68,15 @@ MUTANTS = [
     ("rms_matmul_eps_ignored", "int rc = oracle_rmsnorm(x, gamma, M, K, eps, xn);\n    if (rc == 0)\n        rc = matmul_core",
      "int rc = oracle_rmsnorm(x, gamma, M, K, 0.0, xn);\n    if (rc == 0)\n        rc = matmul_core"),
     ("rms_gateup_up_as_gate", "rc = gateup_core(Wg, Wu, xn", "rc = gateup_core(Wg, Wg, xn"),
+    # Q8 activations
+    ("q8_divide_by_128", "volatile float db = amax / 127.0f;", "volatile float db = amax / 128.0f;"),
+    ("q8_ties_to_even", "const float t = roundf(r);", "const float t = rintf(r);"),
+    ("q8_truncate", "const float t = roundf(r);", "const float t = truncf(r);"),
+    ("q8_amax_half_block", "for (int i = 0; i < 32; ++i) {\n                const float v = fabsf",
+     "for (int i = 0; i < 16; ++i) {\n                const float v = fabsf"),
+    ("q8_scale_of_64", "(double)d[(i / K) * (K / 32) + (i % K) / 32]", "(double)d[(i / K) * (K / 32) + (i % K) / 64]"),
+    ("q8_amax_signed", "const float v = fabsf(oracle_half_to_float(xb[i]));",
+     "const float v = oracle_half_to_float(xb[i]);"),
 ]
 
 
