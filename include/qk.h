@@ -158,6 +158,25 @@ typedef struct qk_matmul_desc {
 qk_status qk_matmul_batch(const qk_matmul_desc *descs, int count, qk_stream_t stream);
 
 /*
+ * int8 activations (the paper has no integer-activation variant: this is a
+ * trade of accuracy for arithmetic this library offers beside the fp16
+ * path).  Decode only (M = 0 or 1).  Each token's x is quantized per block of
+ * 32 to int8 with one fp32 scale: d = amax / 127, q = round(x / d) (IEEE fp32
+ * division, ties away from zero; d = 0 gives q = 0); y = sum_k d q w with the
+ * products done as integer dot products and the block scales applied in fp32.
+ * The result differs from the fp16 path by the quantization of x: per output
+ * at most sum over 32-blocks of (d / 2) * sum |w| (finite x).  Problems whose K
+ * the decode GEMV cannot stage are refused with QK_ERR_SHAPE (there is no
+ * other int8 path).  Descriptors and rules as in qk_matmul_batch (up_blocks:
+ * the fused gate/up + SwiGLU); M > 1 is QK_ERR_SHAPE.
+ */
+qk_status qk_matmul_batch_q8x(const qk_matmul_desc *descs, int count, qk_stream_t stream);
+qk_status qk_matmul_q8x_q4k(const void *blocks, const uint16_t *x_f16, float *y, int64_t M, int64_t N, int64_t K,
+                            qk_stream_t stream);
+qk_status qk_matmul_q8x_q6k(const void *blocks, const uint16_t *x_f16, float *y, int64_t M, int64_t N, int64_t K,
+                            qk_stream_t stream);
+
+/*
  * RMSNorm in front of the linears (DAMASCUS project overview, "[04] one decode
  * step": an RMSNorm comes before the QKV projections and before the SwiGLU
  * FFN; "Building DAMASCUS", "Read the model, then reproduce its operations").

@@ -83,6 +83,9 @@ class Oracle:
         L.oracle_q8_matmul_rows.restype = ctypes.c_int
         L.oracle_q8_matmul_rows.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                             ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        L.oracle_q8_gateup_swiglu_rows.restype = ctypes.c_int
+        L.oracle_q8_gateup_swiglu_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                                   ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.L = L
@@ -200,6 +203,19 @@ class Oracle:
         assert rc == 0, rc
         return y
 
+    def q8_gateup_swiglu(self, Wg, Wu, x, N_ff: int, K: int, rows=None) -> np.ndarray:
+        """fp64 silu(x~.Wg^T) * (x~.Wu^T) with x~ the int8 activations of quantize_q8."""
+        Wg = np.ascontiguousarray(Wg, dtype=np.uint8).reshape(-1)
+        Wu = np.ascontiguousarray(Wu, dtype=np.uint8).reshape(-1)
+        assert Wg.size == Wu.size == N_ff * (K // QK) * BLOCK_BYTES[Q4K]
+        x = np.ascontiguousarray(x, dtype=np.float16).reshape(-1, K)
+        r = _rows(N_ff, rows)
+        out = np.empty((x.shape[0], r.size), dtype=np.float64)
+        rc = self.L.oracle_q8_gateup_swiglu_rows(_ptr(Wg), _ptr(Wu), _ptr(x.view(np.uint16)), x.shape[0], K, _ptr(r),
+                                                 r.size, _ptr(out))
+        assert rc == 0, rc
+        return out
+
 
 _default = None
 
@@ -253,3 +269,7 @@ def quantize_q8(x):
 
 def q8_matmul(qtype, W, x, N, K, rows=None):
     return default().q8_matmul(qtype, W, x, N, K, rows)
+
+
+def q8_gateup_swiglu(Wg, Wu, x, N_ff, K, rows=None):
+    return default().q8_gateup_swiglu(Wg, Wu, x, N_ff, K, rows)

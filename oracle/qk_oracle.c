@@ -398,24 +398,46 @@ int oracle_quantize_q8(const uint16_t *x, int64_t M, int64_t K, int8_t *q, float
     return 0;
 }
 
+/* d * q in fp64 (exact) for every element, or NULL. */
+static double *q8_values(const uint16_t *x, int64_t M, int64_t K)
+{
+    int8_t *q = (int8_t *)malloc((size_t)(M * K) + 1);
+    float *d = (float *)malloc((size_t)(M * (K / 32)) * sizeof(float) + 1);
+    double *xq = (double *)malloc((size_t)(M * K) * sizeof(double) + 1);
+    int ok = q && d && xq && oracle_quantize_q8(x, M, K, q, d) == 0;
+    for (int64_t i = 0; ok && i < M * K; ++i)
+        xq[i] = (double)d[(i / K) * (K / 32) + (i % K) / 32] * (double)q[i];
+    free(q);
+    free(d);
+    if (!ok) {
+        free(xq);
+        return NULL;
+    }
+    return xq;
+}
+
 int oracle_q8_matmul_rows(int qtype, const uint8_t *W, const uint16_t *x, int64_t M, int64_t K,
                           const int64_t *rows, int64_t n_rows, double *y)
 {
     if (!block_bytes(qtype) || M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
         return -1;
-    int8_t *q = (int8_t *)malloc((size_t)(M * K) + 1);
-    float *d = (float *)malloc((size_t)(M * (K / 32)) * sizeof(float) + 1);
-    double *xq = (double *)malloc((size_t)(M * K) * sizeof(double) + 1);
-    int rc = -2;
-    if (q && d && xq) {
-        rc = oracle_quantize_q8(x, M, K, q, d);
-        for (int64_t i = 0; rc == 0 && i < M * K; ++i)
-            xq[i] = (double)d[(i / K) * (K / 32) + (i % K) / 32] * (double)q[i];
-        if (rc == 0)
-            rc = matmul_core(qtype, W, xq, M, K, rows, n_rows, y);
-    }
-    free(q);
-    free(d);
+    double *xq = q8_values(x, M, K);
+    if (!xq)
+        return -2;
+    const int rc = matmul_core(qtype, W, xq, M, K, rows, n_rows, y);
+    free(xq);
+    return rc;
+}
+
+int oracle_q8_gateup_swiglu_rows(const uint8_t *Wg, const uint8_t *Wu, const uint16_t *x, int64_t M, int64_t K,
+                                 const int64_t *rows, int64_t n_rows, double *out)
+{
+    if (M < 0 || K <= 0 || K % ORACLE_QK || n_rows < 0)
+        return -1;
+    double *xq = q8_values(x, M, K);
+    if (!xq)
+        return -2;
+    const int rc = gateup_core(Wg, Wu, xq, M, K, rows, n_rows, out, NULL, NULL);
     free(xq);
     return rc;
 }

@@ -17,7 +17,8 @@ import os
 
 __all__ = [
     "QKError", "lib", "lib_path", "qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k",
-    "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout",
+    "qk_gateup_swiglu_q4k", "qk_matmul_batch", "qk_matmul_batch_q8x", "qk_matmul_q8x_q4k", "qk_matmul_q8x_q6k",
+    "qk_get_device_status", "qk_debug_wait_timeout",
     "qk_decode_uses_gemv", "qk_uses_gemv", "qk_gemm_plan", "qk_rmsnorm_matmul_batch", "qk_rmsnorm_matmul_q4k",
     "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes",
     "qk_rmsnorm_matmul_batch_static", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
@@ -28,7 +29,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 QK_BLOCK_BYTES = {"q4k": 144, "q6k": 210}
 
 SYMBOLS = ("qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k", "qk_gateup_swiglu_q4k",
-           "qk_matmul_batch", "qk_get_device_status", "qk_debug_wait_timeout", "qk_decode_uses_gemv",
+           "qk_matmul_batch", "qk_matmul_batch_q8x", "qk_matmul_q8x_q4k", "qk_matmul_q8x_q6k",
+           "qk_get_device_status", "qk_debug_wait_timeout", "qk_decode_uses_gemv",
            "qk_uses_gemv", "qk_gemm_plan", "qk_rmsnorm_matmul_batch", "qk_rmsnorm_matmul_q4k",
            "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes",
     "qk_rmsnorm_matmul_batch_static", "qk_status_string",
@@ -83,6 +85,10 @@ def lib():
         L.qk_gateup_swiglu_q4k.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
         L.qk_matmul_batch.restype = i32
         L.qk_matmul_batch.argtypes = [ctypes.POINTER(qk_matmul_desc), i32, vp]
+        L.qk_matmul_batch_q8x.restype = i32
+        L.qk_matmul_batch_q8x.argtypes = [ctypes.POINTER(qk_matmul_desc), i32, vp]
+        for f in (L.qk_matmul_q8x_q4k, L.qk_matmul_q8x_q6k):
+            f.restype, f.argtypes = i32, [vp, vp, vp, i64, i64, i64, vp]
         L.qk_get_device_status.restype, L.qk_get_device_status.argtypes = i32, [vp]
         L.qk_debug_wait_timeout.restype, L.qk_debug_wait_timeout.argtypes = i32, [i64, vp]
         L.qk_decode_uses_gemv.restype, L.qk_decode_uses_gemv.argtypes = i32, [i32, i32, i64]
@@ -225,6 +231,22 @@ def qk_matmul_batch(problems, stream=None) -> None:
     optionally up_blocks (fused gate/up + SwiGLU, fp16 y)."""
     arr = _descs(problems)
     _check(lib().qk_matmul_batch(arr, len(problems), _stream(stream)), "qk_matmul_batch")
+
+
+def qk_matmul_batch_q8x(problems, stream=None) -> None:
+    """qk_matmul_batch with int8 activations (decode only; see include/qk.h)."""
+    arr = _descs(problems)
+    _check(lib().qk_matmul_batch_q8x(arr, len(problems), _stream(stream)), "qk_matmul_batch_q8x")
+
+
+def qk_matmul_q8x_q4k(blocks, x_f16, y, M: int, N: int, K: int, stream=None) -> None:
+    """y = int8(x) . W^T for Q4_K W, M <= 1 (see include/qk.h)."""
+    qk_matmul_batch_q8x([dict(qtype=QK_Q4_K, blocks=blocks, x_f16=x_f16, y=y, M=M, N=N, K=K)], stream)
+
+
+def qk_matmul_q8x_q6k(blocks, x_f16, y, M: int, N: int, K: int, stream=None) -> None:
+    """y = int8(x) . W^T for Q6_K W, M <= 1 (see include/qk.h)."""
+    qk_matmul_batch_q8x([dict(qtype=QK_Q6_K, blocks=blocks, x_f16=x_f16, y=y, M=M, N=N, K=K)], stream)
 
 
 def qk_rmsnorm_scratch_bytes(qtype, M: int, K: int, gateup: bool = False) -> int:

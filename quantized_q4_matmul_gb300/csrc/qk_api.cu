@@ -327,6 +327,50 @@ qk_status qk_dequant_q6k(const void* blocks, int64_t n_blocks, float* out, qk_st
   return dequant(qk::kQ6K, blocks, n_blocks, out, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// int8 activations: validated problems with M <= 1, all on the decode GEMV
+// (a problem it cannot stage is refused: there is no other int8 path).
+qk_status matmul_batch_q8x(const qk_matmul_desc* d, int count, cudaStream_t s) {
+  if (count < 0) return QK_ERR_SHAPE;
+  if (count == 0) return QK_OK;
+  if (!d) return QK_ERR_NULL;
+  for (int i = 0; i < count; ++i)
+    if (d[i].M > 1) return QK_ERR_SHAPE;
+  std::vector<Checked> ck;
+  qk_status st = validate_batch(d, count, ck);
+  if (st != QK_OK) return st;
+  std::vector<qk::GemvDesc> group;
+  for (int i = 0; i < count; ++i) {
+    if (d[i].M == 0 || d[i].N == 0) continue;
+    qk::GemvDesc g{d[i].qtype == QK_Q4_K ? qk::kQ4K : qk::kQ6K, d[i].blocks, d[i].up_blocks, d[i].x_f16, d[i].y,
+                   1, d[i].N, d[i].K, nullptr, 0.f};
+    g.q8x = true;
+    if (!qk::gemv_plan_fits(&g, 1)) return QK_ERR_SHAPE;
+    group.push_back(g);
+    if ((int)group.size() == qk::kMaxGemvProbs) {
+      if ((st = map_cuda(qk::launch_gemv_batch(group.data(), (int)group.size(), s))) != QK_OK) return st;
+      group.clear();
+    }
+  }
+  if (!group.empty()) st = map_cuda(qk::launch_gemv_batch(group.data(), (int)group.size(), s));
+  return st;
+}
+
+qk_status qk_matmul_batch_q8x(const qk_matmul_desc* descs, int count, qk_stream_t stream) {
+  return matmul_batch_q8x(descs, count, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qk_status qk_matmul_q8x_q4k(const void* blocks, const uint16_t* x_f16, float* y, int64_t M, int64_t N, int64_t K,
+                            qk_stream_t stream) {
+  const qk_matmul_desc d{QK_Q4_K, blocks, nullptr, x_f16, y, M, N, K};
+  return qk_matmul_batch_q8x(&d, 1, stream);
+}
+
+qk_status qk_matmul_q8x_q6k(const void* blocks, const uint16_t* x_f16, float* y, int64_t M, int64_t N, int64_t K,
+                            qk_stream_t stream) {
+  const qk_matmul_desc d{QK_Q6_K, blocks, nullptr, x_f16, y, M, N, K};
+  return qk_matmul_batch_q8x(&d, 1, stream);
+}
+
 qk_status qk_matmul_q4k(const void* blocks, const uint16_t* x_f16, float* y, int64_t M, int64_t N, int64_t K,
                         qk_stream_t stream) {
   return matmul(qk::kQ4K, blocks, nullptr, x_f16, y, M, N, K, false, reinterpret_cast<cudaStream_t>(stream));

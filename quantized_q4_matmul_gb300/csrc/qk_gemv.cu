@@ -735,6 +735,157 @@ struct DecodeCtl {
   float rss[kMaxGemvM][kDW];    // its per-warp sums of squares
 };
 
+// ---------------------------------------------------------------------------
+// Q8 activations (one token): x is quantized per block of 32 to int8 with one
+// fp32 scale, d = amax / 127 and q = round(x / d) (IEEE fp32 division, ties
+// away from zero, clamped to +-127; d = 0 gives q = 0), and the products run
+// as integer dot products (dp4a: four int8 x times four quant bytes, int32
+// sum).  Per sub-block (Q4_K) or scale group (Q6_K) the integer sum is scaled
+// once in fp32.  x table: the int8 x in k order (K bytes), then per 32-block
+// {d, sum of q over its first 16 k, over its last 16, 0} (16 bytes).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+__device__ void build_x_table_q8(uint32_t xs, int K, uint32_t xq, uint32_t dt, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int b = warp; b < K / 32; b += kDW) {
+    uint32_t h;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=r"(h) : "r"(xs + 2u * (uint32_t)(32 * b + lane)));
+    const float v = half_lo(h);
+    float a = fabsf(v);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    const float d = __fdiv_rn(a, 127.0f);
+    int q = 0;
+    if (d != 0.0f) q = (int)fminf(fmaxf(roundf(__fdiv_rn(v, d)), -127.0f), 127.0f);
+    asm volatile("st.shared.s8 [%0], %1;" ::"r"(xq + (uint32_t)(32 * b + lane)), "r"(q) : "memory");
+    int s = q;
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);  // within each half of the warp
+    if (lane == 0) {
+      asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(dt + 16u * (uint32_t)b), "f"(d), "f"((float)s)
+                   : "memory");
+    } else if (lane == 16) {
+      asm volatile("st.shared.v2.f32 [%0], {%1, %2};" ::"r"(dt + 16u * (uint32_t)b + 8u), "f"((float)s), "f"(0.0f)
+                   : "memory");
+    }
+  }
+}
+
+// One Q4_K block of row r (address rb), lane half s (sub-blocks 4s .. 4s+3):
+// y += sum over those sub-blocks of d_x * (d*sc*IDOT - dmin*m*ISUM).
+__device__ __forceinline__ void q4_block_q8(uint32_t rb, uint32_t xa, uint32_t da, int s, float& y) {
+  const uint4 h = lds128(rb);
+  uint4 w4[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) w4[i] = lds128(rb + 16u + 64u * (uint32_t)s + 16u * (uint32_t)i);
+  uint4 x4[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x4[i] = lds128(xa + 16u * (uint32_t)i);
+  float4 D[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) D[i] = ldsf4(da + 16u * (uint32_t)i);
+  const uint32_t w[16] = {w4[0].x, w4[0].y, w4[0].z, w4[0].w, w4[1].x, w4[1].y, w4[1].z, w4[1].w,
+                          w4[2].x, w4[2].y, w4[2].z, w4[2].w, w4[3].x, w4[3].y, w4[3].z, w4[3].w};
+  const uint32_t X[32] = {x4[0].x, x4[0].y, x4[0].z, x4[0].w, x4[1].x, x4[1].y, x4[1].z, x4[1].w,
+                          x4[2].x, x4[2].y, x4[2].z, x4[2].w, x4[3].x, x4[3].y, x4[3].z, x4[3].w,
+                          x4[4].x, x4[4].y, x4[4].z, x4[4].w, x4[5].x, x4[5].y, x4[5].z, x4[5].w,
+                          x4[6].x, x4[6].y, x4[6].z, x4[6].w, x4[7].x, x4[7].y, x4[7].z, x4[7].w};
+  int acc[4] = {0, 0, 0, 0};  // sub-blocks 4s + t
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const uint32_t a = w[v], b = w[8 + v];  // groups 2s and 2s+1, bytes 4v .. 4v+3
+    acc[0] = dp4a_us(a & 0x0F0F0F0Fu, X[v], acc[0]);
+    acc[1] = dp4a_us((a >> 4) & 0x0F0F0F0Fu, X[8 + v], acc[1]);
+    acc[2] = dp4a_us(b & 0x0F0F0F0Fu, X[16 + v], acc[2]);
+    acc[3] = dp4a_us((b >> 4) & 0x0F0F0F0Fu, X[24 + v], acc[3]);
+  }
+  const float d = half_lo(h.x), dmin = half_lo(h.x >> 16);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    // sub-block j = 4s + t: bytes s[0..3] = h.y, s[4..7] = h.z, s[8..11] = h.w
+    uint32_t sc, m;
+    if (s == 0) {
+      sc = (h.y >> (8 * t)) & 63u;
+      m = (h.z >> (8 * t)) & 63u;
+    } else {
+      sc = ((h.w >> (8 * t)) & 15u) | (((h.y >> (8 * t + 6)) & 3u) << 4);
+      m = ((h.w >> (8 * t + 4)) & 15u) | (((h.z >> (8 * t + 6)) & 3u) << 4);
+    }
+    const float dsc = d * (float)sc, dmn = dmin * (float)m;
+    y = fmaf(D[t].x, fmaf(dsc, (float)acc[t], -dmn * (D[t].y + D[t].z)), y);
+  }
+}
+
+// Two consecutive words at shared address a (4-byte aligned, or 2 mod 4).
+__device__ __forceinline__ void lds_pair(uint32_t a, bool a2, uint32_t& w0, uint32_t& w1) {
+  if (!a2) {
+    w0 = lds32(a);
+    w1 = lds32(a + 4);
+  } else {
+    const uint32_t t0 = lds32(a - 2), t1 = lds32(a + 2), t2 = lds32(a + 6);
+    w0 = __funnelshift_r(t0, t1, 16);
+    w1 = __funnelshift_r(t1, t2, 16);
+  }
+}
+
+// One Q6_K block of row r (address rb), lane half h (weights 128h .. 128h+127,
+// scale groups 8h .. 8h+7): y += sum over the 8 groups of
+// d_x * d * sc * (IDOT(q6 + 32) - 32 * ISUM).
+__device__ __forceinline__ void q6_block_q8(uint32_t rb, uint32_t xa, uint32_t da, int h, float& y) {
+  const bool a2 = (rb & 3u) != 0;
+  uint32_t A[8], B[8], H[8];
+#pragma unroll
+  for (int v = 0; v < 8; v += 2) {
+    lds_pair(rb + 64u * (uint32_t)h + 4u * (uint32_t)v, a2, A[v], A[v + 1]);
+    lds_pair(rb + 64u * (uint32_t)h + 32u + 4u * (uint32_t)v, a2, B[v], B[v + 1]);
+    lds_pair(rb + 128u + 32u * (uint32_t)h + 4u * (uint32_t)v, a2, H[v], H[v + 1]);
+  }
+  uint32_t S[2], dw0, dw1;
+  lds_pair(rb + 192u + 8u * (uint32_t)h, a2, S[0], S[1]);
+  lds_pair(rb + 204u, a2, dw0, dw1);  // bytes 204..211: d is bytes 208..209
+  uint4 x4[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x4[i] = lds128(xa + 16u * (uint32_t)i);
+  float4 D[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) D[i] = ldsf4(da + 16u * (uint32_t)i);
+  const uint32_t X[32] = {x4[0].x, x4[0].y, x4[0].z, x4[0].w, x4[1].x, x4[1].y, x4[1].z, x4[1].w,
+                          x4[2].x, x4[2].y, x4[2].z, x4[2].w, x4[3].x, x4[3].y, x4[3].z, x4[3].w,
+                          x4[4].x, x4[4].y, x4[4].z, x4[4].w, x4[5].x, x4[5].y, x4[5].z, x4[5].w,
+                          x4[6].x, x4[6].y, x4[6].z, x4[6].w, x4[7].x, x4[7].y, x4[7].z, x4[7].w};
+  int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // [field g6][half of l]
+#pragma unroll
+  for (int v = 0; v < 8; ++v) {
+    const int hl = v >> 2;
+    const uint32_t a = A[v], b = B[v], q = H[v];
+    // 6-bit quants + 32 of fields 0..3 for l = 4v .. 4v+3, as unsigned bytes
+    const uint32_t q0 = (a & 0x0F0F0F0Fu) | ((q << 4) & 0x30303030u);
+    const uint32_t q1 = (b & 0x0F0F0F0Fu) | ((q << 2) & 0x30303030u);
+    const uint32_t q2 = ((a >> 4) & 0x0F0F0F0Fu) | (q & 0x30303030u);
+    const uint32_t q3 = ((b >> 4) & 0x0F0F0F0Fu) | ((q >> 2) & 0x30303030u);
+    acc[0 + hl] = dp4a_us(q0, X[v], acc[0 + hl]);
+    acc[2 + hl] = dp4a_us(q1, X[8 + v], acc[2 + hl]);
+    acc[4 + hl] = dp4a_us(q2, X[16 + v], acc[4 + hl]);
+    acc[6 + hl] = dp4a_us(q3, X[24 + v], acc[6 + hl]);
+  }
+  const float d = half_lo(dw1);  // bytes 208..209 are the low half of the second word
+#pragma unroll
+  for (int g6 = 0; g6 < 4; ++g6) {
+#pragma unroll
+    for (int hl = 0; hl < 2; ++hl) {
+      const int gi = 2 * g6 + hl;  // scale group 8h + gi
+      const int sc = (int)(int8_t)((S[gi >> 2] >> (8 * (gi & 3))) & 0xFFu);
+      const float isum = hl ? D[g6].z : D[g6].y;
+      y = fmaf(D[g6].x * (d * (float)sc), fmaf(-32.0f, isum, (float)acc[2 * g6 + hl]), y);
+    }
+  }
+}
+
 __device__ __forceinline__ float quad_sum(float v) {
   v += __shfl_xor_sync(0xffffffffu, v, 1);
   return v + __shfl_xor_sync(0xffffffffu, v, 2);
@@ -742,8 +893,9 @@ __device__ __forceinline__ float quad_sum(float v) {
 
 // Stage geometry of a decode problem (P.pair: two tiles of one tensor per
 // stage; P.cb: blocks per stage and row, nb for whole rows).
-template <int QT, int MT>
+template <int QT, int MT, bool Q8X>
 __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8_t* smem) {
+  static_assert(!Q8X || MT == 1, "int8 activations: one token");
   constexpr int kBB = QT == kQ4K ? kQ4KBytes : kQ6KBytes;
   constexpr int NT = MT / 8;  // several tokens: 8-token n-tiles of the MMA
   const int K = P.K, N = P.N, nb = K / kQK, cb = P.cb, S = P.stages;
@@ -917,7 +1069,9 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kDCompute) : "memory");
   }
-  if constexpr (MT == 1)
+  if constexpr (Q8X)
+    build_x_table_q8(xs, K, base, base + (uint32_t)K, tid);
+  else if constexpr (MT == 1)
     build_x_table<QT>(xs, gs, ctl->rnorm, K, base, sxt, zero, tid);
   else
     build_x_table_tn<QT, MT>(gs, ctl->rnorm, M, K, base, sxt, zero, tid);
@@ -935,7 +1089,44 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
   asm volatile("mov.b32 %0, %1;" : "=r"(fmagic) : "n"(kFMagic));
   const uint32_t ring_s = base + P.ring_off + (uint32_t)L.g * pitch;
 
-  if constexpr (MT == 1) {
+  if constexpr (Q8X) {
+    // lane (r, s): row r of the 16, weights 128s .. 128s+127 of every block
+    const int r = lane & 15, hs = lane >> 4;
+    const uint32_t ring_r = base + P.ring_off + (uint32_t)r * pitch;
+    const uint32_t xq = base + 128u * (uint32_t)hs, dq = base + (uint32_t)K + 64u * (uint32_t)hs;
+    float a0 = 0.f, a1 = 0.f;  // row r of row set 0, of row set 1 (this half)
+    for (int st = 0; st < steps; ++st) {
+      const int s = st % S, chunk = st % nchunks;
+      if (ok) ok = mbar_wait(&ctl->full[s], (uint32_t)(st / S) & 1u, &ctl->abort_flag, &g_gemv_status);
+      const int j0 = chunk * cb;
+      int b = warp - j0 % kDW;
+      if (b < 0) b += kDW;
+      const uint32_t stg = ring_r + (uint32_t)s * SB;
+      for (; ok && b < cb; b += kDW) {
+        const int j = j0 + b;
+        const uint32_t rb = stg + (uint32_t)(b * kBB);
+        const uint32_t xa = xq + 256u * (uint32_t)j, da = dq + 128u * (uint32_t)j;
+        if constexpr (QT == kQ4K) {
+          q4_block_q8(rb, xa, da, hs, a0);
+          if (ncomb == 2) q4_block_q8(rb + comb_bytes, xa, da, hs, a1);
+        } else {
+          q6_block_q8(rb, xa, da, hs, a0);
+          if (ncomb == 2) q6_block_q8(rb + comb_bytes, xa, da, hs, a1);
+        }
+      }
+      if (chunk == nchunks - 1) {
+        const float p0 = a0 + __shfl_xor_sync(0xffffffffu, a0, 16), p1 = a1 + __shfl_xor_sync(0xffffffffu, a1, 16);
+        if (lane < 16) {
+          float* q = red + ((size_t)s * kDW + warp) * redw;
+          q[r] = p0;
+          if (ncomb == 2) q[16 + r] = p1;
+        }
+        a0 = a1 = 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->empty[s]);
+    }
+  } else if constexpr (MT == 1) {
     {
       const int e = L.g & 1;
       const bool reads_x = (L.g >> 1) == L.tig;
@@ -1047,7 +1238,7 @@ __device__ __forceinline__ void decode_problem(const GemvProb& P, int cta, uint8
   }
 }
 
-template <int MT>
+template <int MT, bool Q8X>
 __global__ void __launch_bounds__(kDThreads, 1) gemv_decode_kernel(const __grid_constant__ GemvBatch B) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
@@ -1056,9 +1247,9 @@ __global__ void __launch_bounds__(kDThreads, 1) gemv_decode_kernel(const __grid_
   const GemvProb& P = B.p[i];
   const int cta = (int)blockIdx.x - P.cta_begin;
   if (P.qtype == kQ4K)
-    decode_problem<kQ4K, MT>(P, cta, smem);
+    decode_problem<kQ4K, MT, Q8X>(P, cta, smem);
   else
-    decode_problem<kQ6K, MT>(P, cta, smem);
+    decode_problem<kQ6K, MT, Q8X>(P, cta, smem);
 }
 
 }  // namespace
@@ -1119,8 +1310,10 @@ bool plan_decode_problem(const GemvDesc& d, GemvProb& P, size_t* smem_out) {
   const int bb = P.qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
   const int64_t RB = (int64_t)nb * bb;
   P.tiles = (P.N + 15) / 16;
-  const size_t xt = mt == 1 ? round128((size_t)nb * (kXtBlock + sx_block_bytes(P.qtype)))
-                            : round128((size_t)mt * 2 * P.K + (size_t)nb * (P.qtype == kQ4K ? 8 : 16) * mt * 4);
+  if (d.q8x && (mt != 1 || d.gamma)) return false;  // int8 activations: one token, no RMSNorm prologue
+  const size_t xt = d.q8x   ? round128((size_t)P.K + (size_t)(P.K / 32) * 16)
+                    : mt == 1 ? round128((size_t)nb * (kXtBlock + sx_block_bytes(P.qtype)))
+                              : round128((size_t)mt * 2 * P.K + (size_t)nb * (P.qtype == kQ4K ? 8 : 16) * mt * 4);
   P.ctl_off = (uint32_t)(xt + kZeroBytes);
   const uint32_t after_ctl = P.ctl_off + round128(sizeof(DecodeCtl));
   P.rawx_off = mt == 1 ? after_ctl : 0u;
@@ -1180,7 +1373,7 @@ bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* sm
   size_t smem = 0;
   for (int i = 0; i < count; ++i) {
     size_t s = 0;
-    if (slots_for(d[i].M) != slots_for(d[0].M)) return false;
+    if (slots_for(d[i].M) != slots_for(d[0].M) || d[i].q8x != d[0].q8x) return false;
     if (!plan_decode_problem(d[i], B.p[i], &s)) return false;
     smem = std::max(smem, s);
     const int bb = B.p[i].qtype == kQ4K ? kQ4KBytes : kQ6KBytes;
@@ -1212,13 +1405,13 @@ bool plan_gemv(const GemvDesc* d, int count, int sms, GemvBatch* out, size_t* sm
   return true;
 }
 
-template <int MT>
+template <int MT, bool Q8X>
 cudaError_t launch_decode(const GemvBatch& B, size_t smem, cudaStream_t s) {
   static PerDeviceFlag attr;  // the shared-memory limit is a per-device function attribute
   const int dev = current_device();
   if (!attr.done(dev)) {
     cudaError_t e =
-        cudaFuncSetAttribute(gemv_decode_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
+        cudaFuncSetAttribute(gemv_decode_kernel<MT, Q8X>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemvSmem);
     if (e != cudaSuccess) return e;
     attr.mark(dev);
   }
@@ -1239,10 +1432,10 @@ cudaError_t launch_decode(const GemvBatch& B, size_t smem, cudaStream_t s) {
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_decode_kernel<MT>, B);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemv_decode_kernel<MT, Q8X>, B);
   return e != cudaSuccess ? e : cudaGetLastError();
 #else
-  gemv_decode_kernel<MT><<<ctas, kDThreads, smem, s>>>(B);
+  gemv_decode_kernel<MT, Q8X><<<ctas, kDThreads, smem, s>>>(B);
   return cudaGetLastError();
 #endif
 }
@@ -1263,8 +1456,8 @@ cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s) {
   size_t smem = 0;
   if (!plan_gemv(d, count, device_sms(), &B, &smem)) return cudaErrorInvalidConfiguration;
   switch (slots_for(d[0].M)) {
-    case 1: return launch_decode<1>(B, smem, s);
-    default: return launch_decode<8>(B, smem, s);
+    case 1: return d[0].q8x ? launch_decode<1, true>(B, smem, s) : launch_decode<1, false>(B, smem, s);
+    default: return launch_decode<8, false>(B, smem, s);
   }
 }
 

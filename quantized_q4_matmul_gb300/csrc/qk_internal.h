@@ -96,6 +96,7 @@ struct GemvDesc {
   int64_t M, N, K;
   const uint16_t* gamma;  // RMSNorm prologue over x (fp16 gamma[K]), or null
   float eps;
+  bool q8x = false;       // x quantized to int8 per block of 32 (one token, no gamma)
 };
 cudaError_t launch_gemv_batch(const GemvDesc* d, int count, cudaStream_t s);
 

@@ -598,6 +598,19 @@ def pin_q8_error_bound_and_composition(O):
         assert np.all(np.abs(got - O.matmul(qt, W, x, N, K)) <= bound * (1 + 1e-9) + 1e-300)
 
 
+def pin_q8_gateup_composition(O):
+    """The int8-activation gate/up + SwiGLU equals silu(G) * U of the two
+    int8-activation matmuls (through scipy's expit)."""
+    from scipy.special import expit
+    rng = synth.rng_for(74, 0)
+    K, N = 512, 24
+    x = synth.activations(rng, 2, K)
+    Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+    G, U = O.q8_matmul(Q4K, Wg, x, N, K), O.q8_matmul(Q4K, Wu, x, N, K)
+    assert np.allclose(O.q8_gateup_swiglu(Wg, Wu, x, N, K), G * expit(G) * U, rtol=1e-12,
+                       atol=1e-14 * np.abs(G * U).max())
+
+
 def pin_q8_power_of_two_scaling(O):
     """Doubling x keeps every q and doubles every d exactly, so y doubles exactly."""
     rng = synth.rng_for(73, 0)
@@ -613,7 +626,7 @@ def pin_q8_power_of_two_scaling(O):
 
 ALL_PINS = [
     pin_q8_worked_block, pin_q8_grid_reproduces_fp16, pin_q8_error_bound_and_composition,
-    pin_q8_power_of_two_scaling,
+    pin_q8_power_of_two_scaling, pin_q8_gateup_composition,
     pin_rmsnorm_worked, pin_rmsnorm_constant_vector, pin_rmsnorm_unit_mean_square_and_scale_invariance,
     pin_rmsnorm_gamma_onehot, pin_rmsnorm_matmul_composition,
     pin_half_to_float,

@@ -201,3 +201,13 @@ def test_rmsnorm_rejects_bad_arguments_on_the_host(qk_lib):
     assert sb("q4k", 17, 3072) == 17 * 3072 * 2 and sb("q6k", 1024, 8192) == 1024 * 8192 * 2
     assert L.qk_rmsnorm_scratch_bytes(1, 1, 4, 256) == -1 and L.qk_rmsnorm_scratch_bytes(0, 0, 4, 300) == -1
 
+
+def test_q8x_rejects_on_the_host(qk_lib):
+    """int8 activations: several tokens and bad shapes are refused before any
+    pointer is looked at."""
+    L = qk_lib.lib()
+    assert L.qk_matmul_q8x_q4k(A16, A16, A16, 2, 8, 256, None) == -3   # M > 1
+    assert L.qk_matmul_q8x_q6k(A16, A16, A16, 1, 8, 300, None) == -3   # K % 256
+    assert L.qk_matmul_q8x_q4k(None, None, None, 0, 8, 256, None) == 0  # nothing to do
+    assert L.qk_matmul_batch_q8x(None, 0, None) == 0
+    assert L.qk_matmul_batch_q8x(None, 1, None) == -1
