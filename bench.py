@@ -69,28 +69,28 @@ def step_config(world):
                   % (N_COPIES, (decode_bytes() + 51.5e6 + 28e6) / 1e6)}
 
 
-def kernel_sources_sha():
-    """Hash of the CUDA sources, to tell whether stored ncu counters are current."""
+def kernel_sources_sha(names):
+    """Hash of the CUDA source files a kernel's device code is built from, to
+    tell whether stored ncu counters of that kernel are current."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_q4_matmul_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + b"\0" + f.read())
+    for name in sorted(names):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
     return h.hexdigest()
 
 
 def measured_traffic(key):
     """DRAM bytes per launch from an ncu capture (profiles/traffic.json), or None
-    if there is none or the kernels have changed since it was taken."""
+    if there is none or the kernel's sources have changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     e = d.get(key)
-    if not e or d.get("sources_sha256") != kernel_sources_sha():
+    if not e or e.get("sources_sha256") != kernel_sources_sha(e.get("sources", [])):
         return None
     return e.get("bytes_per_launch")
 
@@ -585,7 +585,25 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
                              "gemv_decode_kernel, %d layers per CUDA graph over %d weight copies (%d MB > L2)" % (
                                  4 * ncopy, ncopy, ncopy * layer_bytes >> 20))
     out["decode_layer_m1"] = {"grouped": grouped, "chained": chained, "per_linear": per, "steady": steady}
-    del Ws, xs, ys, probs, sets, ups
+
+    # int8 activations (qk_matmul_batch_q8x) beside the fp16 path: the grouped
+    # layer and the tied LM head (323 MB, more than L2), both as steady state
+    q8 = {}
+    ms = graph_steady(torch, stream, [lambda ps=ps: qk.qk_matmul_batch_q8x(
+        [dict(p) for p in ps if "up_blocks" not in p], s) for ps in sets], 4 * ncopy, reps)
+    q8["layer_grouped_steady"] = entry("decode layer, grouped, int8 x", layer_flops, layer_bytes, ms,
+                                       "gemv_decode_kernel (int8 activations), one launch per layer")
+    lm = synth.LM_HEAD
+    Wl = device_weights(torch, gen, lm.qtype, lm.N, lm.K, dev)
+    xl = x16(1, lm.K)
+    yl = torch.empty(1, lm.N, dtype=torch.float32, device=dev)
+    for name, call in (("lm_head_fp16", lambda: qk.qk_matmul_q6k(Wl, xl, yl, 1, lm.N, lm.K, s)),
+                       ("lm_head_int8x", lambda: qk.qk_matmul_q8x_q6k(Wl, xl, yl, 1, lm.N, lm.K, s))):
+        ms = graph_steady(torch, stream, [call], 8, reps)
+        q8[name + "_steady"] = entry("LM head, %s, steady" % name.split("_")[-1], 2.0 * lm.N * lm.K,
+                                     lin_bytes(lm, 1), ms, "gemv_decode_kernel, 8 launches per CUDA graph")
+    out["decode_int8_activations"] = q8
+    del Ws, xs, ys, probs, sets, ups, Wl
 
     # config 2: fused gate/up + SwiGLU at M = 1024
     g = synth.Linear("ffn_gate", synth.Q4K, synth.FFN, synth.HIDDEN)
@@ -919,6 +937,14 @@ def run_profile(args):
         "v": lambda: qk.qk_matmul_q6k(d["v"], d["x_v"], wl.y_v, PREFILL_M, v.N, v.K, s),
         "decode": lambda: wl.decode(qk, 0, s),
     }
+    if args.profile == "lmhead":
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(5)
+        lm = synth.LM_HEAD
+        Wl = device_weights(torch, gen, lm.qtype, lm.N, lm.K, dev)
+        xl = torch.from_numpy(synth.activations(synth.rng_for(5, 5), 1, lm.K).view(np.uint16)).to(dev)
+        yl = torch.empty(1, lm.N, dtype=torch.float32, device=dev)
+        calls["lmhead"] = lambda: qk.qk_matmul_q6k(Wl, xl, yl, 1, lm.N, lm.K, s)
     with torch.cuda.stream(stream):
         for _ in range(5):
             calls[args.profile]()
@@ -935,7 +961,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration measurements")
-    ap.add_argument("--profile", choices=["gateup", "down", "v", "decode"],
+    ap.add_argument("--profile", choices=["gateup", "down", "v", "decode", "lmhead"],
                     help="run one call of the step 5 times on one GPU and exit (for ncu)")
     args = ap.parse_args()
     if args.profile:
