@@ -1276,7 +1276,7 @@ constexpr size_t kGemvSmem = 227 * 1024;
 #endif
 constexpr double kQ6CostPerByte = QK_Q6_COST;
 
-// The token slots of the kernel that runs M tokens: 1 (decode layout), 8 or 16.
+// The token slots of the kernel that runs M tokens: 1 (decode layout) or 8.
 int slots_for(int64_t M) { return M <= 1 ? 1 : 8; }
 
 // The plan of one problem, from its shape only (so grouping problems never

@@ -728,8 +728,8 @@ def test_rmsnorm_gateup(qk_lib, cuda, M):
 
 @pytest.mark.parametrize("M", [1, 16, 64])
 def test_rmsnorm_batch_qkv(qk_lib, cuda, M):
-    """q, k, v share x and one RMSNorm: grouped on the GEMV (M <= 16), or
-    normalized once into the scratch for the three GEMMs (M = 64)."""
+    """q, k, v share x and one RMSNorm: grouped on the GEMV (M <= 8), or
+    normalized once into the scratch for the three GEMMs (M = 16, 64)."""
     import torch
     rng = synth.rng_for(M, 92)
     K = 3072
