@@ -6,9 +6,8 @@ its Python binding never import it.
 
 ``qk_oracle.c`` holds the arithmetic (GGUF Q4_K / Q6_K block decoding in fp32,
 fp64-accumulated matmul, fp64 SwiGLU, fp64 RMSNorm in front of a linear, int8
-activations per block of 32); this
-module only builds it with gcc and
-marshals numpy arrays through ctypes.
+activations per block of 32, fp64 GQA attention over a KV cache); this module
+only builds it with gcc and marshals numpy arrays through ctypes.
 """
 from __future__ import annotations
 
@@ -86,6 +85,11 @@ class Oracle:
         L.oracle_q8_gateup_swiglu_rows.restype = ctypes.c_int
         L.oracle_q8_gateup_swiglu_rows.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
                                                    ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
+        L.oracle_gqa_attention.restype = ctypes.c_int
+        L.oracle_gqa_attention.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                           ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int64,
+                                           ctypes.c_void_p]
         L.oracle_num_threads.restype = ctypes.c_int
         L.oracle_set_num_threads.argtypes = [ctypes.c_int]
         self.L = L
@@ -216,6 +220,23 @@ class Oracle:
         assert rc == 0, rc
         return out
 
+    def gqa_attention(self, q, k_cache, v_cache, H: int, Hkv: int, pos0: int, scale: float, qrows=None):
+        """fp64 GQA attention: q fp16 [M][H][D] (query i at position pos0 + i,
+        causal), caches fp16 [Hkv][L_max][D]; out [len(qrows)][H][D]."""
+        kc = np.ascontiguousarray(k_cache, dtype=np.float16)
+        vc = np.ascontiguousarray(v_cache, dtype=np.float16)
+        assert kc.shape == vc.shape and kc.ndim == 3 and kc.shape[0] == Hkv
+        Lmax, D = kc.shape[1], kc.shape[2]
+        q = np.ascontiguousarray(q, dtype=np.float16).reshape(-1, H, D)
+        M = q.shape[0]
+        r = _rows(M, qrows)
+        out = np.empty((r.size, H, D), dtype=np.float64)
+        rc = self.L.oracle_gqa_attention(_ptr(q.view(np.uint16)), _ptr(kc.view(np.uint16)), _ptr(vc.view(np.uint16)),
+                                         M, H, Hkv, D, int(pos0), Lmax, float(scale),
+                                         _ptr(r) if qrows is not None else None, r.size, _ptr(out))
+        assert rc == 0, rc
+        return out
+
 
 _default = None
 
@@ -273,3 +294,7 @@ def q8_matmul(qtype, W, x, N, K, rows=None):
 
 def q8_gateup_swiglu(Wg, Wu, x, N_ff, K, rows=None):
     return default().q8_gateup_swiglu(Wg, Wu, x, N_ff, K, rows)
+
+
+def gqa_attention(q, k_cache, v_cache, H, Hkv, pos0, scale, qrows=None):
+    return default().gqa_attention(q, k_cache, v_cache, H, Hkv, pos0, scale, qrows)

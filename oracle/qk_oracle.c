@@ -32,6 +32,11 @@
  *    in fp64, then the matmul above over xhat (not rounded to fp16).
  *  - Q8 activations (no counterpart in the pages): x quantized to int8 per
  *    block of 32 with one fp32 scale, then the matmul above over d * q.
+ *  - GQA attention over a KV cache (project overview, "[02] the pipeline",
+ *    compartment 06, and "[04] one decode step"; no formula is printed):
+ *    scaled dot-product attention, query head h reading key/value head
+ *    h / (H / H_kv), softmax over the causally visible positions, in fp64
+ *    from fp16 inputs widened exactly.
  *
  * Parity pins live in the test suite (hand-built blocks with closed forms,
  * bit-placement tables, an independent bit-level decoder, one-hot and all-ones
@@ -440,6 +445,70 @@ int oracle_q8_gateup_swiglu_rows(const uint8_t *Wg, const uint8_t *Wu, const uin
     const int rc = gateup_core(Wg, Wu, xq, M, K, rows, n_rows, out, NULL, NULL);
     free(xq);
     return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* GQA attention over a KV cache.                                             */
+/* q: [M][H][D] fp16; query i sits at position pos0 + i and sees positions    */
+/* 0 .. pos0 + i.  kc, vc: the caches, [H_kv][L_max][D] fp16 (head-major).    */
+/* For each selected query i (qrows, or all M if NULL) and head h, with       */
+/* g = h / (H / H_kv):                                                        */
+/*   s_j = scale * sum_d q[i][h][d] * k[g][j][d]                              */
+/*   p_j = exp(s_j - max s) / sum_j' exp(s_j' - max s)                        */
+/*   out[r][h][d] = sum_j p_j * v[g][j][d]                                    */
+/* every sum in fp64 in index order.                                          */
+/* ------------------------------------------------------------------------ */
+int oracle_gqa_attention(const uint16_t *q, const uint16_t *kc, const uint16_t *vc, int64_t M, int64_t H,
+                         int64_t Hkv, int64_t D, int64_t pos0, int64_t Lmax, double scale, const int64_t *qrows,
+                         int64_t n_qrows, double *out)
+{
+    if (M < 0 || H <= 0 || Hkv <= 0 || H % Hkv || D <= 0 || pos0 < 0 || pos0 + M > Lmax || n_qrows < 0)
+        return -1;
+    for (int64_t r = 0; qrows && r < n_qrows; ++r)
+        if (qrows[r] < 0 || qrows[r] >= M)
+            return -1;
+    const int64_t group = H / Hkv;
+    const int64_t nq = qrows ? n_qrows : M;
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+    for (int64_t rh = 0; rh < nq * H; ++rh) {
+        const int64_t r = rh / H, h = rh % H;
+        const int64_t i = qrows ? qrows[r] : r;
+        const int64_t g = h / group;
+        const int64_t n = pos0 + i + 1;
+        const uint16_t *qv = q + (i * H + h) * D;
+        double *s = (double *)malloc((size_t)n * sizeof(double));
+        if (!s) {
+            bad = 1;
+            continue;
+        }
+        double smax = -INFINITY;
+        for (int64_t j = 0; j < n; ++j) {
+            const uint16_t *kj = kc + (g * Lmax + j) * D;
+            double dot = 0.0;
+            for (int64_t d = 0; d < D; ++d)
+                dot += (double)oracle_half_to_float(qv[d]) * (double)oracle_half_to_float(kj[d]);
+            s[j] = scale * dot;
+            if (s[j] > smax)
+                smax = s[j];
+        }
+        double denom = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            s[j] = exp(s[j] - smax);
+            denom += s[j];
+        }
+        double *o = out + (r * H + h) * D;
+        for (int64_t d = 0; d < D; ++d)
+            o[d] = 0.0;
+        for (int64_t j = 0; j < n; ++j) {
+            const uint16_t *vj = vc + (g * Lmax + j) * D;
+            const double p = s[j] / denom;
+            for (int64_t d = 0; d < D; ++d)
+                o[d] += p * (double)oracle_half_to_float(vj[d]);
+        }
+        free(s);
+    }
+    return bad ? -2 : 0;
 }
 
 int oracle_num_threads(void)

@@ -19,6 +19,12 @@ What the pins rest on:
   form of a constant vector, unit mean square and exact invariance to scaling
   x by a power of two, a one-hot gamma, and the composition with the matmul
   and the SwiGLU against float64 library routines.
+* GQA attention: one visible position returns its value row exactly; equal
+  keys (or scale 0) give the mean of the visible value rows; a dominant key
+  returns its value row within the softmax's closed-form remainder; shifting
+  every key by one vector changes nothing; head h reads key/value head
+  h // (H / H_kv); future positions are never read; and a float64 numpy
+  restatement (einsum, scipy softmax, explicit causal mask) on random inputs.
 """
 from __future__ import annotations
 
@@ -624,7 +630,122 @@ def pin_q8_power_of_two_scaling(O):
     assert np.array_equal(O.q8_matmul(Q6K, W, x2, N, K), 2 * O.q8_matmul(Q6K, W, x, N, K))
 
 
+# ---------------------------------------------------------------------------
+# GQA attention over a KV cache
+# ---------------------------------------------------------------------------
+def _attn_inputs(rng, M, H, Hkv, D, Lmax, lo=-3, hi=4):
+    """Small-integer fp16 inputs (exact in fp16 and in every fp64 dot product)."""
+    q = rng.integers(lo, hi, size=(M, H, D)).astype(np.float16)
+    k = rng.integers(lo, hi, size=(Hkv, Lmax, D)).astype(np.float16)
+    v = rng.integers(-8, 9, size=(Hkv, Lmax, D)).astype(np.float16)
+    return q, k, v
+
+
+def pin_attn_single_position(O):
+    """Query at position 0 (one visible key): the output is v_0, exactly."""
+    rng = synth.rng_for(71, 0)
+    q, k, v = _attn_inputs(rng, 1, 4, 2, 8, 3)
+    out = O.gqa_attention(q, k, v, 4, 2, 0, 0.37)
+    for h in range(4):
+        assert np.array_equal(out[0, h], v[h // 2, 0].astype(np.float64))
+
+
+def pin_attn_uniform_weights(O):
+    """Equal keys, or scale 0: every visible position weighs 1/n, so each row
+    is the mean of the value rows 0 .. pos (math.fsum / n)."""
+    import math
+    rng = synth.rng_for(72, 0)
+    H, Hkv, D, M, pos0 = 6, 3, 8, 5, 2
+    q, k, v = _attn_inputs(rng, M, H, Hkv, D, pos0 + M)
+    keq = np.broadcast_to(k[:, :1, :], k.shape).copy()
+    for kk, scale in ((keq, 0.5), (k, 0.0)):
+        out = O.gqa_attention(q, kk, v, H, Hkv, pos0, scale)
+        for i in range(M):
+            n = pos0 + i + 1
+            for h in range(H):
+                g = h // (H // Hkv)
+                want = [math.fsum(float(v[g, j, d]) for j in range(n)) / n for d in range(D)]
+                assert np.allclose(out[i, h], want, rtol=0, atol=1e-12), (i, h)
+
+
+def pin_attn_dominant_key(O):
+    """One key aligned with q far above the others: the output is that key's
+    value row, up to the softmax remainder (n - 1) * exp(-margin) * max|v|."""
+    H, Hkv, D, L = 2, 1, 4, 6
+    q = np.zeros((1, H, D), np.float16)
+    q[0, :, 0] = 8
+    k = np.zeros((Hkv, L, D), np.float16)
+    k[0, 3, 0] = 8                      # s_3 = 64 * scale, every other s_j = 0
+    v = np.arange(Hkv * L * D, dtype=np.float16).reshape(Hkv, L, D)
+    scale = 0.75                        # margin 48
+    out = O.gqa_attention(q, k, v, H, Hkv, L - 1, scale)
+    bound = (L - 1) * np.exp(-64 * scale) * float(np.abs(v).max()) * 2
+    for h in range(H):
+        assert np.max(np.abs(out[0, h] - v[0, 3])) <= bound
+
+
+def pin_attn_key_shift_invariance(O):
+    """Adding one vector u to every key adds scale * q.u to every score of a
+    query, which the softmax removes: the outputs do not change."""
+    rng = synth.rng_for(73, 0)
+    H, Hkv, D, M, pos0 = 4, 2, 8, 4, 3
+    q, k, v = _attn_inputs(rng, M, H, Hkv, D, pos0 + M)
+    u = rng.integers(-2, 3, size=(Hkv, 1, D)).astype(np.float16)
+    a = O.gqa_attention(q, k, v, H, Hkv, pos0, 0.3)
+    b = O.gqa_attention(q, (k + u).astype(np.float16), v, H, Hkv, pos0, 0.3)
+    assert np.max(np.abs(a - b)) <= 1e-12 * float(np.abs(v).max())
+
+
+def pin_attn_gqa_head_mapping(O):
+    """Head h of an (H, H_kv) call equals a one-head call on key/value head
+    h // (H / H_kv) alone."""
+    rng = synth.rng_for(74, 0)
+    H, Hkv, D, M, pos0 = 6, 2, 8, 3, 1
+    q, k, v = _attn_inputs(rng, M, H, Hkv, D, pos0 + M)
+    out = O.gqa_attention(q, k, v, H, Hkv, pos0, 0.2)
+    for h in range(H):
+        g = h // (H // Hkv)
+        one = O.gqa_attention(np.ascontiguousarray(q[:, h:h + 1]), k[g:g + 1], v[g:g + 1], 1, 1, pos0, 0.2)
+        assert np.array_equal(out[:, h], one[:, 0]), h
+
+
+def pin_attn_causal(O):
+    """Query i never reads positions after pos0 + i: changing them (and the
+    cache beyond the last query) leaves its row unchanged."""
+    rng = synth.rng_for(75, 0)
+    H, Hkv, D, M, pos0, Lmax = 4, 2, 8, 4, 2, 9
+    q, k, v = _attn_inputs(rng, M, H, Hkv, D, Lmax)
+    a = O.gqa_attention(q, k, v, H, Hkv, pos0, 0.4)
+    for i in range(M):
+        k2, v2 = k.copy(), v.copy()
+        k2[:, pos0 + i + 1:] = 3
+        v2[:, pos0 + i + 1:] = -7
+        b = O.gqa_attention(q, k2, v2, H, Hkv, pos0, 0.4, qrows=[i])
+        assert np.array_equal(a[i], b[0]), i
+
+
+def pin_attn_vs_numpy(O):
+    """Random fp16 inputs against a float64 numpy restatement."""
+    from scipy.special import softmax
+    rng = synth.rng_for(76, 0)
+    H, Hkv, D, M, pos0, Lmax = 6, 2, 16, 5, 7, 14
+    q = rng.standard_normal((M, H, D)).astype(np.float16)
+    k = rng.standard_normal((Hkv, Lmax, D)).astype(np.float16)
+    v = rng.standard_normal((Hkv, Lmax, D)).astype(np.float16)
+    scale = 1 / np.sqrt(D)
+    out = O.gqa_attention(q, k, v, H, Hkv, pos0, scale)
+    kk = np.repeat(k.astype(np.float64), H // Hkv, axis=0)  # [H][Lmax][D]
+    vv = np.repeat(v.astype(np.float64), H // Hkv, axis=0)
+    s = scale * np.einsum("mhd,hjd->mhj", q.astype(np.float64), kk)
+    visible = np.arange(Lmax)[None, :] <= (pos0 + np.arange(M))[:, None]
+    s = np.where(visible[:, None, :], s, -np.inf)
+    want = np.einsum("mhj,hjd->mhd", softmax(s, axis=-1), vv)
+    assert np.allclose(out, want, rtol=0, atol=1e-12)
+
+
 ALL_PINS = [
+    pin_attn_single_position, pin_attn_uniform_weights, pin_attn_dominant_key, pin_attn_key_shift_invariance,
+    pin_attn_gqa_head_mapping, pin_attn_causal, pin_attn_vs_numpy,
     pin_q8_worked_block, pin_q8_grid_reproduces_fp16, pin_q8_error_bound_and_composition,
     pin_q8_power_of_two_scaling, pin_q8_gateup_composition,
     pin_rmsnorm_worked, pin_rmsnorm_constant_vector, pin_rmsnorm_unit_mean_square_and_scale_invariance,

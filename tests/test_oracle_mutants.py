@@ -77,6 +77,16 @@ MUTANTS = [
     ("q8_scale_of_64", "(double)d[(i / K) * (K / 32) + (i % K) / 32]", "(double)d[(i / K) * (K / 32) + (i % K) / 64]"),
     ("q8_amax_signed", "const float v = fabsf(oracle_half_to_float(xb[i]));",
      "const float v = oracle_half_to_float(xb[i]);"),
+    # GQA attention
+    ("attn_group_modulo", "const int64_t g = h / group;", "const int64_t g = h % Hkv;"),
+    ("attn_sees_one_less", "const int64_t n = pos0 + i + 1;", "const int64_t n = pos0 + i + (i > 0);"),
+    ("attn_sees_one_more", "const int64_t n = pos0 + i + 1;", "const int64_t n = pos0 + i + 1 + (pos0 + i + 1 < Lmax);"),
+    ("attn_scale_dropped", "s[j] = scale * dot;", "s[j] = dot;"),
+    ("attn_not_normalized", "const double p = s[j] / denom;", "const double p = s[j];"),
+    ("attn_token_major_cache", "const uint16_t *kj = kc + (g * Lmax + j) * D;",
+     "const uint16_t *kj = kc + (j * Hkv + g) * D;"),
+    ("attn_values_are_keys", "const uint16_t *vj = vc + (g * Lmax + j) * D;",
+     "const uint16_t *vj = kc + (g * Lmax + j) * D;"),
 ]
 
 
