@@ -242,6 +242,32 @@ qk_status qk_rmsnorm_matmul_batch_static(const qk_matmul_desc *descs, int count,
 int64_t qk_rmsnorm_scratch_bytes(int qtype, int gateup, int64_t M, int64_t K);
 
 /*
+ * Grouped-query attention over a KV cache (DAMASCUS project overview, "[02]
+ * the pipeline", compartment 06: a decoder layer is GQA with a KV cache; "[04]
+ * one decode step": after the QKV projections and RoPE, attention over the
+ * cache).  The pages print no formula; this is scaled dot-product attention:
+ * for query i (0 <= i < M) at position pos0 + i and query head h, with
+ * g = h / (H / H_kv) its key/value head,
+ *   s_j = scale * sum_d q[i][h][d] * k_cache[g][j][d]   for j = 0 .. pos0 + i,
+ *   out[i][h][d] = sum_j softmax(s)_j * v_cache[g][j][d].
+ * q_f16: [M][H][D] fp16 (RoPE already applied); k_cache, v_cache: [H_kv][L_max][D]
+ * fp16, positions 0 .. pos0 + M - 1 filled (those of the M queries included);
+ * out: [M][H][D] fp32.  D must be 128, H a multiple of H_kv with H / H_kv <= 8,
+ * pos0 + M <= L_max; all pointers device memory, 16-byte aligned; out may not
+ * overlap an input.  M = 1 (a decode step) splits the cache over a cluster of
+ * up to 8 CTAs per key/value head; M >= 2 (prefill, or a chunk of it after
+ * pos0 cached positions) runs causal 64-query blocks.  Both score on the
+ * tensor cores (fp16 operands, fp32 sums) and round the softmax weights to
+ * fp16 for the P.V product: the result is within about 2^-10 * max|v| of the
+ * exact value.  M = 0 is a no-op.  Errors: QK_ERR_SHAPE, QK_ERR_NULL, QK_ERR_ALIGN, QK_ERR_ALIAS,
+ * QK_ERR_POINTER, QK_ERR_UNSUPPORTED_DEVICE before anything is enqueued;
+ * QK_ERR_CUDA if the launch fails.
+ */
+qk_status qk_gqa_attention(const uint16_t *q_f16, const uint16_t *k_cache, const uint16_t *v_cache, float *out,
+                           int64_t M, int64_t H, int64_t H_kv, int64_t D, int64_t pos0, int64_t L_max, float scale,
+                           qk_stream_t stream);
+
+/*
  * Synchronise `stream`, then report and clear the device-side status flags
  * that the library's kernels set when a bounded wait expires.  Returns QK_OK,
  * QK_ERR_TIMEOUT, or QK_ERR_CUDA if the synchronisation itself failed.

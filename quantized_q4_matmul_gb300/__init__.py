@@ -22,7 +22,7 @@ __all__ = [
     "qk_decode_uses_gemv", "qk_uses_gemv", "qk_gemm_plan", "qk_rmsnorm_matmul_batch", "qk_rmsnorm_matmul_q4k",
     "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes",
     "qk_rmsnorm_matmul_batch_static", "qk_status_string", "qk_version", "QK_BLOCK_BYTES", "qk_matmul_desc",
-    "qk_gemm_plan_info",
+    "qk_gemm_plan_info", "qk_gqa_attention",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -34,7 +34,7 @@ SYMBOLS = ("qk_dequant_q4k", "qk_dequant_q6k", "qk_matmul_q4k", "qk_matmul_q6k",
            "qk_uses_gemv", "qk_gemm_plan", "qk_rmsnorm_matmul_batch", "qk_rmsnorm_matmul_q4k",
            "qk_rmsnorm_matmul_q6k", "qk_rmsnorm_gateup_swiglu_q4k", "qk_rmsnorm_scratch_bytes",
     "qk_rmsnorm_matmul_batch_static", "qk_status_string",
-           "qk_version")
+           "qk_version", "qk_gqa_attention")
 
 QK_Q4_K, QK_Q6_K = 0, 1
 
@@ -106,6 +106,8 @@ def lib():
         L.qk_rmsnorm_matmul_batch_static.argtypes = [ctypes.POINTER(qk_matmul_desc), i32, vp, f32, vp]
         L.qk_gemm_plan.restype = i32
         L.qk_gemm_plan.argtypes = [i32, i32, i64, i64, i64, ctypes.POINTER(qk_gemm_plan_info)]
+        L.qk_gqa_attention.restype = i32
+        L.qk_gqa_attention.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, vp]
         L.qk_status_string.restype, L.qk_status_string.argtypes = ctypes.c_char_p, [i32]
         L.qk_version.restype, L.qk_version.argtypes = i32, []
         _lib = L
@@ -351,6 +353,20 @@ def qk_gemm_plan(qtype, M: int, N: int, K: int, gateup: bool = False) -> dict:
     _check(lib().qk_gemm_plan(int(qt), int(bool(gateup)), int(M), int(N), int(K), ctypes.byref(info)),
            "qk_gemm_plan")
     return {n: getattr(info, n) for n, _ in qk_gemm_plan_info._fields_}
+
+
+def qk_gqa_attention(q_f16, k_cache, v_cache, out, M: int, H: int, H_kv: int, D: int, pos0: int, L_max: int,
+                     scale: float, stream=None) -> None:
+    """GQA attention over a KV cache (see include/qk.h): q [M][H][D] fp16,
+    caches [H_kv][L_max][D] fp16, out [M][H][D] fp32."""
+    what = "qk_gqa_attention"
+    qn = _n(M) * _n(H) * _n(D)
+    cn = _n(H_kv) * _n(L_max) * _n(D)
+    _check(lib().qk_gqa_attention(_buf(q_f16, 2 * qn, what + ": q_f16", _F16),
+                                  _buf(k_cache, 2 * cn, what + ": k_cache", _F16),
+                                  _buf(v_cache, 2 * cn, what + ": v_cache", _F16),
+                                  _buf(out, 4 * qn, what + ": out", _F32), int(M), int(H), int(H_kv), int(D),
+                                  int(pos0), int(L_max), float(scale), _stream(stream)), what)
 
 
 def qk_get_device_status(stream=None) -> None:

@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libqk.so")
-SOURCES = ["qk_api.cu", "qk_dequant.cu", "qk_gemv.cu", "qk_gemm_tc.cu", "qk_norm.cu"]
+SOURCES = ["qk_api.cu", "qk_attn.cu", "qk_dequant.cu", "qk_gemv.cu", "qk_gemm_tc.cu", "qk_norm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr"]

@@ -458,9 +458,35 @@ qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream) {
   return map_cuda(qk::launch_wait_probe((uint64_t)limit_ns, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+qk_status qk_gqa_attention(const uint16_t* q_f16, const uint16_t* k_cache, const uint16_t* v_cache, float* out,
+                           int64_t M, int64_t H, int64_t H_kv, int64_t D, int64_t pos0, int64_t L_max, float scale,
+                           qk_stream_t stream) {
+  if (M < 0 || H <= 0 || H_kv <= 0 || H % H_kv != 0 || H / H_kv > 8 || D != 128 || pos0 < 0 || L_max <= 0 ||
+      M > L_max - pos0 || H > 1024 || L_max >= ((int64_t)1 << 31))
+    return QK_ERR_SHAPE;
+  if (M == 0) return QK_OK;
+  if (!q_f16 || !k_cache || !v_cache || !out) return QK_ERR_NULL;
+  if (!aligned16(q_f16) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out)) return QK_ERR_ALIGN;
+  int64_t q_elems, c_elems, q_bytes, c_bytes, o_bytes;
+  if (!mul_ok(M * H, D, &q_elems) || !mul_ok(q_elems, 2, &q_bytes) || !mul_ok(q_elems, 4, &o_bytes) ||
+      !mul_ok(H_kv * L_max, D, &c_elems) || !mul_ok(c_elems, 2, &c_bytes))
+    return QK_ERR_SHAPE;
+  qk_status st = check_device();
+  if (st != QK_OK) return st;
+  if ((st = check_pointer(q_f16)) != QK_OK || (st = check_pointer(k_cache)) != QK_OK ||
+      (st = check_pointer(v_cache)) != QK_OK || (st = check_pointer(out)) != QK_OK)
+    return st;
+  if (overlaps(out, o_bytes, q_f16, q_bytes) || overlaps(out, o_bytes, k_cache, c_bytes) ||
+      overlaps(out, o_bytes, v_cache, c_bytes))
+    return QK_ERR_ALIAS;
+  return map_cuda(qk::launch_gqa_attention(q_f16, k_cache, v_cache, out, M, (int)H, (int)H_kv, pos0, L_max, scale,
+                                           reinterpret_cast<cudaStream_t>(stream)));
+}
+
 qk_status qk_get_device_status(qk_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QK_ERR_CUDA;
-  const uint32_t v = qk::dequant_take_status() | qk::gemv_take_status() | qk::gemm_take_status();
+  const uint32_t v =
+      qk::dequant_take_status() | qk::gemv_take_status() | qk::gemm_take_status() | qk::attn_take_status();
   return v ? QK_ERR_TIMEOUT : QK_OK;
 }
 

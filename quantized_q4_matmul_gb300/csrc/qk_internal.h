@@ -72,6 +72,18 @@ cudaError_t launch_rmsnorm_rows(const uint16_t* x, const uint16_t* gamma, float 
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;
 cudaError_t static_scratch_address(void** out);
 
+// Encode a tiled TMA tensor map of fp16 elements into `out` (a CUtensorMap,
+// 64 bytes): `rank` dimensions innermost first, the byte strides of
+// dimensions 1.. (rank - 1 of them), the box, and a 128-byte swizzle or none.
+// Elements outside the dimensions read as zero.  False if the driver refuses.
+bool encode_tensor_map_f16(void* out, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                           const uint32_t* box, bool swizzle128);
+
+// GQA attention (qk_gqa_attention); arguments validated.  Device status word.
+cudaError_t launch_gqa_attention(const uint16_t* q, const uint16_t* kc, const uint16_t* vc, float* out, int64_t M,
+                                 int H, int Hkv, int64_t pos0, int64_t Lmax, float scale, cudaStream_t s);
+uint32_t attn_take_status();
+
 // A kernel whose single bounded wait can never complete (see qk_debug_wait_timeout).
 cudaError_t launch_wait_probe(uint64_t limit_ns, cudaStream_t s);
 
