@@ -489,6 +489,52 @@ def device_weights(torch, gen, qtype, N, K, dev):
     return blk.view(-1)
 
 
+ATTN_L = 4096  # cached positions of the decode-step attention
+
+
+def attention_inputs(torch, dev, M, pos0, L, seed):
+    """q [M][24][128] and caches [8][L][128], fp16 N(0, 1), seeded."""
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed)
+    H, Hkv, Dh = synth.N_HEADS, synth.N_KV_HEADS, synth.HEAD_DIM
+    q = torch.randn(M, H, Dh, device=dev, generator=gen).half()
+    k = torch.randn(Hkv, L, Dh, device=dev, generator=gen).half()
+    v = torch.randn(Hkv, L, Dh, device=dev, generator=gen).half()
+    return q, k, v
+
+
+def measure_attention(torch, qk, dev, stream, reps, entry):
+    """GQA attention of the 3B model (24 query / 8 key-value heads, head dim
+    128, scale 1/sqrt(128)): one decode step over ATTN_L cached positions
+    (rotating caches larger than L2, CUDA graph) and a causal prefill of
+    PREFILL_M tokens (CUDA graph)."""
+    H, Hkv, Dh = synth.N_HEADS, synth.N_KV_HEADS, synth.HEAD_DIM
+    s = stream.cuda_stream
+    scale = 1.0 / np.sqrt(Dh)
+    res = {}
+    L = ATTN_L
+    kvb = 2 * Hkv * L * Dh * 2
+    nc = max(2, int(np.ceil(3 * L2_BYTES / kvb)))
+    sets = [attention_inputs(torch, dev, 1, L - 1, L, 90 + i) for i in range(nc)]
+    o = torch.empty(1, H, Dh, device=dev)
+    ms = graph_steady(torch, stream, [lambda q=q, k=k, v=v: qk.qk_gqa_attention(q, k, v, o, 1, H, Hkv, Dh, L - 1, L, scale, s)
+                                      for q, k, v in sets], 4 * nc, reps)
+    res["decode_L%d" % L] = entry("attention decode L=%d" % L, 4.0 * H * Dh * L, kvb + H * Dh * 6, ms,
+                                  "attn_decode_kernel (cluster split of the cache, tensor-core scores), "
+                                  "%d steps per CUDA graph over %d caches" % (4 * nc, nc))
+    del sets
+    M = PREFILL_M
+    q, k, v = attention_inputs(torch, dev, M, 0, M, 99)
+    o = torch.empty(M, H, Dh, device=dev)
+    ms = graph_steady(torch, stream, [lambda: qk.qk_gqa_attention(q, k, v, o, M, H, Hkv, Dh, 0, M, scale, s)], 8, reps)
+    res["prefill_M%d" % M] = entry("attention prefill M=%d" % M, 4.0 * H * Dh * M * (M + 1) / 2,
+                                   2 * M * H * Dh + 2 * 2 * Hkv * M * Dh + 4 * M * H * Dh, ms,
+                                   "attn_prefill_kernel<3> (causal 64-query blocks, mma.sync), 8 per CUDA graph")
+    res["note"] = ("flops count the causal dot products (4 * H * D per visible query-key pair); decode bytes = "
+                   "the key and value cache read once")
+    return res
+
+
 def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
     """Every workload configuration with its own roofline fraction:
     config 0 (attn_q M=16), config 1 (the decode layer: grouped, chained and per
@@ -521,7 +567,7 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
 
     def kernel_of(qtype, M, K, gateup=False):
         if qk.qk_uses_gemv(qtype, M, K, gateup):
-            return "gemv_decode_kernel (decode GEMV)" if M == 1 else "gemv_stream_kernel (several-token GEMV)"
+            return "gemv_decode_kernel (decode GEMV)" if M == 1 else "gemv_decode_kernel (2..8 tokens in the MMA columns)"
         return "gemm_tc_kernel (tcgen05 GEMM)"
 
     # config 0: attn_q, M = 16
@@ -608,6 +654,8 @@ def measure_configs(torch, qk, dev, stream, reps, pk, log=print):
                                      lin_bytes(lm, 1), ms, "gemv_decode_kernel, 8 launches per CUDA graph")
     out["decode_int8_activations"] = q8
     del Ws, xs, ys, probs, sets, ups, Wl
+
+    out["attention"] = measure_attention(torch, qk, dev, stream, reps, entry)
 
     # config 2: fused gate/up + SwiGLU at M = 1024
     g = synth.Linear("ffn_gate", synth.Q4K, synth.FFN, synth.HIDDEN)
@@ -947,6 +995,20 @@ def run_profile(args):
         xl = torch.from_numpy(synth.activations(synth.rng_for(5, 5), 1, lm.K).view(np.uint16)).to(dev)
         yl = torch.empty(1, lm.N, dtype=torch.float32, device=dev)
         calls["lmhead"] = lambda: qk.qk_matmul_q6k(Wl, xl, yl, 1, lm.N, lm.K, s)
+    if args.profile == "dequant":
+        g = decode_linears()[4]  # ffn_gate, Q4_K 8192 x 3072: 14 MB in, 100 MB out
+        nbk = g.N * g.K // 256
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(6)
+        Wq = device_weights(torch, gen, g.qtype, g.N, g.K, dev)
+        dq_out = torch.empty(nbk * 256, dtype=torch.float32, device=dev)
+        calls["dequant"] = lambda: qk.qk_dequant_q4k(Wq, nbk, dq_out, s)
+    if args.profile in ("attn_decode", "attn_prefill"):
+        H, Hkv, Dh = synth.N_HEADS, synth.N_KV_HEADS, synth.HEAD_DIM
+        M, L = (1, ATTN_L) if args.profile == "attn_decode" else (PREFILL_M, PREFILL_M)
+        qa, ka, va = attention_inputs(torch, dev, M, L - M, L, 7)
+        oa = torch.empty(M, H, Dh, device=dev)
+        calls[args.profile] = lambda: qk.qk_gqa_attention(qa, ka, va, oa, M, H, Hkv, Dh, L - M, L, 1 / np.sqrt(Dh), s)
     with torch.cuda.stream(stream):
         for _ in range(5):
             calls[args.profile]()
@@ -963,7 +1025,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the per-configuration measurements")
-    ap.add_argument("--profile", choices=["gateup", "down", "v", "decode", "lmhead"],
+    ap.add_argument("--profile", choices=["gateup", "down", "v", "decode", "lmhead", "dequant", "attn_decode",
+                                          "attn_prefill"],
                     help="run one call of the step 5 times on one GPU and exit (for ncu)")
     args = ap.parse_args()
     if args.profile:
