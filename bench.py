@@ -529,7 +529,8 @@ def measure_attention(torch, qk, dev, stream, reps, entry):
     ms = graph_steady(torch, stream, [lambda: qk.qk_gqa_attention(q, k, v, o, M, H, Hkv, Dh, 0, M, scale, s)], 8, reps)
     res["prefill_M%d" % M] = entry("attention prefill M=%d" % M, 4.0 * H * Dh * M * (M + 1) / 2,
                                    2 * M * H * Dh + 2 * 2 * Hkv * M * Dh + 4 * M * H * Dh, ms,
-                                   "attn_prefill_kernel<3> (causal 64-query blocks, mma.sync), 8 per CUDA graph")
+                                   "attn_prefill_tc_kernel (tcgen05: S, P and O in tensor memory; causal 128-query "
+                                   "blocks), 8 per CUDA graph")
     res["note"] = ("flops count the causal dot products (4 * H * D per visible query-key pair); decode bytes = "
                    "the key and value cache read once")
     return res

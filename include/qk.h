@@ -256,10 +256,10 @@ int64_t qk_rmsnorm_scratch_bytes(int qtype, int gateup, int64_t M, int64_t K);
  * pos0 + M <= L_max; all pointers device memory, 16-byte aligned; out may not
  * overlap an input.  M = 1 (a decode step) splits the cache over a cluster of
  * up to 8 CTAs per key/value head; M >= 2 (prefill, or a chunk of it after
- * pos0 cached positions) runs causal 64-query blocks.  Both score on the
- * tensor cores (fp16 operands, fp32 sums) and round the softmax weights to
- * fp16 for the P.V product: the result is within about 2^-10 * max|v| of the
- * exact value.  M = 0 is a no-op.  Errors: QK_ERR_SHAPE, QK_ERR_NULL, QK_ERR_ALIGN, QK_ERR_ALIAS,
+ * pos0 cached positions) runs causal 128-query blocks on tcgen05.  Both score
+ * on the tensor cores (fp16 operands, fp32 sums) and round the softmax weights
+ * to fp16 for the P.V product: the result is within about 2^-10 * max|v| of
+ * the exact value.  M = 0 is a no-op.  Errors: QK_ERR_SHAPE, QK_ERR_NULL, QK_ERR_ALIGN, QK_ERR_ALIAS,
  * QK_ERR_POINTER, QK_ERR_UNSUPPORTED_DEVICE before anything is enqueued;
  * QK_ERR_CUDA if the launch fails.
  */
