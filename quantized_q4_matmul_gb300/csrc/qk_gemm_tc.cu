@@ -84,6 +84,15 @@ constexpr int kQ6Win = 240;
 #endif
 constexpr uint32_t kCopyBackoffNs = QK_GEMM_BACKOFF_NS;
 
+// Deepest x-tile ring of single-tensor problems (even, <= 8) and deepest
+// packed-block ring (<= 4).
+#ifndef QK_GEMM_MAX_X
+#define QK_GEMM_MAX_X 8
+#endif
+#ifndef QK_GEMM_MAX_P
+#define QK_GEMM_MAX_P 2
+#endif
+
 template <int QT, bool GATEUP>
 struct Cfg {
   // Dequant warps: two threads per weight row and tensor (each dequantizes
@@ -396,9 +405,8 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
   const int64_t RB = (int64_t)nb * (QT == kQ4K ? kQ4KBytes : kQ6KBytes);
   RingPos pos = {0, 0u};   // A slot of K step 4i of this CTA (Q4_K: the current step)
   RingPos ppos = {0, 0u};  // packed stage of super-block i
-  // Q4_K: done barrier of step - SA (ring D >= SA, one lap back at the start,
-  // so the first SA waits return at once).  Q6_K runs with D == SA and uses
-  // the A slot (phase flipped) directly.
+  // Done barrier of step - SA (ring D >= SA, one lap back at the start, so
+  // the first SA waits return at once); Q6_K: of step 4i - SA.
   RingPos dd = {D - SA, 1u};
   bool ok = true;
   for (int i = 0; i < nkb && ok; ++i, ring_advance(ppos, 1, P)) {
@@ -442,18 +450,22 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
       q6_load_dispatch(mis, pst + q6_slot(rho, q6g), part, q);
       if constexpr (AT) __syncwarp();  // rows of one warp may differ in alignment (tcgen05.st below is collective)
       mbar_arrive(&bars->p_empty[ps]);
-      RingPos sp = pos;  // K step 4i + 2*part
+      RingPos sp = pos, sd = dd;  // A slot of K step 4i + 2*part, done barrier of that step - SA
       ring_advance(sp, 2 * part, SA);
+      ring_advance(sd, 2 * part, D);
 #pragma unroll
       for (int side = 0; side < 2; ++side) {
-        if (side == 1) ring_advance(sp, 1, SA);
+        if (side == 1) {
+          ring_advance(sp, 1, SA);
+          ring_advance(sd, 1, D);
+        }
         const int s = sp.slot;
         uint32_t r[32];
         if (side == 0)
           q6_side<0>(q, r);
         else
           q6_side<1>(q, r);
-        ok = mbar_wait(&bars->done[s], sp.phase ^ 1u, abort_flag, &g_gemm_status);
+        ok = mbar_wait(&bars->done[sd.slot], sd.phase, abort_flag, &g_gemm_status);
         if constexpr (AT) {
           ok = __all_sync(0xffffffffu, ok);  // tcgen05.st is warp-collective
           if (!ok) break;
@@ -474,6 +486,7 @@ __device__ __forceinline__ bool dequant_loop(uint8_t* smem, const Layout& L, Bar
         mbar_arrive(&bars->a_full[s]);
       }
       ring_advance(pos, 4, SA);
+      ring_advance(dd, 4, D);
     }
   }
   return ok;
@@ -1053,23 +1066,36 @@ struct TcPlan {
 
 // Pipeline depths (all measured on GB300).  The K-step rings come first: a
 // single-tensor kernel with fewer than 4 x-tile stages ran ~35 % slower.
-// Single-tensor problems grow A-tile and x-tile stages alternately, A first
-// and never fewer A than x stages; gate/up grows x stages first (its issuers
-// waited on x tiles while its dequant threads had slack: 3 x + 2 A stages
-// ran 12 % faster than 2 + 3).  Up to 5 A and 4 x stages (deeper rings were
-// no faster, and slower for Q6_K attn_v), while shared memory (and, with A
-// in tensor memory, TMEM) allows.  Two packed-block stages where the rings still reach 4 x
-// stages next to them (cold-cache Q6_K ran faster with two), else one (the
-// dequant threads copy a super-block to registers and release its slot at
-// once, so the refill overlaps the block's four K steps).
+// Single-tensor problems grow A-tile and x-tile stages alternately, A first,
+// up to 4 x stages (x stages alone once a TMEM-capped A ring stops growing),
+// then x stages two at a time up to kMaxXDeep.  A per-CTA trace of Q6_K down
+// showed the issuers waiting on x tiles (0.4-0.75 us from a tile's load to
+// its barrier, and a slot is refilled only once the UMMAs of its previous
+// step have completed); 6-8 stages took Q4_K o-proj M = 1024 from 21.0 to
+// 19.4 us and Q6_K attn_v M = 128 from 17.4 to 15.2 us, other shapes within
+// 2 %.  The ring stays even: the two issuers take alternate K steps, so each
+// keeps to its own slots and waits on every phase of them (with an odd ring
+// an issuer would skip the phases of the other's steps, and x tiles can land
+// out of order, so a parity wait could pass on a slot's previous tile).
+// Gate/up grows x stages first (its issuers waited on x tiles while its
+// dequant threads had slack: 3 x + 2 A stages ran 12 % faster than 2 + 3),
+// up to 4.  Up to 5 A stages, while shared memory (and, with A in tensor
+// memory, TMEM) allows.  Packed-block stages: two where they fit next to 4 x
+// stages (cold-cache Q6_K ran faster with two; three or four gained nothing
+// in steady state), else one (the dequant threads copy a super-block to
+// registers and release its slot at once, so the refill overlaps the
+// block's four K steps).
 // Q6_K takes 4 A stages.  Its threads write two consecutive K steps of a
 // super-block and the two halves of a row alternate.  With SA = 2 a half
 // waits on a slot whose previous phase (the other half's step) it never
 // saw, so the parity test can pass a phase early (seen on GB300 as wrong
 // output once the packed copies ran ahead).  From SA = 3 on, the phase a
 // half skips belongs to an earlier step of the same issuer, whose UMMAs
-// complete in order, so it has always completed.  Q6_K keeps SX <= SA (its
-// done ring is indexed by A slot), and its x ring wants 4 stages.
+// complete in order, so it has always completed.  Its done-barrier ring
+// D = max(SX, SA) is even (4, 6 or 8): the next completion of the slot a half
+// waits on is then a later step of the same issuer, which cannot run before
+// the half has written its own step (with D = 5 it would be the other half's
+// next step, which can complete first, and the wait would never pass).
 // Returns false when the A tiles do not fit in tensor memory next to the
 // accumulators (the caller then keeps them in shared memory).
 template <int QT, bool GATEUP, bool AT>
@@ -1077,6 +1103,10 @@ bool plan_tc(int64_t M, int64_t N, TcPlan* out) {
   using C = Cfg<QT, GATEUP>;
   const int BN = choose_bn(M, N);
   constexpr int kMaxXStages = 4, kMaxAStages = QT == kQ6K ? 4 : 5;
+  constexpr int kMaxXDeep = GATEUP ? kMaxXStages : QK_GEMM_MAX_X;
+  static_assert(kMaxXDeep <= 8 && kMaxXDeep % 2 == 0, "x ring capacity");
+  constexpr int kMaxP = QK_GEMM_MAX_P;
+  static_assert(kMaxP >= 1 && kMaxP <= 4, "packed ring capacity");
   auto depths = [&](int P_, int& SX_, int& SA_) {
     auto fits = [&](int sx, int sa) {
       return make_layout<QT, GATEUP, AT>(BN, sx, sa, P_).total <= (uint32_t)kSmemLimit &&
@@ -1102,18 +1132,30 @@ bool plan_tc(int64_t M, int64_t N, TcPlan* out) {
         grew = true;
       }
     }
+    if (!GATEUP) {
+      while (SX_ < kMaxXStages && fits(SX_ + 1, SA_)) ++SX_;  // x stages past a TMEM-capped A ring
+      if (SX_ == kMaxXStages)
+        while (SX_ + 2 <= kMaxXDeep && fits(SX_ + 2, SA_)) SX_ += 2;
+      if (SX_ & 1) --SX_;  // the issuers alternate: each keeps to its own x slots
+    }
   };
-  int P = 2, SX, SA;
-  depths(P, SX, SA);
-  if (SX < kMaxXStages) {
-    int sx1, sa1;
-    depths(1, sx1, sa1);
-    if (sx1 > SX || (sx1 == SX && sa1 > SA)) {
-      P = 1;
-      SX = sx1;
-      SA = sa1;
+  // Packed stages: the most x stages up to 4 first, then the most packed
+  // stages up to kMaxP, then the deepest x ring, then the deepest A ring.
+  int P = 1, SX = 0, SA = 0;
+  auto score = [&](int p_, int sx, int sa) {
+    return ((std::min(sx, kMaxXStages) * 8 + p_) * 16 + sx) * 16 + sa;
+  };
+  for (int p_ = 1; p_ <= kMaxP; ++p_) {
+    int sx, sa;
+    depths(p_, sx, sa);
+    if (make_layout<QT, GATEUP, AT>(BN, sx, sa, p_).total > (uint32_t)kSmemLimit) continue;
+    if (SX == 0 || score(p_, sx, sa) > score(P, SX, SA)) {
+      P = p_;
+      SX = sx;
+      SA = sa;
     }
   }
+  if (SX == 0) return false;
   if (AT && (kIssuers * BN + SA * C::kNumB * 32 > 512 || (QT == kQ6K && SA != 4))) return false;
   const Layout L = make_layout<QT, GATEUP, AT>(BN, SX, SA, P);
   uint32_t sm_smem, reserved;

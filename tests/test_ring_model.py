@@ -30,9 +30,12 @@ awaited one.
 A second model checks Q4_K with an x ring and an A ring of different depths.
 The two rings share one done ring of max(SX, SA) barriers, indexed by K step.
 It covers gate/up, where both issuers take every step and a phase needs both
-commits, and single-tensor problems, where the issuers alternate.
+commits, and single-tensor problems, where the issuers alternate.  A third
+adds the issuers' own parity waits on the x and A slots, x tiles that land
+in any order, and the Q6_K halves on the done ring: it shows why a
+single-tensor x ring is even.
 
-A third model checks the GEMV's ring: a producer warp that refills a stage
+A last model checks the GEMV's ring: a producer warp that refills a stage
 after the compute warps release it and first adds their per-tile partial
 sums, and compute warps that read stages and leave partials in them.  A
 control drops the producer's wait and shows that the model then catches the
@@ -198,6 +201,115 @@ def test_q4k_x_and_a_rings_never_pass_early(sx, sa, gateup):
     """Separate x and A ring depths over one done ring of max(SX, SA): no wait
     passes early and nothing deadlocks (gate/up runs 3 x + 2 A stages)."""
     assert not any(simulate_xa(sx, sa, gateup, seed=s) for s in range(800))
+
+
+def simulate_rings(sx, sa, gateup, q6k, blocks=5, seed=0):
+    """The GEMM's three rings with parity waits everywhere, as the kernel runs
+    them: x tiles (SX slots; the producer loads step t after waiting for
+    done(t - SX), and loads in flight land in any order), A tiles (SA slots;
+    the writers write step t after waiting for done(t - SA); Q4_K one writer
+    of every step in order, Q6_K two halves, part p writing 4i+2p and
+    4i+2p+1), and one done ring of D = max(SX, SA) barriers indexed by K step.
+    An issuer waits on the x and A slots of its step by parity (gate/up: both
+    issuers take every step and a done phase needs both commits; one tensor:
+    the issuers alternate).  Returns "early" if a wait passed before the
+    phase it waits for had completed, "stuck" if every party waits on a
+    phase that has been overtaken (a deadlock), else None."""
+    rng = random.Random(seed)
+    d = max(sx, sa)
+    steps = 4 * blocks
+    need = 2 if gateup else 1
+    done_c, done_n = [0] * d, [0] * d
+    x_c, a_c = [0] * sx, [0] * sa  # completed phases of x_full / a_full per slot
+    if q6k:
+        writers = [[4 * i + 2 * p + j for i in range(blocks) for j in range(2)] for p in range(2)]
+    else:
+        writers = [list(range(steps))]
+    wpos = [0] * len(writers)
+    xp = 0
+    in_flight = []
+    issued = [[False] * steps for _ in range(2)]
+    fooled = False
+
+    def wait_done(t, lag):  # (parity passes, passed early) for done(t - lag)
+        if t < lag:
+            return True, False
+        u = t - lag
+        k, c = u // d, done_c[u % d]
+        return (c & 1) != (k & 1), c <= k
+
+    def wait_slot(cnt, n, t):  # the slot of step t in a ring of n, phase t // n
+        k, c = t // n, cnt[t % n]
+        return (c & 1) != (k & 1), c <= k
+
+    while True:
+        acts = []
+        if xp < steps and wait_done(xp, sx)[0]:
+            acts.append(("x", None))
+        for i in range(len(in_flight)):
+            acts.append(("land", i))
+        for w, lst in enumerate(writers):
+            if wpos[w] < len(lst) and wait_done(lst[wpos[w]], sa)[0]:
+                acts.append(("a", w))
+        for e in range(2):
+            order = range(steps) if gateup else range(e, steps, 2)
+            t = next((u for u in order if not issued[e][u]), None)
+            if t is not None and wait_slot(x_c, sx, t)[0] and wait_slot(a_c, sa, t)[0]:
+                acts.append(("issue", (e, t)))
+        if not acts:
+            break
+        kind, arg = rng.choice(acts)
+        if kind == "x":
+            fooled |= wait_done(xp, sx)[1]
+            in_flight.append(xp)
+            xp += 1
+        elif kind == "land":
+            t = in_flight.pop(arg)
+            x_c[t % sx] += 1
+        elif kind == "a":
+            t = writers[arg][wpos[arg]]
+            fooled |= wait_done(t, sa)[1]
+            a_c[t % sa] += 1
+            wpos[arg] += 1
+        else:
+            e, t = arg
+            fooled |= wait_slot(x_c, sx, t)[1] or wait_slot(a_c, sa, t)[1]
+            issued[e][t] = True
+            done_n[t % d] += 1
+            if done_n[t % d] == need:
+                done_n[t % d] = 0
+                done_c[t % d] += 1
+        if fooled:
+            return "early"  # what follows a wrong pass is not the kernel's protocol
+    if xp < steps or any(p < len(w) for p, w in zip(wpos, writers)):
+        return "stuck"
+    return None
+
+
+# The plans the host picks (x stages, A stages): single-tensor Q4_K and Q6_K
+# with even x rings up to 8, gate/up with up to 4 x stages.
+@pytest.mark.parametrize("sx,sa,gateup,q6k", [
+    (4, 4, False, False), (4, 5, False, False), (6, 2, False, False), (6, 3, False, False),
+    (8, 4, False, False), (8, 5, False, False), (2, 2, False, False),
+    (4, 4, False, True), (6, 4, False, True), (8, 4, False, True),
+    (2, 2, True, False), (3, 2, True, False), (4, 2, True, False), (3, 3, True, False), (4, 4, True, False)])
+def test_rings_never_pass_early_nor_stall(sx, sa, gateup, q6k):
+    assert all(simulate_rings(sx, sa, gateup, q6k, seed=s) is None for s in range(400))
+
+
+def test_odd_x_ring_with_alternating_issuers_can_pass_early():
+    """Why single-tensor x rings are even: with an odd ring an issuer skips
+    the phases of the other issuer's steps, and an x tile landing out of
+    order lets its parity wait pass on the slot's previous tile."""
+    assert any(simulate_rings(3, 4, False, False, seed=s) == "early" for s in range(3000))
+
+
+def test_odd_done_ring_can_stall_q6k():
+    """Q6_K with an odd done ring (D = 5): a half waits on done(t - 4) in the
+    slot that step t + 1 -- the other half's, already written and issued --
+    completes next, so the barrier can run two phases past the wait, which
+    then never passes."""
+    assert any(simulate_rings(5, 4, False, True, seed=s) == "stuck" for s in range(3000))
 
 
 class Bar:
