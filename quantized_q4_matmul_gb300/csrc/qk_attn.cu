@@ -394,8 +394,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
   TcShared& S = *reinterpret_cast<TcShared*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nqb = (int)((M + kTQ - 1) / kTQ);
-  const int qb = nqb - 1 - (int)blockIdx.x;  // the longest query blocks first
-  const int h = (int)blockIdx.y, g = h / G;
+  // Launch order is x fastest: every head's longest query block first, then
+  // the next longest of every head, so the short blocks fill the last wave.
+  const int qb = nqb - 1 - (int)blockIdx.y;
+  const int h = (int)blockIdx.x, g = h / G;
   const int64_t q0 = (int64_t)qb * kTQ;
   const int64_t last_q = q0 + kTQ - 1 < M - 1 ? q0 + kTQ - 1 : M - 1;
   const int nt = (int)((pos0 + last_q) / kTK) + 1;
@@ -727,7 +729,9 @@ cudaError_t launch_gqa_attention(const uint16_t* q, const uint16_t* kc, const ui
       if (e != cudaSuccess) return e;
       attr_set.mark(dev);
     }
-    const dim3 grid((unsigned)((M + kTQ - 1) / kTQ), (unsigned)H);
+    const int64_t nqb = (M + kTQ - 1) / kTQ;
+    if (nqb > 65535) return cudaErrorInvalidConfiguration;
+    const dim3 grid((unsigned)H, (unsigned)nqb);
     attn_prefill_tc_kernel<<<grid, kTThreads, tc_smem(), s>>>(tq, tk, tv, out, H, G, M, pos0, sl2e);
     return cudaGetLastError();
   }
