@@ -29,10 +29,11 @@
 // stages) and A tiles (SA stages), the last two released per K step by the
 // step's UMMA commit (done barriers, a ring of max(SX, SA)).  Grids that
 // would leave half of the SMs idle split K across a thread-block cluster of
-// 2..8 CTAs per tile: each peer sends its fp32 partial tile to CTA 0 with one
-// bulk shared::cluster copy, and CTA 0 adds them in a fixed order (no global
-// scratch, deterministic).  All waits are bounded mbarrier waits; a timeout
-// raises a device status flag and the CTA drains and exits.
+// 2..8 CTAs per tile: each CTA owns a slice of the tile's token columns,
+// receives the peers' fp32 partials of that slice by bulk shared::cluster
+// copies and adds them in rank order (no global scratch, deterministic).
+// All waits are bounded mbarrier waits; a timeout raises a device status flag
+// and the CTA drains and exits.
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -121,7 +122,7 @@ struct Bars {  // capacity: 8 x / A stages, 4 packed stages
   uint64_t p_full[4];
   uint64_t p_empty[4];
   uint64_t acc_full;
-  uint64_t peer_full;  // split K, CTA 0: the peers' partial tiles have landed
+  uint64_t peer_full;  // split K: the peers' partial slices of this CTA's token chunks have landed
   uint32_t tmem_base;
   uint32_t abort_flag;
 };
@@ -148,6 +149,36 @@ __host__ __device__ inline Layout make_layout(int BN, int SX, int SA, int P) {
 }
 
 
+
+// Split-K exchange geometry.  The tile's BN / 16 token chunks are dealt to the
+// ks CTAs of a cluster in contiguous slices; a slot holds one slice's partial
+// sums for kNumB tensors: [tensor][128 rows][slice chunks x 16 fp32], rows
+// padded by 16 bytes so a warp's 16-byte accesses to 32 consecutive rows
+// spread over all banks.
+__host__ __device__ inline uint32_t split_slot_pitch(int BN, int ks) {
+  return (uint32_t)((BN / 16 + ks - 1) / ks) * 64u + 16u;
+}
+template <int kNumB>
+__host__ __device__ inline uint32_t split_slot_bytes(int BN, int ks) {
+  return (uint32_t)kNumB * 128u * split_slot_pitch(BN, ks);
+}
+// Rank zz's slice is chunks [c(zz), c(zz + 1)) of n = BN / 16, with
+// c(zz) = ceil(zz * n / ks) (rank 0 always owns a chunk); with fewer chunks
+// than ranks some slices are empty, and those ranks receive nothing.
+// min(ks, n) ranks own a slice; below rank zz there are min(zz, c(zz)) owners.
+__host__ __device__ inline int split_chunk(int zz, int BN, int ks) { return (zz * (BN / 16) + ks - 1) / ks; }
+__host__ __device__ inline bool split_owns(int zz, int BN, int ks) {
+  return split_chunk(zz + 1, BN, ks) > split_chunk(zz, BN, ks);
+}
+// Shared memory of the exchange: an owner keeps ks - 1 receive slots, then
+// one send slot per other owner; a rank without a slice only sends, one slot
+// per owner from the start of the region.
+template <int kNumB>
+__host__ __device__ inline uint32_t split_exchange_bytes(int BN, int ks) {
+  const int owners = ks < BN / 16 ? ks : BN / 16;
+  const int slots = ks - 2 + owners > owners ? ks - 2 + owners : owners;
+  return (uint32_t)slots * split_slot_bytes<kNumB>(BN, ks);
+}
 
 struct Params {
   const uint8_t* w[2];  // packed weights (gate, up)
@@ -597,9 +628,8 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
     mbar_init(&bars->peer_full, 1);
     bars->abort_flag = 0;
     fence_mbar_init();
-    if (p.ksplit > 1 && z == 0)  // split K: the bytes of the peers' partial tiles
-      mbar_arrive_expect_tx(&bars->peer_full,
-                            (uint32_t)((p.ksplit - 1) * C::kNumB) * 128u * ((uint32_t)BN * 4 + 16));
+    if (p.ksplit > 1 && split_owns(z, BN, p.ksplit))  // split K: the ks - 1 partial slices this CTA receives
+      mbar_arrive_expect_tx(&bars->peer_full, (uint32_t)(p.ksplit - 1) * split_slot_bytes<C::kNumB>(BN, p.ksplit));
   }
   // Accumulators: one per issuer, BN columns each (gate / up, or even / odd K
   // steps); with AT also SA x kNumB A tiles of 32 columns (128 rows x 64 fp16)
@@ -763,108 +793,163 @@ __global__ void __launch_bounds__(Cfg<QT, GATEUP>::kThreads, 1)
 
   // ---------------------------------------------------------------- epilogue
   // Dequant warp w reads TMEM lane quarter w % 4 (rows 32q .. 32q+31); the
-  // warps sharing a quarter split the BN / 16 column chunks.
+  // warps sharing a quarter take alternate 16-column chunks.
   const bool dq_warp = warp >= C::kDqWarp0 && warp < C::kDqWarp0 + C::kDqWarps;
   const int q = warp & 3;
   const int row = q * 32 + lane;
+  const int n = n0 + row;
   const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
   const int nchunks = BN / 16;
   const int ngroups = C::kDqWarps / 4, grp = (warp - C::kDqWarp0) >> 2;
-  const int per = (nchunks + ngroups - 1) / ngroups;
-  const int c_begin = min(nchunks, grp * per), c_end = min(nchunks, c_begin + per);
-  // Split K: CTA z > 0 writes its partial tile(s) (one tensor: D0 + D1;
-  // gate/up: G and U; [tensor][row][BN] fp32 with rows padded by 16 bytes so a warp's
-  // 16-byte accesses to 32 consecutive rows spread over all banks) into its
-  // own stage region, free once its main loop is done, and one bulk copy moves
-  // it into slot z - 1 of CTA 0's stage region (after the first cluster
-  // barrier, i.e. once CTA 0 is past its main loop).  CTA 0 armed peer_full
-  // with the bytes of all peers at start; the second cluster barrier keeps the
-  // peers (the copies' sources) alive until CTA 0 has seen them land.  CTA 0
-  // adds the partials in a fixed order.  (Element-wise remote stores were
-  // measured ~3.5 us slower per tile.)
-  const uint32_t peer_buf = smem_u32(smem);
-  const uint32_t peer_pitch = (uint32_t)BN * 4 + 16;
-  const uint32_t peer_slot = (uint32_t)C::kNumB * 128 * peer_pitch;  // one peer's partials
+  // The result of chunk cc: one tensor's value (va), or gate (va) and up (vb).
+  auto store_chunk = [&](int cc, const uint32_t (&va)[16], const uint32_t (&vb)[16]) {
+    if (n >= p.N) return;
+    if constexpr (!GATEUP) {
+      float* y = static_cast<float*>(p.y);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int m = m0 + 16 * cc + i;
+        if (m < p.M) y[(int64_t)m * p.N + n] = __uint_as_float(va[i]);
+      }
+    } else {
+      __half* y = static_cast<__half*>(p.y);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int m = m0 + 16 * cc + i;
+        const float g = __uint_as_float(va[i]), u = __uint_as_float(vb[i]);
+        // silu(g) * u with sigmoid(g) = 0.5 + 0.5 tanh(g / 2): one
+        // special-function op per element instead of two (exp and a
+        // reciprocal); the epilogue was bound by that unit.
+        const float hg = 0.5f * g;
+        const float o = fmaf(hg, tanh_approx(hg), hg) * u;
+        if (m < p.M) y[(int64_t)m * p.N + n] = __float2half_rn(o);
+      }
+    }
+  };
+  // This CTA's partial of chunk cc from tensor memory: one tensor, D0 + D1
+  // (its even and odd K steps) in va; gate/up, G in va and U in vb.
+  auto own_chunk = [&](int cc, uint32_t (&va)[16], uint32_t (&vb)[16]) {
+    tmem_ld16(lane_addr + (uint32_t)(16 * cc), va);
+    tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), vb);
+    tmem_wait_ld();
+    if constexpr (!GATEUP) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) va[i] = __float_as_uint(__uint_as_float(va[i]) + __uint_as_float(vb[i]));
+    }
+  };
   const int ksplit = KS ? p.ksplit : 1;
   if (KS && ksplit > 1) {
+    // Split K, reduce-scatter: CTA zz of the cluster owns the chunks
+    // [cz(zz), cz(zz + 1)).  Each CTA writes its partial of every peer's
+    // chunks into a send slot of its own stage region (free once its main loop
+    // is done); after the first cluster barrier (every CTA past its main loop)
+    // one bulk copy per peer moves the slot into that peer's receive slot for
+    // this sender, completing on the peer's peer_full (armed at start with the
+    // bytes of its ks - 1 incoming slots).  The second cluster barrier, once
+    // every owner has seen its slots land, lets the CTAs (the copies' sources)
+    // exit; each owner then adds the ks partials of its chunks in rank order
+    // (deterministic) from its own tensor and shared memory and writes them.
+    // split_chunk without a division per call: num / ks == (num * kinv) >> 16
+    // for ks <= 8 and num <= 8 * 16 + 7 (checked for every case on the host)
+    const uint32_t kinv = (65536u + (uint32_t)ksplit - 1u) / (uint32_t)ksplit;
+    auto cz = [&](int zz) { return (int)(((uint32_t)(zz * nchunks + ksplit - 1) * kinv) >> 16); };
+    auto owns = [&](int zz) { return cz(zz + 1) > cz(zz); };
+    const uint32_t xbuf = smem_u32(smem);
+    const uint32_t pitch = split_slot_pitch(BN, ksplit);
+    const uint32_t slot = split_slot_bytes<C::kNumB>(BN, ksplit);
+    const bool owner = owns(z);
+    auto recv_slot = [&](int dst, int src) { return xbuf + (uint32_t)(src < dst ? src : src - 1) * slot; };
+    auto send_slot = [&](int d) {  // d: an owning peer; owners below d: min(d, cz(d))
+      const int below = d < cz(d) ? d : cz(d);
+      const int j = below - (owner && z < d ? 1 : 0);
+      return xbuf + (uint32_t)((owner ? ksplit - 1 : 0) + j) * slot;
+    };
     __syncwarp();        // each warp arrives converged (the cluster barrier is .aligned)
     cluster_sync_all();  // every CTA of the cluster is past its main loop
-    if (dq_warp && z > 0) {
+    // an owner whose peers own nothing (fewer chunks than ranks) sends nothing
+    const bool sends = (ksplit < nchunks ? ksplit : nchunks) > (owner ? 1 : 0);
+    if (dq_warp && sends) {
       if (dq_ok) {
         tc_fence_after();
-        for (int cc = c_begin; cc < c_end; ++cc) {
-          uint32_t r0[16], r1[16];
-          tmem_ld16(lane_addr + (uint32_t)(16 * cc), r0);
-          tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), r1);
-          tmem_wait_ld();
-          const uint32_t a = peer_buf + (uint32_t)row * peer_pitch + (uint32_t)(64 * cc);
-          if constexpr (!GATEUP) {
+        for (int d = 0; d < ksplit; ++d) {
+          if (d == z || !owns(d)) continue;
+          for (int cc = cz(d) + grp; cc < cz(d + 1); cc += ngroups) {
+            uint32_t va[16], vb[16];
+            own_chunk(cc, va, vb);
+            const uint32_t a = send_slot(d) + (uint32_t)row * pitch + (uint32_t)(64 * (cc - cz(d)));
 #pragma unroll
-            for (int i = 0; i < 16; ++i) r0[i] = __float_as_uint(__uint_as_float(r0[i]) + __uint_as_float(r1[i]));
-          }
+            for (int i = 0; i < 4; ++i) sts128_u(a + 16 * i, va[4 * i], va[4 * i + 1], va[4 * i + 2], va[4 * i + 3]);
+            if constexpr (GATEUP) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) sts128_u(a + 16 * i, r0[4 * i], r0[4 * i + 1], r0[4 * i + 2], r0[4 * i + 3]);
-          if constexpr (GATEUP) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              sts128_u(a + 128 * peer_pitch + 16 * i, r1[4 * i], r1[4 * i + 1], r1[4 * i + 2], r1[4 * i + 3]);
+              for (int i = 0; i < 4; ++i)
+                sts128_u(a + 128 * pitch + 16 * i, vb[4 * i], vb[4 * i + 1], vb[4 * i + 2], vb[4 * i + 3]);
+            }
           }
         }
       }
-      fence_proxy_async_smem();  // plain writes, read by the bulk copy (async proxy)
-      named_bar_sync(1, 32 * C::kDqWarps);
-      if (threadIdx.x == 32 * C::kDqWarp0)
-        bulk_copy_s2cluster(mapa_shared(peer_buf + (uint32_t)(z - 1) * peer_slot, 0u), peer_buf, peer_slot,
-                            mapa_shared(smem_u32(&bars->peer_full), 0u));
+      fence_proxy_async_smem();  // plain writes, read by the bulk copies (async proxy)
     }
-    if (dq_warp && z == 0) {  // the peers always send, so this wait ends (bounded in any case)
+    if (dq_warp) named_bar_sync(1, 32 * C::kDqWarps);  // every send slot of this CTA is written
+    if (threadIdx.x == 32 * C::kDqWarp0) {
+      // every owning peer always receives from every other rank, so its wait
+      // ends (bounded in any case)
+      for (int d = 0; d < ksplit; ++d)
+        if (d != z && owns(d))
+          bulk_copy_s2cluster(mapa_shared(recv_slot(d, z), (uint32_t)d), send_slot(d), slot,
+                              mapa_shared(smem_u32(&bars->peer_full), (uint32_t)d));
+    }
+    if (dq_warp && owner) {
       const bool landed = mbar_wait(&bars->peer_full, 0u, abort_flag, &g_gemm_status, true);
       dq_ok = __all_sync(0xffffffffu, dq_ok && landed);
     }
     __syncwarp();
-    cluster_sync_all();  // the peers may exit: their copies have landed
-  }
-  if (dq_warp && dq_ok && z == 0) {
-    tc_fence_after();
-    const int n = n0 + row;
-    for (int cc = c_begin; cc < c_end; ++cc) {
-      // ra / rb: one tensor's even / odd K steps, or gate / up (fp32 bits)
-      uint32_t ra[16], rb[16];
-      tmem_ld16(lane_addr + (uint32_t)(16 * cc), ra);
-      tmem_ld16(lane_addr + (uint32_t)(BN + 16 * cc), rb);
-      tmem_wait_ld();
-      if constexpr (KS) {
+    cluster_sync_all();  // every copy has landed: the peers may exit
+    if (dq_warp && owner && dq_ok) {
+      tc_fence_after();
+      for (int cc = cz(z) + grp; cc < cz(z + 1); cc += ngroups) {
+        uint32_t oa[16], ob[16];
+        own_chunk(cc, oa, ob);
+        uint32_t va[16], vb[16];
+        // rank 0's partial, then ranks 1 .. ks - 1 added in order
 #pragma unroll 1
-        for (int zz = 1; zz < ksplit; ++zz) {
-          const uint32_t src =
-              peer_buf + (uint32_t)(zz - 1) * peer_slot + (uint32_t)row * peer_pitch + (uint32_t)(64 * cc);
-          add_partial16(ra, src);
-          if constexpr (GATEUP) add_partial16(rb, src + 128 * peer_pitch);
-        }
-      }
-      if (n < p.N) {
-        if constexpr (!GATEUP) {
-          float* y = static_cast<float*>(p.y);
+        for (int zz = 0; zz < ksplit; ++zz) {
+          if (zz == z) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int m = m0 + 16 * cc + i;
-            if (m < p.M) y[(int64_t)m * p.N + n] = __uint_as_float(ra[i]) + __uint_as_float(rb[i]);
-          }
-        } else {
-          __half* y = static_cast<__half*>(p.y);
+            for (int i = 0; i < 16; ++i) {
+              va[i] = zz == 0 ? oa[i] : __float_as_uint(__uint_as_float(va[i]) + __uint_as_float(oa[i]));
+              if constexpr (GATEUP)
+                vb[i] = zz == 0 ? ob[i] : __float_as_uint(__uint_as_float(vb[i]) + __uint_as_float(ob[i]));
+            }
+          } else {
+            const uint32_t src = recv_slot(z, zz) + (uint32_t)row * pitch + (uint32_t)(64 * (cc - cz(z)));
+            if (zz == 0) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int m = m0 + 16 * cc + i;
-            const float g = __uint_as_float(ra[i]), u = __uint_as_float(rb[i]);
-            // silu(g) * u with sigmoid(g) = 0.5 + 0.5 tanh(g / 2): one
-            // special-function op per element instead of two (exp and a
-            // reciprocal); the epilogue was bound by that unit.
-            const float hg = 0.5f * g;
-            const float o = fmaf(hg, tanh_approx(hg), hg) * u;
-            if (m < p.M) y[(int64_t)m * p.N + n] = __float2half_rn(o);
+              for (int i = 0; i < 16; i += 4) {
+                const uint4 v = lds128_u(src + 4 * i);
+                va[i] = v.x, va[i + 1] = v.y, va[i + 2] = v.z, va[i + 3] = v.w;
+              }
+              if constexpr (GATEUP) {
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                  const uint4 v = lds128_u(src + 128 * pitch + 4 * i);
+                  vb[i] = v.x, vb[i + 1] = v.y, vb[i + 2] = v.z, vb[i + 3] = v.w;
+                }
+              }
+            } else {
+              add_partial16(va, src);
+              if constexpr (GATEUP) add_partial16(vb, src + 128 * pitch);
+            }
           }
         }
+        store_chunk(cc, va, vb);
       }
+    }
+  } else if (dq_warp && dq_ok) {
+    tc_fence_after();
+    for (int cc = grp; cc < nchunks; cc += ngroups) {
+      uint32_t va[16], vb[16];
+      own_chunk(cc, va, vb);
+      store_chunk(cc, va, vb);
     }
   }
 
@@ -1227,7 +1312,7 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   if (grid.y > 65535u) return cudaErrorInvalidConfiguration;
   // Split K across a cluster when the tiles would leave at least half of the
   // SMs idle (small N or small M): ks CTAs per tile, each with >= 1 super-block,
-  // the peers' fp32 partial tiles fitting in CTA 0's stage region, and every
+  // the send and receive slots of the exchange fitting in the stage region, and every
   // tile's cluster resident at once.  The last condition is the device's
   // answer for this kernel and cluster size: clusters must fit inside one GPC,
   // and on GB300 24 clusters of 6 one-CTA-per-SM CTAs did not (a second wave
@@ -1235,18 +1320,26 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   // Among the feasible sizes, the one with the fewest super-blocks per CTA
   // (ceil(K/256 / ks): the cluster waits for its slowest CTA), then the
   // smallest (less exchange).
+  // A split launch runs one CTA per SM: its shared-memory request is raised so
+  // that no two of its CTAs share an SM (small tiles otherwise fit twice, and
+  // two CTAs of a cluster on one SM share its tensor pipe: M = 16 splits ran
+  // ~1 us slower when the registers allowed it).
   int ks = 1;
+  uint32_t split_smem = smem;
   {
     const int64_t tiles = (int64_t)grid.x * grid.y;
     const int64_t nb = K / kQK;
     int64_t best = nb;
     const int64_t sms = device_sms();
-    if (tiles * 2 <= sms)
+    uint32_t sm_smem, reserved;
+    sm_smem_limits(&sm_smem, &reserved);
+    split_smem = smem_for_tmem(smem, 512u, sm_smem, reserved);
+    if (tiles * 2 <= sms && split_smem <= (uint32_t)kSmemLimit)
       for (int c = 2; c <= 8; ++c) {
         const int64_t per = (nb + c - 1) / c;
         if (per < best && tiles * c <= sms && c <= nb &&
-            (uint64_t)(c - 1) * C::kNumB * kBM * (BN * 4 + 16) <= pl.bar_off &&
-            tiles <= max_active_clusters<QT, GATEUP, AT>(c, smem)) {
+            split_exchange_bytes<C::kNumB>(BN, c) <= pl.bar_off &&
+            tiles <= max_active_clusters<QT, GATEUP, AT>(c, split_smem)) {
           ks = c;
           best = per;
         }
@@ -1262,7 +1355,7 @@ cudaError_t launch_tc(const void* W0, const void* W1, const uint16_t* x, void* y
   memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = grid;
   cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = split_smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
