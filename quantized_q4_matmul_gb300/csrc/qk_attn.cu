@@ -540,21 +540,42 @@ __global__ void __launch_bounds__(kTThreads, 1)
       const int lim = vis >= kTCols ? kTCols : (vis <= 0 ? 0 : (int)vis);
       uint32_t v[kTCols];
       float pmax = -INFINITY;
+      // Every position of this part is visible to every row of the warp (a
+      // tile below the diagonal): the loops below skip the per-position mask.
+      const bool full = __all_sync(0xffffffffu, lim == kTCols);
       if (ok) {
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < kTCols / 16; ++c)
           tmem_ld16(t_s + (uint32_t)(16 * c), *reinterpret_cast<uint32_t(*)[16]>(v + 16 * c));
         tmem_wait_ld();
-        float pm[kTCols / 16];  // independent partial maxima (short dependency chains)
+        // max_e(s_e * c) is c * max_e(s_e) for c >= 0 (rounding is monotonic)
+        // and c * min_e(s_e) for c < 0: one multiply per row instead of one
+        // per position.  Independent partial extrema keep the chains short.
+        float pm[kTCols / 16];
+        const bool neg = scale_log2e < 0.0f;
+        const float empty = neg ? INFINITY : -INFINITY;
 #pragma unroll
         for (int c = 0; c < kTCols / 16; ++c) {
-          pm[c] = -INFINITY;
+          pm[c] = empty;
+          if (full) {
+            if (!neg) {
 #pragma unroll
-          for (int e = 16 * c; e < 16 * c + 16; ++e)
-            pm[c] = fmaxf(pm[c], e < lim ? __uint_as_float(v[e]) * scale_log2e : -INFINITY);
-          pmax = fmaxf(pmax, pm[c]);
+              for (int e = 16 * c; e < 16 * c + 16; ++e) pm[c] = fmaxf(pm[c], __uint_as_float(v[e]));
+            } else {
+#pragma unroll
+              for (int e = 16 * c; e < 16 * c + 16; ++e) pm[c] = fminf(pm[c], __uint_as_float(v[e]));
+            }
+          } else {
+#pragma unroll
+            for (int e = 16 * c; e < 16 * c + 16; ++e)
+              if (e < lim) pm[c] = neg ? fminf(pm[c], __uint_as_float(v[e])) : fmaxf(pm[c], __uint_as_float(v[e]));
+          }
         }
+        float ext = pm[0];
+#pragma unroll
+        for (int c = 1; c < kTCols / 16; ++c) ext = neg ? fminf(ext, pm[c]) : fmaxf(ext, pm[c]);
+        pmax = lim > 0 ? ext * scale_log2e : -INFINITY;
       }
       // S_j is in registers: its buffer may take S_{j+2}
       tc_fence_before();
@@ -607,8 +628,12 @@ __global__ void __launch_bounds__(kTThreads, 1)
 #pragma unroll
           for (int e = 0; e < 32; e += 2) {
             const int e0 = 32 * c + e;
-            const float p0 = e0 < lim ? ex2_approx(fmaf(__uint_as_float(v[e0]), scale_log2e, -m)) : 0.f;
-            const float p1 = e0 + 1 < lim ? ex2_approx(fmaf(__uint_as_float(v[e0 + 1]), scale_log2e, -m)) : 0.f;
+            float p0 = ex2_approx(fmaf(__uint_as_float(v[e0]), scale_log2e, -m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(v[e0 + 1]), scale_log2e, -m));
+            if (!full) {
+              p0 = e0 < lim ? p0 : 0.f;
+              p1 = e0 + 1 < lim ? p1 : 0.f;
+            }
             lp[(e >> 4) & 1] += p0 + p1;
             hp[e >> 1] = pack_h2(p0, p1);
           }
