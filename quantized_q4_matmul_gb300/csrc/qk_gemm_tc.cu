@@ -1146,7 +1146,7 @@ struct TcPlan {
   int BN, SX, SA, P;
   uint32_t smem;       // dynamic shared memory requested per CTA
   uint32_t tmem_cols;  // tensor-memory columns per CTA
-  uint32_t bar_off;    // offset of the barrier block (bounds the split-K partials)
+  uint32_t bar_off;    // offset of the barrier block (bounds the split-K exchange slots)
 };
 
 // Pipeline depths (all measured on GB300).  The K-step rings come first: a
