@@ -387,6 +387,36 @@ def test_gateup_small(qk_lib, cuda, M, N, K):
     check_close_f16out(y.float().cpu().numpy().astype(np.float64), ref, "gateup M%d N%d K%d" % (M, N, K))
 
 
+# Split K with the reduce-scatter exchange: few row tiles, so the planner splits
+# K over up to 8 CTAs, at token tiles of 3, 5, 7 and 16 chunks of 16 -- ranks
+# that own one slice, several, or none of the tile's columns.
+SPLIT_SHAPES = [(48, 1024, 8192), (80, 512, 4096), (112, 256, 12288), (256, 1024, 3072), (200, 640, 2560)]
+
+
+@pytest.mark.parametrize("qtype", ["q4k", "q6k"])
+@pytest.mark.parametrize("M,N,K", SPLIT_SHAPES)
+def test_matmul_split_k_slices(qk_lib, cuda, qtype, M, N, K):
+    rng = synth.rng_for(M * 13 + N, K + 1)
+    W = synth.weights(rng, qtype, N, K)
+    x = synth.activations(rng, M, K)
+    ref = oracle.matmul(QT[qtype], W, x, N, K)
+    check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "split %s M%d N%d K%d" % (qtype, M, N, K))
+
+
+@pytest.mark.parametrize("M,N,K", [(48, 512, 4096), (112, 256, 6144)])
+def test_gateup_split_k_slices(qk_lib, cuda, M, N, K):
+    import torch
+    rng = synth.rng_for(M * 3 + N, K + 2)
+    Wg = synth.q4k_weights(rng, N, K)
+    Wu = synth.q4k_weights(rng, N, K)
+    x = synth.activations(rng, M, K)
+    y = torch.empty(M, N, dtype=torch.float16, device=cuda)
+    qk_lib.qk_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), y, M, N, K)
+    qk_lib.qk_get_device_status()
+    ref = oracle.gateup_swiglu(Wg, Wu, x, N, K)
+    check_close_f16out(y.float().cpu().numpy().astype(np.float64), ref, "split gateup M%d N%d K%d" % (M, N, K))
+
+
 # ---------------------------------------------------------------------------
 # Boundary checks that need a device
 # ---------------------------------------------------------------------------
