@@ -1162,10 +1162,12 @@ struct TcPlan {
 // keeps to its own slots and waits on every phase of them (with an odd ring
 // an issuer would skip the phases of the other's steps, and x tiles can land
 // out of order, so a parity wait could pass on a slot's previous tile).
-// Gate/up grows x stages first (its issuers waited on x tiles while its
-// dequant threads had slack: 3 x + 2 A stages ran 12 % faster than 2 + 3),
-// up to 4.  Up to 5 A stages, while shared memory (and, with A in tensor
-// memory, TMEM) allows.  Packed-block stages: two where they fit next to 4 x
+// Gate/up grows x stages to 3, then A stages to 3, then x to 4 and A on:
+// at 256-token tiles 3 x + 2 A stages ran 12 % faster than 2 + 3, and where
+// 3 + 3 fits it ran 2-6 % faster than 4 + 2 from M = 384 to 2048 (20 % at
+// M = 192), so among packed-stage counts gate/up ranks min(x, 3), then
+// min(A, 3), then the packed stages.  Up to 5 A stages, while shared memory
+// (and, with A in tensor memory, TMEM) allows.  Packed-block stages: two where they fit next to 4 x
 // stages (cold-cache Q6_K ran faster with two; three or four gained nothing
 // in steady state), else one (the dequant threads copy a super-block to
 // registers and release its slot at once, so the refill overlaps the
@@ -1201,8 +1203,14 @@ bool plan_tc(int64_t M, int64_t N, TcPlan* out) {
     SA_ = 2;
     for (bool grew = true; grew;) {
       grew = false;
-      if (GATEUP) {  // x stages first (x_full waits dominated gate/up), then A
-        if (SX_ < kMaxXStages && fits(SX_ + 1, SA_)) {
+      if (GATEUP) {  // x to 3, A to 3, then x to 4 and A on
+        if (SX_ < 3 && fits(SX_ + 1, SA_)) {
+          ++SX_;
+          grew = true;
+        } else if (SA_ < 3 && fits(SX_, SA_ + 1)) {
+          ++SA_;
+          grew = true;
+        } else if (SX_ < kMaxXStages && fits(SX_ + 1, SA_)) {
           ++SX_;
           grew = true;
         } else if (SA_ < kMaxAStages && fits(SX_, SA_ + 1)) {
@@ -1225,9 +1233,11 @@ bool plan_tc(int64_t M, int64_t N, TcPlan* out) {
     }
   };
   // Packed stages: the most x stages up to 4 first, then the most packed
-  // stages up to kMaxP, then the deepest x ring, then the deepest A ring.
+  // stages up to kMaxP, then the deepest x ring, then the deepest A ring
+  // (gate/up: x up to 3, then A up to 3, then packed stages, then x).
   int P = 1, SX = 0, SA = 0;
   auto score = [&](int p_, int sx, int sa) {
+    if (GATEUP) return ((std::min(sx, 3) * 8 + std::min(sa, 3)) * 8 + p_) * 16 + sx;
     return ((std::min(sx, kMaxXStages) * 8 + p_) * 16 + sx) * 16 + sa;
   };
   for (int p_ = 1; p_ <= kMaxP; ++p_) {

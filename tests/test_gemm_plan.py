@@ -51,3 +51,6 @@ def test_plans_fit_tensor_and_shared_memory(qtype, N, K, gateup):
             assert max(p["x_stages"], p["a_stages"]) % 2 == 0, (M, p)
         if gateup:
             assert not p["a_in_tmem"] and p["x_stages"] <= 4
+            # a third A stage before a fourth x stage (measured faster wherever both fit)
+            if p["token_tile"] <= 240:
+                assert p["x_stages"] >= 3 and p["a_stages"] >= 3, (M, p)

@@ -287,12 +287,13 @@ def simulate_rings(sx, sa, gateup, q6k, blocks=5, seed=0):
 
 
 # The plans the host picks (x stages, A stages): single-tensor Q4_K and Q6_K
-# with even x rings up to 8, gate/up with up to 4 x stages.
+# with even x rings up to 8, gate/up with up to 4 x stages and up to 5 A stages.
 @pytest.mark.parametrize("sx,sa,gateup,q6k", [
     (4, 4, False, False), (4, 5, False, False), (6, 2, False, False), (6, 3, False, False),
     (8, 4, False, False), (8, 5, False, False), (2, 2, False, False),
     (4, 4, False, True), (6, 4, False, True), (8, 4, False, True),
-    (2, 2, True, False), (3, 2, True, False), (4, 2, True, False), (3, 3, True, False), (4, 4, True, False)])
+    (2, 2, True, False), (3, 2, True, False), (4, 2, True, False), (3, 3, True, False),
+    (4, 3, True, False), (3, 4, True, False), (3, 5, True, False), (4, 4, True, False), (4, 5, True, False)])
 def test_rings_never_pass_early_nor_stall(sx, sa, gateup, q6k):
     assert all(simulate_rings(sx, sa, gateup, q6k, seed=s) is None for s in range(400))
 
