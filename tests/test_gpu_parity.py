@@ -196,16 +196,18 @@ def test_matmul_deterministic(qk_lib, cuda, qtype):
         assert np.array_equal(a, b)
 
 
-@pytest.mark.parametrize("kind,N,K", [("gateup", 8192, 3072), ("q4k", 8192, 3072), ("q4k", 3072, 3072),
-                                      ("q6k", 3072, 8192), ("q6k", 16384, 3072)])
-def test_full_size_repeatable(qk_lib, cuda, kind, N, K):
-    """Repeated M=1024 launches give bit-identical outputs.  These shapes cover
-    every pipeline configuration of the prefill GEMM (two-tensor split producer,
-    one and two packed stages); a missing ordering between the dequant threads'
-    reads of a packed slot and its refill showed up as run-to-run differences."""
+@pytest.mark.parametrize("kind,N,K,M", [("gateup", 8192, 3072, 1024), ("q4k", 8192, 3072, 1024),
+                                        ("q4k", 3072, 3072, 1024), ("q6k", 3072, 8192, 1024),
+                                        ("q6k", 16384, 3072, 1024), ("gateup", 8192, 3072, 960),
+                                        ("gateup", 8192, 3072, 192)])
+def test_full_size_repeatable(qk_lib, cuda, kind, N, K, M):
+    """Repeated launches give bit-identical outputs.  These shapes cover every
+    pipeline configuration of the prefill GEMM (two-tensor split producer, one
+    and two packed stages, gate/up with 3 x + 2 A and 3 x + 3 A stages); a
+    missing ordering between the dequant threads' reads of a packed slot and its
+    refill showed up as run-to-run differences."""
     import torch
     rng = synth.rng_for(11, N)
-    M = 1024
     x = _x_dev(synth.activations(rng, M, K), cuda)
     if kind == "gateup":
         Wg, Wu = _dev(synth.q4k_weights(rng, N, K), cuda), _dev(synth.q4k_weights(rng, N, K), cuda)
@@ -362,7 +364,7 @@ def test_gateup_model_sweep(qk_lib, cuda):
     N, K = 8192, 3072
     Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
     Wgd, Wud = _dev(Wg, cuda), _dev(Wu, cuda)
-    for M in (16, 128, 512, 2048):
+    for M in (16, 128, 192, 512, 960, 2048):
         x = synth.activations(rng, M, K)
         y = torch.empty(M, N, dtype=torch.float16, device=cuda)
         qk_lib.qk_gateup_swiglu_q4k(Wgd, Wud, _x_dev(x, cuda), y, M, N, K)
