@@ -271,6 +271,13 @@ qk_status qk_gqa_attention(const uint16_t *q_f16, const uint16_t *k_cache, const
  * Synchronise `stream`, then report and clear the device-side status flags
  * that the library's kernels set when a bounded wait expires.  Returns QK_OK,
  * QK_ERR_TIMEOUT, or QK_ERR_CUDA if the synchronisation itself failed.
+ * The flags belong to the current device, not to a stream: every stream of
+ * the process on that device sets the same flags.  A timeout raised by a
+ * kernel on another stream that has already finished is therefore reported
+ * (and cleared) by whichever call reads the flags first, and a kernel still
+ * running on another stream is not waited for.  Callers that run the library
+ * on several streams and need to attribute a timeout synchronise those
+ * streams before calling this, or call it from one thread after all of them.
  */
 qk_status qk_get_device_status(qk_stream_t stream);
 
