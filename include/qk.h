@@ -59,6 +59,8 @@ typedef int qk_status;
 #define QK_ERR_ALIAS (-7)              /* the output overlaps an input */
 #define QK_ERR_POINTER (-8)            /* a pointer is not accessible from the current device */
 #define QK_ERR_SCRATCH (-9)            /* the built-in scratch of qk_rmsnorm_matmul_batch_static is too small */
+#define QK_ERR_BAD_COPY (-10)          /* debug builds (QK_DEBUG) only: a kernel skipped a bulk or tensor copy
+                                          whose addresses, size or shared-memory extent failed its check */
 
 /* A cudaStream_t, spelled without CUDA headers. */
 typedef struct CUstream_st *qk_stream_t;
@@ -270,7 +272,11 @@ qk_status qk_gqa_attention(const uint16_t *q_f16, const uint16_t *k_cache, const
 /*
  * Synchronise `stream`, then report and clear the device-side status flags
  * that the library's kernels set when a bounded wait expires.  Returns QK_OK,
- * QK_ERR_TIMEOUT, or QK_ERR_CUDA if the synchronisation itself failed.
+ * QK_ERR_TIMEOUT, or QK_ERR_CUDA if the synchronisation itself failed.  A
+ * library built with -DQK_DEBUG also checks each bulk and tensor copy before
+ * issuing it (shared-memory destination and mbarrier aligned and inside the
+ * CTA's shared memory; source and size of a plain bulk copy 16-byte aligned)
+ * and returns QK_ERR_BAD_COPY, ahead of QK_ERR_TIMEOUT, when one failed.
  * The flags belong to the current device, not to a stream: every stream of
  * the process on that device sets the same flags.  A timeout raised by a
  * kernel on another stream that has already finished is therefore reported

@@ -37,7 +37,12 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags=(), out_dir: str | None = None) -> str:
+    """Compile and link libqk.so; returns its path.  extra_flags go to every
+    nvcc compile (e.g. "-DQK_DEBUG" for the checked build).  out_dir puts the
+    objects and the library there instead of next to this file."""
+    BUILD = os.path.join(out_dir, "_build") if out_dir else globals()["BUILD"]
+    LIB = os.path.join(out_dir, "libqk.so") if out_dir else globals()["LIB"]
     os.makedirs(BUILD, exist_ok=True)
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     headers.append(os.path.join(os.path.dirname(HERE), "include", "qk.h"))

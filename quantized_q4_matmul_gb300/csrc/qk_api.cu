@@ -487,6 +487,7 @@ qk_status qk_get_device_status(qk_stream_t stream) {
   if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return QK_ERR_CUDA;
   const uint32_t v =
       qk::dequant_take_status() | qk::gemv_take_status() | qk::gemm_take_status() | qk::attn_take_status();
+  if (v & QK_DEV_BAD_COPY) return QK_ERR_BAD_COPY;
   return v ? QK_ERR_TIMEOUT : QK_OK;
 }
 
@@ -528,6 +529,7 @@ const char* qk_status_string(qk_status status) {
     case QK_ERR_SHAPE: return "QK_ERR_SHAPE: K must be a positive multiple of 256 and sizes non-negative";
     case QK_ERR_CUDA: return "QK_ERR_CUDA: a CUDA call or kernel launch failed";
     case QK_ERR_TIMEOUT: return "QK_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+    case QK_ERR_BAD_COPY: return "QK_ERR_BAD_COPY: a debug build skipped a copy that failed its check";
     case QK_ERR_UNSUPPORTED_DEVICE: return "QK_ERR_UNSUPPORTED_DEVICE: the current device is not sm_103";
     case QK_ERR_ALIAS: return "QK_ERR_ALIAS: the output overlaps an input";
     case QK_ERR_POINTER: return "QK_ERR_POINTER: a pointer is not accessible from the current device";

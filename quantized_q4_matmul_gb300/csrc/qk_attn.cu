@@ -690,6 +690,7 @@ uint32_t attn_take_status() {
   uint32_t v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(v)) != cudaSuccess) return 0;
   cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(zero));
+  v |= take_debug_status();
   return v;
 }
 

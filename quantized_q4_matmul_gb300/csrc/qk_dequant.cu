@@ -184,6 +184,7 @@ uint32_t dequant_take_status() {
   uint32_t v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, g_dequant_status, sizeof(v)) != cudaSuccess) return 0;
   cudaMemcpyToSymbol(g_dequant_status, &zero, sizeof(zero));
+  v |= take_debug_status();
   return v;
 }
 

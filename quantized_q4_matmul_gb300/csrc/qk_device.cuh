@@ -14,6 +14,9 @@
 #define QK_DEV_OK 0u
 #define QK_DEV_TIMEOUT 1u
 #define QK_DEV_BAD_ARG 2u
+#ifndef QK_DEV_BAD_COPY
+#define QK_DEV_BAD_COPY 4u
+#endif
 
 // Wall-clock bound of one mbarrier wait, in nanoseconds of %globaltimer.  A
 // healthy wait lasts at most one tile's worth of work (well under a
@@ -27,6 +30,48 @@ namespace qk {
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+
+// Debug builds (-DQK_DEBUG) check every bulk and tensor copy before it is
+// issued: shared-memory destination and mbarrier aligned (16 and 8 bytes) and
+// inside the CTA's shared memory, global source and byte count of a plain
+// bulk copy 16-byte aligned, byte count not zero.  A copy that fails is not
+// issued; QK_DEV_BAD_COPY goes to a status word of the translation unit,
+// which its take_status function reports (the waits on that copy's barrier
+// then time out).  Release builds compile the checks away.
+#ifdef QK_DEBUG
+static __device__ uint32_t g_debug_status;
+
+extern __shared__ uint8_t qk_debug_dyn_smem[];
+
+// End of the CTA's shared memory in the shared window: the dynamic region
+// follows the static one, so its base plus its size bounds both.
+__device__ __forceinline__ uint32_t smem_end() {
+  uint32_t v;
+  asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(v));
+  return smem_u32(qk_debug_dyn_smem) + v;
+}
+
+__device__ __forceinline__ bool copy_ok(uint32_t dst, uint32_t dst_bytes, uint32_t bar, uint64_t src, uint32_t src_align) {
+  const uint64_t end = smem_end();
+  const bool ok = (dst & 15u) == 0u && (bar & 7u) == 0u && (src & (uint64_t)(src_align - 1u)) == 0u &&
+                  dst_bytes > 0u && (uint64_t)dst + dst_bytes <= end && (uint64_t)bar + 8u <= end;
+  if (!ok) atomicOr(&g_debug_status, QK_DEV_BAD_COPY);
+  return ok;
+}
+
+// Reads and clears this translation unit's debug status word.
+static inline uint32_t take_debug_status() {
+  uint32_t v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_debug_status, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_debug_status, &zero, sizeof(zero));
+  return v;
+}
+#define QK_COPY_CHECK(dst, bytes, bar, src, align) \
+  if (!::qk::copy_ok((dst), (bytes), (bar), (uint64_t)(src), (align))) return
+#else
+static inline uint32_t take_debug_status() { return 0; }
+#define QK_COPY_CHECK(dst, bytes, bar, src, align) (void)0
+#endif
 
 // ---------------------------------------------------------------------------
 // mbarrier
@@ -103,6 +148,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // TMA (bulk tensor copies) and proxy fences
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* tmap, int32_t x, uint64_t* bar) {
+  QK_COPY_CHECK(smem_u32(dst), 16u, smem_u32(bar), tmap, 64u);
   asm volatile(
       "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2}], [%3];" ::"r"(
           smem_u32(dst)),
@@ -111,6 +157,7 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* tmap, int32_t
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t x, int32_t y, uint64_t* bar) {
+  QK_COPY_CHECK(smem_u32(dst), 16u, smem_u32(bar), tmap, 64u);
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
       "[%4];" ::"r"(smem_u32(dst)),
@@ -120,6 +167,7 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
 
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t x, int32_t y, int32_t z,
                                             uint64_t* bar) {
+  QK_COPY_CHECK(smem_u32(dst), 16u, smem_u32(bar), tmap, 64u);
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
       "[%5];" ::"r"(smem_u32(dst)),
@@ -130,6 +178,7 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
 // Plain (non-tensor) bulk copy global -> shared: both addresses 16-byte
 // aligned, size a multiple of 16.
 __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  QK_COPY_CHECK(smem_u32(dst), (bytes & 15u) ? 0u : bytes, smem_u32(bar), src, 16u);
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    smem_u32(dst)),
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
@@ -138,6 +187,7 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
 
 // The same with shared-window addresses for the destination and the mbarrier.
 __device__ __forceinline__ void bulk_copy_g2s_u32(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  QK_COPY_CHECK(dst, (bytes & 15u) ? 0u : bytes, bar, src, 16u);
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
@@ -187,6 +237,9 @@ __device__ __forceinline__ void sts128_u(uint32_t a, uint32_t x, uint32_t y, uin
 // (dst and mbar are shared::cluster addresses from mapa): 16-byte aligned
 // addresses, size a multiple of 16; completes tx bytes on mbar.
 __device__ __forceinline__ void bulk_copy_s2cluster(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+  // dst and mbar are cluster-window addresses of a peer CTA: checked for
+  // alignment only; the local source also for its extent.
+  QK_COPY_CHECK(src, (bytes & 15u) || (dst & 15u) || (mbar & 7u) ? 0u : bytes, 0u, 0u, 16u);
   asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                    dst),
                "r"(src), "r"(bytes), "r"(mbar)

@@ -1420,6 +1420,7 @@ uint32_t gemm_take_status() {
   uint32_t v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, g_gemm_status, sizeof(v)) != cudaSuccess) return 0;
   cudaMemcpyToSymbol(g_gemm_status, &zero, sizeof(zero));
+  v |= take_debug_status();
   return v;
 }
 

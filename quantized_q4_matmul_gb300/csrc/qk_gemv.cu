@@ -1260,6 +1260,7 @@ uint32_t gemv_take_status() {
   uint32_t v = 0, zero = 0;
   if (cudaMemcpyFromSymbol(&v, g_gemv_status, sizeof(v)) != cudaSuccess) return 0;
   cudaMemcpyToSymbol(g_gemv_status, &zero, sizeof(zero));
+  v |= take_debug_status();
   return v;
 }
 

@@ -44,6 +44,10 @@ class PerDeviceFlag {
 
 // Each translation unit with kernels that can time out owns one device status
 // word; these read it (after the stream has been synchronised) and clear it.
+// Status bit of a copy that a debug build (QK_DEBUG) skipped (qk_device.cuh).
+#ifndef QK_DEV_BAD_COPY
+#define QK_DEV_BAD_COPY 4u
+#endif
 uint32_t dequant_take_status();
 uint32_t gemv_take_status();
 uint32_t gemm_take_status();

@@ -31,7 +31,7 @@ def test_library_exports_every_declared_symbol(qk_lib):
 
 def test_status_strings(qk_lib):
     L = qk_lib.lib()
-    for code in range(-9, 1):
+    for code in range(-10, 1):
         s = L.qk_status_string(code).decode()
         assert s.startswith("QK_") and "unknown" not in s
     assert "unknown" in L.qk_status_string(-99).decode()
