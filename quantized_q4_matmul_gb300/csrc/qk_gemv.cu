@@ -31,9 +31,9 @@
 //   * Per sub-block, with Sx the sum of x over the lane's k-slots of it:
 //       Q4_K: sum(w*x) = (d*sc/F) * (D - 1024*Sx) - (dmin*m) * Sx
 //       Q6_K: sum(w*x) = (d*sc/F) * (D - (1024 + 32F)*Sx)
-//   * Reduction: compute warp w takes the blocks j = w mod 12 of every tile
+//   * Reduction: compute warp w takes the blocks j = w mod kDW of every tile
 //     and leaves its sums of a finished tile in the stage's partials slot;
-//     the producer adds the 12 warps' sums in warp order before it refills
+//     the producer adds the kDW warps' sums in warp order before it refills
 //     the stage and writes y.  The order of every addition depends on the
 //     problem's shape only (deterministic, and the same alone or grouped).
 // Q6_K blocks are 210 bytes, so a block can start 2 mod 4 bytes into shared
@@ -527,9 +527,11 @@ __device__ __forceinline__ void q6_block_tn(uint32_t r0, uint32_t r1, const uint
 #define QK_GEMV_BACKOFF_NS 0
 #endif
 constexpr uint32_t kBackoffNs = QK_GEMV_BACKOFF_NS;
-// Compute warps per CTA; one more warp streams.
+// Compute warps per CTA; one more warp streams.  8 measured faster than 12
+// or 16 in steady state (a layer's grouped launch 20.1 vs 20.6 and 21.5 us,
+// a 131072 x 3072 Q4_K GEMV 49.4 vs 51.3 and 54.2 us).
 #ifndef QK_DECODE_WARPS
-#define QK_DECODE_WARPS 12
+#define QK_DECODE_WARPS 8
 #endif
 constexpr int kDW = QK_DECODE_WARPS;
 constexpr int kDCompute = 32 * kDW;
