@@ -303,7 +303,7 @@ qk_status qk_debug_wait_timeout(int64_t limit_ns, qk_stream_t stream);
  * (QK_Q4_K / QK_Q6_K; with gateup != 0 the fused gate/up + SwiGLU, Q4_K only)
  * and inner size K runs on the decode GEMV, 0 if it runs on the tensor-core
  * GEMM because the GEMV cannot stage it (the x table of K plus two weight
- * stages must fit in shared memory: K <= 35840 for Q4_K, 34816 for gate/up;
+ * stages must fit in shared memory: K <= 35840 for Q4_K, 35072 for gate/up;
  * Q6_K up to K = 26624 when K / 256 is a multiple of 8, else up to 6912),
  * -1 for an invalid qtype or K.  The answer depends only on these arguments.
  */

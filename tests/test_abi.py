@@ -148,12 +148,12 @@ def test_decode_kernel_choice_on_the_host(qk_lib):
     Q4_K block, 1152 per Q6_K block), x itself, and at least two stages of 16
     rows, either whole rows (one bulk copy per tensor) or a chunk of cb blocks
     per row whose copies start on 16-byte boundaries, in 227 KB.  Q4_K rows
-    chunk at any block count: K <= 35840 (gate/up 34816).  Q6_K blocks are 210
+    chunk at any block count: K <= 35840 (gate/up 35072 with 8 compute warps).  Q6_K blocks are 210
     bytes, so a Q6_K row chunks only when its block count is a multiple of 8;
     other Q6_K rows run on the GEMV while two whole 16-row tiles fit (up to
     K = 6912) and on the GEMM beyond."""
     use = qk_lib.qk_decode_uses_gemv
-    for qt, gu, kmax in (("q4k", False, 35840), ("q4k", True, 34816)):
+    for qt, gu, kmax in (("q4k", False, 35840), ("q4k", True, 35072)):
         for K in list(range(256, 8192 + 1, 256)) + [kmax - 256, kmax]:
             assert use(qt, K, gu), (qt, gu, K)
         for K in (kmax + 256, kmax + 512, 65536):
