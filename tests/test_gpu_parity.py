@@ -569,6 +569,23 @@ def test_decode_fallback_to_gemm(qk_lib, cuda, qtype, N, K):
     check_close(gpu_matmul(qk_lib, qtype, W, x, N, K, cuda), ref, "%s M1 K%d on the GEMM" % (qtype, K))
 
 
+def test_decode_gateup_at_the_gemv_limit(qk_lib, cuda):
+    """Fused gate/up at M = 1 with the longest rows the decode GEMV stages
+    (K = 35072 with 8 compute warps), and one super-block beyond (GEMM)."""
+    import torch
+    N = 96
+    for K, on_gemv in ((35072, True), (35328, False)):
+        assert qk_lib.qk_decode_uses_gemv("q4k", K, gateup=True) == on_gemv
+        rng = synth.rng_for(43, K)
+        Wg, Wu = synth.q4k_weights(rng, N, K), synth.q4k_weights(rng, N, K)
+        x = synth.activations(rng, 1, K)
+        y = torch.empty(1, N, dtype=torch.float16, device=cuda)
+        qk_lib.qk_gateup_swiglu_q4k(_dev(Wg, cuda), _dev(Wu, cuda), _x_dev(x, cuda), y, 1, N, K)
+        qk_lib.qk_get_device_status()
+        check_close_f16out(y.float().cpu().numpy().astype(np.float64), oracle.gateup_swiglu(Wg, Wu, x, N, K),
+                           "gate/up M1 K%d" % K)
+
+
 def test_decode_gateup_fallback_to_gemm(qk_lib, cuda):
     import torch
     N, K = 192, 65536
